@@ -1,0 +1,258 @@
+"""CPU oracle for the DSA decode path -- TEST INFRASTRUCTURE ONLY.
+
+This package wraps ``dsa_oracle.c``: a plain, slow, double-precision C implementation of what the
+DSA decode path computes (Hadamard rotation, FP8-E4M3 quantisation, paged index-K store,
+lightning-indexer logits, per-row top-k, absorbed sparse MLA, log-sum-exp merge).  Only ``tests/``,
+``__graft_entry__.smoke()`` and the ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may
+import it.  The product library (``deepseek_sparse_attention_paged_gb300``) never imports, links or
+runs anything here, and the two share no code.
+
+Every function is pinned by ``-m "not gpu"`` tests against closed forms, library routines, brute
+force and invariants (see ``tests/test_oracle_*.py``).  No function is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dsa_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libdsa_oracle.so")
+_lib = None
+
+PAGE = 64
+DI = 128
+HI = 64
+ROW_BYTES = 132
+PAGE_BYTES = PAGE * ROW_BYTES
+DQK = 576
+DV = 512
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/libdsa_oracle.so`` (host C, gcc, OpenMP)."""
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp", "-fPIC",
+           "-shared", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    lib = ctypes.CDLL(_LIB_PATH)
+    P = ctypes.c_void_p
+    i64, i32, f64 = ctypes.c_int64, ctypes.c_int32, ctypes.c_double
+    sig = {
+        "dsa_oracle_f32_to_bf16": (ctypes.c_uint16, [ctypes.c_float]),
+        "dsa_oracle_bf16_to_f32": (ctypes.c_float, [ctypes.c_uint16]),
+        "dsa_oracle_e4m3_decode": (f64, [ctypes.c_uint8]),
+        "dsa_oracle_e4m3_encode": (ctypes.c_uint8, [ctypes.c_float]),
+        "dsa_oracle_fwht128": (None, [P]),
+        "dsa_oracle_rotate128": (None, [P, P]),
+        "dsa_oracle_quant128": (None, [P, P, P]),
+        "dsa_oracle_store_index_k": (i64, [P, P, i64, P, i64]),
+        "dsa_oracle_visible_len": (i32, [P, P, i32, i64]),
+        "dsa_oracle_indexer_logits": (i64, [P, P, P, i64, P, i32, P, P, i32, i32, P, i64, P, i64, P]),
+        "dsa_oracle_topk": (None, [P, i64, P, P, i32, P, i64, i32, P]),
+        "dsa_oracle_sparse_mla": (i64, [P, P, i64, P, i32, P, P, i32, P, i32, i32, f64, P, i64, P, P, P]),
+        "dsa_oracle_dense_mla": (None, [P, P, i64, P, i32, P, P, i32, i32, f64, P, i64, P, P]),
+        "dsa_oracle_lse_merge": (None, [P, P, P, P, i64, i32, P, P]),
+        "dsa_oracle_num_threads": (ctypes.c_int, []),
+        "dsa_oracle_set_num_threads": (None, [ctypes.c_int]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _p(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ------------------------------------------------------------------ scalar helpers
+
+def f32_to_bf16(x: float) -> int:
+    return int(_load().dsa_oracle_f32_to_bf16(float(x)))
+
+
+def bf16_to_f32(h: int) -> float:
+    return float(_load().dsa_oracle_bf16_to_f32(int(h)))
+
+
+def e4m3_decode(c: int) -> float:
+    return float(_load().dsa_oracle_e4m3_decode(int(c)))
+
+
+def e4m3_encode(x: float) -> int:
+    return int(_load().dsa_oracle_e4m3_encode(float(x)))
+
+
+def f32_to_bf16_array(x: np.ndarray) -> np.ndarray:
+    fn = _load().dsa_oracle_f32_to_bf16
+    flat = np.asarray(x, dtype=np.float32).ravel()
+    return np.array([fn(float(v)) for v in flat], dtype=np.uint16).reshape(np.shape(x))
+
+
+def e4m3_encode_array(x: np.ndarray) -> np.ndarray:
+    fn = _load().dsa_oracle_e4m3_encode
+    flat = np.asarray(x, dtype=np.float32).ravel()
+    return np.array([fn(float(v)) for v in flat], dtype=np.uint8).reshape(np.shape(x))
+
+
+# ------------------------------------------------------------------ vector steps
+
+def fwht128(x: np.ndarray) -> np.ndarray:
+    """Unnormalised fp32 Walsh-Hadamard butterflies of one 128-vector (Sylvester order)."""
+    v = _c(x, np.float32).copy()
+    assert v.shape == (DI,)
+    _load().dsa_oracle_fwht128(_p(v))
+    return v
+
+
+def rotate128(x_bf16: np.ndarray) -> np.ndarray:
+    """Hadamard rotation of one bf16 128-vector (bits in, bits out)."""
+    src = _c(x_bf16, np.uint16)
+    assert src.shape == (DI,)
+    out = np.empty(DI, np.uint16)
+    _load().dsa_oracle_rotate128(_p(src), _p(out))
+    return out
+
+
+def quant128(y: np.ndarray):
+    """Per-128 FP8 quantisation: returns (codes uint8[128], scale float32)."""
+    v = _c(y, np.float32)
+    assert v.shape == (DI,)
+    codes = np.empty(DI, np.uint8)
+    s = np.empty(1, np.float32)
+    _load().dsa_oracle_quant128(_p(v), _p(codes), _p(s))
+    return codes, s[0]
+
+
+# ------------------------------------------------------------------ path stages
+
+def store_index_k(k_bf16: np.ndarray, slot_mapping: np.ndarray, pool: np.ndarray) -> int:
+    """Rotate, quantise and scatter keys into ``pool`` (uint8 [num_pages, 64*132]) in place."""
+    k = _c(k_bf16, np.uint16).reshape(-1, DI)
+    slots = _c(slot_mapping, np.int64)
+    assert pool.dtype == np.uint8 and pool.flags["C_CONTIGUOUS"] and pool.shape[1] == PAGE_BYTES
+    return int(_load().dsa_oracle_store_index_k(_p(k), _p(slots), k.shape[0], _p(pool), pool.shape[0]))
+
+
+def visible_len(seq_lens, cu_q, r: int) -> int:
+    sl = _c(seq_lens, np.int32)
+    cq = _c(cu_q, np.int32)
+    return int(_load().dsa_oracle_visible_len(_p(sl), _p(cq), sl.shape[0], int(r)))
+
+
+def indexer_logits(q_bf16, w, pool, block_table, seq_lens, cu_q, rows, ld, rotate_q=False,
+                   want_mag=False, fill=np.nan):
+    """Indexer logits for the global rows ``rows``; returns float32 [len(rows), ld] (and the
+    float64 magnitude array when ``want_mag``).  Entries past each row's visible length keep
+    ``fill``."""
+    q = _c(q_bf16, np.uint16)
+    wv = _c(w, np.float32)
+    pool = _c(pool, np.uint8)
+    bt = _c(block_table, np.int32)
+    sl = _c(seq_lens, np.int32)
+    cq = _c(cu_q, np.int32)
+    rr = _c(rows, np.int64)
+    out = np.full((rr.shape[0], ld), fill, np.float32)
+    mag = np.zeros((rr.shape[0], ld), np.float64) if want_mag else None
+    bad = _load().dsa_oracle_indexer_logits(
+        _p(q), _p(wv), _p(pool), pool.shape[0], _p(bt), bt.shape[1], _p(sl), _p(cq), sl.shape[0],
+        int(bool(rotate_q)), _p(rr), rr.shape[0], _p(out), ld, _p(mag) if mag is not None else None)
+    if want_mag:
+        return out, mag, int(bad)
+    return out
+
+
+def topk(logits, seq_lens, cu_q, rows, k):
+    """Per-row top-k indices (ascending index order, -1 padded) for logits rows of ``rows``."""
+    lg = _c(logits, np.float32)
+    sl = _c(seq_lens, np.int32)
+    cq = _c(cu_q, np.int32)
+    rr = _c(rows, np.int64)
+    idx = np.empty((rr.shape[0], k), np.int32)
+    _load().dsa_oracle_topk(_p(lg), lg.shape[1], _p(sl), _p(cq), sl.shape[0], _p(rr), rr.shape[0],
+                            int(k), _p(idx))
+    return idx
+
+
+def sparse_mla(q_bf16, kv_bf16, block_table, seq_lens, cu_q, idx, scale, rows, want_psum=False):
+    """Absorbed sparse MLA for the global rows ``rows``; returns (out float64 [n,H,512],
+    lse float64 [n,H]) and, when ``want_psum``, the softmax-weight sums and the skipped count."""
+    q = _c(q_bf16, np.uint16)
+    T, H, D = q.shape
+    assert D == DQK
+    kv = _c(kv_bf16, np.uint16)
+    num_pages = kv.shape[0]
+    bt = _c(block_table, np.int32)
+    sl = _c(seq_lens, np.int32)
+    cq = _c(cu_q, np.int32)
+    ix = _c(idx, np.int32)
+    rr = _c(rows, np.int64)
+    n = rr.shape[0]
+    out = np.zeros((n, H, DV), np.float64)
+    lse = np.zeros((n, H), np.float64)
+    psum = np.zeros((n, H), np.float64)
+    bad = _load().dsa_oracle_sparse_mla(_p(q), _p(kv), num_pages, _p(bt), bt.shape[1], _p(sl), _p(cq),
+                                        sl.shape[0], _p(ix), ix.shape[1], H, float(scale), _p(rr), n,
+                                        _p(out), _p(lse), _p(psum))
+    if want_psum:
+        return out, lse, psum, int(bad)
+    return out, lse
+
+
+def dense_mla(q_bf16, kv_bf16, block_table, seq_lens, cu_q, scale, rows):
+    q = _c(q_bf16, np.uint16)
+    T, H, D = q.shape
+    kv = _c(kv_bf16, np.uint16)
+    bt = _c(block_table, np.int32)
+    sl = _c(seq_lens, np.int32)
+    cq = _c(cu_q, np.int32)
+    rr = _c(rows, np.int64)
+    n = rr.shape[0]
+    out = np.zeros((n, H, DV), np.float64)
+    lse = np.zeros((n, H), np.float64)
+    _load().dsa_oracle_dense_mla(_p(q), _p(kv), kv.shape[0], _p(bt), bt.shape[1], _p(sl), _p(cq),
+                                 sl.shape[0], H, float(scale), _p(rr), n, _p(out), _p(lse))
+    return out, lse
+
+
+def lse_merge(o1, lse1, o2, lse2):
+    o1 = _c(o1, np.float64)
+    o2 = _c(o2, np.float64)
+    l1 = _c(lse1, np.float64)
+    l2 = _c(lse2, np.float64)
+    dv = o1.shape[-1]
+    n = l1.size
+    o = np.zeros_like(o1)
+    lse = np.zeros_like(l1)
+    _load().dsa_oracle_lse_merge(_p(o1), _p(l1), _p(o2), _p(l2), n, dv, _p(o), _p(lse))
+    return o, lse
+
+
+def num_threads() -> int:
+    return int(_load().dsa_oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    _load().dsa_oracle_set_num_threads(int(n))

@@ -1,0 +1,492 @@
+/*
+ * dsa_oracle.c -- plain CPU oracle for the DeepSeek Sparse Attention (DSA) decode path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU-baseline leg of the
+ * benchmark may load this library.  The product path (the CUDA library) never calls it, and the
+ * two share no code, header, table or constant.
+ *
+ * Every function is the plain definition written out: loops in the order the method states them,
+ * double accumulation, no blocking, no fusion.  It is deliberately slow.
+ *
+ * Sources (web pages; each function names the passage it follows):
+ *   [sfa]    vllm_ascend/attention/sfa_v1.py         (vLLM-Ascend SFA backend, DeepSeek-V3.2)
+ *   [dsa]    vllm_ascend/attention/dsa_v1.py         (vLLM-Ascend DSA backend)
+ *   [idx]    sglang/srt/layers/attention/dsa/dsa_indexer.py  (sglang Indexer)
+ *   [mla]    vllm/v1/attention/backends/mla/common.py        (vLLM MLACommonImpl)
+ *
+ * Readings of points the pages leave open are stated at each function; they are the same
+ * readings the CUDA path implements (stated independently there).
+ *
+ * Parity pins: every function here is pinned by tests under tests/ (closed forms, library
+ * routines, brute force, invariants).  No function is "parity unpinned".
+ *
+ * Build: gcc -std=c11 -O2 -ffp-contract=off -fopenmp -fPIC -shared (no fast-math: the
+ * quantisation steps must follow IEEE single precision exactly).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define PAGE 64          /* page size: [idx] Indexer._get_topk_paged asserts page size 64 */
+#define DI 128           /* indexer head dim ([sfa] AscendSFAImpl: head_dim = 128) */
+#define HI 64            /* indexer heads ([sfa] AscendSFAImpl: n_head = 64) */
+#define ROW_BYTES 132    /* 128 FP8 codes + one fp32 scale ([idx] head_dim_with_sf = 132) */
+#define PAGE_BYTES (PAGE * ROW_BYTES)
+#define DQK 576          /* absorbed MLA query/key width: 512 latent + 64 rope ([mla] head size 576) */
+#define DV 512           /* latent value width */
+
+/* ---------------------------------------------------------------- number formats */
+
+/* bf16 -> fp32 is exact: the bf16 bits are the upper half of the fp32 bits. */
+static float bf16_bits_to_f32(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* fp32 -> bf16, round to nearest, ties to even (the IEEE default rounding).  Written from the
+ * definition: keep the upper 16 bits, look at the discarded lower 16 bits, and round up when
+ * they exceed half an ulp, or equal half an ulp and the kept part is odd.  A carry out of the
+ * mantissa correctly bumps the exponent (and overflows to infinity). */
+uint16_t dsa_oracle_f32_to_bf16(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu) != 0u)
+        return (uint16_t)((u >> 16) | 0x0040u); /* NaN stays a (quiet) NaN */
+    uint32_t kept = u >> 16;
+    uint32_t dropped = u & 0xffffu;
+    if (dropped > 0x8000u || (dropped == 0x8000u && (kept & 1u)))
+        kept += 1u;
+    return (uint16_t)kept;
+}
+
+float dsa_oracle_bf16_to_f32(uint16_t h) { return bf16_bits_to_f32(h); }
+
+/* OCP 8-bit floating point, E4M3 "fn" variant (the torch.float8_e4m3fn type the [idx] page uses
+ * for the index-K cache; not the fnuz variant).  1 sign bit, 4 exponent bits with bias 7, 3
+ * mantissa bits; exponent field 0 encodes subnormals m/8 * 2^-6; there is no infinity; the only
+ * NaN patterns are S.1111.111.  Largest finite magnitude: 1.75 * 2^8 = 448. */
+double dsa_oracle_e4m3_decode(uint8_t c) {
+    int s = (c >> 7) & 1;
+    int e = (c >> 3) & 15;
+    int m = c & 7;
+    if (e == 15 && m == 7) return NAN;
+    double v = (e == 0) ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/* fp32 -> E4M3FN, round to nearest with ties to even code, saturating to +-448 (no value maps to
+ * NaN except NaN).  Written as a search over the 127 non-negative finite codes, whose values
+ * increase with the code: find the two neighbours of |x| and take the nearer one; on an exact tie
+ * take the one whose code is even (an even code has an even mantissa LSB).  The sign bit is kept,
+ * so -0 and negative values that round to zero give code 0x80. */
+uint8_t dsa_oracle_e4m3_encode(float x) {
+    if (isnan(x)) return 0x7f;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7e);
+    int lo = 0;
+    for (int c = 0; c <= 0x7e; ++c)
+        if (dsa_oracle_e4m3_decode((uint8_t)c) <= a) lo = c;
+    double vlo = dsa_oracle_e4m3_decode((uint8_t)lo);
+    double vhi = dsa_oracle_e4m3_decode((uint8_t)(lo + 1));
+    double dlo = a - vlo, dhi = vhi - a;
+    int c;
+    if (dlo < dhi) c = lo;
+    else if (dhi < dlo) c = lo + 1;
+    else c = (lo & 1) ? lo + 1 : lo;
+    return (uint8_t)(sign | c);
+}
+
+/* ---------------------------------------------------------------- Hadamard rotation */
+
+/* Unnormalised fast Walsh-Hadamard transform of a 128-vector in fp32, Sylvester (natural)
+ * order: for h = 1, 2, 4, ..., 64, every pair (j, j+h) inside each block of 2h becomes
+ * (a+b, a-b).  This equals multiplication by the Sylvester matrix H_128, the matrix
+ * scipy.linalg.hadamard(128) builds ([sfa] qk_hadamard; [dsa] hadamard_transform_ref multiplies
+ * by that matrix).  The butterfly order is part of the definition here: it fixes the fp32
+ * rounding of every intermediate. */
+void dsa_oracle_fwht128(float* x) {
+    for (int h = 1; h < DI; h <<= 1) {
+        for (int i = 0; i < DI; i += 2 * h) {
+            for (int j = i; j < i + h; ++j) {
+                float a = x[j];
+                float b = x[j + h];
+                x[j] = a + b;
+                x[j + h] = a - b;
+            }
+        }
+    }
+}
+
+/* Rotation of one bf16 128-vector ([idx] rotate_activation: hadamard_transform(x, scale =
+ * 128^-0.5); [dsa] rotate_activation = hadamard_transform_ref(x, H, 128^-0.5)): fp32 butterflies,
+ * one multiply by the fp32 value of 1/sqrt(128), round to bf16 (the pages keep the rotated
+ * activation in the input dtype, bf16).  Output: the rotated values as bf16 bits. */
+void dsa_oracle_rotate128(const uint16_t* in_bf16, uint16_t* out_bf16) {
+    const float inv_sqrt_n = (float)(1.0 / sqrt((double)DI));
+    float x[DI];
+    for (int d = 0; d < DI; ++d) x[d] = bf16_bits_to_f32(in_bf16[d]);
+    dsa_oracle_fwht128(x);
+    for (int d = 0; d < DI; ++d) out_bf16[d] = dsa_oracle_f32_to_bf16(x[d] * inv_sqrt_n);
+}
+
+/* ---------------------------------------------------------------- FP8 quantisation */
+
+/* Per-128-vector FP8 quantisation ([idx] act_quant(x, block_size=128): one scale per block of
+ * 128 values, which for a 128-wide key or query head is one scale per token / per head).
+ * Reading of the unprinted formula: amax = max |y|; scale = max(amax, 1e-4) / 448 in fp32 with
+ * IEEE division; code = E4M3FN(y / scale) with IEEE fp32 division then round-to-nearest-even and
+ * saturation.  The scale is plain fp32 (no power-of-two rounding). */
+void dsa_oracle_quant128(const float* y, uint8_t* codes, float* scale) {
+    float amax = 0.0f;
+    for (int d = 0; d < DI; ++d) {
+        float a = fabsf(y[d]);
+        if (a > amax) amax = a;
+    }
+    float s = fmaxf(amax, 1e-4f) / 448.0f;
+    for (int d = 0; d < DI; ++d) {
+        float t = y[d] / s;
+        codes[d] = dsa_oracle_e4m3_encode(t);
+    }
+    *scale = s;
+}
+
+/* ---------------------------------------------------------------- index-K store */
+
+/* Store new indexer keys into the paged FP8 cache ([idx] Indexer._store_index_k_cache:
+ * fused_store_index_k_cache(key, buf, out_cache_loc, page_size), or act_quant followed by
+ * set_index_k_scale_buffer; [sfa] scatter of the quantised key by slot_mapping).
+ * Steps per token: rotate (Hadamard, bf16), quantise (per token), scatter to slot.
+ * slot < 0 is a padding slot and is skipped ([sfa] pads slot_mapping with -1).
+ * Page layout (reading: the pages fix 132 bytes per token and 64 tokens per page but not the
+ * order inside a page): page-blocked, bytes [0, 8192) hold the 64 x 128 codes row by row,
+ * bytes [8192, 8448) hold the 64 fp32 scales.
+ * Returns the number of tokens whose slot pointed past the pool (those are skipped). */
+int64_t dsa_oracle_store_index_k(const uint16_t* k_bf16, const int64_t* slot_mapping, int64_t n,
+                                 uint8_t* pool, int64_t num_pages) {
+    int64_t bad = 0;
+    for (int64_t t = 0; t < n; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        int64_t page = slot / PAGE, row = slot % PAGE;
+        if (page >= num_pages) { ++bad; continue; }
+        uint16_t rot[DI];
+        float y[DI];
+        uint8_t codes[DI];
+        float s;
+        dsa_oracle_rotate128(k_bf16 + t * DI, rot);
+        for (int d = 0; d < DI; ++d) y[d] = bf16_bits_to_f32(rot[d]);
+        dsa_oracle_quant128(y, codes, &s);
+        uint8_t* pg = pool + page * PAGE_BYTES;
+        memcpy(pg + row * DI, codes, DI);
+        memcpy(pg + PAGE * DI + row * 4, &s, 4);
+    }
+    return bad;
+}
+
+/* ---------------------------------------------------------------- causal visibility */
+
+/* Request of global query row r: the b with cu_q[b] <= r < cu_q[b+1]. */
+static int row_request(const int32_t* cu_q, int32_t B, int64_t r) {
+    for (int b = 0; b < B; ++b)
+        if (r >= cu_q[b] && r < cu_q[b + 1]) return b;
+    return -1;
+}
+
+/* Visible keys of query row r ([idx] ragged key ends ke = start + pos + 1; next_n query tokens of
+ * a request are its last next_n positions; NPU sparse_mode=3 is causal).  Row j of request b
+ * (q_len_b rows, seq_lens[b] cached tokens including this step's) sits at absolute position
+ * p = seq_lens[b] - q_len_b + j and sees keys [0, p]. */
+int32_t dsa_oracle_visible_len(const int32_t* seq_lens, const int32_t* cu_q, int32_t B, int64_t r) {
+    int b = row_request(cu_q, B, r);
+    if (b < 0) return 0;
+    int32_t q_len = cu_q[b + 1] - cu_q[b];
+    int64_t j = r - cu_q[b];
+    int64_t v = (int64_t)seq_lens[b] - q_len + j + 1;
+    if (v < 0) v = 0;
+    return (int32_t)v;
+}
+
+/* ---------------------------------------------------------------- indexer logits */
+
+/* Lightning-indexer logits over the paged FP8 cache ([idx] Indexer._get_topk_paged: paged MQA
+ * logits over block_table / seq_lens with the head gate from _get_logits_head_gate; [sfa]
+ * npu_lightning_indexer):
+ *     I[r,s] = sum_h w'[r,h] * ReLU(k_scale[s] * sum_d dec(cq[r,h,d]) * dec(ck[s,d]))
+ * with w'[r,h] = w[r,h] * q_scale[r,h] (the query scale folded into the head gate, as
+ * _get_logits_head_gate multiplies the gate by q_scale) and the query quantised per head by the
+ * same per-128 rule as the keys.  The input w already carries n_heads^-0.5 * head_dim^-0.5.
+ * rotate_q != 0 first rotates each query head (the pages rotate q before quantising it).
+ * Computed in double, rounded once to fp32.  Only s < v_r is written.
+ * rows[i] lists the global rows to compute; output row i goes to logits[i*ld ...].
+ * mag (nullable, double [n_rows, ld]) receives sum_h |w'| * ReLU(...), the magnitude of the
+ * terms, which bounds the rounding error of any evaluation order.
+ * Returns the number of (row, key) pairs skipped because the page id was out of range. */
+int64_t dsa_oracle_indexer_logits(const uint16_t* q_bf16, const float* w, const uint8_t* pool,
+                                  int64_t num_pages, const int32_t* block_table, int32_t max_pages,
+                                  const int32_t* seq_lens, const int32_t* cu_q, int32_t B,
+                                  int32_t rotate_q, const int64_t* rows, int64_t n_rows,
+                                  float* logits, int64_t ld, double* mag) {
+    int64_t bad = 0;
+    for (int64_t i = 0; i < n_rows; ++i) {
+        int64_t r = rows[i];
+        int b = row_request(cu_q, B, r);
+        if (b < 0) continue;
+        int32_t v = dsa_oracle_visible_len(seq_lens, cu_q, B, r);
+        /* query prologue: per head, optional rotation, then per-128 quantisation */
+        uint8_t cq[HI][DI];
+        double wq[HI];
+        for (int h = 0; h < HI; ++h) {
+            const uint16_t* src = q_bf16 + (r * HI + h) * DI;
+            uint16_t rot[DI];
+            float y[DI];
+            float sq;
+            if (rotate_q) {
+                dsa_oracle_rotate128(src, rot);
+                src = rot;
+            }
+            for (int d = 0; d < DI; ++d) y[d] = bf16_bits_to_f32(src[d]);
+            dsa_oracle_quant128(y, cq[h], &sq);
+            wq[h] = (double)w[r * HI + h] * (double)sq;
+        }
+        double dq[HI][DI];
+        for (int h = 0; h < HI; ++h)
+            for (int d = 0; d < DI; ++d) dq[h][d] = dsa_oracle_e4m3_decode(cq[h][d]);
+        int64_t row_bad = 0;
+#pragma omp parallel for schedule(static) reduction(+ : row_bad)
+        for (int64_t s = 0; s < v; ++s) {
+            int64_t lp = s / PAGE;
+            int32_t page = (lp < max_pages) ? block_table[(int64_t)b * max_pages + lp] : -1;
+            if (page < 0 || page >= num_pages) { ++row_bad; continue; }
+            const uint8_t* pg = pool + (int64_t)page * PAGE_BYTES;
+            const uint8_t* ck = pg + (s % PAGE) * DI;
+            float ks;
+            memcpy(&ks, pg + PAGE * DI + (s % PAGE) * 4, 4);
+            double dk[DI];
+            for (int d = 0; d < DI; ++d) dk[d] = dsa_oracle_e4m3_decode(ck[d]);
+            double acc = 0.0, accm = 0.0;
+            for (int h = 0; h < HI; ++h) {
+                double dot = 0.0;
+                for (int d = 0; d < DI; ++d) dot += dq[h][d] * dk[d];
+                double relu = (double)ks * dot;
+                if (relu < 0.0) relu = 0.0;
+                acc += wq[h] * relu;
+                accm += fabs(wq[h]) * relu;
+            }
+            logits[i * ld + s] = (float)acc;
+            if (mag) mag[i * ld + s] = accm;
+        }
+        bad += row_bad;
+    }
+    return bad;
+}
+
+/* ---------------------------------------------------------------- top-k */
+
+typedef struct {
+    float v;
+    int32_t s;
+} keyed_t;
+
+/* Total order used by the selection: larger value first; -0 equals +0; NaN after every number;
+ * equal values keep the lower index first (a stable descending sort). */
+static int cmp_desc_stable(const void* pa, const void* pb) {
+    const keyed_t* a = (const keyed_t*)pa;
+    const keyed_t* b = (const keyed_t*)pb;
+    int na = isnan(a->v), nb = isnan(b->v);
+    if (na != nb) return na ? 1 : -1;
+    if (!na) {
+        if (a->v > b->v) return -1;
+        if (a->v < b->v) return 1;
+    }
+    return (a->s < b->s) ? -1 : (a->s > b->s) ? 1 : 0;
+}
+
+static int cmp_i32(const void* pa, const void* pb) {
+    int32_t a = *(const int32_t*)pa, b = *(const int32_t*)pb;
+    return (a < b) ? -1 : (a > b) ? 1 : 0;
+}
+
+/* Per-row top-k ([idx] forward_indexer: logits.topk(min(topk, seq_len)) then pad with -1 to the
+ * top-k width; _get_topk_paged pads rows it did not score with -1).  Readings: the kept set is
+ * the first min(k, v) entries of a stable descending sort of I[r, 0:v) (lower index wins ties),
+ * returned in ascending index order, padded with -1 to k.  rows[i] gives the global row (for its
+ * visible length); logits row i is logits[i*ld ...]. */
+void dsa_oracle_topk(const float* logits, int64_t ld, const int32_t* seq_lens, const int32_t* cu_q,
+                     int32_t B, const int64_t* rows, int64_t n_rows, int32_t k, int32_t* idx) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < n_rows; ++i) {
+        int32_t v = dsa_oracle_visible_len(seq_lens, cu_q, B, rows[i]);
+        int32_t* out = idx + i * (int64_t)k;
+        keyed_t* keys = (keyed_t*)malloc(sizeof(keyed_t) * (size_t)(v > 0 ? v : 1));
+        for (int32_t s = 0; s < v; ++s) {
+            keys[s].v = logits[i * ld + s];
+            keys[s].s = s;
+        }
+        qsort(keys, (size_t)v, sizeof(keyed_t), cmp_desc_stable);
+        int32_t n = v < k ? v : k;
+        for (int32_t j = 0; j < n; ++j) out[j] = keys[j].s;
+        qsort(out, (size_t)n, sizeof(int32_t), cmp_i32);
+        for (int32_t j = n; j < k; ++j) out[j] = -1;
+        free(keys);
+    }
+}
+
+/* ---------------------------------------------------------------- sparse MLA */
+
+/* Physical latent-cache row of logical position pos of request b, or -1 when the block table
+ * does not map it (one block table, page size 64, serves both caches: [sfa] passes the same
+ * block_table to the indexer and to the sparse attention). */
+static int64_t latent_row(const int32_t* block_table, int32_t max_pages, int64_t num_pages, int b,
+                          int64_t pos) {
+    int64_t lp = pos / PAGE;
+    if (lp >= max_pages) return -1;
+    int32_t page = block_table[(int64_t)b * max_pages + lp];
+    if (page < 0 || page >= num_pages) return -1;
+    return (int64_t)page * PAGE + pos % PAGE;
+}
+
+/* Attention of one (row, head) over a list of latent rows (absorbed MLA, [mla]
+ * MLACommonImpl.forward decode branch: q = [ql_nope (512), q_pe (64)] against the 576-wide
+ * latent cache rows; key and value are the same latent vector, the value is its first 512 dims;
+ * one shared KV head).  S_i = scale * <q, c_i>; P = softmax(S); o = sum_i P_i c_i[0:512];
+ * lse = max S + log sum exp(S - max S).  No valid row: o = 0, lse = -inf (reading). */
+static void attend_rows(const uint16_t* qh, const uint16_t* kv, const int64_t* g, int64_t n,
+                        double scale, double* o, double* lse, double* ssum_out) {
+    for (int d = 0; d < DV; ++d) o[d] = 0.0;
+    if (n == 0) {
+        *lse = -INFINITY;
+        if (ssum_out) *ssum_out = 0.0;
+        return;
+    }
+    double q[DQK];
+    for (int d = 0; d < DQK; ++d) q[d] = (double)bf16_bits_to_f32(qh[d]);
+    double* S = (double*)malloc(sizeof(double) * (size_t)n);
+    double m = -INFINITY;
+    for (int64_t i = 0; i < n; ++i) {
+        const uint16_t* c = kv + g[i] * DQK;
+        double dot = 0.0;
+        for (int d = 0; d < DQK; ++d) dot += q[d] * (double)bf16_bits_to_f32(c[d]);
+        S[i] = scale * dot;
+        if (S[i] > m) m = S[i];
+    }
+    double l = 0.0;
+    for (int64_t i = 0; i < n; ++i) l += exp(S[i] - m);
+    double psum = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        double p = exp(S[i] - m) / l;
+        psum += p;
+        const uint16_t* c = kv + g[i] * DQK;
+        for (int d = 0; d < DV; ++d) o[d] += p * (double)bf16_bits_to_f32(c[d]);
+    }
+    *lse = m + log(l);
+    if (ssum_out) *ssum_out = psum;
+    free(S);
+}
+
+/* Sparse MLA decode over the selected positions ([sfa] npu_sparse_flash_attention with
+ * sparse_indices = top-k, sparse_block_size = 1, block_table; [mla] decode returns (out, lse)).
+ * idx[r, :] holds logical positions within the request; -1 entries are padding; an entry outside
+ * [0, v_r) or on an unmapped page is skipped (counted in the return value).
+ * q: [T, H, 576] bf16; kv: [num_pages, 64, 576] bf16; out: double [n_rows, H, 512];
+ * lse: double [n_rows, H]; psum (nullable): double [n_rows, H], the sum of the softmax weights. */
+int64_t dsa_oracle_sparse_mla(const uint16_t* q_bf16, const uint16_t* kv, int64_t num_pages,
+                              const int32_t* block_table, int32_t max_pages, const int32_t* seq_lens,
+                              const int32_t* cu_q, int32_t B, const int32_t* idx, int32_t k,
+                              int32_t H, double scale, const int64_t* rows, int64_t n_rows,
+                              double* out, double* lse, double* psum) {
+    int64_t bad_total = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : bad_total)
+    for (int64_t i = 0; i < n_rows * H; ++i) {
+        int64_t ri = i / H;
+        int h = (int)(i % H);
+        int64_t r = rows[ri];
+        int b = row_request(cu_q, B, r);
+        int32_t v = dsa_oracle_visible_len(seq_lens, cu_q, B, r);
+        int64_t* g = (int64_t*)malloc(sizeof(int64_t) * (size_t)k);
+        int64_t n = 0, bad = 0;
+        for (int32_t j = 0; j < k; ++j) {
+            int32_t pos = idx[r * (int64_t)k + j];
+            if (pos < 0) continue;
+            int64_t gr = (b >= 0 && pos < v) ? latent_row(block_table, max_pages, num_pages, b, pos) : -1;
+            if (gr < 0) { ++bad; continue; }
+            g[n++] = gr;
+        }
+        attend_rows(q_bf16 + (r * H + h) * DQK, kv, g, n, scale, out + (ri * H + h) * DV,
+                    lse + ri * H + h, psum ? psum + ri * H + h : NULL);
+        free(g);
+        if (h == 0) bad_total += bad;
+    }
+    return bad_total;
+}
+
+/* Dense MLA decode over every visible position [0, v_r) of the request, the same attention with
+ * no selection ([mla] _forward_decode over the whole paged latent cache).  Used to pin the sparse
+ * form: with k >= v_r the selection keeps every position and the two must agree. */
+void dsa_oracle_dense_mla(const uint16_t* q_bf16, const uint16_t* kv, int64_t num_pages,
+                          const int32_t* block_table, int32_t max_pages, const int32_t* seq_lens,
+                          const int32_t* cu_q, int32_t B, int32_t H, double scale,
+                          const int64_t* rows, int64_t n_rows, double* out, double* lse) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < n_rows * H; ++i) {
+        int64_t ri = i / H;
+        int h = (int)(i % H);
+        int64_t r = rows[ri];
+        int b = row_request(cu_q, B, r);
+        int32_t v = dsa_oracle_visible_len(seq_lens, cu_q, B, r);
+        int64_t* g = (int64_t*)malloc(sizeof(int64_t) * (size_t)(v > 0 ? v : 1));
+        int64_t n = 0;
+        for (int32_t pos = 0; pos < v; ++pos) {
+            int64_t gr = latent_row(block_table, max_pages, num_pages, b, pos);
+            if (gr >= 0) g[n++] = gr;
+        }
+        attend_rows(q_bf16 + (r * H + h) * DQK, kv, g, n, scale, out + (ri * H + h) * DV,
+                    lse + ri * H + h, NULL);
+        free(g);
+    }
+}
+
+/* Merge of two partial attention results by their log-sum-exp ([mla] merge_attn_states(output,
+ * output_lse, prefix_output, prefix_lse, suffix_output, suffix_lse) in the chunked-context loop):
+ * lse = log(e^lse1 + e^lse2); o = e^(lse1 - lse) o1 + e^(lse2 - lse) o2.  Both -inf gives o = 0,
+ * lse = -inf.  n vectors of width dv. */
+void dsa_oracle_lse_merge(const double* o1, const double* lse1, const double* o2, const double* lse2,
+                          int64_t n, int32_t dv, double* o, double* lse) {
+    for (int64_t i = 0; i < n; ++i) {
+        double a = lse1[i], b = lse2[i];
+        double m = a > b ? a : b;
+        if (m == -INFINITY) {
+            lse[i] = -INFINITY;
+            for (int d = 0; d < dv; ++d) o[i * dv + d] = 0.0;
+            continue;
+        }
+        double l = exp(a - m) + exp(b - m);
+        double L = m + log(l);
+        double wa = exp(a - L), wb = exp(b - L);
+        for (int d = 0; d < dv; ++d) o[i * dv + d] = wa * o1[i * dv + d] + wb * o2[i * dv + d];
+        lse[i] = L;
+    }
+}
+
+int dsa_oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void dsa_oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
