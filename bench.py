@@ -1,0 +1,457 @@
+#!/usr/bin/env python
+"""Benchmark of the DSA decode step on GB300: query-tokens/s of one pass of the whole hot path
+(store this step's index keys -> indexer logits -> top-k -> sparse MLA), plus each stage's
+achieved HBM bandwidth against its roofline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Defaults: N = 1, K = 20, W = 5, workload decode_b64_logu64k (64 requests, contexts log-uniform in
+[4096, 65536], 1 query token each, top-k 2048, 128 MLA heads).  Under torchrun (N > 1) every rank
+runs its own independent batch (seed offset by the rank) with no collective on the data path;
+value = all ranks' query rows / the slowest rank's step time (weak scaling).
+
+``--impl reference`` times the CPU oracle (the plain C definition of the path) on the host cores,
+each step a bounded sample of the same workload; under torchrun only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "DSA decode query-tokens/s (indexer+top-k+sparse MLA); HBM GB/s vs roofline"
+UNIT = "query-tokens/s"
+DEFAULT_WORKLOAD = "decode_b64_logu64k"
+L2_FLUSH_BYTES = 256 << 20
+LAUNCHES_PER_STEP = 5       # store, logits, top-k, MLA split, MLA combine
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- algorithmic work
+
+def algorithmic_work(wl):
+    """Bytes (and FLOPs) each stage must move/compute at minimum, per step.
+    indexer: 132 B per visible key per request (K read once per request) + 4 B per (row, key)
+             logit written + q (bf16) and w (fp32) reads; 2*64*128 FLOP per (row, key).
+    top-k:   4 B per (row, visible key) read + 4k B per row written.
+    MLA:     per row: k * 1152 B gathered + q (H*576*2) + out (H*512*2) + idx (4k) + lse (4H);
+             2 * H * k_valid * (576 + 512) FLOP.
+    store:   per new token 256 B read + 132 B written + 8 B slot."""
+    import numpy as np
+    vis = wl.visible_lens().astype(np.int64)
+    keys_per_req = wl.seq_lens.astype(np.int64)
+    T, H, k = wl.T, wl.heads, wl.topk
+    kvalid = np.minimum(vis, k)
+    idx_b = int(keys_per_req.sum()) * 132 + int(vis.sum()) * 4 + T * 64 * 128 * 2 + T * 64 * 4
+    idx_f = int(vis.sum()) * 2 * 64 * 128
+    topk_b = int(vis.sum()) * 4 + T * k * 4
+    mla_b = int(kvalid.sum()) * 1152 + T * H * 576 * 2 + T * H * 512 * 2 + T * k * 4 + T * H * 4
+    mla_f = int(kvalid.sum()) * 2 * H * (576 + 512)
+    store_b = T * (256 + 132 + 8)
+    return {"store": (store_b, 0), "indexer": (idx_b, idx_f), "topk": (topk_b, 0), "mla": (mla_b, mla_f)}
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of this GPU's clocks and throttle reasons while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines = []
+        sel = []
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            sel = []
+        self.cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"] + sel
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- profile traffic
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, "deepseek_sparse_attention_paged_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(stage):
+    """DRAM bytes per launch from the committed ncu summary, only if the kernel source is unchanged."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(stage)
+    if not d:
+        return None
+    if d.get("source_hash") != kernel_source_hash(d["sources"]):
+        return None
+    return d.get("dram_bytes_per_launch_scaled", d.get("dram_bytes_per_launch"))
+
+
+STAGE_SOURCES = {"store": ["store_index_k.cu"], "indexer": ["indexer_logits.cu"], "topk": ["topk.cu"],
+                 "mla": ["sparse_mla.cu"]}
+
+
+# ----------------------------------------------------------------------------- CPU oracle arm
+
+def oracle_sample_step(wl, rows, pools, rng_rows=None):
+    """One decode step of the oracle for the given rows (their requests' index caches prebuilt):
+    store the rows' new keys, score, select, attend.  Returns rows processed."""
+    import numpy as np
+    import oracle
+    rows = np.asarray(rows, np.int64)
+    cu = wl.cu_q
+    new_ids = wl.new_token_ids()
+    for r in rows:
+        b = int(np.searchsorted(cu, r, side="right") - 1)
+        pool = pools[b]
+        oracle.store_index_k(wl.index_keys()[new_ids[r:r + 1]], wl.token_slots()[new_ids[r:r + 1]], pool)
+        lg = oracle.indexer_logits(wl.index_q(), wl.weights(), pool, wl.block_table, wl.seq_lens, wl.cu_q,
+                                   np.array([r]), wl.max_seq_len)
+        idx = oracle.topk(lg, wl.seq_lens, wl.cu_q, np.array([r]), wl.topk)
+        full = np.full((wl.T, wl.topk), -1, np.int32)
+        full[r] = idx[0]
+        oracle.sparse_mla(wl.mla_q(), wl.latent_pool(), wl.block_table, wl.seq_lens, wl.cu_q, full, wl.scale,
+                          np.array([r]))
+    return len(rows)
+
+
+def build_oracle_pools(wl, reqs):
+    import numpy as np
+    import oracle
+    starts = np.concatenate([[0], np.cumsum(wl.seq_lens.astype(np.int64))])
+    pools = {}
+    for b in sorted(set(reqs)):
+        pool = np.zeros((wl.num_pages, oracle.PAGE_BYTES), np.uint8)
+        oracle.store_index_k(wl.index_keys()[starts[b]:starts[b + 1]], wl.token_slots()[starts[b]:starts[b + 1]],
+                             pool)
+        pools[b] = pool
+    return pools
+
+
+def sample_rows(wl, n):
+    import numpy as np
+    # rows evenly spaced over the batch (one per request for decode workloads)
+    return np.unique(np.linspace(0, wl.T - 1, n).round().astype(np.int64))
+
+
+def cpu_oracle_rate(wl, steps, rows_per_step):
+    """Times the oracle on bounded samples: each step takes `rows_per_step` rows (evenly spaced over
+    the batch) and runs the whole path for them; the index cache of their requests is built first,
+    untimed (it is resident state, like the GPU's).  Returns (rows/s, cores, step times, rows)."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    rows = sample_rows(wl, rows_per_step * max(1, steps))
+    cu = wl.cu_q
+    times, done, used = [], 0, []
+    for s in range(steps):
+        sel = rows[(s * rows_per_step) % len(rows):][:rows_per_step]
+        reqs = [int(np.searchsorted(cu, r, side="right") - 1) for r in sel]
+        pools = build_oracle_pools(wl, reqs)
+        t0 = time.perf_counter()
+        done += oracle_sample_step(wl, sel, pools)
+        times.append(time.perf_counter() - t0)
+        used.extend(int(r) for r in sel)
+        del pools
+    return done / sum(times), oracle.num_threads(), times, used
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from deepseek_sparse_attention_paged_gb300 import workloads
+    wl = workloads.make(args.workload)
+    rows_per_step = 1
+    _, cores, _, _ = cpu_oracle_rate(wl, args.warmup, rows_per_step) if args.warmup > 0 else (0, 0, 0, 0)
+    rate, cores, times, rows = cpu_oracle_rate(wl, args.steps, rows_per_step)
+    ms = 1000.0 * sum(times) / max(1, len(times))
+    sample = (f"{rows_per_step} query row per step (rows evenly spaced over the {wl.T}-row batch, each with its "
+              f"full context: store its key, logits over its visible keys, top-{wl.topk}, {wl.heads}-head sparse "
+              f"MLA); index caches of the sampled requests prebuilt untimed")
+    line = {"metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": workload_config(wl),
+            "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def workload_config(wl):
+    import numpy as np
+    return {"workload": wl.name, "batch": wl.B, "query_rows": wl.T,
+            "context_min": int(wl.seq_lens.min()), "context_max": int(wl.seq_lens.max()),
+            "context_total": int(wl.seq_lens.astype(np.int64).sum()), "q_per_request": int(wl.max_q_len),
+            "topk": wl.topk, "mla_heads": wl.heads, "index_heads": 64, "index_dim": 128, "page_size": 64,
+            "index_pool_pages": wl.num_pages, "seed": wl.seed,
+            "l2": "flushed between timed steps (256 MiB write, untimed)",
+            "timing": "CUDA events around one CUDA-graph replay of the step per timed iteration"}
+
+
+def capture(fn, stream):
+    """CUDA graph of fn() on `stream`; returns (graph, kernels captured)."""
+    import torch
+    from deepseek_sparse_attention_paged_gb300 import capi
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()  # warm the path outside capture
+        torch.cuda.synchronize()
+        n0 = capi.launch_count()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        n = capi.launch_count() - n0
+    torch.cuda.synchronize()
+    return g, n
+
+
+def time_graph(g, stream, iters, flush):
+    """Per-iteration CUDA-event time (ms) of one replay; L2 flushed before each, untimed."""
+    import torch
+    pairs = []
+    with torch.cuda.stream(stream):
+        for _ in range(iters):
+            flush.fill_(1.0)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            pairs.append((a, b))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in pairs]
+
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+    from deepseek_sparse_attention_paged_gb300 import capi, workloads
+    from deepseek_sparse_attention_paged_gb300.build import build
+    from deepseek_sparse_attention_paged_gb300.pipeline import DeviceBatch
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        pg = dist
+    if rank == 0:
+        build()
+    if pg is not None:
+        pg.barrier()
+    capi.load()
+
+    wl = workloads.make(args.workload)
+    if rank > 0:   # every rank its own batch of the same shape (weak scaling)
+        wl = workloads.make_custom(wl.name, wl.seed + 1000 * rank, wl.seq_lens, wl.q_lens, wl.topk, wl.heads,
+                                   pool_pages=wl.num_pages)
+    db = DeviceBatch(wl)
+    stream = torch.cuda.Stream()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    step_graph, step_kernels = capture(lambda: db.step(), stream)
+    stage_graphs = {
+        "store": capture(lambda: db.store_new_keys(), stream),
+        "indexer": capture(lambda: db.indexer_logits(), stream),
+        "topk": capture(lambda: db.topk(), stream),
+        "mla": capture(lambda: db.sparse_mla(), stream),
+    }
+    st, word = db.device_error()
+    if st != 0:
+        raise RuntimeError(f"device error word {word} after warm-up")
+
+    # warm-up steps (untimed)
+    time_graph(step_graph, stream, args.warmup, flush)
+    if pg is not None:
+        pg.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall0 = time.perf_counter()
+        step_ms = time_graph(step_graph, stream, args.steps, flush)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+        # stage breakdown (each stage alone in its own graph, same flush discipline)
+        stage_iters = max(3, args.steps // 2)
+        stage_ms = {k: time_graph(g, stream, stage_iters, flush) for k, (g, _) in stage_graphs.items()}
+    timed_launches = step_kernels * args.steps + sum(n * stage_iters for _, n in stage_graphs.values())
+    if pg is not None:
+        pg.barrier()
+    torch.cuda.synchronize()
+    mean_step = sum(step_ms) / len(step_ms)
+    if pg is not None:
+        t = torch.tensor([mean_step], device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        mean_step = float(t.item())
+    value = wl.T * world / (mean_step / 1000.0)
+
+    # e2e: same step through the public API with host buffers (pinned), copies inside the timing
+    e2e = run_e2e(db, stream, args, flush)
+
+    if rank != 0:
+        return
+    hbm, bf16, peak_kind = measured_peaks()
+    work = algorithmic_work(wl)
+    stages = {}
+    for k, ms_list in stage_ms.items():
+        ms = sum(ms_list) / len(ms_list)
+        b, f = work[k]
+        stages[k] = {"ms": ms, "algorithmic_bytes": b, "flops": f, "gbs": b / (ms * 1e-3) / 1e9,
+                     "hbm_frac": (b / (ms * 1e-3) / 1e9) / hbm,
+                     "roofline_ms": max(b / (hbm * 1e9), f / (bf16 * 1e12)) * 1e3}
+    dominant = max(("indexer", "mla"), key=lambda k: stages[k]["ms"])
+    d = stages[dominant]
+    roofline = {"bound": "hbm", "achieved": d["gbs"], "peak": hbm, "unit": "GB/s", "frac": d["gbs"] / hbm,
+                "traffic": recorded_traffic(dominant), "kernel": dominant,
+                "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured" else
+                "fallback 6.8 TB/s"}
+    # CPU oracle baseline on a bounded sample (rank 0, N = 1 only)
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        rate, cores, times, rows = cpu_oracle_rate(wl, 8, 1)
+        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"8 query rows ({', '.join(str(int(r)) for r in rows)}) of the same batch, one per step, "
+                         f"each with its full context (store, logits, top-{wl.topk}, sparse MLA); "
+                         f"{sum(times):.1f} s of CPU time"}
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": mean_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp8e4m3+bf16", "data": "synthetic", "config": workload_config(wl),
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": timed_launches, "kernels_per_step": step_kernels,
+            "clocks": clk.summary(), "stages": stages, "wall_s_timed_region": t_wall}
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(db, stream, args, flush):
+    """Per step: H2D of the step's inputs from pinned host memory (queries, head gates, new keys and
+    slots, lengths, block table), the step, D2H of the attention output and lse."""
+    import torch
+    wl = db.wl
+    dev_bufs = [db.index_q, db.weights, db.mla_q, db.new_keys, db.new_slots, db.seq_lens, db.cu_q,
+                db.block_table]
+    host_in = [t.cpu().pin_memory() for t in dev_bufs]
+    host_out = [torch.empty_like(db.out, device="cpu").pin_memory(), torch.empty_like(db.lse, device="cpu").pin_memory()]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def one():
+        with torch.cuda.stream(stream):
+            for d, h in zip(dev_bufs, host_in):
+                d.copy_(h, non_blocking=True)
+            db.step(stream=stream)
+            host_out[0].copy_(db.out, non_blocking=True)
+            host_out[1].copy_(db.lse, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        one()
+        b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    ms = sum(times) / len(times)
+    return {"value": wl.T / (ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms, "api": "DeviceBatch.step() over the C ABI, ungraphed, inputs copied from pinned host"}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "native":
+        print("note: warm-up raised to 3 (minimum)", file=sys.stderr)
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

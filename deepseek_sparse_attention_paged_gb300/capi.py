@@ -1,0 +1,226 @@
+"""Thin Python binding of the C ABI in ``include/dsa.h`` (ctypes; argument marshalling only).
+
+Every function here has the name of the C entry point it calls, takes torch CUDA tensors, checks
+their dtype/shape/contiguity, passes raw device pointers and the caller's current CUDA stream,
+and raises :class:`DSAError` on a non-OK status.  All computation happens in the CUDA library;
+if the library is missing this module raises instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdsa_gb300.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "dsa.h")
+
+DSA_OK = 0
+DSA_ERR_INVALID_ARG = 1
+DSA_ERR_UNSUPPORTED = 2
+DSA_ERR_CUDA = 3
+DSA_ERR_DEVICE_BOUNDS = 4
+DSA_ERR_TIMEOUT = 5
+DSA_DEVERR_SLOT_RANGE = 0x1
+DSA_DEVERR_PAGE_RANGE = 0x2
+DSA_DEVERR_INDEX_RANGE = 0x4
+DSA_DEVERR_TIMEOUT = 0x8
+DSA_Q_ROTATE = 0x1
+PAGE_SIZE = 64
+INDEX_PAGE_BYTES = 64 * 132
+LATENT_DIM = 576
+VALUE_DIM = 512
+MAX_TOPK = 2048
+
+_lib = None
+_launches = 0   # kernels this process enqueued through the binding (graph captures included)
+
+
+def launch_count() -> int:
+    """Number of CUDA kernels enqueued through this binding so far (a captured launch counts once,
+    at capture)."""
+    return _launches
+
+
+def _count(n: int) -> None:
+    global _launches
+    _launches += n
+
+
+class DSAError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        msg = _lib.dsa_status_str(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{fn} failed: status {status} ({msg})")
+        self.status = status
+
+
+def load(path: str = LIB_PATH):
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library {path} is missing; build it with __graft_entry__.build() "
+                           "(there is no CPU fallback)")
+    lib = ctypes.CDLL(path)
+    P, i32, i64, u32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_size_t
+    sigs = {
+        "dsa_status_str": (ctypes.c_char_p, [ctypes.c_int]),
+        "dsa_store_index_k": (ctypes.c_int, [P, P, i64, P, i64, i32, P, P]),
+        "dsa_indexer_logits": (ctypes.c_int, [P, P, P, i64, P, i32, P, P, i32, i32, i32, i32, i32, P, i64, u32,
+                                              P, P]),
+        "dsa_topk_workspace_size": (sz, [i32, i32, i32]),
+        "dsa_topk": (ctypes.c_int, [P, i64, P, P, i32, i32, i32, i32, i32, P, P, sz, P]),
+        "dsa_sparse_mla_workspace_size": (sz, [i32, i32, i32]),
+        "dsa_sparse_mla_decode": (ctypes.c_int, [P, P, i64, P, i32, P, P, i32, P, i32, i32, i32, ctypes.c_float,
+                                                 P, P, P, sz, P, P]),
+        "dsa_read_device_error": (ctypes.c_int, [P, P, P]),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def header_functions(path: str = HEADER):
+    """Names of the functions declared in ``include/dsa.h``."""
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_[a-z0-9_]+)\s*\(", text)))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _need(cond: bool, what: str):
+    if not cond:
+        raise ValueError(what)
+
+
+def _cuda(t: torch.Tensor, dtype, name: str):
+    _need(t.is_cuda, f"{name} must be a CUDA tensor")
+    _need(t.dtype == dtype, f"{name} must be {dtype}, got {t.dtype}")
+    _need(t.is_contiguous(), f"{name} must be contiguous")
+
+
+def _check(fn: str, status: int):
+    if status != DSA_OK:
+        raise DSAError(fn, status)
+
+
+def dsa_store_index_k(k_bf16: torch.Tensor, slot_mapping: torch.Tensor, index_k_pool: torch.Tensor,
+                      dev_err: Optional[torch.Tensor] = None, stream=None) -> None:
+    lib = load()
+    _cuda(k_bf16, torch.bfloat16, "k_bf16")
+    _cuda(slot_mapping, torch.int64, "slot_mapping")
+    _cuda(index_k_pool, torch.uint8, "index_k_pool")
+    _need(k_bf16.dim() == 2 and k_bf16.shape[1] == 128, "k_bf16 must be [n, 128]")
+    _need(slot_mapping.numel() == k_bf16.shape[0], "slot_mapping must have n entries")
+    _need(index_k_pool.dim() == 2 and index_k_pool.shape[1] == INDEX_PAGE_BYTES, "pool must be [pages, 8448]")
+    _check("dsa_store_index_k", lib.dsa_store_index_k(
+        _ptr(k_bf16), _ptr(slot_mapping), k_bf16.shape[0], _ptr(index_k_pool), index_k_pool.shape[0], PAGE_SIZE,
+        _ptr(dev_err), _stream(stream)))
+    _count(1 if k_bf16.shape[0] > 0 else 0)
+
+
+def dsa_indexer_logits(q_bf16: torch.Tensor, weights: torch.Tensor, index_k_pool: torch.Tensor,
+                       block_table: torch.Tensor, seq_lens: torch.Tensor, cu_q: torch.Tensor,
+                       max_seq_len: int, max_q_len: int, logits: torch.Tensor, row_begin: int = 0,
+                       row_end: Optional[int] = None, flags: int = 0, dev_err: Optional[torch.Tensor] = None,
+                       stream=None) -> None:
+    lib = load()
+    _cuda(q_bf16, torch.bfloat16, "q_bf16")
+    _cuda(weights, torch.float32, "weights")
+    _cuda(index_k_pool, torch.uint8, "index_k_pool")
+    _cuda(block_table, torch.int32, "block_table")
+    _cuda(seq_lens, torch.int32, "seq_lens")
+    _cuda(cu_q, torch.int32, "cu_q")
+    _cuda(logits, torch.float32, "logits")
+    _need(q_bf16.dim() == 3 and tuple(q_bf16.shape[1:]) == (64, 128), "q_bf16 must be [T, 64, 128]")
+    T = q_bf16.shape[0]
+    _need(tuple(weights.shape) == (T, 64), "weights must be [T, 64]")
+    B = seq_lens.numel()
+    _need(cu_q.numel() == B + 1 and block_table.dim() == 2 and block_table.shape[0] == B, "metadata shapes")
+    row_end = T if row_end is None else row_end
+    _need(0 <= row_begin <= row_end <= T, "row range")
+    _need(logits.dim() == 2 and logits.shape[0] >= row_end - row_begin, "logits rows")
+    _check("dsa_indexer_logits", lib.dsa_indexer_logits(
+        _ptr(q_bf16), _ptr(weights), _ptr(index_k_pool), index_k_pool.shape[0], _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), _ptr(cu_q), B, int(max_seq_len), int(max_q_len), int(row_begin),
+        int(row_end), _ptr(logits), logits.stride(0), int(flags), _ptr(dev_err), _stream(stream)))
+    _count(1 if row_end > row_begin else 0)
+
+
+def dsa_topk_workspace_size(rows: int, k: int, max_seq_len: int) -> int:
+    return int(load().dsa_topk_workspace_size(int(rows), int(k), int(max_seq_len)))
+
+
+def dsa_topk(logits: torch.Tensor, seq_lens: torch.Tensor, cu_q: torch.Tensor, max_seq_len: int, k: int,
+             idx: torch.Tensor, row_begin: int = 0, row_end: Optional[int] = None,
+             workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    lib = load()
+    _cuda(logits, torch.float32, "logits")
+    _cuda(seq_lens, torch.int32, "seq_lens")
+    _cuda(cu_q, torch.int32, "cu_q")
+    _cuda(idx, torch.int32, "idx")
+    B = seq_lens.numel()
+    row_end = (row_begin + logits.shape[0]) if row_end is None else row_end
+    rows = row_end - row_begin
+    _need(idx.dim() == 2 and idx.shape[0] >= rows and idx.shape[1] == k, "idx must be [rows, k]")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("dsa_topk", lib.dsa_topk(
+        _ptr(logits), logits.stride(0), _ptr(seq_lens), _ptr(cu_q), B, int(max_seq_len), int(row_begin),
+        int(row_end), int(k), _ptr(idx), _ptr(workspace), ws_bytes, _stream(stream)))
+    _count(1 if rows > 0 else 0)
+
+
+def dsa_sparse_mla_workspace_size(T: int, H: int, k: int) -> int:
+    return int(load().dsa_sparse_mla_workspace_size(int(T), int(H), int(k)))
+
+
+def dsa_sparse_mla_decode(q_bf16: torch.Tensor, kv_pool: torch.Tensor, block_table: torch.Tensor,
+                          seq_lens: torch.Tensor, cu_q: torch.Tensor, idx: torch.Tensor, scale: float,
+                          out: torch.Tensor, workspace: torch.Tensor, lse: Optional[torch.Tensor] = None,
+                          dev_err: Optional[torch.Tensor] = None, stream=None) -> None:
+    lib = load()
+    _cuda(q_bf16, torch.bfloat16, "q_bf16")
+    _cuda(kv_pool, torch.bfloat16, "kv_pool")
+    _cuda(block_table, torch.int32, "block_table")
+    _cuda(seq_lens, torch.int32, "seq_lens")
+    _cuda(cu_q, torch.int32, "cu_q")
+    _cuda(idx, torch.int32, "idx")
+    _cuda(out, torch.bfloat16, "out")
+    _need(workspace.is_cuda and workspace.is_contiguous(), "workspace must be a contiguous CUDA tensor")
+    if lse is not None:
+        _cuda(lse, torch.float32, "lse")
+    _need(q_bf16.dim() == 3 and q_bf16.shape[2] == LATENT_DIM, "q_bf16 must be [T, H, 576]")
+    T, H, _ = q_bf16.shape
+    _need(kv_pool.dim() == 3 and tuple(kv_pool.shape[1:]) == (64, LATENT_DIM), "kv_pool must be [pages, 64, 576]")
+    _need(idx.dim() == 2 and idx.shape[0] == T, "idx must be [T, k]")
+    _need(tuple(out.shape) == (T, H, VALUE_DIM), "out must be [T, H, 512]")
+    B = seq_lens.numel()
+    _check("dsa_sparse_mla_decode", lib.dsa_sparse_mla_decode(
+        _ptr(q_bf16), _ptr(kv_pool), kv_pool.shape[0], _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+        _ptr(cu_q), B, _ptr(idx), idx.shape[1], T, H, float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_err), _stream(stream)))
+    _count(2 if T > 0 else 0)
+
+
+def dsa_read_device_error(dev_err: torch.Tensor, stream=None):
+    """Returns (status, raw word)."""
+    lib = load()
+    word = ctypes.c_int32(0)
+    st = lib.dsa_read_device_error(_ptr(dev_err), ctypes.byref(word), _stream(stream))
+    return int(st), int(word.value)

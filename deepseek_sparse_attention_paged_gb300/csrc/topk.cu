@@ -1,0 +1,167 @@
+// topk.cu -- per-row top-k of the indexer logits, deterministic.
+//
+// Follows sglang dsa_indexer.py, forward_indexer (topk(min(topk, seq_len)) of the row's logits,
+// then -1 padding) and Indexer._get_topk_paged (topk_transform over the paged logits).  The kept
+// set is the k largest of I[r, 0:v_r) with ties broken toward the lower index; it is written in
+// ascending index order and padded with -1.
+//
+// One 1024-thread CTA per row.  Logits map to order-preserving 32-bit keys (larger float ->
+// larger key; -0 and +0 share a key; NaN gets the smallest key).  A 3-digit MSB-first radix
+// select (11 + 11 + 10 bits, histograms in shared memory) finds the exact k-th largest key K and
+// how many of the keys equal to K are kept; a final pass in index order writes every index with
+// key > K plus the first (by index) of those equal to K.  The row is read 4 times, from L2.
+#include "dsa_common.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kTopkThreads = 1024;
+constexpr int kWarps = kTopkThreads / 32;
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+    uint32_t u = __float_as_uint(f);
+    if ((u & 0x7fffffffu) > 0x7f800000u) return 0u;   // NaN: never preferred
+    if (u == 0x80000000u) u = 0u;                      // -0 == +0
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Block-wide inclusive scan of one uint32 per thread; also returns the block total.
+__device__ __forceinline__ uint32_t block_inclusive_scan(uint32_t v, uint32_t* warp_tot, uint32_t* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t o = __shfl_up_sync(0xffffffffu, v, d);
+        if (lane >= d) v += o;
+    }
+    if (lane == 31) warp_tot[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t t = warp_tot[lane];
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t o = __shfl_up_sync(0xffffffffu, t, d);
+            if (lane >= d) t += o;
+        }
+        warp_tot[lane] = t;   // inclusive prefix of warp totals
+    }
+    __syncthreads();
+    const uint32_t before = warp == 0 ? 0u : warp_tot[warp - 1];
+    *total = warp_tot[kWarps - 1];
+    __syncthreads();   // warp_tot may be reused by the caller's next scan
+    return v + before;
+}
+
+struct TopkSmem {
+    uint32_t hist[2048];
+    uint32_t warp_tot[kWarps];
+    uint32_t sel_digit;
+    uint32_t sel_remaining;
+};
+
+// Given a histogram over `bins` digits (bins = 2048 or 1024), find the digit d such that
+// (# keys with digit > d) < need <= (# keys with digit >= d); store d and
+// need - (# keys with digit > d).
+__device__ void select_digit(TopkSmem& sm, int bins, uint32_t need) {
+    // thread t covers the digits (from the top) bins-1-2t and bins-2-2t (bins/1024 digits each)
+    const int per = bins / kTopkThreads;   // 2 or 1
+    uint32_t local = 0;
+    for (int i = 0; i < per; ++i) local += sm.hist[bins - 1 - (threadIdx.x * per + i)];
+    uint32_t total;
+    const uint32_t incl = block_inclusive_scan(local, sm.warp_tot, &total);
+    uint32_t above = incl - local;   // keys with digit greater than this thread's first digit
+    for (int i = 0; i < per; ++i) {
+        const int d = bins - 1 - (threadIdx.x * per + i);
+        const uint32_t c = sm.hist[d];
+        if (above < need && need <= above + c) {
+            sm.sel_digit = static_cast<uint32_t>(d);
+            sm.sel_remaining = need - above;
+        }
+        above += c;
+    }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kTopkThreads)
+topk_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* __restrict__ seq_lens,
+            const int32_t* __restrict__ cu_q, int B, int row_begin, int k, int32_t* __restrict__ idx) {
+    __shared__ TopkSmem sm;
+    const int rl = blockIdx.x;                  // local row
+    const int r = row_begin + rl;
+    const int b = row_request(cu_q, B, r);
+    const int q0 = __ldg(cu_q + b);
+    int v = visible_len(__ldg(seq_lens + b), __ldg(cu_q + b + 1) - q0, r - q0);
+    if (v > ld) v = static_cast<int>(ld);       // never read past the row
+    const float* row = logits + static_cast<int64_t>(rl) * ld;
+    int32_t* out = idx + static_cast<int64_t>(rl) * k;
+
+    if (v <= k) {   // short row: keep everything in index order
+        for (int j = threadIdx.x; j < k; j += kTopkThreads) out[j] = j < v ? j : -1;
+        return;
+    }
+
+    // ---- radix select of the k-th largest key
+    uint32_t prefix = 0, need = static_cast<uint32_t>(k);
+    const int shifts[3] = {21, 10, 0};
+    const int widths[3] = {11, 11, 10};
+    for (int pass = 0; pass < 3; ++pass) {
+        const int bins = 1 << widths[pass];
+        for (int i = threadIdx.x; i < bins; i += kTopkThreads) sm.hist[i] = 0;
+        __syncthreads();
+        const int hi_shift = shifts[pass] + widths[pass];   // bits above this digit must match
+        for (int s = threadIdx.x; s < v; s += kTopkThreads) {
+            const uint32_t key = order_key(__ldg(row + s));
+            const bool match = hi_shift >= 32 || (key >> hi_shift) == (prefix >> hi_shift);
+            if (match) atomicAdd(&sm.hist[(key >> shifts[pass]) & (bins - 1)], 1u);
+        }
+        __syncthreads();
+        select_digit(sm, bins, need);
+        prefix |= sm.sel_digit << shifts[pass];
+        need = sm.sel_remaining;
+        __syncthreads();
+    }
+    const uint32_t kth = prefix;
+    const uint32_t take_equal = need;           // keys equal to kth that are kept (lowest indices)
+
+    // ---- index-ordered compaction
+    uint32_t gt_base = 0, eq_base = 0;
+    for (int base = 0; base < v; base += kTopkThreads) {
+        const int s = base + threadIdx.x;
+        uint32_t key = 0;
+        bool valid = s < v;
+        if (valid) key = order_key(__ldg(row + s));
+        const uint32_t gt = (valid && key > kth) ? 1u : 0u;
+        const uint32_t eq = (valid && key == kth) ? 1u : 0u;
+        uint32_t total;
+        const uint32_t incl = block_inclusive_scan((gt << 16) | eq, sm.warp_tot, &total);
+        const uint32_t excl = incl - ((gt << 16) | eq);
+        const uint32_t gt_before = gt_base + (excl >> 16);
+        const uint32_t eq_before = eq_base + (excl & 0xffffu);
+        if (gt) out[gt_before + min(eq_before, take_equal)] = s;
+        else if (eq && eq_before < take_equal) out[gt_before + eq_before] = s;
+        gt_base += total >> 16;
+        eq_base += total & 0xffffu;
+    }
+}
+
+}  // namespace
+}  // namespace dsa
+
+extern "C" size_t dsa_topk_workspace_size(int32_t rows, int32_t k, int32_t max_seq_len) {
+    (void)rows; (void)k; (void)max_seq_len;
+    return 0;
+}
+
+extern "C" dsa_status dsa_topk(const float* logits, int64_t ld, const int32_t* seq_lens, const int32_t* cu_q,
+                               int32_t B, int32_t max_seq_len, int32_t row_begin, int32_t row_end, int32_t k,
+                               int32_t* idx, void* workspace, size_t workspace_bytes, void* stream) {
+    (void)workspace; (void)workspace_bytes;
+    if (k < 1 || k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
+    if (B < 0 || row_begin < 0 || row_end < row_begin || max_seq_len < 0) return DSA_ERR_INVALID_ARG;
+    if (row_end == row_begin) return DSA_OK;
+    if (B == 0 || !logits || !seq_lens || !cu_q || !idx) return DSA_ERR_INVALID_ARG;
+    if (ld < max_seq_len) return DSA_ERR_INVALID_ARG;
+    if (max_seq_len >= (1 << 16) * 1024) return DSA_ERR_UNSUPPORTED;
+    dsa::topk_kernel<<<row_end - row_begin, dsa::kTopkThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        logits, ld, seq_lens, cu_q, B, row_begin, k, idx);
+    return dsa::launch_status();
+}

@@ -1,0 +1,211 @@
+/*
+ * dsa.h -- C ABI of the GB300 (sm_103a) DeepSeek Sparse Attention decode path.
+ *
+ * Three stages run on one GPU, each a hand-written CUDA kernel:
+ *   1. lightning indexer: I[r,s] = sum_h w[r,h] * ReLU(q_I[r,h] . k_I[s]) over a paged FP8-E4M3
+ *      index-K cache with one fp32 scale per token (64 heads x 128 dims, page size 64);
+ *   2. per-row top-k over the logits (causal and length-masked, lower index wins ties);
+ *   3. absorbed-form sparse MLA over the selected rows of a paged 576-wide bf16 latent cache
+ *      (512 latent + 64 rope, one shared KV head, 512-wide latent output).
+ * A fourth call writes new keys into the index-K cache (Hadamard rotation, per-token FP8
+ * quantisation, paged scatter by slot).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Pointers.  Every array argument is a DEVICE pointer unless stated otherwise; scalars are passed
+ *   by value.  bf16 arrays are passed as `const void*` holding IEEE bfloat16 bit patterns.
+ * Ownership.  The caller owns every buffer.  The library never allocates or frees device memory
+ *   and keeps no state between calls; scratch space is passed in as `workspace` with its size
+ *   queried from the matching *_workspace_size() call.
+ * Streams.  `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls enqueue work on
+ *   it and return without synchronising; results are ready when the stream reaches them.
+ * Requests and rows.  B requests; request b has seq_lens[b] cached tokens (this step's tokens
+ *   included) and q_len_b = cu_q[b+1] - cu_q[b] query tokens; global query row r = cu_q[b] + j,
+ *   0 <= j < q_len_b, sits at absolute position p = seq_lens[b] - q_len_b + j and sees keys
+ *   [0, p], i.e. v_r = p + 1 keys (causal rule of the ragged key ends `ke = start + pos + 1` in
+ *   sglang dsa_indexer.py, Indexer._get_topk_ragged / forward, and sparse_mode=3 in vllm_ascend
+ *   sfa_v1.py).  T = cu_q[B] rows in total.
+ * Paging.  Page size is 64 tokens for both caches (sglang dsa_indexer.py,
+ *   Indexer._get_topk_paged: "only support page size 64").  One int32 block table
+ *   [B, max_pages] maps logical page i of request b to a physical page id; entries that are not
+ *   used may hold -1.  The same table serves the index-K cache and the latent cache (vllm_ascend
+ *   sfa_v1.py passes one block_table to the indexer and to the sparse attention).
+ * Index-K cache layout.  uint8 [num_pages, 64 * 132]: 132 bytes per token (sglang
+ *   Indexer._get_topk_paged: head_dim_with_sf = 132).  Inside a page: bytes [0, 8192) hold the
+ *   64 tokens' 128 FP8-E4M3FN codes row by row, bytes [8192, 8448) hold their 64 fp32 scales
+ *   (page-blocked; the pages fix the byte count, not the order inside a page).  The dequantised
+ *   key is code * scale.
+ * Latent cache layout.  bf16 [num_pages, 64, 576]: per token 512 latent dims then 64 rope dims
+ *   (vllm mla/common.py, MLACommonBackend: head size 576, one KV head).
+ * Errors.  Argument checks on the host return DSA_ERR_INVALID_ARG or DSA_ERR_UNSUPPORTED before
+ *   anything is enqueued.  A failed kernel launch returns DSA_ERR_CUDA.  Data-dependent problems
+ *   found on the device (a slot, page id or top-k index out of range) never fault: the access is
+ *   skipped and a bit is OR-ed into the optional device word `dev_err` (int32, caller-zeroed);
+ *   read it with dsa_read_device_error().
+ */
+#ifndef DSA_GB300_DSA_H
+#define DSA_GB300_DSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DSA_OK = 0,
+    DSA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, inconsistent arguments */
+    DSA_ERR_UNSUPPORTED = 2,   /* valid in principle, not implemented (page size != 64, ...) */
+    DSA_ERR_CUDA = 3,          /* a CUDA launch or runtime call failed */
+    DSA_ERR_DEVICE_BOUNDS = 4, /* the device error word reports skipped out-of-range accesses */
+    DSA_ERR_TIMEOUT = 5        /* the device error word reports a bounded wait that gave up */
+} dsa_status;
+
+/* Bits of the device error word. */
+#define DSA_DEVERR_SLOT_RANGE 0x1  /* store: slot past the pool (token skipped) */
+#define DSA_DEVERR_PAGE_RANGE 0x2  /* a block-table entry outside [0, num_pages) was needed */
+#define DSA_DEVERR_INDEX_RANGE 0x4 /* a top-k index outside [0, v_r) (entry skipped) */
+#define DSA_DEVERR_TIMEOUT 0x8     /* a bounded spin-wait gave up */
+
+/* Flags of dsa_indexer_logits. */
+#define DSA_Q_ROTATE 0x1u          /* Hadamard-rotate each query head before quantising it */
+
+/* Fixed shape constants of the path. */
+#define DSA_PAGE_SIZE 64
+#define DSA_INDEX_HEADS 64
+#define DSA_INDEX_DIM 128
+#define DSA_INDEX_ROW_BYTES 132
+#define DSA_INDEX_PAGE_BYTES (64 * 132)
+#define DSA_LATENT_DIM 576
+#define DSA_VALUE_DIM 512
+#define DSA_MAX_TOPK 2048
+
+/* Human-readable name of a status code (static string). */
+const char* dsa_status_str(dsa_status s);
+
+/*
+ * dsa_store_index_k -- write n new indexer keys into the paged FP8 index-K cache.
+ * Source: sglang dsa_indexer.py, Indexer._store_index_k_cache (fused_store_index_k_cache(key,
+ * buf, out_cache_loc, page_size), or act_quant(key, 128) followed by set_index_k_scale_buffer)
+ * and rotate_activation (Hadamard transform with scale 128^-0.5); vllm_ascend sfa_v1.py,
+ * indexer_select_pre_process (k @ hadamard) and the slot_mapping scatter.
+ * Per token t:
+ *   x = k_bf16[t, 0:128] (bf16 -> fp32, exact);
+ *   Walsh-Hadamard butterflies in fp32, Sylvester order (h = 1, 2, ..., 64: (a, b) -> (a+b, a-b));
+ *   y = bf16_rn(x * fp32(1/sqrt(128)));
+ *   scale = max(max_d |y_d|, 1e-4) / 448 (fp32, IEEE division);
+ *   code_d = E4M3FN round-to-nearest-even with saturation of (y_d / scale) (IEEE division);
+ *   page = slot >> 6, row = slot & 63: codes to bytes [row*128, row*128+128) of the page,
+ *   scale to bytes [8192 + row*4, +4).
+ * Arguments:
+ *   k_bf16        [n, 128] bf16, row-major (16-byte aligned).
+ *   slot_mapping  [n] int64; slot < 0 marks a padding token and is skipped.
+ *   n             number of tokens (0 is allowed and enqueues nothing).
+ *   index_k_pool  uint8 [num_pages, 8448] (16-byte aligned), written in place.
+ *   page_size     must be 64 (DSA_ERR_UNSUPPORTED otherwise).
+ *   dev_err       nullable; DSA_DEVERR_SLOT_RANGE when slot >= num_pages * 64 (token skipped).
+ * Results are bit-exact with the CPU definition above.
+ */
+dsa_status dsa_store_index_k(const void* k_bf16, const int64_t* slot_mapping, int64_t n,
+                             uint8_t* index_k_pool, int64_t num_pages, int32_t page_size,
+                             int32_t* dev_err, void* stream);
+
+/*
+ * dsa_indexer_logits -- lightning-indexer logits over the paged index-K cache.
+ * Source: sglang dsa_indexer.py, Indexer._get_topk_paged (paged MQA logits over block_tables /
+ * seqlens, kv cache viewed as [pages, 64, 1, 132]) with the head gate of _get_logits_head_gate
+ * (weights * q_scale); Indexer.forward_cuda (act_quant of the query per 128 dims);
+ * vllm_ascend sfa_v1.py, npu_lightning_indexer.
+ *   Query prologue, per row r and head h: optional Hadamard rotation (flag DSA_Q_ROTATE; same
+ *   steps as the key rotation above), then per-128 FP8 quantisation with scale q_scale[r,h]
+ *   (same rule as the keys); w'[r,h] = weights[r,h] * q_scale[r,h].
+ *   I[r,s] = sum_h w'[r,h] * ReLU(k_scale[s] * sum_d q_code[r,h,d] * k_code[s,d]),  s < v_r,
+ *   accumulated in fp32 (FP8 x FP8 products are exact in fp32).
+ * Arguments:
+ *   q_bf16       [T, 64, 128] bf16 (16-byte aligned).
+ *   weights      [T, 64] fp32 head gates (already scaled by 64^-0.5 * 128^-0.5 by the caller).
+ *   index_k_pool uint8 [num_pages, 8448] written by dsa_store_index_k (16-byte aligned).
+ *   block_table  int32 [B, max_pages]; seq_lens int32 [B]; cu_q int32 [B + 1] (device).
+ *   max_seq_len  host upper bound of seq_lens (sizes the launch; must be >= every seq_lens[b]).
+ *   max_q_len    host upper bound of the per-request query counts.
+ *   row_begin, row_end  host: the global rows [row_begin, row_end) to score (row tiling of a long
+ *                prefill chunk; pass 0, T for all rows).
+ *   logits       fp32 [row_end - row_begin, ld]; row r goes to logits[(r - row_begin) * ld].
+ *                Entries s >= v_r are left untouched.  ld >= max_seq_len.
+ *   flags        0 or DSA_Q_ROTATE.
+ *   dev_err      nullable; DSA_DEVERR_PAGE_RANGE when a needed page id is out of range (those
+ *                keys' logits are not written).
+ */
+dsa_status dsa_indexer_logits(const void* q_bf16, const float* weights, const uint8_t* index_k_pool,
+                              int64_t num_pages, const int32_t* block_table, int32_t max_pages,
+                              const int32_t* seq_lens, const int32_t* cu_q, int32_t B,
+                              int32_t max_seq_len, int32_t max_q_len, int32_t row_begin,
+                              int32_t row_end, float* logits, int64_t ld, uint32_t flags,
+                              int32_t* dev_err, void* stream);
+
+/*
+ * dsa_topk -- per-row top-k of the indexer logits.
+ * Source: sglang dsa_indexer.py, forward_indexer (logits.topk(min(topk, seq_len)) then -1
+ * padding to 2048), Indexer._get_topk_paged (topk_transform; rows not scored are -1).
+ *   For row r the kept set is the min(k, v_r) largest I[r, 0:v_r) with ties broken toward the
+ *   lower index (a stable descending order); -0 equals +0; NaN is never kept ahead of a number.
+ *   idx[r] lists the kept indices in ASCENDING index order, then -1 up to k.  Logits at
+ *   s >= v_r are never read.
+ * Arguments:
+ *   logits      fp32 rows as written by dsa_indexer_logits for [row_begin, row_end), stride ld.
+ *   k           1 .. 2048.
+ *   idx         int32 [row_end - row_begin, k].
+ *   workspace   device scratch of dsa_topk_workspace_size(rows, k, max_seq_len) bytes (may be
+ *               NULL when that size is 0).
+ * Output is deterministic and bit-exact with the CPU definition.
+ */
+size_t dsa_topk_workspace_size(int32_t rows, int32_t k, int32_t max_seq_len);
+dsa_status dsa_topk(const float* logits, int64_t ld, const int32_t* seq_lens, const int32_t* cu_q,
+                    int32_t B, int32_t max_seq_len, int32_t row_begin, int32_t row_end, int32_t k,
+                    int32_t* idx, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * dsa_sparse_mla_decode -- absorbed sparse MLA over the selected latent rows.
+ * Source: vllm_ascend sfa_v1.py, _execute_sparse_flash_attention_process
+ * (npu_sparse_flash_attention(query = ql_nope, key = value = latent cache, sparse_indices =
+ * top-k, sparse_block_size = 1, block_table, query_rope = q_pe, key_rope)); vllm mla/common.py,
+ * MLACommonImpl.forward decode branch (absorbed query [ql_nope 512, q_pe 64], _forward_decode
+ * returns (out, lse); merge_attn_states combines partial results by log-sum-exp).
+ *   For row r and head h, over every valid entry i of idx[r, 0:k) (valid: 0 <= i < v_r; -1 is
+ *   padding): g(i) = block_table[b][i >> 6] * 64 + (i & 63);
+ *   S_i = scale * <q[r,h,0:576], C[g(i),0:576]>; P = softmax(S);
+ *   out[r,h,0:512] = bf16_rn(sum_i P_i * C[g(i),0:512]);  lse[r,h] = max S + ln sum exp(S - max S).
+ *   A row with no valid entry gives out = 0 and lse = -inf.  Accumulation in fp32; the work is
+ *   split over the selected entries and the partial results are merged by log-sum-exp.
+ * Arguments:
+ *   q_bf16      [T, H, 576] bf16 (16-byte aligned); H in {16, 32, 64, 128}.
+ *   kv_pool     bf16 [num_pages, 64, 576] (16-byte aligned).
+ *   idx         int32 [T, k] logical positions within the request (as dsa_topk writes them).
+ *   k           1 .. 2048.  T: number of rows (= cu_q[B]).
+ *   scale       softmax scale (1/sqrt(192) for the DeepSeek configuration).
+ *   out_bf16    [T, H, 512] bf16.   lse: fp32 [T, H], nullable.
+ *   workspace   device scratch of dsa_sparse_mla_workspace_size(T, H, k) bytes.
+ *   dev_err     nullable; DSA_DEVERR_INDEX_RANGE for an index >= v_r, DSA_DEVERR_PAGE_RANGE for an
+ *               unmapped page (the entry is skipped either way).
+ */
+size_t dsa_sparse_mla_workspace_size(int32_t T, int32_t H, int32_t k);
+dsa_status dsa_sparse_mla_decode(const void* q_bf16, const void* kv_pool, int64_t num_pages,
+                                 const int32_t* block_table, int32_t max_pages,
+                                 const int32_t* seq_lens, const int32_t* cu_q, int32_t B,
+                                 const int32_t* idx, int32_t k, int32_t T, int32_t H, float scale,
+                                 void* out_bf16, float* lse, void* workspace,
+                                 size_t workspace_bytes, int32_t* dev_err, void* stream);
+
+/*
+ * dsa_read_device_error -- synchronise `stream`, copy the device error word to the host
+ * (*host_word, nullable) and map it: 0 -> DSA_OK, a timeout bit -> DSA_ERR_TIMEOUT, any range
+ * bit -> DSA_ERR_DEVICE_BOUNDS.  Does not clear the word.
+ */
+dsa_status dsa_read_device_error(const int32_t* dev_err, int32_t* host_word, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_GB300_DSA_H */

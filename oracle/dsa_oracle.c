@@ -81,21 +81,32 @@ double dsa_oracle_e4m3_decode(uint8_t c) {
     return s ? -v : v;
 }
 
+/* Values of the 127 non-negative finite codes 0x00 .. 0x7e, in increasing order (the E4M3FN
+ * encoding is monotonic for non-negative values), filled from the decoder when the library loads. */
+static double e4m3_pos_values[127];
+
+__attribute__((constructor)) static void e4m3_table_init(void) {
+    for (int c = 0; c <= 0x7e; ++c) e4m3_pos_values[c] = dsa_oracle_e4m3_decode((uint8_t)c);
+}
+
 /* fp32 -> E4M3FN, round to nearest with ties to even code, saturating to +-448 (no value maps to
- * NaN except NaN).  Written as a search over the 127 non-negative finite codes, whose values
- * increase with the code: find the two neighbours of |x| and take the nearer one; on an exact tie
- * take the one whose code is even (an even code has an even mantissa LSB).  The sign bit is kept,
- * so -0 and negative values that round to zero give code 0x80. */
+ * NaN except NaN).  Find the two codes whose values bracket |x| (binary search in the increasing
+ * table of non-negative code values) and take the nearer one; on an exact tie take the one whose
+ * code is even (an even code has an even mantissa LSB).  The sign bit is kept, so -0 and negative
+ * values that round to zero give code 0x80. */
 uint8_t dsa_oracle_e4m3_encode(float x) {
     if (isnan(x)) return 0x7f;
     uint8_t sign = signbit(x) ? 0x80 : 0x00;
     double a = fabs((double)x);
     if (a >= 448.0) return (uint8_t)(sign | 0x7e);
-    int lo = 0;
-    for (int c = 0; c <= 0x7e; ++c)
-        if (dsa_oracle_e4m3_decode((uint8_t)c) <= a) lo = c;
-    double vlo = dsa_oracle_e4m3_decode((uint8_t)lo);
-    double vhi = dsa_oracle_e4m3_decode((uint8_t)(lo + 1));
+    /* lo = largest code with value <= a (exists: code 0 has value 0 <= a) */
+    int lo = 0, hi = 0x7e;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) / 2;
+        if (e4m3_pos_values[mid] <= a) lo = mid; else hi = mid - 1;
+    }
+    double vlo = e4m3_pos_values[lo];
+    double vhi = e4m3_pos_values[lo + 1];
     double dlo = a - vlo, dhi = vhi - a;
     int c;
     if (dlo < dhi) c = lo;

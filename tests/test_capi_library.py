@@ -1,0 +1,43 @@
+"""CPU checks of the C-ABI library: it builds, loads without a GPU, and exports every function
+that include/dsa.h declares.  No compute call is made here."""
+import ctypes
+import os
+
+import pytest
+
+from deepseek_sparse_attention_paged_gb300 import build, capi
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return ctypes.CDLL(capi.LIB_PATH)
+
+
+def test_header_declares_the_four_path_calls():
+    names = capi.header_functions()
+    for n in ("dsa_store_index_k", "dsa_indexer_logits", "dsa_topk", "dsa_sparse_mla_decode"):
+        assert n in names
+
+
+def test_library_exports_every_header_symbol(lib):
+    for name in capi.header_functions():
+        assert hasattr(lib, name), f"{name} declared in include/dsa.h but not exported"
+
+
+def test_status_strings_and_host_side_validation(lib):
+    capi.load()
+    assert capi._lib.dsa_status_str(0) == b"ok"
+    assert capi._lib.dsa_status_str(2).startswith(b"unsupported")
+    # argument checks return before touching the GPU
+    L = capi._lib
+    assert L.dsa_store_index_k(None, None, 0, None, 0, 64, None, None) == 0          # n = 0: nothing to do
+    assert L.dsa_store_index_k(None, None, 4, None, 1, 32, None, None) == 2          # page size 32
+    assert L.dsa_store_index_k(None, None, 4, None, 1, 64, None, None) == 1          # null pointers
+    assert L.dsa_topk(None, 0, None, None, 1, 0, 0, 1, 0, None, None, 0, None) == 2  # k = 0
+    assert L.dsa_topk(None, 0, None, None, 1, 0, 0, 1, 4096, None, None, 0, None) == 2
+    assert L.dsa_sparse_mla_decode(None, None, 0, None, 0, None, None, 1, None, 64, 1, 24, 0.1, None, None,
+                                   None, 0, None, None) == 2                          # H = 24
+    assert L.dsa_indexer_logits(None, None, None, 0, None, 0, None, None, 1, 10, 1, 0, 1, None, 10, 0x10,
+                                None, None) == 1                                      # unknown flag
+    assert L.dsa_sparse_mla_workspace_size(64, 128, 2048) > 0

@@ -1,0 +1,131 @@
+"""GPU parity of dsa_topk (bit-exact) and dsa_sparse_mla_decode (tolerance) against the CPU oracle,
+each fed the same oracle-side inputs, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from deepseek_sparse_attention_paged_gb300 import capi, workloads
+from deepseek_sparse_attention_paged_gb300.pipeline import DeviceBatch
+
+from helpers import bf16_to_np_f64, check_attention, oracle_pool
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu_topk(logits_np, seq_lens, q_lens, k, max_seq_len=None):
+    seq_lens = np.asarray(seq_lens, np.int32)
+    cu = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    T = int(cu[-1])
+    ld = logits_np.shape[1]
+    lg = torch.from_numpy(np.ascontiguousarray(logits_np, np.float32)).cuda()
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    msl = int(seq_lens.max()) if max_seq_len is None else max_seq_len
+    ws_n = capi.dsa_topk_workspace_size(T, k, msl)
+    ws = torch.empty(max(1, ws_n), dtype=torch.uint8, device="cuda")
+    capi.dsa_topk(lg, torch.from_numpy(seq_lens).cuda(), torch.from_numpy(cu).cuda(), msl, k, idx, workspace=ws)
+    ref = oracle.topk(logits_np, seq_lens, cu, np.arange(T), k)
+    return idx.cpu().numpy(), ref
+
+
+def test_topk_on_oracle_logits_tiny():
+    wl = workloads.make("tiny")
+    pool = oracle_pool(wl)
+    lg = oracle.indexer_logits(wl.index_q(), wl.weights(), pool, wl.block_table, wl.seq_lens, wl.cu_q,
+                               np.arange(wl.T), wl.max_seq_len)
+    got, ref = _gpu_topk(lg, wl.seq_lens, wl.q_lens, wl.topk)
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("v,k", [(0, 16), (1, 16), (15, 16), (16, 16), (17, 16), (2048, 2048), (2049, 2048),
+                                 (5000, 2048), (70000, 2048), (131072, 2048), (3000, 1), (3000, 1999)])
+def test_topk_lengths_and_ties(v, k):
+    rng = np.random.default_rng(200 + v + k)
+    width = max(v, 4)
+    lg = np.full((3, width + 4), np.nan, np.float32)
+    lg[0, :v] = rng.standard_normal(v).astype(np.float32)
+    lg[1, :v] = rng.integers(-8, 8, v).astype(np.float32)            # heavy ties
+    lg[2, :v] = np.where(rng.random(v) < 0.5, -0.0, 0.0)              # all zeros of both signs
+    if v > 10:
+        lg[2, 3] = np.nan
+        lg[2, 7] = -np.inf
+        lg[0, 5] = np.inf
+    got, ref = _gpu_topk(lg, [v, v, v], [1, 1, 1], k, max_seq_len=max(v, 1))
+    assert np.array_equal(got, ref)
+
+
+def test_topk_next_n_rows_use_their_own_length():
+    rng = np.random.default_rng(210)
+    L = 3000
+    lg = rng.standard_normal((2, L)).astype(np.float32)
+    lg[:, L - 1] = 100.0      # only row 1 can see the last key
+    got, ref = _gpu_topk(lg, [L], [2], 256)
+    assert np.array_equal(got, ref)
+    assert L - 1 not in got[0] and L - 1 in got[1]
+
+
+def _mla_case(wl, idx, expect_bad=0):
+    db = DeviceBatch(wl, with_latent=True, build_index_cache=False)
+    db.sparse_mla(idx=torch.from_numpy(idx).cuda())
+    out = bf16_to_np_f64(db.out)
+    lse = db.lse.cpu().numpy().astype(np.float64)
+    ref_o, ref_l, _, bad = oracle.sparse_mla(wl.mla_q(), wl.latent_pool(), wl.block_table, wl.seq_lens, wl.cu_q,
+                                             idx, wl.scale, np.arange(wl.T), want_psum=True)
+    assert bad == expect_bad
+    err = check_attention(out, lse, ref_o, ref_l)
+    return db, err
+
+
+def _random_idx(wl, k, fill, rng):
+    idx = np.full((wl.T, k), -1, np.int32)
+    vis = wl.visible_lens()
+    for r in range(wl.T):
+        n = min(int(fill * k), int(vis[r]))
+        idx[r, :n] = np.sort(rng.choice(int(vis[r]), n, replace=False))
+    return idx
+
+
+@pytest.mark.parametrize("H", [16, 32, 64, 128])
+def test_mla_random_selection(H):
+    rng = np.random.default_rng(300 + H)
+    wl = workloads.make_custom("mla", 300 + H, [3000, 700, 129], 1, topk=512, heads=H)
+    _mla_case(wl, _random_idx(wl, 512, 0.9, rng))
+
+
+def test_mla_tiny_full_k_several_splits():
+    rng = np.random.default_rng(311)
+    wl = workloads.make_custom("mla2k", 311, [5000, 2048, 2100], 1, topk=2048, heads=128)
+    idx = _random_idx(wl, 2048, 1.0, rng)
+    _mla_case(wl, idx)
+
+
+def test_mla_empty_rows_and_unsorted_entries():
+    rng = np.random.default_rng(312)
+    wl = workloads.make_custom("mla_e", 312, [400, 400], 1, topk=256, heads=16)
+    idx = _random_idx(wl, 256, 0.5, rng)
+    idx[1] = -1                                  # no valid entry: out = 0, lse = -inf
+    idx[0, :128] = rng.permutation(idx[0, :128])  # order inside the list does not matter
+    db, _ = _mla_case(wl, idx)
+    assert float(db.out[1].abs().max()) == 0.0
+    assert bool(torch.isneginf(db.lse[1]).all())
+
+
+def test_mla_out_of_range_entries_are_skipped_and_reported():
+    rng = np.random.default_rng(313)
+    wl = workloads.make_custom("mla_bad", 313, [500, 300], 1, topk=128, heads=32)
+    idx = _random_idx(wl, 128, 0.5, rng)
+    idx[0, 100] = 500          # == v: future position
+    idx[1, 120] = 10 ** 6
+    db, _ = _mla_case(wl, idx, expect_bad=2)
+    st, word = db.device_error()
+    assert st == capi.DSA_ERR_DEVICE_BOUNDS and word & capi.DSA_DEVERR_INDEX_RANGE
+
+
+def test_mla_workspace_too_small_is_rejected():
+    wl = workloads.make_custom("mla_ws", 314, [300], 1, topk=64, heads=16)
+    db = DeviceBatch(wl, with_latent=True, build_index_cache=False)
+    idx = torch.full((1, 64), -1, dtype=torch.int32, device="cuda")
+    with pytest.raises(capi.DSAError) as e:
+        capi.dsa_sparse_mla_decode(db.mla_q, db.kv_pool, db.block_table, db.seq_lens, db.cu_q, idx, wl.scale,
+                                   db.out, db.mla_ws[:16])
+    assert e.value.status == capi.DSA_ERR_INVALID_ARG
