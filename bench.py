@@ -92,7 +92,7 @@ class ClockSampler:
             sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
         except Exception:
             sel = []
-        self.cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"] + sel
+        self.cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"] + sel
 
     def __enter__(self):
         try:
@@ -206,18 +206,20 @@ def sample_rows(wl, n):
     return np.unique(np.linspace(0, wl.T - 1, n).round().astype(np.int64))
 
 
-def cpu_oracle_rate(wl, steps, rows_per_step):
+def cpu_oracle_rate(wl, steps, rows_per_step, min_seconds=0.0):
     """Times the oracle on bounded samples: each step takes `rows_per_step` rows (evenly spaced over
-    the batch) and runs the whole path for them; the index cache of their requests is built first,
-    untimed (it is resident state, like the GPU's).  Returns (rows/s, cores, step times, rows)."""
+    the batch, cycling) and runs the whole path for them; the index cache of their requests is
+    built first, untimed (it is resident state, like the GPU's).  Runs `steps` steps, and more until
+    `min_seconds` of timed CPU work have accumulated.  Returns (rows/s, cores, step times, rows)."""
     import numpy as np
     import oracle
     oracle.build()
-    rows = sample_rows(wl, rows_per_step * max(1, steps))
+    rows = sample_rows(wl, min(wl.T, 64))
     cu = wl.cu_q
     times, done, used = [], 0, []
-    for s in range(steps):
-        sel = rows[(s * rows_per_step) % len(rows):][:rows_per_step]
+    s = 0
+    while s < steps or sum(times) < min_seconds:
+        sel = [rows[(s * rows_per_step + i) % len(rows)] for i in range(rows_per_step)]
         reqs = [int(np.searchsorted(cu, r, side="right") - 1) for r in sel]
         pools = build_oracle_pools(wl, reqs)
         t0 = time.perf_counter()
@@ -225,6 +227,7 @@ def cpu_oracle_rate(wl, steps, rows_per_step):
         times.append(time.perf_counter() - t0)
         used.extend(int(r) for r in sel)
         del pools
+        s += 1
     return done / sum(times), oracle.num_threads(), times, used
 
 
@@ -335,12 +338,13 @@ def run_gpu(args):
     if st != 0:
         raise RuntimeError(f"device error word {word} after warm-up")
 
+    clk = ClockSampler(local).__enter__()   # samples from warm-up through the e2e run
     # warm-up steps (untimed)
     time_graph(step_graph, stream, args.warmup, flush)
     if pg is not None:
         pg.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+    if True:
         t_wall0 = time.perf_counter()
         step_ms = time_graph(step_graph, stream, args.steps, flush)
         torch.cuda.synchronize()
@@ -361,6 +365,7 @@ def run_gpu(args):
 
     # e2e: same step through the public API with host buffers (pinned), copies inside the timing
     e2e = run_e2e(db, stream, args, flush)
+    clk.__exit__(None, None, None)
 
     if rank != 0:
         return
@@ -382,11 +387,12 @@ def run_gpu(args):
     # CPU oracle baseline on a bounded sample (rank 0, N = 1 only)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        rate, cores, times, rows = cpu_oracle_rate(wl, 8, 1)
+        rate, cores, times, rows = cpu_oracle_rate(wl, 8, 1, min_seconds=10.0)
         cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": f"8 query rows ({', '.join(str(int(r)) for r in rows)}) of the same batch, one per step, "
-                         f"each with its full context (store, logits, top-{wl.topk}, sparse MLA); "
-                         f"{sum(times):.1f} s of CPU time"}
+               "sample": f"{len(rows)} query rows of the same batch (rows evenly spaced, cycling), one per step, "
+                         f"each with its full context (store its key, logits over its visible keys, "
+                         f"top-{wl.topk}, {wl.heads}-head sparse MLA); {sum(times):.1f} s of timed CPU work; "
+                         f"the sampled requests' index caches built untimed"}
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": mean_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "fp8e4m3+bf16", "data": "synthetic", "config": workload_config(wl),

@@ -115,6 +115,13 @@ def _cuda(t: torch.Tensor, dtype, name: str):
     _need(t.is_contiguous(), f"{name} must be contiguous")
 
 
+def _rows(t: torch.Tensor, dtype, name: str):
+    """2-D tensor whose rows may be strided (the row stride is passed as ld) but are dense."""
+    _need(t.is_cuda, f"{name} must be a CUDA tensor")
+    _need(t.dtype == dtype, f"{name} must be {dtype}, got {t.dtype}")
+    _need(t.dim() == 2 and (t.stride(1) == 1 or t.shape[1] <= 1), f"{name} rows must be dense")
+
+
 def _check(fn: str, status: int):
     if status != DSA_OK:
         raise DSAError(fn, status)
@@ -147,7 +154,7 @@ def dsa_indexer_logits(q_bf16: torch.Tensor, weights: torch.Tensor, index_k_pool
     _cuda(block_table, torch.int32, "block_table")
     _cuda(seq_lens, torch.int32, "seq_lens")
     _cuda(cu_q, torch.int32, "cu_q")
-    _cuda(logits, torch.float32, "logits")
+    _rows(logits, torch.float32, "logits")
     _need(q_bf16.dim() == 3 and tuple(q_bf16.shape[1:]) == (64, 128), "q_bf16 must be [T, 64, 128]")
     T = q_bf16.shape[0]
     _need(tuple(weights.shape) == (T, 64), "weights must be [T, 64]")
@@ -171,7 +178,7 @@ def dsa_topk(logits: torch.Tensor, seq_lens: torch.Tensor, cu_q: torch.Tensor, m
              idx: torch.Tensor, row_begin: int = 0, row_end: Optional[int] = None,
              workspace: Optional[torch.Tensor] = None, stream=None) -> None:
     lib = load()
-    _cuda(logits, torch.float32, "logits")
+    _rows(logits, torch.float32, "logits")
     _cuda(seq_lens, torch.int32, "seq_lens")
     _cuda(cu_q, torch.int32, "cu_q")
     _cuda(idx, torch.int32, "idx")

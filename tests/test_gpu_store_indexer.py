@@ -120,6 +120,7 @@ def test_logits_invalid_args():
     wl = workloads.make("tiny")
     db = DeviceBatch(wl, with_latent=False)
     with pytest.raises(capi.DSAError) as e:
+        narrow = torch.empty((wl.T, 10), dtype=torch.float32, device="cuda")   # ld = 10 < max_seq_len
         capi.dsa_indexer_logits(db.index_q, db.weights, db.index_pool, db.block_table, db.seq_lens, db.cu_q,
-                                wl.max_seq_len, 1, db.logits[:, :10])   # ld < max_seq_len
+                                wl.max_seq_len, 1, narrow)
     assert e.value.status == capi.DSA_ERR_INVALID_ARG
