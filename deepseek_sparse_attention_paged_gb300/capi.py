@@ -78,6 +78,8 @@ def load(path: str = LIB_PATH):
         "dsa_sparse_mla_decode": (ctypes.c_int, [P, P, i64, P, i32, P, P, i32, P, i32, i32, i32, ctypes.c_float,
                                                  P, P, P, sz, P, P]),
         "dsa_read_device_error": (ctypes.c_int, [P, P, P]),
+        "dsa_sparse_mla_decode_noalloc": (ctypes.c_int, [P, P, i64, P, i32, P, P, i32, P, i32, i32, i32,
+                                                         ctypes.c_float, P, P, P, P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -222,6 +224,36 @@ def dsa_sparse_mla_decode(q_bf16: torch.Tensor, kv_pool: torch.Tensor, block_tab
         _ptr(q_bf16), _ptr(kv_pool), kv_pool.shape[0], _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
         _ptr(cu_q), B, _ptr(idx), idx.shape[1], T, H, float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(dev_err), _stream(stream)))
+    _count(2 if T > 0 else 0)
+
+
+def dsa_sparse_mla_decode_noalloc(q_bf16: torch.Tensor, kv_pool: torch.Tensor, block_table: torch.Tensor,
+                                  seq_lens: torch.Tensor, cu_q: torch.Tensor, idx: torch.Tensor, scale: float,
+                                  out: torch.Tensor, lse: Optional[torch.Tensor] = None,
+                                  dev_err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """dsa_sparse_mla_decode without a workspace argument: the library's fixed 32 MiB scratch is
+    used, for callers that may not allocate device memory.  Larger problems raise DSAError
+    (DSA_ERR_UNSUPPORTED)."""
+    lib = load()
+    _cuda(q_bf16, torch.bfloat16, "q_bf16")
+    _cuda(kv_pool, torch.bfloat16, "kv_pool")
+    _cuda(block_table, torch.int32, "block_table")
+    _cuda(seq_lens, torch.int32, "seq_lens")
+    _cuda(cu_q, torch.int32, "cu_q")
+    _cuda(idx, torch.int32, "idx")
+    _cuda(out, torch.bfloat16, "out")
+    if lse is not None:
+        _cuda(lse, torch.float32, "lse")
+    _need(q_bf16.dim() == 3 and q_bf16.shape[2] == LATENT_DIM, "q_bf16 must be [T, H, 576]")
+    T, H, _ = q_bf16.shape
+    _need(kv_pool.dim() == 3 and tuple(kv_pool.shape[1:]) == (64, LATENT_DIM), "kv_pool must be [pages, 64, 576]")
+    _need(idx.dim() == 2 and idx.shape[0] == T, "idx must be [T, k]")
+    _need(tuple(out.shape) == (T, H, VALUE_DIM), "out must be [T, H, 512]")
+    B = seq_lens.numel()
+    _check("dsa_sparse_mla_decode_noalloc", lib.dsa_sparse_mla_decode_noalloc(
+        _ptr(q_bf16), _ptr(kv_pool), kv_pool.shape[0], _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+        _ptr(cu_q), B, _ptr(idx), idx.shape[1], T, H, float(scale), _ptr(out), _ptr(lse), _ptr(dev_err),
+        _stream(stream)))
     _count(2 if T > 0 else 0)
 
 

@@ -198,6 +198,31 @@ dsa_status dsa_sparse_mla_decode(const void* q_bf16, const void* kv_pool, int64_
                                  size_t workspace_bytes, int32_t* dev_err, void* stream);
 
 /*
+ * dsa_sparse_mla_decode_noalloc -- dsa_sparse_mla_decode for callers that cannot allocate.
+ * The source pages have no counterpart of this call; it exists for callers that may not
+ * allocate device memory while they run attention (an engine plugin whose per-step hook must
+ * not allocate because the engine owns and budgets all device memory, a loop whose caching
+ * allocator already holds the free memory, code running during CUDA graph capture).
+ * Same arguments, semantics and kernels as dsa_sparse_mla_decode, minus the workspace: the
+ * split-K scratch is a fixed 32 MiB array inside the library, which every GPU that loads the
+ * library holds until the process exits.  The call allocates and frees nothing.
+ *   Limit: problems with dsa_sparse_mla_workspace_size(T, H, k) > 32 MiB are rejected with
+ *   DSA_ERR_UNSUPPORTED before anything is enqueued (at k = 2048, H = 128 that is T > 15 rows).
+ *   Set-up: the first call on each device looks up the array's device address with that device
+ *   current; make that first call before any stream capture.
+ *   Sharing: every call uses the same array.  Calls whose kernels overlap on the GPU (different
+ *   streams, or different host threads, without ordering between them) race on it: order them,
+ *   e.g. on one stream.  Nothing in the array has to start at zero; a call never reads what an
+ *   earlier call left there.
+ */
+dsa_status dsa_sparse_mla_decode_noalloc(const void* q_bf16, const void* kv_pool, int64_t num_pages,
+                                         const int32_t* block_table, int32_t max_pages,
+                                         const int32_t* seq_lens, const int32_t* cu_q, int32_t B,
+                                         const int32_t* idx, int32_t k, int32_t T, int32_t H,
+                                         float scale, void* out_bf16, float* lse, int32_t* dev_err,
+                                         void* stream);
+
+/*
  * dsa_read_device_error -- synchronise `stream`, copy the device error word to the host
  * (*host_word, nullable) and map it: 0 -> DSA_OK, a timeout bit -> DSA_ERR_TIMEOUT, any range
  * bit -> DSA_ERR_DEVICE_BOUNDS.  Does not clear the word.

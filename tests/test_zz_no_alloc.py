@@ -1,0 +1,74 @@
+"""dsa_sparse_mla_decode_noalloc: the sparse-MLA entry point for callers that may not allocate device
+memory (it takes no workspace and uses the library's fixed 32 MiB scratch instead).
+
+Checked through the C ABI against the workspace-taking dsa_sparse_mla_decode on the same inputs,
+on two calls in a row with different inputs (the scratch is shared between calls and keeps the
+previous call's contents), and for the size limit.  This file is collected last so that a run that
+stops at the first failure has already run every other test."""
+import numpy as np
+import pytest
+import torch
+
+from deepseek_sparse_attention_paged_gb300 import capi, workloads
+from deepseek_sparse_attention_paged_gb300.pipeline import DeviceBatch
+
+pytestmark = pytest.mark.gpu
+
+ATTN_ABS = 2e-2   # the attention tolerance of the parity tests
+
+
+def _inputs(seed, lens, heads, k):
+    wl = workloads.make_custom("noalloc", seed, lens, 1, topk=k, heads=heads)
+    db = DeviceBatch(wl, with_latent=True, build_index_cache=False)
+    rng = np.random.default_rng(seed)
+    idx = np.full((wl.T, k), -1, np.int32)
+    for r, v in enumerate(wl.visible_lens()):
+        n = min(k, int(v))
+        idx[r, :n] = np.sort(rng.choice(int(v), n, replace=False))
+    return wl, db, torch.from_numpy(idx).cuda()
+
+
+def _with_workspace(wl, db, idx):
+    out = torch.empty_like(db.out)
+    lse = torch.empty_like(db.lse)
+    capi.dsa_sparse_mla_decode(db.mla_q, db.kv_pool, db.block_table, db.seq_lens, db.cu_q, idx, wl.scale, out,
+                               db.mla_ws, lse=lse)
+    return out, lse
+
+
+def _no_alloc(wl, db, idx):
+    out = torch.full_like(db.out, float("nan"))
+    lse = torch.full_like(db.lse, float("nan"))
+    capi.dsa_sparse_mla_decode_noalloc(db.mla_q, db.kv_pool, db.block_table, db.seq_lens, db.cu_q, idx, wl.scale,
+                                       out, lse=lse)
+    return out, lse
+
+
+def _compare(a, b):
+    oa, la = a
+    ob, lb = b
+    torch.cuda.synchronize()
+    assert float((oa.float() - ob.float()).abs().max()) <= ATTN_ABS
+    fin = torch.isfinite(la)
+    assert torch.equal(fin, torch.isfinite(lb))
+    assert float((la[fin] - lb[fin]).abs().max()) <= 1e-3 if bool(fin.any()) else True
+
+
+def test_no_alloc_matches_workspace_entry_point_twice_in_a_row():
+    # first call: 3 rows, 128 heads, k = 2048 (8.4 MB of the 32 MiB scratch)
+    wl1, db1, idx1 = _inputs(901, [4000, 2500, 9000], 128, 2048)
+    _compare(_no_alloc(wl1, db1, idx1), _with_workspace(wl1, db1, idx1))
+    # second call, different shapes and values: nothing left over from the first call may leak in
+    wl2, db2, idx2 = _inputs(902, [700, 3000, 150, 2048, 64], 64, 512)
+    idx2[2] = -1                                      # an empty row: out = 0, lse = -inf
+    got = _no_alloc(wl2, db2, idx2)
+    _compare(got, _with_workspace(wl2, db2, idx2))
+    assert float(got[0][2].abs().max()) == 0.0 and bool(torch.isneginf(got[1][2]).all())
+
+
+def test_no_alloc_rejects_problems_larger_than_its_scratch():
+    wl, db, idx = _inputs(903, [2048] * 16, 128, 2048)   # 16 rows x 128 heads x k 2048 > 32 MiB
+    assert capi.dsa_sparse_mla_workspace_size(wl.T, wl.heads, wl.topk) > (32 << 20)
+    with pytest.raises(capi.DSAError) as e:
+        _no_alloc(wl, db, idx)
+    assert e.value.status == capi.DSA_ERR_UNSUPPORTED
