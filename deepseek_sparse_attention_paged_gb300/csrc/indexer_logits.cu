@@ -6,19 +6,19 @@
 //     I[r,s] = sum_h w[r,h] * q_scale[r,h] * ReLU(k_scale[s] * sum_d q_code[r,h,d] * k_code[s,d])
 // for s < v_r.
 //
-// This translation unit holds the query prologue (shared by every logits kernel) and the launch
-// logic.  One CTA scores one 64-token page of one request against a group of up to 4 query rows.
+// The contraction over the 128 dims is an FP8 tensor-core product (tcgen05, fp32 accumulation in
+// tensor memory); the ReLU, head gates and head sum are fused into the epilogue that reads the
+// accumulator, so only the final fp32 logit of each (row, key) reaches global memory.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
 #include "dsa_common.cuh"
+#include "sm100_ptx.cuh"
 
 namespace dsa {
 namespace {
 
 constexpr float kInvSqrt128 = 0x1.6a09e6p-4f;
-constexpr int kRowsPerGroup = 4;
-constexpr int kThreads = 256;
 
 // Quantise one 128-wide query head held as 4 values per lane (lane l: dims 4l .. 4l+3), with the
 // optional Hadamard rotation first (same butterflies and rounding as the key store).  Returns the
@@ -62,87 +62,233 @@ __device__ __forceinline__ uint32_t quantise_head(float x[4], bool rotate, int l
     return packed;
 }
 
-__device__ __forceinline__ float e4m3_to_float(uint32_t c) {
-    const __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(c), __NV_E4M3);
-    return __half2float(__half(h));
-}
+// ---------------------------------------------------------------------------------------------
+// tcgen05 kernel.  CTA = (request b, group of R query rows, chunk of `chunk_tiles` 128-key tiles).
+//
+//   D[key, n] = sum_d k_code[key, d] * q_code[n, d]      n = row_in_group * 64 + head
+//
+// is one M = 128 (keys) x N = 64 R x K = 128 FP8 UMMA per tile (4 instructions of K = 32), the
+// key tile (two 64-token pages, 8 KB of codes each) arriving by TMA with the 128-byte swizzle and
+// the quantised query tile resident in shared memory in the same layout.  The accumulator sits in
+// tensor memory, double-buffered so the epilogue of tile i overlaps the MMA of tile i + 1.
+//
+// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM owner + MMA issuer, warps 2-5 =
+// epilogue (warp w reads TMEM lanes 32 (w % 4) .. +31, i.e. one key per thread), which applies
+// ReLU, the per-head gate w' = w * q_scale, the sum over heads and the key scale, and writes the
+// logit.  All six warps quantise the query tile first.
+// ---------------------------------------------------------------------------------------------
 
-struct SimtSmem {
-    uint32_t qcode[kRowsPerGroup][kIndexHeads][kIndexDim / 4];  // packed FP8 query codes
-    float wq[kRowsPerGroup][kIndexHeads];                        // w * q_scale
-    float key[kPage][kIndexDim + 1];                             // decoded key codes (padded)
-    float kscale[kPage];
+constexpr int kTileKeys = 128;
+constexpr int kTileCodeBytes = kTileKeys * kIndexDim;  // 16 KB: two pages of codes
+constexpr int kUmmaThreads = 192;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;       // 2 s: bounded waits
+
+template <int R>
+struct IdxCfg {
+    static constexpr int N = 64 * R;
+    static constexpr int kStages = (R == 2) ? 5 : 6;
+    static constexpr int kQBytes = N * kIndexDim;
+    static constexpr uint32_t kTmemCols = (2 * N < 32) ? 32 : 2 * N;   // two accumulator buffers
+    static constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + size_t(kStages) * kTileCodeBytes + kQBytes +
+                                         size_t(kStages) * kTileKeys * 4 /*scales*/ + R * 64 * 4 /*w'*/ +
+                                         (2 * kStages + 4) * 8 /*barriers*/ + 16 + 2 * kStages;
 };
 
-__global__ void __launch_bounds__(kThreads)
-indexer_logits_simt_kernel(const uint16_t* __restrict__ q, const float* __restrict__ w,
-                           const uint8_t* __restrict__ pool, int64_t num_pages,
+template <int R>
+__global__ void __launch_bounds__(kUmmaThreads, (R == 4) ? 1 : 2)
+indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint16_t* __restrict__ q,
+                           const float* __restrict__ w, const uint8_t* __restrict__ pool, int64_t num_pages,
                            const int32_t* __restrict__ block_table, int max_pages,
-                           const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q,
-                           int row_begin, int row_end, float* __restrict__ logits, int64_t ld,
-                           bool rotate, int32_t* err) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    SimtSmem& sm = *reinterpret_cast<SimtSmem*>(smem_raw);
+                           const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q, int row_begin,
+                           int row_end, float* __restrict__ logits, int64_t ld, int rotate, int chunk_tiles,
+                           int32_t* err) {
+    using C = IdxCfg<R>;
+    constexpr int S = C::kStages;
+    constexpr int N = C::N;
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw_addr = ptx::smem_addr(smem_raw);
+    unsigned char* base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    unsigned char* codes = base;                                         // [S][16 KB], 1024-aligned
+    unsigned char* qtile = codes + S * kTileCodeBytes;                   // [N][128] swizzled
+    float* scales = reinterpret_cast<float*>(qtile + C::kQBytes);        // [S][128]
+    float* wq = scales + S * kTileKeys;                                  // [R][64]
+    uint64_t* full = reinterpret_cast<uint64_t*>(wq + R * 64);
+    uint64_t* empty = full + S;
+    uint64_t* tfull = empty + S;
+    uint64_t* tempty = tfull + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+    uint8_t* page_ok = reinterpret_cast<uint8_t*>(tmem_slot + 4);        // [S][2]
+
     const int b = blockIdx.z;
-    const int lp = blockIdx.x;
     const int L = __ldg(seq_lens + b);
     const int q0 = __ldg(cu_q + b);
     const int q_len = __ldg(cu_q + b + 1) - q0;
-    const int j0 = blockIdx.y * kRowsPerGroup;
+    const int j0 = blockIdx.y * R;
     if (j0 >= q_len) return;
-    const int nrows = min(kRowsPerGroup, q_len - j0);
+    const int nrows = min(R, q_len - j0);
     if (q0 + j0 >= row_end || q0 + j0 + nrows <= row_begin) return;
     const int vmax = visible_len(L, q_len, j0 + nrows - 1);
-    if (lp * kPage >= vmax) return;
+    const int tiles_total = (vmax + kTileKeys - 1) / kTileKeys;
+    const int t_begin = blockIdx.x * chunk_tiles;
+    if (t_begin >= tiles_total) return;
+    const int ntiles = min(tiles_total, t_begin + chunk_tiles) - t_begin;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // query prologue: one warp per (row, head)
-    for (int p = warp; p < nrows * kIndexHeads; p += kThreads / 32) {
-        const int row = p / kIndexHeads, h = p % kIndexHeads;
-        const int64_t r = q0 + j0 + row;
-        const uint2 raw = __ldg(reinterpret_cast<const uint2*>(q + (r * kIndexHeads + h) * kIndexDim) + lane);
-        float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
-        float s;
-        sm.qcode[row][h][lane] = quantise_head(x, rotate, lane, &s);
-        if (lane == 0) sm.wq[row][h] = __ldg(w + r * kIndexHeads + h) * s;
-    }
-    // key page
-    const int32_t page = __ldg(block_table + static_cast<int64_t>(b) * max_pages + lp);
-    const bool page_ok = page >= 0 && page < num_pages;
-    if (page_ok) {
-        const uint8_t* pg = pool + static_cast<int64_t>(page) * kIndexPageBytes;
-        for (int i = threadIdx.x; i < kPage * kIndexDim / 4; i += kThreads) {
-            const uint32_t c4 = __ldg(reinterpret_cast<const uint32_t*>(pg) + i);
-            const int key = i / (kIndexDim / 4), d = (i % (kIndexDim / 4)) * 4;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sm.key[key][d + e] = e4m3_to_float((c4 >> (8 * e)) & 0xffu);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&empty[s], 1 + 4);   // MMA commit + one arrive per epilogue warp
         }
-        if (threadIdx.x < kPage) sm.kscale[threadIdx.x] = __ldg(reinterpret_cast<const float*>(pg + kIndexScaleOffset) + threadIdx.x);
-    } else if (threadIdx.x == 0) {
-        raise_error(err, DSA_DEVERR_PAGE_RANGE);
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(&tfull[a], 1);
+            ptx::mbar_init(&tempty[a], 4);
+        }
+        ptx::fence_barrier_init();
     }
+    if (warp == 1) {
+        ptx::tmem_alloc(tmem_slot, C::kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    // query prologue: every warp quantises (row, head) vectors into the swizzled B tile
+    for (int p = warp; p < R * kIndexHeads; p += kUmmaThreads / 32) {
+        const int jj = p / kIndexHeads, h = p % kIndexHeads;
+        uint32_t packed = 0;
+        float sq = 0.0f;
+        if (jj < nrows) {
+            const int64_t r = q0 + j0 + jj;
+            const uint2 raw = __ldg(reinterpret_cast<const uint2*>(q + (r * kIndexHeads + h) * kIndexDim) + lane);
+            float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
+            packed = quantise_head(x, rotate != 0, lane, &sq);
+        }
+        const int n = jj * kIndexHeads + h;
+        const uint32_t off = n * 128 + ((((lane >> 2) ^ (n & 7))) << 4) + ((lane & 3) << 2);
+        *reinterpret_cast<uint32_t*>(qtile + off) = packed;
+        if (lane == 0) wq[n] = (jj < nrows) ? __ldg(w + static_cast<int64_t>(q0 + j0 + jj) * kIndexHeads + h) * sq : 0.0f;
+    }
+    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before_sync();
     __syncthreads();
-    if (!page_ok) return;
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const uint64_t deadline = ptx::globaltimer_ns() + kWaitLimitNs;
+    bool timed_out = false;
 
-    const int key = threadIdx.x & (kPage - 1);
-    const int row = threadIdx.x / kPage;
-    if (row >= nrows) return;
-    const int64_t r = q0 + j0 + row;
-    const int s = lp * kPage + key;
-    const int v = visible_len(L, q_len, j0 + row);
-    if (s >= v || s >= ld || r < row_begin || r >= row_end) return;
-    float acc = 0.0f;
-    for (int h = 0; h < kIndexHeads; ++h) {
-        float dot = 0.0f;
-#pragma unroll 8
-        for (int d4 = 0; d4 < kIndexDim / 4; ++d4) {
-            const uint32_t c4 = sm.qcode[row][h][d4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) dot = fmaf(e4m3_to_float((c4 >> (8 * e)) & 0xffu), sm.key[key][d4 * 4 + e], dot);
+    if (warp == 0) {
+        if (lane == 0) {   // ---------------- TMA producer
+            for (int i = 0; i < ntiles; ++i) {
+                const int s = i % S;
+                const uint32_t ph = (i / S) & 1;
+                if (!ptx::mbar_wait(&empty[s], ph ^ 1u, deadline)) { timed_out = true; break; }
+                const int t = t_begin + i;
+                const int lp0 = 2 * t, lp1 = 2 * t + 1;
+                const bool need1 = t * kTileKeys + kPage < vmax;
+                int32_t pg0 = -1, pg1 = -1;
+                if (lp0 < max_pages) pg0 = __ldg(block_table + static_cast<int64_t>(b) * max_pages + lp0);
+                if (need1 && lp1 < max_pages) pg1 = __ldg(block_table + static_cast<int64_t>(b) * max_pages + lp1);
+                const bool ok0 = pg0 >= 0 && pg0 < num_pages;
+                const bool ok1 = need1 && pg1 >= 0 && pg1 < num_pages;
+                if (!ok0 || (need1 && !ok1)) raise_error(err, DSA_DEVERR_PAGE_RANGE);
+                page_ok[2 * s] = ok0;
+                page_ok[2 * s + 1] = ok1;
+                const uint32_t bytes = (ok0 ? (kPage * kIndexDim + kPage * 4) : 0) + (ok1 ? (kPage * kIndexDim + kPage * 4) : 0);
+                ptx::mbar_arrive_expect_tx(&full[s], bytes);
+                unsigned char* dst = codes + s * kTileCodeBytes;
+                if (ok0) {
+                    ptx::tma_load_3d(dst, &kmap, &full[s], 0, 0, pg0);
+                    ptx::bulk_load(scales + s * kTileKeys, pool + static_cast<int64_t>(pg0) * kIndexPageBytes + kIndexScaleOffset,
+                                   kPage * 4, &full[s]);
+                }
+                if (ok1) {
+                    ptx::tma_load_3d(dst + kPage * kIndexDim, &kmap, &full[s], 0, 0, pg1);
+                    ptx::bulk_load(scales + s * kTileKeys + kPage,
+                                   pool + static_cast<int64_t>(pg1) * kIndexPageBytes + kIndexScaleOffset, kPage * 4, &full[s]);
+                }
+            }
         }
-        acc = fmaf(sm.wq[row][h], fmaxf(dot * sm.kscale[key], 0.0f), acc);
+    } else if (warp == 1) {
+        if (lane == 0) {   // ---------------- MMA issuer
+            constexpr uint32_t idesc = ptx::instr_desc(0, 0, kTileKeys, N);
+            const uint32_t q_addr = ptx::smem_addr(qtile);
+            for (int i = 0; i < ntiles; ++i) {
+                const int s = i % S;
+                const uint32_t ph = (i / S) & 1;
+                const int a = i & 1;
+                const uint32_t aph = (i >> 1) & 1;
+                if (!ptx::mbar_wait(&full[s], ph, deadline)) { timed_out = true; break; }
+                if (!ptx::mbar_wait(&tempty[a], aph ^ 1u, deadline)) { timed_out = true; break; }
+                ptx::tc_fence_after_sync();
+                const uint32_t a_addr = ptx::smem_addr(codes + s * kTileCodeBytes);
+                const uint32_t d = tmem + static_cast<uint32_t>(a * N);
+#pragma unroll
+                for (int k = 0; k < kIndexDim / 32; ++k)
+                    ptx::umma_f8f6f4(d, ptx::sw128_kmajor_desc(a_addr + k * 32), ptx::sw128_kmajor_desc(q_addr + k * 32),
+                                     idesc, k > 0 ? 1u : 0u);
+                ptx::umma_commit(&empty[s]);
+                ptx::umma_commit(&tfull[a]);
+            }
+        }
+    } else {               // ---------------- epilogue: warps 2..5
+        const int quad = warp & 3;
+        const int key_in_tile = quad * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        for (int i = 0; i < ntiles; ++i) {
+            const int s = i % S;
+            const uint32_t ph = (i / S) & 1;
+            const int a = i & 1;
+            const uint32_t aph = (i >> 1) & 1;
+            if (!ptx::mbar_wait(&full[s], ph, deadline)) { timed_out = true; break; }
+            if (!ptx::mbar_wait(&tfull[a], aph, deadline)) { timed_out = true; break; }
+            ptx::tc_fence_after_sync();
+            const bool ok = page_ok[2 * s + (key_in_tile >> 6)] != 0;
+            const float ks = scales[s * kTileKeys + key_in_tile];
+            const int key = (t_begin + i) * kTileKeys + key_in_tile;
+#pragma unroll 1
+            for (int jj = 0; jj < nrows; ++jj) {   // one query row at a time: 64 accumulator columns
+                uint32_t r0[32], r1[32];
+                const uint32_t col = tmem + lane_base + static_cast<uint32_t>(a * N + jj * kIndexHeads);
+                ptx::tmem_ld_32x32b_x32(col, r0);
+                ptx::tmem_ld_32x32b_x32(col + 32, r1);
+                ptx::tmem_wait_ld();
+                const float* g = wq + jj * kIndexHeads;
+                float acc = 0.0f;
+#pragma unroll
+                for (int h = 0; h < 32; ++h) acc = fmaf(g[h], fmaxf(__uint_as_float(r0[h]), 0.0f), acc);
+#pragma unroll
+                for (int h = 0; h < 32; ++h) acc = fmaf(g[32 + h], fmaxf(__uint_as_float(r1[h]), 0.0f), acc);
+                const int r = q0 + j0 + jj;
+                const int v = visible_len(L, q_len, j0 + jj);
+                if (ok && key < v && key < ld && r >= row_begin && r < row_end)
+                    logits[static_cast<int64_t>(r - row_begin) * ld + key] = acc * ks;
+            }
+            ptx::tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                ptx::mbar_arrive(&tempty[a]);
+                ptx::mbar_arrive(&empty[s]);
+            }
+        }
     }
-    logits[(r - row_begin) * ld + s] = acc;
+    if (timed_out) raise_error(err, DSA_DEVERR_TIMEOUT);
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after_sync();
+        ptx::tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up through the runtime (no link against libcuda).
+EncodeTiledFn tensor_map_encoder() {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(fn);
 }
 
 }  // namespace
@@ -165,16 +311,47 @@ extern "C" dsa_status dsa_indexer_logits(const void* q_bf16, const float* weight
     if (!aligned16(q_bf16) || !aligned16(index_k_pool)) return DSA_ERR_INVALID_ARG;
     if (ld < max_seq_len) return DSA_ERR_INVALID_ARG;
     if (static_cast<int64_t>(max_pages) * kPage < max_seq_len) return DSA_ERR_INVALID_ARG;
-    const int pages = (max_seq_len + kPage - 1) / kPage;
-    const int groups = (max_q_len + kRowsPerGroup - 1) / kRowsPerGroup;
+    const int R = max_q_len >= 4 ? 4 : (max_q_len >= 2 ? 2 : 1);
+    const int groups = (max_q_len + R - 1) / R;
     if (groups > 65535 || B > 65535) return DSA_ERR_UNSUPPORTED;
-    const size_t smem = sizeof(SimtSmem);
-    if (cudaFuncSetAttribute(indexer_logits_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-        return DSA_ERR_CUDA;
-    dim3 grid(pages, groups, B);
-    indexer_logits_simt_kernel<<<grid, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t*>(q_bf16), weights, index_k_pool, num_pages, block_table, max_pages, seq_lens,
-        cu_q, row_begin, row_end, logits, ld, (flags & DSA_Q_ROTATE) != 0u, dev_err);
+    if (num_pages > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
+    const int tiles = (max_seq_len + kTileKeys - 1) / kTileKeys;
+    const int chunk_tiles = (R == 1) ? 8 : 16;
+    const int chunks = (tiles + chunk_tiles - 1) / chunk_tiles;
+
+    // tensor map over the code bytes of the page-blocked pool: (byte in row, row in page, page)
+    static_assert(sizeof(CUtensorMap) == 128, "CUtensorMap size");
+    CUtensorMap kmap;
+    {
+        auto encode = tensor_map_encoder();
+        if (encode == nullptr) return DSA_ERR_CUDA;
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kIndexDim), static_cast<cuuint64_t>(kPage),
+                                    static_cast<cuuint64_t>(num_pages)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kIndexDim), static_cast<cuuint64_t>(kIndexPageBytes)};
+        const cuuint32_t box[3] = {static_cast<cuuint32_t>(kIndexDim), static_cast<cuuint32_t>(kPage), 1};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        if (encode(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(index_k_pool), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return DSA_ERR_CUDA;
+    }
+    dim3 grid(chunks, groups, B);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int rotate = (flags & DSA_Q_ROTATE) != 0u ? 1 : 0;
+    const uint16_t* qp = static_cast<const uint16_t*>(q_bf16);
+#define DSA_LAUNCH_IDX(RR)                                                                                      \
+    do {                                                                                                        \
+        const size_t smem = IdxCfg<RR>::kSmemBytes;                                                             \
+        if (cudaFuncSetAttribute(indexer_logits_umma_kernel<RR>, cudaFuncAttributeMaxDynamicSharedMemorySize,    \
+                                 static_cast<int>(smem)) != cudaSuccess)                                        \
+            return DSA_ERR_CUDA;                                                                                \
+        indexer_logits_umma_kernel<RR><<<grid, kUmmaThreads, smem, st>>>(                                       \
+            kmap, qp, weights, index_k_pool, num_pages, block_table, max_pages, seq_lens, cu_q, row_begin,      \
+            row_end, logits, ld, rotate, chunk_tiles, dev_err);                                                 \
+    } while (0)
+    if (R == 1) DSA_LAUNCH_IDX(1);
+    else if (R == 2) DSA_LAUNCH_IDX(2);
+    else DSA_LAUNCH_IDX(4);
+#undef DSA_LAUNCH_IDX
     return launch_status();
 }
