@@ -441,8 +441,37 @@ def run_e2e(db, stream, args, flush):
             "ms_per_step": ms, "api": "DeviceBatch.step() over the C ABI, ungraphed, inputs copied from pinned host"}
 
 
+def run_profile(args):
+    """Launches one stage (or the whole step) warmup + steps times with no timing, for a profiler.
+    Only what the stage needs is put on the device (the latent cache only for `mla` / `step`)."""
+    import torch
+    from deepseek_sparse_attention_paged_gb300 import capi, workloads
+    from deepseek_sparse_attention_paged_gb300.build import build
+    from deepseek_sparse_attention_paged_gb300.pipeline import DeviceBatch
+    build()
+    capi.load()
+    wl = workloads.make(args.workload)
+    need_latent = args.profile in ("mla", "step")
+    db = DeviceBatch(wl, with_latent=need_latent)
+    if args.profile in ("topk", "mla"):
+        db.indexer_logits()
+        db.topk()
+    fn = {"store": db.store_new_keys, "indexer": db.indexer_logits, "topk": db.topk,
+          "mla": db.sparse_mla, "step": db.step}[args.profile]
+    for _ in range(args.warmup + args.steps):
+        fn()
+    torch.cuda.synchronize()
+    st, word = db.device_error()
+    print(json.dumps({"profile": args.profile, "workload": wl.name, "launches": args.warmup + args.steps,
+                      "device_error": word}))
+    if st != 0:
+        raise SystemExit(1)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--profile", choices=["store", "indexer", "topk", "mla", "step"], default=None,
+                    help="launch one stage warmup+steps times without timing (for ncu) and exit")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
@@ -450,6 +479,9 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.profile is not None:
+        run_profile(args)
+        return
     if args.warmup < 3 and args.impl == "native":
         print("note: warm-up raised to 3 (minimum)", file=sys.stderr)
         args.warmup = 3

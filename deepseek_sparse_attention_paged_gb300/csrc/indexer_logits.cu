@@ -91,7 +91,7 @@ struct IdxCfg {
     static constexpr uint32_t kTmemCols = (2 * N < 32) ? 32 : 2 * N;   // two accumulator buffers
     static constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + size_t(kStages) * kTileCodeBytes + kQBytes +
                                          size_t(kStages) * kTileKeys * 4 /*scales*/ + R * 64 * 4 /*w'*/ +
-                                         (2 * kStages + 4) * 8 /*barriers*/ + 16 + 2 * kStages;
+                                         (2 * kStages + 5) * 8 /*barriers*/ + 16 + 2 * kStages;
 };
 
 template <int R>
@@ -116,7 +116,8 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint1
     uint64_t* empty = full + S;
     uint64_t* tfull = empty + S;
     uint64_t* tempty = tfull + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+    uint64_t* q_ready = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 1);
     uint8_t* page_ok = reinterpret_cast<uint8_t*>(tmem_slot + 4);        // [S][2]
 
     const int b = blockIdx.z;
@@ -143,29 +144,13 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint1
             ptx::mbar_init(&tfull[a], 1);
             ptx::mbar_init(&tempty[a], 4);
         }
+        ptx::mbar_init(q_ready, 4);             // one arrive per query-prologue warp
         ptx::fence_barrier_init();
     }
     if (warp == 1) {
         ptx::tmem_alloc(tmem_slot, C::kTmemCols);
         ptx::tmem_relinquish();
     }
-    // query prologue: every warp quantises (row, head) vectors into the swizzled B tile
-    for (int p = warp; p < R * kIndexHeads; p += kUmmaThreads / 32) {
-        const int jj = p / kIndexHeads, h = p % kIndexHeads;
-        uint32_t packed = 0;
-        float sq = 0.0f;
-        if (jj < nrows) {
-            const int64_t r = q0 + j0 + jj;
-            const uint2 raw = __ldg(reinterpret_cast<const uint2*>(q + (r * kIndexHeads + h) * kIndexDim) + lane);
-            float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
-            packed = quantise_head(x, rotate != 0, lane, &sq);
-        }
-        const int n = jj * kIndexHeads + h;
-        const uint32_t off = n * 128 + ((((lane >> 2) ^ (n & 7))) << 4) + ((lane & 3) << 2);
-        *reinterpret_cast<uint32_t*>(qtile + off) = packed;
-        if (lane == 0) wq[n] = (jj < nrows) ? __ldg(w + static_cast<int64_t>(q0 + j0 + jj) * kIndexHeads + h) * sq : 0.0f;
-    }
-    ptx::fence_proxy_async_smem();
     ptx::tc_fence_before_sync();
     __syncthreads();
     ptx::tc_fence_after_sync();
@@ -173,18 +158,20 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint1
     const uint64_t deadline = ptx::globaltimer_ns() + kWaitLimitNs;
     bool timed_out = false;
 
-    if (warp == 0) {
-        if (lane == 0) {   // ---------------- TMA producer
-            for (int i = 0; i < ntiles; ++i) {
-                const int s = i % S;
-                const uint32_t ph = (i / S) & 1;
+    if (warp == 0) {       // ---------------- TMA producer (key tiles start streaming at once)
+        // the chunk's block-table entries, one per lane (2 pages per tile, <= 32 entries)
+        int32_t my_page = -1;
+        if (lane < 2 * ntiles && 2 * t_begin + lane < max_pages)
+            my_page = __ldg(block_table + static_cast<int64_t>(b) * max_pages + 2 * t_begin + lane);
+        for (int i = 0; i < ntiles; ++i) {
+            const int s = i % S;
+            const uint32_t ph = (i / S) & 1;
+            const int32_t pg0 = __shfl_sync(0xffffffffu, my_page, 2 * i);
+            const int32_t pg1 = __shfl_sync(0xffffffffu, my_page, 2 * i + 1);
+            if (lane == 0) {
                 if (!ptx::mbar_wait(&empty[s], ph ^ 1u, deadline)) { timed_out = true; break; }
                 const int t = t_begin + i;
-                const int lp0 = 2 * t, lp1 = 2 * t + 1;
                 const bool need1 = t * kTileKeys + kPage < vmax;
-                int32_t pg0 = -1, pg1 = -1;
-                if (lp0 < max_pages) pg0 = __ldg(block_table + static_cast<int64_t>(b) * max_pages + lp0);
-                if (need1 && lp1 < max_pages) pg1 = __ldg(block_table + static_cast<int64_t>(b) * max_pages + lp1);
                 const bool ok0 = pg0 >= 0 && pg0 < num_pages;
                 const bool ok1 = need1 && pg1 >= 0 && pg1 < num_pages;
                 if (!ok0 || (need1 && !ok1)) raise_error(err, DSA_DEVERR_PAGE_RANGE);
@@ -209,7 +196,8 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint1
         if (lane == 0) {   // ---------------- MMA issuer
             constexpr uint32_t idesc = ptx::instr_desc(0, 0, kTileKeys, N);
             const uint32_t q_addr = ptx::smem_addr(qtile);
-            for (int i = 0; i < ntiles; ++i) {
+            if (!ptx::mbar_wait(q_ready, 0, deadline)) timed_out = true;
+            for (int i = 0; i < ntiles && !timed_out; ++i) {
                 const int s = i % S;
                 const uint32_t ph = (i / S) & 1;
                 const int a = i & 1;
@@ -227,11 +215,52 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint1
                 ptx::umma_commit(&tfull[a]);
             }
         }
-    } else {               // ---------------- epilogue: warps 2..5
+    } else {               // ---------------- warps 2..5: query prologue, then epilogue
+        {
+            // quantise the group's (row, head) vectors: warp pw takes vectors p = pw, pw + 4, ...;
+            // all loads of a batch are issued before any is used
+            const int pw = warp - 2;
+            constexpr int kPerWarp = R * kIndexHeads / 4;
+            constexpr int kBatch = 16;
+            for (int v0 = 0; v0 < kPerWarp; v0 += kBatch) {
+                uint2 raw[kBatch];
+                float wv[kBatch];
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    const int p = pw + 4 * (v0 + u);
+                    const int jj = p / kIndexHeads, h = p % kIndexHeads;
+                    raw[u] = make_uint2(0u, 0u);
+                    wv[u] = 0.0f;
+                    if (jj < nrows) {
+                        const int64_t r = q0 + j0 + jj;
+                        raw[u] = __ldg(reinterpret_cast<const uint2*>(q + (r * kIndexHeads + h) * kIndexDim) + lane);
+                        wv[u] = __ldg(w + r * kIndexHeads + h);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    const int p = pw + 4 * (v0 + u);   // = row_in_group * 64 + head = B-operand row
+                    const int jj = p / kIndexHeads;
+                    uint32_t packed = 0;
+                    float sq = 0.0f;
+                    if (jj < nrows) {
+                        float x[4] = {bf16_lo(raw[u].x), bf16_hi(raw[u].x), bf16_lo(raw[u].y), bf16_hi(raw[u].y)};
+                        packed = quantise_head(x, rotate != 0, lane, &sq);
+                    }
+                    const uint32_t off = p * 128 + ((((lane >> 2) ^ (p & 7))) << 4) + ((lane & 3) << 2);
+                    *reinterpret_cast<uint32_t*>(qtile + off) = packed;
+                    if (lane == 0) wq[p] = wv[u] * sq;
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(q_ready);
+        }
+        if (!ptx::mbar_wait(q_ready, 0, deadline)) timed_out = true;   // every warp's w' is visible
         const int quad = warp & 3;
         const int key_in_tile = quad * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        for (int i = 0; i < ntiles; ++i) {
+        for (int i = 0; i < ntiles && !timed_out; ++i) {
             const int s = i % S;
             const uint32_t ph = (i / S) & 1;
             const int a = i & 1;
