@@ -231,7 +231,7 @@ def dsa_sparse_mla_decode_noalloc(q_bf16: torch.Tensor, kv_pool: torch.Tensor, b
                                   seq_lens: torch.Tensor, cu_q: torch.Tensor, idx: torch.Tensor, scale: float,
                                   out: torch.Tensor, lse: Optional[torch.Tensor] = None,
                                   dev_err: Optional[torch.Tensor] = None, stream=None) -> None:
-    """dsa_sparse_mla_decode without a workspace argument: the library's fixed 32 MiB scratch is
+    """dsa_sparse_mla_decode without a workspace argument: the library's fixed 16 MiB scratch is
     used, for callers that may not allocate device memory.  Larger problems raise DSAError
     (DSA_ERR_UNSUPPORTED)."""
     lib = load()

@@ -1,4 +1,4 @@
-// sparse_mla.cu -- absorbed sparse MLA decode over the top-k selected latent rows.
+// sparse_mla.cu -- absorbed sparse MLA decode over the top-k selected latent rows (sm_103a).
 //
 // Follows vllm_ascend sfa_v1.py, _execute_sparse_flash_attention_process
 // (npu_sparse_flash_attention with query = ql_nope, key = value = latent cache, query_rope /
@@ -6,68 +6,180 @@
 // MLACommonImpl.forward decode branch (absorbed 576-wide query, one shared KV head; _forward_decode
 // returns (out, lse); merge_attn_states merges partial results by their log-sum-exp).
 //
-// Work split: CTA = (row, 16-head group, split of the k selected entries).  Each CTA streams its
-// entries' 1152-byte latent rows through shared memory in tiles of 32, keeps an online softmax
-// per head, and writes a normalised partial output and its log-sum-exp.  A second kernel merges
-// the splits: lse = log sum_j e^{lse_j}, o = sum_j e^{lse_j - lse} o_j.
+// Work split.  CTA = (query row r, split j of the k selected entries, half h of the 512 output
+// dims).  Tensor memory holds 512 fp32 columns per SM, exactly one 128-head x 512-dim output, so
+// each CTA keeps only its 256 output dims (256 columns) next to a double-buffered score tile; the
+// two halves each compute the full score tile (the scores are the smaller product), read the same
+// latent rows (the second read is served by L2) and need no communication.
+//
+// Per CTA, for tiles of 32 selected entries:
+//   producer warp : TMA tile::gather4 of the tiles' latent rows (zero rows for padding / invalid
+//                   entries), 9 chunks of 64 dims x 32 keys, 128-byte swizzle, 2 stages;
+//   MMA warp      : S = Q K^T   (M = 128 heads, N = 32 keys, K = 576; bf16, fp32 in TMEM)
+//                   O += P V_h  (M = 128 heads, N = 256 dims, K = 32 keys)
+//   4 softmax warps (thread = head = TMEM lane): online softmax in the log2 domain with lazy
+//                   rescaling (O and l are rescaled only when the running max grows by > 8, i.e.
+//                   p <= 2^8 otherwise), P to shared memory as bf16; at the end O / l and the lse.
+// With one split the CTA writes bf16 output directly; with several, normalised fp32 partials and
+// their lse go to the workspace and a combine kernel merges them.
 #include <cuda_bf16.h>
 
 #include "dsa_common.cuh"
+#include "sm100_ptx.cuh"
 
 namespace dsa {
 namespace {
 
-constexpr int kHeadGroup = 16;
-constexpr int kTile = 32;
-constexpr int kSplitEntries = 256;
-constexpr int kMlaThreads = 256;
-constexpr int kRowStride = kLatentDim + 8;   // padded bf16 row in shared memory
+constexpr int kHeadsPerCta = 128;                 // M of both MMAs (fewer heads: rows unused)
+constexpr int kKeysPerTile = 32;
+constexpr int kChunks = kLatentDim / 64;          // 9 chunks of 64 dims (128 bytes)
+constexpr int kHalfDims = kValueDim / 2;          // 256 output dims per CTA
+constexpr int kQBytes = kChunks * kHeadsPerCta * 128;          // 147456
+constexpr int kKvStageBytes = kChunks * kKeysPerTile * 128;    // 36864
+constexpr int kKvStages = 2;
+constexpr int kPBytes = kHeadsPerCta * kKeysPerTile * 2;       // 8192
+constexpr int kMlaThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemS = kHalfDims;                         // S buffers at columns 256, 288
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.0f;                      // log2 units
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr size_t kMlaSmemBytes = 1024 + kQBytes + size_t(kKvStages) * kKvStageBytes + kPBytes + 256;
 
-struct MlaSmem {
-    float q[kHeadGroup][kLatentDim];            // query, pre-multiplied by scale * log2(e)
-    uint16_t kv[kTile][kRowStride];             // bf16 latent rows of the tile
-    float s[kHeadGroup][kTile];                 // scores (log2 domain), then probabilities
-    float alpha[kHeadGroup];
-    int64_t grow[kTile];                        // physical latent row, -1 = skip
+// Shared-memory matrix descriptor (sm_100 format): start, leading / stride byte offsets, layout.
+__device__ __forceinline__ uint64_t make_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(layout) << 61;
+    return d;
+}
+constexpr uint32_t kLayoutNone = 0;
+constexpr uint32_t kLayoutSw128 = 2;
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(ptx::smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(ptx::smem_addr(bar)), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+// Four rows (arbitrary row coordinates) x one box width, written to consecutive 128-byte rows.
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar, int col, int r0,
+                                            int r1, int r2, int r3) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(ptx::smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(ptx::smem_addr(bar)), "r"(col), "r"(r0), "r"(r1), "r"(r2),
+        "r"(r3)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+struct MlaBars {
+    uint64_t q_full;
+    uint64_t kv_full[kKvStages];
+    uint64_t kv_empty[kKvStages];
+    uint64_t s_full[2];
+    uint64_t s_empty[2];
+    uint64_t p_full;
+    uint64_t p_empty;
+    uint64_t o_full;
+    uint32_t tmem_slot;
+    uint32_t pad;
+    uint32_t valid[kKvStages];   // bit i: entry i of the tile is a real latent row
 };
 
-__global__ void __launch_bounds__(kMlaThreads)
-sparse_mla_split_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ kv, int64_t num_pages,
-                        const int32_t* __restrict__ block_table, int max_pages,
-                        const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q, int B,
-                        const int32_t* __restrict__ idx, int k, int H, float scale, int splits,
-                        float* __restrict__ part_o, float* __restrict__ part_lse, int32_t* err) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    MlaSmem& sm = *reinterpret_cast<MlaSmem*>(smem_raw);
-    const int split = blockIdx.x;
-    const int hg = blockIdx.y;
+__global__ void __launch_bounds__(kMlaThreads, 1)
+sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kvmap,
+                       int64_t num_pages, const int32_t* __restrict__ block_table, int max_pages,
+                       const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q, int B,
+                       const int32_t* __restrict__ idx, int k, int H, float scale, int splits,
+                       uint16_t* __restrict__ out, float* __restrict__ lse_out, float* __restrict__ part_o,
+                       float* __restrict__ part_lse, int32_t* err) {
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw_addr = ptx::smem_addr(smem_raw);
+    unsigned char* base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    unsigned char* qs = base;                                   // [9][128 heads][128 B], SW128
+    unsigned char* kvs = qs + kQBytes;                          // [2][9][32 keys][128 B], SW128
+    unsigned char* ps = kvs + kKvStages * kKvStageBytes;        // P: [16 row groups][4 k groups][8][16 B]
+    MlaBars& bar = *reinterpret_cast<MlaBars*>(ps + kPBytes);
+
+    const int half = blockIdx.x;
+    const int split = blockIdx.y;
     const int r = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = row_request(cu_q, B, r);
     const int q0 = __ldg(cu_q + b);
     const int v = visible_len(__ldg(seq_lens + b), __ldg(cu_q + b + 1) - q0, r - q0);
-    const float qscale = scale * kLog2e;
+    const int per_split = (k + splits - 1) / splits;
+    const int e_begin = split * per_split;
+    const int e_end = min(k, e_begin + per_split);
+    const int ntiles = e_end > e_begin ? (e_end - e_begin + kKeysPerTile - 1) / kKeysPerTile : 0;
 
-    for (int i = threadIdx.x; i < kHeadGroup * kLatentDim; i += kMlaThreads) {
-        const int h = i / kLatentDim, d = i % kLatentDim;
-        const uint16_t bits = __ldg(q + (static_cast<int64_t>(r) * H + hg * kHeadGroup + h) * kLatentDim + d);
-        sm.q[h][d] = __uint_as_float(static_cast<uint32_t>(bits) << 16) * qscale;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(&bar.q_full, 1);
+        for (int s = 0; s < kKvStages; ++s) {
+            ptx::mbar_init(&bar.kv_full[s], 1);
+            ptx::mbar_init(&bar.kv_empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(&bar.s_full[a], 1);
+            ptx::mbar_init(&bar.s_empty[a], 4);
+        }
+        ptx::mbar_init(&bar.p_full, 4);
+        ptx::mbar_init(&bar.p_empty, 1);
+        ptx::mbar_init(&bar.o_full, 1);
+        ptx::fence_barrier_init();
     }
-    // output accumulators: thread owns dims 2t, 2t+1 for the 16 heads
-    float o[kHeadGroup][2];
-#pragma unroll
-    for (int h = 0; h < kHeadGroup; ++h) o[h][0] = o[h][1] = 0.0f;
-    float m_run = -INFINITY, l_run = 0.0f;   // per head, owned by lane h of warp (h / 2)... see below
+    if (warp == 1) {
+        ptx::tmem_alloc(&bar.tmem_slot, kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    if (H < kHeadsPerCta) {   // query rows of heads that do not exist: zeros (their output is never written)
+        for (int i = threadIdx.x; i < kChunks * (kHeadsPerCta - H) * 8; i += kMlaThreads) {
+            const int c = i / ((kHeadsPerCta - H) * 8), rem = i % ((kHeadsPerCta - H) * 8);
+            *reinterpret_cast<uint4*>(qs + c * (kHeadsPerCta * 128) + (H + rem / 8) * 128 + (rem % 8) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+        ptx::fence_proxy_async_smem();
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem = bar.tmem_slot;
+    const uint64_t deadline = ptx::globaltimer_ns() + kWaitLimitNs;
+    bool timed_out = false;
 
-    const int e_begin = split * kSplitEntries;
-    const int e_end = min(k, e_begin + kSplitEntries);
-    for (int t0 = e_begin; t0 < e_end; t0 += kTile) {
-        __syncthreads();
-        if (threadIdx.x < kTile) {
-            const int e = t0 + threadIdx.x;
-            int64_t g = -1;
-            if (e < e_end) {
+    if (warp == 0) {
+        // ---------------------------------------------------------------- producer
+        // lane i resolves entry i of a tile to a latent row, or -1 (padding / invalid entry: row 0
+        // is gathered in its place and its probability is forced to 0)
+        auto resolve = [&](int tile) -> int {
+            const int e = e_begin + tile * kKeysPerTile + lane;
+            int row = -1;
+            if (tile < ntiles && e < e_end) {
                 const int pos = __ldg(idx + static_cast<int64_t>(r) * k + e);
                 if (pos >= 0) {
                     if (pos >= v || (pos >> 6) >= max_pages) {
@@ -75,101 +187,227 @@ sparse_mla_split_kernel(const uint16_t* __restrict__ q, const uint16_t* __restri
                     } else {
                         const int32_t page = __ldg(block_table + static_cast<int64_t>(b) * max_pages + (pos >> 6));
                         if (page < 0 || page >= num_pages) raise_error(err, DSA_DEVERR_PAGE_RANGE);
-                        else g = static_cast<int64_t>(page) * kPage + (pos & 63);
+                        else row = page * kPage + (pos & 63);
                     }
                 }
             }
-            sm.grow[threadIdx.x] = g;
+            return row;
+        };
+        if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(&bar.q_full, kChunks * H * 128);
+            for (int c = 0; c < kChunks; ++c) tma_load_2d(qs + c * (kHeadsPerCta * 128), &qmap, &bar.q_full, c * 64, r * H);
         }
-        __syncthreads();
-        // gather the tile: 72 x 16-byte chunks per row
-        for (int i = threadIdx.x; i < kTile * (kLatentDim / 8); i += kMlaThreads) {
-            const int row = i / (kLatentDim / 8), c = i % (kLatentDim / 8);
-            const int64_t g = sm.grow[row];
-            uint4 val = make_uint4(0, 0, 0, 0);
-            if (g >= 0) val = __ldg(reinterpret_cast<const uint4*>(kv + g * kLatentDim) + c);
-            *reinterpret_cast<uint4*>(&sm.kv[row][c * 8]) = val;
-        }
-        __syncthreads();
-        // scores: thread -> (key = t & 31, heads (t >> 5) and (t >> 5) + 8)
-        {
-            const int key = threadIdx.x & (kTile - 1);
-            const int h0 = threadIdx.x >> 5;
-            float a0 = 0.0f, a1 = 0.0f;
-            const uint32_t* krow = reinterpret_cast<const uint32_t*>(sm.kv[key]);
-#pragma unroll 4
-            for (int d2 = 0; d2 < kLatentDim / 2; ++d2) {
-                const uint32_t p = krow[d2];
-                const float k0 = bf16_lo(p), k1 = bf16_hi(p);
-                a0 = fmaf(sm.q[h0][2 * d2], k0, a0);
-                a0 = fmaf(sm.q[h0][2 * d2 + 1], k1, a0);
-                a1 = fmaf(sm.q[h0 + 8][2 * d2], k0, a1);
-                a1 = fmaf(sm.q[h0 + 8][2 * d2 + 1], k1, a1);
+        int row_cur = resolve(0);
+        for (int t = 0; t < ntiles; ++t) {
+            const int s = t % kKvStages;
+            const uint32_t ph = (t / kKvStages) & 1;
+            const int row_next = resolve(t + 1);        // overlaps the wait below
+            const uint32_t vbits = __ballot_sync(0xffffffffu, row_cur >= 0);
+            const int row_tma = row_cur >= 0 ? row_cur : 0;
+            if (lane == 0) {
+                if (!ptx::mbar_wait(&bar.kv_empty[s], ph ^ 1u, deadline)) timed_out = true;
             }
-            const bool ok = sm.grow[key] >= 0;
-            sm.s[h0][key] = ok ? a0 : -INFINITY;
-            sm.s[h0 + 8][key] = ok ? a1 : -INFINITY;
-        }
-        __syncthreads();
-        // online softmax: warp w handles heads w and w + 8, lane = key
-        for (int hh = 0; hh < 2; ++hh) {
-            const int h = warp + 8 * hh;
-            const float sv = sm.s[h][lane];
-            const float tmax = warp_max(sv);
-            // every lane of the warp tracks the running stats of head h redundantly
-            float m_old = __shfl_sync(0xffffffffu, m_run, hh);
-            float l_old = __shfl_sync(0xffffffffu, l_run, hh);
-            const float m_new = fmaxf(m_old, tmax);
-            const float p = (m_new == -INFINITY) ? 0.0f : exp2f(sv - m_new);
-            const float alpha = (m_old == -INFINITY) ? 0.0f : exp2f(m_old - m_new);
-            const float psum = warp_sum(p);
-            sm.s[h][lane] = p;
-            if (lane == 0) sm.alpha[h] = (m_new == -INFINITY) ? 1.0f : alpha;
-            const float l_new = l_old * alpha + psum;
-            if (lane == hh) { m_run = m_new; l_run = l_new; }
-        }
-        __syncthreads();
-        // O update: thread owns dims 2t, 2t+1
-        {
-#pragma unroll
-            for (int h = 0; h < kHeadGroup; ++h) {
-                const float a = sm.alpha[h];
-                o[h][0] *= a;
-                o[h][1] *= a;
+            timed_out = __shfl_sync(0xffffffffu, timed_out ? 1 : 0, 0) != 0;
+            if (timed_out) break;
+            if (lane == 0) {
+                bar.valid[s] = vbits;
+                ptx::mbar_arrive_expect_tx(&bar.kv_full[s], kKvStageBytes);
             }
-            for (int key = 0; key < kTile; ++key) {
-                const uint32_t p2 = reinterpret_cast<const uint32_t*>(sm.kv[key])[threadIdx.x];
-                const float v0 = bf16_lo(p2), v1 = bf16_hi(p2);
+            __syncwarp();
+            // 8 groups of 4 keys x 9 chunks; lane l < 8 issues group l's 9 gathers
+            {
+                int rr[4];
 #pragma unroll
-                for (int h = 0; h < kHeadGroup; ++h) {
-                    const float p = sm.s[h][key];
-                    o[h][0] = fmaf(p, v0, o[h][0]);
-                    o[h][1] = fmaf(p, v1, o[h][1]);
+                for (int u = 0; u < 4; ++u) rr[u] = __shfl_sync(0xffffffffu, row_tma, (4 * (lane & 7) + u) & 31);
+                if (lane < kKeysPerTile / 4) {
+                    unsigned char* dst = kvs + s * kKvStageBytes + lane * 4 * 128;
+#pragma unroll 1
+                    for (int c = 0; c < kChunks; ++c)
+                        tma_gather4(dst + c * (kKeysPerTile * 128), &kvmap, &bar.kv_full[s], c * 64, rr[0], rr[1], rr[2],
+                                    rr[3]);
                 }
             }
+            row_cur = row_next;
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = ptx::instr_desc(1, 1, kHeadsPerCta, kKeysPerTile);
+            constexpr uint32_t idesc_pv = ptx::instr_desc(1, 1, kHeadsPerCta, kHalfDims) | (1u << 16);  // B MN-major
+            const uint32_t q_addr = ptx::smem_addr(qs);
+            const uint32_t kv_addr = ptx::smem_addr(kvs);
+            const uint32_t p_addr = ptx::smem_addr(ps);
+            auto issue_qk = [&](int t) -> bool {
+                const int s = t % kKvStages;
+                const int a = t & 1;
+                if (!ptx::mbar_wait(&bar.kv_full[s], (t / kKvStages) & 1, deadline)) return false;
+                if (!ptx::mbar_wait(&bar.s_empty[a], ((t >> 1) & 1) ^ 1u, deadline)) return false;
+                ptx::tc_fence_after_sync();
+                const uint32_t d = tmem + kTmemS + a * kKeysPerTile;
+                const uint32_t kb = kv_addr + s * kKvStageBytes;
+#pragma unroll 1
+                for (int c = 0; c < kChunks; ++c) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t da = make_desc(q_addr + c * (kHeadsPerCta * 128) + kk * 32, 16, 1024, kLayoutSw128);
+                        const uint64_t db = make_desc(kb + c * (kKeysPerTile * 128) + kk * 32, 16, 1024, kLayoutSw128);
+                        ptx::umma_f16(d, da, db, idesc_qk, (c | kk) != 0 ? 1u : 0u);
+                    }
+                }
+                ptx::umma_commit(&bar.s_full[a]);
+                return true;
+            };
+            bool ok = ptx::mbar_wait(&bar.q_full, 0, deadline);
+            if (ok && ntiles > 0) ok = issue_qk(0);
+            for (int t = 0; t < ntiles && ok; ++t) {
+                if (t + 1 < ntiles && !issue_qk(t + 1)) { ok = false; break; }
+                // O += P(t) V(t)
+                if (!ptx::mbar_wait(&bar.p_full, t & 1, deadline)) { ok = false; break; }
+                ptx::tc_fence_after_sync();
+                const int s = t % kKvStages;
+                const uint32_t vb = kv_addr + s * kKvStageBytes + (half * 4) * (kKeysPerTile * 128);
+#pragma unroll
+                for (int ks = 0; ks < kKeysPerTile / 16; ++ks) {
+                    const uint64_t da = make_desc(p_addr + ks * 256, 128, 512, kLayoutNone);
+                    const uint64_t db = make_desc(vb + ks * 16 * 128, kKeysPerTile * 128, 1024, kLayoutSw128);
+                    ptx::umma_f16(tmem, da, db, idesc_pv, (t | ks) != 0 ? 1u : 0u);
+                }
+                ptx::umma_commit(&bar.kv_empty[s]);
+                ptx::umma_commit(&bar.p_empty);
+            }
+            if (ok && ntiles > 0) ptx::umma_commit(&bar.o_full);
+            if (!ok) timed_out = true;
+        }
+    } else {
+        // ---------------------------------------------------------------- softmax + epilogue
+        const int quad = warp & 3;
+        const int head = quad * 32 + lane;          // TMEM lane = head
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        const float c = scale * kLog2e;
+        float m_run = -INFINITY, l_run = 0.0f;
+        for (int t = 0; t < ntiles; ++t) {
+            const int a = t & 1;
+            const int s = t % kKvStages;
+            if (!ptx::mbar_wait(&bar.s_full[a], (t >> 1) & 1, deadline)) { timed_out = true; break; }
+            if (!ptx::mbar_wait(&bar.kv_full[s], (t / kKvStages) & 1, deadline)) { timed_out = true; break; }
+            ptx::tc_fence_after_sync();
+            uint32_t sr[32];
+            ptx::tmem_ld_32x32b_x32(tmem + lane_base + kTmemS + a * kKeysPerTile, sr);
+            ptx::tmem_wait_ld();
+            ptx::tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&bar.s_empty[a]);
+            const uint32_t vbits = bar.valid[s];
+            float sv[32];
+            float tmax = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                sv[i] = ((vbits >> i) & 1u) ? __uint_as_float(sr[i]) * c : -INFINITY;
+                tmax = fmaxf(tmax, sv[i]);
+            }
+            // lazy rescale: move the reference max only when the tile max exceeds it by > 8
+            const bool grow = tmax > m_run + kRescaleThreshold || (m_run == -INFINITY && tmax > -INFINITY);
+            const float m_new = grow ? tmax : m_run;
+            const float alpha = grow ? ((m_run == -INFINITY) ? 0.0f : exp2f(m_run - m_new)) : 1.0f;
+            // P buffer and O are free once PV(t-1) has completed
+            if (!ptx::mbar_wait(&bar.p_empty, (t & 1) ^ 1u, deadline)) { timed_out = true; break; }
+            ptx::tc_fence_after_sync();
+            if (t > 0 && __any_sync(0xffffffffu, grow)) {
+#pragma unroll 1
+                for (int cc = 0; cc < kHalfDims; cc += 32) {
+                    uint32_t o[32];
+                    ptx::tmem_ld_32x32b_x32(tmem + lane_base + cc, o);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st_32x32b_x32(tmem + lane_base + cc, o);
+                }
+                tmem_wait_st();
+            }
+            l_run *= alpha;
+            m_run = m_new;
+            float psum = 0.0f;
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                const float p0 = (m_run == -INFINITY) ? 0.0f : exp2f(sv[i] - m_run);
+                const float p1 = (m_run == -INFINITY) ? 0.0f : exp2f(sv[i + 1] - m_run);
+                psum += p0 + p1;
+                pk[i / 2] = pack_bf16x2(p0, p1);
+            }
+            l_run += psum;
+            // P row of this head: 4 core matrices (8 keys x 16 B each) along K
+            unsigned char* prow = ps + (head >> 3) * 512 + (head & 7) * 16;
+#pragma unroll
+            for (int kg = 0; kg < 4; ++kg)
+                *reinterpret_cast<uint4*>(prow + kg * 128) = make_uint4(pk[4 * kg], pk[4 * kg + 1], pk[4 * kg + 2], pk[4 * kg + 3]);
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&bar.p_full);
+        }
+        // ---------------- epilogue: O / l, lse
+        bool have_o = ntiles > 0 && !timed_out;
+        if (have_o && !ptx::mbar_wait(&bar.o_full, 0, deadline)) { timed_out = true; have_o = false; }
+        ptx::tc_fence_after_sync();
+        const float inv_l = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+        const float lse = l_run > 0.0f ? (m_run + log2f(l_run)) / kLog2e : -INFINITY;
+        const bool write_head = head < H;
+        const int64_t rh = static_cast<int64_t>(r) * H + head;
+        if (splits == 1) {
+            uint16_t* dst = out + rh * kValueDim + half * kHalfDims;
+#pragma unroll 1
+            for (int cc = 0; cc < kHalfDims; cc += 32) {
+                uint32_t o[32];
+                if (have_o) {
+                    ptx::tmem_ld_32x32b_x32(tmem + lane_base + cc, o);
+                    ptx::tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = 0u;
+                }
+                if (write_head) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(o[i]) * inv_l, __uint_as_float(o[i + 1]) * inv_l);
+                        w.y = pack_bf16x2(__uint_as_float(o[i + 2]) * inv_l, __uint_as_float(o[i + 3]) * inv_l);
+                        w.z = pack_bf16x2(__uint_as_float(o[i + 4]) * inv_l, __uint_as_float(o[i + 5]) * inv_l);
+                        w.w = pack_bf16x2(__uint_as_float(o[i + 6]) * inv_l, __uint_as_float(o[i + 7]) * inv_l);
+                        *reinterpret_cast<uint4*>(dst + cc + i) = w;
+                    }
+                }
+            }
+            if (write_head && half == 0 && lse_out != nullptr) lse_out[rh] = lse;
+        } else {
+            float* dst = part_o + (rh * splits + split) * kValueDim + half * kHalfDims;
+#pragma unroll 1
+            for (int cc = 0; cc < kHalfDims; cc += 32) {
+                uint32_t o[32];
+                if (have_o) {
+                    ptx::tmem_ld_32x32b_x32(tmem + lane_base + cc, o);
+                    ptx::tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = 0u;
+                }
+                if (write_head) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        *reinterpret_cast<float4*>(dst + cc + i) =
+                            make_float4(__uint_as_float(o[i]) * inv_l, __uint_as_float(o[i + 1]) * inv_l,
+                                        __uint_as_float(o[i + 2]) * inv_l, __uint_as_float(o[i + 3]) * inv_l);
+                }
+            }
+            if (write_head && half == 0) part_lse[rh * splits + split] = lse;
         }
     }
-    // publish per-head stats: lane hh of warp w holds head w + 8*hh
+    if (timed_out) raise_error(err, DSA_DEVERR_TIMEOUT);
+    ptx::tc_fence_before_sync();
     __syncthreads();
-    if (lane < 2) {
-        const int h = warp + 8 * lane;
-        sm.alpha[h] = l_run;            // reuse: l
-        sm.s[h][0] = m_run;             // reuse: m (log2 domain)
-    }
-    __syncthreads();
-    const int64_t base = (static_cast<int64_t>(r) * H + hg * kHeadGroup) * splits + split;
-#pragma unroll
-    for (int h = 0; h < kHeadGroup; ++h) {
-        const float l = sm.alpha[h];
-        const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-        float2 w2 = make_float2(o[h][0] * inv, o[h][1] * inv);
-        reinterpret_cast<float2*>(part_o + (base + static_cast<int64_t>(h) * splits) * kValueDim)[threadIdx.x] = w2;
-    }
-    if (threadIdx.x < kHeadGroup) {
-        const int h = threadIdx.x;
-        const float l = sm.alpha[h], m = sm.s[h][0];
-        // natural-log lse of the scaled scores: (m + log2 l) / log2(e)
-        part_lse[base + static_cast<int64_t>(h) * splits] = (l > 0.0f) ? (m + log2f(l)) / kLog2e : -INFINITY;
+    if (warp == 1) {
+        ptx::tc_fence_after_sync();
+        ptx::tmem_dealloc(tmem, kTmemCols);
     }
 }
 
@@ -199,24 +437,56 @@ sparse_mla_combine_kernel(const float* __restrict__ part_o, const float* __restr
                 acc.w = fmaf(wj, oj.w, acc.w);
             }
         }
-        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-        const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
         uint2 packed;
-        packed.x = *reinterpret_cast<const uint32_t*>(&lo);
-        packed.y = *reinterpret_cast<const uint32_t*>(&hi);
+        packed.x = pack_bf16x2(acc.x, acc.y);
+        packed.y = pack_bf16x2(acc.z, acc.w);
         reinterpret_cast<uint2*>(out + rh * kValueDim + d)[0] = packed;
     }
     if (lse != nullptr && threadIdx.x == 0) lse[rh] = (m == -INFINITY) ? -INFINITY : m + logf(wsum);
 }
 
-int mla_splits(int k) { return (k + kSplitEntries - 1) / kSplitEntries; }
+// Splits of the k entries per row: the largest power of two (<= 8) for which the (row, split,
+// half) grid still fits one wave of one CTA per SM (152 SMs) and every split keeps >= 256 entries.
+constexpr int kSmCount = 152;
+int mla_splits(int T, int k) {
+    int s = 1;
+    while (2 * T * (2 * s) <= kSmCount && k / (2 * s) >= 256 && s < 8) s *= 2;
+    return s;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn tensor_map_encoder() {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(fn);
+}
+
+// 2-D bf16 tensor map: rows of 576 elements (1152 bytes), box of 64 elements x box_rows rows.
+bool encode_rows_576(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
+    auto encode = tensor_map_encoder();
+    if (encode == nullptr) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kLatentDim), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kLatentDim) * 2};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 }  // namespace
 }  // namespace dsa
 
 extern "C" size_t dsa_sparse_mla_workspace_size(int32_t T, int32_t H, int32_t k) {
     if (T <= 0 || H <= 0 || k <= 0) return 0;
-    const size_t splits = static_cast<size_t>(dsa::mla_splits(k));
+    const size_t splits = static_cast<size_t>(dsa::mla_splits(T, k));
+    if (splits == 1) return 0;
     return static_cast<size_t>(T) * H * splits * (dsa::kValueDim + 1) * sizeof(float);
 }
 
@@ -231,26 +501,33 @@ extern "C" dsa_status dsa_sparse_mla_decode(const void* q_bf16, const void* kv_p
     if (H != 16 && H != 32 && H != 64 && H != 128) return DSA_ERR_UNSUPPORTED;
     if (T < 0 || B < 0 || max_pages < 0 || num_pages < 0) return DSA_ERR_INVALID_ARG;
     if (T == 0) return DSA_OK;
-    if (B == 0 || !q_bf16 || !kv_pool || !block_table || !seq_lens || !cu_q || !idx || !out_bf16 || !workspace)
-        return DSA_ERR_INVALID_ARG;
-    if (!aligned16(q_bf16) || !aligned16(kv_pool) || !aligned16(out_bf16) || !aligned16(workspace))
-        return DSA_ERR_INVALID_ARG;
+    if (num_pages < 1) return DSA_ERR_INVALID_ARG;
+    if (B == 0 || !q_bf16 || !kv_pool || !block_table || !seq_lens || !cu_q || !idx || !out_bf16) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q_bf16) || !aligned16(kv_pool) || !aligned16(out_bf16)) return DSA_ERR_INVALID_ARG;
     if (!(scale > 0.0f) || T > 65535) return DSA_ERR_INVALID_ARG;
-    if (workspace_bytes < dsa_sparse_mla_workspace_size(T, H, k)) return DSA_ERR_INVALID_ARG;
-    const int splits = mla_splits(k);
+    if (num_pages * kPage >= 0x7fffffffLL || static_cast<int64_t>(T) * H >= 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
+    const size_t ws_need = dsa_sparse_mla_workspace_size(T, H, k);
+    if (ws_need > 0 && (workspace == nullptr || !aligned16(workspace) || workspace_bytes < ws_need))
+        return DSA_ERR_INVALID_ARG;
+    const int splits = mla_splits(T, k);
     float* part_o = static_cast<float*>(workspace);
-    float* part_lse = part_o + static_cast<size_t>(T) * H * splits * kValueDim;
+    float* part_lse = splits > 1 ? part_o + static_cast<size_t>(T) * H * splits * kValueDim : nullptr;
+    CUtensorMap qmap, kvmap;
+    if (!encode_rows_576(&qmap, q_bf16, static_cast<uint64_t>(T) * H, static_cast<uint32_t>(H))) return DSA_ERR_CUDA;
+    if (!encode_rows_576(&kvmap, kv_pool, static_cast<uint64_t>(num_pages) * kPage, 1)) return DSA_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const size_t smem = sizeof(MlaSmem);
-    if (cudaFuncSetAttribute(sparse_mla_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
+    if (cudaFuncSetAttribute(sparse_mla_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kMlaSmemBytes)) != cudaSuccess)
         return DSA_ERR_CUDA;
-    dim3 grid(splits, H / kHeadGroup, T);
-    sparse_mla_split_kernel<<<grid, kMlaThreads, smem, s>>>(
-        static_cast<const uint16_t*>(q_bf16), static_cast<const uint16_t*>(kv_pool), num_pages, block_table,
-        max_pages, seq_lens, cu_q, B, idx, k, H, scale, splits, part_o, part_lse, dev_err);
+    dim3 grid(2, splits, T);
+    sparse_mla_umma_kernel<<<grid, kMlaThreads, kMlaSmemBytes, s>>>(
+        qmap, kvmap, num_pages, block_table, max_pages, seq_lens, cu_q, B, idx, k, H, scale, splits,
+        static_cast<uint16_t*>(out_bf16), lse, part_o, part_lse, dev_err);
     if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
-    sparse_mla_combine_kernel<<<static_cast<unsigned>(static_cast<int64_t>(T) * H), 128, 0, s>>>(
-        part_o, part_lse, splits, static_cast<uint16_t*>(out_bf16), lse);
-    return launch_status();
+    if (splits > 1) {
+        sparse_mla_combine_kernel<<<static_cast<unsigned>(static_cast<int64_t>(T) * H), 128, 0, s>>>(
+            part_o, part_lse, splits, static_cast<uint16_t*>(out_bf16), lse);
+        if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
+    }
+    return DSA_OK;
 }

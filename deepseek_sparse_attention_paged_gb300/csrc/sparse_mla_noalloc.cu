@@ -18,8 +18,8 @@
 namespace dsa {
 namespace {
 
-// 32 MiB of split-K scratch (partial outputs and their log-sum-exps).
-constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
+// 16 MiB of split-K scratch (partial outputs and their log-sum-exps).
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_mla_scratch[kNoAllocScratchBytes];

@@ -204,10 +204,12 @@ dsa_status dsa_sparse_mla_decode(const void* q_bf16, const void* kv_pool, int64_
  * not allocate because the engine owns and budgets all device memory, a loop whose caching
  * allocator already holds the free memory, code running during CUDA graph capture).
  * Same arguments, semantics and kernels as dsa_sparse_mla_decode, minus the workspace: the
- * split-K scratch is a fixed 32 MiB array inside the library, which every GPU that loads the
+ * split-K scratch is a fixed 16 MiB array inside the library, which every GPU that loads the
  * library holds until the process exits.  The call allocates and frees nothing.
- *   Limit: problems with dsa_sparse_mla_workspace_size(T, H, k) > 32 MiB are rejected with
- *   DSA_ERR_UNSUPPORTED before anything is enqueued (at k = 2048, H = 128 that is T > 15 rows).
+ *   Limit: problems with dsa_sparse_mla_workspace_size(T, H, k) > 16 MiB are rejected with
+ *   DSA_ERR_UNSUPPORTED before anything is enqueued.  That size is T * H * splits * 2052 bytes,
+ *   the split count depending on T and k (and 0 when one split suffices, from 38 rows up); at
+ *   H = 128, k = 2048 it exceeds 16 MiB when T * splits >= 64, e.g. for 8, 16 or 32 rows.
  *   Set-up: the first call on each device looks up the array's device address with that device
  *   current; make that first call before any stream capture.
  *   Sharing: every call uses the same array.  Calls whose kernels overlap on the GPU (different

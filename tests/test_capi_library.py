@@ -40,4 +40,5 @@ def test_status_strings_and_host_side_validation(lib):
                                    None, 0, None, None) == 2                          # H = 24
     assert L.dsa_indexer_logits(None, None, None, 0, None, 0, None, None, 1, 10, 1, 0, 1, None, 10, 0x10,
                                 None, None) == 1                                      # unknown flag
-    assert L.dsa_sparse_mla_workspace_size(64, 128, 2048) > 0
+    assert L.dsa_sparse_mla_workspace_size(64, 128, 2048) == 0     # one split per row: no scratch
+    assert L.dsa_sparse_mla_workspace_size(16, 128, 2048) > 0      # few rows: split over k

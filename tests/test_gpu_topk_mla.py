@@ -122,9 +122,10 @@ def test_mla_out_of_range_entries_are_skipped_and_reported():
 
 
 def test_mla_workspace_too_small_is_rejected():
-    wl = workloads.make_custom("mla_ws", 314, [300], 1, topk=64, heads=16)
+    wl = workloads.make_custom("mla_ws", 314, [3000], 1, topk=2048, heads=16)   # one row: split over k
     db = DeviceBatch(wl, with_latent=True, build_index_cache=False)
-    idx = torch.full((1, 64), -1, dtype=torch.int32, device="cuda")
+    assert capi.dsa_sparse_mla_workspace_size(wl.T, wl.heads, wl.topk) > 16
+    idx = torch.full((1, 2048), -1, dtype=torch.int32, device="cuda")
     with pytest.raises(capi.DSAError) as e:
         capi.dsa_sparse_mla_decode(db.mla_q, db.kv_pool, db.block_table, db.seq_lens, db.cu_q, idx, wl.scale,
                                    db.out, db.mla_ws[:16])

@@ -1,5 +1,5 @@
 """dsa_sparse_mla_decode_noalloc: the sparse-MLA entry point for callers that may not allocate device
-memory (it takes no workspace and uses the library's fixed 32 MiB scratch instead).
+memory (it takes no workspace and uses the library's fixed 16 MiB scratch instead).
 
 Checked through the C ABI against the workspace-taking dsa_sparse_mla_decode on the same inputs,
 on two calls in a row with different inputs (the scratch is shared between calls and keeps the
@@ -55,7 +55,7 @@ def _compare(a, b):
 
 
 def test_no_alloc_matches_workspace_entry_point_twice_in_a_row():
-    # first call: 3 rows, 128 heads, k = 2048 (8.4 MB of the 32 MiB scratch)
+    # first call: 3 rows, 128 heads, k = 2048 (8 splits: 6.3 MB of the 16 MiB scratch)
     wl1, db1, idx1 = _inputs(901, [4000, 2500, 9000], 128, 2048)
     _compare(_no_alloc(wl1, db1, idx1), _with_workspace(wl1, db1, idx1))
     # second call, different shapes and values: nothing left over from the first call may leak in
@@ -67,8 +67,8 @@ def test_no_alloc_matches_workspace_entry_point_twice_in_a_row():
 
 
 def test_no_alloc_rejects_problems_larger_than_its_scratch():
-    wl, db, idx = _inputs(903, [2048] * 16, 128, 2048)   # 16 rows x 128 heads x k 2048 > 32 MiB
-    assert capi.dsa_sparse_mla_workspace_size(wl.T, wl.heads, wl.topk) > (32 << 20)
+    wl, db, idx = _inputs(903, [2048] * 16, 128, 2048)   # 16 rows x 128 heads x 4 splits > 16 MiB
+    assert capi.dsa_sparse_mla_workspace_size(wl.T, wl.heads, wl.topk) > (16 << 20)
     with pytest.raises(capi.DSAError) as e:
         _no_alloc(wl, db, idx)
     assert e.value.status == capi.DSA_ERR_UNSUPPORTED
