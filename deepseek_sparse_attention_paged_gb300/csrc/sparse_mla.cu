@@ -8,18 +8,26 @@
 //
 // Work split.  CTA = (query row r, split j of the k selected entries, half h of the 512 output
 // dims).  Tensor memory holds 512 fp32 columns per SM, exactly one 128-head x 512-dim output, so
-// each CTA keeps only its 256 output dims (256 columns) next to a double-buffered score tile; the
-// two halves each compute the full score tile (the scores are the smaller product), read the same
-// latent rows (the second read is served by L2) and need no communication.
+// each CTA keeps only its 256 output dims next to a double-buffered score tile; the two halves
+// each compute the full score tile (the scores are the smaller product), read the same latent rows
+// (the second read is served by L2) and need no communication.
 //
-// Per CTA, for tiles of 32 selected entries:
-//   producer warp : TMA tile::gather4 of the tiles' latent rows (zero rows for padding / invalid
-//                   entries), 9 chunks of 64 dims x 32 keys, 128-byte swizzle, 2 stages;
-//   MMA warp      : S = Q K^T   (M = 128 heads, N = 32 keys, K = 576; bf16, fp32 in TMEM)
-//                   O += P V_h  (M = 128 heads, N = 256 dims, K = 32 keys)
-//   4 softmax warps (thread = head = TMEM lane): online softmax in the log2 domain with lazy
-//                   rescaling (O and l are rescaled only when the running max grows by > 8, i.e.
-//                   p <= 2^8 otherwise), P to shared memory as bf16; at the end O / l and the lse.
+// Tensor memory (512 columns x 128 lanes, lane = head):
+//   [0, 256)   O, this CTA's 256 output dims (fp32)
+//   [256, 320) two score tiles S of 32 keys (fp32)
+//   [320, 512) query dims 0..383 as the A operand of the score MMA (bf16 pairs)
+// Shared memory: query dims 384..575 (3 chunks of 64 dims, 128-byte swizzle), 4 stages of 32
+// gathered latent rows (9 chunks x 32 rows x 128 B, 128-byte swizzle), 2 buffers of P (bf16).
+//
+// Roles, for tiles of 32 selected entries:
+//   warp 0 (producer): resolves entries to latent rows two batches of 4 tiles ahead (independent
+//           loads, no dependent load on the critical path), then TMA tile::gather4 of each tile;
+//           padding / invalid entries gather row 0 and get probability 0;
+//   warp 1 (MMA):  S = Q K^T  (M = 128 heads, N = 32 keys, K = 576; A from TMEM for dims 0..383,
+//                  from shared memory for 384..575) and O += P V_h (M = 128, N = 256, K = 32);
+//   warps 2-5 (thread = head): load the query into TMEM; online softmax in the log2 domain with
+//           lazy rescaling (O and l are rescaled only when the running max grows by more than 8,
+//           so p <= 2^8 otherwise); P to shared memory as bf16; at the end O / l and the lse.
 // With one split the CTA writes bf16 output directly; with several, normalised fp32 partials and
 // their lse go to the workspace and a combine kernel merges them.
 #include <cuda_bf16.h>
@@ -33,18 +41,27 @@ namespace {
 constexpr int kHeadsPerCta = 128;                 // M of both MMAs (fewer heads: rows unused)
 constexpr int kKeysPerTile = 32;
 constexpr int kChunks = kLatentDim / 64;          // 9 chunks of 64 dims (128 bytes)
+constexpr int kTmemQChunks = 6;                   // query chunks 0..5 live in tensor memory
+constexpr int kSmemQChunks = kChunks - kTmemQChunks;
 constexpr int kHalfDims = kValueDim / 2;          // 256 output dims per CTA
-constexpr int kQBytes = kChunks * kHeadsPerCta * 128;          // 147456
-constexpr int kKvStageBytes = kChunks * kKeysPerTile * 128;    // 36864
-constexpr int kKvStages = 2;
-constexpr int kPBytes = kHeadsPerCta * kKeysPerTile * 2;       // 8192
+constexpr int kQChunkBytes = kHeadsPerCta * 128;                // 16384
+constexpr int kQSmemBytes = kSmemQChunks * kQChunkBytes;        // 49152
+constexpr int kKvChunkBytes = kKeysPerTile * 128;               // 4096
+constexpr int kKvStageBytes = kChunks * kKvChunkBytes;          // 36864
+constexpr int kKvStages = 4;
+constexpr int kPBytes = kHeadsPerCta * kKeysPerTile * 2;        // 8192
 constexpr int kMlaThreads = 192;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = kHalfDims;                         // S buffers at columns 256, 288
+constexpr uint32_t kTmemS = kHalfDims;                          // S buffers at columns 256, 288
+constexpr uint32_t kTmemQ = kTmemS + 2 * kKeysPerTile;         // query at columns 320 .. 511
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kRescaleThreshold = 8.0f;                      // log2 units
+constexpr float kRescaleThreshold = 8.0f;                       // log2 units
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-constexpr size_t kMlaSmemBytes = 1024 + kQBytes + size_t(kKvStages) * kKvStageBytes + kPBytes + 256;
+constexpr int kBatch = 4;                                       // tiles resolved per batch
+constexpr size_t kMlaSmemBytes =
+    1024 + kQSmemBytes + size_t(kKvStages) * kKvStageBytes + 2 * kPBytes + 256;
+
+static_assert(kTmemQ + kTmemQChunks * 32 == kTmemCols, "tensor-memory budget");
 
 // Shared-memory matrix descriptor (sm_100 format): start, leading / stride byte offsets, layout.
 __device__ __forceinline__ uint64_t make_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
@@ -78,6 +95,17 @@ __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] x B[smem]^T, bf16 operands, fp32 accumulate (one thread issues).
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -98,33 +126,33 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 struct MlaBars {
-    uint64_t q_full;
+    uint64_t q_full;               // smem query chunks (TMA) + TMEM query chunks (4 warps)
     uint64_t kv_full[kKvStages];
     uint64_t kv_empty[kKvStages];
     uint64_t s_full[2];
     uint64_t s_empty[2];
-    uint64_t p_full;
-    uint64_t p_empty;
+    uint64_t p_full[2];
+    uint64_t p_empty[2];
     uint64_t o_full;
     uint32_t tmem_slot;
     uint32_t pad;
-    uint32_t valid[kKvStages];   // bit i: entry i of the tile is a real latent row
+    uint32_t valid[kKvStages];     // bit i: entry i of the stage's tile is a real latent row
 };
 
 __global__ void __launch_bounds__(kMlaThreads, 1)
 sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kvmap,
-                       int64_t num_pages, const int32_t* __restrict__ block_table, int max_pages,
-                       const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q, int B,
+                       const uint16_t* __restrict__ q, int64_t num_pages, const int32_t* __restrict__ block_table,
+                       int max_pages, const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q, int B,
                        const int32_t* __restrict__ idx, int k, int H, float scale, int splits,
                        uint16_t* __restrict__ out, float* __restrict__ lse_out, float* __restrict__ part_o,
                        float* __restrict__ part_lse, int32_t* err) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw_addr = ptx::smem_addr(smem_raw);
     unsigned char* base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-    unsigned char* qs = base;                                   // [9][128 heads][128 B], SW128
-    unsigned char* kvs = qs + kQBytes;                          // [2][9][32 keys][128 B], SW128
-    unsigned char* ps = kvs + kKvStages * kKvStageBytes;        // P: [16 row groups][4 k groups][8][16 B]
-    MlaBars& bar = *reinterpret_cast<MlaBars*>(ps + kPBytes);
+    unsigned char* qs = base;                                   // [3][128 heads][128 B], SW128
+    unsigned char* kvs = qs + kQSmemBytes;                      // [4][9][32 keys][128 B], SW128
+    unsigned char* ps = kvs + kKvStages * kKvStageBytes;        // [2][16 row groups][4 k groups][8][16 B]
+    MlaBars& bar = *reinterpret_cast<MlaBars*>(ps + 2 * kPBytes);
 
     const int half = blockIdx.x;
     const int split = blockIdx.y;
@@ -139,7 +167,7 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
     const int ntiles = e_end > e_begin ? (e_end - e_begin + kKeysPerTile - 1) / kKeysPerTile : 0;
 
     if (threadIdx.x == 0) {
-        ptx::mbar_init(&bar.q_full, 1);
+        ptx::mbar_init(&bar.q_full, 1 + 4);
         for (int s = 0; s < kKvStages; ++s) {
             ptx::mbar_init(&bar.kv_full[s], 1);
             ptx::mbar_init(&bar.kv_empty[s], 1);
@@ -147,9 +175,9 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(&bar.s_full[a], 1);
             ptx::mbar_init(&bar.s_empty[a], 4);
+            ptx::mbar_init(&bar.p_full[a], 4);
+            ptx::mbar_init(&bar.p_empty[a], 1);
         }
-        ptx::mbar_init(&bar.p_full, 4);
-        ptx::mbar_init(&bar.p_empty, 1);
         ptx::mbar_init(&bar.o_full, 1);
         ptx::fence_barrier_init();
     }
@@ -157,10 +185,10 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         ptx::tmem_alloc(&bar.tmem_slot, kTmemCols);
         ptx::tmem_relinquish();
     }
-    if (H < kHeadsPerCta) {   // query rows of heads that do not exist: zeros (their output is never written)
-        for (int i = threadIdx.x; i < kChunks * (kHeadsPerCta - H) * 8; i += kMlaThreads) {
+    if (H < kHeadsPerCta) {   // smem query rows of heads that do not exist: zeros (never written out)
+        for (int i = threadIdx.x; i < kSmemQChunks * (kHeadsPerCta - H) * 8; i += kMlaThreads) {
             const int c = i / ((kHeadsPerCta - H) * 8), rem = i % ((kHeadsPerCta - H) * 8);
-            *reinterpret_cast<uint4*>(qs + c * (kHeadsPerCta * 128) + (H + rem / 8) * 128 + (rem % 8) * 16) =
+            *reinterpret_cast<uint4*>(qs + c * kQChunkBytes + (H + rem / 8) * 128 + (rem % 8) * 16) =
                 make_uint4(0u, 0u, 0u, 0u);
         }
         ptx::fence_proxy_async_smem();
@@ -174,60 +202,74 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
 
     if (warp == 0) {
         // ---------------------------------------------------------------- producer
-        // lane i resolves entry i of a tile to a latent row, or -1 (padding / invalid entry: row 0
-        // is gathered in its place and its probability is forced to 0)
-        auto resolve = [&](int tile) -> int {
-            const int e = e_begin + tile * kKeysPerTile + lane;
-            int row = -1;
-            if (tile < ntiles && e < e_end) {
-                const int pos = __ldg(idx + static_cast<int64_t>(r) * k + e);
-                if (pos >= 0) {
-                    if (pos >= v || (pos >> 6) >= max_pages) {
-                        raise_error(err, DSA_DEVERR_INDEX_RANGE);
-                    } else {
-                        const int32_t page = __ldg(block_table + static_cast<int64_t>(b) * max_pages + (pos >> 6));
-                        if (page < 0 || page >= num_pages) raise_error(err, DSA_DEVERR_PAGE_RANGE);
-                        else row = page * kPage + (pos & 63);
-                    }
-                }
-            }
-            return row;
-        };
         if (lane == 0) {
-            ptx::mbar_arrive_expect_tx(&bar.q_full, kChunks * H * 128);
-            for (int c = 0; c < kChunks; ++c) tma_load_2d(qs + c * (kHeadsPerCta * 128), &qmap, &bar.q_full, c * 64, r * H);
+            ptx::mbar_arrive_expect_tx(&bar.q_full, kSmemQChunks * H * 128);
+            for (int c = 0; c < kSmemQChunks; ++c)
+                tma_load_2d(qs + c * kQChunkBytes, &qmap, &bar.q_full, (kTmemQChunks + c) * 64, r * H);
         }
-        int row_cur = resolve(0);
-        for (int t = 0; t < ntiles; ++t) {
-            const int s = t % kKvStages;
-            const uint32_t ph = (t / kKvStages) & 1;
-            const int row_next = resolve(t + 1);        // overlaps the wait below
-            const uint32_t vbits = __ballot_sync(0xffffffffu, row_cur >= 0);
-            const int row_tma = row_cur >= 0 ? row_cur : 0;
-            if (lane == 0) {
-                if (!ptx::mbar_wait(&bar.kv_empty[s], ph ^ 1u, deadline)) timed_out = true;
+        // lane i owns entry i of every tile.  Batches of kBatch tiles: entry positions are loaded two
+        // batches ahead, page ids one batch ahead, so no load waits on another on the critical path.
+        auto load_pos = [&](int tile) -> int {
+            const int e = e_begin + tile * kKeysPerTile + lane;
+            return (tile < ntiles && e < e_end) ? __ldg(idx + static_cast<int64_t>(r) * k + e) : -1;
+        };
+        auto pos_ok = [&](int pos) -> bool { return pos >= 0 && pos < v && (pos >> 6) < max_pages; };
+        auto load_page = [&](int pos) -> int {
+            return pos_ok(pos) ? __ldg(block_table + static_cast<int64_t>(b) * max_pages + (pos >> 6)) : -1;
+        };
+        auto to_row = [&](int pos, int page) -> int {   // -1: padding or invalid (reported)
+            if (pos < 0) return -1;
+            if (!pos_ok(pos)) { raise_error(err, DSA_DEVERR_INDEX_RANGE); return -1; }
+            if (page < 0 || page >= num_pages) { raise_error(err, DSA_DEVERR_PAGE_RANGE); return -1; }
+            return page * kPage + (pos & 63);
+        };
+        int pos1[kBatch], page1[kBatch], pos2[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) pos1[u] = load_pos(u);
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) page1[u] = load_page(pos1[u]);
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) pos2[u] = load_pos(kBatch + u);
+        for (int t0 = 0; t0 < ntiles && !timed_out; t0 += kBatch) {
+            int rows[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) rows[u] = to_row(pos1[u], page1[u]);
+            // next batch's page ids, the batch after's positions
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                pos1[u] = pos2[u];
+                page1[u] = load_page(pos2[u]);
             }
-            timed_out = __shfl_sync(0xffffffffu, timed_out ? 1 : 0, 0) != 0;
-            if (timed_out) break;
-            if (lane == 0) {
-                bar.valid[s] = vbits;
-                ptx::mbar_arrive_expect_tx(&bar.kv_full[s], kKvStageBytes);
-            }
-            __syncwarp();
-            // 8 groups of 4 keys x 9 chunks; lane l < 8 issues group l's 9 gathers
-            {
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) pos2[u] = load_pos(t0 + 2 * kBatch + u);
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int t = t0 + u;
+                if (t >= ntiles) break;
+                const int s = t % kKvStages;
+                const uint32_t ph = (t / kKvStages) & 1;
+                const uint32_t vbits = __ballot_sync(0xffffffffu, rows[u] >= 0);
+                const int row_tma = rows[u] >= 0 ? rows[u] : 0;
                 int rr[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) rr[u] = __shfl_sync(0xffffffffu, row_tma, (4 * (lane & 7) + u) & 31);
+                for (int w = 0; w < 4; ++w) rr[w] = __shfl_sync(0xffffffffu, row_tma, (4 * (lane & 7) + w) & 31);
+                if (lane == 0) {
+                    if (!ptx::mbar_wait(&bar.kv_empty[s], ph ^ 1u, deadline)) timed_out = true;
+                    if (!timed_out) {
+                        bar.valid[s] = vbits;
+                        ptx::mbar_arrive_expect_tx(&bar.kv_full[s], kKvStageBytes);
+                    }
+                }
+                timed_out = __shfl_sync(0xffffffffu, timed_out ? 1 : 0, 0) != 0;
+                if (timed_out) break;
+                // 8 groups of 4 keys x 9 chunks; lane l < 8 issues group l's 9 gathers
                 if (lane < kKeysPerTile / 4) {
                     unsigned char* dst = kvs + s * kKvStageBytes + lane * 4 * 128;
 #pragma unroll 1
                     for (int c = 0; c < kChunks; ++c)
-                        tma_gather4(dst + c * (kKeysPerTile * 128), &kvmap, &bar.kv_full[s], c * 64, rr[0], rr[1], rr[2],
-                                    rr[3]);
+                        tma_gather4(dst + c * kKvChunkBytes, &kvmap, &bar.kv_full[s], c * 64, rr[0], rr[1], rr[2], rr[3]);
                 }
             }
-            row_cur = row_next;
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
@@ -246,12 +288,21 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
                 const uint32_t d = tmem + kTmemS + a * kKeysPerTile;
                 const uint32_t kb = kv_addr + s * kKvStageBytes;
 #pragma unroll 1
-                for (int c = 0; c < kChunks; ++c) {
+                for (int c = 0; c < kTmemQChunks; ++c) {
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t da = make_desc(q_addr + c * (kHeadsPerCta * 128) + kk * 32, 16, 1024, kLayoutSw128);
-                        const uint64_t db = make_desc(kb + c * (kKeysPerTile * 128) + kk * 32, 16, 1024, kLayoutSw128);
-                        ptx::umma_f16(d, da, db, idesc_qk, (c | kk) != 0 ? 1u : 0u);
+                        const uint64_t db = make_desc(kb + c * kKvChunkBytes + kk * 32, 16, 1024, kLayoutSw128);
+                        umma_f16_ts(d, tmem + kTmemQ + c * 32 + kk * 8, db, idesc_qk, (c | kk) != 0 ? 1u : 0u);
+                    }
+                }
+#pragma unroll 1
+                for (int c = 0; c < kSmemQChunks; ++c) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t da = make_desc(q_addr + c * kQChunkBytes + kk * 32, 16, 1024, kLayoutSw128);
+                        const uint64_t db =
+                            make_desc(kb + (kTmemQChunks + c) * kKvChunkBytes + kk * 32, 16, 1024, kLayoutSw128);
+                        ptx::umma_f16(d, da, db, idesc_qk, 1u);
                     }
                 }
                 ptx::umma_commit(&bar.s_full[a]);
@@ -262,32 +313,61 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
             for (int t = 0; t < ntiles && ok; ++t) {
                 if (t + 1 < ntiles && !issue_qk(t + 1)) { ok = false; break; }
                 // O += P(t) V(t)
-                if (!ptx::mbar_wait(&bar.p_full, t & 1, deadline)) { ok = false; break; }
+                const int pb = t & 1;
+                if (!ptx::mbar_wait(&bar.p_full[pb], (t >> 1) & 1, deadline)) { ok = false; break; }
                 ptx::tc_fence_after_sync();
                 const int s = t % kKvStages;
-                const uint32_t vb = kv_addr + s * kKvStageBytes + (half * 4) * (kKeysPerTile * 128);
+                const uint32_t vb = kv_addr + s * kKvStageBytes + (half * 4) * kKvChunkBytes;
 #pragma unroll
                 for (int ks = 0; ks < kKeysPerTile / 16; ++ks) {
-                    const uint64_t da = make_desc(p_addr + ks * 256, 128, 512, kLayoutNone);
-                    const uint64_t db = make_desc(vb + ks * 16 * 128, kKeysPerTile * 128, 1024, kLayoutSw128);
+                    const uint64_t da = make_desc(p_addr + pb * kPBytes + ks * 256, 128, 512, kLayoutNone);
+                    const uint64_t db = make_desc(vb + ks * 16 * 128, kKvChunkBytes, 1024, kLayoutSw128);
                     ptx::umma_f16(tmem, da, db, idesc_pv, (t | ks) != 0 ? 1u : 0u);
                 }
                 ptx::umma_commit(&bar.kv_empty[s]);
-                ptx::umma_commit(&bar.p_empty);
+                ptx::umma_commit(&bar.p_empty[pb]);
             }
             if (ok && ntiles > 0) ptx::umma_commit(&bar.o_full);
             if (!ok) timed_out = true;
         }
     } else {
-        // ---------------------------------------------------------------- softmax + epilogue
+        // ---------------------------------------------------------------- query -> TMEM, softmax, epilogue
         const int quad = warp & 3;
         const int head = quad * 32 + lane;          // TMEM lane = head
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        const float c = scale * kLog2e;
+        {
+            // query dims 0..383 of this head into TMEM columns 320.., two bf16 per column
+            const uint4* src = reinterpret_cast<const uint4*>(q + (static_cast<int64_t>(r) * H + head) * kLatentDim);
+            const bool live = head < H;
+#pragma unroll 1
+            for (int c0 = 0; c0 < kTmemQChunks; c0 += 2) {
+                uint4 raw[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) raw[i] = live ? __ldg(src + c0 * 8 + i) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    uint32_t w[32];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        w[4 * i + 0] = raw[cc * 8 + i].x;
+                        w[4 * i + 1] = raw[cc * 8 + i].y;
+                        w[4 * i + 2] = raw[cc * 8 + i].z;
+                        w[4 * i + 3] = raw[cc * 8 + i].w;
+                    }
+                    tmem_st_32x32b_x32(tmem + lane_base + kTmemQ + (c0 + cc) * 32, w);
+                }
+            }
+            tmem_wait_st();
+            ptx::tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&bar.q_full);
+        }
+        const float cscale = scale * kLog2e;
         float m_run = -INFINITY, l_run = 0.0f;
         for (int t = 0; t < ntiles; ++t) {
             const int a = t & 1;
             const int s = t % kKvStages;
+            const int pb = t & 1;
             if (!ptx::mbar_wait(&bar.s_full[a], (t >> 1) & 1, deadline)) { timed_out = true; break; }
             if (!ptx::mbar_wait(&bar.kv_full[s], (t / kKvStages) & 1, deadline)) { timed_out = true; break; }
             ptx::tc_fence_after_sync();
@@ -302,17 +382,19 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
             float tmax = -INFINITY;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                sv[i] = ((vbits >> i) & 1u) ? __uint_as_float(sr[i]) * c : -INFINITY;
+                sv[i] = ((vbits >> i) & 1u) ? __uint_as_float(sr[i]) * cscale : -INFINITY;
                 tmax = fmaxf(tmax, sv[i]);
             }
             // lazy rescale: move the reference max only when the tile max exceeds it by > 8
             const bool grow = tmax > m_run + kRescaleThreshold || (m_run == -INFINITY && tmax > -INFINITY);
             const float m_new = grow ? tmax : m_run;
             const float alpha = grow ? ((m_run == -INFINITY) ? 0.0f : exp2f(m_run - m_new)) : 1.0f;
-            // P buffer and O are free once PV(t-1) has completed
-            if (!ptx::mbar_wait(&bar.p_empty, (t & 1) ^ 1u, deadline)) { timed_out = true; break; }
-            ptx::tc_fence_after_sync();
+            // this P buffer is free once PV(t-2) has completed
+            if (!ptx::mbar_wait(&bar.p_empty[pb], ((t >> 1) & 1) ^ 1u, deadline)) { timed_out = true; break; }
             if (t > 0 && __any_sync(0xffffffffu, grow)) {
+                // O may only be rescaled once PV(t-1) has completed
+                if (!ptx::mbar_wait(&bar.p_empty[pb ^ 1], ((t - 1) >> 1) & 1, deadline)) { timed_out = true; break; }
+                ptx::tc_fence_after_sync();
 #pragma unroll 1
                 for (int cc = 0; cc < kHalfDims; cc += 32) {
                     uint32_t o[32];
@@ -337,14 +419,14 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
             }
             l_run += psum;
             // P row of this head: 4 core matrices (8 keys x 16 B each) along K
-            unsigned char* prow = ps + (head >> 3) * 512 + (head & 7) * 16;
+            unsigned char* prow = ps + pb * kPBytes + (head >> 3) * 512 + (head & 7) * 16;
 #pragma unroll
             for (int kg = 0; kg < 4; ++kg)
                 *reinterpret_cast<uint4*>(prow + kg * 128) = make_uint4(pk[4 * kg], pk[4 * kg + 1], pk[4 * kg + 2], pk[4 * kg + 3]);
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&bar.p_full);
+            if (lane == 0) ptx::mbar_arrive(&bar.p_full[pb]);
         }
         // ---------------- epilogue: O / l, lse
         bool have_o = ntiles > 0 && !timed_out;
@@ -521,8 +603,8 @@ extern "C" dsa_status dsa_sparse_mla_decode(const void* q_bf16, const void* kv_p
         return DSA_ERR_CUDA;
     dim3 grid(2, splits, T);
     sparse_mla_umma_kernel<<<grid, kMlaThreads, kMlaSmemBytes, s>>>(
-        qmap, kvmap, num_pages, block_table, max_pages, seq_lens, cu_q, B, idx, k, H, scale, splits,
-        static_cast<uint16_t*>(out_bf16), lse, part_o, part_lse, dev_err);
+        qmap, kvmap, static_cast<const uint16_t*>(q_bf16), num_pages, block_table, max_pages, seq_lens, cu_q, B, idx,
+        k, H, scale, splits, static_cast<uint16_t*>(out_bf16), lse, part_o, part_lse, dev_err);
     if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
     if (splits > 1) {
         sparse_mla_combine_kernel<<<static_cast<unsigned>(static_cast<int64_t>(T) * H), 128, 0, s>>>(
