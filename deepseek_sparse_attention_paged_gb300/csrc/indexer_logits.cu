@@ -81,7 +81,6 @@ __device__ __forceinline__ uint32_t quantise_head(float x[4], bool rotate, int l
 constexpr int kTileKeys = 128;
 constexpr int kTileCodeBytes = kTileKeys * kIndexDim;  // 16 KB: two pages of codes
 constexpr int kUmmaThreads = 192;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;       // 2 s: bounded waits
 
 template <int R>
 struct IdxCfg {
@@ -155,7 +154,7 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint1
     __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const uint64_t deadline = ptx::globaltimer_ns() + kWaitLimitNs;
+    const uint64_t deadline = ptx::wait_deadline();
     bool timed_out = false;
 
     if (warp == 0) {       // ---------------- TMA producer (key tiles start streaming at once)

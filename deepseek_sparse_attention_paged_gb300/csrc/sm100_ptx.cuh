@@ -51,14 +51,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return done != 0;
 }
 
-// Wait until the phase with the given parity has completed, or until the global deadline passes.
-// Returns false on timeout (the caller reports it and unwinds); never spins unboundedly.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t deadline_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() > deadline_ns) return false;
+// Deadline for bounded waits: `cycles` SM clock cycles from now (clock64 is a cheap per-SM counter;
+// 4e9 cycles is about 2 s at the maximum clock).
+__device__ __forceinline__ uint64_t wait_deadline(uint64_t cycles = 4000000000ull) {
+    return static_cast<uint64_t>(clock64()) + cycles;
+}
+
+// Wait until the phase with the given parity has completed, or until the deadline (a clock64
+// value) passes.  Returns false on timeout (the caller reports it and unwinds); never spins
+// unboundedly.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t deadline) {
+    while (!mbar_try_wait(bar, parity)) {
+        if (static_cast<uint64_t>(clock64()) > deadline) return false;
     }
+    return true;
 }
 
 // ---------------------------------------------------------------- bulk / tensor copies

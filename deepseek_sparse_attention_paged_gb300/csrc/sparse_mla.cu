@@ -56,8 +56,7 @@ constexpr uint32_t kTmemS = kHalfDims;                          // S buffers at 
 constexpr uint32_t kTmemQ = kTmemS + 2 * kKeysPerTile;         // query at columns 320 .. 511
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;                       // log2 units
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
-constexpr int kBatch = 4;                                       // tiles resolved per batch
+constexpr int kBatch = 4;                                      // tiles resolved per batch
 constexpr size_t kMlaSmemBytes =
     1024 + kQSmemBytes + size_t(kKvStages) * kKvStageBytes + 2 * kPBytes + 256;
 
@@ -197,7 +196,7 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
     __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem = bar.tmem_slot;
-    const uint64_t deadline = ptx::globaltimer_ns() + kWaitLimitNs;
+    const uint64_t deadline = ptx::wait_deadline();
     bool timed_out = false;
 
     if (warp == 0) {
