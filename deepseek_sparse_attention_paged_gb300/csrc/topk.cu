@@ -143,6 +143,179 @@ topk_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* __restr
     }
 }
 
+// ---------------------------------------------------------------------------------------------
+// Two-read kernel for rows of up to kMaxBitmapWords * 32 keys.  Read 1: histogram of the top 12
+// key bits.  Read 2: keys in bins above the threshold bin are marked in a shared-memory bitmap;
+// keys in the threshold bin are collected (key, index) as candidates in shared memory.  The low 20
+// bits are then resolved on the candidates (two 10-bit digits), the selected candidates marked,
+// and a scan over the bitmap words writes the indices in ascending order.  If the threshold bin
+// holds more candidates than fit, the low digits are resolved by re-reading the row instead.
+// ---------------------------------------------------------------------------------------------
+constexpr int kTopBins = 4096;                 // top 12 bits of the key
+constexpr int kMaxBitmapWords = 4096;          // rows up to 131072 keys
+constexpr int kCandidateCap = 8192;
+
+struct BitmapSmem {
+    uint32_t hist[kTopBins];
+    uint32_t warp_tot[kWarps];
+    uint32_t sel_digit;
+    uint32_t sel_remaining;
+    uint32_t cand_count;
+    uint32_t pad;
+};
+
+// Digit d (from the top) of `bins` histogram bins such that (# keys with digit > d) < need <=
+// (# keys with digit >= d); stores d and need - (# keys with digit > d).  bins: 1024 or 4096.
+__device__ void select_bin(uint32_t* hist, BitmapSmem& sm, int bins, uint32_t need) {
+    const int per = bins / kTopkThreads;
+    uint32_t local = 0;
+    for (int i = 0; i < per; ++i) local += hist[bins - 1 - (threadIdx.x * per + i)];
+    uint32_t total;
+    const uint32_t incl = block_inclusive_scan(local, sm.warp_tot, &total);
+    uint32_t above = incl - local;
+    for (int i = 0; i < per; ++i) {
+        const int d = bins - 1 - (threadIdx.x * per + i);
+        const uint32_t c = hist[d];
+        if (above < need && need <= above + c) {
+            sm.sel_digit = static_cast<uint32_t>(d);
+            sm.sel_remaining = need - above;
+        }
+        above += c;
+    }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kTopkThreads)
+topk_bitmap_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* __restrict__ seq_lens,
+                   const int32_t* __restrict__ cu_q, int B, int row_begin, int k, int32_t* __restrict__ idx,
+                   int words_cap) {
+    extern __shared__ __align__(16) unsigned char dsm[];
+    BitmapSmem& sm = *reinterpret_cast<BitmapSmem*>(dsm);
+    uint32_t* sel = reinterpret_cast<uint32_t*>(dsm + sizeof(BitmapSmem));   // key > k-th: kept
+    uint32_t* tie = sel + words_cap;                                         // key == k-th
+    uint32_t* ckey = tie + words_cap;
+    int32_t* cidx = reinterpret_cast<int32_t*>(ckey + kCandidateCap);
+
+    const int rl = blockIdx.x;
+    const int r = row_begin + rl;
+    const int b = row_request(cu_q, B, r);
+    const int q0 = __ldg(cu_q + b);
+    int v = visible_len(__ldg(seq_lens + b), __ldg(cu_q + b + 1) - q0, r - q0);
+    if (v > ld) v = static_cast<int>(ld);
+    if (v > words_cap * 32) v = words_cap * 32;   // the launcher guarantees this never clips
+    const float* row = logits + static_cast<int64_t>(rl) * ld;
+    int32_t* out = idx + static_cast<int64_t>(rl) * k;
+    if (v <= k) {
+        for (int j = threadIdx.x; j < k; j += kTopkThreads) out[j] = j < v ? j : -1;
+        return;
+    }
+    const int W = (v + 31) / 32;
+
+    // ---- read 1: top-12-bit histogram
+    for (int i = threadIdx.x; i < kTopBins; i += kTopkThreads) sm.hist[i] = 0;
+    __syncthreads();
+    for (int s = threadIdx.x; s < v; s += kTopkThreads) atomicAdd(&sm.hist[order_key(__ldg(row + s)) >> 20], 1u);
+    __syncthreads();
+    select_bin(sm.hist, sm, kTopBins, static_cast<uint32_t>(k));
+    const uint32_t b1 = sm.sel_digit;
+    uint32_t need = sm.sel_remaining;
+
+    // ---- read 2: mark keys above the threshold bin, collect the threshold bin
+    for (int w = threadIdx.x; w < W; w += kTopkThreads) sel[w] = tie[w] = 0u;
+    if (threadIdx.x == 0) sm.cand_count = 0;
+    __syncthreads();
+    for (int s = threadIdx.x; s < v; s += kTopkThreads) {
+        const uint32_t key = order_key(__ldg(row + s));
+        const uint32_t bin = key >> 20;
+        if (bin > b1) {
+            atomicOr(&sel[s >> 5], 1u << (s & 31));
+        } else if (bin == b1) {
+            const uint32_t p = atomicAdd(&sm.cand_count, 1u);
+            if (p < static_cast<uint32_t>(kCandidateCap)) {
+                ckey[p] = key;
+                cidx[p] = s;
+            }
+        }
+    }
+    __syncthreads();
+    const uint32_t n = sm.cand_count;
+    const bool in_smem = n <= static_cast<uint32_t>(kCandidateCap);
+    // ---- low digits: bits [19:10], then [9:0], of the threshold-bin keys
+    uint32_t prefix = b1 << 20;
+    for (int pass = 0; pass < 2; ++pass) {
+        const int shift = pass == 0 ? 10 : 0;
+        const int hi = shift + 10;   // bits above the digit must equal the prefix
+        for (int i = threadIdx.x; i < 1024; i += kTopkThreads) sm.hist[i] = 0;
+        __syncthreads();
+        if (in_smem) {
+            for (uint32_t i = threadIdx.x; i < n; i += kTopkThreads) {
+                const uint32_t key = ckey[i];
+                if ((key >> hi) == (prefix >> hi)) atomicAdd(&sm.hist[(key >> shift) & 1023u], 1u);
+            }
+        } else {
+            for (int s = threadIdx.x; s < v; s += kTopkThreads) {
+                const uint32_t key = order_key(__ldg(row + s));
+                if ((key >> hi) == (prefix >> hi)) atomicAdd(&sm.hist[(key >> shift) & 1023u], 1u);
+            }
+        }
+        __syncthreads();
+        select_bin(sm.hist, sm, 1024, need);
+        prefix |= sm.sel_digit << shift;
+        need = sm.sel_remaining;
+        __syncthreads();
+    }
+    const uint32_t kth = prefix;
+    const uint32_t take_equal = need;   // keys equal to kth that are kept (lowest indices first)
+    if (in_smem) {
+        for (uint32_t i = threadIdx.x; i < n; i += kTopkThreads) {
+            const uint32_t key = ckey[i];
+            const int s = cidx[i];
+            if (key > kth) atomicOr(&sel[s >> 5], 1u << (s & 31));
+            else if (key == kth) atomicOr(&tie[s >> 5], 1u << (s & 31));
+        }
+    } else {
+        for (int s = threadIdx.x; s < v; s += kTopkThreads) {
+            const uint32_t key = order_key(__ldg(row + s));
+            if ((key >> 20) != b1) continue;
+            if (key > kth) atomicOr(&sel[s >> 5], 1u << (s & 31));
+            else if (key == kth) atomicOr(&tie[s >> 5], 1u << (s & 31));
+        }
+    }
+    __syncthreads();
+
+    // ---- index-ordered output: thread t scans a contiguous range of bitmap words
+    const int wpt = (W + kTopkThreads - 1) / kTopkThreads;
+    const int w0 = min(W, threadIdx.x * wpt), w1 = min(W, w0 + wpt);
+    uint32_t gt = 0, eq = 0;
+    for (int w = w0; w < w1; ++w) {
+        gt += __popc(sel[w]);
+        eq += __popc(tie[w]);
+    }
+    uint32_t tot;
+    uint32_t gt_before = block_inclusive_scan(gt, sm.warp_tot, &tot) - gt;
+    uint32_t eq_before = block_inclusive_scan(eq, sm.warp_tot, &tot) - eq;
+    for (int w = w0; w < w1; ++w) {
+        const uint32_t sw = sel[w], tw = tie[w];
+        uint32_t bits = sw | tw;
+        while (bits) {
+            const int bit = __ffs(bits) - 1;
+            bits &= bits - 1;
+            const int s = w * 32 + bit;
+            if ((sw >> bit) & 1u) {
+                out[gt_before + min(eq_before, take_equal)] = s;
+                ++gt_before;
+            } else {
+                if (eq_before < take_equal) out[gt_before + eq_before] = s;
+                ++eq_before;
+            }
+        }
+    }
+}
+
+size_t bitmap_smem_bytes(int words) {
+    return sizeof(BitmapSmem) + 2 * static_cast<size_t>(words) * 4 + static_cast<size_t>(kCandidateCap) * 8;
+}
+
 }  // namespace
 }  // namespace dsa
 
@@ -160,8 +333,19 @@ extern "C" dsa_status dsa_topk(const float* logits, int64_t ld, const int32_t* s
     if (row_end == row_begin) return DSA_OK;
     if (B == 0 || !logits || !seq_lens || !cu_q || !idx) return DSA_ERR_INVALID_ARG;
     if (ld < max_seq_len) return DSA_ERR_INVALID_ARG;
-    if (max_seq_len >= (1 << 16) * 1024) return DSA_ERR_UNSUPPORTED;
-    dsa::topk_kernel<<<row_end - row_begin, dsa::kTopkThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        logits, ld, seq_lens, cu_q, B, row_begin, k, idx);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int words = (max_seq_len + 31) / 32;
+    if (words <= dsa::kMaxBitmapWords) {
+        const int words_cap = words < 32 ? 32 : words;
+        const size_t smem = dsa::bitmap_smem_bytes(words_cap);
+        if (cudaFuncSetAttribute(dsa::topk_bitmap_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem)) != cudaSuccess)
+            return DSA_ERR_CUDA;
+        dsa::topk_bitmap_kernel<<<row_end - row_begin, dsa::kTopkThreads, smem, s>>>(logits, ld, seq_lens, cu_q, B,
+                                                                                      row_begin, k, idx, words_cap);
+    } else {
+        dsa::topk_kernel<<<row_end - row_begin, dsa::kTopkThreads, 0, s>>>(logits, ld, seq_lens, cu_q, B, row_begin, k,
+                                                                          idx);
+    }
     return dsa::launch_status();
 }
