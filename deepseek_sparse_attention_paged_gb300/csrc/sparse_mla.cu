@@ -7,27 +7,32 @@
 // returns (out, lse); merge_attn_states merges partial results by their log-sum-exp).
 //
 // Work split.  CTA = (query row r, split j of the k selected entries, half h of the 512 output
-// dims).  Tensor memory holds 512 fp32 columns per SM, exactly one 128-head x 512-dim output, so
-// each CTA keeps only its 256 output dims next to a double-buffered score tile; the two halves
-// each compute the full score tile (the scores are the smaller product), read the same latent rows
-// (the second read is served by L2) and need no communication.
+// dims); the two halves of a (row, split) form a cluster of 2 CTAs.  Tensor memory holds 512 fp32
+// columns per SM, exactly one 128-head x 512-dim output, so each CTA keeps only its 256 output
+// dims next to the score tile and computes the full score tile itself; the latent rows of each tile
+// are gathered once per cluster: each CTA gathers half of the tile's rows by TMA with cluster
+// multicast, which writes them into both CTAs' shared memory.
 //
 // Tensor memory (512 columns x 128 lanes, lane = head):
 //   [0, 256)   O, this CTA's 256 output dims (fp32)
-//   [256, 320) two score tiles S of 32 keys (fp32)
-//   [320, 512) query dims 0..383 as the A operand of the score MMA (bf16 pairs)
-// Shared memory: query dims 384..575 (3 chunks of 64 dims, 128-byte swizzle), 4 stages of 32
-// gathered latent rows (9 chunks x 32 rows x 128 B, 128-byte swizzle), 2 buffers of P (bf16).
+//   [256, 320) score tile S of 64 keys (fp32)
+//   [320, 512) query dims 0..383, the A operand of the score MMA (two bf16 per column)
+// Shared memory: query dims 384..575 (3 chunks of 64 dims, 128-byte swizzle, by TMA); 2 stages of
+// 64 gathered latent rows (9 chunks x 64 rows x 128 B, 128-byte swizzle); 2 buffers of P (bf16).
 //
-// Roles, for tiles of 32 selected entries:
-//   warp 0 (producer): resolves entries to latent rows two batches of 4 tiles ahead (independent
-//           loads, no dependent load on the critical path), then TMA tile::gather4 of each tile;
-//           padding / invalid entries gather row 0 and get probability 0;
-//   warp 1 (MMA):  S = Q K^T  (M = 128 heads, N = 32 keys, K = 576; A from TMEM for dims 0..383,
-//                  from shared memory for 384..575) and O += P V_h (M = 128, N = 256, K = 32);
-//   warps 2-5 (thread = head): load the query into TMEM; online softmax in the log2 domain with
-//           lazy rescaling (O and l are rescaled only when the running max grows by more than 8,
-//           so p <= 2^8 otherwise); P to shared memory as bf16; at the end O / l and the lse.
+// Roles (224 threads), for tiles of 64 selected entries:
+//   warps 0-3 (thread = head = TMEM lane): query dims 0..383 into TMEM; online softmax in the log2
+//           domain with lazy rescaling (O and l are rescaled only when the running max grows by
+//           more than 8, so p <= 2^8 otherwise); P to shared memory as bf16; O / l and lse at the end;
+//   warp 4 (MMA):  S = Q K^T  (M = 128 heads, N = 64 keys, K = 576) and O += P V_h (M = 128,
+//           N = 256 dims, K = 64 keys), bf16 in, fp32 accumulate in TMEM; the completion of PV(t)
+//           is signalled to both CTAs of the cluster (the stage is free only when both are done);
+//   warps 5-6 (producers): warp 5 + w resolves entries 32 w .. 32 w + 31 of each tile to latent
+//           rows two batches ahead (independent loads), and, in the CTA of cluster rank w, gathers
+//           those rows with TMA tile::gather4 multicast to both CTAs (padding / invalid entries
+//           gather row 0 and get probability 0).
+// Score MMAs are issued with N = 64: on this tensor core an M = 128, K = 16 MMA takes the same time
+// for N = 32 and N = 64, so wider key tiles halve the score cost per key.
 // With one split the CTA writes bf16 output directly; with several, normalised fp32 partials and
 // their lse go to the workspace and a combine kernel merges them.
 #include <cuda_bf16.h>
@@ -39,28 +44,34 @@ namespace dsa {
 namespace {
 
 constexpr int kHeadsPerCta = 128;                 // M of both MMAs (fewer heads: rows unused)
-constexpr int kKeysPerTile = 32;
+constexpr int kKeysPerTile = 64;
 constexpr int kChunks = kLatentDim / 64;          // 9 chunks of 64 dims (128 bytes)
 constexpr int kTmemQChunks = 6;                   // query chunks 0..5 live in tensor memory
 constexpr int kSmemQChunks = kChunks - kTmemQChunks;
 constexpr int kHalfDims = kValueDim / 2;          // 256 output dims per CTA
 constexpr int kQChunkBytes = kHeadsPerCta * 128;                // 16384
 constexpr int kQSmemBytes = kSmemQChunks * kQChunkBytes;        // 49152
-constexpr int kKvChunkBytes = kKeysPerTile * 128;               // 4096
-constexpr int kKvStageBytes = kChunks * kKvChunkBytes;          // 36864
-constexpr int kKvStages = 4;
-constexpr int kPBytes = kHeadsPerCta * kKeysPerTile * 2;        // 8192
-constexpr int kMlaThreads = 192;
+constexpr int kKvChunkBytes = kKeysPerTile * 128;               // 8192
+constexpr int kKvStageBytes = kChunks * kKvChunkBytes;          // 73728
+constexpr int kKvStages = 2;
+constexpr int kPBytes = kHeadsPerCta * kKeysPerTile * 2;        // 16384
+constexpr int kSoftmaxWarps = 4;
+constexpr int kMmaWarp = 4;
+constexpr int kProducerWarp0 = 5;
+constexpr int kProducerWarps = 2;
+constexpr int kMlaThreads = 32 * (kProducerWarp0 + kProducerWarps);   // 224
+constexpr int kKeysPerProducer = kKeysPerTile / kProducerWarps;       // 32
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = kHalfDims;                          // S buffers at columns 256, 288
-constexpr uint32_t kTmemQ = kTmemS + 2 * kKeysPerTile;         // query at columns 320 .. 511
+constexpr uint32_t kTmemS = kHalfDims;                          // S at columns 256 .. 319
+constexpr uint32_t kTmemQ = kTmemS + kKeysPerTile;              // query at columns 320 .. 511
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;                       // log2 units
-constexpr int kBatch = 4;                                      // tiles resolved per batch
+constexpr int kBatch = 4;                                       // tiles resolved per batch
 constexpr size_t kMlaSmemBytes =
     1024 + kQSmemBytes + size_t(kKvStages) * kKvStageBytes + 2 * kPBytes + 256;
 
 static_assert(kTmemQ + kTmemQChunks * 32 == kTmemCols, "tensor-memory budget");
+static_assert(kMlaSmemBytes <= 232448, "shared-memory budget");
 
 // Shared-memory matrix descriptor (sm_100 format): start, leading / stride byte offsets, layout.
 __device__ __forceinline__ uint64_t make_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
@@ -83,15 +94,37 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
-// Four rows (arbitrary row coordinates) x one box width, written to consecutive 128-byte rows.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar, int col, int r0,
-                                            int r1, int r2, int r3) {
+// Four rows (arbitrary row coordinates) x one 128-byte box, written to consecutive 128-byte rows
+// at the same shared-memory offset of every CTA in cta_mask; completion counted on the mbarrier at
+// the same offset in each of them.
+__device__ __forceinline__ void tma_gather4_mc(void* dst, const CUtensorMap* map, uint64_t* bar, int col, int r0,
+                                               int r1, int r2, int r3, uint16_t cta_mask) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(ptx::smem_addr(dst)),
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(ptx::smem_addr(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(ptx::smem_addr(bar)), "r"(col), "r"(r0), "r"(r1), "r"(r2),
-        "r"(r3)
+        "r"(r3), "h"(cta_mask)
         : "memory");
+}
+
+// Arrive once on the mbarrier at this offset in every CTA of cta_mask when all previously issued
+// tcgen05.mma of this thread have completed.
+__device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            ptx::smem_addr(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
 }
 
 // D[tmem] (+)= A[tmem] x B[smem]^T, bf16 operands, fp32 accumulate (one thread issues).
@@ -126,16 +159,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 struct MlaBars {
     uint64_t q_full;               // smem query chunks (TMA) + TMEM query chunks (4 warps)
-    uint64_t kv_full[kKvStages];
+    uint64_t kv_full[kKvStages];   // one arrive per producer warp, after its copies landed
     uint64_t kv_empty[kKvStages];
-    uint64_t s_full[2];
-    uint64_t s_empty[2];
+    uint64_t s_full;
+    uint64_t s_empty;
     uint64_t p_full[2];
     uint64_t p_empty[2];
     uint64_t o_full;
     uint32_t tmem_slot;
     uint32_t pad;
-    uint32_t valid[kKvStages];     // bit i: entry i of the stage's tile is a real latent row
+    uint32_t valid[kKvStages][kProducerWarps];   // bit i: entry 32 w + i of the stage's tile is real
 };
 
 __global__ void __launch_bounds__(kMlaThreads, 1)
@@ -149,8 +182,8 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
     const uint32_t raw_addr = ptx::smem_addr(smem_raw);
     unsigned char* base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     unsigned char* qs = base;                                   // [3][128 heads][128 B], SW128
-    unsigned char* kvs = qs + kQSmemBytes;                      // [4][9][32 keys][128 B], SW128
-    unsigned char* ps = kvs + kKvStages * kKvStageBytes;        // [2][16 row groups][4 k groups][8][16 B]
+    unsigned char* kvs = qs + kQSmemBytes;                      // [2][9][64 keys][128 B], SW128
+    unsigned char* ps = kvs + kKvStages * kKvStageBytes;        // [2][16 head groups][8 key groups][8][16 B]
     MlaBars& bar = *reinterpret_cast<MlaBars*>(ps + 2 * kPBytes);
 
     const int half = blockIdx.x;
@@ -166,21 +199,23 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
     const int ntiles = e_end > e_begin ? (e_end - e_begin + kKeysPerTile - 1) / kKeysPerTile : 0;
 
     if (threadIdx.x == 0) {
-        ptx::mbar_init(&bar.q_full, 1 + 4);
+        ptx::mbar_init(&bar.q_full, 1 + kSoftmaxWarps);
         for (int s = 0; s < kKvStages; ++s) {
-            ptx::mbar_init(&bar.kv_full[s], 1);
-            ptx::mbar_init(&bar.kv_empty[s], 1);
+            // one arrival per producer warp (the issuing one with the tile's byte count)
+            ptx::mbar_init(&bar.kv_full[s], kProducerWarps);
+            // PV completion of this CTA and of its cluster peer
+            ptx::mbar_init(&bar.kv_empty[s], 2);
         }
+        ptx::mbar_init(&bar.s_full, 1);
+        ptx::mbar_init(&bar.s_empty, kSoftmaxWarps);
         for (int a = 0; a < 2; ++a) {
-            ptx::mbar_init(&bar.s_full[a], 1);
-            ptx::mbar_init(&bar.s_empty[a], 4);
-            ptx::mbar_init(&bar.p_full[a], 4);
+            ptx::mbar_init(&bar.p_full[a], kSoftmaxWarps);
             ptx::mbar_init(&bar.p_empty[a], 1);
         }
         ptx::mbar_init(&bar.o_full, 1);
         ptx::fence_barrier_init();
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         ptx::tmem_alloc(&bar.tmem_slot, kTmemCols);
         ptx::tmem_relinquish();
     }
@@ -193,23 +228,27 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         ptx::fence_proxy_async_smem();
     }
     ptx::tc_fence_before_sync();
-    __syncthreads();
+    cluster_sync_all();   // both CTAs' barriers exist before any multicast reaches them
     ptx::tc_fence_after_sync();
     const uint32_t tmem = bar.tmem_slot;
+    const uint32_t crank = cluster_ctarank();
     const uint64_t deadline = ptx::wait_deadline();
     bool timed_out = false;
 
-    if (warp == 0) {
-        // ---------------------------------------------------------------- producer
-        if (lane == 0) {
+    if (warp >= kProducerWarp0) {
+        // ---------------------------------------------------------------- producers
+        const int pw = warp - kProducerWarp0;
+        if (pw == 0 && lane == 0) {
             ptx::mbar_arrive_expect_tx(&bar.q_full, kSmemQChunks * H * 128);
             for (int c = 0; c < kSmemQChunks; ++c)
                 tma_load_2d(qs + c * kQChunkBytes, &qmap, &bar.q_full, (kTmemQChunks + c) * 64, r * H);
         }
-        // lane i owns entry i of every tile.  Batches of kBatch tiles: entry positions are loaded two
-        // batches ahead, page ids one batch ahead, so no load waits on another on the critical path.
+        // lane l owns entry 32 pw + l of every tile.  Batches of kBatch tiles: positions are loaded two
+        // batches ahead and page ids one batch ahead, so no load waits on another on the critical path.
+        const int my_entry = pw * kKeysPerProducer + lane;
+        const bool issuer = static_cast<uint32_t>(pw) == crank;   // this CTA gathers these entries
         auto load_pos = [&](int tile) -> int {
-            const int e = e_begin + tile * kKeysPerTile + lane;
+            const int e = e_begin + tile * kKeysPerTile + my_entry;
             return (tile < ntiles && e < e_end) ? __ldg(idx + static_cast<int64_t>(r) * k + e) : -1;
         };
         auto pos_ok = [&](int pos) -> bool { return pos >= 0 && pos < v && (pos >> 6) < max_pages; };
@@ -233,7 +272,6 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
             int rows[kBatch];
 #pragma unroll
             for (int u = 0; u < kBatch; ++u) rows[u] = to_row(pos1[u], page1[u]);
-            // next batch's page ids, the batch after's positions
 #pragma unroll
             for (int u = 0; u < kBatch; ++u) {
                 pos1[u] = pos2[u];
@@ -248,29 +286,37 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
                 const int s = t % kKvStages;
                 const uint32_t ph = (t / kKvStages) & 1;
                 const uint32_t vbits = __ballot_sync(0xffffffffu, rows[u] >= 0);
-                const int row_tma = rows[u] >= 0 ? rows[u] : 0;
-                int rr[4];
-#pragma unroll
-                for (int w = 0; w < 4; ++w) rr[w] = __shfl_sync(0xffffffffu, row_tma, (4 * (lane & 7) + w) & 31);
-                if (lane == 0) {
-                    if (!ptx::mbar_wait(&bar.kv_empty[s], ph ^ 1u, deadline)) timed_out = true;
-                    if (!timed_out) {
-                        bar.valid[s] = vbits;
-                        ptx::mbar_arrive_expect_tx(&bar.kv_full[s], kKvStageBytes);
-                    }
-                }
+                const int row_src = rows[u] >= 0 ? rows[u] : 0;
+                // the stage is free once PV of its previous tile finished in both CTAs
+                if (lane == 0 && !ptx::mbar_wait(&bar.kv_empty[s], ph ^ 1u, deadline)) timed_out = true;
                 timed_out = __shfl_sync(0xffffffffu, timed_out ? 1 : 0, 0) != 0;
                 if (timed_out) break;
-                // 8 groups of 4 keys x 9 chunks; lane l < 8 issues group l's 9 gathers
-                if (lane < kKeysPerTile / 4) {
-                    unsigned char* dst = kvs + s * kKvStageBytes + lane * 4 * 128;
+                if (lane == 0) {
+                    bar.valid[s][pw] = vbits;
+                    if (issuer) ptx::mbar_arrive_expect_tx(&bar.kv_full[s], kKvStageBytes);   // both halves
+                    else ptx::mbar_arrive(&bar.kv_full[s]);
+                }
+                __syncwarp();
+                if (issuer) {
+                    int rr[4];
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) rr[w] = __shfl_sync(0xffffffffu, row_src, (4 * (lane & 7) + w) & 31);
+                    if (lane < kKeysPerProducer / 4) {   // 8 groups of 4 keys, 9 chunks each
+                        unsigned char* dst = kvs + s * kKvStageBytes + (pw * kKeysPerProducer + lane * 4) * 128;
 #pragma unroll 1
-                    for (int c = 0; c < kChunks; ++c)
-                        tma_gather4(dst + c * kKvChunkBytes, &kvmap, &bar.kv_full[s], c * 64, rr[0], rr[1], rr[2], rr[3]);
+                        for (int c = 0; c < kChunks; ++c)
+                            tma_gather4_mc(dst + c * kKvChunkBytes, &kvmap, &bar.kv_full[s], c * 64, rr[0], rr[1], rr[2],
+                                           rr[3], static_cast<uint16_t>(0x3));
+                    }
                 }
             }
         }
-    } else if (warp == 1) {
+        // drain: the last PV completions of both CTAs must have reached this CTA's barriers
+        if (pw == 0 && lane == 0 && !timed_out) {
+            for (int t = (ntiles > kKvStages ? ntiles - kKvStages : 0); t < ntiles; ++t)
+                if (!ptx::mbar_wait(&bar.kv_empty[t % kKvStages], (t / kKvStages) & 1, deadline)) timed_out = true;
+        }
+    } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_qk = ptx::instr_desc(1, 1, kHeadsPerCta, kKeysPerTile);
@@ -280,11 +326,10 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
             const uint32_t p_addr = ptx::smem_addr(ps);
             auto issue_qk = [&](int t) -> bool {
                 const int s = t % kKvStages;
-                const int a = t & 1;
                 if (!ptx::mbar_wait(&bar.kv_full[s], (t / kKvStages) & 1, deadline)) return false;
-                if (!ptx::mbar_wait(&bar.s_empty[a], ((t >> 1) & 1) ^ 1u, deadline)) return false;
+                if (!ptx::mbar_wait(&bar.s_empty, (t & 1) ^ 1u, deadline)) return false;
                 ptx::tc_fence_after_sync();
-                const uint32_t d = tmem + kTmemS + a * kKeysPerTile;
+                const uint32_t d = tmem + kTmemS;
                 const uint32_t kb = kv_addr + s * kKvStageBytes;
 #pragma unroll 1
                 for (int c = 0; c < kTmemQChunks; ++c) {
@@ -304,7 +349,7 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
                         ptx::umma_f16(d, da, db, idesc_qk, 1u);
                     }
                 }
-                ptx::umma_commit(&bar.s_full[a]);
+                ptx::umma_commit(&bar.s_full);
                 return true;
             };
             bool ok = ptx::mbar_wait(&bar.q_full, 0, deadline);
@@ -319,11 +364,11 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
                 const uint32_t vb = kv_addr + s * kKvStageBytes + (half * 4) * kKvChunkBytes;
 #pragma unroll
                 for (int ks = 0; ks < kKeysPerTile / 16; ++ks) {
-                    const uint64_t da = make_desc(p_addr + pb * kPBytes + ks * 256, 128, 512, kLayoutNone);
+                    const uint64_t da = make_desc(p_addr + pb * kPBytes + ks * 256, 128, 1024, kLayoutNone);
                     const uint64_t db = make_desc(vb + ks * 16 * 128, kKvChunkBytes, 1024, kLayoutSw128);
                     ptx::umma_f16(tmem, da, db, idesc_pv, (t | ks) != 0 ? 1u : 0u);
                 }
-                ptx::umma_commit(&bar.kv_empty[s]);
+                umma_commit_mc(&bar.kv_empty[s], static_cast<uint16_t>(0x3));   // stage free here and in the peer
                 ptx::umma_commit(&bar.p_empty[pb]);
             }
             if (ok && ntiles > 0) ptx::umma_commit(&bar.o_full);
@@ -331,7 +376,7 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         }
     } else {
         // ---------------------------------------------------------------- query -> TMEM, softmax, epilogue
-        const int quad = warp & 3;
+        const int quad = warp;                      // warps 0..3: TMEM lanes 32 quad .. +31
         const int head = quad * 32 + lane;          // TMEM lane = head
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         {
@@ -364,25 +409,25 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         const float cscale = scale * kLog2e;
         float m_run = -INFINITY, l_run = 0.0f;
         for (int t = 0; t < ntiles; ++t) {
-            const int a = t & 1;
             const int s = t % kKvStages;
             const int pb = t & 1;
-            if (!ptx::mbar_wait(&bar.s_full[a], (t >> 1) & 1, deadline)) { timed_out = true; break; }
+            if (!ptx::mbar_wait(&bar.s_full, t & 1, deadline)) { timed_out = true; break; }
             if (!ptx::mbar_wait(&bar.kv_full[s], (t / kKvStages) & 1, deadline)) { timed_out = true; break; }
             ptx::tc_fence_after_sync();
-            uint32_t sr[32];
-            ptx::tmem_ld_32x32b_x32(tmem + lane_base + kTmemS + a * kKeysPerTile, sr);
+            uint32_t sr[64];
+            ptx::tmem_ld_32x32b_x32(tmem + lane_base + kTmemS, *reinterpret_cast<uint32_t(*)[32]>(sr));
+            ptx::tmem_ld_32x32b_x32(tmem + lane_base + kTmemS + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
             ptx::tmem_wait_ld();
             ptx::tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&bar.s_empty[a]);
-            const uint32_t vbits = bar.valid[s];
-            float sv[32];
+            if (lane == 0) ptx::mbar_arrive(&bar.s_empty);
+            const uint64_t vbits = static_cast<uint64_t>(bar.valid[s][0]) | (static_cast<uint64_t>(bar.valid[s][1]) << 32);
             float tmax = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                sv[i] = ((vbits >> i) & 1u) ? __uint_as_float(sr[i]) * cscale : -INFINITY;
-                tmax = fmaxf(tmax, sv[i]);
+            for (int i = 0; i < 64; ++i) {
+                const float sv = ((vbits >> i) & 1u) ? __uint_as_float(sr[i]) * cscale : -INFINITY;
+                sr[i] = __float_as_uint(sv);
+                tmax = fmaxf(tmax, sv);
             }
             // lazy rescale: move the reference max only when the tile max exceeds it by > 8
             const bool grow = tmax > m_run + kRescaleThreshold || (m_run == -INFINITY && tmax > -INFINITY);
@@ -408,19 +453,19 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
             l_run *= alpha;
             m_run = m_new;
             float psum = 0.0f;
-            uint32_t pk[16];
+            uint32_t pk[32];
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                const float p0 = (m_run == -INFINITY) ? 0.0f : exp2f(sv[i] - m_run);
-                const float p1 = (m_run == -INFINITY) ? 0.0f : exp2f(sv[i + 1] - m_run);
+            for (int i = 0; i < 64; i += 2) {
+                const float p0 = (m_run == -INFINITY) ? 0.0f : exp2f(__uint_as_float(sr[i]) - m_run);
+                const float p1 = (m_run == -INFINITY) ? 0.0f : exp2f(__uint_as_float(sr[i + 1]) - m_run);
                 psum += p0 + p1;
                 pk[i / 2] = pack_bf16x2(p0, p1);
             }
             l_run += psum;
-            // P row of this head: 4 core matrices (8 keys x 16 B each) along K
-            unsigned char* prow = ps + pb * kPBytes + (head >> 3) * 512 + (head & 7) * 16;
+            // P row of this head: 8 core matrices (8 keys x 16 B each) along K, 128 B apart
+            unsigned char* prow = ps + pb * kPBytes + (head >> 3) * 1024 + (head & 7) * 16;
 #pragma unroll
-            for (int kg = 0; kg < 4; ++kg)
+            for (int kg = 0; kg < 8; ++kg)
                 *reinterpret_cast<uint4*>(prow + kg * 128) = make_uint4(pk[4 * kg], pk[4 * kg + 1], pk[4 * kg + 2], pk[4 * kg + 3]);
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before_sync();
@@ -486,10 +531,11 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
     if (timed_out) raise_error(err, DSA_DEVERR_TIMEOUT);
     ptx::tc_fence_before_sync();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         ptx::tc_fence_after_sync();
         ptx::tmem_dealloc(tmem, kTmemCols);
     }
+    cluster_sync_all();   // neither CTA leaves while its peer may still signal or write into it
 }
 
 __global__ void __launch_bounds__(128)
@@ -600,10 +646,22 @@ extern "C" dsa_status dsa_sparse_mla_decode(const void* q_bf16, const void* kv_p
     if (cudaFuncSetAttribute(sparse_mla_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kMlaSmemBytes)) != cudaSuccess)
         return DSA_ERR_CUDA;
-    dim3 grid(2, splits, T);
-    sparse_mla_umma_kernel<<<grid, kMlaThreads, kMlaSmemBytes, s>>>(
-        qmap, kvmap, static_cast<const uint16_t*>(q_bf16), num_pages, block_table, max_pages, seq_lens, cu_q, B, idx,
-        k, H, scale, splits, static_cast<uint16_t*>(out_bf16), lse, part_o, part_lse, dev_err);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, splits, T);   // x: the two halves of a (row, split) = one cluster
+    cfg.blockDim = dim3(kMlaThreads, 1, 1);
+    cfg.dynamicSmemBytes = kMlaSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, sparse_mla_umma_kernel, qmap, kvmap, static_cast<const uint16_t*>(q_bf16), num_pages,
+                           block_table, max_pages, seq_lens, cu_q, B, idx, k, H, scale, splits,
+                           static_cast<uint16_t*>(out_bf16), lse, part_o, part_lse, dev_err) != cudaSuccess)
+        return DSA_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
     if (splits > 1) {
         sparse_mla_combine_kernel<<<static_cast<unsigned>(static_cast<int64_t>(T) * H), 128, 0, s>>>(
