@@ -103,6 +103,11 @@ class ClockSampler:
             self.proc = None
         return self
 
+    def wait_first_sample(self, timeout_s: float = 5.0):
+        t0 = time.time()
+        while self.proc is not None and not self.lines and time.time() - t0 < timeout_s:
+            time.sleep(0.02)
+
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
@@ -319,10 +324,8 @@ def run_gpu(args):
         pg.barrier()
     capi.load()
 
-    wl = workloads.make(args.workload)
-    if rank > 0:   # every rank its own batch of the same shape (weak scaling)
-        wl = workloads.make_custom(wl.name, wl.seed + 1000 * rank, wl.seq_lens, wl.q_lens, wl.topk, wl.heads,
-                                   pool_pages=wl.num_pages)
+    from deepseek_sparse_attention_paged_gb300 import distributed as D
+    wl = D.rank_workload(args.workload, rank)   # every rank its own batch of the same shape
     db = DeviceBatch(wl)
     stream = torch.cuda.Stream()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
@@ -339,29 +342,25 @@ def run_gpu(args):
         raise RuntimeError(f"device error word {word} after warm-up")
 
     clk = ClockSampler(local).__enter__()   # samples from warm-up through the e2e run
+    clk.wait_first_sample()
     # warm-up steps (untimed)
     time_graph(step_graph, stream, args.warmup, flush)
     if pg is not None:
         pg.barrier()
     torch.cuda.synchronize()
-    if True:
-        t_wall0 = time.perf_counter()
-        step_ms = time_graph(step_graph, stream, args.steps, flush)
-        torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall0
-        # stage breakdown (each stage alone in its own graph, same flush discipline)
-        stage_iters = max(3, args.steps // 2)
-        stage_ms = {k: time_graph(g, stream, stage_iters, flush) for k, (g, _) in stage_graphs.items()}
-    timed_launches = step_kernels * args.steps + sum(n * stage_iters for _, n in stage_graphs.values())
+    t_wall0 = time.perf_counter()
+    step_ms = time_graph(step_graph, stream, args.steps, flush)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
     if pg is not None:
         pg.barrier()
     torch.cuda.synchronize()
-    mean_step = sum(step_ms) / len(step_ms)
-    if pg is not None:
-        t = torch.tensor([mean_step], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        mean_step = float(t.item())
-    value = wl.T * world / (mean_step / 1000.0)
+    # stage breakdown (each stage alone in its own graph, same flush discipline), outside the K steps
+    stage_iters = max(3, args.steps // 2)
+    stage_ms = {k: time_graph(g, stream, stage_iters, flush) for k, (g, _) in stage_graphs.items()}
+    timed_launches = step_kernels * args.steps
+    mean_step = D.max_over_ranks(sum(step_ms) / len(step_ms), device=torch.device("cuda", local))
+    value = D.aggregate_rate(wl.T, world, mean_step)
 
     # e2e: same step through the public API with host buffers (pinned), copies inside the timing
     e2e = run_e2e(db, stream, args, flush)
@@ -473,8 +472,8 @@ def main():
     ap.add_argument("--profile", choices=["store", "indexer", "topk", "mla", "step"], default=None,
                     help="launch one stage warmup+steps times without timing (for ncu) and exit")
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")

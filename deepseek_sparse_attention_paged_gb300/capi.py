@@ -78,6 +78,7 @@ def load(path: str = LIB_PATH):
         "dsa_sparse_mla_decode": (ctypes.c_int, [P, P, i64, P, i32, P, P, i32, P, i32, i32, i32, ctypes.c_float,
                                                  P, P, P, sz, P, P]),
         "dsa_read_device_error": (ctypes.c_int, [P, P, P]),
+        "dsa_selftest_wait_timeout": (ctypes.c_int, [P, ctypes.c_uint64, P]),
         "dsa_sparse_mla_decode_noalloc": (ctypes.c_int, [P, P, i64, P, i32, P, P, i32, P, i32, i32, i32,
                                                          ctypes.c_float, P, P, P, P]),
     }
@@ -255,6 +256,14 @@ def dsa_sparse_mla_decode_noalloc(q_bf16: torch.Tensor, kv_pool: torch.Tensor, b
         _ptr(cu_q), B, _ptr(idx), idx.shape[1], T, H, float(scale), _ptr(out), _ptr(lse), _ptr(dev_err),
         _stream(stream)))
     _count(2 if T > 0 else 0)
+
+
+def dsa_selftest_wait_timeout(dev_err: torch.Tensor, cycles: int, stream=None) -> None:
+    """Runs a bounded wait that can never complete; it must give up and set DSA_DEVERR_TIMEOUT."""
+    lib = load()
+    _cuda(dev_err, torch.int32, "dev_err")
+    _check("dsa_selftest_wait_timeout", lib.dsa_selftest_wait_timeout(_ptr(dev_err), int(cycles), _stream(stream)))
+    _count(1)
 
 
 def dsa_read_device_error(dev_err: torch.Tensor, stream=None):

@@ -1,5 +1,33 @@
-// dsa_api.cu -- status strings and the device error word reader of the C ABI.
+// dsa_api.cu -- status strings, the device error word reader and the bounded-wait self-test of the
+// C ABI.
 #include "dsa_common.cuh"
+#include "sm100_ptx.cuh"
+
+namespace dsa {
+namespace {
+
+// Waits on an mbarrier that nothing ever arrives on, with the same bounded wait the pipelined
+// kernels use; the wait must give up after `cycles` SM clock cycles and report the timeout in the
+// error word instead of hanging.
+__global__ void selftest_wait_kernel(int32_t* err, unsigned long long cycles) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(&bar, 1);
+        ptx::fence_barrier_init();
+    }
+    __syncthreads();
+    const uint64_t deadline = ptx::wait_deadline(cycles);
+    if (!ptx::mbar_wait(&bar, 0, deadline) && threadIdx.x == 0) raise_error(err, DSA_DEVERR_TIMEOUT);
+}
+
+}  // namespace
+}  // namespace dsa
+
+extern "C" dsa_status dsa_selftest_wait_timeout(int32_t* dev_err, uint64_t cycles, void* stream) {
+    if (dev_err == nullptr || cycles == 0 || cycles > 4000000000ull) return DSA_ERR_INVALID_ARG;
+    dsa::selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(dev_err, cycles);
+    return dsa::launch_status();
+}
 
 extern "C" const char* dsa_status_str(dsa_status s) {
     switch (s) {

@@ -231,6 +231,17 @@ dsa_status dsa_sparse_mla_decode_noalloc(const void* q_bf16, const void* kv_pool
  */
 dsa_status dsa_read_device_error(const int32_t* dev_err, int32_t* host_word, void* stream);
 
+/*
+ * dsa_selftest_wait_timeout -- failure-detection self-test of the bounded waits.
+ * The pipelined kernels (indexer logits, sparse MLA) synchronise their warps through mbarriers
+ * and never wait without a limit: a wait that has not completed after its cycle budget gives up,
+ * sets DSA_DEVERR_TIMEOUT in the error word and lets the kernel return.  This call runs one such
+ * wait on a barrier that nothing ever arrives on, with a budget of `cycles` SM clock cycles
+ * (1 .. 4e9), so that a test can check the timeout path end to end: afterwards *dev_err has
+ * DSA_DEVERR_TIMEOUT set and the CUDA context is still usable.  No fault, trap or hang is involved.
+ */
+dsa_status dsa_selftest_wait_timeout(int32_t* dev_err, uint64_t cycles, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
