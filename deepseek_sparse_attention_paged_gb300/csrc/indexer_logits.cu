@@ -87,10 +87,13 @@ struct IdxCfg {
     static constexpr int N = 64 * R;
     static constexpr int kStages = (R == 2) ? 5 : 6;
     static constexpr int kQBytes = N * kIndexDim;
-    static constexpr uint32_t kTmemCols = (2 * N < 32) ? 32 : 2 * N;   // two accumulator buffers
+    // accumulator buffers in tensor memory: the MMA runs this many tiles ahead of the epilogue
+    // (4 x 64 columns for one row; 2 x N columns for row groups, so that 2 CTAs fit one SM)
+    static constexpr int kAcc = (R == 1) ? 4 : 2;
+    static constexpr uint32_t kTmemCols = kAcc * N;
     static constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + size_t(kStages) * kTileCodeBytes + kQBytes +
                                          size_t(kStages) * kTileKeys * 4 /*scales*/ + R * 64 * 4 /*w'*/ +
-                                         (2 * kStages + 5) * 8 /*barriers*/ + 16 + 2 * kStages;
+                                         (2 * kStages + 2 * kAcc + 1) * 8 /*barriers*/ + 16 + 2 * kStages;
 };
 
 template <int R>
@@ -113,9 +116,10 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint1
     float* wq = scales + S * kTileKeys;                                  // [R][64]
     uint64_t* full = reinterpret_cast<uint64_t*>(wq + R * 64);
     uint64_t* empty = full + S;
+    constexpr int NA = C::kAcc;
     uint64_t* tfull = empty + S;
-    uint64_t* tempty = tfull + 2;
-    uint64_t* q_ready = tempty + 2;
+    uint64_t* tempty = tfull + NA;
+    uint64_t* q_ready = tempty + NA;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 1);
     uint8_t* page_ok = reinterpret_cast<uint8_t*>(tmem_slot + 4);        // [S][2]
 
@@ -139,7 +143,7 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint1
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], 1 + 4);   // MMA commit + one arrive per epilogue warp
         }
-        for (int a = 0; a < 2; ++a) {
+        for (int a = 0; a < NA; ++a) {
             ptx::mbar_init(&tfull[a], 1);
             ptx::mbar_init(&tempty[a], 4);
         }
@@ -199,8 +203,8 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint1
             for (int i = 0; i < ntiles && !timed_out; ++i) {
                 const int s = i % S;
                 const uint32_t ph = (i / S) & 1;
-                const int a = i & 1;
-                const uint32_t aph = (i >> 1) & 1;
+                const int a = i % NA;
+                const uint32_t aph = (i / NA) & 1;
                 if (!ptx::mbar_wait(&full[s], ph, deadline)) { timed_out = true; break; }
                 if (!ptx::mbar_wait(&tempty[a], aph ^ 1u, deadline)) { timed_out = true; break; }
                 ptx::tc_fence_after_sync();
@@ -262,8 +266,8 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint1
         for (int i = 0; i < ntiles && !timed_out; ++i) {
             const int s = i % S;
             const uint32_t ph = (i / S) & 1;
-            const int a = i & 1;
-            const uint32_t aph = (i >> 1) & 1;
+            const int a = i % NA;
+            const uint32_t aph = (i / NA) & 1;
             if (!ptx::mbar_wait(&full[s], ph, deadline)) { timed_out = true; break; }
             if (!ptx::mbar_wait(&tfull[a], aph, deadline)) { timed_out = true; break; }
             ptx::tc_fence_after_sync();

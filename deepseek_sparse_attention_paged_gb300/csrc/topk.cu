@@ -211,10 +211,31 @@ topk_bitmap_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* 
     }
     const int W = (v + 31) / 32;
 
+    // Visit every (index, key) of the row: 16-byte loads when the row is 16-byte aligned (several
+    // loads in flight per thread), scalar otherwise and for the tail.
+    const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+    const int v4 = vec ? (v >> 2) : 0;
+    auto for_each_key = [&](auto&& fn) {
+        const float4* row4 = reinterpret_cast<const float4*>(row);
+        int i = threadIdx.x;
+        for (; i + kTopkThreads < v4; i += 2 * kTopkThreads) {
+            const float4 a = __ldg(row4 + i);
+            const float4 c = __ldg(row4 + i + kTopkThreads);
+            fn(4 * i, order_key(a.x)); fn(4 * i + 1, order_key(a.y)); fn(4 * i + 2, order_key(a.z)); fn(4 * i + 3, order_key(a.w));
+            const int j = i + kTopkThreads;
+            fn(4 * j, order_key(c.x)); fn(4 * j + 1, order_key(c.y)); fn(4 * j + 2, order_key(c.z)); fn(4 * j + 3, order_key(c.w));
+        }
+        for (; i < v4; i += kTopkThreads) {
+            const float4 a = __ldg(row4 + i);
+            fn(4 * i, order_key(a.x)); fn(4 * i + 1, order_key(a.y)); fn(4 * i + 2, order_key(a.z)); fn(4 * i + 3, order_key(a.w));
+        }
+        for (int s = 4 * v4 + threadIdx.x; s < v; s += kTopkThreads) fn(s, order_key(__ldg(row + s)));
+    };
+
     // ---- read 1: top-12-bit histogram
     for (int i = threadIdx.x; i < kTopBins; i += kTopkThreads) sm.hist[i] = 0;
     __syncthreads();
-    for (int s = threadIdx.x; s < v; s += kTopkThreads) atomicAdd(&sm.hist[order_key(__ldg(row + s)) >> 20], 1u);
+    for_each_key([&](int, uint32_t key) { atomicAdd(&sm.hist[key >> 20], 1u); });
     __syncthreads();
     select_bin(sm.hist, sm, kTopBins, static_cast<uint32_t>(k));
     const uint32_t b1 = sm.sel_digit;
@@ -224,8 +245,7 @@ topk_bitmap_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* 
     for (int w = threadIdx.x; w < W; w += kTopkThreads) sel[w] = tie[w] = 0u;
     if (threadIdx.x == 0) sm.cand_count = 0;
     __syncthreads();
-    for (int s = threadIdx.x; s < v; s += kTopkThreads) {
-        const uint32_t key = order_key(__ldg(row + s));
+    for_each_key([&](int s, uint32_t key) {
         const uint32_t bin = key >> 20;
         if (bin > b1) {
             atomicOr(&sel[s >> 5], 1u << (s & 31));
@@ -236,7 +256,7 @@ topk_bitmap_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* 
                 cidx[p] = s;
             }
         }
-    }
+    });
     __syncthreads();
     const uint32_t n = sm.cand_count;
     const bool in_smem = n <= static_cast<uint32_t>(kCandidateCap);
