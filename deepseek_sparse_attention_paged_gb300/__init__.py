@@ -7,6 +7,7 @@ the library build (``build``) and the seeded synthetic workloads (``workloads``)
 from .capi import (  # noqa: F401
     DSAError,
     dsa_indexer_logits,
+    dsa_indexer_logits_workspace_size,
     dsa_read_device_error,
     dsa_sparse_mla_decode,
     dsa_sparse_mla_workspace_size,

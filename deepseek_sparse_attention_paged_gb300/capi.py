@@ -70,8 +70,9 @@ def load(path: str = LIB_PATH):
     sigs = {
         "dsa_status_str": (ctypes.c_char_p, [ctypes.c_int]),
         "dsa_store_index_k": (ctypes.c_int, [P, P, i64, P, i64, i32, P, P]),
+        "dsa_indexer_logits_workspace_size": (sz, [i32]),
         "dsa_indexer_logits": (ctypes.c_int, [P, P, P, i64, P, i32, P, P, i32, i32, i32, i32, i32, P, i64, u32,
-                                              P, P]),
+                                              P, sz, P, P]),
         "dsa_topk_workspace_size": (sz, [i32, i32, i32]),
         "dsa_topk": (ctypes.c_int, [P, i64, P, P, i32, i32, i32, i32, i32, P, P, sz, P]),
         "dsa_sparse_mla_workspace_size": (sz, [i32, i32, i32]),
@@ -149,7 +150,10 @@ def dsa_indexer_logits(q_bf16: torch.Tensor, weights: torch.Tensor, index_k_pool
                        block_table: torch.Tensor, seq_lens: torch.Tensor, cu_q: torch.Tensor,
                        max_seq_len: int, max_q_len: int, logits: torch.Tensor, row_begin: int = 0,
                        row_end: Optional[int] = None, flags: int = 0, dev_err: Optional[torch.Tensor] = None,
-                       stream=None) -> None:
+                       stream=None, workspace: Optional[torch.Tensor] = None) -> None:
+    """Logits of rows [row_begin, row_end).  `workspace` is device scratch of at least
+    dsa_indexer_logits_workspace_size(row_end - row_begin) bytes; when it is None a buffer of that
+    size is taken from torch's allocator for this call."""
     lib = load()
     _cuda(q_bf16, torch.bfloat16, "q_bf16")
     _cuda(weights, torch.float32, "weights")
@@ -166,11 +170,20 @@ def dsa_indexer_logits(q_bf16: torch.Tensor, weights: torch.Tensor, index_k_pool
     row_end = T if row_end is None else row_end
     _need(0 <= row_begin <= row_end <= T, "row range")
     _need(logits.dim() == 2 and logits.shape[0] >= row_end - row_begin, "logits rows")
+    if workspace is None:
+        workspace = torch.empty(max(16, dsa_indexer_logits_workspace_size(row_end - row_begin)), dtype=torch.uint8,
+                                device=q_bf16.device)
+    _need(workspace.is_cuda and workspace.is_contiguous(), "workspace must be a contiguous CUDA tensor")
     _check("dsa_indexer_logits", lib.dsa_indexer_logits(
         _ptr(q_bf16), _ptr(weights), _ptr(index_k_pool), index_k_pool.shape[0], _ptr(block_table),
         block_table.shape[1], _ptr(seq_lens), _ptr(cu_q), B, int(max_seq_len), int(max_q_len), int(row_begin),
-        int(row_end), _ptr(logits), logits.stride(0), int(flags), _ptr(dev_err), _stream(stream)))
-    _count(1 if row_end > row_begin else 0)
+        int(row_end), _ptr(logits), logits.stride(0), int(flags), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_err), _stream(stream)))
+    _count(2 if row_end > row_begin else 0)
+
+
+def dsa_indexer_logits_workspace_size(rows: int) -> int:
+    return int(load().dsa_indexer_logits_workspace_size(int(rows)))
 
 
 def dsa_topk_workspace_size(rows: int, k: int, max_seq_len: int) -> int:

@@ -6,9 +6,15 @@
 //     I[r,s] = sum_h w[r,h] * q_scale[r,h] * ReLU(k_scale[s] * sum_d q_code[r,h,d] * k_code[s,d])
 // for s < v_r.
 //
-// The contraction over the 128 dims is an FP8 tensor-core product (tcgen05, fp32 accumulation in
-// tensor memory); the ReLU, head gates and head sum are fused into the epilogue that reads the
-// accumulator, so only the final fp32 logit of each (row, key) reaches global memory.
+// Two kernels.  The query prologue quantises every (row, head) vector exactly once into the
+// caller's workspace, already in the shared-memory layout the tensor cores read.  The logits
+// kernel is persistent: one CTA per SM takes an equal share of all 128-key tiles of all requests
+// (tiles of one (request, row group) are consecutive), streams the key pages through a deep TMA
+// ring, multiplies them with the resident query tile on the FP8 tensor cores (tcgen05, fp32
+// accumulation in tensor memory) and reduces ReLU, head gates and head sum in the epilogue that
+// reads the accumulator, so only the final fp32 logit of each (row, key) reaches global memory.
+// The logits kernel is launched as a programmatic dependent of the prologue, so its setup and its
+// first key pages overlap the prologue; only the query-tile loads wait for it.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -62,241 +68,395 @@ __device__ __forceinline__ uint32_t quantise_head(float x[4], bool rotate, int l
     return packed;
 }
 
-// ---------------------------------------------------------------------------------------------
-// tcgen05 kernel.  CTA = (request b, group of R query rows, chunk of `chunk_tiles` 128-key tiles).
-//
-//   D[key, n] = sum_d k_code[key, d] * q_code[n, d]      n = row_in_group * 64 + head
-//
-// is one M = 128 (keys) x N = 64 R x K = 128 FP8 UMMA per tile (4 instructions of K = 32), the
-// key tile (two 64-token pages, 8 KB of codes each) arriving by TMA with the 128-byte swizzle and
-// the quantised query tile resident in shared memory in the same layout.  The accumulator sits in
-// tensor memory, double-buffered so the epilogue of tile i overlaps the MMA of tile i + 1.
-//
-// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM owner + MMA issuer, warps 2-5 =
-// epilogue (warp w reads TMEM lanes 32 (w % 4) .. +31, i.e. one key per thread), which applies
-// ReLU, the per-head gate w' = w * q_scale, the sum over heads and the key scale, and writes the
-// logit.  All six warps quantise the query tile first.
-// ---------------------------------------------------------------------------------------------
-
 constexpr int kTileKeys = 128;
-constexpr int kTileCodeBytes = kTileKeys * kIndexDim;  // 16 KB: two pages of codes
-constexpr int kUmmaThreads = 192;
+constexpr int kTileCodeBytes = kTileKeys * kIndexDim;    // 16 KB: two pages of codes
+constexpr int kQRowBytes = kIndexHeads * kIndexDim;       // 8 KB of codes per query row
+constexpr int kQGateBytes = kIndexHeads * 4;              // 64 fp32 gates w' per query row
+constexpr int kThreads = 352;                             // 11 warps
+constexpr int kEpiWarp0 = 2;                              // warps 2..9: two epilogue warpgroups
+constexpr int kLoaderWarp = 10;
 
+// ---------------------------------------------------------------------------------------------
+// Query prologue: one warp per (row, head) vector.  Writes the 128 codes of the vector into the
+// row's 8 KB block of the workspace at the position the 128-byte swizzle gives B-operand row
+// `head` (16-byte chunk c of row h lands at chunk c ^ (h & 7)), and w' = w * q_scale.
+// ---------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+indexer_q_prologue_kernel(const uint16_t* __restrict__ q, const float* __restrict__ w,
+                          const int32_t* __restrict__ cu_q, int B, int row_begin, int row_end, int rotate,
+                          uint8_t* __restrict__ q_codes, float* __restrict__ q_gates) {
+    ptx::griddep_launch_dependents();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t v = static_cast<int64_t>(blockIdx.x) * 8 + warp;   // (row - row_begin) * 64 + head
+    if (v >= static_cast<int64_t>(row_end - row_begin) * kIndexHeads) return;
+    const int64_t r = row_begin + v / kIndexHeads;
+    const int h = static_cast<int>(v % kIndexHeads);
+    if (r >= __ldg(cu_q + B)) return;
+    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(q + (r * kIndexHeads + h) * kIndexDim) + lane);
+    float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
+    float scale;
+    const uint32_t packed = quantise_head(x, rotate != 0, lane, &scale);
+    uint8_t* dst = q_codes + (v / kIndexHeads) * kQRowBytes;
+    const uint32_t off = h * 128 + (((lane >> 2) ^ (h & 7)) << 4) + ((lane & 3) << 2);
+    *reinterpret_cast<uint32_t*>(dst + off) = packed;
+    if (lane == 0) q_gates[v] = __ldg(w + r * kIndexHeads + h) * scale;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Work decomposition.  A segment is one (request b, group g of R consecutive query rows); its
+// tiles are the 128-key tiles [0, ceil(vmax / 128)) of the group's longest visible prefix.  The
+// segments are numbered b * G + g (G = groups of the longest request) and their tiles
+// concatenated; CTA c of the grid takes the tiles [T c / grid, T (c+1) / grid).
+// ---------------------------------------------------------------------------------------------
+struct Seg {
+    int sidx;     // b * G + g
+    int b, L, q0, q_len, j0, nrows, vmax;
+    int ntiles;   // tiles of the whole segment
+    int tile;     // current tile within the segment
+};
+
+struct SegArgs {
+    const int32_t* seq_lens;
+    const int32_t* cu_q;
+    int B, G, R, row_begin, row_end;
+};
+
+__device__ __forceinline__ int seg_load(const SegArgs& a, int sidx, Seg& s) {
+    s.sidx = sidx;
+    s.ntiles = 0;
+    const int b = sidx / a.G;
+    const int g = sidx - b * a.G;
+    if (b >= a.B) return 0;
+    const int q0 = __ldg(a.cu_q + b);
+    const int q_len = __ldg(a.cu_q + b + 1) - q0;
+    const int j0 = g * a.R;
+    if (j0 >= q_len) return 0;
+    const int nrows = min(a.R, q_len - j0);
+    if (q0 + j0 >= a.row_end || q0 + j0 + nrows <= a.row_begin) return 0;
+    const int L = __ldg(a.seq_lens + b);
+    s.b = b; s.L = L; s.q0 = q0; s.q_len = q_len; s.j0 = j0; s.nrows = nrows;
+    s.vmax = visible_len(L, q_len, j0 + nrows - 1);
+    s.ntiles = (s.vmax + kTileKeys - 1) / kTileKeys;
+    return s.ntiles;
+}
+
+// Move to the first tile of the next segment that has tiles (the caller knows one exists).
+__device__ __forceinline__ void seg_next(const SegArgs& a, Seg& s) {
+    int sidx = s.sidx;
+    while (seg_load(a, ++sidx, s) == 0 && sidx < a.B * a.G) {
+    }
+    s.tile = 0;
+}
+
+// Block-wide (warps kEpiWarp0 .. kEpiWarp0 + 7, named barrier 1) inclusive scan of one int64 per
+// thread; `scratch` holds 8 partials.  Returns this thread's inclusive prefix and the total.
+__device__ __forceinline__ int64_t epi_scan(int64_t v, int64_t* scratch, int64_t* total) {
+    const int t = threadIdx.x - kEpiWarp0 * 32;
+    const int lane = t & 31, w = t >> 5;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int64_t o = __shfl_up_sync(0xffffffffu, v, d);
+        if (lane >= d) v += o;
+    }
+    if (lane == 31) scratch[w] = v;
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    int64_t before = 0, all = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int64_t x = scratch[i];
+        if (i < w) before += x;
+        all += x;
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    *total = all;
+    return before + v;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Logits kernel.  Per tile, with n = row_in_group * 64 + head:
+//     D[key, n] = sum_d k_code[key, d] * q_code[n, d]
+// is one M = 128 (keys) x N = 64 R x K = 128 FP8 UMMA (4 instructions of K = 32), the key tile
+// (two 64-token pages, 8 KB of codes each) arriving by TMA with the 128-byte swizzle and the query
+// tile of the segment (R rows x 8 KB, double-buffered across segments) by bulk copy from the
+// prologue's workspace.
+//
+// Warp roles (352 threads): warp 0 = key producer, warp 1 = TMEM owner + MMA issuer, warps 2-9 =
+// two epilogue warpgroups taking alternate tiles (warp w reads TMEM lanes 32 (w % 4) .. +31, one
+// key per thread: ReLU, gates w', head sum, key scale, store), warp 10 = query-tile loader.
+// ---------------------------------------------------------------------------------------------
 template <int R>
 struct IdxCfg {
     static constexpr int N = 64 * R;
-    static constexpr int kStages = (R == 2) ? 5 : 6;
-    static constexpr int kQBytes = N * kIndexDim;
-    // accumulator buffers in tensor memory: the MMA runs this many tiles ahead of the epilogue
-    // (4 x 64 columns for one row; 2 x N columns for row groups, so that 2 CTAs fit one SM)
-    static constexpr int kAcc = (R == 1) ? 4 : 2;
-    static constexpr uint32_t kTmemCols = kAcc * N;
-    static constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + size_t(kStages) * kTileCodeBytes + kQBytes +
-                                         size_t(kStages) * kTileKeys * 4 /*scales*/ + R * 64 * 4 /*w'*/ +
-                                         (2 * kStages + 2 * kAcc + 1) * 8 /*barriers*/ + 16 + 2 * kStages;
+    static constexpr int kStages = (R == 1) ? 12 : (R == 2 ? 11 : 9);
+    static constexpr int kAcc = (R == 4) ? 2 : 4;                 // accumulators of N columns
+    static constexpr uint32_t kTmemCols = kAcc * N;               // 256 / 512 / 512
+    static constexpr int kQBytes = R * kQRowBytes;
+    static constexpr size_t kCodesOff = 0;
+    static constexpr size_t kQOff = kCodesOff + size_t(kStages) * kTileCodeBytes;
+    static constexpr size_t kScalesOff = kQOff + 2 * size_t(kQBytes);
+    static constexpr size_t kGatesOff = kScalesOff + size_t(kStages) * kTileKeys * 4;
+    static constexpr size_t kBarOff = kGatesOff + 2 * size_t(R) * kQGateBytes;
+    static constexpr int kBars = 2 * kStages + 2 * kAcc + 4;
+    static constexpr size_t kMiscOff = kBarOff + size_t(kBars) * 8;   // tmem slot, partition, scan
+    static constexpr size_t kPageOkOff = kMiscOff + 16 + 8 * 8;
+    static constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kPageOkOff + 2 * kStages;
 };
 
 template <int R>
-__global__ void __launch_bounds__(kUmmaThreads, (R == 4) ? 1 : 2)
-indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint16_t* __restrict__ q,
-                           const float* __restrict__ w, const uint8_t* __restrict__ pool, int64_t num_pages,
+__global__ void __launch_bounds__(kThreads, 1)
+indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8_t* __restrict__ q_codes,
+                           const float* __restrict__ q_gates, const uint8_t* __restrict__ pool, int64_t num_pages,
                            const int32_t* __restrict__ block_table, int max_pages,
-                           const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q, int row_begin,
-                           int row_end, float* __restrict__ logits, int64_t ld, int rotate, int chunk_tiles,
-                           int32_t* err) {
+                           const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q, int B, int G,
+                           int row_begin, int row_end, float* __restrict__ logits, int64_t ld, int32_t* err) {
     using C = IdxCfg<R>;
     constexpr int S = C::kStages;
     constexpr int N = C::N;
+    constexpr int NA = C::kAcc;
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw_addr = ptx::smem_addr(smem_raw);
     unsigned char* base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-    unsigned char* codes = base;                                         // [S][16 KB], 1024-aligned
-    unsigned char* qtile = codes + S * kTileCodeBytes;                   // [N][128] swizzled
-    float* scales = reinterpret_cast<float*>(qtile + C::kQBytes);        // [S][128]
-    float* wq = scales + S * kTileKeys;                                  // [R][64]
-    uint64_t* full = reinterpret_cast<uint64_t*>(wq + R * 64);
+    unsigned char* codes = base + C::kCodesOff;                               // [S][16 KB]
+    unsigned char* qtile = base + C::kQOff;                                   // [2][R * 8 KB]
+    float* scales = reinterpret_cast<float*>(base + C::kScalesOff);           // [S][128]
+    float* gates = reinterpret_cast<float*>(base + C::kGatesOff);             // [2][R * 64]
+    uint64_t* full = reinterpret_cast<uint64_t*>(base + C::kBarOff);
     uint64_t* empty = full + S;
-    constexpr int NA = C::kAcc;
     uint64_t* tfull = empty + S;
     uint64_t* tempty = tfull + NA;
-    uint64_t* q_ready = tempty + NA;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 1);
-    uint8_t* page_ok = reinterpret_cast<uint8_t*>(tmem_slot + 4);        // [S][2]
-
-    const int b = blockIdx.z;
-    const int L = __ldg(seq_lens + b);
-    const int q0 = __ldg(cu_q + b);
-    const int q_len = __ldg(cu_q + b + 1) - q0;
-    const int j0 = blockIdx.y * R;
-    if (j0 >= q_len) return;
-    const int nrows = min(R, q_len - j0);
-    if (q0 + j0 >= row_end || q0 + j0 + nrows <= row_begin) return;
-    const int vmax = visible_len(L, q_len, j0 + nrows - 1);
-    const int tiles_total = (vmax + kTileKeys - 1) / kTileKeys;
-    const int t_begin = blockIdx.x * chunk_tiles;
-    if (t_begin >= tiles_total) return;
-    const int ntiles = min(tiles_total, t_begin + chunk_tiles) - t_begin;
+    uint64_t* qfull = tempty + NA;     // [2]
+    uint64_t* qempty = qfull + 2;      // [2]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + C::kMiscOff);
+    int32_t* part = reinterpret_cast<int32_t*>(base + C::kMiscOff + 4);      // start segment, tile, count
+    int64_t* scan_scratch = reinterpret_cast<int64_t*>(base + C::kMiscOff + 16);
+    uint8_t* page_ok = base + C::kPageOkOff;                                  // [S][2]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const SegArgs sa{seq_lens, cu_q, B, G, R, row_begin, row_end};
+    const int nseg = B * G;
+
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(&full[s], 1);
-            ptx::mbar_init(&empty[s], 1 + 4);   // MMA commit + one arrive per epilogue warp
+            ptx::mbar_init(&empty[s], 1 + 4);   // MMA commit + the 4 warps of the tile's epilogue group
         }
         for (int a = 0; a < NA; ++a) {
             ptx::mbar_init(&tfull[a], 1);
             ptx::mbar_init(&tempty[a], 4);
         }
-        ptx::mbar_init(q_ready, 4);             // one arrive per query-prologue warp
+        for (int b2 = 0; b2 < 2; ++b2) {
+            ptx::mbar_init(&qfull[b2], 1);
+            ptx::mbar_init(&qempty[b2], 1 + 8);  // MMA commit + every epilogue warp
+        }
         ptx::fence_barrier_init();
     }
     if (warp == 1) {
         ptx::tmem_alloc(tmem_slot, C::kTmemCols);
         ptx::tmem_relinquish();
     }
+    if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 8) {
+        // this CTA's share of the tiles: total over all segments, then the segment holding t0
+        const int t = threadIdx.x - kEpiWarp0 * 32;
+        int64_t mine = 0;
+        Seg tmp;
+        for (int sidx = t; sidx < nseg; sidx += 256) mine += seg_load(sa, sidx, tmp);
+        int64_t total;
+        epi_scan(mine, scan_scratch, &total);
+        const int64_t t0 = total * blockIdx.x / gridDim.x;
+        const int64_t t1 = total * (blockIdx.x + 1) / gridDim.x;
+        if (t == 0) {
+            part[0] = nseg;
+            part[1] = 0;
+            part[2] = static_cast<int32_t>(t1 - t0);
+        }
+        if (t1 > t0) {
+            int64_t seen = 0;
+            for (int c0 = 0; c0 < nseg; c0 += 256) {
+                const int n = (c0 + t < nseg) ? seg_load(sa, c0 + t, tmp) : 0;
+                int64_t chunk_total;
+                const int64_t incl = epi_scan(n, scan_scratch, &chunk_total) + seen;
+                if (n > 0 && incl - n <= t0 && t0 < incl) {
+                    part[0] = c0 + t;
+                    part[1] = static_cast<int32_t>(t0 - (incl - n));
+                }
+                seen += chunk_total;
+                if (seen > t0) break;
+            }
+        }
+    }
     ptx::tc_fence_before_sync();
     __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    const int count = part[2];
     const uint64_t deadline = ptx::wait_deadline();
     bool timed_out = false;
+    Seg sg;
+    if (count > 0) {
+        seg_load(sa, part[0], sg);
+        sg.tile = part[1];
+    }
 
-    if (warp == 0) {       // ---------------- TMA producer (key tiles start streaming at once)
-        // the chunk's block-table entries, one per lane (2 pages per tile, <= 32 entries)
-        int32_t my_page = -1;
-        if (lane < 2 * ntiles && 2 * t_begin + lane < max_pages)
-            my_page = __ldg(block_table + static_cast<int64_t>(b) * max_pages + 2 * t_begin + lane);
-        for (int i = 0; i < ntiles; ++i) {
-            const int s = i % S;
-            const uint32_t ph = (i / S) & 1;
-            const int32_t pg0 = __shfl_sync(0xffffffffu, my_page, 2 * i);
-            const int32_t pg1 = __shfl_sync(0xffffffffu, my_page, 2 * i + 1);
+    if (warp == 0 && count > 0) {   // ---------------- key producer
+        int32_t win = -1;           // block-table entries 2 * wbase + lane of segment wseg
+        int wbase = -1, wseg = -1;
+        int s = 0;
+        uint32_t ph = 0;
+        for (int i = 0; i < count; ++i) {
+            const int wb = sg.tile & ~15;
+            if (wb != wbase || sg.sidx != wseg) {
+                wbase = wb;
+                wseg = sg.sidx;
+                const int e = 2 * wb + lane;
+                win = (e < 2 * sg.ntiles && e < max_pages)
+                          ? __ldg(block_table + static_cast<int64_t>(sg.b) * max_pages + e)
+                          : -1;
+            }
+            const int32_t pg0 = __shfl_sync(0xffffffffu, win, 2 * (sg.tile - wb));
+            const int32_t pg1 = __shfl_sync(0xffffffffu, win, 2 * (sg.tile - wb) + 1);
             if (lane == 0) {
-                if (!ptx::mbar_wait(&empty[s], ph ^ 1u, deadline)) { timed_out = true; break; }
-                const int t = t_begin + i;
-                const bool need1 = t * kTileKeys + kPage < vmax;
-                const bool ok0 = pg0 >= 0 && pg0 < num_pages;
-                const bool ok1 = need1 && pg1 >= 0 && pg1 < num_pages;
-                if (!ok0 || (need1 && !ok1)) raise_error(err, DSA_DEVERR_PAGE_RANGE);
-                page_ok[2 * s] = ok0;
-                page_ok[2 * s + 1] = ok1;
-                const uint32_t bytes = (ok0 ? (kPage * kIndexDim + kPage * 4) : 0) + (ok1 ? (kPage * kIndexDim + kPage * 4) : 0);
-                ptx::mbar_arrive_expect_tx(&full[s], bytes);
-                unsigned char* dst = codes + s * kTileCodeBytes;
-                if (ok0) {
-                    ptx::tma_load_3d(dst, &kmap, &full[s], 0, 0, pg0);
-                    ptx::bulk_load(scales + s * kTileKeys, pool + static_cast<int64_t>(pg0) * kIndexPageBytes + kIndexScaleOffset,
-                                   kPage * 4, &full[s]);
-                }
-                if (ok1) {
-                    ptx::tma_load_3d(dst + kPage * kIndexDim, &kmap, &full[s], 0, 0, pg1);
-                    ptx::bulk_load(scales + s * kTileKeys + kPage,
-                                   pool + static_cast<int64_t>(pg1) * kIndexPageBytes + kIndexScaleOffset, kPage * 4, &full[s]);
+                if (!ptx::mbar_wait(&empty[s], ph ^ 1u, deadline)) timed_out = true;
+                if (!timed_out) {
+                    const bool need1 = sg.tile * kTileKeys + kPage < sg.vmax;
+                    const bool ok0 = pg0 >= 0 && pg0 < num_pages;
+                    const bool ok1 = need1 && pg1 >= 0 && pg1 < num_pages;
+                    if (!ok0 || (need1 && !ok1)) raise_error(err, DSA_DEVERR_PAGE_RANGE);
+                    page_ok[2 * s] = ok0;
+                    page_ok[2 * s + 1] = ok1;
+                    const uint32_t bytes = (ok0 ? (kPage * kIndexDim + kPage * 4) : 0) +
+                                           (ok1 ? (kPage * kIndexDim + kPage * 4) : 0);
+                    ptx::mbar_arrive_expect_tx(&full[s], bytes);
+                    unsigned char* dst = codes + s * kTileCodeBytes;
+                    if (ok0) {
+                        ptx::tma_load_3d(dst, &kmap, &full[s], 0, 0, pg0);
+                        ptx::bulk_load(scales + s * kTileKeys,
+                                       pool + static_cast<int64_t>(pg0) * kIndexPageBytes + kIndexScaleOffset,
+                                       kPage * 4, &full[s]);
+                    }
+                    if (ok1) {
+                        ptx::tma_load_3d(dst + kPage * kIndexDim, &kmap, &full[s], 0, 0, pg1);
+                        ptx::bulk_load(scales + s * kTileKeys + kPage,
+                                       pool + static_cast<int64_t>(pg1) * kIndexPageBytes + kIndexScaleOffset,
+                                       kPage * 4, &full[s]);
+                    }
                 }
             }
+            if (__shfl_sync(0xffffffffu, timed_out ? 1 : 0, 0)) { timed_out = true; break; }
+            if (++s == S) { s = 0; ph ^= 1u; }
+            if (++sg.tile == sg.ntiles && i + 1 < count) seg_next(sa, sg);
         }
-    } else if (warp == 1) {
-        if (lane == 0) {   // ---------------- MMA issuer
+    } else if (warp == kLoaderWarp && count > 0) {   // ---------------- query-tile loader
+        if (lane == 0) {
+            ptx::griddep_wait();   // the prologue's workspace is complete and visible
+            int remaining = count;
+            for (int n = 0; remaining > 0; ++n) {
+                const int qb = n & 1;
+                if (!ptx::mbar_wait(&qempty[qb], ((n >> 1) & 1) ^ 1u, deadline)) { timed_out = true; break; }
+                uint32_t bytes = 0;
+                for (int jj = 0; jj < sg.nrows; ++jj) {
+                    const int r = sg.q0 + sg.j0 + jj;
+                    if (r >= row_begin && r < row_end) bytes += kQRowBytes + kQGateBytes;
+                }
+                ptx::mbar_arrive_expect_tx(&qfull[qb], bytes);
+                for (int jj = 0; jj < sg.nrows; ++jj) {
+                    const int r = sg.q0 + sg.j0 + jj;
+                    if (r < row_begin || r >= row_end) continue;
+                    const int64_t rr = r - row_begin;
+                    ptx::bulk_load(qtile + qb * C::kQBytes + jj * kQRowBytes, q_codes + rr * kQRowBytes, kQRowBytes,
+                                   &qfull[qb]);
+                    ptx::bulk_load(gates + (qb * R + jj) * kIndexHeads, q_gates + rr * kIndexHeads, kQGateBytes,
+                                   &qfull[qb]);
+                }
+                remaining -= sg.ntiles - sg.tile;
+                if (remaining > 0) seg_next(sa, sg);
+            }
+        }
+    } else if (warp == 1 && count > 0) {   // ---------------- MMA issuer
+        if (lane == 0) {
             constexpr uint32_t idesc = ptx::instr_desc(0, 0, kTileKeys, N);
-            const uint32_t q_addr = ptx::smem_addr(qtile);
-            if (!ptx::mbar_wait(q_ready, 0, deadline)) timed_out = true;
-            for (int i = 0; i < ntiles && !timed_out; ++i) {
-                const int s = i % S;
-                const uint32_t ph = (i / S) & 1;
+            int s = 0, n = 0;
+            uint32_t ph = 0;
+            bool seg_start = true;
+            for (int i = 0; i < count && !timed_out; ++i) {
+                const int qb = n & 1;
+                if (seg_start && !ptx::mbar_wait(&qfull[qb], (n >> 1) & 1, deadline)) { timed_out = true; break; }
+                seg_start = false;
                 const int a = i % NA;
                 const uint32_t aph = (i / NA) & 1;
                 if (!ptx::mbar_wait(&full[s], ph, deadline)) { timed_out = true; break; }
                 if (!ptx::mbar_wait(&tempty[a], aph ^ 1u, deadline)) { timed_out = true; break; }
                 ptx::tc_fence_after_sync();
                 const uint32_t a_addr = ptx::smem_addr(codes + s * kTileCodeBytes);
+                const uint32_t q_addr = ptx::smem_addr(qtile + qb * C::kQBytes);
                 const uint32_t d = tmem + static_cast<uint32_t>(a * N);
 #pragma unroll
                 for (int k = 0; k < kIndexDim / 32; ++k)
-                    ptx::umma_f8f6f4(d, ptx::sw128_kmajor_desc(a_addr + k * 32), ptx::sw128_kmajor_desc(q_addr + k * 32),
-                                     idesc, k > 0 ? 1u : 0u);
+                    ptx::umma_f8f6f4(d, ptx::sw128_kmajor_desc(a_addr + k * 32),
+                                     ptx::sw128_kmajor_desc(q_addr + k * 32), idesc, k > 0 ? 1u : 0u);
                 ptx::umma_commit(&empty[s]);
                 ptx::umma_commit(&tfull[a]);
-            }
-        }
-    } else {               // ---------------- warps 2..5: query prologue, then epilogue
-        {
-            // quantise the group's (row, head) vectors: warp pw takes vectors p = pw, pw + 4, ...;
-            // all loads of a batch are issued before any is used
-            const int pw = warp - 2;
-            constexpr int kPerWarp = R * kIndexHeads / 4;
-            constexpr int kBatch = 16;
-            for (int v0 = 0; v0 < kPerWarp; v0 += kBatch) {
-                uint2 raw[kBatch];
-                float wv[kBatch];
-#pragma unroll
-                for (int u = 0; u < kBatch; ++u) {
-                    const int p = pw + 4 * (v0 + u);
-                    const int jj = p / kIndexHeads, h = p % kIndexHeads;
-                    raw[u] = make_uint2(0u, 0u);
-                    wv[u] = 0.0f;
-                    if (jj < nrows) {
-                        const int64_t r = q0 + j0 + jj;
-                        raw[u] = __ldg(reinterpret_cast<const uint2*>(q + (r * kIndexHeads + h) * kIndexDim) + lane);
-                        wv[u] = __ldg(w + r * kIndexHeads + h);
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < kBatch; ++u) {
-                    const int p = pw + 4 * (v0 + u);   // = row_in_group * 64 + head = B-operand row
-                    const int jj = p / kIndexHeads;
-                    uint32_t packed = 0;
-                    float sq = 0.0f;
-                    if (jj < nrows) {
-                        float x[4] = {bf16_lo(raw[u].x), bf16_hi(raw[u].x), bf16_lo(raw[u].y), bf16_hi(raw[u].y)};
-                        packed = quantise_head(x, rotate != 0, lane, &sq);
-                    }
-                    const uint32_t off = p * 128 + ((((lane >> 2) ^ (p & 7))) << 4) + ((lane & 3) << 2);
-                    *reinterpret_cast<uint32_t*>(qtile + off) = packed;
-                    if (lane == 0) wq[p] = wv[u] * sq;
+                if (++s == S) { s = 0; ph ^= 1u; }
+                if (++sg.tile == sg.ntiles || i + 1 == count) {   // last tile of the segment here
+                    ptx::umma_commit(&qempty[qb]);
+                    ++n;
+                    seg_start = true;
+                    if (i + 1 < count) seg_next(sa, sg);
                 }
             }
-            ptx::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(q_ready);
         }
-        if (!ptx::mbar_wait(q_ready, 0, deadline)) timed_out = true;   // every warp's w' is visible
+    } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 8 && count > 0) {   // ---------------- epilogue
+        const int grp = (warp - kEpiWarp0) >> 2;          // takes the tiles i with i % 2 == grp
         const int quad = warp & 3;
         const int key_in_tile = quad * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        for (int i = 0; i < ntiles && !timed_out; ++i) {
-            const int s = i % S;
-            const uint32_t ph = (i / S) & 1;
-            const int a = i % NA;
-            const uint32_t aph = (i / NA) & 1;
-            if (!ptx::mbar_wait(&full[s], ph, deadline)) { timed_out = true; break; }
-            if (!ptx::mbar_wait(&tfull[a], aph, deadline)) { timed_out = true; break; }
-            ptx::tc_fence_after_sync();
-            const bool ok = page_ok[2 * s + (key_in_tile >> 6)] != 0;
-            const float ks = scales[s * kTileKeys + key_in_tile];
-            const int key = (t_begin + i) * kTileKeys + key_in_tile;
+        int s = 0, n = 0;
+        uint32_t ph = 0;
+        bool seg_start = true;
+        for (int i = 0; i < count; ++i) {
+            const int qb = n & 1;
+            if (seg_start && !ptx::mbar_wait(&qfull[qb], (n >> 1) & 1, deadline)) { timed_out = true; break; }
+            seg_start = false;
+            if ((i & 1) == grp) {
+                const int a = i % NA;
+                const uint32_t aph = (i / NA) & 1;
+                if (!ptx::mbar_wait(&full[s], ph, deadline)) { timed_out = true; break; }
+                if (!ptx::mbar_wait(&tfull[a], aph, deadline)) { timed_out = true; break; }
+                ptx::tc_fence_after_sync();
+                const bool ok = page_ok[2 * s + (key_in_tile >> 6)] != 0;
+                const float ks = scales[s * kTileKeys + key_in_tile];
+                const int key = sg.tile * kTileKeys + key_in_tile;
 #pragma unroll 1
-            for (int jj = 0; jj < nrows; ++jj) {   // one query row at a time: 64 accumulator columns
-                uint32_t r0[32], r1[32];
-                const uint32_t col = tmem + lane_base + static_cast<uint32_t>(a * N + jj * kIndexHeads);
-                ptx::tmem_ld_32x32b_x32(col, r0);
-                ptx::tmem_ld_32x32b_x32(col + 32, r1);
-                ptx::tmem_wait_ld();
-                const float* g = wq + jj * kIndexHeads;
-                float acc = 0.0f;
+                for (int jj = 0; jj < sg.nrows; ++jj) {   // one query row at a time: 64 accumulator columns
+                    uint32_t r0[32], r1[32];
+                    const uint32_t col = tmem + lane_base + static_cast<uint32_t>(a * N + jj * kIndexHeads);
+                    ptx::tmem_ld_32x32b_x32(col, r0);
+                    ptx::tmem_ld_32x32b_x32(col + 32, r1);
+                    ptx::tmem_wait_ld();
+                    const float* g = gates + (qb * R + jj) * kIndexHeads;
+                    float acc = 0.0f;
 #pragma unroll
-                for (int h = 0; h < 32; ++h) acc = fmaf(g[h], fmaxf(__uint_as_float(r0[h]), 0.0f), acc);
+                    for (int h = 0; h < 32; ++h) acc = fmaf(g[h], fmaxf(__uint_as_float(r0[h]), 0.0f), acc);
 #pragma unroll
-                for (int h = 0; h < 32; ++h) acc = fmaf(g[32 + h], fmaxf(__uint_as_float(r1[h]), 0.0f), acc);
-                const int r = q0 + j0 + jj;
-                const int v = visible_len(L, q_len, j0 + jj);
-                if (ok && key < v && key < ld && r >= row_begin && r < row_end)
-                    logits[static_cast<int64_t>(r - row_begin) * ld + key] = acc * ks;
+                    for (int h = 0; h < 32; ++h) acc = fmaf(g[32 + h], fmaxf(__uint_as_float(r1[h]), 0.0f), acc);
+                    const int r = sg.q0 + sg.j0 + jj;
+                    const int v = visible_len(sg.L, sg.q_len, sg.j0 + jj);
+                    if (ok && key < v && key < ld && r >= row_begin && r < row_end)
+                        logits[static_cast<int64_t>(r - row_begin) * ld + key] = acc * ks;
+                }
+                ptx::tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::mbar_arrive(&tempty[a]);
+                    ptx::mbar_arrive(&empty[s]);
+                }
             }
-            ptx::tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) {
-                ptx::mbar_arrive(&tempty[a]);
-                ptx::mbar_arrive(&empty[s]);
+            if (++s == S) { s = 0; ph ^= 1u; }
+            if (++sg.tile == sg.ntiles || i + 1 == count) {   // leaving the segment: its gates are free
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&qempty[qb]);
+                ++n;
+                seg_start = true;
+                if (i + 1 < count) seg_next(sa, sg);
             }
         }
     }
@@ -326,30 +486,40 @@ EncodeTiledFn tensor_map_encoder() {
 }  // namespace
 }  // namespace dsa
 
+extern "C" size_t dsa_indexer_logits_workspace_size(int32_t rows) {
+    using namespace dsa;
+    return rows <= 0 ? 0 : static_cast<size_t>(rows) * (kQRowBytes + kQGateBytes);
+}
+
 extern "C" dsa_status dsa_indexer_logits(const void* q_bf16, const float* weights, const uint8_t* index_k_pool,
                                          int64_t num_pages, const int32_t* block_table, int32_t max_pages,
                                          const int32_t* seq_lens, const int32_t* cu_q, int32_t B,
                                          int32_t max_seq_len, int32_t max_q_len, int32_t row_begin,
                                          int32_t row_end, float* logits, int64_t ld, uint32_t flags,
-                                         int32_t* dev_err, void* stream) {
+                                         void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream) {
     using namespace dsa;
     if (B < 0 || max_seq_len < 0 || max_q_len < 0 || row_begin < 0 || row_end < row_begin || max_pages < 0 ||
         num_pages < 0)
         return DSA_ERR_INVALID_ARG;
     if ((flags & ~DSA_Q_ROTATE) != 0u) return DSA_ERR_INVALID_ARG;
     if (B == 0 || row_end == row_begin || max_seq_len == 0 || max_q_len == 0) return DSA_OK;
-    if (!q_bf16 || !weights || !index_k_pool || !block_table || !seq_lens || !cu_q || !logits)
+    if (!q_bf16 || !weights || !index_k_pool || !block_table || !seq_lens || !cu_q || !logits || !workspace)
         return DSA_ERR_INVALID_ARG;
-    if (!aligned16(q_bf16) || !aligned16(index_k_pool)) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q_bf16) || !aligned16(index_k_pool) || !aligned16(workspace)) return DSA_ERR_INVALID_ARG;
+    if (ws_bytes < dsa_indexer_logits_workspace_size(row_end - row_begin)) return DSA_ERR_INVALID_ARG;
     if (ld < max_seq_len) return DSA_ERR_INVALID_ARG;
     if (static_cast<int64_t>(max_pages) * kPage < max_seq_len) return DSA_ERR_INVALID_ARG;
     const int R = max_q_len >= 4 ? 4 : (max_q_len >= 2 ? 2 : 1);
     const int groups = (max_q_len + R - 1) / R;
-    if (groups > 65535 || B > 65535) return DSA_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(groups) * B > 0x7fffffffLL - 1) return DSA_ERR_UNSUPPORTED;
     if (num_pages > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
-    const int tiles = (max_seq_len + kTileKeys - 1) / kTileKeys;
-    const int chunk_tiles = (R == 1) ? 8 : 16;
-    const int chunks = (tiles + chunk_tiles - 1) / chunk_tiles;
+    const int64_t tiles_per_seg = (max_seq_len + kTileKeys - 1) / kTileKeys;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        return DSA_ERR_CUDA;
+    const int64_t upper = tiles_per_seg * groups * B;   // bound on the tiles of all segments
+    const int ctas = static_cast<int>(upper < sms ? upper : sms);
 
     // tensor map over the code bytes of the page-blocked pool: (byte in row, row in page, page)
     static_assert(sizeof(CUtensorMap) == 128, "CUtensorMap size");
@@ -367,19 +537,40 @@ extern "C" dsa_status dsa_indexer_logits(const void* q_bf16, const float* weight
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return DSA_ERR_CUDA;
     }
-    dim3 grid(chunks, groups, B);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int rotate = (flags & DSA_Q_ROTATE) != 0u ? 1 : 0;
-    const uint16_t* qp = static_cast<const uint16_t*>(q_bf16);
+    const int rows = row_end - row_begin;
+    uint8_t* q_codes = static_cast<uint8_t*>(workspace);
+    float* q_gates = reinterpret_cast<float*>(q_codes + static_cast<size_t>(rows) * kQRowBytes);
+
+    // query prologue: 8 vectors per 256-thread block
+    indexer_q_prologue_kernel<<<static_cast<unsigned>(rows) * (kIndexHeads / 8), 256, 0, st>>>(
+        static_cast<const uint16_t*>(q_bf16), weights, cu_q, B, row_begin, row_end, rotate, q_codes, q_gates);
+    if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
+
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const uint8_t* qc = q_codes;
+    const float* qg = q_gates;
 #define DSA_LAUNCH_IDX(RR)                                                                                      \
     do {                                                                                                        \
         const size_t smem = IdxCfg<RR>::kSmemBytes;                                                             \
         if (cudaFuncSetAttribute(indexer_logits_umma_kernel<RR>, cudaFuncAttributeMaxDynamicSharedMemorySize,    \
                                  static_cast<int>(smem)) != cudaSuccess)                                        \
             return DSA_ERR_CUDA;                                                                                \
-        indexer_logits_umma_kernel<RR><<<grid, kUmmaThreads, smem, st>>>(                                       \
-            kmap, qp, weights, index_k_pool, num_pages, block_table, max_pages, seq_lens, cu_q, row_begin,      \
-            row_end, logits, ld, rotate, chunk_tiles, dev_err);                                                 \
+        cfg.dynamicSmemBytes = smem;                                                                            \
+        if (cudaLaunchKernelEx(&cfg, indexer_logits_umma_kernel<RR>, kmap, qc, qg, index_k_pool, num_pages,     \
+                               block_table, static_cast<int>(max_pages), seq_lens, cu_q, static_cast<int>(B),  \
+                               groups, static_cast<int>(row_begin), static_cast<int>(row_end), logits, ld,     \
+                               dev_err) != cudaSuccess)                                                         \
+            return DSA_ERR_CUDA;                                                                                \
     } while (0)
     if (R == 1) DSA_LAUNCH_IDX(1);
     else if (R == 2) DSA_LAUNCH_IDX(2);

@@ -14,6 +14,16 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Programmatic dependent launch: a grid launched with programmatic stream serialization may
+// start before the previous grid on its stream has finished.  The dependent grid calls
+// griddep_wait() before it touches anything that grid writes (the wait returns once that grid
+// has completed and its memory is visible; it is a no-op for a normally launched grid); the
+// previous grid calls griddep_launch_dependents() to let the dependent grid be scheduled.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));

@@ -59,6 +59,8 @@ class DeviceBatch:
         self.ld = logits_ld(wl.max_seq_len)
         self.logits = torch.empty((wl.T, self.ld), dtype=torch.float32, device=dev)
         self.idx = torch.empty((wl.T, wl.topk), dtype=torch.int32, device=dev)
+        self.idx_ws = torch.empty(max(16, capi.dsa_indexer_logits_workspace_size(wl.T)), dtype=torch.uint8,
+                                  device=dev)
         self.topk_ws = torch.empty(max(1, capi.dsa_topk_workspace_size(wl.T, wl.topk, wl.max_seq_len)),
                                    dtype=torch.uint8, device=dev)
         self.kv_pool = None
@@ -81,7 +83,7 @@ class DeviceBatch:
                                 self.block_table, self.seq_lens, self.cu_q, self.wl.max_seq_len,
                                 self.wl.max_q_len, self.logits if logits is None else logits,
                                 row_begin=row_begin, row_end=row_end, flags=flags, dev_err=self.dev_err,
-                                stream=stream)
+                                stream=stream, workspace=self.idx_ws)
 
     def topk(self, logits=None, idx=None, row_begin: int = 0, row_end: Optional[int] = None, stream=None):
         lg = self.logits if logits is None else logits

@@ -134,15 +134,23 @@ dsa_status dsa_store_index_k(const void* k_bf16, const int64_t* slot_mapping, in
  *   logits       fp32 [row_end - row_begin, ld]; row r goes to logits[(r - row_begin) * ld].
  *                Entries s >= v_r are left untouched.  ld >= max_seq_len.
  *   flags        0 or DSA_Q_ROTATE.
+ *   workspace    device scratch of at least dsa_indexer_logits_workspace_size(row_end - row_begin)
+ *                bytes, 16-byte aligned, owned by the caller.  It holds the quantised query rows
+ *                (the prologue runs once per row instead of once per key tile); its contents need
+ *                no initialisation and are dead after the call, but two calls in flight at the
+ *                same time must not share it.
  *   dev_err      nullable; DSA_DEVERR_PAGE_RANGE when a needed page id is out of range (those
  *                keys' logits are not written).
+ * Two kernels are enqueued on `stream`: the query prologue, then the logits kernel as its
+ * programmatic dependent (it may start before the prologue ends and waits for it on the device).
  */
+size_t dsa_indexer_logits_workspace_size(int32_t rows);
 dsa_status dsa_indexer_logits(const void* q_bf16, const float* weights, const uint8_t* index_k_pool,
                               int64_t num_pages, const int32_t* block_table, int32_t max_pages,
                               const int32_t* seq_lens, const int32_t* cu_q, int32_t B,
                               int32_t max_seq_len, int32_t max_q_len, int32_t row_begin,
                               int32_t row_end, float* logits, int64_t ld, uint32_t flags,
-                              int32_t* dev_err, void* stream);
+                              void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream);
 
 /*
  * dsa_topk -- per-row top-k of the indexer logits.

@@ -39,6 +39,10 @@ def test_status_strings_and_host_side_validation(lib):
     assert L.dsa_sparse_mla_decode(None, None, 0, None, 0, None, None, 1, None, 64, 1, 24, 0.1, None, None,
                                    None, 0, None, None) == 2                          # H = 24
     assert L.dsa_indexer_logits(None, None, None, 0, None, 0, None, None, 1, 10, 1, 0, 1, None, 10, 0x10,
-                                None, None) == 1                                      # unknown flag
+                                None, 0, None, None) == 1                             # unknown flag
+    assert L.dsa_indexer_logits(None, None, None, 0, None, 0, None, None, 1, 10, 1, 0, 1, None, 10, 0,
+                                None, 0, None, None) == 1                             # null pointers
+    assert L.dsa_indexer_logits_workspace_size(3) == 3 * (64 * 128 + 64 * 4)          # codes + gates per row
+    assert L.dsa_indexer_logits_workspace_size(0) == 0
     assert L.dsa_sparse_mla_workspace_size(64, 128, 2048) == 0     # one split per row: no scratch
     assert L.dsa_sparse_mla_workspace_size(16, 128, 2048) > 0      # few rows: split over k

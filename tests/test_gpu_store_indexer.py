@@ -97,6 +97,22 @@ def test_logits_prefill_chunk_causal_and_row_tiles():
     assert np.array_equal(part, full[37:101], equal_nan=True)
 
 
+def test_logits_mixed_query_counts_and_empty_requests():
+    # q_len 5 -> groups of 4 rows with a 1-row tail; a request without query rows; short contexts
+    wl = workloads.make_custom("mixed", 106, [500, 64, 900, 130, 7, 260], [3, 0, 5, 1, 2, 4], topk=64, heads=16)
+    _logits_case(wl)
+
+
+def test_logits_fewer_tiles_than_sms():
+    _logits_case(workloads.make_custom("few", 107, [5, 17, 3], 1, topk=64, heads=16))
+
+
+def test_logits_many_requests_shares_split_inside_requests():
+    # ~2900 key tiles over one CTA per SM: most CTAs start and end inside a request
+    lens = np.random.default_rng(108).integers(1, 6000, size=120).tolist()
+    _logits_case(workloads.make_custom("many", 108, lens, 1, topk=64, heads=16))
+
+
 def test_logits_rotate_q_flag():
     _logits_case(workloads.make("tiny"), flags=capi.DSA_Q_ROTATE)
 
@@ -123,4 +139,9 @@ def test_logits_invalid_args():
         narrow = torch.empty((wl.T, 10), dtype=torch.float32, device="cuda")   # ld = 10 < max_seq_len
         capi.dsa_indexer_logits(db.index_q, db.weights, db.index_pool, db.block_table, db.seq_lens, db.cu_q,
                                 wl.max_seq_len, 1, narrow)
+    assert e.value.status == capi.DSA_ERR_INVALID_ARG
+    with pytest.raises(capi.DSAError) as e:   # workspace one byte short
+        short = torch.empty(capi.dsa_indexer_logits_workspace_size(wl.T) - 1, dtype=torch.uint8, device="cuda")
+        capi.dsa_indexer_logits(db.index_q, db.weights, db.index_pool, db.block_table, db.seq_lens, db.cu_q,
+                                wl.max_seq_len, 1, db.logits, workspace=short)
     assert e.value.status == capi.DSA_ERR_INVALID_ARG
