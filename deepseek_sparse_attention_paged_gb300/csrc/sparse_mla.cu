@@ -9,9 +9,12 @@
 // Work split.  CTA = (query row r, split j of the k selected entries, half h of the 512 output
 // dims); the two halves of a (row, split) form a cluster of 2 CTAs.  Tensor memory holds 512 fp32
 // columns per SM, exactly one 128-head x 512-dim output, so each CTA keeps only its 256 output
-// dims next to the score tile and computes the full score tile itself; the latent rows of each tile
-// are gathered once per cluster: each CTA gathers half of the tile's rows by TMA with cluster
-// multicast, which writes them into both CTAs' shared memory.
+// dims next to the score tile and computes the full score tile itself.  The latent rows of each tile
+// are read from global memory once per cluster: CTA 0 gathers dims 0..319 (chunks 0-4) and CTA 1
+// dims 320..575 (chunks 5-8) of every selected row with 16-byte cp.async copies straight into the
+// swizzled operand layout, and each then forwards its part to the other CTA's shared memory with
+// one bulk shared-to-shared copy.  (Per-row TMA copies cost a roughly fixed time each, which caps a
+// gather of random 1152-byte rows well below the HBM rate; the load/store units do not.)
 //
 // Tensor memory (512 columns x 128 lanes, lane = head):
 //   [0, 256)   O, this CTA's 256 output dims (fp32)
@@ -27,10 +30,11 @@
 //   warp 4 (MMA):  S = Q K^T  (M = 128 heads, N = 64 keys, K = 576) and O += P V_h (M = 128,
 //           N = 256 dims, K = 64 keys), bf16 in, fp32 accumulate in TMEM; the completion of PV(t)
 //           is signalled to both CTAs of the cluster (the stage is free only when both are done);
-//   warps 5-6 (producers): warp 5 + w resolves entries 32 w .. 32 w + 31 of each tile to latent
-//           rows two batches ahead (independent loads), and, in the CTA of cluster rank w, gathers
-//           those rows with TMA tile::gather4 multicast to both CTAs (padding / invalid entries
-//           gather row 0 and get probability 0).
+//   warps 5-8 (producers): warp 5 + w resolves entries 16 w .. 16 w + 15 of each tile to latent
+//           rows two batches ahead (independent loads) and copies this CTA's chunks of those rows
+//           (padding / invalid entries read row 0 and get probability 0);
+//   warp 9 (exchange): once this CTA's chunks of a tile have landed, copies them into the peer's
+//           stage and accounts for the peer's chunks arriving here.
 // Score MMAs are issued with N = 64: on this tensor core an M = 128, K = 16 MMA takes the same time
 // for N = 32 and N = 64, so wider key tiles halve the score cost per key.
 // With one split the CTA writes bf16 output directly; with several, normalised fp32 partials and
@@ -58,9 +62,11 @@ constexpr int kPBytes = kHeadsPerCta * kKeysPerTile * 2;        // 16384
 constexpr int kSoftmaxWarps = 4;
 constexpr int kMmaWarp = 4;
 constexpr int kProducerWarp0 = 5;
-constexpr int kProducerWarps = 2;
-constexpr int kMlaThreads = 32 * (kProducerWarp0 + kProducerWarps);   // 224
-constexpr int kKeysPerProducer = kKeysPerTile / kProducerWarps;       // 32
+constexpr int kProducerWarps = 4;
+constexpr int kXchgWarp = kProducerWarp0 + kProducerWarps;              // 9
+constexpr int kMlaThreads = 32 * (kXchgWarp + 1);                       // 320
+constexpr int kKeysPerProducer = kKeysPerTile / kProducerWarps;         // 16
+constexpr int kRank0Chunks = 5;                                         // chunks 0-4 by rank 0, 5-8 by rank 1
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = kHalfDims;                          // S at columns 256 .. 319
 constexpr uint32_t kTmemQ = kTmemS + kKeysPerTile;              // query at columns 320 .. 511
@@ -94,19 +100,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
-// Four rows (arbitrary row coordinates) x one 128-byte box, written to consecutive 128-byte rows
-// at the same shared-memory offset of every CTA in cta_mask; completion counted on the mbarrier at
-// the same offset in each of them.
-__device__ __forceinline__ void tma_gather4_mc(void* dst, const CUtensorMap* map, uint64_t* bar, int col, int r0,
-                                               int r1, int r2, int r3, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(ptx::smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(ptx::smem_addr(bar)), "r"(col), "r"(r0), "r"(r1), "r"(r2),
-        "r"(r3), "h"(cta_mask)
-        : "memory");
-}
-
 // Arrive once on the mbarrier at this offset in every CTA of cta_mask when all previously issued
 // tcgen05.mma of this thread have completed.
 __device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
@@ -115,6 +108,32 @@ __device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t cta_mask)
             ptx::smem_addr(bar)),
         "h"(cta_mask)
         : "memory");
+}
+
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Arrive on `bar` (without raising its expected count) once all cp.async of this thread so far landed.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(ptx::smem_addr(bar)) : "memory");
+}
+
+// Shared::cluster address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+    return r;
+}
+
+// Bulk copy of `bytes` from this CTA's shared memory into another CTA's (cluster address), counted
+// as transaction bytes on the mbarrier at `bar_cluster` in that CTA.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
+                                                  uint32_t bar_cluster) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst_cluster),
+                 "r"(src), "r"(bytes), "r"(bar_cluster)
+                 : "memory");
 }
 
 __device__ __forceinline__ void cluster_sync_all() {
@@ -159,7 +178,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 struct MlaBars {
     uint64_t q_full;               // smem query chunks (TMA) + TMEM query chunks (4 warps)
-    uint64_t kv_full[kKvStages];   // one arrive per producer warp, after its copies landed
+    uint64_t kv_local[kKvStages];  // this CTA's chunks of the tile landed (+ the valid bits)
+    uint64_t kv_full[kKvStages];   // all 9 chunks present: exchange warp's arrive + the peer's bytes
     uint64_t kv_empty[kKvStages];
     uint64_t s_full;
     uint64_t s_empty;
@@ -168,11 +188,11 @@ struct MlaBars {
     uint64_t o_full;
     uint32_t tmem_slot;
     uint32_t pad;
-    uint32_t valid[kKvStages][kProducerWarps];   // bit i: entry 32 w + i of the stage's tile is real
+    uint32_t valid[kKvStages][kProducerWarps];   // bit i: entry 16 w + i of the stage's tile is real
 };
 
 __global__ void __launch_bounds__(kMlaThreads, 1)
-sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kvmap,
+sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const uint16_t* __restrict__ kv,
                        const uint16_t* __restrict__ q, int64_t num_pages, const int32_t* __restrict__ block_table,
                        int max_pages, const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q, int B,
                        const int32_t* __restrict__ idx, int k, int H, float scale, int splits,
@@ -201,8 +221,10 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
     if (threadIdx.x == 0) {
         ptx::mbar_init(&bar.q_full, 1 + kSoftmaxWarps);
         for (int s = 0; s < kKvStages; ++s) {
-            // one arrival per producer warp (the issuing one with the tile's byte count)
-            ptx::mbar_init(&bar.kv_full[s], kProducerWarps);
+            // every producer thread's cp.async completion + one arrive per producer warp (valid bits)
+            ptx::mbar_init(&bar.kv_local[s], kProducerWarps * 32 + kProducerWarps);
+            // the exchange warp's arrive (this CTA's chunks landed) + the peer's chunks as bytes
+            ptx::mbar_init(&bar.kv_full[s], 1);
             // PV completion of this CTA and of its cluster peer
             ptx::mbar_init(&bar.kv_empty[s], 2);
         }
@@ -235,7 +257,10 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
     const uint64_t deadline = ptx::wait_deadline();
     bool timed_out = false;
 
-    if (warp >= kProducerWarp0) {
+    const int c_lo = crank == 0 ? 0 : kRank0Chunks;                // this CTA's chunks [c_lo, c_hi)
+    const int c_hi = crank == 0 ? kRank0Chunks : kChunks;
+    const uint32_t kv_addr0 = ptx::smem_addr(kvs);
+    if (warp >= kProducerWarp0 && warp < kXchgWarp) {
         // ---------------------------------------------------------------- producers
         const int pw = warp - kProducerWarp0;
         if (pw == 0 && lane == 0) {
@@ -243,13 +268,14 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
             for (int c = 0; c < kSmemQChunks; ++c)
                 tma_load_2d(qs + c * kQChunkBytes, &qmap, &bar.q_full, (kTmemQChunks + c) * 64, r * H);
         }
-        // lane l owns entry 32 pw + l of every tile.  Batches of kBatch tiles: positions are loaded two
-        // batches ahead and page ids one batch ahead, so no load waits on another on the critical path.
+        // lane l < 16 owns entry 16 pw + l of every tile.  Batches of kBatch tiles: positions are
+        // loaded two batches ahead and page ids one batch ahead, so no load waits on another on the
+        // critical path.
         const int my_entry = pw * kKeysPerProducer + lane;
-        const bool issuer = static_cast<uint32_t>(pw) == crank;   // this CTA gathers these entries
         auto load_pos = [&](int tile) -> int {
             const int e = e_begin + tile * kKeysPerTile + my_entry;
-            return (tile < ntiles && e < e_end) ? __ldg(idx + static_cast<int64_t>(r) * k + e) : -1;
+            return (lane < kKeysPerProducer && tile < ntiles && e < e_end) ? __ldg(idx + static_cast<int64_t>(r) * k + e)
+                                                                          : -1;
         };
         auto pos_ok = [&](int pos) -> bool { return pos >= 0 && pos < v && (pos >> 6) < max_pages; };
         auto load_page = [&](int pos) -> int {
@@ -268,6 +294,8 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         for (int u = 0; u < kBatch; ++u) page1[u] = load_page(pos1[u]);
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) pos2[u] = load_pos(kBatch + u);
+        // copy lane layout: lane = 8 * (key % 4) + 16-byte piece of a 128-byte chunk row
+        const int piece = lane & 7;
         for (int t0 = 0; t0 < ntiles && !timed_out; t0 += kBatch) {
             int rows[kBatch];
 #pragma unroll
@@ -285,29 +313,29 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
                 if (t >= ntiles) break;
                 const int s = t % kKvStages;
                 const uint32_t ph = (t / kKvStages) & 1;
-                const uint32_t vbits = __ballot_sync(0xffffffffu, rows[u] >= 0);
+                const uint32_t vbits = __ballot_sync(0xffffffffu, rows[u] >= 0) & 0xffffu;
                 const int row_src = rows[u] >= 0 ? rows[u] : 0;
                 // the stage is free once PV of its previous tile finished in both CTAs
                 if (lane == 0 && !ptx::mbar_wait(&bar.kv_empty[s], ph ^ 1u, deadline)) timed_out = true;
                 timed_out = __shfl_sync(0xffffffffu, timed_out ? 1 : 0, 0) != 0;
                 if (timed_out) break;
+                int rk[kKeysPerProducer / 4];
+#pragma unroll
+                for (int kq = 0; kq < kKeysPerProducer / 4; ++kq) rk[kq] = __shfl_sync(0xffffffffu, row_src, kq * 4 + (lane >> 3));
+                const uint32_t stage = kv_addr0 + s * kKvStageBytes;
+#pragma unroll 1
+                for (int c = c_lo; c < c_hi; ++c) {
+#pragma unroll
+                    for (int kq = 0; kq < kKeysPerProducer / 4; ++kq) {
+                        const int key = pw * kKeysPerProducer + kq * 4 + (lane >> 3);
+                        const uint32_t dst = stage + c * kKvChunkBytes + key * 128 + ((piece ^ (key & 7)) << 4);
+                        cp_async_16(dst, kv + static_cast<int64_t>(rk[kq]) * kLatentDim + c * 64 + piece * 8);
+                    }
+                }
+                cp_async_arrive_noinc(&bar.kv_local[s]);
                 if (lane == 0) {
                     bar.valid[s][pw] = vbits;
-                    if (issuer) ptx::mbar_arrive_expect_tx(&bar.kv_full[s], kKvStageBytes);   // both halves
-                    else ptx::mbar_arrive(&bar.kv_full[s]);
-                }
-                __syncwarp();
-                if (issuer) {
-                    int rr[4];
-#pragma unroll
-                    for (int w = 0; w < 4; ++w) rr[w] = __shfl_sync(0xffffffffu, row_src, (4 * (lane & 7) + w) & 31);
-                    if (lane < kKeysPerProducer / 4) {   // 8 groups of 4 keys, 9 chunks each
-                        unsigned char* dst = kvs + s * kKvStageBytes + (pw * kKeysPerProducer + lane * 4) * 128;
-#pragma unroll 1
-                        for (int c = 0; c < kChunks; ++c)
-                            tma_gather4_mc(dst + c * kKvChunkBytes, &kvmap, &bar.kv_full[s], c * 64, rr[0], rr[1], rr[2],
-                                           rr[3], static_cast<uint16_t>(0x3));
-                    }
+                    ptx::mbar_arrive(&bar.kv_local[s]);
                 }
             }
         }
@@ -315,6 +343,23 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
         if (pw == 0 && lane == 0 && !timed_out) {
             for (int t = (ntiles > kKvStages ? ntiles - kKvStages : 0); t < ntiles; ++t)
                 if (!ptx::mbar_wait(&bar.kv_empty[t % kKvStages], (t / kKvStages) & 1, deadline)) timed_out = true;
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+    } else if (warp == kXchgWarp) {
+        // ---------------------------------------------------------------- exchange with the peer
+        if (lane == 0) {
+            const uint32_t peer = crank ^ 1u;
+            const uint32_t my_bytes = static_cast<uint32_t>(c_hi - c_lo) * kKvChunkBytes;
+            const uint32_t peer_bytes = static_cast<uint32_t>(kChunks - (c_hi - c_lo)) * kKvChunkBytes;
+            for (int t = 0; t < ntiles; ++t) {
+                const int s = t % kKvStages;
+                if (!ptx::mbar_wait(&bar.kv_local[s], (t / kKvStages) & 1, deadline)) { timed_out = true; break; }
+                ptx::fence_proxy_async_smem();   // the cp.async data is read by the bulk copy (async proxy)
+                const uint32_t src = kv_addr0 + s * kKvStageBytes + c_lo * kKvChunkBytes;
+                bulk_copy_to_peer(map_to_rank(src, peer), src, my_bytes,
+                                  map_to_rank(ptx::smem_addr(&bar.kv_full[s]), peer));
+                ptx::mbar_arrive_expect_tx(&bar.kv_full[s], peer_bytes);
+            }
         }
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issuer
@@ -328,6 +373,7 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
                 const int s = t % kKvStages;
                 if (!ptx::mbar_wait(&bar.kv_full[s], (t / kKvStages) & 1, deadline)) return false;
                 if (!ptx::mbar_wait(&bar.s_empty, (t & 1) ^ 1u, deadline)) return false;
+                ptx::fence_proxy_async_smem();   // chunks written by cp.async, read by the tensor cores
                 ptx::tc_fence_after_sync();
                 const uint32_t d = tmem + kTmemS;
                 const uint32_t kb = kv_addr + s * kKvStageBytes;
@@ -421,7 +467,9 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_co
             ptx::tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&bar.s_empty);
-            const uint64_t vbits = static_cast<uint64_t>(bar.valid[s][0]) | (static_cast<uint64_t>(bar.valid[s][1]) << 32);
+            const uint64_t vbits = static_cast<uint64_t>(bar.valid[s][0]) | (static_cast<uint64_t>(bar.valid[s][1]) << 16) |
+                                   (static_cast<uint64_t>(bar.valid[s][2]) << 32) |
+                                   (static_cast<uint64_t>(bar.valid[s][3]) << 48);
             float tmax = -INFINITY;
 #pragma unroll
             for (int i = 0; i < 64; ++i) {
@@ -639,9 +687,8 @@ extern "C" dsa_status dsa_sparse_mla_decode(const void* q_bf16, const void* kv_p
     const int splits = mla_splits(T, k);
     float* part_o = static_cast<float*>(workspace);
     float* part_lse = splits > 1 ? part_o + static_cast<size_t>(T) * H * splits * kValueDim : nullptr;
-    CUtensorMap qmap, kvmap;
+    CUtensorMap qmap;
     if (!encode_rows_576(&qmap, q_bf16, static_cast<uint64_t>(T) * H, static_cast<uint32_t>(H))) return DSA_ERR_CUDA;
-    if (!encode_rows_576(&kvmap, kv_pool, static_cast<uint64_t>(num_pages) * kPage, 1)) return DSA_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaFuncSetAttribute(sparse_mla_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kMlaSmemBytes)) != cudaSuccess)
@@ -658,7 +705,8 @@ extern "C" dsa_status dsa_sparse_mla_decode(const void* q_bf16, const void* kv_p
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, sparse_mla_umma_kernel, qmap, kvmap, static_cast<const uint16_t*>(q_bf16), num_pages,
+    if (cudaLaunchKernelEx(&cfg, sparse_mla_umma_kernel, qmap, static_cast<const uint16_t*>(kv_pool),
+                           static_cast<const uint16_t*>(q_bf16), num_pages,
                            block_table, max_pages, seq_lens, cu_q, B, idx, k, H, scale, splits,
                            static_cast<uint16_t*>(out_bf16), lse, part_o, part_lse, dev_err) != cudaSuccess)
         return DSA_ERR_CUDA;
