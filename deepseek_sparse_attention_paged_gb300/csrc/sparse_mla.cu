@@ -6,35 +6,35 @@
 // MLACommonImpl.forward decode branch (absorbed 576-wide query, one shared KV head; _forward_decode
 // returns (out, lse); merge_attn_states merges partial results by their log-sum-exp).
 //
-// Work split.  CTA = (query row r, split j of the k selected entries, half h of the 512 output
-// dims); the two halves of a (row, split) form a cluster of 2 CTAs.  Tensor memory holds 512 fp32
-// columns per SM, exactly one 128-head x 512-dim output, so each CTA keeps only its 256 output
-// dims next to the score tile and computes the full score tile itself.  The latent rows of each tile
-// are read from global memory once per cluster: CTA 0 gathers dims 0..319 (chunks 0-4) and CTA 1
-// dims 320..575 (chunks 5-8) of every selected row with 16-byte cp.async copies straight into the
-// swizzled operand layout, and each then forwards its part to the other CTA's shared memory with
-// one bulk shared-to-shared copy.  (Per-row TMA copies cost a roughly fixed time each, which caps a
-// gather of random 1152-byte rows well below the HBM rate; the load/store units do not.)
+// Work split.  CTA = (query row r, split j of the k selected entries, rank h of a 2-CTA cluster).
+// The 576 latent dims are cut into 9 chunks of 64; rank 0 owns chunks 0-3 and 8 (value dims
+// 0..255 and the 64 rope dims), rank 1 owns chunks 4-7 (value dims 256..511).  Each CTA reads only
+// its own chunks of every selected row (16-byte cp.async straight into the swizzled operand
+// layout), keeps only its own query chunks (in tensor memory), computes the partial score tile
+// over its dims, and the two CTAs swap partial score tiles through distributed shared memory; both
+// then hold the full scores, run the same softmax (identical P: the fp32 sum is commutative) and
+// each accumulates its 256 output dims from its own value chunks.  Nothing of a latent row is read
+// twice or copied between the CTAs, and their key stages are private, so each CTA runs a 4-deep
+// load pipeline of its own.
 //
 // Tensor memory (512 columns x 128 lanes, lane = head):
 //   [0, 256)   O, this CTA's 256 output dims (fp32)
-//   [256, 320) score tile S of 64 keys (fp32)
-//   [320, 512) query dims 0..383, the A operand of the score MMA (two bf16 per column)
-// Shared memory: query dims 384..575 (3 chunks of 64 dims, 128-byte swizzle, by TMA); 2 stages of
-// 64 gathered latent rows (9 chunks x 64 rows x 128 B, 128-byte swizzle); 2 buffers of P (bf16).
+//   [256, 320) partial score tile of 64 keys (fp32)
+//   [320, 480) this CTA's query chunks, the A operand of the score MMA (two bf16 per column)
+// Shared memory: 4 stages of 64 rows x this CTA's chunks (128-byte swizzle, K-major; the first 4
+// chunks double as the MN-major value operand); the peer's partial scores (32 KB); 2 buffers of P.
 //
-// Roles (224 threads), for tiles of 64 selected entries:
-//   warps 0-3 (thread = head = TMEM lane): query dims 0..383 into TMEM; online softmax in the log2
-//           domain with lazy rescaling (O and l are rescaled only when the running max grows by
-//           more than 8, so p <= 2^8 otherwise); P to shared memory as bf16; O / l and lse at the end;
-//   warp 4 (MMA):  S = Q K^T  (M = 128 heads, N = 64 keys, K = 576) and O += P V_h (M = 128,
-//           N = 256 dims, K = 64 keys), bf16 in, fp32 accumulate in TMEM; the completion of PV(t)
-//           is signalled to both CTAs of the cluster (the stage is free only when both are done);
+// Roles (288 threads), for tiles of 64 selected entries:
+//   warps 0-3 (thread = head = TMEM lane): query chunks into TMEM; per tile: read the partial
+//           scores, send them to the peer, add the peer's, online softmax in the log2 domain with
+//           lazy rescaling (O and l are rescaled only when the running max grows by more than 8,
+//           so p <= 2^8 otherwise), P to shared memory as bf16; O / l and lse at the end;
+//   warp 4 (MMA):  S_h = Q_h K_h^T (M = 128 heads, N = 64 keys, K = 320 or 256) and O += P V_h
+//           (M = 128, N = 256 dims, K = 64 keys), bf16 in, fp32 accumulate in TMEM; issues
+//           whichever of the next score MMA and the next PV is ready first;
 //   warps 5-8 (producers): warp 5 + w resolves entries 16 w .. 16 w + 15 of each tile to latent
 //           rows two batches ahead (independent loads) and copies this CTA's chunks of those rows
-//           (padding / invalid entries read row 0 and get probability 0);
-//   warp 9 (exchange): once this CTA's chunks of a tile have landed, copies them into the peer's
-//           stage and accounts for the peer's chunks arriving here.
+//           (padding / invalid entries read row 0 and get probability 0).
 // Score MMAs are issued with N = 64: on this tensor core an M = 128, K = 16 MMA takes the same time
 // for N = 32 and N = 64, so wider key tiles halve the score cost per key.
 // With one split the CTA writes bf16 output directly; with several, normalised fp32 partials and
@@ -50,34 +50,36 @@ namespace {
 constexpr int kHeadsPerCta = 128;                 // M of both MMAs (fewer heads: rows unused)
 constexpr int kKeysPerTile = 64;
 constexpr int kChunks = kLatentDim / 64;          // 9 chunks of 64 dims (128 bytes)
-constexpr int kTmemQChunks = 6;                   // query chunks 0..5 live in tensor memory
-constexpr int kSmemQChunks = kChunks - kTmemQChunks;
+constexpr int kMaxOwnChunks = 5;                  // rank 0: chunks 0-3 and 8; rank 1: chunks 4-7
 constexpr int kHalfDims = kValueDim / 2;          // 256 output dims per CTA
-constexpr int kQChunkBytes = kHeadsPerCta * 128;                // 16384
-constexpr int kQSmemBytes = kSmemQChunks * kQChunkBytes;        // 49152
 constexpr int kKvChunkBytes = kKeysPerTile * 128;               // 8192
-constexpr int kKvStageBytes = kChunks * kKvChunkBytes;          // 73728
-constexpr int kKvStages = 2;
+constexpr int kKvStageBytes = kMaxOwnChunks * kKvChunkBytes;    // 40960
+constexpr int kKvStages = 4;
+constexpr int kXBytes = kHeadsPerCta * kKeysPerTile * 4;        // 32768: the peer's partial scores
 constexpr int kPBytes = kHeadsPerCta * kKeysPerTile * 2;        // 16384
 constexpr int kSoftmaxWarps = 4;
+constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
 constexpr int kMmaWarp = 4;
 constexpr int kProducerWarp0 = 5;
 constexpr int kProducerWarps = 4;
-constexpr int kXchgWarp = kProducerWarp0 + kProducerWarps;              // 9
-constexpr int kMlaThreads = 32 * (kXchgWarp + 1);                       // 320
-constexpr int kKeysPerProducer = kKeysPerTile / kProducerWarps;         // 16
-constexpr int kRank0Chunks = 5;                                         // chunks 0-4 by rank 0, 5-8 by rank 1
+constexpr int kMlaThreads = 32 * (kProducerWarp0 + kProducerWarps);   // 288
+constexpr int kKeysPerProducer = kKeysPerTile / kProducerWarps;       // 16
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = kHalfDims;                          // S at columns 256 .. 319
-constexpr uint32_t kTmemQ = kTmemS + kKeysPerTile;              // query at columns 320 .. 511
+constexpr uint32_t kTmemS = kHalfDims;                          // partial scores at columns 256 .. 319
+constexpr uint32_t kTmemQ = kTmemS + kKeysPerTile;              // query chunks at columns 320 .. 479
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;                       // log2 units
 constexpr int kBatch = 4;                                       // tiles resolved per batch
-constexpr size_t kMlaSmemBytes =
-    1024 + kQSmemBytes + size_t(kKvStages) * kKvStageBytes + 2 * kPBytes + 256;
+constexpr size_t kMlaSmemBytes = 1024 + size_t(kKvStages) * kKvStageBytes + kXBytes + 2 * kPBytes + 512;
 
-static_assert(kTmemQ + kTmemQChunks * 32 == kTmemCols, "tensor-memory budget");
+static_assert(kChunks == 9 && kMaxOwnChunks + 4 == kChunks, "chunk ownership: 5 + 4");
+static_assert(kTmemQ + kMaxOwnChunks * 32 <= kTmemCols, "tensor-memory budget");
 static_assert(kMlaSmemBytes <= 232448, "shared-memory budget");
+
+// Global chunk index of this CTA's local chunk j.
+__device__ __forceinline__ int own_chunk(uint32_t rank, int j) {
+    return rank == 0 ? (j < 4 ? j : 8) : 4 + j;
+}
 
 // Shared-memory matrix descriptor (sm_100 format): start, leading / stride byte offsets, layout.
 __device__ __forceinline__ uint64_t make_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
@@ -91,24 +93,6 @@ __device__ __forceinline__ uint64_t make_desc(uint32_t addr, uint32_t lbo, uint3
 }
 constexpr uint32_t kLayoutNone = 0;
 constexpr uint32_t kLayoutSw128 = 2;
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(ptx::smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(ptx::smem_addr(bar)), "r"(c0), "r"(c1)
-        : "memory");
-}
-
-// Arrive once on the mbarrier at this offset in every CTA of cta_mask when all previously issued
-// tcgen05.mma of this thread have completed.
-__device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            ptx::smem_addr(bar)),
-        "h"(cta_mask)
-        : "memory");
-}
 
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -126,14 +110,30 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t ran
     return r;
 }
 
-// Bulk copy of `bytes` from this CTA's shared memory into another CTA's (cluster address), counted
-// as transaction bytes on the mbarrier at `bar_cluster` in that CTA.
-__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
-                                                  uint32_t bar_cluster) {
-    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     dst_cluster),
-                 "r"(src), "r"(bytes), "r"(bar_cluster)
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                  : "memory");
+}
+
+// Arrive (release at cluster scope) on an mbarrier of another CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
+// Bounded wait with acquire at cluster scope (for phases completed by the peer CTA).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint64_t deadline) {
+    while (true) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(ptx::smem_addr(bar)), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if (static_cast<uint64_t>(clock64()) > deadline) return false;
+    }
 }
 
 __device__ __forceinline__ void cluster_sync_all() {
@@ -144,6 +144,13 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
     return r;
+}
+
+// 2^x on the special-function unit (PTX ex2.approx; relative error about 2^-22, ample for P in bf16).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // D[tmem] (+)= A[tmem] x B[smem]^T, bf16 operands, fp32 accumulate (one thread issues).
@@ -177,12 +184,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 struct MlaBars {
-    uint64_t q_full;               // smem query chunks (TMA) + TMEM query chunks (4 warps)
-    uint64_t kv_local[kKvStages];  // this CTA's chunks of the tile landed (+ the valid bits)
-    uint64_t kv_full[kKvStages];   // all 9 chunks present: exchange warp's arrive + the peer's bytes
-    uint64_t kv_empty[kKvStages];
-    uint64_t s_full;
-    uint64_t s_empty;
+    uint64_t q_full;               // query chunks in TMEM (4 softmax warps)
+    uint64_t kv_full[kKvStages];   // every producer thread's cp.async landed + one arrive per producer warp
+    uint64_t kv_empty[kKvStages];  // PV of the stage's tile completed
+    uint64_t s_full;               // partial score MMAs completed
+    uint64_t s_empty;              // partial scores read out of TMEM
+    uint64_t x_full;               // the peer's partial scores are in x (128 peer threads)
+    uint64_t x_empty;              // the peer has read the scores this CTA sent it (128 peer threads)
     uint64_t p_full[2];
     uint64_t p_empty[2];
     uint64_t o_full;
@@ -190,23 +198,22 @@ struct MlaBars {
     uint32_t pad;
     uint32_t valid[kKvStages][kProducerWarps];   // bit i: entry 16 w + i of the stage's tile is real
 };
+static_assert(sizeof(MlaBars) <= 512, "barrier block");
 
 __global__ void __launch_bounds__(kMlaThreads, 1)
-sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const uint16_t* __restrict__ kv,
-                       const uint16_t* __restrict__ q, int64_t num_pages, const int32_t* __restrict__ block_table,
-                       int max_pages, const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q, int B,
-                       const int32_t* __restrict__ idx, int k, int H, float scale, int splits,
-                       uint16_t* __restrict__ out, float* __restrict__ lse_out, float* __restrict__ part_o,
-                       float* __restrict__ part_lse, int32_t* err) {
+sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restrict__ q, int64_t num_pages,
+                       const int32_t* __restrict__ block_table, int max_pages, const int32_t* __restrict__ seq_lens,
+                       const int32_t* __restrict__ cu_q, int B, const int32_t* __restrict__ idx, int k, int H,
+                       float scale, int splits, uint16_t* __restrict__ out, float* __restrict__ lse_out,
+                       float* __restrict__ part_o, float* __restrict__ part_lse, int32_t* err) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw_addr = ptx::smem_addr(smem_raw);
     unsigned char* base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-    unsigned char* qs = base;                                   // [3][128 heads][128 B], SW128
-    unsigned char* kvs = qs + kQSmemBytes;                      // [2][9][64 keys][128 B], SW128
-    unsigned char* ps = kvs + kKvStages * kKvStageBytes;        // [2][16 head groups][8 key groups][8][16 B]
+    unsigned char* kvs = base;                                  // [4][5 chunks][64 keys][128 B], SW128
+    float* xs = reinterpret_cast<float*>(kvs + kKvStages * kKvStageBytes);   // [16 key quads][128 heads][4]
+    unsigned char* ps = reinterpret_cast<unsigned char*>(xs) + kXBytes;     // [2][16 head groups][8 key groups][8][16 B]
     MlaBars& bar = *reinterpret_cast<MlaBars*>(ps + 2 * kPBytes);
 
-    const int half = blockIdx.x;
     const int split = blockIdx.y;
     const int r = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -217,19 +224,21 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const uint16_t*
     const int e_begin = split * per_split;
     const int e_end = min(k, e_begin + per_split);
     const int ntiles = e_end > e_begin ? (e_end - e_begin + kKeysPerTile - 1) / kKeysPerTile : 0;
+    const uint32_t crank = cluster_ctarank();
+    const uint32_t peer = crank ^ 1u;
+    const int nown = crank == 0 ? kMaxOwnChunks : kMaxOwnChunks - 1;   // own chunks: 5 or 4
+    const int half = static_cast<int>(crank);                          // output dims 256 half ..
 
     if (threadIdx.x == 0) {
-        ptx::mbar_init(&bar.q_full, 1 + kSoftmaxWarps);
+        ptx::mbar_init(&bar.q_full, kSoftmaxWarps);
         for (int s = 0; s < kKvStages; ++s) {
-            // every producer thread's cp.async completion + one arrive per producer warp (valid bits)
-            ptx::mbar_init(&bar.kv_local[s], kProducerWarps * 32 + kProducerWarps);
-            // the exchange warp's arrive (this CTA's chunks landed) + the peer's chunks as bytes
-            ptx::mbar_init(&bar.kv_full[s], 1);
-            // PV completion of this CTA and of its cluster peer
-            ptx::mbar_init(&bar.kv_empty[s], 2);
+            ptx::mbar_init(&bar.kv_full[s], kProducerWarps * 32 + kProducerWarps);
+            ptx::mbar_init(&bar.kv_empty[s], 1);
         }
         ptx::mbar_init(&bar.s_full, 1);
         ptx::mbar_init(&bar.s_empty, kSoftmaxWarps);
+        ptx::mbar_init(&bar.x_full, kSoftmaxThreads);
+        ptx::mbar_init(&bar.x_empty, kSoftmaxThreads);
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(&bar.p_full[a], kSoftmaxWarps);
             ptx::mbar_init(&bar.p_empty[a], 1);
@@ -241,33 +250,17 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const uint16_t*
         ptx::tmem_alloc(&bar.tmem_slot, kTmemCols);
         ptx::tmem_relinquish();
     }
-    if (H < kHeadsPerCta) {   // smem query rows of heads that do not exist: zeros (never written out)
-        for (int i = threadIdx.x; i < kSmemQChunks * (kHeadsPerCta - H) * 8; i += kMlaThreads) {
-            const int c = i / ((kHeadsPerCta - H) * 8), rem = i % ((kHeadsPerCta - H) * 8);
-            *reinterpret_cast<uint4*>(qs + c * kQChunkBytes + (H + rem / 8) * 128 + (rem % 8) * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
-        }
-        ptx::fence_proxy_async_smem();
-    }
     ptx::tc_fence_before_sync();
-    cluster_sync_all();   // both CTAs' barriers exist before any multicast reaches them
+    cluster_sync_all();   // both CTAs' barriers exist before the peer signals or writes into them
     ptx::tc_fence_after_sync();
     const uint32_t tmem = bar.tmem_slot;
-    const uint32_t crank = cluster_ctarank();
     const uint64_t deadline = ptx::wait_deadline();
     bool timed_out = false;
-
-    const int c_lo = crank == 0 ? 0 : kRank0Chunks;                // this CTA's chunks [c_lo, c_hi)
-    const int c_hi = crank == 0 ? kRank0Chunks : kChunks;
     const uint32_t kv_addr0 = ptx::smem_addr(kvs);
-    if (warp >= kProducerWarp0 && warp < kXchgWarp) {
+
+    if (warp >= kProducerWarp0) {
         // ---------------------------------------------------------------- producers
         const int pw = warp - kProducerWarp0;
-        if (pw == 0 && lane == 0) {
-            ptx::mbar_arrive_expect_tx(&bar.q_full, kSmemQChunks * H * 128);
-            for (int c = 0; c < kSmemQChunks; ++c)
-                tma_load_2d(qs + c * kQChunkBytes, &qmap, &bar.q_full, (kTmemQChunks + c) * 64, r * H);
-        }
         // lane l < 16 owns entry 16 pw + l of every tile.  Batches of kBatch tiles: positions are
         // loaded two batches ahead and page ids one batch ahead, so no load waits on another on the
         // critical path.
@@ -296,6 +289,9 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const uint16_t*
         for (int u = 0; u < kBatch; ++u) pos2[u] = load_pos(kBatch + u);
         // copy lane layout: lane = 8 * (key % 4) + 16-byte piece of a 128-byte chunk row
         const int piece = lane & 7;
+        int gch[kMaxOwnChunks];
+#pragma unroll
+        for (int j = 0; j < kMaxOwnChunks; ++j) gch[j] = own_chunk(crank, j);
         for (int t0 = 0; t0 < ntiles && !timed_out; t0 += kBatch) {
             int rows[kBatch];
 #pragma unroll
@@ -315,107 +311,80 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const uint16_t*
                 const uint32_t ph = (t / kKvStages) & 1;
                 const uint32_t vbits = __ballot_sync(0xffffffffu, rows[u] >= 0) & 0xffffu;
                 const int row_src = rows[u] >= 0 ? rows[u] : 0;
-                // the stage is free once PV of its previous tile finished in both CTAs
+                // the stage is free once PV of its previous tile completed
                 if (lane == 0 && !ptx::mbar_wait(&bar.kv_empty[s], ph ^ 1u, deadline)) timed_out = true;
                 timed_out = __shfl_sync(0xffffffffu, timed_out ? 1 : 0, 0) != 0;
                 if (timed_out) break;
                 int rk[kKeysPerProducer / 4];
 #pragma unroll
-                for (int kq = 0; kq < kKeysPerProducer / 4; ++kq) rk[kq] = __shfl_sync(0xffffffffu, row_src, kq * 4 + (lane >> 3));
+                for (int kq = 0; kq < kKeysPerProducer / 4; ++kq)
+                    rk[kq] = __shfl_sync(0xffffffffu, row_src, kq * 4 + (lane >> 3));
                 const uint32_t stage = kv_addr0 + s * kKvStageBytes;
-#pragma unroll 1
-                for (int c = c_lo; c < c_hi; ++c) {
+#pragma unroll
+                for (int j = 0; j < kMaxOwnChunks; ++j) {
+                    if (j >= nown) break;
 #pragma unroll
                     for (int kq = 0; kq < kKeysPerProducer / 4; ++kq) {
                         const int key = pw * kKeysPerProducer + kq * 4 + (lane >> 3);
-                        const uint32_t dst = stage + c * kKvChunkBytes + key * 128 + ((piece ^ (key & 7)) << 4);
-                        cp_async_16(dst, kv + static_cast<int64_t>(rk[kq]) * kLatentDim + c * 64 + piece * 8);
+                        const uint32_t dst = stage + j * kKvChunkBytes + key * 128 + ((piece ^ (key & 7)) << 4);
+                        cp_async_16(dst, kv + static_cast<int64_t>(rk[kq]) * kLatentDim + gch[j] * 64 + piece * 8);
                     }
                 }
-                cp_async_arrive_noinc(&bar.kv_local[s]);
+                cp_async_arrive_noinc(&bar.kv_full[s]);
                 if (lane == 0) {
                     bar.valid[s][pw] = vbits;
-                    ptx::mbar_arrive(&bar.kv_local[s]);
+                    ptx::mbar_arrive(&bar.kv_full[s]);
                 }
             }
         }
-        // drain: the last PV completions of both CTAs must have reached this CTA's barriers
-        if (pw == 0 && lane == 0 && !timed_out) {
-            for (int t = (ntiles > kKvStages ? ntiles - kKvStages : 0); t < ntiles; ++t)
-                if (!ptx::mbar_wait(&bar.kv_empty[t % kKvStages], (t / kKvStages) & 1, deadline)) timed_out = true;
-        }
         asm volatile("cp.async.wait_all;" ::: "memory");
-    } else if (warp == kXchgWarp) {
-        // ---------------------------------------------------------------- exchange with the peer
-        if (lane == 0) {
-            const uint32_t peer = crank ^ 1u;
-            const uint32_t my_bytes = static_cast<uint32_t>(c_hi - c_lo) * kKvChunkBytes;
-            const uint32_t peer_bytes = static_cast<uint32_t>(kChunks - (c_hi - c_lo)) * kKvChunkBytes;
-            for (int t = 0; t < ntiles; ++t) {
-                const int s = t % kKvStages;
-                if (!ptx::mbar_wait(&bar.kv_local[s], (t / kKvStages) & 1, deadline)) { timed_out = true; break; }
-                ptx::fence_proxy_async_smem();   // the cp.async data is read by the bulk copy (async proxy)
-                const uint32_t src = kv_addr0 + s * kKvStageBytes + c_lo * kKvChunkBytes;
-                bulk_copy_to_peer(map_to_rank(src, peer), src, my_bytes,
-                                  map_to_rank(ptx::smem_addr(&bar.kv_full[s]), peer));
-                ptx::mbar_arrive_expect_tx(&bar.kv_full[s], peer_bytes);
-            }
-        }
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_qk = ptx::instr_desc(1, 1, kHeadsPerCta, kKeysPerTile);
             constexpr uint32_t idesc_pv = ptx::instr_desc(1, 1, kHeadsPerCta, kHalfDims) | (1u << 16);  // B MN-major
-            const uint32_t q_addr = ptx::smem_addr(qs);
-            const uint32_t kv_addr = ptx::smem_addr(kvs);
             const uint32_t p_addr = ptx::smem_addr(ps);
-            auto issue_qk = [&](int t) -> bool {
-                const int s = t % kKvStages;
-                if (!ptx::mbar_wait(&bar.kv_full[s], (t / kKvStages) & 1, deadline)) return false;
-                if (!ptx::mbar_wait(&bar.s_empty, (t & 1) ^ 1u, deadline)) return false;
-                ptx::fence_proxy_async_smem();   // chunks written by cp.async, read by the tensor cores
-                ptx::tc_fence_after_sync();
-                const uint32_t d = tmem + kTmemS;
-                const uint32_t kb = kv_addr + s * kKvStageBytes;
-#pragma unroll 1
-                for (int c = 0; c < kTmemQChunks; ++c) {
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t db = make_desc(kb + c * kKvChunkBytes + kk * 32, 16, 1024, kLayoutSw128);
-                        umma_f16_ts(d, tmem + kTmemQ + c * 32 + kk * 8, db, idesc_qk, (c | kk) != 0 ? 1u : 0u);
-                    }
-                }
-#pragma unroll 1
-                for (int c = 0; c < kSmemQChunks; ++c) {
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t da = make_desc(q_addr + c * kQChunkBytes + kk * 32, 16, 1024, kLayoutSw128);
-                        const uint64_t db =
-                            make_desc(kb + (kTmemQChunks + c) * kKvChunkBytes + kk * 32, 16, 1024, kLayoutSw128);
-                        ptx::umma_f16(d, da, db, idesc_qk, 1u);
-                    }
-                }
-                ptx::umma_commit(&bar.s_full);
-                return true;
-            };
             bool ok = ptx::mbar_wait(&bar.q_full, 0, deadline);
-            if (ok && ntiles > 0) ok = issue_qk(0);
-            for (int t = 0; t < ntiles && ok; ++t) {
-                if (t + 1 < ntiles && !issue_qk(t + 1)) { ok = false; break; }
-                // O += P(t) V(t)
-                const int pb = t & 1;
-                if (!ptx::mbar_wait(&bar.p_full[pb], (t >> 1) & 1, deadline)) { ok = false; break; }
-                ptx::tc_fence_after_sync();
-                const int s = t % kKvStages;
-                const uint32_t vb = kv_addr + s * kKvStageBytes + (half * 4) * kKvChunkBytes;
+            int tq = 0, tp = 0;   // next score tile, next PV tile
+            while (ok && tp < ntiles) {
+                bool issued = false;
+                // score MMAs of tile tq: its chunks landed and the previous partial scores were read
+                if (tq < ntiles && ptx::mbar_try_wait(&bar.kv_full[tq % kKvStages], (tq / kKvStages) & 1) &&
+                    ptx::mbar_try_wait(&bar.s_empty, (tq & 1) ^ 1u)) {
+                    ptx::fence_proxy_async_smem();   // chunks written by cp.async, read by the tensor cores
+                    ptx::tc_fence_after_sync();
+                    const uint32_t kb = kv_addr0 + (tq % kKvStages) * kKvStageBytes;
+                    const uint32_t d = tmem + kTmemS;
+#pragma unroll 1
+                    for (int j = 0; j < nown; ++j) {
 #pragma unroll
-                for (int ks = 0; ks < kKeysPerTile / 16; ++ks) {
-                    const uint64_t da = make_desc(p_addr + pb * kPBytes + ks * 256, 128, 1024, kLayoutNone);
-                    const uint64_t db = make_desc(vb + ks * 16 * 128, kKvChunkBytes, 1024, kLayoutSw128);
-                    ptx::umma_f16(tmem, da, db, idesc_pv, (t | ks) != 0 ? 1u : 0u);
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t db = make_desc(kb + j * kKvChunkBytes + kk * 32, 16, 1024, kLayoutSw128);
+                            umma_f16_ts(d, tmem + kTmemQ + j * 32 + kk * 8, db, idesc_qk, (j | kk) != 0 ? 1u : 0u);
+                        }
+                    }
+                    ptx::umma_commit(&bar.s_full);
+                    ++tq;
+                    issued = true;
                 }
-                umma_commit_mc(&bar.kv_empty[s], static_cast<uint16_t>(0x3));   // stage free here and in the peer
-                ptx::umma_commit(&bar.p_empty[pb]);
+                // O += P(tp) V(tp)
+                if (tp < tq && ptx::mbar_try_wait(&bar.p_full[tp & 1], (tp >> 1) & 1)) {
+                    ptx::tc_fence_after_sync();
+                    const int s = tp % kKvStages;
+                    const int pb = tp & 1;
+                    const uint32_t vb = kv_addr0 + s * kKvStageBytes;   // own chunks 0-3 = this CTA's value dims
+#pragma unroll
+                    for (int ks = 0; ks < kKeysPerTile / 16; ++ks) {
+                        const uint64_t da = make_desc(p_addr + pb * kPBytes + ks * 256, 128, 1024, kLayoutNone);
+                        const uint64_t db = make_desc(vb + ks * 16 * 128, kKvChunkBytes, 1024, kLayoutSw128);
+                        ptx::umma_f16(tmem, da, db, idesc_pv, (tp | ks) != 0 ? 1u : 0u);
+                    }
+                    ptx::umma_commit(&bar.kv_empty[s]);
+                    ptx::umma_commit(&bar.p_empty[pb]);
+                    ++tp;
+                    issued = true;
+                }
+                if (!issued && static_cast<uint64_t>(clock64()) > deadline) ok = false;
             }
             if (ok && ntiles > 0) ptx::umma_commit(&bar.o_full);
             if (!ok) timed_out = true;
@@ -426,26 +395,24 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const uint16_t*
         const int head = quad * 32 + lane;          // TMEM lane = head
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         {
-            // query dims 0..383 of this head into TMEM columns 320.., two bf16 per column
+            // this CTA's query chunks of this head into TMEM columns 320.., two bf16 per column
             const uint4* src = reinterpret_cast<const uint4*>(q + (static_cast<int64_t>(r) * H + head) * kLatentDim);
             const bool live = head < H;
 #pragma unroll 1
-            for (int c0 = 0; c0 < kTmemQChunks; c0 += 2) {
-                uint4 raw[16];
+            for (int j = 0; j < nown; ++j) {
+                const int c = own_chunk(crank, j);
+                uint4 raw[8];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) raw[i] = live ? __ldg(src + c0 * 8 + i) : make_uint4(0u, 0u, 0u, 0u);
+                for (int i = 0; i < 8; ++i) raw[i] = live ? __ldg(src + c * 8 + i) : make_uint4(0u, 0u, 0u, 0u);
+                uint32_t w[32];
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    uint32_t w[32];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        w[4 * i + 0] = raw[cc * 8 + i].x;
-                        w[4 * i + 1] = raw[cc * 8 + i].y;
-                        w[4 * i + 2] = raw[cc * 8 + i].z;
-                        w[4 * i + 3] = raw[cc * 8 + i].w;
-                    }
-                    tmem_st_32x32b_x32(tmem + lane_base + kTmemQ + (c0 + cc) * 32, w);
+                for (int i = 0; i < 8; ++i) {
+                    w[4 * i + 0] = raw[i].x;
+                    w[4 * i + 1] = raw[i].y;
+                    w[4 * i + 2] = raw[i].z;
+                    w[4 * i + 3] = raw[i].w;
                 }
+                tmem_st_32x32b_x32(tmem + lane_base + kTmemQ + j * 32, w);
             }
             tmem_wait_st();
             ptx::tc_fence_before_sync();
@@ -453,6 +420,9 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const uint16_t*
             if (lane == 0) ptx::mbar_arrive(&bar.q_full);
         }
         const float cscale = scale * kLog2e;
+        const uint32_t x_peer = map_to_rank(ptx::smem_addr(xs), peer) + head * 16;
+        const uint32_t xf_peer = map_to_rank(ptx::smem_addr(&bar.x_full), peer);
+        const uint32_t xe_peer = map_to_rank(ptx::smem_addr(&bar.x_empty), peer);
         float m_run = -INFINITY, l_run = 0.0f;
         for (int t = 0; t < ntiles; ++t) {
             const int s = t % kKvStages;
@@ -467,6 +437,23 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const uint16_t*
             ptx::tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&bar.s_empty);
+            // swap partial scores with the peer: ours go to its x buffer once it has read the last ones
+            if (!mbar_wait_cluster(&bar.x_empty, (t & 1) ^ 1u, deadline)) { timed_out = true; break; }
+#pragma unroll
+            for (int kq = 0; kq < 16; ++kq)
+                st_cluster_v4(x_peer + kq * (kHeadsPerCta * 16), __uint_as_float(sr[4 * kq]), __uint_as_float(sr[4 * kq + 1]),
+                              __uint_as_float(sr[4 * kq + 2]), __uint_as_float(sr[4 * kq + 3]));
+            mbar_arrive_remote(xf_peer);
+            if (!mbar_wait_cluster(&bar.x_full, t & 1, deadline)) { timed_out = true; break; }
+#pragma unroll
+            for (int kq = 0; kq < 16; ++kq) {
+                const float4 o = *reinterpret_cast<const float4*>(xs + kq * (kHeadsPerCta * 4) + head * 4);
+                sr[4 * kq + 0] = __float_as_uint(__uint_as_float(sr[4 * kq + 0]) + o.x);
+                sr[4 * kq + 1] = __float_as_uint(__uint_as_float(sr[4 * kq + 1]) + o.y);
+                sr[4 * kq + 2] = __float_as_uint(__uint_as_float(sr[4 * kq + 2]) + o.z);
+                sr[4 * kq + 3] = __float_as_uint(__uint_as_float(sr[4 * kq + 3]) + o.w);
+            }
+            mbar_arrive_remote(xe_peer);   // the peer may overwrite our x buffer now
             const uint64_t vbits = static_cast<uint64_t>(bar.valid[s][0]) | (static_cast<uint64_t>(bar.valid[s][1]) << 16) |
                                    (static_cast<uint64_t>(bar.valid[s][2]) << 32) |
                                    (static_cast<uint64_t>(bar.valid[s][3]) << 48);
@@ -502,10 +489,11 @@ sparse_mla_umma_kernel(const __grid_constant__ CUtensorMap qmap, const uint16_t*
             m_run = m_new;
             float psum = 0.0f;
             uint32_t pk[32];
+            const bool any = m_run != -INFINITY;
 #pragma unroll
             for (int i = 0; i < 64; i += 2) {
-                const float p0 = (m_run == -INFINITY) ? 0.0f : exp2f(__uint_as_float(sr[i]) - m_run);
-                const float p1 = (m_run == -INFINITY) ? 0.0f : exp2f(__uint_as_float(sr[i + 1]) - m_run);
+                const float p0 = any ? fast_exp2(__uint_as_float(sr[i]) - m_run) : 0.0f;
+                const float p1 = any ? fast_exp2(__uint_as_float(sr[i + 1]) - m_run) : 0.0f;
                 psum += p0 + p1;
                 pk[i / 2] = pack_bf16x2(p0, p1);
             }
@@ -629,32 +617,6 @@ int mla_splits(int T, int k) {
     return s;
 }
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn tensor_map_encoder() {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-        return nullptr;
-    return reinterpret_cast<EncodeTiledFn>(fn);
-}
-
-// 2-D bf16 tensor map: rows of 576 elements (1152 bytes), box of 64 elements x box_rows rows.
-bool encode_rows_576(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
-    auto encode = tensor_map_encoder();
-    if (encode == nullptr) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kLatentDim), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kLatentDim) * 2};
-    const cuuint32_t box[2] = {64, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 }  // namespace dsa
 
@@ -687,14 +649,12 @@ extern "C" dsa_status dsa_sparse_mla_decode(const void* q_bf16, const void* kv_p
     const int splits = mla_splits(T, k);
     float* part_o = static_cast<float*>(workspace);
     float* part_lse = splits > 1 ? part_o + static_cast<size_t>(T) * H * splits * kValueDim : nullptr;
-    CUtensorMap qmap;
-    if (!encode_rows_576(&qmap, q_bf16, static_cast<uint64_t>(T) * H, static_cast<uint32_t>(H))) return DSA_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaFuncSetAttribute(sparse_mla_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kMlaSmemBytes)) != cudaSuccess)
         return DSA_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2, splits, T);   // x: the two halves of a (row, split) = one cluster
+    cfg.gridDim = dim3(2, splits, T);   // x: the two ranks of a (row, split) = one cluster
     cfg.blockDim = dim3(kMlaThreads, 1, 1);
     cfg.dynamicSmemBytes = kMlaSmemBytes;
     cfg.stream = s;
@@ -705,10 +665,10 @@ extern "C" dsa_status dsa_sparse_mla_decode(const void* q_bf16, const void* kv_p
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, sparse_mla_umma_kernel, qmap, static_cast<const uint16_t*>(kv_pool),
-                           static_cast<const uint16_t*>(q_bf16), num_pages,
-                           block_table, max_pages, seq_lens, cu_q, B, idx, k, H, scale, splits,
-                           static_cast<uint16_t*>(out_bf16), lse, part_o, part_lse, dev_err) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, sparse_mla_umma_kernel, static_cast<const uint16_t*>(kv_pool),
+                           static_cast<const uint16_t*>(q_bf16), num_pages, block_table, static_cast<int>(max_pages),
+                           seq_lens, cu_q, static_cast<int>(B), idx, static_cast<int>(k), static_cast<int>(H), scale,
+                           splits, static_cast<uint16_t*>(out_bf16), lse, part_o, part_lse, dev_err) != cudaSuccess)
         return DSA_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
     if (splits > 1) {
