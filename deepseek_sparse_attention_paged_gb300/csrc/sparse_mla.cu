@@ -58,7 +58,6 @@ constexpr int kKvStages = 4;
 constexpr int kXBytes = kHeadsPerCta * kKeysPerTile * 4;        // 32768: the peer's partial scores
 constexpr int kPBytes = kHeadsPerCta * kKeysPerTile * 2;        // 16384
 constexpr int kSoftmaxWarps = 4;
-constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
 constexpr int kMmaWarp = 4;
 constexpr int kProducerWarp0 = 5;
 constexpr int kProducerWarps = 4;
@@ -110,8 +109,12 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t ran
     return r;
 }
 
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+// 16-byte store into another CTA's shared memory, counted as transaction bytes on that CTA's
+// mbarrier (no fence needed: the receiver's wait on the mbarrier orders the data).
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, float c, float d, uint32_t bar_cluster) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     addr),
+                 "f"(a), "f"(b), "f"(c), "f"(d), "r"(bar_cluster)
                  : "memory");
 }
 
@@ -189,8 +192,8 @@ struct MlaBars {
     uint64_t kv_empty[kKvStages];  // PV of the stage's tile completed
     uint64_t s_full;               // partial score MMAs completed
     uint64_t s_empty;              // partial scores read out of TMEM
-    uint64_t x_full;               // the peer's partial scores are in x (128 peer threads)
-    uint64_t x_empty;              // the peer has read the scores this CTA sent it (128 peer threads)
+    uint64_t x_full;               // the peer's partial scores are in x (local arm + the peer's 32 KB)
+    uint64_t x_empty;              // the peer has read the scores this CTA sent it (4 peer warps)
     uint64_t p_full[2];
     uint64_t p_empty[2];
     uint64_t o_full;
@@ -237,8 +240,8 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
         }
         ptx::mbar_init(&bar.s_full, 1);
         ptx::mbar_init(&bar.s_empty, kSoftmaxWarps);
-        ptx::mbar_init(&bar.x_full, kSoftmaxThreads);
-        ptx::mbar_init(&bar.x_empty, kSoftmaxThreads);
+        ptx::mbar_init(&bar.x_full, 1);
+        ptx::mbar_init(&bar.x_empty, kSoftmaxWarps);
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(&bar.p_full[a], kSoftmaxWarps);
             ptx::mbar_init(&bar.p_empty[a], 1);
@@ -427,6 +430,7 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
         for (int t = 0; t < ntiles; ++t) {
             const int s = t % kKvStages;
             const int pb = t & 1;
+            if (threadIdx.x == 0) ptx::mbar_arrive_expect_tx(&bar.x_full, kXBytes);   // the peer's tile-t scores
             if (!ptx::mbar_wait(&bar.s_full, t & 1, deadline)) { timed_out = true; break; }
             if (!ptx::mbar_wait(&bar.kv_full[s], (t / kKvStages) & 1, deadline)) { timed_out = true; break; }
             ptx::tc_fence_after_sync();
@@ -437,13 +441,18 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
             ptx::tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&bar.s_empty);
-            // swap partial scores with the peer: ours go to its x buffer once it has read the last ones
+            // swap partial scores with the peer: ours go to its x buffer once it has read the last ones.
+            // Our reads of x for tile t-1 finished long ago; releasing them only now keeps the
+            // cluster-scope release (a fence) off the path between receiving and using the scores.
+            if (t > 0) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(xe_peer);
+            }
             if (!mbar_wait_cluster(&bar.x_empty, (t & 1) ^ 1u, deadline)) { timed_out = true; break; }
 #pragma unroll
             for (int kq = 0; kq < 16; ++kq)
-                st_cluster_v4(x_peer + kq * (kHeadsPerCta * 16), __uint_as_float(sr[4 * kq]), __uint_as_float(sr[4 * kq + 1]),
-                              __uint_as_float(sr[4 * kq + 2]), __uint_as_float(sr[4 * kq + 3]));
-            mbar_arrive_remote(xf_peer);
+                st_async_v4(x_peer + kq * (kHeadsPerCta * 16), __uint_as_float(sr[4 * kq]), __uint_as_float(sr[4 * kq + 1]),
+                            __uint_as_float(sr[4 * kq + 2]), __uint_as_float(sr[4 * kq + 3]), xf_peer);
             if (!mbar_wait_cluster(&bar.x_full, t & 1, deadline)) { timed_out = true; break; }
 #pragma unroll
             for (int kq = 0; kq < 16; ++kq) {
@@ -453,7 +462,6 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
                 sr[4 * kq + 2] = __float_as_uint(__uint_as_float(sr[4 * kq + 2]) + o.z);
                 sr[4 * kq + 3] = __float_as_uint(__uint_as_float(sr[4 * kq + 3]) + o.w);
             }
-            mbar_arrive_remote(xe_peer);   // the peer may overwrite our x buffer now
             const uint64_t vbits = static_cast<uint64_t>(bar.valid[s][0]) | (static_cast<uint64_t>(bar.valid[s][1]) << 16) |
                                    (static_cast<uint64_t>(bar.valid[s][2]) << 32) |
                                    (static_cast<uint64_t>(bar.valid[s][3]) << 48);
