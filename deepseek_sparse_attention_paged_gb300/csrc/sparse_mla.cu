@@ -11,18 +11,23 @@
 // 0..255 and the 64 rope dims), rank 1 owns chunks 4-7 (value dims 256..511).  Each CTA reads only
 // its own chunks of every selected row (16-byte cp.async straight into the swizzled operand
 // layout), keeps only its own query chunks (in tensor memory), computes the partial score tile
-// over its dims, and the two CTAs swap partial score tiles through distributed shared memory; both
+// over its dims, and the two CTAs swap partial score tiles through distributed shared memory
+// (st.async into a double buffer, counted as transaction bytes on the receiver's mbarrier); both
 // then hold the full scores, run the same softmax (identical P: the fp32 sum is commutative) and
 // each accumulates its 256 output dims from its own value chunks.  Nothing of a latent row is read
-// twice or copied between the CTAs, and their key stages are private, so each CTA runs a 4-deep
+// twice or copied between the CTAs, and their key stages are private, so each CTA runs a 3-deep
 // load pipeline of its own.
 //
 // Tensor memory (512 columns x 128 lanes, lane = head):
 //   [0, 256)   O, this CTA's 256 output dims (fp32)
 //   [256, 320) partial score tile of 64 keys (fp32)
 //   [320, 480) this CTA's query chunks, the A operand of the score MMA (two bf16 per column)
-// Shared memory: 4 stages of 64 rows x this CTA's chunks (128-byte swizzle, K-major; the first 4
-// chunks double as the MN-major value operand); the peer's partial scores (32 KB); 2 buffers of P.
+// Shared memory: 3 stages of 64 rows x this CTA's chunks (128-byte swizzle, K-major; the first 4
+// chunks double as the MN-major value operand); 2 buffers of the peer's partial scores (32 KB
+// each); 2 buffers of P.
+// The score buffers need no "free" signal: the peer writes tile t + 2 into the buffer of tile t
+// only after it has received this CTA's tile t + 1 scores, which this CTA sends after it has
+// consumed tile t's buffer.
 //
 // Roles (288 threads), for tiles of 64 selected entries:
 //   warps 0-3 (thread = head = TMEM lane): query chunks into TMEM; per tile: read the partial
@@ -54,7 +59,7 @@ constexpr int kMaxOwnChunks = 5;                  // rank 0: chunks 0-3 and 8; r
 constexpr int kHalfDims = kValueDim / 2;          // 256 output dims per CTA
 constexpr int kKvChunkBytes = kKeysPerTile * 128;               // 8192
 constexpr int kKvStageBytes = kMaxOwnChunks * kKvChunkBytes;    // 40960
-constexpr int kKvStages = 4;
+constexpr int kKvStages = 3;
 constexpr int kXBytes = kHeadsPerCta * kKeysPerTile * 4;        // 32768: the peer's partial scores
 constexpr int kPBytes = kHeadsPerCta * kKeysPerTile * 2;        // 16384
 constexpr int kSoftmaxWarps = 4;
@@ -69,7 +74,7 @@ constexpr uint32_t kTmemQ = kTmemS + kKeysPerTile;              // query chunks 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;                       // log2 units
 constexpr int kBatch = 4;                                       // tiles resolved per batch
-constexpr size_t kMlaSmemBytes = 1024 + size_t(kKvStages) * kKvStageBytes + kXBytes + 2 * kPBytes + 512;
+constexpr size_t kMlaSmemBytes = 1024 + size_t(kKvStages) * kKvStageBytes + 2 * kXBytes + 2 * kPBytes + 512;
 
 static_assert(kChunks == 9 && kMaxOwnChunks + 4 == kChunks, "chunk ownership: 5 + 4");
 static_assert(kTmemQ + kMaxOwnChunks * 32 <= kTmemCols, "tensor-memory budget");
@@ -116,27 +121,6 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, flo
                      addr),
                  "f"(a), "f"(b), "f"(c), "f"(d), "r"(bar_cluster)
                  : "memory");
-}
-
-// Arrive (release at cluster scope) on an mbarrier of another CTA of the cluster.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
-}
-
-// Bounded wait with acquire at cluster scope (for phases completed by the peer CTA).
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint64_t deadline) {
-    while (true) {
-        uint32_t done;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(done)
-            : "r"(ptx::smem_addr(bar)), "r"(parity)
-            : "memory");
-        if (done) return true;
-        if (static_cast<uint64_t>(clock64()) > deadline) return false;
-    }
 }
 
 __device__ __forceinline__ void cluster_sync_all() {
@@ -192,8 +176,7 @@ struct MlaBars {
     uint64_t kv_empty[kKvStages];  // PV of the stage's tile completed
     uint64_t s_full;               // partial score MMAs completed
     uint64_t s_empty;              // partial scores read out of TMEM
-    uint64_t x_full;               // the peer's partial scores are in x (local arm + the peer's 32 KB)
-    uint64_t x_empty;              // the peer has read the scores this CTA sent it (4 peer warps)
+    uint64_t x_full[2];            // the peer's partial scores are in x[b] (local arm + the peer's 32 KB)
     uint64_t p_full[2];
     uint64_t p_empty[2];
     uint64_t o_full;
@@ -213,8 +196,8 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
     const uint32_t raw_addr = ptx::smem_addr(smem_raw);
     unsigned char* base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     unsigned char* kvs = base;                                  // [4][5 chunks][64 keys][128 B], SW128
-    float* xs = reinterpret_cast<float*>(kvs + kKvStages * kKvStageBytes);   // [16 key quads][128 heads][4]
-    unsigned char* ps = reinterpret_cast<unsigned char*>(xs) + kXBytes;     // [2][16 head groups][8 key groups][8][16 B]
+    float* xs = reinterpret_cast<float*>(kvs + kKvStages * kKvStageBytes);   // [2][16 key quads][128 heads][4]
+    unsigned char* ps = reinterpret_cast<unsigned char*>(xs) + 2 * kXBytes; // [2][16 head groups][8 key groups][8][16 B]
     MlaBars& bar = *reinterpret_cast<MlaBars*>(ps + 2 * kPBytes);
 
     const int split = blockIdx.y;
@@ -240,8 +223,8 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
         }
         ptx::mbar_init(&bar.s_full, 1);
         ptx::mbar_init(&bar.s_empty, kSoftmaxWarps);
-        ptx::mbar_init(&bar.x_full, 1);
-        ptx::mbar_init(&bar.x_empty, kSoftmaxWarps);
+        ptx::mbar_init(&bar.x_full[0], 1);
+        ptx::mbar_init(&bar.x_full[1], 1);
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(&bar.p_full[a], kSoftmaxWarps);
             ptx::mbar_init(&bar.p_empty[a], 1);
@@ -424,13 +407,13 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
         }
         const float cscale = scale * kLog2e;
         const uint32_t x_peer = map_to_rank(ptx::smem_addr(xs), peer) + head * 16;
-        const uint32_t xf_peer = map_to_rank(ptx::smem_addr(&bar.x_full), peer);
-        const uint32_t xe_peer = map_to_rank(ptx::smem_addr(&bar.x_empty), peer);
+        const uint32_t xf_peer = map_to_rank(ptx::smem_addr(&bar.x_full[0]), peer);
         float m_run = -INFINITY, l_run = 0.0f;
         for (int t = 0; t < ntiles; ++t) {
             const int s = t % kKvStages;
             const int pb = t & 1;
-            if (threadIdx.x == 0) ptx::mbar_arrive_expect_tx(&bar.x_full, kXBytes);   // the peer's tile-t scores
+            const int xb = t & 1;
+            if (threadIdx.x == 0) ptx::mbar_arrive_expect_tx(&bar.x_full[xb], kXBytes);   // the peer's tile-t scores
             if (!ptx::mbar_wait(&bar.s_full, t & 1, deadline)) { timed_out = true; break; }
             if (!ptx::mbar_wait(&bar.kv_full[s], (t / kKvStages) & 1, deadline)) { timed_out = true; break; }
             ptx::tc_fence_after_sync();
@@ -441,22 +424,17 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
             ptx::tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&bar.s_empty);
-            // swap partial scores with the peer: ours go to its x buffer once it has read the last ones.
-            // Our reads of x for tile t-1 finished long ago; releasing them only now keeps the
-            // cluster-scope release (a fence) off the path between receiving and using the scores.
-            if (t > 0) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive_remote(xe_peer);
-            }
-            if (!mbar_wait_cluster(&bar.x_empty, (t & 1) ^ 1u, deadline)) { timed_out = true; break; }
+            // swap partial scores with the peer (buffer t % 2 on both sides)
 #pragma unroll
             for (int kq = 0; kq < 16; ++kq)
-                st_async_v4(x_peer + kq * (kHeadsPerCta * 16), __uint_as_float(sr[4 * kq]), __uint_as_float(sr[4 * kq + 1]),
-                            __uint_as_float(sr[4 * kq + 2]), __uint_as_float(sr[4 * kq + 3]), xf_peer);
-            if (!mbar_wait_cluster(&bar.x_full, t & 1, deadline)) { timed_out = true; break; }
+                st_async_v4(x_peer + xb * kXBytes + kq * (kHeadsPerCta * 16), __uint_as_float(sr[4 * kq]),
+                            __uint_as_float(sr[4 * kq + 1]), __uint_as_float(sr[4 * kq + 2]), __uint_as_float(sr[4 * kq + 3]),
+                            xf_peer + xb * 8);
+            if (!ptx::mbar_wait(&bar.x_full[xb], (t >> 1) & 1, deadline)) { timed_out = true; break; }
+            const float* xr = xs + xb * (kXBytes / 4);
 #pragma unroll
             for (int kq = 0; kq < 16; ++kq) {
-                const float4 o = *reinterpret_cast<const float4*>(xs + kq * (kHeadsPerCta * 4) + head * 4);
+                const float4 o = *reinterpret_cast<const float4*>(xr + kq * (kHeadsPerCta * 4) + head * 4);
                 sr[4 * kq + 0] = __float_as_uint(__uint_as_float(sr[4 * kq + 0]) + o.x);
                 sr[4 * kq + 1] = __float_as_uint(__uint_as_float(sr[4 * kq + 1]) + o.y);
                 sr[4 * kq + 2] = __float_as_uint(__uint_as_float(sr[4 * kq + 2]) + o.z);
