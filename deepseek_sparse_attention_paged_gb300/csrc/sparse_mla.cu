@@ -335,8 +335,8 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
             while (ok && tp < ntiles) {
                 bool issued = false;
                 // score MMAs of tile tq: its chunks landed and the previous partial scores were read
-                if (tq < ntiles && ptx::mbar_try_wait(&bar.kv_full[tq % kKvStages], (tq / kKvStages) & 1) &&
-                    ptx::mbar_try_wait(&bar.s_empty, (tq & 1) ^ 1u)) {
+                if (tq < ntiles && ptx::mbar_test_wait(&bar.kv_full[tq % kKvStages], (tq / kKvStages) & 1) &&
+                    ptx::mbar_test_wait(&bar.s_empty, (tq & 1) ^ 1u)) {
                     ptx::fence_proxy_async_smem();   // chunks written by cp.async, read by the tensor cores
                     ptx::tc_fence_after_sync();
                     const uint32_t kb = kv_addr0 + (tq % kKvStages) * kKvStageBytes;
@@ -354,7 +354,7 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
                     issued = true;
                 }
                 // O += P(tp) V(tp)
-                if (tp < tq && ptx::mbar_try_wait(&bar.p_full[tp & 1], (tp >> 1) & 1)) {
+                if (tp < tq && ptx::mbar_test_wait(&bar.p_full[tp & 1], (tp >> 1) & 1)) {
                     ptx::tc_fence_after_sync();
                     const int s = tp % kKvStages;
                     const int pb = tp & 1;

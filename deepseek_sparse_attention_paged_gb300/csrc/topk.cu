@@ -217,13 +217,18 @@ topk_bitmap_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* 
     const int v4 = vec ? (v >> 2) : 0;
     auto for_each_key = [&](auto&& fn) {
         const float4* row4 = reinterpret_cast<const float4*>(row);
+        constexpr int U = 4;   // 16-byte loads in flight per thread
         int i = threadIdx.x;
-        for (; i + kTopkThreads < v4; i += 2 * kTopkThreads) {
-            const float4 a = __ldg(row4 + i);
-            const float4 c = __ldg(row4 + i + kTopkThreads);
-            fn(4 * i, order_key(a.x)); fn(4 * i + 1, order_key(a.y)); fn(4 * i + 2, order_key(a.z)); fn(4 * i + 3, order_key(a.w));
-            const int j = i + kTopkThreads;
-            fn(4 * j, order_key(c.x)); fn(4 * j + 1, order_key(c.y)); fn(4 * j + 2, order_key(c.z)); fn(4 * j + 3, order_key(c.w));
+        for (; i + (U - 1) * kTopkThreads < v4; i += U * kTopkThreads) {
+            float4 a[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) a[u] = __ldg(row4 + i + u * kTopkThreads);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = i + u * kTopkThreads;
+                fn(4 * j, order_key(a[u].x)); fn(4 * j + 1, order_key(a[u].y));
+                fn(4 * j + 2, order_key(a[u].z)); fn(4 * j + 3, order_key(a[u].w));
+            }
         }
         for (; i < v4; i += kTopkThreads) {
             const float4 a = __ldg(row4 + i);
