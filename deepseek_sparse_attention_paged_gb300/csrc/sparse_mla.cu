@@ -12,22 +12,19 @@
 // its own chunks of every selected row (16-byte cp.async straight into the swizzled operand
 // layout), keeps only its own query chunks (in tensor memory), computes the partial score tile
 // over its dims, and the two CTAs swap partial score tiles through distributed shared memory
-// (st.async into a double buffer, counted as transaction bytes on the receiver's mbarrier); both
-// then hold the full scores, run the same softmax (identical P: the fp32 sum is commutative) and
+// (st.async, counted as transaction bytes on the receiver's mbarrier; the receiver answers with a
+// 4-byte st.async per warp once it has consumed them, so no fence is needed); both then hold the
+// full scores, run the same softmax (identical P: the fp32 sum is commutative) and
 // each accumulates its 256 output dims from its own value chunks.  Nothing of a latent row is read
-// twice or copied between the CTAs, and their key stages are private, so each CTA runs a 3-deep
+// twice or copied between the CTAs, and their key stages are private, so each CTA runs a 4-deep
 // load pipeline of its own.
 //
 // Tensor memory (512 columns x 128 lanes, lane = head):
 //   [0, 256)   O, this CTA's 256 output dims (fp32)
 //   [256, 320) partial score tile of 64 keys (fp32)
 //   [320, 480) this CTA's query chunks, the A operand of the score MMA (two bf16 per column)
-// Shared memory: 3 stages of 64 rows x this CTA's chunks (128-byte swizzle, K-major; the first 4
-// chunks double as the MN-major value operand); 2 buffers of the peer's partial scores (32 KB
-// each); 2 buffers of P.
-// The score buffers need no "free" signal: the peer writes tile t + 2 into the buffer of tile t
-// only after it has received this CTA's tile t + 1 scores, which this CTA sends after it has
-// consumed tile t's buffer.
+// Shared memory: 4 stages of 64 rows x this CTA's chunks (128-byte swizzle, K-major; the first 4
+// chunks double as the MN-major value operand); the peer's partial scores (32 KB); 2 buffers of P.
 //
 // Roles (288 threads), for tiles of 64 selected entries:
 //   warps 0-3 (thread = head = TMEM lane): query chunks into TMEM; per tile: read the partial
@@ -59,7 +56,7 @@ constexpr int kMaxOwnChunks = 5;                  // rank 0: chunks 0-3 and 8; r
 constexpr int kHalfDims = kValueDim / 2;          // 256 output dims per CTA
 constexpr int kKvChunkBytes = kKeysPerTile * 128;               // 8192
 constexpr int kKvStageBytes = kMaxOwnChunks * kKvChunkBytes;    // 40960
-constexpr int kKvStages = 3;
+constexpr int kKvStages = 4;
 constexpr int kXBytes = kHeadsPerCta * kKeysPerTile * 4;        // 32768: the peer's partial scores
 constexpr int kPBytes = kHeadsPerCta * kKeysPerTile * 2;        // 16384
 constexpr int kSoftmaxWarps = 4;
@@ -74,7 +71,7 @@ constexpr uint32_t kTmemQ = kTmemS + kKeysPerTile;              // query chunks 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;                       // log2 units
 constexpr int kBatch = 4;                                       // tiles resolved per batch
-constexpr size_t kMlaSmemBytes = 1024 + size_t(kKvStages) * kKvStageBytes + 2 * kXBytes + 2 * kPBytes + 512;
+constexpr size_t kMlaSmemBytes = 1024 + size_t(kKvStages) * kKvStageBytes + kXBytes + 2 * kPBytes + 512;
 
 static_assert(kChunks == 9 && kMaxOwnChunks + 4 == kChunks, "chunk ownership: 5 + 4");
 static_assert(kTmemQ + kMaxOwnChunks * 32 <= kTmemCols, "tensor-memory budget");
@@ -120,6 +117,12 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, flo
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
                      addr),
                  "f"(a), "f"(b), "f"(c), "f"(d), "r"(bar_cluster)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t v, uint32_t bar_cluster) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr), "r"(v),
+                 "r"(bar_cluster)
                  : "memory");
 }
 
@@ -176,7 +179,9 @@ struct MlaBars {
     uint64_t kv_empty[kKvStages];  // PV of the stage's tile completed
     uint64_t s_full;               // partial score MMAs completed
     uint64_t s_empty;              // partial scores read out of TMEM
-    uint64_t x_full[2];            // the peer's partial scores are in x[b] (local arm + the peer's 32 KB)
+    uint64_t x_full;               // the peer's partial scores are in x (local arm + the peer's 32 KB)
+    uint64_t x_free;               // the peer consumed the scores this CTA sent (local arm + 4 x 4 B)
+    uint32_t x_sink[4];            // target of the peer's 4-byte consumed signals
     uint64_t p_full[2];
     uint64_t p_empty[2];
     uint64_t o_full;
@@ -197,7 +202,7 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
     unsigned char* base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     unsigned char* kvs = base;                                  // [4][5 chunks][64 keys][128 B], SW128
     float* xs = reinterpret_cast<float*>(kvs + kKvStages * kKvStageBytes);   // [2][16 key quads][128 heads][4]
-    unsigned char* ps = reinterpret_cast<unsigned char*>(xs) + 2 * kXBytes; // [2][16 head groups][8 key groups][8][16 B]
+    unsigned char* ps = reinterpret_cast<unsigned char*>(xs) + kXBytes;     // [2][16 head groups][8 key groups][8][16 B]
     MlaBars& bar = *reinterpret_cast<MlaBars*>(ps + 2 * kPBytes);
 
     const int split = blockIdx.y;
@@ -223,8 +228,8 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
         }
         ptx::mbar_init(&bar.s_full, 1);
         ptx::mbar_init(&bar.s_empty, kSoftmaxWarps);
-        ptx::mbar_init(&bar.x_full[0], 1);
-        ptx::mbar_init(&bar.x_full[1], 1);
+        ptx::mbar_init(&bar.x_full, 1);
+        ptx::mbar_init(&bar.x_free, 1);
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(&bar.p_full[a], kSoftmaxWarps);
             ptx::mbar_init(&bar.p_empty[a], 1);
@@ -407,13 +412,14 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
         }
         const float cscale = scale * kLog2e;
         const uint32_t x_peer = map_to_rank(ptx::smem_addr(xs), peer) + head * 16;
-        const uint32_t xf_peer = map_to_rank(ptx::smem_addr(&bar.x_full[0]), peer);
+        const uint32_t xf_peer = map_to_rank(ptx::smem_addr(&bar.x_full), peer);
+        const uint32_t xfree_peer = map_to_rank(ptx::smem_addr(&bar.x_free), peer);
+        const uint32_t xsink_peer = map_to_rank(ptx::smem_addr(&bar.x_sink[warp]), peer);
         float m_run = -INFINITY, l_run = 0.0f;
         for (int t = 0; t < ntiles; ++t) {
             const int s = t % kKvStages;
             const int pb = t & 1;
-            const int xb = t & 1;
-            if (threadIdx.x == 0) ptx::mbar_arrive_expect_tx(&bar.x_full[xb], kXBytes);   // the peer's tile-t scores
+            if (threadIdx.x == 0) ptx::mbar_arrive_expect_tx(&bar.x_full, kXBytes);   // the peer's tile-t scores
             if (!ptx::mbar_wait(&bar.s_full, t & 1, deadline)) { timed_out = true; break; }
             if (!ptx::mbar_wait(&bar.kv_full[s], (t / kKvStages) & 1, deadline)) { timed_out = true; break; }
             ptx::tc_fence_after_sync();
@@ -424,14 +430,16 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
             ptx::tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&bar.s_empty);
-            // swap partial scores with the peer (buffer t % 2 on both sides)
+            // our tile-t scores go to the peer's x once it consumed our tile t-1 ones
+            if (t > 0 && !ptx::mbar_wait(&bar.x_free, (t - 1) & 1, deadline)) { timed_out = true; break; }
+            // arm the next phase (the peer's 4 consumed signals of tile t) only after phase t-1 completed
+            if (threadIdx.x == 0) ptx::mbar_arrive_expect_tx(&bar.x_free, 16);
 #pragma unroll
             for (int kq = 0; kq < 16; ++kq)
-                st_async_v4(x_peer + xb * kXBytes + kq * (kHeadsPerCta * 16), __uint_as_float(sr[4 * kq]),
-                            __uint_as_float(sr[4 * kq + 1]), __uint_as_float(sr[4 * kq + 2]), __uint_as_float(sr[4 * kq + 3]),
-                            xf_peer + xb * 8);
-            if (!ptx::mbar_wait(&bar.x_full[xb], (t >> 1) & 1, deadline)) { timed_out = true; break; }
-            const float* xr = xs + xb * (kXBytes / 4);
+                st_async_v4(x_peer + kq * (kHeadsPerCta * 16), __uint_as_float(sr[4 * kq]), __uint_as_float(sr[4 * kq + 1]),
+                            __uint_as_float(sr[4 * kq + 2]), __uint_as_float(sr[4 * kq + 3]), xf_peer);
+            if (!ptx::mbar_wait(&bar.x_full, t & 1, deadline)) { timed_out = true; break; }
+            const float* xr = xs;
 #pragma unroll
             for (int kq = 0; kq < 16; ++kq) {
                 const float4 o = *reinterpret_cast<const float4*>(xr + kq * (kHeadsPerCta * 4) + head * 4);
@@ -440,6 +448,8 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
                 sr[4 * kq + 2] = __float_as_uint(__uint_as_float(sr[4 * kq + 2]) + o.z);
                 sr[4 * kq + 3] = __float_as_uint(__uint_as_float(sr[4 * kq + 3]) + o.w);
             }
+            __syncwarp();   // every lane's reads of x have returned (their values are in sr)
+            if (lane == 0) st_async_b32(xsink_peer, 1u, xfree_peer);
             const uint64_t vbits = static_cast<uint64_t>(bar.valid[s][0]) | (static_cast<uint64_t>(bar.valid[s][1]) << 16) |
                                    (static_cast<uint64_t>(bar.valid[s][2]) << 32) |
                                    (static_cast<uint64_t>(bar.valid[s][3]) << 48);
@@ -494,6 +504,8 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&bar.p_full[pb]);
         }
+        // the peer's last consumed signals land here before this CTA may finish
+        if (ntiles > 0 && !timed_out && !ptx::mbar_wait(&bar.x_free, (ntiles - 1) & 1, deadline)) timed_out = true;
         // ---------------- epilogue: O / l, lse
         bool have_o = ntiles > 0 && !timed_out;
         if (have_o && !ptx::mbar_wait(&bar.o_full, 0, deadline)) { timed_out = true; have_o = false; }
