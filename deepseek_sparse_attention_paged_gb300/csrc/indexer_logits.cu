@@ -256,31 +256,50 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
     }
     if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 8) {
         // this CTA's share of the tiles: total over all segments, then the segment holding t0
+        // (one scan when every segment has its own thread, else a total pass and a search pass)
         const int t = threadIdx.x - kEpiWarp0 * 32;
-        int64_t mine = 0;
         Seg tmp;
-        for (int sidx = t; sidx < nseg; sidx += 256) mine += seg_load(sa, sidx, tmp);
-        int64_t total;
-        epi_scan(mine, scan_scratch, &total);
-        const int64_t t0 = total * blockIdx.x / gridDim.x;
-        const int64_t t1 = total * (blockIdx.x + 1) / gridDim.x;
-        if (t == 0) {
-            part[0] = nseg;
-            part[1] = 0;
-            part[2] = static_cast<int32_t>(t1 - t0);
-        }
-        if (t1 > t0) {
-            int64_t seen = 0;
-            for (int c0 = 0; c0 < nseg; c0 += 256) {
-                const int n = (c0 + t < nseg) ? seg_load(sa, c0 + t, tmp) : 0;
-                int64_t chunk_total;
-                const int64_t incl = epi_scan(n, scan_scratch, &chunk_total) + seen;
-                if (n > 0 && incl - n <= t0 && t0 < incl) {
-                    part[0] = c0 + t;
-                    part[1] = static_cast<int32_t>(t0 - (incl - n));
+        if (nseg <= 256) {
+            const int n = (t < nseg) ? seg_load(sa, t, tmp) : 0;
+            int64_t total;
+            const int64_t incl = epi_scan(n, scan_scratch, &total);
+            const int64_t t0 = total * blockIdx.x / gridDim.x;
+            const int64_t t1 = total * (blockIdx.x + 1) / gridDim.x;
+            if (t == 0) {
+                part[0] = nseg;
+                part[1] = 0;
+                part[2] = static_cast<int32_t>(t1 - t0);
+            }
+            asm volatile("bar.sync 1, 256;" ::: "memory");   // the defaults above before the search result
+            if (t1 > t0 && n > 0 && incl - n <= t0 && t0 < incl) {
+                part[0] = t;
+                part[1] = static_cast<int32_t>(t0 - (incl - n));
+            }
+        } else {
+            int64_t mine = 0;
+            for (int sidx = t; sidx < nseg; sidx += 256) mine += seg_load(sa, sidx, tmp);
+            int64_t total;
+            epi_scan(mine, scan_scratch, &total);
+            const int64_t t0 = total * blockIdx.x / gridDim.x;
+            const int64_t t1 = total * (blockIdx.x + 1) / gridDim.x;
+            if (t == 0) {
+                part[0] = nseg;
+                part[1] = 0;
+                part[2] = static_cast<int32_t>(t1 - t0);
+            }
+            if (t1 > t0) {
+                int64_t seen = 0;
+                for (int c0 = 0; c0 < nseg; c0 += 256) {
+                    const int n = (c0 + t < nseg) ? seg_load(sa, c0 + t, tmp) : 0;
+                    int64_t chunk_total;
+                    const int64_t incl = epi_scan(n, scan_scratch, &chunk_total) + seen;
+                    if (n > 0 && incl - n <= t0 && t0 < incl) {
+                        part[0] = c0 + t;
+                        part[1] = static_cast<int32_t>(t0 - (incl - n));
+                    }
+                    seen += chunk_total;
+                    if (seen > t0) break;
                 }
-                seen += chunk_total;
-                if (seen > t0) break;
             }
         }
     }
