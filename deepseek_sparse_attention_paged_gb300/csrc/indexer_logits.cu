@@ -233,6 +233,7 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const SegArgs sa{seq_lens, cu_q, B, G, R, row_begin, row_end};
+    ptx::griddep_launch_dependents();   // the top-k kernel may be scheduled; it waits for this grid
     const int nseg = B * G;
 
     if (threadIdx.x == 0) {

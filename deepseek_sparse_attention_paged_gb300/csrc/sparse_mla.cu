@@ -252,6 +252,7 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
     if (warp >= kProducerWarp0) {
         // ---------------------------------------------------------------- producers
         const int pw = warp - kProducerWarp0;
+        ptx::griddep_wait();   // launched as a programmatic dependent: the top-k indices are complete
         // lane l < 16 owns entry 16 pw + l of every tile.  Batches of kBatch tiles: positions are
         // loaded two batches ahead and page ids one batch ahead, so no load waits on another on the
         // critical path.
@@ -656,13 +657,17 @@ extern "C" dsa_status dsa_sparse_mla_decode(const void* q_bf16, const void* kv_p
     cfg.blockDim = dim3(kMlaThreads, 1, 1);
     cfg.dynamicSmemBytes = kMlaSmemBytes;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    // clusters of 2; a programmatic dependent of the previous kernel on the stream (top-k): barrier
+    // setup, TMEM allocation and the query load overlap it, the index reads wait for it
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, sparse_mla_umma_kernel, static_cast<const uint16_t*>(kv_pool),
                            static_cast<const uint16_t*>(q_bf16), num_pages, block_table, static_cast<int>(max_pages),
                            seq_lens, cu_q, static_cast<int>(B), idx, static_cast<int>(k), static_cast<int>(H), scale,

@@ -11,6 +11,7 @@
 // how many of the keys equal to K are kept; a final pass in index order writes every index with
 // key > K plus the first (by index) of those equal to K.  The row is read 4 times, from L2.
 #include "dsa_common.cuh"
+#include "sm100_ptx.cuh"
 
 namespace dsa {
 namespace {
@@ -85,6 +86,8 @@ __global__ void __launch_bounds__(kTopkThreads)
 topk_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* __restrict__ seq_lens,
             const int32_t* __restrict__ cu_q, int B, int row_begin, int k, int32_t* __restrict__ idx) {
     __shared__ TopkSmem sm;
+    ptx::griddep_wait();   // launched as a programmatic dependent: the logits are complete from here on
+    ptx::griddep_launch_dependents();
     const int rl = blockIdx.x;                  // local row
     const int r = row_begin + rl;
     const int b = row_request(cu_q, B, r);
@@ -196,6 +199,8 @@ topk_bitmap_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* 
     uint32_t* ckey = tie + words_cap;
     int32_t* cidx = reinterpret_cast<int32_t*>(ckey + kCandidateCap);
 
+    ptx::griddep_wait();   // launched as a programmatic dependent: the logits are complete from here on
+    ptx::griddep_launch_dependents();
     const int rl = blockIdx.x;
     const int r = row_begin + rl;
     const int b = row_request(cu_q, B, r);
@@ -360,17 +365,32 @@ extern "C" dsa_status dsa_topk(const float* logits, int64_t ld, const int32_t* s
     if (ld < max_seq_len) return DSA_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int words = (max_seq_len + 31) / 32;
+    // a programmatic dependent of the previous kernel on the stream (the logits kernel): its CTAs
+    // may be scheduled early and wait on the device for that kernel's results
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(row_end - row_begin), 1, 1);
+    cfg.blockDim = dim3(dsa::kTopkThreads, 1, 1);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (words <= dsa::kMaxBitmapWords) {
         const int words_cap = words < 32 ? 32 : words;
         const size_t smem = dsa::bitmap_smem_bytes(words_cap);
         if (cudaFuncSetAttribute(dsa::topk_bitmap_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem)) != cudaSuccess)
             return DSA_ERR_CUDA;
-        dsa::topk_bitmap_kernel<<<row_end - row_begin, dsa::kTopkThreads, smem, s>>>(logits, ld, seq_lens, cu_q, B,
-                                                                                      row_begin, k, idx, words_cap);
+        cfg.dynamicSmemBytes = smem;
+        if (cudaLaunchKernelEx(&cfg, dsa::topk_bitmap_kernel, logits, ld, seq_lens, cu_q, static_cast<int>(B),
+                               static_cast<int>(row_begin), static_cast<int>(k), idx, words_cap) != cudaSuccess)
+            return DSA_ERR_CUDA;
     } else {
-        dsa::topk_kernel<<<row_end - row_begin, dsa::kTopkThreads, 0, s>>>(logits, ld, seq_lens, cu_q, B, row_begin, k,
-                                                                          idx);
+        cfg.dynamicSmemBytes = 0;
+        if (cudaLaunchKernelEx(&cfg, dsa::topk_kernel, logits, ld, seq_lens, cu_q, static_cast<int>(B),
+                               static_cast<int>(row_begin), static_cast<int>(k), idx) != cudaSuccess)
+            return DSA_ERR_CUDA;
     }
     return dsa::launch_status();
 }
