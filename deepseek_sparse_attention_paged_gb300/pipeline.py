@@ -104,5 +104,56 @@ class DeviceBatch:
         self.topk(stream=stream)
         self.sparse_mla(stream=stream)
 
+    # ---- end to end: host inputs -> step -> host outputs
+    def io_inputs(self):
+        """Device tensors a serving loop refills from the host before every step (queries, head
+        gates, this step's new keys and slots, lengths, block table), in a fixed order."""
+        return [self.index_q, self.weights, self.mla_q, self.new_keys, self.new_slots, self.seq_lens, self.cu_q,
+                self.block_table]
+
+    def io_outputs(self):
+        """Device tensors a serving loop reads back after every step (attention output, lse)."""
+        return [self.out, self.lse]
+
+    def step_io(self, host_in, host_out, stream=None, graph: bool = True):
+        """One decode step end to end: copy `host_in` (pinned host tensors shaped like
+        io_inputs()) to the device, run step(), copy io_outputs() into `host_out` (pinned host
+        tensors).  With graph=True the copies and the four library calls are captured once per
+        (host_in, host_out) set as one CUDA graph and replayed on later calls; every replay moves
+        the data again.  Returns when the work is enqueued on `stream`."""
+        stream = torch.cuda.current_stream(self.device) if stream is None else stream
+        ins, outs = self.io_inputs(), self.io_outputs()
+        if len(host_in) != len(ins) or len(host_out) != len(outs):
+            raise ValueError("host_in / host_out must match io_inputs() / io_outputs()")
+
+        def enqueue():
+            for d, h in zip(ins, host_in):
+                d.copy_(h, non_blocking=True)
+            self.step(stream=torch.cuda.current_stream(self.device))
+            for h, d in zip(host_out, outs):
+                h.copy_(d, non_blocking=True)
+
+        if not graph:
+            with torch.cuda.stream(stream):
+                enqueue()
+            return
+        key = tuple(t.data_ptr() for t in host_in) + tuple(t.data_ptr() for t in host_out)
+        g = getattr(self, "_io_graphs", {}).get(key)
+        if g is None:
+            side = torch.cuda.Stream(self.device)
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                enqueue()   # one eager run first (library and allocator warm)
+            stream.wait_stream(side)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                enqueue()
+            stream.wait_stream(side)
+            if not hasattr(self, "_io_graphs"):
+                self._io_graphs = {}
+            self._io_graphs[key] = g
+        with torch.cuda.stream(stream):
+            g.replay()
+
     def device_error(self):
         return capi.dsa_read_device_error(self.dev_err)

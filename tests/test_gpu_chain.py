@@ -115,3 +115,27 @@ def test_chain_full_size_sampled_rows(name):
     got_pages = db.index_pool[torch.from_numpy(pages.astype(np.int64)).cuda()].cpu().numpy()
     assert np.array_equal(got_pages, pool[pages])
     check_rows(wl, db, rows, pool)
+
+
+def test_step_io_graph_matches_eager_step():
+    """DeviceBatch.step_io (copies + four calls as one CUDA graph) gives the eager step's outputs,
+    and replays move fresh host data every time."""
+    wl = workloads.make("tiny")
+    db = DeviceBatch(wl)
+    db.step()
+    ref_out = db.out.cpu().clone()
+    ref_lse = db.lse.cpu().clone()
+    host_in = [t.cpu().pin_memory() for t in db.io_inputs()]
+    host_out = [torch.empty_like(t, device="cpu").pin_memory() for t in db.io_outputs()]
+    for _ in range(2):   # capture, then replay
+        for h in host_out:
+            h.zero_()
+        db.step_io(host_in, host_out)
+        torch.cuda.synchronize()
+        assert torch.equal(host_out[0], ref_out) and torch.equal(host_out[1], ref_lse)
+    # a changed query on the host reaches the device on replay
+    host_in[2].copy_(-host_in[2])
+    db.step_io(host_in, host_out)
+    torch.cuda.synchronize()
+    assert not torch.equal(host_out[0], ref_out)
+    assert db.device_error() == (0, 0)
