@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle
-from deepseek_sparse_attention_paged_gb300 import workloads
+from deepseek_sparse_attention_paged_gb300 import capi, workloads
 from deepseek_sparse_attention_paged_gb300.pipeline import DeviceBatch
 
 from helpers import (bf16_to_np_f64, check_attention, check_logits, check_topk_valid, kth_gap_ok,
@@ -138,4 +138,35 @@ def test_step_io_graph_matches_eager_step():
     db.step_io(host_in, host_out)
     torch.cuda.synchronize()
     assert not torch.equal(host_out[0], ref_out)
+    assert db.device_error() == (0, 0)
+
+
+def test_back_to_back_calls_keep_stream_order():
+    """The logits, top-k and attention kernels overlap their successors' launch; a call that
+    overwrites a buffer the previous call still reads must still see stream order.  Here a second
+    top-k (on different logits, into the same idx) is enqueued right after the attention call that
+    reads idx, and a second indexer call right after the top-k that reads the logits."""
+    wl = workloads.make("tiny")
+    db = DeviceBatch(wl)
+    db.step()
+    torch.cuda.synchronize()
+    ref_out = db.out.clone()
+    ref_idx = db.idx.clone()
+    flipped = -db.logits   # made before the sequence, so that attention and top-k are adjacent launches
+    # attention reads idx, then top-k rewrites idx from reversed logits, in one stream, no sync
+    db.logits.zero_()
+    db.indexer_logits()
+    db.topk()
+    db.sparse_mla()
+    db.topk(logits=flipped)
+    torch.cuda.synchronize()
+    assert torch.equal(db.out, ref_out)            # attention used the first idx
+    assert not torch.equal(db.idx, ref_idx)        # the second top-k did run afterwards
+    # top-k reads the logits, then the indexer rewrites them with a rotated query, no sync
+    db.indexer_logits()
+    db.topk()
+    idx_first = db.idx.clone()
+    db.indexer_logits(flags=capi.DSA_Q_ROTATE)
+    torch.cuda.synchronize()
+    assert torch.equal(idx_first, ref_idx)
     assert db.device_error() == (0, 0)
