@@ -61,6 +61,11 @@ def _load():
         "dsa_oracle_rotate128": (None, [P, P]),
         "dsa_oracle_quant128": (None, [P, P, P]),
         "dsa_oracle_store_index_k": (i64, [P, P, i64, P, i64]),
+        "dsa_oracle_k_norm128": (None, [P, P, P, ctypes.c_float, ctypes.c_int, P]),
+        "dsa_oracle_rope64": (None, [P, P, ctypes.c_int, P]),
+        "dsa_oracle_store_index_k_prologue": (i64, [P, P, P, ctypes.c_float, ctypes.c_int, P, i64, P, ctypes.c_int,
+                                                    P, i64, P, i64]),
+        "dsa_oracle_rope_q": (i64, [P, P, i64, P, ctypes.c_int, i64, P]),
         "dsa_oracle_visible_len": (i32, [P, P, i32, i64]),
         "dsa_oracle_indexer_logits": (i64, [P, P, P, i64, P, i32, P, P, i32, i32, P, i64, P, i64, P]),
         "dsa_oracle_topk": (None, [P, i64, P, P, i32, P, i64, i32, P]),
@@ -154,6 +159,53 @@ def store_index_k(k_bf16: np.ndarray, slot_mapping: np.ndarray, pool: np.ndarray
     slots = _c(slot_mapping, np.int64)
     assert pool.dtype == np.uint8 and pool.flags["C_CONTIGUOUS"] and pool.shape[1] == PAGE_BYTES
     return int(_load().dsa_oracle_store_index_k(_p(k), _p(slots), k.shape[0], _p(pool), pool.shape[0]))
+
+
+def k_norm128(x_bf16: np.ndarray, w: np.ndarray, b, eps: float, rms: bool = False) -> np.ndarray:
+    """LayerNorm (or RMSNorm) of one bf16 128-vector, bf16 bits out."""
+    src = _c(x_bf16, np.uint16)
+    assert src.shape == (DI,)
+    wv = _c(w, np.float32)
+    bv = _c(np.zeros(DI) if b is None else b, np.float32)
+    out = np.empty(DI, np.uint16)
+    _load().dsa_oracle_k_norm128(_p(src), _p(wv), _p(bv), float(eps), int(bool(rms)), _p(out))
+    return out
+
+
+def rope64(x_bf16: np.ndarray, cos_sin_row: np.ndarray, neox: bool = True) -> np.ndarray:
+    """Rotary embedding of dims 0..63 of one bf16 128-vector with one cos/sin cache row."""
+    src = _c(x_bf16, np.uint16)
+    cs = _c(cos_sin_row, np.float32)
+    assert src.shape == (DI,) and cs.shape == (64,)
+    out = np.empty(DI, np.uint16)
+    _load().dsa_oracle_rope64(_p(src), _p(cs), int(bool(neox)), _p(out))
+    return out
+
+
+def store_index_k_prologue(k_raw: np.ndarray, w: np.ndarray, b, eps: float, cos_sin: np.ndarray,
+                           positions: np.ndarray, slot_mapping: np.ndarray, pool: np.ndarray, rms: bool = False,
+                           neox: bool = True) -> int:
+    """Norm, rotary embedding, rotate, quantise and scatter raw keys into ``pool`` in place."""
+    k = _c(k_raw, np.uint16).reshape(-1, DI)
+    wv = _c(w, np.float32)
+    bv = _c(np.zeros(DI) if b is None else b, np.float32)
+    cs = _c(cos_sin, np.float32).reshape(-1, 64)
+    pos = _c(positions, np.int64)
+    slots = _c(slot_mapping, np.int64)
+    assert pool.dtype == np.uint8 and pool.flags["C_CONTIGUOUS"] and pool.shape[1] == PAGE_BYTES
+    return int(_load().dsa_oracle_store_index_k_prologue(_p(k), _p(wv), _p(bv), float(eps), int(bool(rms)), _p(cs),
+                                                         cs.shape[0], _p(pos), int(bool(neox)), _p(slots),
+                                                         k.shape[0], _p(pool), pool.shape[0]))
+
+
+def rope_q(q_raw: np.ndarray, cos_sin: np.ndarray, positions: np.ndarray, neox: bool = True):
+    """Rotary embedding of every head of every query row: returns (bf16 bits [T, 64, 128], bad rows)."""
+    q = _c(q_raw, np.uint16).reshape(-1, HI, DI)
+    cs = _c(cos_sin, np.float32).reshape(-1, 64)
+    pos = _c(positions, np.int64)
+    out = np.empty_like(q)
+    bad = _load().dsa_oracle_rope_q(_p(q), _p(cs), cs.shape[0], _p(pos), int(bool(neox)), q.shape[0], _p(out))
+    return out, int(bad)
 
 
 def visible_len(seq_lens, cu_q, r: int) -> int:

@@ -202,6 +202,113 @@ int64_t dsa_oracle_store_index_k(const uint16_t* k_bf16, const int64_t* slot_map
     return bad;
 }
 
+/* ---------------------------------------------------------------- indexer key / query prologues */
+
+/* Sum of 128 fp32 values in a fixed pairwise order: blocks of 4 consecutive values as
+ * (x0 + x1) + (x2 + x3), then adjacent block sums pairwise (1+1, 2+2, 4+4, ... blocks), the left
+ * operand first.  Reading: the pages do not print the norm kernel; since the normalised key feeds
+ * the bit-exact FP8 codes, the summation order (and fp32 arithmetic) is part of the definition. */
+static float sum128_pairwise(const float* x) {
+    float s[32];
+    for (int l = 0; l < 32; ++l) s[l] = (x[4 * l] + x[4 * l + 1]) + (x[4 * l + 2] + x[4 * l + 3]);
+    for (int m = 1; m < 32; m <<= 1)
+        for (int l = 0; l < 32; l += 2 * m) s[l] = s[l] + s[l + m];
+    return s[0];
+}
+
+/* Norm of one bf16 128-vector ([idx] Indexer.k_norm: LayerNorm(head_dim) with weight and bias,
+ * eps = k_norm.variance_epsilon, or RMSNorm(head_dim) when the config's index_k_norm_type is
+ * "rms"; [sfa] indexer_select_pre_process: k_li = k_norm(wk(x))).
+ * LayerNorm: mean = sum(x) / 128; d = x - mean; var = sum(d * d) / 128; rstd = 1 / sqrt(var + eps);
+ * y = (d * rstd) * w + b.  RMSNorm: ms = sum(x * x) / 128; rstd = 1 / sqrt(ms + eps);
+ * y = (x * rstd) * w.  Reading: every step in fp32 (IEEE sqrt and division, no fused multiply-add,
+ * the pairwise sums above; the division by 128 is exact); the result is rounded to bf16, the
+ * dtype of the k_norm output the pages pass on. */
+void dsa_oracle_k_norm128(const uint16_t* in_bf16, const float* w, const float* b, float eps, int rms,
+                          uint16_t* out_bf16) {
+    float x[DI], t[DI];
+    for (int d = 0; d < DI; ++d) x[d] = bf16_bits_to_f32(in_bf16[d]);
+    if (rms) {
+        for (int d = 0; d < DI; ++d) t[d] = x[d] * x[d];
+        const float ms = sum128_pairwise(t) * (1.0f / DI);
+        const float rstd = 1.0f / sqrtf(ms + eps);
+        for (int d = 0; d < DI; ++d) out_bf16[d] = dsa_oracle_f32_to_bf16((x[d] * rstd) * w[d]);
+        return;
+    }
+    const float mean = sum128_pairwise(x) * (1.0f / DI);
+    float dv[DI];
+    for (int d = 0; d < DI; ++d) {
+        dv[d] = x[d] - mean;
+        t[d] = dv[d] * dv[d];
+    }
+    const float var = sum128_pairwise(t) * (1.0f / DI);
+    const float rstd = 1.0f / sqrtf(var + eps);
+    for (int d = 0; d < DI; ++d) out_bf16[d] = dsa_oracle_f32_to_bf16(((dv[d] * rstd) * w[d]) + b[d]);
+}
+
+/* Rotary embedding of the first 64 dims of one bf16 128-vector ([idx] rotary_emb with rotary_dim
+ * = rope_head_dim = 64 on the split [64 rope, 64 nope], fused_q_indexer_rope_first_quant;
+ * [sfa] npu_rotary_mul / rope_forward_triton_siso).  cs = the position's row of cos_sin_cache,
+ * cos in cs[0:32] and sin in cs[32:64] ([idx] NPU path: cos_sin_cache[positions].chunk(2)).
+ * neox style (default): pairs (i, i + 32): y_i = x_i c_i - x_{i+32} s_i,
+ * y_{i+32} = x_{i+32} c_i + x_i s_i; interleaved style ([sfa] GLM models): pairs (2i, 2i + 1).
+ * Reading: fp32 products and sum without fused multiply-add, rounded to bf16; dims 64 .. 127 pass
+ * through. */
+void dsa_oracle_rope64(const uint16_t* in_bf16, const float* cs, int neox, uint16_t* out_bf16) {
+    memcpy(out_bf16, in_bf16, DI * sizeof(uint16_t));
+    for (int i = 0; i < 32; ++i) {
+        const int ia = neox ? i : 2 * i, ib = neox ? i + 32 : 2 * i + 1;
+        const float a = bf16_bits_to_f32(in_bf16[ia]), b = bf16_bits_to_f32(in_bf16[ib]);
+        const float c = cs[i], sn = cs[32 + i];
+        const float ya = a * c - b * sn;
+        const float yb = b * c + a * sn;
+        out_bf16[ia] = dsa_oracle_f32_to_bf16(ya);
+        out_bf16[ib] = dsa_oracle_f32_to_bf16(yb);
+    }
+}
+
+/* Fused key prologue and store ([idx] Indexer._fused_k_prepare_and_store:
+ * fused_k_indexer_norm_rope_store(key_raw, buffer, out_cache_loc, k_norm.weight, k_norm.bias,
+ * eps, cos_sin_cache, positions, page_size), equal to fused_k_indexer_norm_rope followed by
+ * _store_index_k_cache).  Per token: norm, rotary embedding at the token's position, then the
+ * store above (rotate, quantise, scatter).  A position outside [0, max_pos) skips the token.
+ * Returns the number of skipped tokens (slot past the pool or position out of range). */
+int64_t dsa_oracle_store_index_k_prologue(const uint16_t* k_raw, const float* w, const float* b, float eps, int rms,
+                                          const float* cos_sin, int64_t max_pos, const int64_t* positions,
+                                          int neox, const int64_t* slot_mapping, int64_t n, uint8_t* pool,
+                                          int64_t num_pages) {
+    int64_t bad = 0;
+    for (int64_t t = 0; t < n; ++t) {
+        if (slot_mapping[t] < 0) continue;
+        if (positions[t] < 0 || positions[t] >= max_pos) { ++bad; continue; }
+        uint16_t nrm[DI], rop[DI];
+        dsa_oracle_k_norm128(k_raw + t * DI, w, b, eps, rms, nrm);
+        dsa_oracle_rope64(nrm, cos_sin + positions[t] * 64, neox, rop);
+        bad += dsa_oracle_store_index_k(rop, slot_mapping + t, 1, pool, num_pages);
+    }
+    return bad;
+}
+
+/* Query rotary embedding ([idx] fused_q_indexer_rope_first_quant(q, weights, gate, cos_sin_cache,
+ * positions): the rope part; the Hadamard rotation and per-head quantisation that follow are the
+ * logits call's query prologue): every head of row t at positions[t].  A row whose position is
+ * outside [0, max_pos) is copied unchanged.  Returns the number of such rows. */
+int64_t dsa_oracle_rope_q(const uint16_t* q_raw, const float* cos_sin, int64_t max_pos, const int64_t* positions,
+                          int neox, int64_t T, uint16_t* out) {
+    int64_t bad = 0;
+    for (int64_t t = 0; t < T; ++t) {
+        const int ok = positions[t] >= 0 && positions[t] < max_pos;
+        if (!ok) ++bad;
+        for (int h = 0; h < HI; ++h) {
+            const uint16_t* src = q_raw + (t * HI + h) * DI;
+            uint16_t* dst = out + (t * HI + h) * DI;
+            if (ok) dsa_oracle_rope64(src, cos_sin + positions[t] * 64, neox, dst);
+            else memcpy(dst, src, DI * sizeof(uint16_t));
+        }
+    }
+    return bad;
+}
+
 /* ---------------------------------------------------------------- causal visibility */
 
 /* Request of global query row r: the b with cu_q[b] <= r < cu_q[b+1]. */

@@ -1,0 +1,168 @@
+"""Pins of the oracle's indexer prologue steps (key norm, rotary embedding, fused key store, query
+rotary embedding) against independent definitions: numpy float64 LayerNorm / RMSNorm, complex
+multiplication, exact identities and the permutation relating the two rotary pairings."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+DI = oracle.DI
+
+
+def _bf16_bits(x):
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _f32(bits):
+    return torch.from_numpy(np.asarray(bits, np.uint16).view(np.int16)).view(torch.bfloat16).float().numpy()
+
+
+def _ulp_close(got_f32, ref_f64, ulps=1.0):
+    """|got - ref| within `ulps` bf16 units of the reference magnitude (plus a tiny absolute floor)."""
+    tol = ulps * np.maximum(np.abs(ref_f64), 1e-30) * 2.0 ** -8 + 1e-30
+    return np.all(np.abs(got_f32 - ref_f64) <= tol)
+
+
+@pytest.mark.parametrize("scale", [1e-3, 1.0, 50.0])
+def test_layernorm_matches_float64_definition(scale):
+    rng = np.random.default_rng(11)
+    for _ in range(20):
+        x = _bf16_bits(rng.standard_normal(DI) * scale + rng.standard_normal() * scale)
+        w = rng.standard_normal(DI).astype(np.float32)
+        b = rng.standard_normal(DI).astype(np.float32)
+        eps = 1e-6
+        got = _f32(oracle.k_norm128(x, w, b, eps))
+        xf = _f32(x).astype(np.float64)
+        mu = xf.mean()
+        ref = (xf - mu) / np.sqrt(((xf - mu) ** 2).mean() + eps) * w + b
+        # one bf16 rounding of a value computed in fp32 (a few fp32 ulps): within 1 bf16 ulp + slack
+        assert _ulp_close(got, ref, ulps=1.01)
+
+
+def test_layernorm_unit_affine_gives_zero_mean_unit_variance():
+    rng = np.random.default_rng(12)
+    x = _bf16_bits(rng.standard_normal(DI) * 7.0 + 3.0)
+    y = _f32(oracle.k_norm128(x, np.ones(DI, np.float32), np.zeros(DI, np.float32), 0.0)).astype(np.float64)
+    assert abs(y.mean()) < 1e-2 and abs(y.var() - 1.0) < 1e-2
+
+
+def test_layernorm_of_a_constant_vector_is_the_bias():
+    x = _bf16_bits(np.full(DI, 3.25, np.float32))
+    b = np.linspace(-1, 1, DI).astype(np.float32)
+    y = oracle.k_norm128(x, np.full(DI, 5.0, np.float32), b, 1e-6)
+    assert np.array_equal(y, _bf16_bits(b))
+
+
+def test_rmsnorm_matches_float64_definition():
+    rng = np.random.default_rng(13)
+    for _ in range(20):
+        x = _bf16_bits(rng.standard_normal(DI) * 3.0)
+        w = rng.standard_normal(DI).astype(np.float32)
+        got = _f32(oracle.k_norm128(x, w, None, 1e-6, rms=True))
+        xf = _f32(x).astype(np.float64)
+        ref = xf / np.sqrt((xf ** 2).mean() + 1e-6) * w
+        assert _ulp_close(got, ref, ulps=1.01)
+
+
+def _cos_sin(angles):
+    return np.concatenate([np.cos(angles), np.sin(angles)]).astype(np.float32)
+
+
+def test_rope_neox_matches_complex_rotation():
+    rng = np.random.default_rng(14)
+    for _ in range(20):
+        x = _bf16_bits(rng.standard_normal(DI))
+        ang = rng.uniform(-np.pi, np.pi, 32)
+        cs = _cos_sin(ang)
+        got = _f32(oracle.rope64(x, cs, neox=True)).astype(np.float64)
+        xf = _f32(x).astype(np.float64)
+        c, s = cs[:32].astype(np.float64), cs[32:].astype(np.float64)
+        z = (xf[:32] + 1j * xf[32:64]) * (c + 1j * s)
+        ref = np.concatenate([z.real, z.imag, xf[64:]])
+        err = np.abs(got - ref)
+        # each output: two fp32 products and a sum (a few fp32 ulps of the inputs), then one bf16 rounding
+        bound = np.abs(ref) * 2.0 ** -8 + 2.0 ** -20 * (np.abs(np.concatenate([xf[:32], xf[32:64]])) +
+                                                        np.abs(np.concatenate([xf[32:64], xf[:32]])) + 0).max()
+        assert np.all(err[:64] <= bound[:64] + 1e-6)
+        assert np.array_equal(got[64:], xf[64:])
+
+
+def test_rope_identity_angle_and_passthrough():
+    rng = np.random.default_rng(15)
+    x = _bf16_bits(rng.standard_normal(DI))
+    x[3] = 0x8000   # -0 (x*1 - y*0 may come out as +0: compare values, not bits)
+    cs = _cos_sin(np.zeros(32))
+    for neox in (True, False):
+        assert np.array_equal(_f32(oracle.rope64(x, cs, neox=neox)), _f32(x))
+
+
+def test_rope_interleaved_is_neox_on_permuted_dims():
+    """Interleaved pairing (2i, 2i+1) equals neox pairing (i, i+32) on dims permuted by
+    2i -> i, 2i+1 -> i+32: the same fp32 operations on the same pairs, so bit-identical."""
+    rng = np.random.default_rng(16)
+    perm = np.arange(DI)
+    perm[:64] = np.concatenate([np.arange(0, 64, 2), np.arange(1, 64, 2)])   # neox position p holds interleaved dim perm[p]
+    for _ in range(10):
+        x = _bf16_bits(rng.standard_normal(DI) * 4)
+        cs = _cos_sin(rng.uniform(-3, 3, 32))
+        inter = oracle.rope64(x, cs, neox=False)
+        neox_on_perm = oracle.rope64(x[perm], cs, neox=True)
+        back = np.empty_like(neox_on_perm)
+        back[perm] = neox_on_perm
+        assert np.array_equal(inter, back)
+
+
+def test_rope_preserves_pair_norms_and_composes_angles():
+    rng = np.random.default_rng(17)
+    x = _bf16_bits(rng.standard_normal(DI))
+    a1, a2 = rng.uniform(-1, 1, 32), rng.uniform(-1, 1, 32)
+    y1 = oracle.rope64(x, _cos_sin(a1))
+    y12 = _f32(oracle.rope64(y1, _cos_sin(a2))).astype(np.float64)
+    yd = _f32(oracle.rope64(x, _cos_sin(a1 + a2))).astype(np.float64)
+    assert np.allclose(y12, yd, rtol=2e-2, atol=2e-2)
+    xf = _f32(x).astype(np.float64)
+    yf = _f32(y1).astype(np.float64)
+    assert np.allclose(np.hypot(yf[:32], yf[32:64]), np.hypot(xf[:32], xf[32:64]), rtol=1e-2)
+
+
+def test_fused_key_store_is_norm_then_rope_then_store():
+    rng = np.random.default_rng(18)
+    n, pages, max_pos = 50, 3, 300
+    k_raw = _bf16_bits(rng.standard_normal((n, DI)) * 2 + 0.5)
+    w = rng.standard_normal(DI).astype(np.float32)
+    b = rng.standard_normal(DI).astype(np.float32)
+    cos_sin = np.stack([_cos_sin(rng.uniform(-3, 3, 32)) for _ in range(max_pos)])
+    pos = rng.integers(0, max_pos, n).astype(np.int64)
+    slots = rng.permutation(pages * 64)[:n].astype(np.int64)
+    slots[4] = -1                 # padding token
+    pos[7] = max_pos              # position out of range: skipped
+    slots[9] = pages * 64 + 1     # slot out of range: skipped
+    for rms in (False, True):
+        for neox in (True, False):
+            got = np.zeros((pages, oracle.PAGE_BYTES), np.uint8)
+            bad = oracle.store_index_k_prologue(k_raw, w, None if rms else b, 1e-6, cos_sin, pos, slots, got,
+                                                rms=rms, neox=neox)
+            assert bad == 2
+            ref = np.zeros_like(got)
+            keys = []
+            keep = [t for t in range(n) if slots[t] >= 0 and pos[t] < max_pos]
+            for t in keep:
+                nrm = oracle.k_norm128(k_raw[t], w, None if rms else b, 1e-6, rms=rms)
+                keys.append(oracle.rope64(nrm, cos_sin[pos[t]], neox=neox))
+            oracle.store_index_k(np.stack(keys), slots[keep], ref)
+            assert np.array_equal(got, ref)
+
+
+def test_query_rope_rotates_every_head_and_keeps_bad_rows():
+    rng = np.random.default_rng(19)
+    T, max_pos = 5, 40
+    q = _bf16_bits(rng.standard_normal((T, oracle.HI, DI)))
+    cos_sin = np.stack([_cos_sin(rng.uniform(-3, 3, 32)) for _ in range(max_pos)])
+    pos = np.array([0, 39, 7, -1, 40], np.int64)
+    out, bad = oracle.rope_q(q, cos_sin, pos)
+    assert bad == 2
+    for t in range(T):
+        for h in (0, 17, 63):
+            exp = oracle.rope64(q[t, h], cos_sin[pos[t]]) if 0 <= pos[t] < max_pos else q[t, h]
+            assert np.array_equal(out[t, h], exp)
