@@ -39,7 +39,7 @@ def test_topk_on_oracle_logits_tiny():
 
 @pytest.mark.parametrize("v,k", [(0, 16), (1, 16), (15, 16), (16, 16), (17, 16), (2048, 2048), (2049, 2048),
                                  (5000, 2048), (70000, 2048), (131072, 2048), (3000, 1), (3000, 1999),
-                                 (40, 3), (100, 7), (131071, 2048)])
+                                 (40, 3), (100, 7), (131071, 2048), (140000, 2048), (140000, 100)])
 def test_topk_lengths_and_ties(v, k):
     rng = np.random.default_rng(200 + v + k)
     width = max(v, 4)
