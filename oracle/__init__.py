@@ -64,7 +64,7 @@ def _load():
         "dsa_oracle_k_norm128": (None, [P, P, P, ctypes.c_float, ctypes.c_int, P]),
         "dsa_oracle_rope64": (None, [P, P, ctypes.c_int, P]),
         "dsa_oracle_store_index_k_prologue": (i64, [P, P, P, ctypes.c_float, ctypes.c_int, P, i64, P, ctypes.c_int,
-                                                    P, i64, P, i64]),
+                                                    ctypes.c_int, P, i64, P, i64]),
         "dsa_oracle_rope_q": (i64, [P, P, i64, P, ctypes.c_int, i64, P]),
         "dsa_oracle_visible_len": (i32, [P, P, i32, i64]),
         "dsa_oracle_indexer_logits": (i64, [P, P, P, i64, P, i32, P, P, i32, i32, P, i64, P, i64, P]),
@@ -184,8 +184,9 @@ def rope64(x_bf16: np.ndarray, cos_sin_row: np.ndarray, neox: bool = True) -> np
 
 def store_index_k_prologue(k_raw: np.ndarray, w: np.ndarray, b, eps: float, cos_sin: np.ndarray,
                            positions: np.ndarray, slot_mapping: np.ndarray, pool: np.ndarray, rms: bool = False,
-                           neox: bool = True) -> int:
-    """Norm, rotary embedding, rotate, quantise and scatter raw keys into ``pool`` in place."""
+                           neox: bool = True, rotate: bool = True) -> int:
+    """Norm, rotary embedding, rotate (unless ``rotate`` is False), quantise and scatter raw keys
+    into ``pool`` in place."""
     k = _c(k_raw, np.uint16).reshape(-1, DI)
     wv = _c(w, np.float32)
     bv = _c(np.zeros(DI) if b is None else b, np.float32)
@@ -194,7 +195,8 @@ def store_index_k_prologue(k_raw: np.ndarray, w: np.ndarray, b, eps: float, cos_
     slots = _c(slot_mapping, np.int64)
     assert pool.dtype == np.uint8 and pool.flags["C_CONTIGUOUS"] and pool.shape[1] == PAGE_BYTES
     return int(_load().dsa_oracle_store_index_k_prologue(_p(k), _p(wv), _p(bv), float(eps), int(bool(rms)), _p(cs),
-                                                         cs.shape[0], _p(pos), int(bool(neox)), _p(slots),
+                                                         cs.shape[0], _p(pos), int(bool(neox)), int(bool(rotate)),
+                                                         _p(slots),
                                                          k.shape[0], _p(pool), pool.shape[0]))
 
 

@@ -180,24 +180,31 @@ void dsa_oracle_quant128(const float* y, uint8_t* codes, float* scale) {
  * order inside a page): page-blocked, bytes [0, 8192) hold the 64 x 128 codes row by row,
  * bytes [8192, 8448) hold the 64 fp32 scales.
  * Returns the number of tokens whose slot pointed past the pool (those are skipped). */
+/* Quantise one bf16 key (rotated first when `rotate`) into its slot; returns 1 when the slot is
+ * past the pool (nothing written), else 0. */
+static int store_one(const uint16_t* key, int rotate, int64_t slot, uint8_t* pool, int64_t num_pages) {
+    int64_t page = slot / PAGE, row = slot % PAGE;
+    if (page >= num_pages) return 1;
+    uint16_t rot[DI];
+    float y[DI];
+    uint8_t codes[DI];
+    float s;
+    if (rotate) dsa_oracle_rotate128(key, rot);
+    else memcpy(rot, key, sizeof(rot));
+    for (int d = 0; d < DI; ++d) y[d] = bf16_bits_to_f32(rot[d]);
+    dsa_oracle_quant128(y, codes, &s);
+    uint8_t* pg = pool + page * PAGE_BYTES;
+    memcpy(pg + row * DI, codes, DI);
+    memcpy(pg + PAGE * DI + row * 4, &s, 4);
+    return 0;
+}
+
 int64_t dsa_oracle_store_index_k(const uint16_t* k_bf16, const int64_t* slot_mapping, int64_t n,
                                  uint8_t* pool, int64_t num_pages) {
     int64_t bad = 0;
     for (int64_t t = 0; t < n; ++t) {
-        int64_t slot = slot_mapping[t];
-        if (slot < 0) continue;
-        int64_t page = slot / PAGE, row = slot % PAGE;
-        if (page >= num_pages) { ++bad; continue; }
-        uint16_t rot[DI];
-        float y[DI];
-        uint8_t codes[DI];
-        float s;
-        dsa_oracle_rotate128(k_bf16 + t * DI, rot);
-        for (int d = 0; d < DI; ++d) y[d] = bf16_bits_to_f32(rot[d]);
-        dsa_oracle_quant128(y, codes, &s);
-        uint8_t* pg = pool + page * PAGE_BYTES;
-        memcpy(pg + row * DI, codes, DI);
-        memcpy(pg + PAGE * DI + row * 4, &s, 4);
+        if (slot_mapping[t] < 0) continue;
+        bad += store_one(k_bf16 + t * DI, 1, slot_mapping[t], pool, num_pages);
     }
     return bad;
 }
@@ -267,16 +274,19 @@ void dsa_oracle_rope64(const uint16_t* in_bf16, const float* cs, int neox, uint1
     }
 }
 
-/* Fused key prologue and store ([idx] Indexer._fused_k_prepare_and_store:
+/* Key prologue and store.  With `rotate` ([idx] Indexer._get_k_bf16, the path without indexer
+ * fusion: k_norm, rotary_emb on the rope dims, rotate_activation, then _store_index_k_cache):
+ * norm, rotary embedding at the token's position, then the store above (rotate, quantise,
+ * scatter).  Without it ([idx] Indexer._fused_k_prepare_and_store:
  * fused_k_indexer_norm_rope_store(key_raw, buffer, out_cache_loc, k_norm.weight, k_norm.bias,
- * eps, cos_sin_cache, positions, page_size), equal to fused_k_indexer_norm_rope followed by
- * _store_index_k_cache).  Per token: norm, rotary embedding at the token's position, then the
- * store above (rotate, quantise, scatter).  A position outside [0, max_pos) skips the token.
- * Returns the number of skipped tokens (slot past the pool or position out of range). */
+ * eps, cos_sin_cache, positions, page_size); Indexer._maybe_rotate: the fused path drops the
+ * Hadamard rotation, which is orthogonal and applied to both sides): norm, rotary embedding,
+ * quantise, scatter.  A position outside [0, max_pos) skips the token.  Returns the number of
+ * skipped tokens (slot past the pool or position out of range). */
 int64_t dsa_oracle_store_index_k_prologue(const uint16_t* k_raw, const float* w, const float* b, float eps, int rms,
                                           const float* cos_sin, int64_t max_pos, const int64_t* positions,
-                                          int neox, const int64_t* slot_mapping, int64_t n, uint8_t* pool,
-                                          int64_t num_pages) {
+                                          int neox, int rotate, const int64_t* slot_mapping, int64_t n,
+                                          uint8_t* pool, int64_t num_pages) {
     int64_t bad = 0;
     for (int64_t t = 0; t < n; ++t) {
         if (slot_mapping[t] < 0) continue;
@@ -284,7 +294,7 @@ int64_t dsa_oracle_store_index_k_prologue(const uint16_t* k_raw, const float* w,
         uint16_t nrm[DI], rop[DI];
         dsa_oracle_k_norm128(k_raw + t * DI, w, b, eps, rms, nrm);
         dsa_oracle_rope64(nrm, cos_sin + positions[t] * 64, neox, rop);
-        bad += dsa_oracle_store_index_k(rop, slot_mapping + t, 1, pool, num_pages);
+        bad += store_one(rop, rotate, slot_mapping[t], pool, num_pages);
     }
     return bad;
 }

@@ -166,3 +166,36 @@ def test_query_rope_rotates_every_head_and_keeps_bad_rows():
         for h in (0, 17, 63):
             exp = oracle.rope64(q[t, h], cos_sin[pos[t]]) if 0 <= pos[t] < max_pos else q[t, h]
             assert np.array_equal(out[t, h], exp)
+
+
+def _torch_quant(y):
+    """Per-128 FP8 quantisation written with torch library calls: scale = max(amax, 1e-4) / 448,
+    codes = e4m3fn(y / scale)."""
+    t = torch.from_numpy(np.asarray(y, np.float32))
+    s = torch.clamp(t.abs().max(), min=torch.tensor(1e-4)) / torch.tensor(448.0)
+    return (t / s).to(torch.float8_e4m3fn).view(torch.uint8).numpy(), np.float32(s.item())
+
+
+def test_fused_key_store_without_rotation_quantises_the_roped_key():
+    """The fused path without the Hadamard rotation stores e4m3(n / scale) of the normed, roped
+    key n itself; with the rotation it stores the rotated key's codes instead."""
+    rng = np.random.default_rng(20)
+    n, pages, max_pos = 40, 1, 100
+    k_raw = _bf16_bits(rng.standard_normal((n, DI)) * 3)
+    w = rng.standard_normal(DI).astype(np.float32)
+    b = rng.standard_normal(DI).astype(np.float32)
+    cos_sin = np.stack([_cos_sin(rng.uniform(-3, 3, 32)) for _ in range(max_pos)])
+    pos = rng.integers(0, max_pos, n).astype(np.int64)
+    slots = rng.permutation(pages * 64)[:n].astype(np.int64)
+    plain = np.zeros((pages, oracle.PAGE_BYTES), np.uint8)
+    assert oracle.store_index_k_prologue(k_raw, w, b, 1e-6, cos_sin, pos, slots, plain, rotate=False) == 0
+    rotated = np.zeros_like(plain)
+    assert oracle.store_index_k_prologue(k_raw, w, b, 1e-6, cos_sin, pos, slots, rotated, rotate=True) == 0
+    scales = plain[0, 64 * DI:].view(np.float32)
+    for t in range(n):
+        key = oracle.rope64(oracle.k_norm128(k_raw[t], w, b, 1e-6), cos_sin[pos[t]])
+        codes, s = _torch_quant(_f32(key))
+        row = slots[t]
+        assert np.array_equal(plain[0, row * DI:(row + 1) * DI], codes)
+        assert scales[row] == s
+    assert not np.array_equal(plain, rotated)
