@@ -365,6 +365,7 @@ def run_gpu(args):
     # e2e: same step through the public API with host buffers (pinned), copies inside the timing
     e2e = run_e2e(db, stream, args, flush)
     clk.__exit__(None, None, None)
+    prologues = run_prologues(wl, stream, flush, stage_iters) if rank == 0 else None
 
     if rank != 0:
         return
@@ -398,7 +399,57 @@ def run_gpu(args):
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": timed_launches, "kernels_per_step": step_kernels,
             "clocks": clk.summary(), "stages": stages, "wall_s_timed_region": t_wall}
+    hbm_peak = hbm
+    for v in prologues.values():
+        v["hbm_frac"] = v["gbs"] / hbm_peak
+    line["indexer_prologues"] = prologues
     print(json.dumps(line), flush=True)
+
+
+def run_prologues(wl, stream, flush, iters):
+    """Time the indexer prologue calls (key norm + rotary + rotate/quantise/store, and the query
+    rotary embedding) at the decode shape of `wl` (its new keys, its query rows) and at a bulk,
+    HBM-bound shape (a 131072-token prompt: keys at positions 0 .. 131071; 8192 query rows), each
+    call alone in a CUDA graph, L2 flushed before every replay.  Algorithmic bytes: key prologue
+    256 (raw key) + 256 (cos/sin row) + 16 (position, slot) read + 132 written per token; query
+    rotary 64 x 256 read + 64 x 256 written + 256 + 8 read per row."""
+    import numpy as np
+    import torch
+    from deepseek_sparse_attention_paged_gb300 import capi
+    g = torch.Generator().manual_seed(wl.seed + 77)
+    max_pos = 163840
+    inv = 10000.0 ** (-torch.arange(0, 64, 2, dtype=torch.float64) / 64.0)
+    ang = torch.arange(max_pos, dtype=torch.float64)[:, None] * inv[None, :]
+    cos_sin = torch.cat([ang.cos(), ang.sin()], dim=1).float().cuda()
+    w = (1.0 + 0.1 * torch.randn(128, generator=g)).float().cuda()
+    b = (0.1 * torch.randn(128, generator=g)).float().cuda()
+    out = {}
+
+    def key_case(n, positions, pages):
+        k = torch.randn(n, 128, generator=g).to(torch.bfloat16).cuda()
+        slots = torch.randperm(pages * 64, generator=g)[:n].cuda()
+        pool = torch.zeros(pages, capi.INDEX_PAGE_BYTES, dtype=torch.uint8, device="cuda")
+        pos = positions.cuda()
+        gr, _ = capture(lambda: capi.dsa_store_index_k_prologue(k, w, b, 1e-6, cos_sin, pos, slots, pool), stream)
+        ms = sum(time_graph(gr, stream, iters, flush)) / iters
+        by = n * (256 + 256 + 16 + 132)
+        return {"tokens": n, "us": ms * 1e3, "algorithmic_bytes": by, "gbs": by / (ms * 1e-3) / 1e9}
+
+    def q_case(T):
+        q = torch.randn(T, 64, 128, generator=g).to(torch.bfloat16).cuda()
+        qo = torch.empty_like(q)
+        pos = torch.randint(0, max_pos, (T,), generator=g).cuda()
+        gr, _ = capture(lambda: capi.dsa_indexer_rope_q(q, cos_sin, pos, qo), stream)
+        ms = sum(time_graph(gr, stream, iters, flush)) / iters
+        by = T * (64 * 256 * 2 + 256 + 8)
+        return {"rows": T, "us": ms * 1e3, "algorithmic_bytes": by, "gbs": by / (ms * 1e-3) / 1e9}
+
+    new_pos = torch.from_numpy((wl.seq_lens.astype(np.int64) - 1) % max_pos)
+    out["store_prologue_decode"] = key_case(wl.B, new_pos, max(1, (wl.B + 63) // 64) * 4)
+    out["store_prologue_bulk"] = key_case(131072, torch.arange(131072), 131072 // 64)
+    out["rope_q_decode"] = q_case(wl.T)
+    out["rope_q_bulk"] = q_case(8192)
+    return out
 
 
 def run_e2e(db, stream, args, flush):

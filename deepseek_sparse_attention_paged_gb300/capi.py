@@ -28,7 +28,11 @@ DSA_DEVERR_SLOT_RANGE = 0x1
 DSA_DEVERR_PAGE_RANGE = 0x2
 DSA_DEVERR_INDEX_RANGE = 0x4
 DSA_DEVERR_TIMEOUT = 0x8
+DSA_DEVERR_POSITION = 0x10
 DSA_Q_ROTATE = 0x1
+DSA_NORM_RMS = 0x2
+DSA_ROPE_INTERLEAVED = 0x4
+DSA_K_NO_ROTATE = 0x8
 PAGE_SIZE = 64
 INDEX_PAGE_BYTES = 64 * 132
 LATENT_DIM = 576
@@ -70,6 +74,9 @@ def load(path: str = LIB_PATH):
     sigs = {
         "dsa_status_str": (ctypes.c_char_p, [ctypes.c_int]),
         "dsa_store_index_k": (ctypes.c_int, [P, P, i64, P, i64, i32, P, P]),
+        "dsa_store_index_k_prologue": (ctypes.c_int, [P, P, P, ctypes.c_float, P, i64, P, P, i64, P, i64, i32, u32,
+                                                      P, P]),
+        "dsa_indexer_rope_q": (ctypes.c_int, [P, P, i64, P, i64, u32, P, P, P]),
         "dsa_indexer_logits_workspace_size": (sz, [i32]),
         "dsa_indexer_logits": (ctypes.c_int, [P, P, P, i64, P, i32, P, P, i32, i32, i32, i32, i32, P, i64, u32,
                                               P, sz, P, P]),
@@ -144,6 +151,58 @@ def dsa_store_index_k(k_bf16: torch.Tensor, slot_mapping: torch.Tensor, index_k_
         _ptr(k_bf16), _ptr(slot_mapping), k_bf16.shape[0], _ptr(index_k_pool), index_k_pool.shape[0], PAGE_SIZE,
         _ptr(dev_err), _stream(stream)))
     _count(1 if k_bf16.shape[0] > 0 else 0)
+
+
+def dsa_store_index_k_prologue(k_raw_bf16: torch.Tensor, norm_weight: torch.Tensor,
+                               norm_bias: Optional[torch.Tensor], eps: float, cos_sin_cache: torch.Tensor,
+                               positions: torch.Tensor, slot_mapping: torch.Tensor, index_k_pool: torch.Tensor,
+                               flags: int = 0, dev_err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Key norm (LayerNorm, or RMSNorm with DSA_NORM_RMS), rotary embedding at `positions`, then
+    the rotate / quantise / paged store of dsa_store_index_k (no rotation with DSA_K_NO_ROTATE)."""
+    lib = load()
+    _cuda(k_raw_bf16, torch.bfloat16, "k_raw_bf16")
+    _cuda(norm_weight, torch.float32, "norm_weight")
+    if not flags & DSA_NORM_RMS:
+        _need(norm_bias is not None, "LayerNorm needs norm_bias")
+    if norm_bias is not None:
+        _cuda(norm_bias, torch.float32, "norm_bias")
+        _need(norm_bias.numel() == 128, "norm_bias must have 128 entries")
+    _cuda(cos_sin_cache, torch.float32, "cos_sin_cache")
+    _cuda(positions, torch.int64, "positions")
+    _cuda(slot_mapping, torch.int64, "slot_mapping")
+    _cuda(index_k_pool, torch.uint8, "index_k_pool")
+    _need(k_raw_bf16.dim() == 2 and k_raw_bf16.shape[1] == 128, "k_raw_bf16 must be [n, 128]")
+    _need(norm_weight.numel() == 128, "norm_weight must have 128 entries")
+    _need(cos_sin_cache.dim() == 2 and cos_sin_cache.shape[1] == 64, "cos_sin_cache must be [max_position, 64]")
+    n = k_raw_bf16.shape[0]
+    _need(positions.numel() == n and slot_mapping.numel() == n, "positions / slot_mapping must have n entries")
+    _need(index_k_pool.dim() == 2 and index_k_pool.shape[1] == INDEX_PAGE_BYTES, "pool must be [pages, 8448]")
+    _check("dsa_store_index_k_prologue", lib.dsa_store_index_k_prologue(
+        _ptr(k_raw_bf16), _ptr(norm_weight), _ptr(norm_bias), float(eps), _ptr(cos_sin_cache),
+        cos_sin_cache.shape[0], _ptr(positions), _ptr(slot_mapping), n, _ptr(index_k_pool), index_k_pool.shape[0],
+        PAGE_SIZE, flags, _ptr(dev_err), _stream(stream)))
+    _count(1 if n > 0 else 0)
+
+
+def dsa_indexer_rope_q(q_raw_bf16: torch.Tensor, cos_sin_cache: torch.Tensor, positions: torch.Tensor,
+                       q_out_bf16: torch.Tensor, flags: int = 0, dev_err: Optional[torch.Tensor] = None,
+                       stream=None) -> None:
+    """Rotary embedding of the first 64 dims of every head of the indexer query [T, 64, 128]
+    (q_out_bf16 may be q_raw_bf16)."""
+    lib = load()
+    _cuda(q_raw_bf16, torch.bfloat16, "q_raw_bf16")
+    _cuda(q_out_bf16, torch.bfloat16, "q_out_bf16")
+    _cuda(cos_sin_cache, torch.float32, "cos_sin_cache")
+    _cuda(positions, torch.int64, "positions")
+    _need(q_raw_bf16.dim() == 3 and tuple(q_raw_bf16.shape[1:]) == (64, 128), "q_raw_bf16 must be [T, 64, 128]")
+    _need(q_out_bf16.shape == q_raw_bf16.shape, "q_out_bf16 must match q_raw_bf16")
+    _need(cos_sin_cache.dim() == 2 and cos_sin_cache.shape[1] == 64, "cos_sin_cache must be [max_position, 64]")
+    T = q_raw_bf16.shape[0]
+    _need(positions.numel() == T, "positions must have T entries")
+    _check("dsa_indexer_rope_q", lib.dsa_indexer_rope_q(
+        _ptr(q_raw_bf16), _ptr(cos_sin_cache), cos_sin_cache.shape[0], _ptr(positions), T, flags,
+        _ptr(q_out_bf16), _ptr(dev_err), _stream(stream)))
+    _count(1 if T > 0 else 0)
 
 
 def dsa_indexer_logits(q_bf16: torch.Tensor, weights: torch.Tensor, index_k_pool: torch.Tensor,

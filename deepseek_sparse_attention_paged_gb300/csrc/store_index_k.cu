@@ -22,24 +22,25 @@ namespace {
 // fp32 value nearest to 1/sqrt(128) = 2^-3.5.
 constexpr float kInvSqrt128 = 0x1.6a09e6p-4f;
 
-__global__ void __launch_bounds__(256)
-store_index_k_kernel(const uint16_t* __restrict__ keys, const int64_t* __restrict__ slots, int64_t n,
-                     uint8_t* __restrict__ pool, int64_t num_pages, int32_t* err) {
-    const int64_t token = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (token >= n) return;                      // warp-uniform
-    const int64_t slot = __ldg(slots + token);
-    if (slot < 0) return;                        // padding token
-    const int64_t page = slot >> 6;
-    const int row = static_cast<int>(slot & 63);
-    if (page >= num_pages) {
-        if (lane == 0) raise_error(err, DSA_DEVERR_SLOT_RANGE);
-        return;
+// Quantise and store one key held by a warp (lane l: elements 4l .. 4l+3, exact fp32 values of
+// bf16 numbers) at row `row` of page `pg`.
+__device__ __forceinline__ void quant_store(const float (&y)[4], int lane, uint8_t* __restrict__ pg, int row) {
+    float amax = fmaxf(fmaxf(fabsf(y[0]), fabsf(y[1])), fmaxf(fabsf(y[2]), fabsf(y[3])));
+    amax = warp_max(amax);
+    const float scale = __fdiv_rn(fmaxf(amax, 1e-4f), 448.0f);
+
+    uint32_t packed = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(__fdiv_rn(y[e], scale), __NV_SATFINITE, __NV_E4M3);
+        packed |= static_cast<uint32_t>(c) << (8 * e);
     }
+    reinterpret_cast<uint32_t*>(pg + row * kIndexDim)[lane] = packed;
+    if (lane == 0) reinterpret_cast<float*>(pg + kIndexScaleOffset)[row] = scale;
+}
 
-    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(keys + token * kIndexDim) + lane);
-    float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
-
+// Rotate, quantise and store one key held by a warp (layout as above).
+__device__ __forceinline__ void rotate_quant_store(float (&x)[4], int lane, uint8_t* __restrict__ pg, int row) {
     // h = 1: pairs (0,1), (2,3) of this lane's elements
     {
         float a = x[0], b = x[1];
@@ -70,20 +71,168 @@ store_index_k_kernel(const uint16_t* __restrict__ keys, const int64_t* __restric
     float y[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) y[e] = __bfloat162float(__float2bfloat16_rn(__fmul_rn(x[e], kInvSqrt128)));
+    quant_store(y, lane, pg, row);
+}
 
-    float amax = fmaxf(fmaxf(fabsf(y[0]), fabsf(y[1])), fmaxf(fabsf(y[2]), fabsf(y[3])));
-    amax = warp_max(amax);
-    const float scale = __fdiv_rn(fmaxf(amax, 1e-4f), 448.0f);
+__global__ void __launch_bounds__(256)
+store_index_k_kernel(const uint16_t* __restrict__ keys, const int64_t* __restrict__ slots, int64_t n,
+                     uint8_t* __restrict__ pool, int64_t num_pages, int32_t* err) {
+    const int64_t token = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (token >= n) return;                      // warp-uniform
+    const int64_t slot = __ldg(slots + token);
+    if (slot < 0) return;                        // padding token
+    const int64_t page = slot >> 6;
+    const int row = static_cast<int>(slot & 63);
+    if (page >= num_pages) {
+        if (lane == 0) raise_error(err, DSA_DEVERR_SLOT_RANGE);
+        return;
+    }
 
-    uint32_t packed = 0;
+    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(keys + token * kIndexDim) + lane);
+    float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
+    rotate_quant_store(x, lane, pool + page * kIndexPageBytes, row);
+}
+
+// ---------------------------------------------------------------- key norm and rotary embedding
+
+__device__ __forceinline__ float round_bf16(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
+// Sum of the 128 values a warp holds (lane l: v[0..3] = elements 4l .. 4l+3) in one fixed order:
+// ((v0 + v1) + (v2 + v3)) inside each lane, then a pairwise tree over lanes (distance 1, 2, 4, 8,
+// 16).  At each level a lane adds its partner's partial to its own; both lanes of a pair add the
+// same two numbers, so every lane ends with the same bits, those of the tree rooted at lane 0.
+__device__ __forceinline__ float warp_sum128_tree(const float (&v)[4]) {
+    float s = __fadd_rn(__fadd_rn(v[0], v[1]), __fadd_rn(v[2], v[3]));
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, m));
+    return s;
+}
+
+// In place: LayerNorm (rms = false: y = ((x - mean) * rstd) * w + b) or RMSNorm (rms = true:
+// y = (x * rstd) * w) of the 128-vector a warp holds, every step an IEEE fp32 operation without
+// fused multiply-add, rstd = 1 / sqrt(var + eps), the result rounded to bf16.
+__device__ __forceinline__ void warp_norm128(float (&x)[4], int lane, const float* __restrict__ w,
+                                             const float* __restrict__ b, float eps, bool rms) {
+    const float4 wv = __ldg(reinterpret_cast<const float4*>(w) + lane);
+    const float wl[4] = {wv.x, wv.y, wv.z, wv.w};
+    float t[4];
+    if (rms) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) t[e] = __fmul_rn(x[e], x[e]);
+        const float ms = __fmul_rn(warp_sum128_tree(t), 1.0f / kIndexDim);
+        const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[e] = round_bf16(__fmul_rn(__fmul_rn(x[e], rstd), wl[e]));
+        return;
+    }
+    const float4 bv = __ldg(reinterpret_cast<const float4*>(b) + lane);
+    const float bl[4] = {bv.x, bv.y, bv.z, bv.w};
+    const float mean = __fmul_rn(warp_sum128_tree(x), 1.0f / kIndexDim);
+    float d[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(__fdiv_rn(y[e], scale), __NV_SATFINITE, __NV_E4M3);
-        packed |= static_cast<uint32_t>(c) << (8 * e);
+        d[e] = __fsub_rn(x[e], mean);
+        t[e] = __fmul_rn(d[e], d[e]);
     }
-    uint8_t* pg = pool + page * kIndexPageBytes;
-    reinterpret_cast<uint32_t*>(pg + row * kIndexDim)[lane] = packed;
-    if (lane == 0) reinterpret_cast<float*>(pg + kIndexScaleOffset)[row] = scale;
+    const float var = __fmul_rn(warp_sum128_tree(t), 1.0f / kIndexDim);
+    const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, eps)));
+#pragma unroll
+    for (int e = 0; e < 4; ++e) x[e] = round_bf16(__fadd_rn(__fmul_rn(__fmul_rn(d[e], rstd), wl[e]), bl[e]));
+}
+
+// In place: rotary embedding of dims 0 .. 63 of the 128-vector a warp holds (exact fp32 values
+// of bf16 numbers), cs = the position's cos/sin row (cos in cs[0:32], sin in cs[32:64]).  neox
+// pairing (i, i + 32): lane l < 8 holds i = 4l + e and lane l + 8 holds i + 32, exchanged with
+// one shuffle; interleaved pairing (2i, 2i + 1): both halves in one lane.  ya = a c - b s,
+// yb = b c + a s in fp32 without fused multiply-add, rounded to bf16; dims 64 .. 127 (lanes
+// 16 .. 31) pass through.
+__device__ __forceinline__ void warp_rope64(float (&x)[4], int lane, const float* __restrict__ cs, bool neox) {
+    if (neox) {
+        float other[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) other[e] = __shfl_xor_sync(0xffffffffu, x[e], 8);
+        if (lane >= 16) return;
+        const int i0 = 4 * (lane & 7);
+        const float4 c = __ldg(reinterpret_cast<const float4*>(cs + i0));
+        const float4 s = __ldg(reinterpret_cast<const float4*>(cs + 32 + i0));
+        const float cl[4] = {c.x, c.y, c.z, c.w}, sl[4] = {s.x, s.y, s.z, s.w};
+        if (lane < 8) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                x[e] = round_bf16(__fsub_rn(__fmul_rn(x[e], cl[e]), __fmul_rn(other[e], sl[e])));
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                x[e] = round_bf16(__fadd_rn(__fmul_rn(x[e], cl[e]), __fmul_rn(other[e], sl[e])));
+        }
+        return;
+    }
+    if (lane >= 16) return;
+    const float2 c = __ldg(reinterpret_cast<const float2*>(cs + 2 * lane));
+    const float2 s = __ldg(reinterpret_cast<const float2*>(cs + 32 + 2 * lane));
+    const float cl[2] = {c.x, c.y}, sl[2] = {s.x, s.y};
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+        const float a = x[2 * p], bb = x[2 * p + 1];
+        x[2 * p] = round_bf16(__fsub_rn(__fmul_rn(a, cl[p]), __fmul_rn(bb, sl[p])));
+        x[2 * p + 1] = round_bf16(__fadd_rn(__fmul_rn(bb, cl[p]), __fmul_rn(a, sl[p])));
+    }
+}
+
+__global__ void __launch_bounds__(256)
+store_index_k_prologue_kernel(const uint16_t* __restrict__ keys, const float* __restrict__ norm_w,
+                              const float* __restrict__ norm_b, float eps, const float* __restrict__ cos_sin,
+                              int64_t max_position, const int64_t* __restrict__ positions,
+                              const int64_t* __restrict__ slots, int64_t n, uint8_t* __restrict__ pool,
+                              int64_t num_pages, uint32_t flags, int32_t* err) {
+    const int64_t token = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (token >= n) return;                      // warp-uniform
+    const int64_t slot = __ldg(slots + token);
+    if (slot < 0) return;                        // padding token
+    const int64_t pos = __ldg(positions + token);
+    if (pos < 0 || pos >= max_position) {
+        if (lane == 0) raise_error(err, DSA_DEVERR_POSITION);
+        return;
+    }
+    const int64_t page = slot >> 6;
+    const int row = static_cast<int>(slot & 63);
+    if (page >= num_pages) {
+        if (lane == 0) raise_error(err, DSA_DEVERR_SLOT_RANGE);
+        return;
+    }
+    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(keys + token * kIndexDim) + lane);
+    float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
+    warp_norm128(x, lane, norm_w, norm_b, eps, (flags & DSA_NORM_RMS) != 0);
+    warp_rope64(x, lane, cos_sin + pos * 64, (flags & DSA_ROPE_INTERLEAVED) == 0);
+    if (flags & DSA_K_NO_ROTATE) quant_store(x, lane, pool + page * kIndexPageBytes, row);
+    else rotate_quant_store(x, lane, pool + page * kIndexPageBytes, row);
+}
+
+// One warp per (row, head) vector of the indexer query: rotary embedding at the row's position,
+// written as bf16; a row whose position is out of range is copied unchanged.
+__global__ void __launch_bounds__(256)
+indexer_rope_q_kernel(const uint16_t* q, const float* __restrict__ cos_sin, int64_t max_position,
+                      const int64_t* __restrict__ positions, int64_t vectors, uint32_t flags, uint16_t* out,
+                      int32_t* err) {
+    const int64_t v = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (v >= vectors) return;                    // warp-uniform
+    const int64_t pos = __ldg(positions + v / kIndexHeads);
+    // q and out may be the same array: each lane reads its 8 bytes before it writes them
+    const uint2 raw = reinterpret_cast<const uint2*>(q + v * kIndexDim)[lane];
+    uint2* dst = reinterpret_cast<uint2*>(out + v * kIndexDim) + lane;
+    if (pos < 0 || pos >= max_position) {
+        *dst = raw;
+        if (lane == 0 && (v % kIndexHeads) == 0) raise_error(err, DSA_DEVERR_POSITION);
+        return;
+    }
+    float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
+    warp_rope64(x, lane, cos_sin + pos * 64, (flags & DSA_ROPE_INTERLEAVED) == 0);
+    // every value is an exact bf16 number: its bits are the top half of the fp32 word
+    *dst = make_uint2((__float_as_uint(x[0]) >> 16) | (__float_as_uint(x[1]) & 0xffff0000u),
+                      (__float_as_uint(x[2]) >> 16) | (__float_as_uint(x[3]) & 0xffff0000u));
 }
 
 }  // namespace
@@ -101,5 +250,51 @@ extern "C" dsa_status dsa_store_index_k(const void* k_bf16, const int64_t* slot_
     if (blocks > 0x7fffffffLL) return DSA_ERR_INVALID_ARG;
     dsa::store_index_k_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint16_t*>(k_bf16), slot_mapping, n, index_k_pool, num_pages, dev_err);
+    return dsa::launch_status();
+}
+
+
+extern "C" dsa_status dsa_store_index_k_prologue(const void* k_raw_bf16, const float* norm_weight,
+                                                 const float* norm_bias, float eps, const float* cos_sin_cache,
+                                                 int64_t max_position, const int64_t* positions,
+                                                 const int64_t* slot_mapping, int64_t n, uint8_t* index_k_pool,
+                                                 int64_t num_pages, int32_t page_size, uint32_t flags,
+                                                 int32_t* dev_err, void* stream) {
+    if (n < 0 || num_pages < 0 || max_position < 0) return DSA_ERR_INVALID_ARG;
+    if (page_size != dsa::kPage) return DSA_ERR_UNSUPPORTED;
+    if (flags & ~static_cast<uint32_t>(DSA_NORM_RMS | DSA_ROPE_INTERLEAVED | DSA_K_NO_ROTATE))
+        return DSA_ERR_INVALID_ARG;
+    if (n == 0) return DSA_OK;
+    const bool rms = (flags & DSA_NORM_RMS) != 0;
+    if (!k_raw_bf16 || !norm_weight || (!rms && !norm_bias) || !cos_sin_cache || !positions || !slot_mapping ||
+        !index_k_pool)
+        return DSA_ERR_INVALID_ARG;
+    if (!dsa::aligned16(k_raw_bf16) || !dsa::aligned16(index_k_pool) || !dsa::aligned16(norm_weight) ||
+        (!rms && !dsa::aligned16(norm_bias)) || !dsa::aligned16(cos_sin_cache))
+        return DSA_ERR_INVALID_ARG;
+    const int64_t blocks = (n + 7) / 8;
+    if (blocks > 0x7fffffffLL) return DSA_ERR_INVALID_ARG;
+    dsa::store_index_k_prologue_kernel<<<static_cast<unsigned>(blocks), 256, 0,
+                                         static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t*>(k_raw_bf16), norm_weight, rms ? nullptr : norm_bias, eps, cos_sin_cache,
+        max_position, positions, slot_mapping, n, index_k_pool, num_pages, flags, dev_err);
+    return dsa::launch_status();
+}
+
+extern "C" dsa_status dsa_indexer_rope_q(const void* q_raw_bf16, const float* cos_sin_cache, int64_t max_position,
+                                         const int64_t* positions, int64_t T, uint32_t flags, void* q_out_bf16,
+                                         int32_t* dev_err, void* stream) {
+    if (T < 0 || max_position < 0) return DSA_ERR_INVALID_ARG;
+    if (flags & ~static_cast<uint32_t>(DSA_ROPE_INTERLEAVED)) return DSA_ERR_INVALID_ARG;
+    if (T == 0) return DSA_OK;
+    if (!q_raw_bf16 || !cos_sin_cache || !positions || !q_out_bf16) return DSA_ERR_INVALID_ARG;
+    if (!dsa::aligned16(q_raw_bf16) || !dsa::aligned16(q_out_bf16) || !dsa::aligned16(cos_sin_cache))
+        return DSA_ERR_INVALID_ARG;
+    const int64_t vectors = T * dsa::kIndexHeads;
+    const int64_t blocks = (vectors + 7) / 8;
+    if (blocks > 0x7fffffffLL) return DSA_ERR_INVALID_ARG;
+    dsa::indexer_rope_q_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t*>(q_raw_bf16), cos_sin_cache, max_position, positions, vectors, flags,
+        static_cast<uint16_t*>(q_out_bf16), dev_err);
     return dsa::launch_status();
 }

@@ -8,7 +8,8 @@
  *   3. absorbed-form sparse MLA over the selected rows of a paged 576-wide bf16 latent cache
  *      (512 latent + 64 rope, one shared KV head, 512-wide latent output).
  * A fourth call writes new keys into the index-K cache (Hadamard rotation, per-token FP8
- * quantisation, paged scatter by slot).
+ * quantisation, paged scatter by slot); two prologue calls add the key norm and rotary embedding
+ * in front of that store and the rotary embedding of the indexer query.
  *
  * Conventions shared by every call
  * --------------------------------
@@ -67,9 +68,15 @@ typedef enum {
 #define DSA_DEVERR_PAGE_RANGE 0x2  /* a block-table entry outside [0, num_pages) was needed */
 #define DSA_DEVERR_INDEX_RANGE 0x4 /* a top-k index outside [0, v_r) (entry skipped) */
 #define DSA_DEVERR_TIMEOUT 0x8     /* a bounded spin-wait gave up */
+#define DSA_DEVERR_POSITION 0x10   /* a rotary position outside [0, max_position) */
 
 /* Flags of dsa_indexer_logits. */
 #define DSA_Q_ROTATE 0x1u          /* Hadamard-rotate each query head before quantising it */
+
+/* Flags of dsa_store_index_k_prologue and dsa_indexer_rope_q. */
+#define DSA_NORM_RMS 0x2u          /* key norm is RMSNorm (default: LayerNorm with bias) */
+#define DSA_ROPE_INTERLEAVED 0x4u  /* rotary pairs (2i, 2i+1) (default: neox pairs (i, i+32)) */
+#define DSA_K_NO_ROTATE 0x8u       /* key prologue: quantise without the Hadamard rotation */
 
 /* Fixed shape constants of the path. */
 #define DSA_PAGE_SIZE 64
@@ -110,6 +117,69 @@ const char* dsa_status_str(dsa_status s);
 dsa_status dsa_store_index_k(const void* k_bf16, const int64_t* slot_mapping, int64_t n,
                              uint8_t* index_k_pool, int64_t num_pages, int32_t page_size,
                              int32_t* dev_err, void* stream);
+
+/*
+ * dsa_store_index_k_prologue -- key norm, rotary embedding, then dsa_store_index_k, in one kernel.
+ * Source: sglang dsa_indexer.py, Indexer._get_k_bf16 (k_norm, rotary_emb on the first 64 (rope)
+ * dims of the 64 rope + 64 nope split, rotate_activation) followed by _store_index_k_cache;
+ * Indexer._fused_k_prepare_and_store (fused_k_indexer_norm_rope_store(key, buffer,
+ * out_cache_loc, k_norm weight / bias / eps, cos_sin_cache, positions)), which drops the Hadamard
+ * rotation (Indexer._maybe_rotate: the rotation is orthogonal and applied to both query and key)
+ * -- flag DSA_K_NO_ROTATE; Indexer.k_norm (LayerNorm over the 128 dims, RMSNorm when the model
+ * config asks for it); vllm_ascend sfa_v1.py, indexer_select_pre_process (k_norm, then rope on
+ * k_pe, then the Hadamard rotation and the slot_mapping scatter).
+ * Per token t with slot >= 0:
+ *   x = k_raw_bf16[t, 0:128];
+ *   LayerNorm: mean = S(x) / 128, d = x - mean, var = S(d * d) / 128, rstd = 1 / sqrt(var + eps),
+ *     n = bf16_rn((d * rstd) * w + b);  RMSNorm (DSA_NORM_RMS): rstd = 1 / sqrt(S(x * x) / 128 + eps),
+ *     n = bf16_rn((x * rstd) * w).  S() sums in one fixed order: ((v0 + v1) + (v2 + v3)) per group
+ *     of 4 consecutive dims, then a pairwise tree over the 32 group sums (distance 1, 2, 4, 8, 16).
+ *   Rotary: c, s = cos_sin_cache[positions[t], 0:32], [32:64]; neox pairs (a, b) = (n_i, n_{i+32})
+ *     (DSA_ROPE_INTERLEAVED: (n_{2i}, n_{2i+1})), i < 32: a' = bf16_rn(a c_i - b s_i),
+ *     b' = bf16_rn(b c_i + a s_i); dims 64 .. 127 unchanged.
+ *   Then the steps of dsa_store_index_k on the result; with DSA_K_NO_ROTATE the rotation is
+ *   skipped and the rotary output itself is quantised and stored.
+ *   Every operation is one IEEE fp32 operation (no fused multiply-add), so results are bit-exact
+ *   with the CPU definition.
+ * Arguments:
+ *   k_raw_bf16     [n, 128] bf16 (16-byte aligned): the key projection before the norm.
+ *   norm_weight    fp32 [128] (16-byte aligned).  norm_bias: fp32 [128] (16-byte aligned) for
+ *                  LayerNorm; ignored (may be NULL) with DSA_NORM_RMS.
+ *   eps            the norm's epsilon.
+ *   cos_sin_cache  fp32 [max_position, 64] (16-byte aligned): cos in [0, 32), sin in [32, 64).
+ *   positions      int64 [n].  slot_mapping int64 [n] (slot < 0: padding, skipped).
+ *   index_k_pool, num_pages, page_size  as for dsa_store_index_k.
+ *   flags          0 or a combination of DSA_NORM_RMS, DSA_ROPE_INTERLEAVED and DSA_K_NO_ROTATE.
+ *   dev_err        nullable; DSA_DEVERR_POSITION for a position outside [0, max_position),
+ *                  DSA_DEVERR_SLOT_RANGE for a slot past the pool (the token is skipped either way).
+ */
+dsa_status dsa_store_index_k_prologue(const void* k_raw_bf16, const float* norm_weight,
+                                      const float* norm_bias, float eps, const float* cos_sin_cache,
+                                      int64_t max_position, const int64_t* positions,
+                                      const int64_t* slot_mapping, int64_t n, uint8_t* index_k_pool,
+                                      int64_t num_pages, int32_t page_size, uint32_t flags,
+                                      int32_t* dev_err, void* stream);
+
+/*
+ * dsa_indexer_rope_q -- rotary embedding of the indexer query (the rope step that precedes the
+ * query prologue of dsa_indexer_logits).
+ * Source: sglang dsa_indexer.py, Indexer.forward_cuda / fused_q_indexer_rope_first_quant (rope on
+ * the first 64 dims of every head, then the Hadamard rotation and FP8 quantisation, which
+ * dsa_indexer_logits does with DSA_Q_ROTATE); vllm_ascend sfa_v1.py, indexer_select_pre_process
+ * (q_pe rope before the indexer).
+ *   Every head h of row t: the rotary step of dsa_store_index_k_prologue at positions[t].
+ *   A row whose position is outside [0, max_position) is copied unchanged and
+ *   DSA_DEVERR_POSITION is set.
+ * Arguments:
+ *   q_raw_bf16     [T, 64, 128] bf16 (16-byte aligned).  q_out_bf16: same shape (may equal
+ *                  q_raw_bf16: each vector is read before it is written by the same warp).
+ *   cos_sin_cache, max_position  as above.  positions int64 [T].
+ *   flags          0 or DSA_ROPE_INTERLEAVED.
+ * Bit-exact with the CPU definition.
+ */
+dsa_status dsa_indexer_rope_q(const void* q_raw_bf16, const float* cos_sin_cache, int64_t max_position,
+                              const int64_t* positions, int64_t T, uint32_t flags, void* q_out_bf16,
+                              int32_t* dev_err, void* stream);
 
 /*
  * dsa_indexer_logits -- lightning-indexer logits over the paged index-K cache.

@@ -55,6 +55,26 @@ def test_topk_lengths_and_ties(v, k):
     assert np.array_equal(got, ref)
 
 
+@pytest.mark.parametrize("v,k", [(70000, 2048), (70000, 1500), (9000, 2048), (131072, 100)])
+def test_topk_rows_that_mislead_the_sample(v, k):
+    """Rows whose evenly spaced sample misjudges the cut: the largest values sit on sampled
+    positions only (fewer than k keys reach the cut), everywhere but the sampled positions (far
+    more keys than fit pass it), or the row is one value with sparse outliers."""
+    S = 2048
+    sampled = (np.arange(S, dtype=np.int64) * v) // S
+    lg = np.zeros((4, v + 4), np.float32)
+    lg[0, :v] = np.random.default_rng(220).standard_normal(v).astype(np.float32) - 10.0
+    lg[0, sampled[::2]] = 50.0 + np.arange(S // 2, dtype=np.float32) * 1e-3   # large values only where sampled
+    lg[1, :v] = 100.0
+    lg[1, sampled] = -5.0                                                  # the sample sees only small values
+    lg[2, :v] = 1.0
+    lg[2, np.arange(0, v, 997)] = 2.0                                      # one value plus sparse outliers
+    lg[3, :v] = np.random.default_rng(221).standard_normal(v).astype(np.float32)
+    lg[3, sampled[::2]] = 7.0                                              # ties at the top on half the sample
+    got, ref = _gpu_topk(lg, [v] * 4, [1] * 4, k, max_seq_len=v)
+    assert np.array_equal(got, ref)
+
+
 def test_topk_next_n_rows_use_their_own_length():
     rng = np.random.default_rng(210)
     L = 3000
