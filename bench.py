@@ -495,6 +495,32 @@ def run_profile(args):
     build()
     capi.load()
     wl = workloads.make(args.workload)
+    if args.profile in ("prologue", "rope_q"):
+        # the bulk shapes of run_prologues: a 131072-token prompt's keys, 8192 query rows
+        g = torch.Generator().manual_seed(wl.seed + 77)
+        max_pos = 163840
+        inv = 10000.0 ** (-torch.arange(0, 64, 2, dtype=torch.float64) / 64.0)
+        ang = torch.arange(max_pos, dtype=torch.float64)[:, None] * inv[None, :]
+        cos_sin = torch.cat([ang.cos(), ang.sin()], dim=1).float().cuda()
+        if args.profile == "prologue":
+            n = 131072
+            k = torch.randn(n, 128, generator=g).to(torch.bfloat16).cuda()
+            w = (1.0 + 0.1 * torch.randn(128, generator=g)).float().cuda()
+            b = (0.1 * torch.randn(128, generator=g)).float().cuda()
+            slots = torch.randperm(n, generator=g).cuda()
+            pos = torch.arange(n).cuda()
+            pool = torch.zeros(n // 64, capi.INDEX_PAGE_BYTES, dtype=torch.uint8, device="cuda")
+            fn = lambda: capi.dsa_store_index_k_prologue(k, w, b, 1e-6, cos_sin, pos, slots, pool)
+        else:
+            q = torch.randn(8192, 64, 128, generator=g).to(torch.bfloat16).cuda()
+            qo = torch.empty_like(q)
+            pos = torch.randint(0, max_pos, (8192,), generator=g).cuda()
+            fn = lambda: capi.dsa_indexer_rope_q(q, cos_sin, pos, qo)
+        for _ in range(args.warmup + args.steps):
+            fn()
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": args.profile, "launches": args.warmup + args.steps}))
+        return
     need_latent = args.profile in ("mla", "step")
     db = DeviceBatch(wl, with_latent=need_latent)
     if args.profile in ("topk", "mla"):
@@ -514,7 +540,8 @@ def run_profile(args):
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
-    ap.add_argument("--profile", choices=["store", "indexer", "topk", "mla", "step"], default=None,
+    ap.add_argument("--profile", choices=["store", "indexer", "topk", "mla", "step", "prologue", "rope_q"],
+                    default=None,
                     help="launch one stage warmup+steps times without timing (for ncu) and exit")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)

@@ -80,7 +80,9 @@ store_index_k_kernel(const uint16_t* __restrict__ keys, const int64_t* __restric
     const int64_t token = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (token >= n) return;                      // warp-uniform
+    // both loads in flight before the slot is examined
     const int64_t slot = __ldg(slots + token);
+    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(keys + token * kIndexDim) + lane);
     if (slot < 0) return;                        // padding token
     const int64_t page = slot >> 6;
     const int row = static_cast<int>(slot & 63);
@@ -88,8 +90,6 @@ store_index_k_kernel(const uint16_t* __restrict__ keys, const int64_t* __restric
         if (lane == 0) raise_error(err, DSA_DEVERR_SLOT_RANGE);
         return;
     }
-
-    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(keys + token * kIndexDim) + lane);
     float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
     rotate_quant_store(x, lane, pool + page * kIndexPageBytes, row);
 }
@@ -112,9 +112,7 @@ __device__ __forceinline__ float warp_sum128_tree(const float (&v)[4]) {
 // In place: LayerNorm (rms = false: y = ((x - mean) * rstd) * w + b) or RMSNorm (rms = true:
 // y = (x * rstd) * w) of the 128-vector a warp holds, every step an IEEE fp32 operation without
 // fused multiply-add, rstd = 1 / sqrt(var + eps), the result rounded to bf16.
-__device__ __forceinline__ void warp_norm128(float (&x)[4], int lane, const float* __restrict__ w,
-                                             const float* __restrict__ b, float eps, bool rms) {
-    const float4 wv = __ldg(reinterpret_cast<const float4*>(w) + lane);
+__device__ __forceinline__ void warp_norm128(float (&x)[4], const float4 wv, const float4 bv, float eps, bool rms) {
     const float wl[4] = {wv.x, wv.y, wv.z, wv.w};
     float t[4];
     if (rms) {
@@ -126,7 +124,6 @@ __device__ __forceinline__ void warp_norm128(float (&x)[4], int lane, const floa
         for (int e = 0; e < 4; ++e) x[e] = round_bf16(__fmul_rn(__fmul_rn(x[e], rstd), wl[e]));
         return;
     }
-    const float4 bv = __ldg(reinterpret_cast<const float4*>(b) + lane);
     const float bl[4] = {bv.x, bv.y, bv.z, bv.w};
     const float mean = __fmul_rn(warp_sum128_tree(x), 1.0f / kIndexDim);
     float d[4];
@@ -141,42 +138,58 @@ __device__ __forceinline__ void warp_norm128(float (&x)[4], int lane, const floa
     for (int e = 0; e < 4; ++e) x[e] = round_bf16(__fadd_rn(__fmul_rn(__fmul_rn(d[e], rstd), wl[e]), bl[e]));
 }
 
-// In place: rotary embedding of dims 0 .. 63 of the 128-vector a warp holds (exact fp32 values
-// of bf16 numbers), cs = the position's cos/sin row (cos in cs[0:32], sin in cs[32:64]).  neox
-// pairing (i, i + 32): lane l < 8 holds i = 4l + e and lane l + 8 holds i + 32, exchanged with
-// one shuffle; interleaved pairing (2i, 2i + 1): both halves in one lane.  ya = a c - b s,
+// Rotary embedding of dims 0 .. 63 of the 128-vector a warp holds (exact fp32 values of bf16
+// numbers), from the position's cos/sin row (cos in [0, 32), sin in [32, 64)).  neox pairing
+// (i, i + 32): lane l < 8 holds i = 4l + e and lane l + 8 holds i + 32, exchanged with one
+// shuffle; interleaved pairing (2i, 2i + 1): both halves in one lane.  ya = a c - b s,
 // yb = b c + a s in fp32 without fused multiply-add, rounded to bf16; dims 64 .. 127 (lanes
 // 16 .. 31) pass through.
-__device__ __forceinline__ void warp_rope64(float (&x)[4], int lane, const float* __restrict__ cs, bool neox) {
+struct RopeCoef {
+    float c[4], s[4];   // neox: c[e], s[e] of i = 4 (lane & 7) + e; interleaved: c[p], s[p] of i = 2 lane + p
+};
+
+// This lane's cos / sin values (lanes 16 .. 31 need none).
+__device__ __forceinline__ RopeCoef load_rope(const float* __restrict__ cs, int lane, bool neox) {
+    RopeCoef r = {};
+    if (lane >= 16) return r;
+    if (neox) {
+        const int i0 = 4 * (lane & 7);
+        const float4 c = __ldg(reinterpret_cast<const float4*>(cs + i0));
+        const float4 s = __ldg(reinterpret_cast<const float4*>(cs + 32 + i0));
+        r.c[0] = c.x; r.c[1] = c.y; r.c[2] = c.z; r.c[3] = c.w;
+        r.s[0] = s.x; r.s[1] = s.y; r.s[2] = s.z; r.s[3] = s.w;
+    } else {
+        const float2 c = __ldg(reinterpret_cast<const float2*>(cs + 2 * lane));
+        const float2 s = __ldg(reinterpret_cast<const float2*>(cs + 32 + 2 * lane));
+        r.c[0] = c.x; r.c[1] = c.y;
+        r.s[0] = s.x; r.s[1] = s.y;
+    }
+    return r;
+}
+
+__device__ __forceinline__ void warp_rope64(float (&x)[4], int lane, const RopeCoef& k, bool neox) {
     if (neox) {
         float other[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) other[e] = __shfl_xor_sync(0xffffffffu, x[e], 8);
         if (lane >= 16) return;
-        const int i0 = 4 * (lane & 7);
-        const float4 c = __ldg(reinterpret_cast<const float4*>(cs + i0));
-        const float4 s = __ldg(reinterpret_cast<const float4*>(cs + 32 + i0));
-        const float cl[4] = {c.x, c.y, c.z, c.w}, sl[4] = {s.x, s.y, s.z, s.w};
         if (lane < 8) {
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-                x[e] = round_bf16(__fsub_rn(__fmul_rn(x[e], cl[e]), __fmul_rn(other[e], sl[e])));
+                x[e] = round_bf16(__fsub_rn(__fmul_rn(x[e], k.c[e]), __fmul_rn(other[e], k.s[e])));
         } else {
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-                x[e] = round_bf16(__fadd_rn(__fmul_rn(x[e], cl[e]), __fmul_rn(other[e], sl[e])));
+                x[e] = round_bf16(__fadd_rn(__fmul_rn(x[e], k.c[e]), __fmul_rn(other[e], k.s[e])));
         }
         return;
     }
     if (lane >= 16) return;
-    const float2 c = __ldg(reinterpret_cast<const float2*>(cs + 2 * lane));
-    const float2 s = __ldg(reinterpret_cast<const float2*>(cs + 32 + 2 * lane));
-    const float cl[2] = {c.x, c.y}, sl[2] = {s.x, s.y};
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
         const float a = x[2 * p], bb = x[2 * p + 1];
-        x[2 * p] = round_bf16(__fsub_rn(__fmul_rn(a, cl[p]), __fmul_rn(bb, sl[p])));
-        x[2 * p + 1] = round_bf16(__fadd_rn(__fmul_rn(bb, cl[p]), __fmul_rn(a, sl[p])));
+        x[2 * p] = round_bf16(__fsub_rn(__fmul_rn(a, k.c[p]), __fmul_rn(bb, k.s[p])));
+        x[2 * p + 1] = round_bf16(__fadd_rn(__fmul_rn(bb, k.c[p]), __fmul_rn(a, k.s[p])));
     }
 }
 
@@ -189,50 +202,75 @@ store_index_k_prologue_kernel(const uint16_t* __restrict__ keys, const float* __
     const int64_t token = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (token >= n) return;                      // warp-uniform
+    const bool rms = (flags & DSA_NORM_RMS) != 0;
+    const bool neox = (flags & DSA_ROPE_INTERLEAVED) == 0;
+    // every load that does not depend on another is in flight before anything is examined
     const int64_t slot = __ldg(slots + token);
-    if (slot < 0) return;                        // padding token
     const int64_t pos = __ldg(positions + token);
+    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(keys + token * kIndexDim) + lane);
+    const float4 wv = __ldg(reinterpret_cast<const float4*>(norm_w) + lane);
+    const float4 bv = __ldg(reinterpret_cast<const float4*>(norm_b) + lane);   // unused with RMSNorm
+    if (slot < 0) return;                        // padding token
     if (pos < 0 || pos >= max_position) {
         if (lane == 0) raise_error(err, DSA_DEVERR_POSITION);
         return;
     }
+    const RopeCoef rc = load_rope(cos_sin + pos * 64, lane, neox);   // in flight during the norm
     const int64_t page = slot >> 6;
     const int row = static_cast<int>(slot & 63);
     if (page >= num_pages) {
         if (lane == 0) raise_error(err, DSA_DEVERR_SLOT_RANGE);
         return;
     }
-    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(keys + token * kIndexDim) + lane);
     float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
-    warp_norm128(x, lane, norm_w, norm_b, eps, (flags & DSA_NORM_RMS) != 0);
-    warp_rope64(x, lane, cos_sin + pos * 64, (flags & DSA_ROPE_INTERLEAVED) == 0);
+    warp_norm128(x, wv, bv, eps, rms);
+    warp_rope64(x, lane, rc, neox);
     if (flags & DSA_K_NO_ROTATE) quant_store(x, lane, pool + page * kIndexPageBytes, row);
     else rotate_quant_store(x, lane, pool + page * kIndexPageBytes, row);
 }
 
-// One warp per (row, head) vector of the indexer query: rotary embedding at the row's position,
-// written as bf16; a row whose position is out of range is copied unchanged.
+// One warp per (row, group of HPW heads) of the indexer query: the row's cos/sin values are loaded
+// once, the group's head vectors are read up to 8 at a time (independent 256-byte loads in flight
+// per warp), rotated and written as bf16; a row whose position is out of range is copied
+// unchanged.  HPW = 16 for many rows (fewer cos/sin loads, more bytes in flight per warp), 1 for
+// few rows (more warps).
+template <int HPW>
 __global__ void __launch_bounds__(256)
 indexer_rope_q_kernel(const uint16_t* q, const float* __restrict__ cos_sin, int64_t max_position,
-                      const int64_t* __restrict__ positions, int64_t vectors, uint32_t flags, uint16_t* out,
+                      const int64_t* __restrict__ positions, int64_t T, uint32_t flags, uint16_t* out,
                       int32_t* err) {
-    const int64_t v = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    constexpr int kGroups = kIndexHeads / HPW;
+    constexpr int kBatch = HPW < 8 ? HPW : 8;
+    const int64_t wg = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    if (v >= vectors) return;                    // warp-uniform
-    const int64_t pos = __ldg(positions + v / kIndexHeads);
-    // q and out may be the same array: each lane reads its 8 bytes before it writes them
-    const uint2 raw = reinterpret_cast<const uint2*>(q + v * kIndexDim)[lane];
-    uint2* dst = reinterpret_cast<uint2*>(out + v * kIndexDim) + lane;
-    if (pos < 0 || pos >= max_position) {
-        *dst = raw;
-        if (lane == 0 && (v % kIndexHeads) == 0) raise_error(err, DSA_DEVERR_POSITION);
-        return;
+    const int64_t t = wg / kGroups;
+    if (t >= T) return;                          // warp-uniform
+    const int64_t v0 = t * kIndexHeads + (wg % kGroups) * HPW;
+    const int64_t pos = __ldg(positions + t);
+    const bool ok = pos >= 0 && pos < max_position;
+    if (!ok && lane == 0 && v0 % kIndexHeads == 0) raise_error(err, DSA_DEVERR_POSITION);
+    const bool neox = (flags & DSA_ROPE_INTERLEAVED) == 0;
+    RopeCoef rc = {};
+    if (ok) rc = load_rope(cos_sin + pos * 64, lane, neox);
+#pragma unroll 1
+    for (int h0 = 0; h0 < HPW; h0 += kBatch) {
+        // q and out may be the same array: each lane reads its 8 bytes before it writes them
+        uint2 raw[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) raw[j] = reinterpret_cast<const uint2*>(q + (v0 + h0 + j) * kIndexDim)[lane];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            uint2 y = raw[j];
+            if (ok) {
+                float x[4] = {bf16_lo(raw[j].x), bf16_hi(raw[j].x), bf16_lo(raw[j].y), bf16_hi(raw[j].y)};
+                warp_rope64(x, lane, rc, neox);
+                // every value is an exact bf16 number: its bits are the top half of the fp32 word
+                y = make_uint2((__float_as_uint(x[0]) >> 16) | (__float_as_uint(x[1]) & 0xffff0000u),
+                               (__float_as_uint(x[2]) >> 16) | (__float_as_uint(x[3]) & 0xffff0000u));
+            }
+            reinterpret_cast<uint2*>(out + (v0 + h0 + j) * kIndexDim)[lane] = y;
+        }
     }
-    float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
-    warp_rope64(x, lane, cos_sin + pos * 64, (flags & DSA_ROPE_INTERLEAVED) == 0);
-    // every value is an exact bf16 number: its bits are the top half of the fp32 word
-    *dst = make_uint2((__float_as_uint(x[0]) >> 16) | (__float_as_uint(x[1]) & 0xffff0000u),
-                      (__float_as_uint(x[2]) >> 16) | (__float_as_uint(x[3]) & 0xffff0000u));
 }
 
 }  // namespace
@@ -276,7 +314,7 @@ extern "C" dsa_status dsa_store_index_k_prologue(const void* k_raw_bf16, const f
     if (blocks > 0x7fffffffLL) return DSA_ERR_INVALID_ARG;
     dsa::store_index_k_prologue_kernel<<<static_cast<unsigned>(blocks), 256, 0,
                                          static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t*>(k_raw_bf16), norm_weight, rms ? nullptr : norm_bias, eps, cos_sin_cache,
+        static_cast<const uint16_t*>(k_raw_bf16), norm_weight, rms ? norm_weight : norm_bias, eps, cos_sin_cache,
         max_position, positions, slot_mapping, n, index_k_pool, num_pages, flags, dev_err);
     return dsa::launch_status();
 }
@@ -290,11 +328,19 @@ extern "C" dsa_status dsa_indexer_rope_q(const void* q_raw_bf16, const float* co
     if (!q_raw_bf16 || !cos_sin_cache || !positions || !q_out_bf16) return DSA_ERR_INVALID_ARG;
     if (!dsa::aligned16(q_raw_bf16) || !dsa::aligned16(q_out_bf16) || !dsa::aligned16(cos_sin_cache))
         return DSA_ERR_INVALID_ARG;
-    const int64_t vectors = T * dsa::kIndexHeads;
-    const int64_t blocks = (vectors + 7) / 8;
+    // 16 heads per warp once that still gives about 32 warps per SM, else one
+    const bool wide = T * (dsa::kIndexHeads / 16) >= 152 * 32;
+    const int64_t warps = T * (wide ? dsa::kIndexHeads / 16 : dsa::kIndexHeads);
+    const int64_t blocks = (warps + 7) / 8;
     if (blocks > 0x7fffffffLL) return DSA_ERR_INVALID_ARG;
-    dsa::indexer_rope_q_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t*>(q_raw_bf16), cos_sin_cache, max_position, positions, vectors, flags,
-        static_cast<uint16_t*>(q_out_bf16), dev_err);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const uint16_t* qi = static_cast<const uint16_t*>(q_raw_bf16);
+    uint16_t* qo = static_cast<uint16_t*>(q_out_bf16);
+    if (wide)
+        dsa::indexer_rope_q_kernel<16><<<static_cast<unsigned>(blocks), 256, 0, s>>>(qi, cos_sin_cache, max_position,
+                                                                                     positions, T, flags, qo, dev_err);
+    else
+        dsa::indexer_rope_q_kernel<1><<<static_cast<unsigned>(blocks), 256, 0, s>>>(qi, cos_sin_cache, max_position,
+                                                                                    positions, T, flags, qo, dev_err);
     return dsa::launch_status();
 }

@@ -108,9 +108,10 @@ def test_store_prologue_empty_and_bad_flags():
 
 
 @pytest.mark.parametrize("interleaved", [False, True])
-def test_rope_q_bit_exact_and_in_place(interleaved):
-    rng = np.random.default_rng(320 + interleaved)
-    T, max_pos = 37, 70000
+@pytest.mark.parametrize("T", [37, 1300])   # one head per warp / 16 heads per warp
+def test_rope_q_bit_exact_and_in_place(interleaved, T):
+    rng = np.random.default_rng(320 + interleaved + T)
+    max_pos = 70000
     q = _bf16_bits(rng.standard_normal((T, 64, 128)) * rng.uniform(0.1, 10.0, (T, 64, 1)))
     cs = _cos_sin_cache(max_pos)
     pos = rng.integers(0, max_pos, T).astype(np.int64)
