@@ -2,7 +2,8 @@
 
 This package wraps ``dsa_oracle.c``: a plain, slow, double-precision C implementation of what the
 DSA decode path computes (Hadamard rotation, FP8-E4M3 quantisation, paged index-K store,
-lightning-indexer logits, per-row top-k, absorbed sparse MLA, log-sum-exp merge).  Only ``tests/``,
+lightning-indexer logits, per-row top-k, absorbed sparse MLA, log-sum-exp merge, the indexer
+prologues, and the per-head projections around the absorbed attention).  Only ``tests/``,
 ``__graft_entry__.smoke()`` and the ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may
 import it.  The product library (``deepseek_sparse_attention_paged_gb300``) never imports, links or
 runs anything here, and the two share no code.
@@ -55,6 +56,8 @@ def _load():
     sig = {
         "dsa_oracle_f32_to_bf16": (ctypes.c_uint16, [ctypes.c_float]),
         "dsa_oracle_bf16_to_f32": (ctypes.c_float, [ctypes.c_uint16]),
+        "dsa_oracle_f64_to_bf16": (ctypes.c_uint16, [ctypes.c_double]),
+        "dsa_oracle_f64_to_bf16_array": (None, [P, i64, P]),
         "dsa_oracle_e4m3_decode": (f64, [ctypes.c_uint8]),
         "dsa_oracle_e4m3_encode": (ctypes.c_uint8, [ctypes.c_float]),
         "dsa_oracle_fwht128": (None, [P]),
@@ -289,6 +292,59 @@ def dense_mla(q_bf16, kv_bf16, block_table, seq_lens, cu_q, scale, rows):
     _load().dsa_oracle_dense_mla(_p(q), _p(kv), kv.shape[0], _p(bt), bt.shape[1], _p(sl), _p(cq),
                                  sl.shape[0], H, float(scale), _p(rr), n, _p(out), _p(lse))
     return out, lse
+
+
+# ------------------------------------------------------------------ projections around the attention
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    """Exact float64 values of bf16 bit patterns."""
+    b = np.ascontiguousarray(bits, np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def f64_to_bf16_array(x: np.ndarray) -> np.ndarray:
+    """Nearest bf16 (ties to even) of each double, one rounding."""
+    v = _c(x, np.float64)
+    out = np.empty(v.shape, np.uint16)
+    _load().dsa_oracle_f64_to_bf16_array(_p(v), v.size, _p(out))
+    return out
+
+
+def mla_absorb_q(q_nope_bf16, w_uk_t_bf16, want_mag=False):
+    """Absorbed latent query ([mla] MLACommonImpl.forward decode branch and
+    _q_proj_and_k_up_proj: ql_nope = bmm(q_nope as (N, B, P), W_UK_T (N, P, L)) with
+    W_UK_T = W_UK.permute(1, 2, 0), W_UK the qk_nope part of kv_b_proj viewed (L, N, P)):
+        ql[t, n, l] = sum_p q_nope[t, n, p] * W_UK_T[n, p, l].
+    q_nope: bf16 bits [T, N, P]; W_UK_T: bf16 bits [N, P, L].  The products of bf16 values are
+    exact in float64 and so are their sums for data of ordinary range; the result is rounded once
+    to bf16 (the output dtype of the pages' bmm).  Returns bf16 bits [T, N, L] (and the float64
+    magnitude sum_p |q| |W| when ``want_mag``)."""
+    q = bf16_bits_to_f64(q_nope_bf16)
+    w = bf16_bits_to_f64(w_uk_t_bf16)
+    T, N, P = q.shape
+    assert w.shape[0] == N and w.shape[1] == P
+    acc = np.matmul(q.transpose(1, 0, 2), w).transpose(1, 0, 2)          # [T, N, L]
+    out = f64_to_bf16_array(acc)
+    if want_mag:
+        return out, np.matmul(np.abs(q).transpose(1, 0, 2), np.abs(w)).transpose(1, 0, 2)
+    return out
+
+
+def mla_v_up(o_lat_bf16, w_uv_bf16, want_mag=False):
+    """Value up-projection of the latent attention output ([mla] MLACommonImpl._v_up_proj:
+    bmm(x as (N, B, L), W_UV (N, L, V)) with W_UV = the v part of kv_b_proj viewed (L, N, V),
+    transposed to (N, L, V)):  out[t, n, v] = sum_l o_lat[t, n, l] * W_UV[n, l, v].
+    o_lat: bf16 bits [T, N, L]; W_UV: bf16 bits [N, L, V]; float64 sums rounded once to bf16.
+    Returns bf16 bits [T, N, V] (and the magnitude sum_l |o| |W| when ``want_mag``)."""
+    o = bf16_bits_to_f64(o_lat_bf16)
+    w = bf16_bits_to_f64(w_uv_bf16)
+    T, N, L = o.shape
+    assert w.shape[0] == N and w.shape[1] == L
+    acc = np.matmul(o.transpose(1, 0, 2), w).transpose(1, 0, 2)          # [T, N, V]
+    out = f64_to_bf16_array(acc)
+    if want_mag:
+        return out, np.matmul(np.abs(o).transpose(1, 0, 2), np.abs(w)).transpose(1, 0, 2)
+    return out
 
 
 def lse_merge(o1, lse1, o2, lse2):

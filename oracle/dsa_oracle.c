@@ -68,6 +68,26 @@ uint16_t dsa_oracle_f32_to_bf16(float f) {
 
 float dsa_oracle_bf16_to_f32(uint16_t h) { return bf16_bits_to_f32(h); }
 
+/* Round a double to the nearest bf16 (ties to even) with a single rounding: the double is first
+ * narrowed to fp32 rounding toward zero with a sticky last bit ("round to odd"; fp32 keeps 16 more
+ * bits than bf16, so the second rounding cannot be misled), then rounded to bf16 as above. */
+uint16_t dsa_oracle_f64_to_bf16(double x) {
+    if (isnan(x)) return 0x7fc0u;
+    float f = (float)x;                     /* nearest fp32 */
+    if ((double)f != x && !isinf(f)) {
+        if (fabs((double)f) > fabs(x)) f = nextafterf(f, 0.0f);   /* truncate toward zero */
+        uint32_t u;
+        memcpy(&u, &f, 4);
+        u |= 1u;                            /* inexact: sticky bit */
+        memcpy(&f, &u, 4);
+    }
+    return dsa_oracle_f32_to_bf16(f);
+}
+
+void dsa_oracle_f64_to_bf16_array(const double* x, int64_t n, uint16_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = dsa_oracle_f64_to_bf16(x[i]);
+}
+
 /* OCP 8-bit floating point, E4M3 "fn" variant (the torch.float8_e4m3fn type the [idx] page uses
  * for the index-K cache; not the fnuz variant).  1 sign bit, 4 exponent bits with bias 7, 3
  * mantissa bits; exponent field 0 encodes subnormals m/8 * 2^-6; there is no infinity; the only
