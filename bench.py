@@ -366,6 +366,7 @@ def run_gpu(args):
     e2e = run_e2e(db, stream, args, flush)
     clk.__exit__(None, None, None)
     prologues = run_prologues(wl, stream, flush, stage_iters) if rank == 0 else None
+    projections = run_projections(stream, flush, stage_iters) if rank == 0 else None
 
     if rank != 0:
         return
@@ -403,6 +404,10 @@ def run_gpu(args):
     for v in prologues.values():
         v["hbm_frac"] = v["gbs"] / hbm_peak
     line["indexer_prologues"] = prologues
+    for v in projections.values():
+        v["hbm_frac"] = v["gbs"] / hbm_peak
+        v["tensor_frac"] = v["tflops"] / bf16
+    line["mla_projections"] = projections
     print(json.dumps(line), flush=True)
 
 
@@ -452,6 +457,37 @@ def run_prologues(wl, stream, flush, iters):
     return out
 
 
+def run_projections(stream, flush, iters, heads=128):
+    """Time the per-head projections around the absorbed attention (dsa_mla_absorb_q,
+    dsa_mla_v_up) at a decode shape (64 rows) and a prefill-chunk shape (4096 rows), 128 heads,
+    each call alone in a CUDA graph, L2 flushed before every replay.  Algorithmic work per call:
+    the weights (heads x 128 x 512 bf16) read once, the input and output rows read / written once;
+    2 x rows x heads x 128 x 512 FLOP."""
+    import math
+    import torch
+    from deepseek_sparse_attention_paged_gb300 import capi
+    g = torch.Generator().manual_seed(91)
+    w_uk_t = (torch.randn(heads, 128, 512, generator=g) / math.sqrt(128)).to(torch.bfloat16).cuda()
+    w_uv = (torch.randn(heads, 512, 128, generator=g) / math.sqrt(512)).to(torch.bfloat16).cuda()
+    out = {}
+    for T in (64, 4096):
+        q = torch.randn(T, heads, 192, generator=g).to(torch.bfloat16).cuda()
+        mla_q = torch.empty(T, heads, 576, dtype=torch.bfloat16, device="cuda")
+        o = torch.randn(T, heads, 512, generator=g).to(torch.bfloat16).cuda()
+        y = torch.empty(T, heads * 128, dtype=torch.bfloat16, device="cuda")
+        flop = 2 * T * heads * 128 * 512
+        wbytes = heads * 128 * 512 * 2
+        for name, fn, by in (("absorb", lambda: capi.dsa_mla_absorb_q(q[..., :128], w_uk_t, mla_q[..., :512]),
+                              wbytes + T * heads * (128 + 512) * 2),
+                             ("v_up", lambda: capi.dsa_mla_v_up(o, w_uv, y.view(T, heads, 128)),
+                              wbytes + T * heads * (512 + 128) * 2)):
+            gr, _ = capture(fn, stream)
+            ms = sum(time_graph(gr, stream, iters, flush)) / iters
+            out[f"{name}_T{T}"] = {"rows": T, "heads": heads, "us": ms * 1e3, "algorithmic_bytes": by, "flops": flop,
+                                   "gbs": by / (ms * 1e-3) / 1e9, "tflops": flop / (ms * 1e-3) / 1e12}
+    return out
+
+
 def run_e2e(db, stream, args, flush):
     """Per step, through DeviceBatch.step_io() (the library's end-to-end call, one CUDA graph of the
     copies and the four C-ABI calls): H2D of the step's inputs from pinned host memory (queries,
@@ -495,6 +531,26 @@ def run_profile(args):
     build()
     capi.load()
     wl = workloads.make(args.workload)
+    if args.profile in ("absorb", "v_up"):
+        # the decode shape of run_projections: 64 rows, 128 heads
+        import math
+        g = torch.Generator().manual_seed(91)
+        T, H = 64, 128
+        if args.profile == "absorb":
+            w = (torch.randn(H, 128, 512, generator=g) / math.sqrt(128)).to(torch.bfloat16).cuda()
+            q = torch.randn(T, H, 192, generator=g).to(torch.bfloat16).cuda()
+            mla_q = torch.empty(T, H, 576, dtype=torch.bfloat16, device="cuda")
+            fn = lambda: capi.dsa_mla_absorb_q(q[..., :128], w, mla_q[..., :512])
+        else:
+            w = (torch.randn(H, 512, 128, generator=g) / math.sqrt(512)).to(torch.bfloat16).cuda()
+            o = torch.randn(T, H, 512, generator=g).to(torch.bfloat16).cuda()
+            y = torch.empty(T, H * 128, dtype=torch.bfloat16, device="cuda")
+            fn = lambda: capi.dsa_mla_v_up(o, w, y.view(T, H, 128))
+        for _ in range(args.warmup + args.steps):
+            fn()
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": args.profile, "launches": args.warmup + args.steps}))
+        return
     if args.profile in ("prologue", "rope_q"):
         # the bulk shapes of run_prologues: a 131072-token prompt's keys, 8192 query rows
         g = torch.Generator().manual_seed(wl.seed + 77)
@@ -540,7 +596,8 @@ def run_profile(args):
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
-    ap.add_argument("--profile", choices=["store", "indexer", "topk", "mla", "step", "prologue", "rope_q"],
+    ap.add_argument("--profile", choices=["store", "indexer", "topk", "mla", "step", "prologue", "rope_q", "absorb",
+                                          "v_up"],
                     default=None,
                     help="launch one stage warmup+steps times without timing (for ncu) and exit")
     ap.add_argument("--gpus", type=int, default=1)

@@ -77,6 +77,8 @@ def load(path: str = LIB_PATH):
         "dsa_store_index_k_prologue": (ctypes.c_int, [P, P, P, ctypes.c_float, P, i64, P, P, i64, P, i64, i32, u32,
                                                       P, P]),
         "dsa_indexer_rope_q": (ctypes.c_int, [P, P, i64, P, i64, u32, P, P, P]),
+        "dsa_mla_absorb_q": (ctypes.c_int, [P, i64, i64, P, i32, i32, P, i64, i64, P, P]),
+        "dsa_mla_v_up": (ctypes.c_int, [P, i64, i64, P, i32, i32, P, i64, i64, P, P]),
         "dsa_indexer_logits_workspace_size": (sz, [i32]),
         "dsa_indexer_logits": (ctypes.c_int, [P, P, P, i64, P, i32, P, P, i32, i32, i32, i32, i32, P, i64, u32,
                                               P, sz, P, P]),
@@ -203,6 +205,44 @@ def dsa_indexer_rope_q(q_raw_bf16: torch.Tensor, cos_sin_cache: torch.Tensor, po
         _ptr(q_raw_bf16), _ptr(cos_sin_cache), cos_sin_cache.shape[0], _ptr(positions), T, flags,
         _ptr(q_out_bf16), _ptr(dev_err), _stream(stream)))
     _count(1 if T > 0 else 0)
+
+
+def _strided3(t: torch.Tensor, inner: int, name: str):
+    """(row stride, head stride) of a [T, H, inner] bf16 CUDA view whose last dim is dense."""
+    _need(t.is_cuda and t.dtype == torch.bfloat16, f"{name} must be a bf16 CUDA tensor")
+    _need(t.dim() == 3 and t.shape[2] == inner and (t.stride(2) == 1), f"{name} must be [T, H, {inner}], last dim dense")
+    return t.stride(0), t.stride(1)
+
+
+def dsa_mla_absorb_q(q_nope: torch.Tensor, w_uk_t: torch.Tensor, ql: torch.Tensor,
+                     dev_err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """ql[t, n, :512] = q_nope[t, n, :128] @ w_uk_t[n] (q_nope / ql may be strided views, e.g.
+    q[..., :128] of a [T, H, 192] projection and out[..., :512] of the [T, H, 576] MLA query)."""
+    lib = load()
+    qs_t, qs_n = _strided3(q_nope, 128, "q_nope")
+    os_t, os_n = _strided3(ql, 512, "ql")
+    _cuda(w_uk_t, torch.bfloat16, "w_uk_t")
+    T, H = q_nope.shape[0], q_nope.shape[1]
+    _need(tuple(w_uk_t.shape) == (H, 128, 512), "w_uk_t must be [H, 128, 512]")
+    _need(tuple(ql.shape[:2]) == (T, H), "ql must be [T, H, 512]")
+    _check("dsa_mla_absorb_q", lib.dsa_mla_absorb_q(_ptr(q_nope), qs_t, qs_n, _ptr(w_uk_t), T, H, _ptr(ql), os_t, os_n,
+                                                    _ptr(dev_err), _stream(stream)))
+    _count(1 if T > 0 and H > 0 else 0)
+
+
+def dsa_mla_v_up(o_lat: torch.Tensor, w_uv: torch.Tensor, out: torch.Tensor,
+                 dev_err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """out[t, n, :128] = o_lat[t, n, :512] @ w_uv[n] (out may be a [T, H, 128] view of [T, H * 128])."""
+    lib = load()
+    is_t, is_n = _strided3(o_lat, 512, "o_lat")
+    os_t, os_n = _strided3(out, 128, "out")
+    _cuda(w_uv, torch.bfloat16, "w_uv")
+    T, H = o_lat.shape[0], o_lat.shape[1]
+    _need(tuple(w_uv.shape) == (H, 512, 128), "w_uv must be [H, 512, 128]")
+    _need(tuple(out.shape[:2]) == (T, H), "out must be [T, H, 128]")
+    _check("dsa_mla_v_up", lib.dsa_mla_v_up(_ptr(o_lat), is_t, is_n, _ptr(w_uv), T, H, _ptr(out), os_t, os_n,
+                                            _ptr(dev_err), _stream(stream)))
+    _count(1 if T > 0 and H > 0 else 0)
 
 
 def dsa_indexer_logits(q_bf16: torch.Tensor, weights: torch.Tensor, index_k_pool: torch.Tensor,

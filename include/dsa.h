@@ -9,7 +9,8 @@
  *      (512 latent + 64 rope, one shared KV head, 512-wide latent output).
  * A fourth call writes new keys into the index-K cache (Hadamard rotation, per-token FP8
  * quantisation, paged scatter by slot); two prologue calls add the key norm and rotary embedding
- * in front of that store and the rotary embedding of the indexer query.
+ * in front of that store and the rotary embedding of the indexer query; two more compute the
+ * per-head projections around the absorbed attention (absorbed query, value up-projection).
  *
  * Conventions shared by every call
  * --------------------------------
@@ -301,6 +302,47 @@ dsa_status dsa_sparse_mla_decode_noalloc(const void* q_bf16, const void* kv_pool
                                          const int32_t* idx, int32_t k, int32_t T, int32_t H,
                                          float scale, void* out_bf16, float* lse, int32_t* dev_err,
                                          void* stream);
+
+/*
+ * dsa_mla_absorb_q -- absorbed latent query: ql[t, n, 0:512] = q_nope[t, n, 0:128] W_UK_T[n].
+ * Source: vllm mla/common.py, MLACommonImpl.forward decode branch and _q_proj_and_k_up_proj
+ * (torch.bmm(q_nope as (N, B, P), W_UK_T (N, P, L)); W_UK_T = W_UK.permute(1, 2, 0) where W_UK is
+ * the qk_nope part of kv_b_proj's weight viewed (L, N, P)).
+ *   ql[t, n, l] = bf16_rn(sum_{p < 128} q_nope[t, n, p] * W_UK_T[n, p, l]), bf16 operands,
+ *   fp32 accumulation on the tensor cores.
+ * Arguments:
+ *   q_nope_bf16     element (t, n, p) at q_nope_bf16[t * q_row_stride + n * q_head_stride + p];
+ *                   16-byte aligned; both strides multiples of 8 elements (e.g. the q_nope part of
+ *                   a [T, H, 192] projection output: strides H * 192 and 192).
+ *   w_uk_t_bf16     [H, 128, 512] bf16, contiguous, 16-byte aligned.
+ *   ql_bf16         element (t, n, l) at ql_bf16[t * out_row_stride + n * out_head_stride + l];
+ *                   e.g. the first 512 columns of the [T, H, 576] attention query (strides H * 576
+ *                   and 576).  Distinct (t, n) outputs must not overlap.
+ *   dev_err         nullable; DSA_DEVERR_TIMEOUT if a bounded wait gave up.
+ */
+dsa_status dsa_mla_absorb_q(const void* q_nope_bf16, int64_t q_row_stride, int64_t q_head_stride,
+                            const void* w_uk_t_bf16, int32_t T, int32_t H, void* ql_bf16,
+                            int64_t out_row_stride, int64_t out_head_stride, int32_t* dev_err,
+                            void* stream);
+
+/*
+ * dsa_mla_v_up -- value up-projection of the latent attention output:
+ * out[t, n, 0:128] = o_lat[t, n, 0:512] W_UV[n].
+ * Source: vllm mla/common.py, MLACommonImpl._v_up_proj (torch.bmm(o_lat as (N, B, L), W_UV
+ * (N, L, V)); W_UV = the v part of kv_b_proj's weight viewed (L, N, V), transposed to (N, L, V)).
+ *   out[t, n, v] = bf16_rn(sum_{l < 512} o_lat[t, n, l] * W_UV[n, l, v]), fp32 accumulation.
+ * Arguments:
+ *   o_lat_bf16      element (t, n, l) at o_lat_bf16[t * o_row_stride + n * o_head_stride + l]
+ *                   (dsa_sparse_mla_decode's output: strides H * 512 and 512); 16-byte aligned,
+ *                   strides multiples of 8 elements.
+ *   w_uv_bf16       [H, 512, 128] bf16, contiguous, 16-byte aligned.
+ *   out_bf16        element (t, n, v) at out_bf16[t * out_row_stride + n * out_head_stride + v]
+ *                   (e.g. [T, H * 128]: strides H * 128 and 128).
+ *   dev_err         nullable; DSA_DEVERR_TIMEOUT if a bounded wait gave up.
+ */
+dsa_status dsa_mla_v_up(const void* o_lat_bf16, int64_t o_row_stride, int64_t o_head_stride,
+                        const void* w_uv_bf16, int32_t T, int32_t H, void* out_bf16,
+                        int64_t out_row_stride, int64_t out_head_stride, int32_t* dev_err, void* stream);
 
 /*
  * dsa_read_device_error -- synchronise `stream`, copy the device error word to the host
