@@ -161,11 +161,58 @@ constexpr int kCandidateCap = 8192;
 struct BitmapSmem {
     uint32_t hist[kTopBins];
     uint32_t warp_tot[kWarps];
+    uint32_t warp_tot2[kWarps];
     uint32_t sel_digit;
     uint32_t sel_remaining;
     uint32_t cand_count;
-    uint32_t pad;
+    int32_t row_v;
 };
+
+// Visible length of global row r, looked up by all threads at once: thread t < B tests whether r
+// falls in request t (one round of independent loads instead of a chain of dependent ones).
+__device__ __forceinline__ int locate_visible(const int32_t* __restrict__ cu_q, const int32_t* __restrict__ seq_lens,
+                                              int B, int r, BitmapSmem& sm) {
+    if (threadIdx.x == 0) sm.row_v = 0;
+    __syncthreads();
+    for (int t = threadIdx.x; t < B; t += kTopkThreads) {
+        const int a = __ldg(cu_q + t), e = __ldg(cu_q + t + 1), L = __ldg(seq_lens + t);
+        if (a <= r && r < e) sm.row_v = visible_len(L, e - a, r - a);
+    }
+    __syncthreads();
+    return sm.row_v;
+}
+
+// Block-wide exclusive scans of two uint32 per thread at once (one set of barriers); also the
+// block totals.
+__device__ __forceinline__ void block_exclusive_scan2(uint32_t& a, uint32_t& b, BitmapSmem& sm, uint32_t* tot_a,
+                                                      uint32_t* tot_b) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t ia = a, ib = b;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t oa = __shfl_up_sync(0xffffffffu, ia, d), ob = __shfl_up_sync(0xffffffffu, ib, d);
+        if (lane >= d) { ia += oa; ib += ob; }
+    }
+    if (lane == 31) { sm.warp_tot[warp] = ia; sm.warp_tot2[warp] = ib; }
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t ta = sm.warp_tot[lane], tb = sm.warp_tot2[lane];
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t oa = __shfl_up_sync(0xffffffffu, ta, d), ob = __shfl_up_sync(0xffffffffu, tb, d);
+            if (lane >= d) { ta += oa; tb += ob; }
+        }
+        sm.warp_tot[lane] = ta;
+        sm.warp_tot2[lane] = tb;
+    }
+    __syncthreads();
+    const uint32_t ba = warp == 0 ? 0u : sm.warp_tot[warp - 1], bb = warp == 0 ? 0u : sm.warp_tot2[warp - 1];
+    *tot_a = sm.warp_tot[kWarps - 1];
+    *tot_b = sm.warp_tot2[kWarps - 1];
+    a = ia - a + ba;
+    b = ib - b + bb;
+    __syncthreads();
+}
 
 // Digit d (from the top) of `bins` histogram bins such that (# keys with digit > d) < need <=
 // (# keys with digit >= d); stores d and need - (# keys with digit > d).  bins: 1024 or 4096.
@@ -203,9 +250,7 @@ topk_bitmap_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* 
     ptx::griddep_launch_dependents();
     const int rl = blockIdx.x;
     const int r = row_begin + rl;
-    const int b = row_request(cu_q, B, r);
-    const int q0 = __ldg(cu_q + b);
-    int v = visible_len(__ldg(seq_lens + b), __ldg(cu_q + b + 1) - q0, r - q0);
+    int v = locate_visible(cu_q, seq_lens, B, r, sm);
     if (v > ld) v = static_cast<int>(ld);
     if (v > words_cap * 32) v = words_cap * 32;   // the launcher guarantees this never clips
     const float* row = logits + static_cast<int64_t>(rl) * ld;
@@ -321,9 +366,8 @@ topk_bitmap_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* 
         gt += __popc(sel[w]);
         eq += __popc(tie[w]);
     }
-    uint32_t tot;
-    uint32_t gt_before = block_inclusive_scan(gt, sm.warp_tot, &tot) - gt;
-    uint32_t eq_before = block_inclusive_scan(eq, sm.warp_tot, &tot) - eq;
+    uint32_t gt_before = gt, eq_before = eq, tot_gt, tot_eq;
+    block_exclusive_scan2(gt_before, eq_before, sm, &tot_gt, &tot_eq);
     for (int w = w0; w < w1; ++w) {
         const uint32_t sw = sel[w], tw = tie[w];
         uint32_t bits = sw | tw;
@@ -340,6 +384,228 @@ topk_bitmap_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* 
             }
         }
     }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Cluster kernel: the same two-read scheme with each long row split over a 2-CTA cluster (for
+// batches with fewer rows than SM pairs).  CTA h takes keys [h ? split : 0, h ? v : split), split
+// a multiple of 128.  Every histogram (the 12-bit top digit, then each 10-bit low digit, each in a
+// buffer of its own) is built locally in shared memory and summed with the peer's through
+// distributed shared memory after one cluster barrier (16-byte remote reads, no remote atomics),
+// so both CTAs take the same digit decisions; each marks its own half's bitmaps and writes its
+// kept indices, the second half offset by the first half's counts.
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The 16 bytes at the same shared-memory offset as `p` (16-byte aligned) in CTA `rank`.
+__device__ __forceinline__ uint4 ld_rank_v4(const uint32_t* p, uint32_t rank) {
+    uint32_t a;
+    uint4 v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(ptx::smem_addr(p)), "r"(rank));
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(a)
+                 : "memory");
+    return v;
+}
+
+// total[b] = this CTA's hist[b] + the peer's hist[b], b < bins (a multiple of 4).  Both CTAs'
+// histograms are complete on entry.  A histogram buffer is never written again after it has been
+// summed, and the kernel ends with a cluster barrier, so no barrier is needed after the reads.
+__device__ __forceinline__ void sum_with_peer(const uint32_t* hist, uint32_t* total, int bins, uint32_t peer) {
+    cluster_sync();   // the peer's histogram is complete and visible
+    for (int q = threadIdx.x; q < bins / 4; q += kTopkThreads) {
+        const uint4 mine = reinterpret_cast<const uint4*>(hist)[q];
+        const uint4 theirs = ld_rank_v4(hist + 4 * q, peer);
+        reinterpret_cast<uint4*>(total)[q] =
+            make_uint4(mine.x + theirs.x, mine.y + theirs.y, mine.z + theirs.z, mine.w + theirs.w);
+    }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kTopkThreads)
+topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* __restrict__ seq_lens,
+                    const int32_t* __restrict__ cu_q, int B, int row_begin, int k, int32_t* __restrict__ idx,
+                    int words_cap) {
+    extern __shared__ __align__(16) unsigned char dsm[];
+    BitmapSmem& sm = *reinterpret_cast<BitmapSmem*>(dsm);                      // hist: the top digit
+    uint32_t* total = reinterpret_cast<uint32_t*>(dsm + sizeof(BitmapSmem));   // summed histogram
+    uint32_t* lo_hist = total + kTopBins;                                        // [2][1024]: low digits
+    uint32_t* xcnt = lo_hist + 2 * 1024;                                         // this half's kept counts
+    uint32_t* sel = xcnt + 4;
+    uint32_t* tie = sel + words_cap;
+    uint32_t* ckey = tie + words_cap;
+    int32_t* cidx = reinterpret_cast<int32_t*>(ckey + kCandidateCap);
+
+    ptx::griddep_wait();   // launched as a programmatic dependent: the logits are complete from here on
+    ptx::griddep_launch_dependents();
+    const uint32_t half = cluster_rank();
+    const uint32_t peer = half ^ 1u;
+    const int rl = blockIdx.y;
+    const int r = row_begin + rl;
+    // histogram buffers zeroed while the row's request is looked up
+    for (int i = threadIdx.x; i < kTopBins; i += kTopkThreads) sm.hist[i] = 0;
+    for (int i = threadIdx.x; i < 2 * 1024; i += kTopkThreads) lo_hist[i] = 0;
+    if (threadIdx.x == 0) sm.cand_count = 0;
+    int v = locate_visible(cu_q, seq_lens, B, r, sm);
+    if (v > ld) v = static_cast<int>(ld);
+    if (v > 2 * words_cap * 32 - 256) v = 2 * words_cap * 32 - 256;   // the launcher guarantees this never clips
+    const float* row = logits + static_cast<int64_t>(rl) * ld;
+    int32_t* out = idx + static_cast<int64_t>(rl) * k;
+    if (v <= k) {   // both CTAs leave here, before any cluster barrier
+        if (half == 0)
+            for (int j = threadIdx.x; j < k; j += kTopkThreads) out[j] = j < v ? j : -1;
+        return;
+    }
+    const int split = min(v, ((v + 1) / 2 + 127) & ~127);
+    const int lo = half == 0 ? 0 : split;
+    const int nloc = (half == 0 ? split : v) - lo;
+    const int W = (nloc + 31) / 32;
+    const float* part = row + lo;
+    for (int w = threadIdx.x; w < W; w += kTopkThreads) sel[w] = tie[w] = 0u;
+
+    const bool vec = (reinterpret_cast<uintptr_t>(part) & 15u) == 0;
+    const int v4 = vec ? (nloc >> 2) : 0;
+    auto for_each_key = [&](auto&& fn) {   // (local index, key) of this half
+        const float4* p4 = reinterpret_cast<const float4*>(part);
+        constexpr int U = 4;
+        int i = threadIdx.x;
+        for (; i + (U - 1) * kTopkThreads < v4; i += U * kTopkThreads) {
+            float4 a[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) a[u] = __ldg(p4 + i + u * kTopkThreads);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = i + u * kTopkThreads;
+                fn(4 * j, order_key(a[u].x)); fn(4 * j + 1, order_key(a[u].y));
+                fn(4 * j + 2, order_key(a[u].z)); fn(4 * j + 3, order_key(a[u].w));
+            }
+        }
+        for (; i < v4; i += kTopkThreads) {
+            const float4 a = __ldg(p4 + i);
+            fn(4 * i, order_key(a.x)); fn(4 * i + 1, order_key(a.y)); fn(4 * i + 2, order_key(a.z)); fn(4 * i + 3, order_key(a.w));
+        }
+        for (int s = 4 * v4 + threadIdx.x; s < nloc; s += kTopkThreads) fn(s, order_key(__ldg(part + s)));
+    };
+
+    // ---- read 1: top-12-bit histogram of this half, summed with the peer's
+    for_each_key([&](int, uint32_t key) { atomicAdd(&sm.hist[key >> 20], 1u); });
+    __syncthreads();
+    sum_with_peer(sm.hist, total, kTopBins, peer);
+    select_bin(total, sm, kTopBins, static_cast<uint32_t>(k));
+    const uint32_t b1 = sm.sel_digit;
+    uint32_t need = sm.sel_remaining;
+
+    // ---- read 2: mark keys above the threshold bin, collect the threshold bin (this half)
+    for_each_key([&](int s, uint32_t key) {
+        const uint32_t bin = key >> 20;
+        if (bin > b1) {
+            atomicOr(&sel[s >> 5], 1u << (s & 31));
+        } else if (bin == b1) {
+            const uint32_t p = atomicAdd(&sm.cand_count, 1u);
+            if (p < static_cast<uint32_t>(kCandidateCap)) {
+                ckey[p] = key;
+                cidx[p] = s;
+            }
+        }
+    });
+    __syncthreads();
+    const uint32_t n = sm.cand_count;
+    const bool in_smem = n <= static_cast<uint32_t>(kCandidateCap);
+    // ---- low digits: bits [19:10], then [9:0], over both halves' threshold-bin keys
+    uint32_t prefix = b1 << 20;
+    for (int pass = 0; pass < 2; ++pass) {
+        const int shift = pass == 0 ? 10 : 0;
+        const int hi = shift + 10;
+        uint32_t* h = lo_hist + pass * 1024;
+        if (in_smem) {
+            for (uint32_t i = threadIdx.x; i < n; i += kTopkThreads) {
+                const uint32_t key = ckey[i];
+                if ((key >> hi) == (prefix >> hi)) atomicAdd(&h[(key >> shift) & 1023u], 1u);
+            }
+        } else {
+            for (int s = threadIdx.x; s < nloc; s += kTopkThreads) {
+                const uint32_t key = order_key(__ldg(part + s));
+                if ((key >> hi) == (prefix >> hi)) atomicAdd(&h[(key >> shift) & 1023u], 1u);
+            }
+        }
+        __syncthreads();
+        sum_with_peer(h, total, 1024, peer);
+        select_bin(total, sm, 1024, need);
+        prefix |= sm.sel_digit << shift;
+        need = sm.sel_remaining;
+        __syncthreads();
+    }
+    const uint32_t kth = prefix;
+    const uint32_t take_equal = need;   // keys equal to kth that are kept (lowest indices first)
+    if (in_smem) {
+        for (uint32_t i = threadIdx.x; i < n; i += kTopkThreads) {
+            const uint32_t key = ckey[i];
+            const int s = cidx[i];
+            if (key > kth) atomicOr(&sel[s >> 5], 1u << (s & 31));
+            else if (key == kth) atomicOr(&tie[s >> 5], 1u << (s & 31));
+        }
+    } else {
+        for (int s = threadIdx.x; s < nloc; s += kTopkThreads) {
+            const uint32_t key = order_key(__ldg(part + s));
+            if ((key >> 20) != b1) continue;
+            if (key > kth) atomicOr(&sel[s >> 5], 1u << (s & 31));
+            else if (key == kth) atomicOr(&tie[s >> 5], 1u << (s & 31));
+        }
+    }
+    __syncthreads();
+
+    // ---- index-ordered output; the second half starts after the first half's kept keys
+    const int wpt = (W + kTopkThreads - 1) / kTopkThreads;
+    const int w0 = min(W, threadIdx.x * wpt), w1 = min(W, w0 + wpt);
+    uint32_t gt_before = 0, eq_before = 0;
+    for (int w = w0; w < w1; ++w) {
+        gt_before += __popc(sel[w]);
+        eq_before += __popc(tie[w]);
+    }
+    uint32_t gt_tot, eq_tot;
+    block_exclusive_scan2(gt_before, eq_before, sm, &gt_tot, &eq_tot);
+    if (threadIdx.x == 0) {
+        xcnt[0] = gt_tot;
+        xcnt[1] = eq_tot;
+    }
+    __syncthreads();
+    cluster_sync();   // both halves' counts are visible
+    if (half == 1) {
+        const uint4 c = ld_rank_v4(xcnt, peer);
+        gt_before += c.x;
+        eq_before += c.y;
+    }
+    for (int w = w0; w < w1; ++w) {
+        const uint32_t sw = sel[w], tw = tie[w];
+        uint32_t bits = sw | tw;
+        while (bits) {
+            const int bit = __ffs(bits) - 1;
+            bits &= bits - 1;
+            const int s = lo + w * 32 + bit;
+            if ((sw >> bit) & 1u) {
+                out[gt_before + min(eq_before, take_equal)] = s;
+                ++gt_before;
+            } else {
+                if (eq_before < take_equal) out[gt_before + eq_before] = s;
+                ++eq_before;
+            }
+        }
+    }
+    cluster_sync();   // the peer has read this CTA's histograms and counts before either leaves
+}
+
+size_t cluster_smem_bytes(int words) {
+    return sizeof(BitmapSmem) + static_cast<size_t>(kTopBins) * 4 + 2 * 1024 * 4 + 16 +
+           2 * static_cast<size_t>(words) * 4 + static_cast<size_t>(kCandidateCap) * 8;
 }
 
 size_t bitmap_smem_bytes(int words) {
@@ -376,7 +642,33 @@ extern "C" dsa_status dsa_topk(const float* logits, int64_t ld, const int32_t* s
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (words <= dsa::kMaxBitmapWords) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        return DSA_ERR_CUDA;
+    if (words <= dsa::kMaxBitmapWords && max_seq_len >= 16384 && (row_end - row_begin) <= sms / 2) {
+        // long rows, fewer rows than SM pairs: each row on a 2-CTA cluster
+        const int half_keys = ((max_seq_len + 1) / 2 + 127) & ~127;
+        int words_cap = ((half_keys + 256 + 31) / 32 + 3) & ~3;
+        if (words_cap < 32) words_cap = 32;
+        const size_t smem = dsa::cluster_smem_bytes(words_cap);
+        if (cudaFuncSetAttribute(dsa::topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem)) != cudaSuccess)
+            return DSA_ERR_CUDA;
+        cudaLaunchAttribute cattr[2];
+        cattr[0].id = cudaLaunchAttributeClusterDimension;
+        cattr[0].val.clusterDim.x = 2;
+        cattr[0].val.clusterDim.y = 1;
+        cattr[0].val.clusterDim.z = 1;
+        cattr[1] = attr[0];
+        cfg.gridDim = dim3(2, static_cast<unsigned>(row_end - row_begin), 1);
+        cfg.attrs = cattr;
+        cfg.numAttrs = 2;
+        cfg.dynamicSmemBytes = smem;
+        if (cudaLaunchKernelEx(&cfg, dsa::topk_cluster_kernel, logits, ld, seq_lens, cu_q, static_cast<int>(B),
+                               static_cast<int>(row_begin), static_cast<int>(k), idx, words_cap) != cudaSuccess)
+            return DSA_ERR_CUDA;
+    } else if (words <= dsa::kMaxBitmapWords) {
         const int words_cap = words < 32 ? 32 : words;
         const size_t smem = dsa::bitmap_smem_bytes(words_cap);
         if (cudaFuncSetAttribute(dsa::topk_bitmap_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -39,7 +39,8 @@ def test_topk_on_oracle_logits_tiny():
 
 @pytest.mark.parametrize("v,k", [(0, 16), (1, 16), (15, 16), (16, 16), (17, 16), (2048, 2048), (2049, 2048),
                                  (5000, 2048), (70000, 2048), (131072, 2048), (3000, 1), (3000, 1999),
-                                 (40, 3), (100, 7), (131071, 2048), (140000, 2048), (140000, 100)])
+                                 (40, 3), (100, 7), (131071, 2048), (140000, 2048), (140000, 100),
+                                 (20000, 2048), (20001, 2048), (33000, 100), (65536, 2048), (65792, 2048)])
 def test_topk_lengths_and_ties(v, k):
     rng = np.random.default_rng(200 + v + k)
     width = max(v, 4)
@@ -55,7 +56,7 @@ def test_topk_lengths_and_ties(v, k):
     assert np.array_equal(got, ref)
 
 
-@pytest.mark.parametrize("v,k", [(70000, 2048), (70000, 1500), (9000, 2048), (131072, 100)])
+@pytest.mark.parametrize("v,k", [(70000, 2048), (70000, 1500), (9000, 2048), (131072, 100), (40000, 2048)])
 def test_topk_rows_that_mislead_the_sample(v, k):
     """Rows whose evenly spaced sample misjudges the cut: the largest values sit on sampled
     positions only (fewer than k keys reach the cut), everywhere but the sampled positions (far
