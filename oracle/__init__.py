@@ -253,6 +253,20 @@ def topk(logits, seq_lens, cu_q, rows, k):
     return idx
 
 
+def topk_forced(logits, seq_lens, cu_q, rows, k, n_init, n_local):
+    """Top-k with forced initial and local tokens ([idx] Indexer._mask_init_and_local_tokens: the
+    logits at the row's first n_init and last n_local positions are set to +inf before the top-k).
+    Reading: the positions are taken inside the row's visible range [0, v_r); then ``topk``."""
+    lg = np.array(logits, dtype=np.float32, copy=True)
+    rr = np.asarray(rows, np.int64)
+    for i, r in enumerate(rr):
+        v = visible_len(seq_lens, cu_q, int(r))
+        v = min(v, lg.shape[1])
+        lg[i, :min(n_init, v)] = np.inf
+        lg[i, max(0, v - n_local):v] = np.inf
+    return topk(lg, seq_lens, cu_q, rows, k)
+
+
 def sparse_mla(q_bf16, kv_bf16, block_table, seq_lens, cu_q, idx, scale, rows, want_psum=False):
     """Absorbed sparse MLA for the global rows ``rows``; returns (out float64 [n,H,512],
     lse float64 [n,H]) and, when ``want_psum``, the softmax-weight sums and the skipped count."""

@@ -157,3 +157,35 @@ def test_topk_uses_visible_length_per_row():
     lg = np.array([[0, 1, 2, 3, 4, 99, 7], [0, 1, 2, 3, 4, 99, 7]], np.float32)
     idx = oracle.topk(lg, np.array([6], np.int32), np.array([0, 2], np.int32), np.array([0, 1]), 2)
     assert idx.tolist() == [[3, 4], [4, 5]]
+
+
+def _forced_brute(row, k, n_init, n_local):
+    """Forced positions first (they count as +inf, lower index first among equals), then the
+    largest of the rest by (value descending, index ascending); the kept indices ascending."""
+    v = len(row)
+    forced = sorted(set(range(min(n_init, v))) | set(range(max(0, v - n_local), v)))
+    val = [np.inf if i in forced else float(row[i]) for i in range(v)]
+    order = sorted(range(v), key=lambda i: (-val[i] if not np.isnan(val[i]) else np.inf, i))
+    kept = sorted(order[:min(k, v)])
+    return kept + [-1] * (k - len(kept))
+
+
+@pytest.mark.parametrize("v,k,n_init,n_local", [(50, 8, 2, 3), (50, 4, 3, 3), (10, 20, 2, 2), (200, 16, 0, 5),
+                                                 (200, 16, 5, 0), (30, 10, 40, 0), (30, 10, 0, 40)])
+def test_topk_forced_matches_brute_force(v, k, n_init, n_local):
+    rng = np.random.default_rng(900 + v + k + n_init)
+    row = rng.standard_normal(v).astype(np.float32)
+    row[v // 2] = np.inf                      # a real +inf competes with the forced ones by index
+    got = oracle.topk_forced(row[None, :], np.array([v], np.int32), np.array([0, 1], np.int32), [0], k,
+                             n_init, n_local)[0]
+    assert list(got) == _forced_brute(row, k, n_init, n_local)
+
+
+def test_topk_forced_keeps_every_forced_position_that_fits():
+    rng = np.random.default_rng(910)
+    v, k = 1000, 64
+    row = rng.standard_normal(v).astype(np.float32) + 100.0   # every real logit large
+    got = oracle.topk_forced(row[None, :], np.array([v], np.int32), np.array([0, 1], np.int32), [0], k, 4, 16)[0]
+    assert set(range(4)) <= set(got) and set(range(v - 16, v)) <= set(got)
+    plain = oracle.topk(row[None, :], np.array([v], np.int32), np.array([0, 1], np.int32), [0], k)[0]
+    assert set(got) - set(range(4)) - set(range(v - 16, v)) <= set(plain)
