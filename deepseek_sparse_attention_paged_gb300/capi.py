@@ -84,6 +84,10 @@ def load(path: str = LIB_PATH):
                                               P, sz, P, P]),
         "dsa_topk_workspace_size": (sz, [i32, i32, i32]),
         "dsa_topk": (ctypes.c_int, [P, i64, P, P, i32, i32, i32, i32, i32, P, P, sz, P]),
+        "dsa_topk_forced": (ctypes.c_int, [P, i64, P, P, i32, i32, i32, i32, i32, i32, i32, P, P, sz, P]),
+        "dsa_lightning_indexer_workspace_size": (sz, [i32, i32]),
+        "dsa_lightning_indexer": (ctypes.c_int, [P, P, P, i64, P, i32, P, P, i32, i32, i32, i32, i32, i32, i32, u32,
+                                                 P, P, sz, P, P]),
         "dsa_sparse_mla_workspace_size": (sz, [i32, i32, i32]),
         "dsa_sparse_mla_decode": (ctypes.c_int, [P, P, i64, P, i32, P, P, i32, P, i32, i32, i32, ctypes.c_float,
                                                  P, P, P, sz, P, P]),
@@ -291,7 +295,9 @@ def dsa_topk_workspace_size(rows: int, k: int, max_seq_len: int) -> int:
 
 def dsa_topk(logits: torch.Tensor, seq_lens: torch.Tensor, cu_q: torch.Tensor, max_seq_len: int, k: int,
              idx: torch.Tensor, row_begin: int = 0, row_end: Optional[int] = None,
-             workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+             workspace: Optional[torch.Tensor] = None, stream=None, n_init: int = 0, n_local: int = 0) -> None:
+    """Per-row top-k; with n_init / n_local > 0 (dsa_topk_forced) the first n_init and the last
+    n_local visible positions of every row count as +inf."""
     lib = load()
     _rows(logits, torch.float32, "logits")
     _cuda(seq_lens, torch.int32, "seq_lens")
@@ -302,10 +308,47 @@ def dsa_topk(logits: torch.Tensor, seq_lens: torch.Tensor, cu_q: torch.Tensor, m
     rows = row_end - row_begin
     _need(idx.dim() == 2 and idx.shape[0] >= rows and idx.shape[1] == k, "idx must be [rows, k]")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check("dsa_topk", lib.dsa_topk(
-        _ptr(logits), logits.stride(0), _ptr(seq_lens), _ptr(cu_q), B, int(max_seq_len), int(row_begin),
-        int(row_end), int(k), _ptr(idx), _ptr(workspace), ws_bytes, _stream(stream)))
+    if n_init or n_local:
+        _check("dsa_topk_forced", lib.dsa_topk_forced(
+            _ptr(logits), logits.stride(0), _ptr(seq_lens), _ptr(cu_q), B, int(max_seq_len), int(row_begin),
+            int(row_end), int(k), int(n_init), int(n_local), _ptr(idx), _ptr(workspace), ws_bytes, _stream(stream)))
+    else:
+        _check("dsa_topk", lib.dsa_topk(
+            _ptr(logits), logits.stride(0), _ptr(seq_lens), _ptr(cu_q), B, int(max_seq_len), int(row_begin),
+            int(row_end), int(k), _ptr(idx), _ptr(workspace), ws_bytes, _stream(stream)))
     _count(1 if rows > 0 else 0)
+
+
+def dsa_lightning_indexer_workspace_size(T: int, max_seq_len: int) -> int:
+    return int(load().dsa_lightning_indexer_workspace_size(int(T), int(max_seq_len)))
+
+
+def dsa_lightning_indexer(q_bf16: torch.Tensor, weights: torch.Tensor, index_k_pool: torch.Tensor,
+                          block_table: torch.Tensor, seq_lens: torch.Tensor, cu_q: torch.Tensor, max_seq_len: int,
+                          max_q_len: int, k: int, idx: torch.Tensor, workspace: torch.Tensor, n_init: int = 0,
+                          n_local: int = 0, flags: int = 0, dev_err: Optional[torch.Tensor] = None,
+                          stream=None) -> None:
+    """Top-k indices of the indexer logits of every row in one call (the logits stay in
+    `workspace`, dsa_lightning_indexer_workspace_size(T, max_seq_len) bytes)."""
+    lib = load()
+    _cuda(q_bf16, torch.bfloat16, "q_bf16")
+    _cuda(weights, torch.float32, "weights")
+    _cuda(index_k_pool, torch.uint8, "index_k_pool")
+    _cuda(block_table, torch.int32, "block_table")
+    _cuda(seq_lens, torch.int32, "seq_lens")
+    _cuda(cu_q, torch.int32, "cu_q")
+    _cuda(idx, torch.int32, "idx")
+    _cuda(workspace, torch.uint8, "workspace")
+    T = q_bf16.shape[0]
+    B = seq_lens.numel()
+    _need(q_bf16.dim() == 3 and tuple(q_bf16.shape[1:]) == (64, 128), "q_bf16 must be [T, 64, 128]")
+    _need(tuple(idx.shape) == (T, k), "idx must be [T, k]")
+    _check("dsa_lightning_indexer", lib.dsa_lightning_indexer(
+        _ptr(q_bf16), _ptr(weights), _ptr(index_k_pool), index_k_pool.shape[0], _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), _ptr(cu_q), B, int(max_seq_len), int(max_q_len), T, int(k),
+        int(n_init), int(n_local), int(flags), _ptr(idx), _ptr(workspace), workspace.numel(), _ptr(dev_err),
+        _stream(stream)))
+    _count(3 if T > 0 else 0)
 
 
 def dsa_sparse_mla_workspace_size(T: int, H: int, k: int) -> int:

@@ -26,6 +26,25 @@ __device__ __forceinline__ uint32_t order_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Positions whose logit counts as +inf (the forced initial and local tokens): [0, init_end) and
+// [local_begin, v).  With nothing forced, init_end = 0 and local_begin = v.
+// ON = false (nothing forced) compiles the test away.
+template <bool ON>
+struct Forced {
+    int init_end, local_begin;
+    __device__ __forceinline__ uint32_t operator()(int s, uint32_t key) const {
+        if (!ON) return key;
+        return (s < init_end || s >= local_begin) ? 0xFF800000u : key;   // order key of +inf
+    }
+};
+template <bool ON>
+__device__ __forceinline__ Forced<ON> make_forced(int v, int n_init, int n_local) {
+    Forced<ON> f;
+    f.init_end = min(n_init, v);
+    f.local_begin = max(0, v - n_local);
+    return f;
+}
+
 // Block-wide inclusive scan of one uint32 per thread; also returns the block total.
 __device__ __forceinline__ uint32_t block_inclusive_scan(uint32_t v, uint32_t* warp_tot, uint32_t* total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -82,9 +101,10 @@ __device__ void select_digit(TopkSmem& sm, int bins, uint32_t need) {
     __syncthreads();
 }
 
+template <bool FORCED>
 __global__ void __launch_bounds__(kTopkThreads)
 topk_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* __restrict__ seq_lens,
-            const int32_t* __restrict__ cu_q, int B, int row_begin, int k, int32_t* __restrict__ idx) {
+            const int32_t* __restrict__ cu_q, int B, int row_begin, int k, int n_init, int n_local, int32_t* __restrict__ idx) {
     __shared__ TopkSmem sm;
     ptx::griddep_wait();   // launched as a programmatic dependent: the logits are complete from here on
     ptx::griddep_launch_dependents();
@@ -95,6 +115,7 @@ topk_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* __restr
     int v = visible_len(__ldg(seq_lens + b), __ldg(cu_q + b + 1) - q0, r - q0);
     if (v > ld) v = static_cast<int>(ld);       // never read past the row
     const float* row = logits + static_cast<int64_t>(rl) * ld;
+    const Forced<FORCED> F = make_forced<FORCED>(v, n_init, n_local);
     int32_t* out = idx + static_cast<int64_t>(rl) * k;
 
     if (v <= k) {   // short row: keep everything in index order
@@ -112,7 +133,7 @@ topk_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* __restr
         __syncthreads();
         const int hi_shift = shifts[pass] + widths[pass];   // bits above this digit must match
         for (int s = threadIdx.x; s < v; s += kTopkThreads) {
-            const uint32_t key = order_key(__ldg(row + s));
+            const uint32_t key = F(s, order_key(__ldg(row + s)));
             const bool match = hi_shift >= 32 || (key >> hi_shift) == (prefix >> hi_shift);
             if (match) atomicAdd(&sm.hist[(key >> shifts[pass]) & (bins - 1)], 1u);
         }
@@ -131,7 +152,7 @@ topk_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* __restr
         const int s = base + threadIdx.x;
         uint32_t key = 0;
         bool valid = s < v;
-        if (valid) key = order_key(__ldg(row + s));
+        if (valid) key = F(s, order_key(__ldg(row + s)));
         const uint32_t gt = (valid && key > kth) ? 1u : 0u;
         const uint32_t eq = (valid && key == kth) ? 1u : 0u;
         uint32_t total;
@@ -235,9 +256,10 @@ __device__ void select_bin(uint32_t* hist, BitmapSmem& sm, int bins, uint32_t ne
     __syncthreads();
 }
 
+template <bool FORCED>
 __global__ void __launch_bounds__(kTopkThreads)
 topk_bitmap_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* __restrict__ seq_lens,
-                   const int32_t* __restrict__ cu_q, int B, int row_begin, int k, int32_t* __restrict__ idx,
+                   const int32_t* __restrict__ cu_q, int B, int row_begin, int k, int n_init, int n_local, int32_t* __restrict__ idx,
                    int words_cap) {
     extern __shared__ __align__(16) unsigned char dsm[];
     BitmapSmem& sm = *reinterpret_cast<BitmapSmem*>(dsm);
@@ -260,6 +282,7 @@ topk_bitmap_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* 
         return;
     }
     const int W = (v + 31) / 32;
+    const Forced<FORCED> F = make_forced<FORCED>(v, n_init, n_local);
 
     // Visit every (index, key) of the row: 16-byte loads when the row is 16-byte aligned (several
     // loads in flight per thread), scalar otherwise and for the tail.
@@ -276,15 +299,16 @@ topk_bitmap_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* 
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int j = i + u * kTopkThreads;
-                fn(4 * j, order_key(a[u].x)); fn(4 * j + 1, order_key(a[u].y));
-                fn(4 * j + 2, order_key(a[u].z)); fn(4 * j + 3, order_key(a[u].w));
+                fn(4 * j, F(4 * j, order_key(a[u].x))); fn(4 * j + 1, F(4 * j + 1, order_key(a[u].y)));
+                fn(4 * j + 2, F(4 * j + 2, order_key(a[u].z))); fn(4 * j + 3, F(4 * j + 3, order_key(a[u].w)));
             }
         }
         for (; i < v4; i += kTopkThreads) {
             const float4 a = __ldg(row4 + i);
-            fn(4 * i, order_key(a.x)); fn(4 * i + 1, order_key(a.y)); fn(4 * i + 2, order_key(a.z)); fn(4 * i + 3, order_key(a.w));
+            fn(4 * i, F(4 * i, order_key(a.x))); fn(4 * i + 1, F(4 * i + 1, order_key(a.y)));
+            fn(4 * i + 2, F(4 * i + 2, order_key(a.z))); fn(4 * i + 3, F(4 * i + 3, order_key(a.w)));
         }
-        for (int s = 4 * v4 + threadIdx.x; s < v; s += kTopkThreads) fn(s, order_key(__ldg(row + s)));
+        for (int s = 4 * v4 + threadIdx.x; s < v; s += kTopkThreads) fn(s, F(s, order_key(__ldg(row + s))));
     };
 
     // ---- read 1: top-12-bit histogram
@@ -329,7 +353,7 @@ topk_bitmap_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* 
             }
         } else {
             for (int s = threadIdx.x; s < v; s += kTopkThreads) {
-                const uint32_t key = order_key(__ldg(row + s));
+                const uint32_t key = F(s, order_key(__ldg(row + s)));
                 if ((key >> hi) == (prefix >> hi)) atomicAdd(&sm.hist[(key >> shift) & 1023u], 1u);
             }
         }
@@ -350,7 +374,7 @@ topk_bitmap_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* 
         }
     } else {
         for (int s = threadIdx.x; s < v; s += kTopkThreads) {
-            const uint32_t key = order_key(__ldg(row + s));
+            const uint32_t key = F(s, order_key(__ldg(row + s)));
             if ((key >> 20) != b1) continue;
             if (key > kth) atomicOr(&sel[s >> 5], 1u << (s & 31));
             else if (key == kth) atomicOr(&tie[s >> 5], 1u << (s & 31));
@@ -431,9 +455,10 @@ __device__ __forceinline__ void sum_with_peer(const uint32_t* hist, uint32_t* to
     __syncthreads();
 }
 
+template <bool FORCED>
 __global__ void __launch_bounds__(kTopkThreads)
 topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* __restrict__ seq_lens,
-                    const int32_t* __restrict__ cu_q, int B, int row_begin, int k, int32_t* __restrict__ idx,
+                    const int32_t* __restrict__ cu_q, int B, int row_begin, int k, int n_init, int n_local, int32_t* __restrict__ idx,
                     int words_cap) {
     extern __shared__ __align__(16) unsigned char dsm[];
     BitmapSmem& sm = *reinterpret_cast<BitmapSmem*>(dsm);                      // hist: the top digit
@@ -470,6 +495,8 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t*
     const int nloc = (half == 0 ? split : v) - lo;
     const int W = (nloc + 31) / 32;
     const float* part = row + lo;
+    const Forced<FORCED> Fg = make_forced<FORCED>(v, n_init, n_local);
+    const Forced<FORCED> F = {Fg.init_end - lo, Fg.local_begin - lo};   // in this half's local indices
     for (int w = threadIdx.x; w < W; w += kTopkThreads) sel[w] = tie[w] = 0u;
 
     const bool vec = (reinterpret_cast<uintptr_t>(part) & 15u) == 0;
@@ -485,15 +512,16 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t*
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int j = i + u * kTopkThreads;
-                fn(4 * j, order_key(a[u].x)); fn(4 * j + 1, order_key(a[u].y));
-                fn(4 * j + 2, order_key(a[u].z)); fn(4 * j + 3, order_key(a[u].w));
+                fn(4 * j, F(4 * j, order_key(a[u].x))); fn(4 * j + 1, F(4 * j + 1, order_key(a[u].y)));
+                fn(4 * j + 2, F(4 * j + 2, order_key(a[u].z))); fn(4 * j + 3, F(4 * j + 3, order_key(a[u].w)));
             }
         }
         for (; i < v4; i += kTopkThreads) {
             const float4 a = __ldg(p4 + i);
-            fn(4 * i, order_key(a.x)); fn(4 * i + 1, order_key(a.y)); fn(4 * i + 2, order_key(a.z)); fn(4 * i + 3, order_key(a.w));
+            fn(4 * i, F(4 * i, order_key(a.x))); fn(4 * i + 1, F(4 * i + 1, order_key(a.y)));
+            fn(4 * i + 2, F(4 * i + 2, order_key(a.z))); fn(4 * i + 3, F(4 * i + 3, order_key(a.w)));
         }
-        for (int s = 4 * v4 + threadIdx.x; s < nloc; s += kTopkThreads) fn(s, order_key(__ldg(part + s)));
+        for (int s = 4 * v4 + threadIdx.x; s < nloc; s += kTopkThreads) fn(s, F(s, order_key(__ldg(part + s))));
     };
 
     // ---- read 1: top-12-bit histogram of this half, summed with the peer's
@@ -533,7 +561,7 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t*
             }
         } else {
             for (int s = threadIdx.x; s < nloc; s += kTopkThreads) {
-                const uint32_t key = order_key(__ldg(part + s));
+                const uint32_t key = F(s, order_key(__ldg(part + s)));
                 if ((key >> hi) == (prefix >> hi)) atomicAdd(&h[(key >> shift) & 1023u], 1u);
             }
         }
@@ -555,7 +583,7 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t*
         }
     } else {
         for (int s = threadIdx.x; s < nloc; s += kTopkThreads) {
-            const uint32_t key = order_key(__ldg(part + s));
+            const uint32_t key = F(s, order_key(__ldg(part + s)));
             if ((key >> 20) != b1) continue;
             if (key > kth) atomicOr(&sel[s >> 5], 1u << (s & 31));
             else if (key == kth) atomicOr(&tie[s >> 5], 1u << (s & 31));
@@ -620,11 +648,14 @@ extern "C" size_t dsa_topk_workspace_size(int32_t rows, int32_t k, int32_t max_s
     return 0;
 }
 
-extern "C" dsa_status dsa_topk(const float* logits, int64_t ld, const int32_t* seq_lens, const int32_t* cu_q,
-                               int32_t B, int32_t max_seq_len, int32_t row_begin, int32_t row_end, int32_t k,
-                               int32_t* idx, void* workspace, size_t workspace_bytes, void* stream) {
+extern "C" dsa_status dsa_topk_forced(const float* logits, int64_t ld, const int32_t* seq_lens, const int32_t* cu_q,
+                                      int32_t B, int32_t max_seq_len, int32_t row_begin, int32_t row_end, int32_t k,
+                                      int32_t n_init, int32_t n_local, int32_t* idx, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
     (void)workspace; (void)workspace_bytes;
     if (k < 1 || k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
+    if (n_init < 0 || n_local < 0) return DSA_ERR_INVALID_ARG;
+    const bool forced = n_init > 0 || n_local > 0;
     if (B < 0 || row_begin < 0 || row_end < row_begin || max_seq_len < 0) return DSA_ERR_INVALID_ARG;
     if (row_end == row_begin) return DSA_OK;
     if (B == 0 || !logits || !seq_lens || !cu_q || !idx) return DSA_ERR_INVALID_ARG;
@@ -652,8 +683,9 @@ extern "C" dsa_status dsa_topk(const float* logits, int64_t ld, const int32_t* s
         int words_cap = ((half_keys + 256 + 31) / 32 + 3) & ~3;
         if (words_cap < 32) words_cap = 32;
         const size_t smem = dsa::cluster_smem_bytes(words_cap);
-        if (cudaFuncSetAttribute(dsa::topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem)) != cudaSuccess)
+        auto kern = forced ? dsa::topk_cluster_kernel<true> : dsa::topk_cluster_kernel<false>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+            cudaSuccess)
             return DSA_ERR_CUDA;
         cudaLaunchAttribute cattr[2];
         cattr[0].id = cudaLaunchAttributeClusterDimension;
@@ -665,24 +697,36 @@ extern "C" dsa_status dsa_topk(const float* logits, int64_t ld, const int32_t* s
         cfg.attrs = cattr;
         cfg.numAttrs = 2;
         cfg.dynamicSmemBytes = smem;
-        if (cudaLaunchKernelEx(&cfg, dsa::topk_cluster_kernel, logits, ld, seq_lens, cu_q, static_cast<int>(B),
-                               static_cast<int>(row_begin), static_cast<int>(k), idx, words_cap) != cudaSuccess)
+        if (cudaLaunchKernelEx(&cfg, kern, logits, ld, seq_lens, cu_q, static_cast<int>(B),
+                               static_cast<int>(row_begin), static_cast<int>(k), n_init, n_local, idx, words_cap) !=
+                                   cudaSuccess)
             return DSA_ERR_CUDA;
     } else if (words <= dsa::kMaxBitmapWords) {
         const int words_cap = words < 32 ? 32 : words;
         const size_t smem = dsa::bitmap_smem_bytes(words_cap);
-        if (cudaFuncSetAttribute(dsa::topk_bitmap_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem)) != cudaSuccess)
+        auto kern = forced ? dsa::topk_bitmap_kernel<true> : dsa::topk_bitmap_kernel<false>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+            cudaSuccess)
             return DSA_ERR_CUDA;
         cfg.dynamicSmemBytes = smem;
-        if (cudaLaunchKernelEx(&cfg, dsa::topk_bitmap_kernel, logits, ld, seq_lens, cu_q, static_cast<int>(B),
-                               static_cast<int>(row_begin), static_cast<int>(k), idx, words_cap) != cudaSuccess)
+        if (cudaLaunchKernelEx(&cfg, kern, logits, ld, seq_lens, cu_q, static_cast<int>(B),
+                               static_cast<int>(row_begin), static_cast<int>(k), n_init, n_local, idx, words_cap) !=
+                                   cudaSuccess)
             return DSA_ERR_CUDA;
     } else {
         cfg.dynamicSmemBytes = 0;
-        if (cudaLaunchKernelEx(&cfg, dsa::topk_kernel, logits, ld, seq_lens, cu_q, static_cast<int>(B),
-                               static_cast<int>(row_begin), static_cast<int>(k), idx) != cudaSuccess)
+        auto kern = forced ? dsa::topk_kernel<true> : dsa::topk_kernel<false>;
+        if (cudaLaunchKernelEx(&cfg, kern, logits, ld, seq_lens, cu_q, static_cast<int>(B),
+                               static_cast<int>(row_begin), static_cast<int>(k), n_init, n_local, idx) !=
+                                   cudaSuccess)
             return DSA_ERR_CUDA;
     }
     return dsa::launch_status();
+}
+
+extern "C" dsa_status dsa_topk(const float* logits, int64_t ld, const int32_t* seq_lens, const int32_t* cu_q,
+                               int32_t B, int32_t max_seq_len, int32_t row_begin, int32_t row_end, int32_t k,
+                               int32_t* idx, void* workspace, size_t workspace_bytes, void* stream) {
+    return dsa_topk_forced(logits, ld, seq_lens, cu_q, B, max_seq_len, row_begin, row_end, k, 0, 0, idx, workspace,
+                           workspace_bytes, stream);
 }

@@ -245,6 +245,41 @@ dsa_status dsa_topk(const float* logits, int64_t ld, const int32_t* seq_lens, co
                     int32_t* idx, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * dsa_topk_forced -- dsa_topk with forced initial and local tokens.
+ * Source: sglang dsa_indexer.py, Indexer._mask_init_and_local_tokens (the logits of the first
+ * index_init_tokens and of the last index_local_tokens positions of each row are set to +inf
+ * before the top-k; the model config's index_init_tokens / index_local_tokens, 0 by default).
+ *   For row r with v_r visible keys, positions [0, min(n_init, v_r)) and [max(0, v_r - n_local),
+ *   v_r) count as +inf; then the rule of dsa_topk (ties, including a logit that is itself +inf,
+ *   go to the lower index).  n_init = n_local = 0 is dsa_topk.
+ *   n_init, n_local >= 0 (DSA_ERR_INVALID_ARG otherwise); other arguments as for dsa_topk.
+ */
+dsa_status dsa_topk_forced(const float* logits, int64_t ld, const int32_t* seq_lens, const int32_t* cu_q,
+                           int32_t B, int32_t max_seq_len, int32_t row_begin, int32_t row_end, int32_t k,
+                           int32_t n_init, int32_t n_local, int32_t* idx, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/*
+ * dsa_lightning_indexer -- indexer logits and top-k in one call that returns the indices.
+ * Source: vllm_ascend sfa_v1.py, the indexer's npu_lightning_indexer(query, key = paged index
+ * cache, weights, actual_seq_lengths_query / _key, block_table, sparse_count, sparse_mode = 3)
+ * returning topk_indices; sglang dsa_indexer.py, Indexer._get_topk_paged (logits, the
+ * init / local token mask, then topk_transform).
+ *   idx[r] = dsa_topk_forced(dsa_indexer_logits(...)[r]) for every row r < T.  The logits are
+ *   kept in `workspace` (dsa_lightning_indexer_workspace_size(T, max_seq_len) bytes, 16-byte
+ *   aligned) and are dead afterwards; the two stages are chained on the device.
+ * Arguments: as for dsa_indexer_logits (all rows, 0 .. T) and dsa_topk_forced; flags: as for
+ * dsa_indexer_logits.
+ */
+size_t dsa_lightning_indexer_workspace_size(int32_t T, int32_t max_seq_len);
+dsa_status dsa_lightning_indexer(const void* q_bf16, const float* weights, const uint8_t* index_k_pool,
+                                 int64_t num_pages, const int32_t* block_table, int32_t max_pages,
+                                 const int32_t* seq_lens, const int32_t* cu_q, int32_t B,
+                                 int32_t max_seq_len, int32_t max_q_len, int32_t T, int32_t k,
+                                 int32_t n_init, int32_t n_local, uint32_t flags, int32_t* idx,
+                                 void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream);
+
+/*
  * dsa_sparse_mla_decode -- absorbed sparse MLA over the selected latent rows.
  * Source: vllm_ascend sfa_v1.py, _execute_sparse_flash_attention_process
  * (npu_sparse_flash_attention(query = ql_nope, key = value = latent cache, sparse_indices =

@@ -76,6 +76,26 @@ def test_topk_rows_that_mislead_the_sample(v, k):
     assert np.array_equal(got, ref)
 
 
+@pytest.mark.parametrize("v,k,n_init,n_local", [(100, 16, 2, 3), (5000, 2048, 4, 64), (20000, 2048, 1, 1),
+                                                 (70000, 2048, 16, 512), (70000, 100, 0, 300), (140000, 2048, 4, 64),
+                                                 (3000, 64, 3000, 0)])
+def test_topk_forced_init_and_local_tokens(v, k, n_init, n_local):
+    rng = np.random.default_rng(230 + v + n_local)
+    lg = np.full((3, v + 4), np.nan, np.float32)
+    lg[0, :v] = rng.standard_normal(v).astype(np.float32)
+    lg[1, :v] = rng.integers(-8, 8, v).astype(np.float32)      # heavy ties
+    lg[2, :v] = rng.standard_normal(v).astype(np.float32)
+    lg[2, v // 3] = np.inf                                      # ties with the forced positions by index
+    seq_lens = np.array([v, v, v], np.int32)
+    cu = np.array([0, 1, 2, 3], np.int32)
+    dev = torch.from_numpy(lg).cuda()
+    idx = torch.empty((3, k), dtype=torch.int32, device="cuda")
+    capi.dsa_topk(dev, torch.from_numpy(seq_lens).cuda(), torch.from_numpy(cu).cuda(), v, k, idx,
+                  n_init=n_init, n_local=n_local)
+    ref = oracle.topk_forced(lg, seq_lens, cu, np.arange(3), k, n_init, n_local)
+    assert np.array_equal(idx.cpu().numpy(), ref)
+
+
 def test_topk_next_n_rows_use_their_own_length():
     rng = np.random.default_rng(210)
     L = 3000
@@ -152,3 +172,23 @@ def test_mla_workspace_too_small_is_rejected():
         capi.dsa_sparse_mla_decode(db.mla_q, db.kv_pool, db.block_table, db.seq_lens, db.cu_q, idx, wl.scale,
                                    db.out, db.mla_ws[:16])
     assert e.value.status == capi.DSA_ERR_INVALID_ARG
+
+
+def test_lightning_indexer_equals_logits_then_topk():
+    """The one-call indexer returns exactly the indices of the logits call followed by the top-k
+    call (the same kernels), with and without forced tokens."""
+    wl = workloads.make_custom("li", 240, [500, 64, 3000, 17000, 40000], [1, 2, 3, 1, 1], topk=256, heads=16)
+    db = DeviceBatch(wl, with_latent=False)
+    db.indexer_logits()
+    ws = torch.empty(capi.dsa_lightning_indexer_workspace_size(wl.T, wl.max_seq_len), dtype=torch.uint8,
+                     device="cuda")
+    for n_init, n_local in ((0, 0), (2, 8)):
+        ref = torch.empty((wl.T, wl.topk), dtype=torch.int32, device="cuda")
+        capi.dsa_topk(db.logits, db.seq_lens, db.cu_q, wl.max_seq_len, wl.topk, ref, n_init=n_init, n_local=n_local)
+        got = torch.full((wl.T, wl.topk), -7, dtype=torch.int32, device="cuda")
+        capi.dsa_lightning_indexer(db.index_q, db.weights, db.index_pool, db.block_table, db.seq_lens, db.cu_q,
+                                   wl.max_seq_len, wl.max_q_len, wl.topk, got, ws, n_init=n_init, n_local=n_local)
+        assert torch.equal(got, ref)
+    with pytest.raises(capi.DSAError):     # short workspace
+        capi.dsa_lightning_indexer(db.index_q, db.weights, db.index_pool, db.block_table, db.seq_lens, db.cu_q,
+                                   wl.max_seq_len, wl.max_q_len, wl.topk, got, ws[:1024])
