@@ -65,6 +65,7 @@ class DeviceBatch:
                                    dtype=torch.uint8, device=dev)
         self.kv_pool = None
         self.mla_q = None
+        self._io_in = self._io_out = None
         if with_latent:
             self.kv_pool = _bf16(wl.latent_pool(), dev)
             self.mla_q = _bf16(wl.mla_q(), dev)
@@ -72,6 +73,105 @@ class DeviceBatch:
             self.lse = torch.empty((wl.T, wl.heads), dtype=torch.float32, device=dev)
             self.mla_ws = torch.empty(max(16, capi.dsa_sparse_mla_workspace_size(wl.T, wl.heads, wl.topk)),
                                       dtype=torch.uint8, device=dev)
+            self._pack_io()
+
+    # ---- packed step I/O: one contiguous device buffer for the inputs, one for the outputs
+    @staticmethod
+    def _packed(tensors, device):
+        """A byte buffer holding `tensors` at 256-byte aligned offsets, and views of it shaped like them."""
+        offs, total = [], 0
+        for t in tensors:
+            offs.append(total)
+            total += (t.numel() * t.element_size() + 255) // 256 * 256
+        buf = torch.zeros(max(total, 256), dtype=torch.uint8, device=device)   # padding stays zero
+        views = [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for o, t in zip(offs, tensors)]
+        return buf, views
+
+    def _pack_io(self):
+        """Re-home the step's host-fed inputs and its outputs in two packed buffers, so that a step
+        moves one block each way; the named tensors become views of those buffers."""
+        ins = self.io_inputs()
+        self._io_in, views = self._packed(ins, self.device)
+        for v, t in zip(views, ins):
+            v.copy_(t)
+        (self.index_q, self.weights, self.mla_q, self.new_keys, self.new_slots, self.seq_lens, self.cu_q,
+         self.block_table) = views
+        self._io_out, (self.out, self.lse) = self._packed(self.io_outputs(), self.device)
+
+    def io_buffers(self):
+        """(inputs, outputs): the packed device byte buffers behind io_inputs() / io_outputs()."""
+        return self._io_in, self._io_out
+
+    def _bind_io(self, ins_views, out_views):
+        (self.index_q, self.weights, self.mla_q, self.new_keys, self.new_slots, self.seq_lens, self.cu_q,
+         self.block_table) = ins_views
+        self.out, self.lse = out_views
+
+    def run_io(self, host_ins, host_outs, stream=None):
+        """A sequence of decode steps end to end, pipelined: step i copies host_ins[i] (pinned,
+        shaped like io_buffers()[0]) to the device, runs the four calls and copies the outputs into
+        host_outs[i] (pinned, like io_buffers()[1]).  Two device input / output sets alternate, so
+        the host->device copy of step i + 1 and the device->host copy of step i - 1 run on their
+        own streams while step i computes; events keep a set's inputs until its step has read them
+        and its outputs until they have been copied out.  Every step moves its data.  The four
+        calls of a step are one CUDA graph per set.  Returns when everything is enqueued; the work
+        is ordered after `stream` and `stream` waits for all of it."""
+        if self._io_in is None:
+            raise RuntimeError("run_io needs the latent cache (DeviceBatch(with_latent=True))")
+        if len(host_ins) != len(host_outs):
+            raise ValueError("one output buffer per input buffer")
+        stream = torch.cuda.current_stream(self.device) if stream is None else stream
+        if not hasattr(self, "_pipe"):
+            primary = (self.io_inputs(), self.io_outputs())
+            in2, in_views2 = self._packed(primary[0], self.device)
+            out2, out_views2 = self._packed(primary[1], self.device)
+            in2.copy_(self._io_in)
+            sets = [(self._io_in, self._io_out, primary[0], primary[1]), (in2, out2, in_views2, out_views2)]
+            side = torch.cuda.Stream(self.device)
+            side.wait_stream(stream)
+            graphs = []
+            for _, _, iv, ov in sets:
+                self._bind_io(iv, ov)
+                with torch.cuda.stream(side):
+                    self.step(stream=side)   # warm the path outside capture
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=side):
+                    self.step(stream=torch.cuda.current_stream(self.device))
+                graphs.append(g)
+            stream.wait_stream(side)
+            self._bind_io(*primary)
+            self._pipe = {"sets": sets, "graphs": graphs,
+                          "h2d": torch.cuda.Stream(self.device), "d2h": torch.cuda.Stream(self.device),
+                          "ev": [[torch.cuda.Event() for _ in range(3)] for _ in range(2)]}
+        p = self._pipe
+        h2d, d2h = p["h2d"], p["d2h"]
+        h2d.wait_stream(stream)
+        d2h.wait_stream(stream)
+        used = [False, False]
+        for i, (hin, hout) in enumerate(zip(host_ins, host_outs)):
+            k = i & 1
+            din, dout, _, _ = p["sets"][k]
+            ev_in, ev_comp, ev_out = p["ev"][k]
+            if hin.numel() != din.numel() or hout.numel() != dout.numel():
+                raise ValueError("host buffers must match io_buffers()")
+            if used[k]:
+                h2d.wait_event(ev_comp)          # the set's inputs have been read by its last step
+            with torch.cuda.stream(h2d):
+                din.copy_(hin, non_blocking=True)
+            ev_in.record(h2d)
+            stream.wait_event(ev_in)
+            if used[k]:
+                stream.wait_event(ev_out)        # the set's last outputs have been copied out
+            with torch.cuda.stream(stream):
+                p["graphs"][k].replay()
+            ev_comp.record(stream)
+            d2h.wait_event(ev_comp)
+            with torch.cuda.stream(d2h):
+                hout.copy_(dout, non_blocking=True)
+            ev_out.record(d2h)
+            used[k] = True
+        stream.wait_stream(d2h)
+        stream.wait_stream(h2d)
 
     # ---- the four stages
     def store_new_keys(self, stream=None):
@@ -117,12 +217,17 @@ class DeviceBatch:
 
     def step_io(self, host_in, host_out, stream=None, graph: bool = True):
         """One decode step end to end: copy `host_in` (pinned host tensors shaped like
-        io_inputs()) to the device, run step(), copy io_outputs() into `host_out` (pinned host
-        tensors).  With graph=True the copies and the four library calls are captured once per
+        io_inputs(), or a one-element list holding a pinned copy of the packed io_buffers()[0])
+        to the device, run step(), copy io_outputs() (or the packed io_buffers()[1]) into
+        `host_out`.  With graph=True the copies and the four library calls are captured once per
         (host_in, host_out) set as one CUDA graph and replayed on later calls; every replay moves
         the data again.  Returns when the work is enqueued on `stream`."""
         stream = torch.cuda.current_stream(self.device) if stream is None else stream
         ins, outs = self.io_inputs(), self.io_outputs()
+        if len(host_in) == 1 and len(host_out) == 1 and self._io_in is not None:
+            ins, outs = [self._io_in], [self._io_out]
+            if host_in[0].numel() != ins[0].numel() or host_out[0].numel() != outs[0].numel():
+                raise ValueError("packed host buffers must match io_buffers()")
         if len(host_in) != len(ins) or len(host_out) != len(outs):
             raise ValueError("host_in / host_out must match io_inputs() / io_outputs()")
 

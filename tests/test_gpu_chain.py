@@ -141,6 +141,62 @@ def test_step_io_graph_matches_eager_step():
     assert db.device_error() == (0, 0)
 
 
+def test_step_io_packed_buffers_match_eager_step():
+    """The packed form of step_io (one pinned block in, one out) gives the eager step's outputs
+    and moves fresh host data on every replay."""
+    wl = workloads.make("tiny")
+    db = DeviceBatch(wl)
+    db.step()
+    ref_out = db.out.clone()
+    dev_in, dev_out = db.io_buffers()
+    host_in = [dev_in.cpu().pin_memory()]
+    host_out = [torch.empty_like(dev_out, device="cpu").pin_memory()]
+    for _ in range(2):   # capture, then replay
+        host_out[0].zero_()
+        db.step_io(host_in, host_out)
+        torch.cuda.synchronize()
+        assert torch.equal(db.out, ref_out)
+        assert torch.equal(host_out[0], dev_out.cpu())
+    # a changed query on the host reaches the device on replay
+    q_off = db.mla_q.data_ptr() - dev_in.data_ptr()
+    mod = dev_in.clone()
+    mod[q_off:q_off + db.mla_q.numel() * 2].view(torch.bfloat16).neg_()
+    host_in[0].copy_(mod.cpu())
+    db.step_io(host_in, host_out)
+    torch.cuda.synchronize()
+    assert not torch.equal(db.out, ref_out)
+    assert torch.equal(host_out[0], dev_out.cpu())
+    assert db.device_error() == (0, 0)
+
+
+def test_run_io_pipelined_steps_match_eager_steps():
+    """run_io over several steps with different host inputs: every step's outputs equal the eager
+    step's outputs for that step's inputs (the two device I/O sets and the overlapped copies keep
+    each step's data apart)."""
+    wl = workloads.make("tiny")
+    db = DeviceBatch(wl)
+    dev_in, dev_out = db.io_buffers()
+    q_off = db.mla_q.data_ptr() - dev_in.data_ptr()
+    nq = db.mla_q.numel() * 2
+    base = dev_in.clone()
+    host_ins, refs = [], []
+    for i in range(5):                       # step i: the query scaled by (1 + i / 4)
+        mod = base.clone()
+        mod[q_off:q_off + nq].view(torch.bfloat16).mul_(1.0 + i / 4.0)
+        dev_in.copy_(mod)
+        db.step()
+        torch.cuda.synchronize()
+        refs.append(dev_out.cpu().clone())
+        host_ins.append(mod.cpu().pin_memory())
+    host_outs = [torch.zeros_like(refs[0]).pin_memory() for _ in range(5)]
+    db.run_io(host_ins, host_outs)
+    torch.cuda.synchronize()
+    for i in range(5):
+        assert torch.equal(host_outs[i], refs[i]), f"step {i}"
+    assert not torch.equal(refs[0], refs[1])
+    assert db.device_error() == (0, 0)
+
+
 def test_back_to_back_calls_keep_stream_order():
     """The logits, top-k and attention kernels overlap their successors' launch; a call that
     overwrites a buffer the previous call still reads must still see stream order.  Here a second
