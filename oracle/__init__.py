@@ -63,11 +63,12 @@ def _load():
         "dsa_oracle_fwht128": (None, [P]),
         "dsa_oracle_rotate128": (None, [P, P]),
         "dsa_oracle_quant128": (None, [P, P, P]),
+        "dsa_oracle_quant128_fmt": (None, [P, P, P, ctypes.c_int]),
         "dsa_oracle_store_index_k": (i64, [P, P, i64, P, i64]),
         "dsa_oracle_k_norm128": (None, [P, P, P, ctypes.c_float, ctypes.c_int, P]),
         "dsa_oracle_rope64": (None, [P, P, ctypes.c_int, P]),
         "dsa_oracle_store_index_k_prologue": (i64, [P, P, P, ctypes.c_float, ctypes.c_int, P, i64, P, ctypes.c_int,
-                                                    ctypes.c_int, P, i64, P, i64]),
+                                                    ctypes.c_int, ctypes.c_int, P, i64, P, i64]),
         "dsa_oracle_rope_q": (i64, [P, P, i64, P, ctypes.c_int, i64, P]),
         "dsa_oracle_visible_len": (i32, [P, P, i32, i64]),
         "dsa_oracle_indexer_logits": (i64, [P, P, P, i64, P, i32, P, P, i32, i32, P, i64, P, i64, P]),
@@ -144,13 +145,17 @@ def rotate128(x_bf16: np.ndarray) -> np.ndarray:
     return out
 
 
-def quant128(y: np.ndarray):
-    """Per-128 FP8 quantisation: returns (codes uint8[128], scale float32)."""
+def quant128(y: np.ndarray, ue8m0: bool = False):
+    """Per-128 FP8 quantisation: returns (codes uint8[128], scale float32); ``ue8m0`` rounds the
+    scale up to a power of two."""
     v = _c(y, np.float32)
     assert v.shape == (DI,)
     codes = np.empty(DI, np.uint8)
     s = np.empty(1, np.float32)
-    _load().dsa_oracle_quant128(_p(v), _p(codes), _p(s))
+    if ue8m0:
+        _load().dsa_oracle_quant128_fmt(_p(v), _p(codes), _p(s), 1)
+    else:
+        _load().dsa_oracle_quant128(_p(v), _p(codes), _p(s))
     return codes, s[0]
 
 
@@ -187,9 +192,9 @@ def rope64(x_bf16: np.ndarray, cos_sin_row: np.ndarray, neox: bool = True) -> np
 
 def store_index_k_prologue(k_raw: np.ndarray, w: np.ndarray, b, eps: float, cos_sin: np.ndarray,
                            positions: np.ndarray, slot_mapping: np.ndarray, pool: np.ndarray, rms: bool = False,
-                           neox: bool = True, rotate: bool = True) -> int:
-    """Norm, rotary embedding, rotate (unless ``rotate`` is False), quantise and scatter raw keys
-    into ``pool`` in place."""
+                           neox: bool = True, rotate: bool = True, ue8m0: bool = False) -> int:
+    """Norm, rotary embedding, rotate (unless ``rotate`` is False), quantise (power-of-two scales
+    with ``ue8m0``) and scatter raw keys into ``pool`` in place."""
     k = _c(k_raw, np.uint16).reshape(-1, DI)
     wv = _c(w, np.float32)
     bv = _c(np.zeros(DI) if b is None else b, np.float32)
@@ -199,7 +204,7 @@ def store_index_k_prologue(k_raw: np.ndarray, w: np.ndarray, b, eps: float, cos_
     assert pool.dtype == np.uint8 and pool.flags["C_CONTIGUOUS"] and pool.shape[1] == PAGE_BYTES
     return int(_load().dsa_oracle_store_index_k_prologue(_p(k), _p(wv), _p(bv), float(eps), int(bool(rms)), _p(cs),
                                                          cs.shape[0], _p(pos), int(bool(neox)), int(bool(rotate)),
-                                                         _p(slots),
+                                                         int(bool(ue8m0)), _p(slots),
                                                          k.shape[0], _p(pool), pool.shape[0]))
 
 
@@ -220,7 +225,7 @@ def visible_len(seq_lens, cu_q, r: int) -> int:
 
 
 def indexer_logits(q_bf16, w, pool, block_table, seq_lens, cu_q, rows, ld, rotate_q=False,
-                   want_mag=False, fill=np.nan):
+                   want_mag=False, fill=np.nan, ue8m0_q=False):
     """Indexer logits for the global rows ``rows``; returns float32 [len(rows), ld] (and the
     float64 magnitude array when ``want_mag``).  Entries past each row's visible length keep
     ``fill``."""
@@ -235,7 +240,8 @@ def indexer_logits(q_bf16, w, pool, block_table, seq_lens, cu_q, rows, ld, rotat
     mag = np.zeros((rr.shape[0], ld), np.float64) if want_mag else None
     bad = _load().dsa_oracle_indexer_logits(
         _p(q), _p(wv), _p(pool), pool.shape[0], _p(bt), bt.shape[1], _p(sl), _p(cq), sl.shape[0],
-        int(bool(rotate_q)), _p(rr), rr.shape[0], _p(out), ld, _p(mag) if mag is not None else None)
+        int(bool(rotate_q)) | (int(bool(ue8m0_q)) << 1), _p(rr), rr.shape[0], _p(out), ld,
+        _p(mag) if mag is not None else None)
     if want_mag:
         return out, mag, int(bad)
     return out

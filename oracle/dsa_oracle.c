@@ -175,19 +175,32 @@ void dsa_oracle_rotate128(const uint16_t* in_bf16, uint16_t* out_bf16) {
  * Reading of the unprinted formula: amax = max |y|; scale = max(amax, 1e-4) / 448 in fp32 with
  * IEEE division; code = E4M3FN(y / scale) with IEEE fp32 division then round-to-nearest-even and
  * saturation.  The scale is plain fp32 (no power-of-two rounding). */
-void dsa_oracle_quant128(const float* y, uint8_t* codes, float* scale) {
+/* Quantisation with the scale format of act_quant's scale_fmt ([idx] Indexer(scale_fmt=...),
+ * act_quant(x, block_size, scale_fmt); the rule itself is not printed).  Reading: plain format:
+ * the fp32 scale above; "ue8m0" (an unsigned 8-bit exponent, no mantissa): the smallest power of
+ * two >= that fp32 scale, so that every |y / scale| <= 448 still holds. */
+static float pow2_at_least(float s) {
+    int e;
+    const float m = frexpf(s, &e); /* s = m * 2^e, m in [0.5, 1) */
+    return m == 0.5f ? s : ldexpf(1.0f, e);
+}
+
+void dsa_oracle_quant128_fmt(const float* y, uint8_t* codes, float* scale, int ue8m0) {
     float amax = 0.0f;
     for (int d = 0; d < DI; ++d) {
         float a = fabsf(y[d]);
         if (a > amax) amax = a;
     }
     float s = fmaxf(amax, 1e-4f) / 448.0f;
+    if (ue8m0) s = pow2_at_least(s);
     for (int d = 0; d < DI; ++d) {
         float t = y[d] / s;
         codes[d] = dsa_oracle_e4m3_encode(t);
     }
     *scale = s;
 }
+
+void dsa_oracle_quant128(const float* y, uint8_t* codes, float* scale) { dsa_oracle_quant128_fmt(y, codes, scale, 0); }
 
 /* ---------------------------------------------------------------- index-K store */
 
@@ -202,7 +215,7 @@ void dsa_oracle_quant128(const float* y, uint8_t* codes, float* scale) {
  * Returns the number of tokens whose slot pointed past the pool (those are skipped). */
 /* Quantise one bf16 key (rotated first when `rotate`) into its slot; returns 1 when the slot is
  * past the pool (nothing written), else 0. */
-static int store_one(const uint16_t* key, int rotate, int64_t slot, uint8_t* pool, int64_t num_pages) {
+static int store_one(const uint16_t* key, int rotate, int ue8m0, int64_t slot, uint8_t* pool, int64_t num_pages) {
     int64_t page = slot / PAGE, row = slot % PAGE;
     if (page >= num_pages) return 1;
     uint16_t rot[DI];
@@ -212,7 +225,7 @@ static int store_one(const uint16_t* key, int rotate, int64_t slot, uint8_t* poo
     if (rotate) dsa_oracle_rotate128(key, rot);
     else memcpy(rot, key, sizeof(rot));
     for (int d = 0; d < DI; ++d) y[d] = bf16_bits_to_f32(rot[d]);
-    dsa_oracle_quant128(y, codes, &s);
+    dsa_oracle_quant128_fmt(y, codes, &s, ue8m0);
     uint8_t* pg = pool + page * PAGE_BYTES;
     memcpy(pg + row * DI, codes, DI);
     memcpy(pg + PAGE * DI + row * 4, &s, 4);
@@ -224,7 +237,7 @@ int64_t dsa_oracle_store_index_k(const uint16_t* k_bf16, const int64_t* slot_map
     int64_t bad = 0;
     for (int64_t t = 0; t < n; ++t) {
         if (slot_mapping[t] < 0) continue;
-        bad += store_one(k_bf16 + t * DI, 1, slot_mapping[t], pool, num_pages);
+        bad += store_one(k_bf16 + t * DI, 1, 0, slot_mapping[t], pool, num_pages);
     }
     return bad;
 }
@@ -305,8 +318,8 @@ void dsa_oracle_rope64(const uint16_t* in_bf16, const float* cs, int neox, uint1
  * skipped tokens (slot past the pool or position out of range). */
 int64_t dsa_oracle_store_index_k_prologue(const uint16_t* k_raw, const float* w, const float* b, float eps, int rms,
                                           const float* cos_sin, int64_t max_pos, const int64_t* positions,
-                                          int neox, int rotate, const int64_t* slot_mapping, int64_t n,
-                                          uint8_t* pool, int64_t num_pages) {
+                                          int neox, int rotate, int ue8m0, const int64_t* slot_mapping,
+                                          int64_t n, uint8_t* pool, int64_t num_pages) {
     int64_t bad = 0;
     for (int64_t t = 0; t < n; ++t) {
         if (slot_mapping[t] < 0) continue;
@@ -314,7 +327,7 @@ int64_t dsa_oracle_store_index_k_prologue(const uint16_t* k_raw, const float* w,
         uint16_t nrm[DI], rop[DI];
         dsa_oracle_k_norm128(k_raw + t * DI, w, b, eps, rms, nrm);
         dsa_oracle_rope64(nrm, cos_sin + positions[t] * 64, neox, rop);
-        bad += store_one(rop, rotate, slot_mapping[t], pool, num_pages);
+        bad += store_one(rop, rotate, ue8m0, slot_mapping[t], pool, num_pages);
     }
     return bad;
 }
@@ -371,7 +384,8 @@ int32_t dsa_oracle_visible_len(const int32_t* seq_lens, const int32_t* cu_q, int
  * with w'[r,h] = w[r,h] * q_scale[r,h] (the query scale folded into the head gate, as
  * _get_logits_head_gate multiplies the gate by q_scale) and the query quantised per head by the
  * same per-128 rule as the keys.  The input w already carries n_heads^-0.5 * head_dim^-0.5.
- * rotate_q != 0 first rotates each query head (the pages rotate q before quantising it).
+ * q_mode bit 0 first rotates each query head (the pages rotate q before quantising it); bit 1
+ * quantises the query with the ue8m0 scale format (see dsa_oracle_quant128_fmt).
  * Computed in double, rounded once to fp32.  Only s < v_r is written.
  * rows[i] lists the global rows to compute; output row i goes to logits[i*ld ...].
  * mag (nullable, double [n_rows, ld]) receives sum_h |w'| * ReLU(...), the magnitude of the
@@ -380,7 +394,7 @@ int32_t dsa_oracle_visible_len(const int32_t* seq_lens, const int32_t* cu_q, int
 int64_t dsa_oracle_indexer_logits(const uint16_t* q_bf16, const float* w, const uint8_t* pool,
                                   int64_t num_pages, const int32_t* block_table, int32_t max_pages,
                                   const int32_t* seq_lens, const int32_t* cu_q, int32_t B,
-                                  int32_t rotate_q, const int64_t* rows, int64_t n_rows,
+                                  int32_t q_mode, const int64_t* rows, int64_t n_rows,
                                   float* logits, int64_t ld, double* mag) {
     int64_t bad = 0;
     for (int64_t i = 0; i < n_rows; ++i) {
@@ -396,12 +410,12 @@ int64_t dsa_oracle_indexer_logits(const uint16_t* q_bf16, const float* w, const 
             uint16_t rot[DI];
             float y[DI];
             float sq;
-            if (rotate_q) {
+            if (q_mode & 1) {
                 dsa_oracle_rotate128(src, rot);
                 src = rot;
             }
             for (int d = 0; d < DI; ++d) y[d] = bf16_bits_to_f32(src[d]);
-            dsa_oracle_quant128(y, cq[h], &sq);
+            dsa_oracle_quant128_fmt(y, cq[h], &sq, (q_mode >> 1) & 1);
             wq[h] = (double)w[r * HI + h] * (double)sq;
         }
         double dq[HI][DI];

@@ -159,3 +159,69 @@ def test_store_layout_and_padding_slots():
         touched[page, row * 128:(row + 1) * 128] = True
         touched[page, 8192 + row * 4:8192 + row * 4 + 4] = True
     assert np.all(pool[~touched] == 0xAB)
+
+
+def test_ue8m0_scale_is_the_smallest_power_of_two_not_below_the_plain_scale():
+    rng = np.random.default_rng(77)
+    cases = [rng.standard_normal(128) * 10.0 ** rng.uniform(-6, 3) for _ in range(200)]
+    cases.append(np.full(128, 448.0 * 2.0 ** -3))        # plain scale exactly 2^-3: kept
+    cases.append(np.zeros(128))                            # floor 1e-4 / 448
+    for y in cases:
+        y = np.asarray(y, np.float32)
+        _, s_plain = oracle.quant128(y)
+        codes, s = oracle.quant128(y, ue8m0=True)
+        m, e = math.frexp(float(s))
+        assert m == 0.5                                    # a power of two
+        assert s >= s_plain and (s == s_plain or s / 2 < s_plain)
+        # dividing by a power of two is exact: the codes are torch's conversion of y / s
+        ref = torch.from_numpy(y / np.float32(s)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(codes, ref)
+        dec = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+        assert np.all(np.abs(dec) <= 448.0)
+
+
+def test_ue8m0_key_store_writes_power_of_two_scales():
+    """With ue8m0 the stored scale of every key (through the fused key prologue) is a power of two."""
+    rng = np.random.default_rng(78)
+    n, pages, max_pos = 64, 1, 128
+    k_raw = bf16_bits(rng.standard_normal((n, 128)))
+    w = np.ones(128, np.float32)
+    b = np.zeros(128, np.float32)
+    cs = np.concatenate([np.ones((max_pos, 32)), np.zeros((max_pos, 32))], axis=1).astype(np.float32)  # identity rope
+    pos = np.arange(n, dtype=np.int64)
+    slots = np.arange(n, dtype=np.int64)
+    pool = np.zeros((pages, oracle.PAGE_BYTES), np.uint8)
+    assert oracle.store_index_k_prologue(k_raw, w, b, 1e-6, cs, pos, slots, pool, ue8m0=True) == 0
+    scales = pool[0, 64 * 128:].view(np.float32)
+    for sc in scales:
+        assert math.frexp(float(sc))[0] == 0.5
+
+
+def test_ue8m0_query_equals_plain_when_the_plain_scale_is_a_power_of_two():
+    """Query heads whose amax is 448 * 2^-j have a plain fp32 scale of exactly 2^-j, so the ue8m0
+    and plain query quantisations coincide and so do the logits; for general heads they differ
+    by no more than the FP8 rounding allows."""
+    from deepseek_sparse_attention_paged_gb300 import workloads
+    wl = workloads.make("tiny")
+    pool = np.zeros((wl.num_pages, oracle.PAGE_BYTES), np.uint8)
+    assert oracle.store_index_k(wl.index_keys(), wl.token_slots(), pool) == 0
+    rng = np.random.default_rng(79)
+    q = rng.standard_normal((wl.T, 64, 128)).astype(np.float32)
+    q /= np.abs(q).max(axis=-1, keepdims=True)
+    q *= (448.0 * 2.0 ** -rng.integers(2, 9, (wl.T, 64, 1))).astype(np.float32)
+    qb = bf16_bits(q)
+    assert np.all(bf16_value(qb).reshape(wl.T, 64, 128).__abs__().max(-1) == np.abs(q).max(-1))
+    rows = np.arange(wl.T)
+    plain = oracle.indexer_logits(qb, wl.weights(), pool, wl.block_table, wl.seq_lens, wl.cu_q, rows, 1000)
+    pow2 = oracle.indexer_logits(qb, wl.weights(), pool, wl.block_table, wl.seq_lens, wl.cu_q, rows, 1000,
+                                 ue8m0_q=True)
+    assert np.array_equal(plain, pow2, equal_nan=True)
+    qg = bf16_bits(rng.standard_normal((wl.T, 64, 128)) * 3.0)
+    p2, mag, _ = oracle.indexer_logits(qg, wl.weights(), pool, wl.block_table, wl.seq_lens, wl.cu_q, rows, 1000,
+                                       ue8m0_q=True, want_mag=True)
+    pl = oracle.indexer_logits(qg, wl.weights(), pool, wl.block_table, wl.seq_lens, wl.cu_q, rows, 1000)
+    v = wl.visible_lens()
+    for i in range(wl.T):
+        d = np.abs(p2[i, :v[i]].astype(np.float64) - pl[i, :v[i]])
+        assert np.all(d <= 2.0 ** -3 * mag[i, :v[i]] + 1e-6)      # two e4m3 roundings of each product term
+        assert d.max() > 0                                           # the formats do differ
