@@ -33,6 +33,7 @@ DSA_Q_ROTATE = 0x1
 DSA_NORM_RMS = 0x2
 DSA_ROPE_INTERLEAVED = 0x4
 DSA_K_NO_ROTATE = 0x8
+DSA_SCALE_UE8M0 = 0x10
 PAGE_SIZE = 64
 INDEX_PAGE_BYTES = 64 * 132
 LATENT_DIM = 576

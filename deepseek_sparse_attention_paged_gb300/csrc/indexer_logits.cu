@@ -29,7 +29,13 @@ constexpr float kInvSqrt128 = 0x1.6a09e6p-4f;
 // Quantise one 128-wide query head held as 4 values per lane (lane l: dims 4l .. 4l+3), with the
 // optional Hadamard rotation first (same butterflies and rounding as the key store).  Returns the
 // 4 codes packed little-endian and the fp32 scale.
-__device__ __forceinline__ uint32_t quantise_head(float x[4], bool rotate, int lane, float* scale_out) {
+// Scale format "ue8m0": the smallest power of two not below the fp32 scale s (s positive, normal).
+__device__ __forceinline__ float pow2_at_least(float s) {
+    const uint32_t u = __float_as_uint(s);
+    return (u & 0x007fffffu) ? __uint_as_float((u & 0x7f800000u) + 0x00800000u) : s;
+}
+
+__device__ __forceinline__ uint32_t quantise_head(float x[4], bool rotate, bool ue8m0, int lane, float* scale_out) {
     if (rotate) {
         {
             float a = x[0], b = x[1];
@@ -57,7 +63,8 @@ __device__ __forceinline__ uint32_t quantise_head(float x[4], bool rotate, int l
     }
     float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
     amax = warp_max(amax);
-    const float scale = __fdiv_rn(fmaxf(amax, 1e-4f), 448.0f);
+    float scale = __fdiv_rn(fmaxf(amax, 1e-4f), 448.0f);
+    if (ue8m0) scale = pow2_at_least(scale);
     uint32_t packed = 0;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -83,7 +90,7 @@ constexpr int kLoaderWarp = 10;
 // ---------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256)
 indexer_q_prologue_kernel(const uint16_t* __restrict__ q, const float* __restrict__ w,
-                          const int32_t* __restrict__ cu_q, int B, int row_begin, int row_end, int rotate,
+                          const int32_t* __restrict__ cu_q, int B, int row_begin, int row_end, int mode,
                           uint8_t* __restrict__ q_codes, float* __restrict__ q_gates) {
     ptx::griddep_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -95,7 +102,7 @@ indexer_q_prologue_kernel(const uint16_t* __restrict__ q, const float* __restric
     const uint2 raw = __ldg(reinterpret_cast<const uint2*>(q + (r * kIndexHeads + h) * kIndexDim) + lane);
     float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
     float scale;
-    const uint32_t packed = quantise_head(x, rotate != 0, lane, &scale);
+    const uint32_t packed = quantise_head(x, (mode & 1) != 0, (mode & 2) != 0, lane, &scale);
     uint8_t* dst = q_codes + (v / kIndexHeads) * kQRowBytes;
     const uint32_t off = h * 128 + (((lane >> 2) ^ (h & 7)) << 4) + ((lane & 3) << 2);
     *reinterpret_cast<uint32_t*>(dst + off) = packed;
@@ -521,7 +528,7 @@ extern "C" dsa_status dsa_indexer_logits(const void* q_bf16, const float* weight
     if (B < 0 || max_seq_len < 0 || max_q_len < 0 || row_begin < 0 || row_end < row_begin || max_pages < 0 ||
         num_pages < 0)
         return DSA_ERR_INVALID_ARG;
-    if ((flags & ~DSA_Q_ROTATE) != 0u) return DSA_ERR_INVALID_ARG;
+    if ((flags & ~(DSA_Q_ROTATE | DSA_SCALE_UE8M0)) != 0u) return DSA_ERR_INVALID_ARG;
     if (B == 0 || row_end == row_begin || max_seq_len == 0 || max_q_len == 0) return DSA_OK;
     if (!q_bf16 || !weights || !index_k_pool || !block_table || !seq_lens || !cu_q || !logits || !workspace)
         return DSA_ERR_INVALID_ARG;
@@ -558,14 +565,15 @@ extern "C" dsa_status dsa_indexer_logits(const void* q_bf16, const float* weight
             return DSA_ERR_CUDA;
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const int rotate = (flags & DSA_Q_ROTATE) != 0u ? 1 : 0;
+    // query prologue mode: bit 0 rotate, bit 1 power-of-two scales
+    const int mode = ((flags & DSA_Q_ROTATE) != 0u ? 1 : 0) | ((flags & DSA_SCALE_UE8M0) != 0u ? 2 : 0);
     const int rows = row_end - row_begin;
     uint8_t* q_codes = static_cast<uint8_t*>(workspace);
     float* q_gates = reinterpret_cast<float*>(q_codes + static_cast<size_t>(rows) * kQRowBytes);
 
     // query prologue: 8 vectors per 256-thread block
     indexer_q_prologue_kernel<<<static_cast<unsigned>(rows) * (kIndexHeads / 8), 256, 0, st>>>(
-        static_cast<const uint16_t*>(q_bf16), weights, cu_q, B, row_begin, row_end, rotate, q_codes, q_gates);
+        static_cast<const uint16_t*>(q_bf16), weights, cu_q, B, row_begin, row_end, mode, q_codes, q_gates);
     if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
 
     cudaLaunchAttribute attr[1];

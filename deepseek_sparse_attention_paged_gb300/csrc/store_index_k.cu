@@ -24,10 +24,16 @@ constexpr float kInvSqrt128 = 0x1.6a09e6p-4f;
 
 // Quantise and store one key held by a warp (lane l: elements 4l .. 4l+3, exact fp32 values of
 // bf16 numbers) at row `row` of page `pg`.
-__device__ __forceinline__ void quant_store(const float (&y)[4], int lane, uint8_t* __restrict__ pg, int row) {
+// ue8m0: the scale is the smallest power of two not below the fp32 scale.
+__device__ __forceinline__ void quant_store(const float (&y)[4], int lane, uint8_t* __restrict__ pg, int row,
+                                            bool ue8m0) {
     float amax = fmaxf(fmaxf(fabsf(y[0]), fabsf(y[1])), fmaxf(fabsf(y[2]), fabsf(y[3])));
     amax = warp_max(amax);
-    const float scale = __fdiv_rn(fmaxf(amax, 1e-4f), 448.0f);
+    float scale = __fdiv_rn(fmaxf(amax, 1e-4f), 448.0f);
+    if (ue8m0) {
+        const uint32_t u = __float_as_uint(scale);
+        if (u & 0x007fffffu) scale = __uint_as_float((u & 0x7f800000u) + 0x00800000u);
+    }
 
     uint32_t packed = 0;
 #pragma unroll
@@ -40,7 +46,8 @@ __device__ __forceinline__ void quant_store(const float (&y)[4], int lane, uint8
 }
 
 // Rotate, quantise and store one key held by a warp (layout as above).
-__device__ __forceinline__ void rotate_quant_store(float (&x)[4], int lane, uint8_t* __restrict__ pg, int row) {
+__device__ __forceinline__ void rotate_quant_store(float (&x)[4], int lane, uint8_t* __restrict__ pg, int row,
+                                                   bool ue8m0 = false) {
     // h = 1: pairs (0,1), (2,3) of this lane's elements
     {
         float a = x[0], b = x[1];
@@ -71,7 +78,7 @@ __device__ __forceinline__ void rotate_quant_store(float (&x)[4], int lane, uint
     float y[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) y[e] = __bfloat162float(__float2bfloat16_rn(__fmul_rn(x[e], kInvSqrt128)));
-    quant_store(y, lane, pg, row);
+    quant_store(y, lane, pg, row, ue8m0);
 }
 
 __global__ void __launch_bounds__(256)
@@ -225,8 +232,9 @@ store_index_k_prologue_kernel(const uint16_t* __restrict__ keys, const float* __
     float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
     warp_norm128(x, wv, bv, eps, rms);
     warp_rope64(x, lane, rc, neox);
-    if (flags & DSA_K_NO_ROTATE) quant_store(x, lane, pool + page * kIndexPageBytes, row);
-    else rotate_quant_store(x, lane, pool + page * kIndexPageBytes, row);
+    const bool ue8m0 = (flags & DSA_SCALE_UE8M0) != 0;
+    if (flags & DSA_K_NO_ROTATE) quant_store(x, lane, pool + page * kIndexPageBytes, row, ue8m0);
+    else rotate_quant_store(x, lane, pool + page * kIndexPageBytes, row, ue8m0);
 }
 
 // One warp per (row, group of HPW heads) of the indexer query: the row's cos/sin values are loaded
@@ -300,7 +308,7 @@ extern "C" dsa_status dsa_store_index_k_prologue(const void* k_raw_bf16, const f
                                                  int32_t* dev_err, void* stream) {
     if (n < 0 || num_pages < 0 || max_position < 0) return DSA_ERR_INVALID_ARG;
     if (page_size != dsa::kPage) return DSA_ERR_UNSUPPORTED;
-    if (flags & ~static_cast<uint32_t>(DSA_NORM_RMS | DSA_ROPE_INTERLEAVED | DSA_K_NO_ROTATE))
+    if (flags & ~static_cast<uint32_t>(DSA_NORM_RMS | DSA_ROPE_INTERLEAVED | DSA_K_NO_ROTATE | DSA_SCALE_UE8M0))
         return DSA_ERR_INVALID_ARG;
     if (n == 0) return DSA_OK;
     const bool rms = (flags & DSA_NORM_RMS) != 0;

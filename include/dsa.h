@@ -79,6 +79,11 @@ typedef enum {
 #define DSA_ROPE_INTERLEAVED 0x4u  /* rotary pairs (2i, 2i+1) (default: neox pairs (i, i+32)) */
 #define DSA_K_NO_ROTATE 0x8u       /* key prologue: quantise without the Hadamard rotation */
 
+/* Flag of dsa_store_index_k_prologue and dsa_indexer_logits: the "ue8m0" scale format -- every
+ * quantisation scale is the smallest power of two not below the fp32 scale max(amax, 1e-4) / 448
+ * (sglang dsa_indexer.py, Indexer(scale_fmt) handed to act_quant). */
+#define DSA_SCALE_UE8M0 0x10u
+
 /* Fixed shape constants of the path. */
 #define DSA_PAGE_SIZE 64
 #define DSA_INDEX_HEADS 64
@@ -150,7 +155,8 @@ dsa_status dsa_store_index_k(const void* k_bf16, const int64_t* slot_mapping, in
  *   cos_sin_cache  fp32 [max_position, 64] (16-byte aligned): cos in [0, 32), sin in [32, 64).
  *   positions      int64 [n].  slot_mapping int64 [n] (slot < 0: padding, skipped).
  *   index_k_pool, num_pages, page_size  as for dsa_store_index_k.
- *   flags          0 or a combination of DSA_NORM_RMS, DSA_ROPE_INTERLEAVED and DSA_K_NO_ROTATE.
+ *   flags          0 or a combination of DSA_NORM_RMS, DSA_ROPE_INTERLEAVED, DSA_K_NO_ROTATE and
+ *                  DSA_SCALE_UE8M0 (power-of-two key scales).
  *   dev_err        nullable; DSA_DEVERR_POSITION for a position outside [0, max_position),
  *                  DSA_DEVERR_SLOT_RANGE for a slot past the pool (the token is skipped either way).
  */
@@ -204,7 +210,7 @@ dsa_status dsa_indexer_rope_q(const void* q_raw_bf16, const float* cos_sin_cache
  *                prefill chunk; pass 0, T for all rows).
  *   logits       fp32 [row_end - row_begin, ld]; row r goes to logits[(r - row_begin) * ld].
  *                Entries s >= v_r are left untouched.  ld >= max_seq_len.
- *   flags        0 or DSA_Q_ROTATE.
+ *   flags        0 or a combination of DSA_Q_ROTATE and DSA_SCALE_UE8M0 (power-of-two query scales).
  *   workspace    device scratch of at least dsa_indexer_logits_workspace_size(row_end - row_begin)
  *                bytes, 16-byte aligned, owned by the caller.  It holds the quantised query rows
  *                (the prologue runs once per row instead of once per key tile); its contents need

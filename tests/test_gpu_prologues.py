@@ -34,11 +34,11 @@ def _keys(rng, n):
     return _bf16_bits(x)
 
 
-@pytest.mark.parametrize("rms", [False, True])
-@pytest.mark.parametrize("interleaved", [False, True])
-@pytest.mark.parametrize("rotate", [True, False])
-def test_store_prologue_bit_exact(rms, interleaved, rotate):
-    rng = np.random.default_rng(300 + 4 * rotate + 2 * rms + interleaved)
+@pytest.mark.parametrize("rms,interleaved,rotate,ue8m0", [(r, i, o, False) for r in (False, True)
+                                                          for i in (False, True) for o in (True, False)] +
+                         [(False, False, True, True), (True, True, False, True)])
+def test_store_prologue_bit_exact(rms, interleaved, rotate, ue8m0):
+    rng = np.random.default_rng(300 + 8 * ue8m0 + 4 * rotate + 2 * rms + interleaved)
     n, pages, max_pos = 1500, 30, 4096
     keys = _keys(rng, n)
     w = rng.standard_normal(128).astype(np.float32)
@@ -52,11 +52,11 @@ def test_store_prologue_bit_exact(rms, interleaved, rotate):
     pos[12] = -3
     slots[13] = pages * 64 + 7                # slot past the pool
     flags = ((capi.DSA_NORM_RMS if rms else 0) | (capi.DSA_ROPE_INTERLEAVED if interleaved else 0) |
-             (0 if rotate else capi.DSA_K_NO_ROTATE))
+             (0 if rotate else capi.DSA_K_NO_ROTATE) | (capi.DSA_SCALE_UE8M0 if ue8m0 else 0))
 
     ref = np.full((pages, oracle.PAGE_BYTES), 0x33, np.uint8)
     bad = oracle.store_index_k_prologue(keys, w, None if rms else b, eps, cs, pos, slots, ref, rms=rms,
-                                        neox=not interleaved, rotate=rotate)
+                                        neox=not interleaved, rotate=rotate, ue8m0=ue8m0)
     assert bad == 3
     pool = torch.full((pages, oracle.PAGE_BYTES), 0x33, dtype=torch.uint8, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")

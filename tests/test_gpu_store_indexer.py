@@ -67,7 +67,8 @@ def _logits_case(wl, flags=0, row_begin=0, row_end=None):
     pool = oracle_pool(wl)
     rows = np.arange(row_begin, row_end)
     ref, mag, bad = oracle.indexer_logits(wl.index_q(), wl.weights(), pool, wl.block_table, wl.seq_lens, wl.cu_q,
-                                          rows, db.ld, rotate_q=bool(flags & capi.DSA_Q_ROTATE), want_mag=True)
+                                          rows, db.ld, rotate_q=bool(flags & capi.DSA_Q_ROTATE), want_mag=True,
+                                          ue8m0_q=bool(flags & capi.DSA_SCALE_UE8M0))
     assert bad == 0
     vis = wl.visible_lens()[row_begin:row_end]
     check_logits(got, ref, mag, vis)
@@ -115,6 +116,11 @@ def test_logits_many_requests_shares_split_inside_requests():
 
 def test_logits_rotate_q_flag():
     _logits_case(workloads.make("tiny"), flags=capi.DSA_Q_ROTATE)
+
+
+def test_logits_ue8m0_query_scales():
+    _logits_case(workloads.make_custom("ue8m0", 108, [300, 1000, 70], 2, topk=64, heads=16),
+                 flags=capi.DSA_SCALE_UE8M0 | capi.DSA_Q_ROTATE)
 
 
 def test_logits_bad_page_sets_error_word_and_does_not_fault():
