@@ -389,7 +389,13 @@ def run_gpu(args):
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         rate, cores, times, rows = cpu_oracle_rate(wl, 8, 1, min_seconds=10.0)
+        # the same oracle on one host thread (a few rows)
+        import oracle
+        oracle.set_num_threads(1)
+        rate1, _, times1, rows1 = cpu_oracle_rate(wl, 2, 1)
+        oracle.set_num_threads(cores)
         cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "single_thread": {"value": rate1, "rows": len(rows1), "seconds": sum(times1)},
                "sample": f"{len(rows)} query rows of the same batch (rows evenly spaced, cycling), one per step, "
                          f"each with its full context (store its key, logits over its visible keys, "
                          f"top-{wl.topk}, {wl.heads}-head sparse MLA); {sum(times):.1f} s of timed CPU work; "
