@@ -34,7 +34,7 @@ def _check(got_bits, ref_bits, mag):
     assert np.all(err <= bound), f"max err {err.max()} (worst ratio {np.max(err / np.maximum(bound, 1e-30))})"
 
 
-@pytest.mark.parametrize("T,H", [(64, 128), (1, 8), (100, 16), (300, 4)])
+@pytest.mark.parametrize("T,H", [(64, 128), (1, 8), (100, 16), (300, 4), (1100, 8), (4096, 8)])
 def test_absorb_matches_oracle_into_strided_query(T, H):
     g = torch.Generator().manual_seed(700 + T + H)
     q = torch.randn(T, H, 192, generator=g).to(torch.bfloat16).cuda()             # [q_nope 128 | q_pe 64]
