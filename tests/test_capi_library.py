@@ -38,7 +38,7 @@ def test_status_strings_and_host_side_validation(lib):
     assert L.dsa_topk(None, 0, None, None, 1, 0, 0, 1, 4096, None, None, 0, None) == 2
     assert L.dsa_sparse_mla_decode(None, None, 0, None, 0, None, None, 1, None, 64, 1, 24, 0.1, None, None,
                                    None, 0, None, None) == 2                          # H = 24
-    assert L.dsa_indexer_logits(None, None, None, 0, None, 0, None, None, 1, 10, 1, 0, 1, None, 10, 0x10,
+    assert L.dsa_indexer_logits(None, None, None, 0, None, 0, None, None, 1, 10, 1, 0, 1, None, 10, 0x40,
                                 None, 0, None, None) == 1                             # unknown flag
     assert L.dsa_indexer_logits(None, None, None, 0, None, 0, None, None, 1, 10, 1, 0, 1, None, 10, 0,
                                 None, 0, None, None) == 1                             # null pointers
@@ -46,3 +46,45 @@ def test_status_strings_and_host_side_validation(lib):
     assert L.dsa_indexer_logits_workspace_size(0) == 0
     assert L.dsa_sparse_mla_workspace_size(64, 128, 2048) == 0     # one split per row: no scratch
     assert L.dsa_sparse_mla_workspace_size(16, 128, 2048) > 0      # few rows: split over k
+
+
+def test_host_side_validation_of_the_next_row_calls(lib):
+    """Argument checks of the prologue, projection, forced top-k and one-call indexer entry points
+    (all return before any CUDA call)."""
+    capi.load()
+    L = capi._lib
+    f = ctypes.c_float
+    # key prologue: page size, unknown flag, nothing to do, null pointers
+    assert L.dsa_store_index_k_prologue(None, None, None, f(1e-6), None, 8, None, None, 4, None, 1, 32, 0,
+                                        None, None) == 2
+    assert L.dsa_store_index_k_prologue(None, None, None, f(1e-6), None, 8, None, None, 4, None, 1, 64, 0x40,
+                                        None, None) == 1
+    assert L.dsa_store_index_k_prologue(None, None, None, f(1e-6), None, 8, None, None, 0, None, 1, 64, 0,
+                                        None, None) == 0
+    assert L.dsa_store_index_k_prologue(None, None, None, f(1e-6), None, 8, None, None, 4, None, 1, 64,
+                                        capi.DSA_NORM_RMS | capi.DSA_SCALE_UE8M0, None, None) == 1
+    # query rope
+    assert L.dsa_indexer_rope_q(None, None, 8, None, 2, 0x1, None, None, None) == 1   # flag of another call
+    assert L.dsa_indexer_rope_q(None, None, 8, None, 0, 0, None, None, None) == 0
+    assert L.dsa_indexer_rope_q(None, None, 8, None, -1, 0, None, None, None) == 1
+    # projections: empty, null, misaligned base, stride not a multiple of 8 elements, overlapping outputs
+    assert L.dsa_mla_absorb_q(None, 0, 0, None, 0, 128, None, 0, 0, None, None) == 0
+    assert L.dsa_mla_absorb_q(None, 24576, 192, None, 4, 128, None, 73728, 576, None, None) == 1
+    assert L.dsa_mla_absorb_q(ctypes.c_void_p(0x1008), 24576, 192, ctypes.c_void_p(0x2000), 4, 128,
+                              ctypes.c_void_p(0x3000), 73728, 576, None, None) == 1
+    assert L.dsa_mla_absorb_q(ctypes.c_void_p(0x1000), 24576, 196, ctypes.c_void_p(0x2000), 4, 128,
+                              ctypes.c_void_p(0x3000), 73728, 576, None, None) == 1
+    assert L.dsa_mla_v_up(ctypes.c_void_p(0x1000), 65536, 512, ctypes.c_void_p(0x2000), 4, 128,
+                          ctypes.c_void_p(0x3000), 16384, 64, None, None) == 1            # head stride < 128
+    # forced top-k
+    assert L.dsa_topk_forced(None, 0, None, None, 1, 0, 0, 1, 16, -1, 0, None, None, 0, None) == 1
+    assert L.dsa_topk_forced(None, 0, None, None, 1, 0, 0, 1, 0, 0, 0, None, None, 0, None) == 2
+    # one-call indexer: k, empty batch, missing or short workspace
+    assert L.dsa_lightning_indexer(None, None, None, 0, None, 0, None, None, 1, 100, 1, 2, 0, 0, 0, 0, None,
+                                   None, 0, None, None) == 1
+    assert L.dsa_lightning_indexer(None, None, None, 0, None, 0, None, None, 1, 100, 1, 0, 16, 0, 0, 0, None,
+                                   None, 0, None, None) == 0
+    need = L.dsa_lightning_indexer_workspace_size(2, 100)
+    assert need == (2 * (64 * 128 + 64 * 4) + 255) // 256 * 256 + 2 * 100 * 4
+    assert L.dsa_lightning_indexer(None, None, None, 0, None, 0, None, None, 1, 100, 1, 2, 16, 0, 0, 0,
+                                   ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000), need - 16, None, None) == 1
