@@ -1,9 +1,11 @@
 """Shared helpers of the GPU parity tests: oracle-side references and the tolerance rules.
 
-Tolerances (derived in DESIGN.md, section "Parity bars"):
+Tolerances:
   * FP8 codes, scales and top-k indices: bit-exact.
   * logits: |I_gpu - I_ref| <= 1e-3 * |I_ref| + 1e-5 * M_ref, where M_ref = sum_h |w'| ReLU(...)
-    is the magnitude of the summed terms (the sum cancels; its rounding error scales with M).
+    is the magnitude of the summed terms (the sum cancels, so its rounding error scales with M, not
+    with |I|: the fp32 accumulation of 128 exact FP8 products and the 64-term head sum each stay
+    below ~2^-20 M, well inside 1e-5 M; 1e-3 |I| is the stated relative bar).
   * attention output: max |o_gpu - o_ref| <= 2e-2 on unit-variance data; lse within 1e-3.
 """
 import numpy as np
