@@ -560,12 +560,12 @@ def run_profile(args):
     build()
     capi.load()
     wl = workloads.make(args.workload)
-    if args.profile in ("absorb", "v_up"):
-        # the decode shape of run_projections: 64 rows, 128 heads
+    if args.profile in ("absorb", "v_up", "absorb4k"):
+        # the shapes of run_projections: 64 rows (4096 for absorb4k), 128 heads
         import math
         g = torch.Generator().manual_seed(91)
-        T, H = 64, 128
-        if args.profile == "absorb":
+        T, H = (4096 if args.profile == "absorb4k" else 64), 128
+        if args.profile in ("absorb", "absorb4k"):
             w = (torch.randn(H, 128, 512, generator=g) / math.sqrt(128)).to(torch.bfloat16).cuda()
             q = torch.randn(T, H, 192, generator=g).to(torch.bfloat16).cuda()
             mla_q = torch.empty(T, H, 576, dtype=torch.bfloat16, device="cuda")
@@ -626,7 +626,7 @@ def run_profile(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--profile", choices=["store", "indexer", "topk", "mla", "step", "prologue", "rope_q", "absorb",
-                                          "v_up"],
+                                          "v_up", "absorb4k"],
                     default=None,
                     help="launch one stage warmup+steps times without timing (for ncu) and exit")
     ap.add_argument("--gpus", type=int, default=1)
