@@ -92,13 +92,29 @@ class ClockSampler:
             sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
         except Exception:
             sel = []
-        self.cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"] + sel
+        self.sel = sel
+        self.cmd = self._cmd(25)
+
+    def _cmd(self, ms: int):
+        return ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", str(ms)] + self.sel
+
+    def _start(self):
+        self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
 
     def __enter__(self):
+        # sample every 25 ms (the timed region lasts tens of milliseconds); fall back to 100 ms if
+        # this nvidia-smi gives nothing at that rate
         try:
-            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
-            self.thread.start()
+            self._start()
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 2.0 and self.proc.poll() is None:
+                time.sleep(0.02)
+            if not self.lines:
+                self.__exit__(None, None, None)
+                self.cmd = self._cmd(100)
+                self._start()
         except Exception:
             self.proc = None
         return self
@@ -113,7 +129,7 @@ class ClockSampler:
             self.lines.append(line.strip())
 
     def __exit__(self, *exc):
-        if self.proc is not None:
+        if self.proc is not None and self.proc.poll() is None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
