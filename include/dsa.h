@@ -11,6 +11,9 @@
  * quantisation, paged scatter by slot); two prologue calls add the key norm and rotary embedding
  * in front of that store and the rotary embedding of the indexer query; two more compute the
  * per-head projections around the absorbed attention (absorbed query, value up-projection).
+ * Variants: the top-k with forced initial / local tokens, power-of-two (ue8m0) quantisation
+ * scales, a one-call indexer that returns top-k indices, and a sparse MLA call that needs no
+ * workspace.
  *
  * Conventions shared by every call
  * --------------------------------
@@ -18,7 +21,8 @@
  *   by value.  bf16 arrays are passed as `const void*` holding IEEE bfloat16 bit patterns.
  * Ownership.  The caller owns every buffer.  The library never allocates or frees device memory
  *   and keeps no state between calls; scratch space is passed in as `workspace` with its size
- *   queried from the matching *_workspace_size() call.
+ *   queried from the matching *_workspace_size() call.  The one exception is
+ *   dsa_sparse_mla_decode_noalloc, whose scratch is a fixed array inside the library.
  * Streams.  `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls enqueue work on
  *   it and return without synchronising; results are ready when the stream reaches them.
  * Requests and rows.  B requests; request b has seq_lens[b] cached tokens (this step's tokens
