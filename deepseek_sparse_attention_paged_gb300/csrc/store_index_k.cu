@@ -105,10 +105,11 @@ store_index_k_kernel(const uint16_t* __restrict__ keys, const int64_t* __restric
 
 __device__ __forceinline__ float round_bf16(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 
-// Sum of the 128 values a warp holds (lane l: v[0..3] = elements 4l .. 4l+3) in one fixed order:
-// ((v0 + v1) + (v2 + v3)) inside each lane, then a pairwise tree over lanes (distance 1, 2, 4, 8,
-// 16).  At each level a lane adds its partner's partial to its own; both lanes of a pair add the
-// same two numbers, so every lane ends with the same bits, those of the tree rooted at lane 0.
+// fp32 sum of the 128 values a warp holds (lane l: v[0..3] = elements 4l .. 4l+3): within each
+// lane, then a butterfly over lanes (distance 1, 2, 4, 8, 16).  At each level a lane adds its
+// partner's partial to its own; both lanes of a pair add the same two numbers, so every lane ends
+// with the same bits.  (The norm's definition sums exactly; this fp32 evaluation is within a few
+// fp32 units of it.)
 __device__ __forceinline__ float warp_sum128_tree(const float (&v)[4]) {
     float s = __fadd_rn(__fadd_rn(v[0], v[1]), __fadd_rn(v[2], v[3]));
 #pragma unroll

@@ -142,15 +142,17 @@ dsa_status dsa_store_index_k(const void* k_bf16, const int64_t* slot_mapping, in
  *   x = k_raw_bf16[t, 0:128];
  *   LayerNorm: mean = S(x) / 128, d = x - mean, var = S(d * d) / 128, rstd = 1 / sqrt(var + eps),
  *     n = bf16_rn((d * rstd) * w + b);  RMSNorm (DSA_NORM_RMS): rstd = 1 / sqrt(S(x * x) / 128 + eps),
- *     n = bf16_rn((x * rstd) * w).  S() sums in one fixed order: ((v0 + v1) + (v2 + v3)) per group
- *     of 4 consecutive dims, then a pairwise tree over the 32 group sums (distance 1, 2, 4, 8, 16).
+ *     n = bf16_rn((x * rstd) * w).  The definition is exact (the sums, square root and division
+ *     exact, one rounding to bf16); the kernel evaluates it in fp32, so where the exact n lies within
+ *     that fp32 error of a bf16 rounding boundary (about 2 outputs in 10^5) its n is one bf16 unit
+ *     away and that token's codes may move by one E4M3 step.
  *   Rotary: c, s = cos_sin_cache[positions[t], 0:32], [32:64]; neox pairs (a, b) = (n_i, n_{i+32})
  *     (DSA_ROPE_INTERLEAVED: (n_{2i}, n_{2i+1})), i < 32: a' = bf16_rn(a c_i - b s_i),
  *     b' = bf16_rn(b c_i + a s_i); dims 64 .. 127 unchanged.
  *   Then the steps of dsa_store_index_k on the result; with DSA_K_NO_ROTATE the rotation is
  *   skipped and the rotary output itself is quantised and stored.
- *   Every operation is one IEEE fp32 operation (no fused multiply-add), so results are bit-exact
- *   with the CPU definition.
+ *   The rotary embedding and everything after it are IEEE fp32 operations without fused
+ *   multiply-add, as the definition states them.
  * Arguments:
  *   k_raw_bf16     [n, 128] bf16 (16-byte aligned): the key projection before the norm.
  *   norm_weight    fp32 [128] (16-byte aligned).  norm_bias: fp32 [128] (16-byte aligned) for

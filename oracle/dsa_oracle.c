@@ -244,46 +244,33 @@ int64_t dsa_oracle_store_index_k(const uint16_t* k_bf16, const int64_t* slot_map
 
 /* ---------------------------------------------------------------- indexer key / query prologues */
 
-/* Sum of 128 fp32 values in a fixed pairwise order: blocks of 4 consecutive values as
- * (x0 + x1) + (x2 + x3), then adjacent block sums pairwise (1+1, 2+2, 4+4, ... blocks), the left
- * operand first.  Reading: the pages do not print the norm kernel; since the normalised key feeds
- * the bit-exact FP8 codes, the summation order (and fp32 arithmetic) is part of the definition. */
-static float sum128_pairwise(const float* x) {
-    float s[32];
-    for (int l = 0; l < 32; ++l) s[l] = (x[4 * l] + x[4 * l + 1]) + (x[4 * l + 2] + x[4 * l + 3]);
-    for (int m = 1; m < 32; m <<= 1)
-        for (int l = 0; l < 32; l += 2 * m) s[l] = s[l] + s[l + m];
-    return s[0];
-}
-
 /* Norm of one bf16 128-vector ([idx] Indexer.k_norm: LayerNorm(head_dim) with weight and bias,
  * eps = k_norm.variance_epsilon, or RMSNorm(head_dim) when the config's index_k_norm_type is
  * "rms"; [sfa] indexer_select_pre_process: k_li = k_norm(wk(x))).
  * LayerNorm: mean = sum(x) / 128; d = x - mean; var = sum(d * d) / 128; rstd = 1 / sqrt(var + eps);
  * y = (d * rstd) * w + b.  RMSNorm: ms = sum(x * x) / 128; rstd = 1 / sqrt(ms + eps);
- * y = (x * rstd) * w.  Reading: every step in fp32 (IEEE sqrt and division, no fused multiply-add,
- * the pairwise sums above; the division by 128 is exact); the result is rounded to bf16, the
- * dtype of the k_norm output the pages pass on. */
+ * y = (x * rstd) * w.  Reading: the pages do not print the norm kernel, so the definition is the
+ * exact one: every step in float64 (standing in for exact arithmetic; the sums run in index
+ * order), and the result rounded once to bf16, the dtype of the k_norm output the pages pass on. */
 void dsa_oracle_k_norm128(const uint16_t* in_bf16, const float* w, const float* b, float eps, int rms,
                           uint16_t* out_bf16) {
-    float x[DI], t[DI];
-    for (int d = 0; d < DI; ++d) x[d] = bf16_bits_to_f32(in_bf16[d]);
+    double x[DI];
+    for (int d = 0; d < DI; ++d) x[d] = (double)bf16_bits_to_f32(in_bf16[d]);
     if (rms) {
-        for (int d = 0; d < DI; ++d) t[d] = x[d] * x[d];
-        const float ms = sum128_pairwise(t) * (1.0f / DI);
-        const float rstd = 1.0f / sqrtf(ms + eps);
-        for (int d = 0; d < DI; ++d) out_bf16[d] = dsa_oracle_f32_to_bf16((x[d] * rstd) * w[d]);
+        double ss = 0.0;
+        for (int d = 0; d < DI; ++d) ss += x[d] * x[d];
+        const double rstd = 1.0 / sqrt(ss / DI + (double)eps);
+        for (int d = 0; d < DI; ++d) out_bf16[d] = dsa_oracle_f64_to_bf16((x[d] * rstd) * (double)w[d]);
         return;
     }
-    const float mean = sum128_pairwise(x) * (1.0f / DI);
-    float dv[DI];
-    for (int d = 0; d < DI; ++d) {
-        dv[d] = x[d] - mean;
-        t[d] = dv[d] * dv[d];
-    }
-    const float var = sum128_pairwise(t) * (1.0f / DI);
-    const float rstd = 1.0f / sqrtf(var + eps);
-    for (int d = 0; d < DI; ++d) out_bf16[d] = dsa_oracle_f32_to_bf16(((dv[d] * rstd) * w[d]) + b[d]);
+    double sum = 0.0;
+    for (int d = 0; d < DI; ++d) sum += x[d];
+    const double mean = sum / DI;
+    double sq = 0.0;
+    for (int d = 0; d < DI; ++d) sq += (x[d] - mean) * (x[d] - mean);
+    const double rstd = 1.0 / sqrt(sq / DI + (double)eps);
+    for (int d = 0; d < DI; ++d)
+        out_bf16[d] = dsa_oracle_f64_to_bf16(((x[d] - mean) * rstd) * (double)w[d] + (double)b[d]);
 }
 
 /* Rotary embedding of the first 64 dims of one bf16 128-vector ([idx] rotary_emb with rotary_dim

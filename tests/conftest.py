@@ -13,6 +13,21 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "slow: full-size workload (minutes of CPU oracle time)")
 
 
+def pytest_terminal_summary(terminalreporter):
+    """Prints the parity counters the tests recorded (rows, elements compared, elements that pass
+    only through a tolerance term, admissible near-boundary tokens, ...), one line per entry."""
+    try:
+        from helpers import PARITY_COUNTS
+    except Exception:
+        return
+    if not PARITY_COUNTS:
+        return
+    terminalreporter.write_line("parity counts:")
+    for key in sorted(PARITY_COUNTS):
+        items = ", ".join(f"{k}={v}" for k, v in sorted(PARITY_COUNTS[key].items()))
+        terminalreporter.write_line(f"  {key}: {items}")
+
+
 @pytest.fixture(scope="session")
 def oracle_lib():
     import oracle

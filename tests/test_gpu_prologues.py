@@ -1,12 +1,16 @@
-"""GPU parity of the indexer prologue calls against the CPU oracle, through the C ABI, bit for
-bit: dsa_store_index_k_prologue (key norm, rotary embedding, rotate, quantise, paged store) and
-dsa_indexer_rope_q (rotary embedding of the indexer query)."""
+"""GPU parity of the indexer prologue calls against the CPU oracle, through the C ABI:
+dsa_store_index_k_prologue (key norm, rotary embedding, rotate, quantise, paged store) token by
+token against the oracle's exact norm (codes and scale equal, or -- for the few tokens whose exact
+norm output lies within the fp32 evaluation's error of a bf16 rounding boundary -- admissible by the
+bar in helpers.prologue_token_admissible), and dsa_indexer_rope_q (rotary embedding of the indexer
+query, the same fp32 operations on both sides) bit for bit."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 from deepseek_sparse_attention_paged_gb300 import capi
+from helpers import compare_prologue_pools
 
 pytestmark = pytest.mark.gpu
 
@@ -37,7 +41,7 @@ def _keys(rng, n):
 @pytest.mark.parametrize("rms,interleaved,rotate,ue8m0", [(r, i, o, False) for r in (False, True)
                                                           for i in (False, True) for o in (True, False)] +
                          [(False, False, True, True), (True, True, False, True)])
-def test_store_prologue_bit_exact(rms, interleaved, rotate, ue8m0):
+def test_store_prologue_matches_oracle(rms, interleaved, rotate, ue8m0):
     rng = np.random.default_rng(300 + 8 * ue8m0 + 4 * rotate + 2 * rms + interleaved)
     n, pages, max_pos = 1500, 30, 4096
     keys = _keys(rng, n)
@@ -65,14 +69,16 @@ def test_store_prologue_bit_exact(rms, interleaved, rotate, ue8m0):
                                     torch.from_numpy(pos).cuda(), torch.from_numpy(slots).cuda(), pool,
                                     flags=flags, dev_err=err)
     got = pool.cpu().numpy()
-    assert np.array_equal(got, ref)
+    compare_prologue_pools(got, ref, keys, w, None if rms else b, eps, cs, pos, slots, rms, not interleaved, rotate,
+                           ue8m0)
     st, word = capi.dsa_read_device_error(err)
     assert st == capi.DSA_ERR_DEVICE_BOUNDS
     assert word == capi.DSA_DEVERR_POSITION | capi.DSA_DEVERR_SLOT_RANGE
 
 
 def test_store_prologue_equals_norm_rope_then_store():
-    """The fused call stores what the plain store writes for the oracle's normed, rotated keys."""
+    """The fused call stores what the plain store writes for the oracle's normed, rotated keys
+    (up to the norm's rounding-boundary tokens, under the same bar)."""
     rng = np.random.default_rng(310)
     n, pages, max_pos = 300, 8, 1000
     keys = _keys(rng, n)
@@ -88,7 +94,8 @@ def test_store_prologue_equals_norm_rope_then_store():
     capi.dsa_store_index_k_prologue(_bf16_dev(keys), torch.from_numpy(w).cuda(), torch.from_numpy(b).cuda(), 1e-5,
                                     torch.from_numpy(cs).cuda(), torch.from_numpy(pos).cuda(),
                                     torch.from_numpy(slots).cuda(), fused)
-    assert torch.equal(plain, fused)
+    compare_prologue_pools(fused.cpu().numpy(), plain.cpu().numpy(), keys, w, b, 1e-5, cs, pos, slots, False, True,
+                           True, False, key="key_prologue_vs_store")
 
 
 def test_store_prologue_empty_and_bad_flags():

@@ -18,16 +18,59 @@ def _f32(bits):
     return torch.from_numpy(np.asarray(bits, np.uint16).view(np.int16)).view(torch.bfloat16).float().numpy()
 
 
-def _ulp_close(got_f32, ref_f64, ulps=1.0):
-    """|got - ref| within `ulps` bf16 units of the reference magnitude (plus a tiny absolute floor)."""
-    tol = ulps * np.maximum(np.abs(ref_f64), 1e-30) * 2.0 ** -8 + 1e-30
-    return np.all(np.abs(got_f32 - ref_f64) <= tol)
+def _round_once_bf16(v: float) -> float:
+    """The bf16 value nearest to the float64 value v (ties to even), by exact rational arithmetic."""
+    from fractions import Fraction
+    if v == 0.0:
+        return 0.0
+    q = Fraction(v)
+    a = abs(q)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    ulp = Fraction(2) ** (e - 7)            # bf16 keeps 8 significant bits
+    n, rem = divmod(a, ulp)
+    if rem > ulp / 2 or (rem == ulp / 2 and n % 2 == 1):
+        n += 1
+    r = float(n * ulp)
+    return -r if q < 0 else r
+
+
+def _rounded_once(ref_f64: np.ndarray) -> np.ndarray:
+    """float64 -> nearest bf16 value (ties to even), vectorised: torch's RNE conversion of the
+    nearest fp32, except where that fp32 is itself a bf16 midpoint (the only case in which two
+    roundings can differ from one), which goes through exact rational arithmetic."""
+    f = ref_f64.astype(np.float32)
+    out = torch.from_numpy(f).to(torch.bfloat16).float().numpy().astype(np.float64)
+    mid = (f.view(np.uint32) & 0xFFFF) == 0x8000
+    for i in np.flatnonzero(mid):
+        out[i] = _round_once_bf16(float(ref_f64[i]))
+    return out
+
+
+def _assert_rounded_once(got_f32, ref_f64):
+    """Every output equals the float64 reference rounded once to bf16.  The reference is numpy's
+    float64 (its own summation order), so an element whose value lies within 1e-12 (relative) of a
+    bf16 rounding midpoint may legitimately round either way; none is expected in these draws."""
+    got = np.asarray(got_f32, np.float64).ravel()
+    ref = np.asarray(ref_f64, np.float64).ravel()
+    want = _rounded_once(ref)
+    off = np.flatnonzero(got != want)
+    for i in off:
+        lo, hi = _rounded_once(np.array([ref[i] * (1 - 1e-12), ref[i] * (1 + 1e-12)]))
+        assert got[i] in (lo, hi), (got[i], want[i], ref[i])
+    assert off.size <= 1
 
 
 @pytest.mark.parametrize("scale", [1e-3, 1.0, 50.0])
 def test_layernorm_matches_float64_definition(scale):
+    """1000 vectors per scale: an fp32 evaluation of the same formula (in any summation order)
+    lands on the other side of a bf16 rounding boundary for about 2 in 10^5 outputs, so it fails
+    this pin with near certainty; the float64 definition rounded once passes it exactly."""
     rng = np.random.default_rng(11)
-    for _ in range(20):
+    for _ in range(1000):
         x = _bf16_bits(rng.standard_normal(DI) * scale + rng.standard_normal() * scale)
         w = rng.standard_normal(DI).astype(np.float32)
         b = rng.standard_normal(DI).astype(np.float32)
@@ -35,9 +78,10 @@ def test_layernorm_matches_float64_definition(scale):
         got = _f32(oracle.k_norm128(x, w, b, eps))
         xf = _f32(x).astype(np.float64)
         mu = xf.mean()
-        ref = (xf - mu) / np.sqrt(((xf - mu) ** 2).mean() + eps) * w + b
-        # one bf16 rounding of a value computed in fp32 (a few fp32 ulps): within 1 bf16 ulp + slack
-        assert _ulp_close(got, ref, ulps=1.01)
+        ref = (xf - mu) / np.sqrt(((xf - mu) ** 2).mean() + np.float64(np.float32(eps))) * w.astype(np.float64) \
+            + b.astype(np.float64)
+        # the definition: the exact normalised value, rounded once to bf16
+        _assert_rounded_once(got, ref)
 
 
 def test_layernorm_unit_affine_gives_zero_mean_unit_variance():
@@ -56,13 +100,13 @@ def test_layernorm_of_a_constant_vector_is_the_bias():
 
 def test_rmsnorm_matches_float64_definition():
     rng = np.random.default_rng(13)
-    for _ in range(20):
+    for _ in range(3000):
         x = _bf16_bits(rng.standard_normal(DI) * 3.0)
         w = rng.standard_normal(DI).astype(np.float32)
         got = _f32(oracle.k_norm128(x, w, None, 1e-6, rms=True))
         xf = _f32(x).astype(np.float64)
-        ref = xf / np.sqrt((xf ** 2).mean() + 1e-6) * w
-        assert _ulp_close(got, ref, ulps=1.01)
+        ref = xf / np.sqrt((xf ** 2).mean() + np.float64(np.float32(1e-6))) * w.astype(np.float64)
+        _assert_rounded_once(got, ref)
 
 
 def _cos_sin(angles):
