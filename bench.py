@@ -167,13 +167,14 @@ def kernel_source_hash(files):
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(stage):
-    """DRAM bytes per launch from the committed ncu summary, only if the kernel source is unchanged."""
+def recorded_traffic(stage, workload=DEFAULT_WORKLOAD):
+    """DRAM bytes per launch from the committed ncu summary, only if the kernel source is unchanged
+    and the summary is of this workload."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p)).get(stage)
-    if not d:
+    if not d or d.get("workload", DEFAULT_WORKLOAD) != workload:
         return None
     if d.get("source_hash") != kernel_source_hash(d["sources"]):
         return None
@@ -182,6 +183,9 @@ def recorded_traffic(stage):
 
 STAGE_SOURCES = {"store": ["store_index_k.cu"], "indexer": ["indexer_logits.cu"], "topk": ["topk.cu"],
                  "mla": ["sparse_mla.cu"]}
+# tensor peak of each stage relative to the measured dense bf16 peak: the indexer contracts FP8
+# operands (nominal dense FP8 : BF16 = 4.5 : 2.25 PFLOP/s), the attention bf16
+STAGE_TENSOR_PEAK_RATIO = {"indexer": 2.0, "mla": 1.0}
 
 
 # ----------------------------------------------------------------------------- CPU oracle arm
@@ -349,8 +353,8 @@ def run_gpu(args):
     step_graph, step_kernels = capture(lambda: db.step(), stream)
     stage_graphs = {
         "store": capture(lambda: db.store_new_keys(), stream),
-        "indexer": capture(lambda: db.indexer_logits(), stream),
-        "topk": capture(lambda: db.topk(), stream),
+        "indexer": capture(lambda: db.indexer_stage(), stream),
+        "topk": capture(lambda: db.topk_stage(), stream),
         "mla": capture(lambda: db.sparse_mla(), stream),
     }
     st, word = db.device_error()
@@ -392,15 +396,27 @@ def run_gpu(args):
     for k, ms_list in stage_ms.items():
         ms = sum(ms_list) / len(ms_list)
         b, f = work[k]
+        tc = STAGE_TENSOR_PEAK_RATIO.get(k, 1.0) * bf16      # the stage's own operand type
+        t_hbm, t_tc = b / (hbm * 1e9), f / (tc * 1e12)
         stages[k] = {"ms": ms, "algorithmic_bytes": b, "flops": f, "gbs": b / (ms * 1e-3) / 1e9,
                      "hbm_frac": (b / (ms * 1e-3) / 1e9) / hbm,
-                     "roofline_ms": max(b / (hbm * 1e9), f / (bf16 * 1e12)) * 1e3}
+                     "tflops": f / (ms * 1e-3) / 1e12, "tensor_peak_tflops": tc,
+                     "tensor_frac": (f / (ms * 1e-3) / 1e12) / tc,
+                     "bound": "tensor" if t_tc > t_hbm else "hbm",
+                     "roofline_ms": max(t_hbm, t_tc) * 1e3, "roofline_frac": max(t_hbm, t_tc) * 1e3 / ms}
     dominant = max(("indexer", "mla"), key=lambda k: stages[k]["ms"])
     d = stages[dominant]
-    roofline = {"bound": "hbm", "achieved": d["gbs"], "peak": hbm, "unit": "GB/s", "frac": d["gbs"] / hbm,
-                "traffic": recorded_traffic(dominant), "kernel": dominant,
-                "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured" else
-                "fallback 6.8 TB/s"}
+    src = "measured" if peak_kind == "measured" else "fallback"
+    if d["bound"] == "hbm":
+        roofline = {"bound": "hbm", "achieved": d["gbs"], "peak": hbm, "unit": "GB/s", "frac": d["gbs"] / hbm,
+                    "traffic": recorded_traffic(dominant, wl.name), "kernel": dominant,
+                    "peak_source": f"{src} hbm_gbs (MEASURED_PEAKS.json)" if src == "measured" else "fallback 6.8 TB/s"}
+    else:
+        roofline = {"bound": "tensor", "achieved": d["tflops"], "peak": d["tensor_peak_tflops"], "unit": "TFLOP/s",
+                    "frac": d["tensor_frac"], "traffic": recorded_traffic(dominant, wl.name), "kernel": dominant,
+                    "peak_source": (f"{src} bf16_tflops (MEASURED_PEAKS.json, burst)"
+                                    + (" x 2, the nominal FP8 : BF16 dense ratio" if
+                                       STAGE_TENSOR_PEAK_RATIO.get(dominant, 1.0) == 2.0 else ""))}
     # CPU oracle baseline on a bounded sample (rank 0, N = 1 only)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -625,9 +641,8 @@ def run_profile(args):
     need_latent = args.profile in ("mla", "step")
     db = DeviceBatch(wl, with_latent=need_latent)
     if args.profile in ("topk", "mla"):
-        db.indexer_logits()
-        db.topk()
-    fn = {"store": db.store_new_keys, "indexer": db.indexer_logits, "topk": db.topk,
+        db.select()
+    fn = {"store": db.store_new_keys, "indexer": db.indexer_stage, "topk": db.topk_stage,
           "mla": db.sparse_mla, "step": db.step}[args.profile]
     for _ in range(args.warmup + args.steps):
         fn()

@@ -7,7 +7,9 @@ plain C header ``include/dsa.h``.
 from __future__ import annotations
 
 import glob
+import hashlib
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -34,17 +36,40 @@ def sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+STAMP = LIB + ".hash"
+
+
+def _inputs_hash() -> str:
+    """sha256 over every source and header the library is built from, the nvcc flags and nvcc's
+    version line: the library is rebuilt whenever any of them differs from the last build's."""
+    h = hashlib.sha256()
+    deps = sorted(sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h")))
+    for p in deps:
+        h.update(os.path.relpath(p, ROOT).encode())
+        with open(p, "rb") as f:
+            h.update(f.read())
+    h.update(" ".join(ARCH + NVCC_FLAGS).replace(ROOT, "<root>").encode())
+    try:
+        v = subprocess.run([nvcc(), "--version"], stdout=subprocess.PIPE, stderr=subprocess.STDOUT).stdout
+        h.update(v.strip().splitlines()[-1] if v.strip() else b"")
+    except Exception:
+        pass
+    h.update(platform.machine().encode())
+    return h.hexdigest()
+
+
+def _stale(digest: str) -> bool:
+    if not os.path.exists(LIB) or not os.path.exists(STAMP):
         return True
-    t = os.path.getmtime(LIB)
-    deps = sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
-    return any(os.path.getmtime(p) > t for p in deps)
+    with open(STAMP) as f:
+        return f.read().strip() != digest
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile and link the library if any source changed; returns the library path."""
-    if not force and not _stale():
+    """Compile and link the library unless the last build was made from the same sources, flags,
+    compiler and machine type (a hash stored beside the library); returns the library path."""
+    digest = _inputs_hash()
+    if not force and not _stale(digest):
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     exe = nvcc()
@@ -74,6 +99,9 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stdout.decode(errors="replace"))
     os.replace(tmp, LIB)
+    with open(STAMP + f".tmp{os.getpid()}", "w") as f:
+        f.write(digest + "\n")
+    os.replace(STAMP + f".tmp{os.getpid()}", STAMP)
     return LIB
 
 

@@ -55,6 +55,18 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Multiprocessor count of the current device (the launch heuristics size grids by it); `fallback`
+// when no device can be queried (a size query made without a GPU).
+inline int device_sm_count(int fallback = 152) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+        cudaGetLastError();   // leave no sticky error behind
+        return fallback;
+    }
+    return sms;
+}
+
 inline dsa_status launch_status() {
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;

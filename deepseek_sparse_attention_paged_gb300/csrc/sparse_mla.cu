@@ -608,11 +608,11 @@ sparse_mla_combine_kernel(const float* __restrict__ part_o, const float* __restr
 }
 
 // Splits of the k entries per row: the largest power of two (<= 8) for which the (row, split,
-// half) grid still fits one wave of one CTA per SM (152 SMs) and every split keeps >= 256 entries.
-constexpr int kSmCount = 152;
+// half) grid still fits one wave of one CTA per SM and every split keeps >= 256 entries.
 int mla_splits(int T, int k) {
+    const int sms = device_sm_count();
     int s = 1;
-    while (2 * T * (2 * s) <= kSmCount && k / (2 * s) >= 256 && s < 8) s *= 2;
+    while (2 * T * (2 * s) <= sms && k / (2 * s) >= 256 && s < 8) s *= 2;
     return s;
 }
 

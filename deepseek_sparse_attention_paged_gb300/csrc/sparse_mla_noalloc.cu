@@ -3,10 +3,9 @@
 // Some callers of this library cannot call cudaMalloc (or any allocator) when they run the
 // attention: an inference-engine plugin whose per-step "enqueue" hook is forbidden to allocate
 // because the host engine owns every byte of device memory and budgets it up front; a serving
-// loop that has given all free memory to its own caching allocator; code that runs while a CUDA
-// graph is being captured, where an allocation would either fail or silently become part of the
-// graph.  They still own the inputs and outputs, but have nowhere to get the split-K scratch that
-// dsa_sparse_mla_decode() takes as `workspace`.
+// loop that has given all free memory to its own caching allocator.  They still own the inputs and
+// outputs, but have nowhere to get the split-K scratch that dsa_sparse_mla_decode() takes as
+// `workspace`.
 //
 // dsa_sparse_mla_decode_noalloc() serves them: it runs exactly the same kernels as
 // dsa_sparse_mla_decode(), with the scratch taken from the fixed array below, which the CUDA
@@ -26,8 +25,10 @@ static __device__ __align__(256) unsigned char g_mla_scratch[kNoAllocScratchByte
 
 // Device address of g_mla_scratch, per device ordinal.  In host code the name g_mla_scratch is a
 // host-side stand-in, not a device address, so it is never passed to a kernel; the address comes
-// from cudaGetSymbolAddress, taken once per device with that device current.  Concurrent first
-// calls on one device may both look it up; they store the same value.
+// from cudaGetSymbolAddress, taken once per device with that device current.  Under lazy module
+// loading that first lookup also loads this library's device code on the device, which is when
+// the array is placed in device memory (and can fail for lack of it).  Concurrent first calls on
+// one device may both look it up; they store the same value.
 std::atomic<void*> g_scratch_addr[kMaxDevices];
 
 dsa_status scratch_address(void** out) {

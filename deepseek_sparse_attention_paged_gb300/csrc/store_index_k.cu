@@ -338,7 +338,7 @@ extern "C" dsa_status dsa_indexer_rope_q(const void* q_raw_bf16, const float* co
     if (!dsa::aligned16(q_raw_bf16) || !dsa::aligned16(q_out_bf16) || !dsa::aligned16(cos_sin_cache))
         return DSA_ERR_INVALID_ARG;
     // 16 heads per warp once that still gives about 32 warps per SM, else one
-    const bool wide = T * (dsa::kIndexHeads / 16) >= 152 * 32;
+    const bool wide = T * (dsa::kIndexHeads / 16) >= static_cast<int64_t>(dsa::device_sm_count()) * 32;
     const int64_t warps = T * (wide ? dsa::kIndexHeads / 16 : dsa::kIndexHeads);
     const int64_t blocks = (warps + 7) / 8;
     if (blocks > 0x7fffffffLL) return DSA_ERR_INVALID_ARG;

@@ -32,9 +32,28 @@ def logits_ld(max_seq_len: int) -> int:
     return max(4, (max_seq_len + 3) // 4 * 4)
 
 
+# Logits row tiling (sglang dsa_indexer.py, Indexer._should_chunk_mqa_logits: rows x keys below 8M
+# elements are never chunked; above that the fp32 logits are produced in row chunks under a byte
+# budget).  The budget here is 64 MiB: half of the 129 MB L2, so the top-k call of a tile reads the
+# logits the indexer call of the same tile has just written from L2 rather than from HBM.
+LOGITS_STATIC_SKIP_ELEMS = 8_000_000
+LOGITS_TILE_BUDGET_BYTES = 64 << 20
+
+
+def logits_tile_rows(T: int, ld: int, budget_bytes: int = LOGITS_TILE_BUDGET_BYTES) -> int:
+    """Query rows per logits tile: all T rows when T * ld is below the static skip size or the
+    whole buffer fits the budget, else as many rows as fit the budget (at least one)."""
+    if T <= 0:
+        return 1
+    if T * ld < LOGITS_STATIC_SKIP_ELEMS or T * ld * 4 <= budget_bytes:
+        return T
+    return max(1, min(T, budget_bytes // (ld * 4)))
+
+
 class DeviceBatch:
     def __init__(self, wl: Workload, device: str = "cuda", with_latent: bool = True,
-                 build_index_cache: bool = True, key_chunk: int = 1 << 20):
+                 build_index_cache: bool = True, key_chunk: int = 1 << 20,
+                 logits_budget_bytes: int = LOGITS_TILE_BUDGET_BYTES):
         self.wl = wl
         self.device = torch.device(device)
         dev = self.device
@@ -57,11 +76,13 @@ class DeviceBatch:
                 capi.dsa_store_index_k(k, s, self.index_pool, self.dev_err)
             torch.cuda.synchronize(dev)
         self.ld = logits_ld(wl.max_seq_len)
-        self.logits = torch.empty((wl.T, self.ld), dtype=torch.float32, device=dev)
+        # the logits buffer holds one row tile; the step walks the tiles (indexer, then top-k)
+        self.tile_rows = logits_tile_rows(wl.T, self.ld, logits_budget_bytes)
+        self.logits = torch.empty((self.tile_rows, self.ld), dtype=torch.float32, device=dev)
         self.idx = torch.empty((wl.T, wl.topk), dtype=torch.int32, device=dev)
-        self.idx_ws = torch.empty(max(16, capi.dsa_indexer_logits_workspace_size(wl.T)), dtype=torch.uint8,
+        self.idx_ws = torch.empty(max(16, capi.dsa_indexer_logits_workspace_size(self.tile_rows)), dtype=torch.uint8,
                                   device=dev)
-        self.topk_ws = torch.empty(max(1, capi.dsa_topk_workspace_size(wl.T, wl.topk, wl.max_seq_len)),
+        self.topk_ws = torch.empty(max(1, capi.dsa_topk_workspace_size(self.tile_rows, wl.topk, wl.max_seq_len)),
                                    dtype=torch.uint8, device=dev)
         self.kv_pool = None
         self.mla_q = None
@@ -197,11 +218,36 @@ class DeviceBatch:
                                    self.idx if idx is None else idx, self.wl.scale, self.out, self.mla_ws,
                                    lse=self.lse, dev_err=self.dev_err, stream=stream)
 
-    def step(self, stream=None):
-        """One decode step: store the new keys, score, select, attend."""
+    def tiles(self):
+        """(row_begin, row_end) of every logits row tile, in order."""
+        T, n = self.wl.T, self.tile_rows
+        return [(rb, min(T, rb + n)) for rb in range(0, T, n)]
+
+    def select(self, stream=None, logits_hook=None):
+        """Indexer logits and top-k of every query row, tile by tile (one tile when the whole
+        logits buffer is small): the logits of rows [rb, re) go to logits[0 : re - rb], their top-k
+        to idx[rb : re].  `logits_hook(rb, re, logits)`, if given, runs after each tile's logits
+        call (tests read the tile there)."""
+        for rb, re in self.tiles():
+            self.indexer_logits(row_begin=rb, row_end=re, stream=stream)
+            if logits_hook is not None:
+                logits_hook(rb, re, self.logits)
+            self.topk(idx=self.idx[rb:re], row_begin=rb, row_end=re, logits=self.logits[:re - rb], stream=stream)
+
+    def indexer_stage(self, stream=None):
+        """The indexer logits of every tile (no top-k): the logits stage timed alone."""
+        for rb, re in self.tiles():
+            self.indexer_logits(row_begin=rb, row_end=re, stream=stream)
+
+    def topk_stage(self, stream=None):
+        """The top-k of every tile over the logits buffer as it stands: the top-k stage timed alone."""
+        for rb, re in self.tiles():
+            self.topk(idx=self.idx[rb:re], row_begin=rb, row_end=re, logits=self.logits[:re - rb], stream=stream)
+
+    def step(self, stream=None, logits_hook=None):
+        """One decode step: store the new keys, score and select (per row tile), attend."""
         self.store_new_keys(stream)
-        self.indexer_logits(stream=stream)
-        self.topk(stream=stream)
+        self.select(stream=stream, logits_hook=logits_hook)
         self.sparse_mla(stream=stream)
 
     # ---- end to end: host inputs -> step -> host outputs

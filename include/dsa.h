@@ -328,16 +328,21 @@ dsa_status dsa_sparse_mla_decode(const void* q_bf16, const void* kv_pool, int64_
  * The source pages have no counterpart of this call; it exists for callers that may not
  * allocate device memory while they run attention (an engine plugin whose per-step hook must
  * not allocate because the engine owns and budgets all device memory, a loop whose caching
- * allocator already holds the free memory, code running during CUDA graph capture).
+ * allocator already holds the free memory).
  * Same arguments, semantics and kernels as dsa_sparse_mla_decode, minus the workspace: the
  * split-K scratch is a fixed 16 MiB array inside the library, which every GPU that loads the
- * library holds until the process exits.  The call allocates and frees nothing.
+ * library holds until the process exits.  The call itself calls no allocator.
  *   Limit: problems with dsa_sparse_mla_workspace_size(T, H, k) > 16 MiB are rejected with
  *   DSA_ERR_UNSUPPORTED before anything is enqueued.  That size is T * H * splits * 2052 bytes,
- *   the split count depending on T and k (and 0 when one split suffices, from 38 rows up); at
- *   H = 128, k = 2048 it exceeds 16 MiB when T * splits >= 64, e.g. for 8, 16 or 32 rows.
+ *   the split count depending on T, k and the GPU's multiprocessor count (no scratch at all once
+ *   one split per row fills the GPU: on a 152-SM GB300, at k >= 512, from 39 rows up); at
+ *   H = 128, k = 2048 on that GPU it exceeds 16 MiB for 8-9, 16-19 and 32-38 rows.
  *   Set-up: the first call on each device looks up the array's device address with that device
- *   current; make that first call before any stream capture.
+ *   current.  With lazy module loading (CUDA's default) that lookup is also what loads the
+ *   library's device code on that device and so makes the 16 MiB array resident there: it can
+ *   fail with DSA_ERR_CUDA if the device has no free memory left.  Make that first call before the
+ *   caller hands its free memory to its own allocator or fixes its memory budget, and before any
+ *   stream capture.
  *   Sharing: every call uses the same array.  Calls whose kernels overlap on the GPU (different
  *   streams, or different host threads, without ordering between them) race on it: order them,
  *   e.g. on one stream.  Nothing in the array has to start at zero; a call never reads what an

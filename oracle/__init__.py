@@ -33,15 +33,36 @@ DQK = 576
 DV = 512
 
 
+_CMD = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp", "-fPIC", "-shared"]
+
+
+def _digest() -> str:
+    """Hash of the source, the compiler command and the machine type: the library is rebuilt
+    whenever it differs from the one stored beside the last build."""
+    import hashlib
+    import platform
+    h = hashlib.sha256()
+    with open(_SRC, "rb") as f:
+        h.update(f.read())
+    h.update(" ".join(_CMD).encode())
+    h.update(platform.machine().encode())
+    return h.hexdigest()
+
+
 def build(force: bool = False) -> str:
     """Compile the oracle into ``oracle/libdsa_oracle.so`` (host C, gcc, OpenMP)."""
-    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
-        return _LIB_PATH
+    digest = _digest()
+    stamp = _LIB_PATH + ".hash"
+    if not force and os.path.exists(_LIB_PATH) and os.path.exists(stamp):
+        with open(stamp) as f:
+            if f.read().strip() == digest:
+                return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp", "-fPIC",
-           "-shared", _SRC, "-o", tmp, "-lm"]
-    subprocess.run(cmd, check=True)
+    subprocess.run(_CMD + [_SRC, "-o", tmp, "-lm"], check=True)
     os.replace(tmp, _LIB_PATH)
+    with open(stamp + f".tmp{os.getpid()}", "w") as f:
+        f.write(digest + "\n")
+    os.replace(stamp + f".tmp{os.getpid()}", stamp)
     return _LIB_PATH
 
 

@@ -31,9 +31,12 @@ def oracle_pool(wl) -> np.ndarray:
     return pool
 
 
-def check_logits(got_rows: np.ndarray, ref_rows: np.ndarray, mag_rows: np.ndarray, vis: np.ndarray):
-    """got/ref/mag: [n, >= max vis]; only s < vis[i] is compared."""
+def check_logits(got_rows: np.ndarray, ref_rows: np.ndarray, mag_rows: np.ndarray, vis: np.ndarray, key=None):
+    """got/ref/mag: [n, >= max vis]; only s < vis[i] is compared.  Records, under `key`, how many
+    logits were compared and how many pass only through the 1e-5 M term (their error exceeds
+    1e-3 |I_ref|)."""
     worst = 0.0
+    n_el = n_mag = 0
     for i, v in enumerate(vis):
         g = got_rows[i, :v].astype(np.float64)
         r = ref_rows[i, :v].astype(np.float64)
@@ -44,8 +47,12 @@ def check_logits(got_rows: np.ndarray, ref_rows: np.ndarray, mag_rows: np.ndarra
         bad = err > bound
         assert not bad.any(), (f"row {i}: {bad.sum()} logits out of tolerance; worst at s={int(np.argmax(err - bound))} "
                                f"got {g[np.argmax(err - bound)]} ref {r[np.argmax(err - bound)]}")
+        n_el += int(v)
+        n_mag += int(np.count_nonzero(err > LOGIT_REL * np.abs(r)))
         if v:
             worst = max(worst, float(np.max(err / np.maximum(bound, 1e-30))))
+    if key is not None:
+        record(key, logits=n_el, logits_only_by_mag_term=n_mag)
     return worst
 
 
@@ -61,7 +68,8 @@ def kth_gap_ok(ref_row: np.ndarray, k: int) -> bool:
 
 def check_topk_valid(idx_row: np.ndarray, ref_row: np.ndarray, k: int, mag_row=None):
     """A top-k row is valid when it has min(k, v) distinct in-range ascending indices, -1 after,
-    and every kept logit is >= every dropped one up to the logit tolerance."""
+    and every kept logit is >= every dropped one up to the two logits' own tolerances
+    (1e-3 |I| + 1e-5 M of each, M per element)."""
     v = ref_row.shape[0]
     n = min(k, v)
     kept = idx_row[:n]
@@ -71,19 +79,23 @@ def check_topk_valid(idx_row: np.ndarray, ref_row: np.ndarray, k: int, mag_row=N
     if n < v:
         mask = np.ones(v, bool)
         mask[kept] = False
-        lo_kept = ref_row[kept].min()
-        hi_drop = ref_row[mask].max()
-        tol = LOGIT_REL * abs(hi_drop) + (LOGIT_MAG * float(mag_row.max()) if mag_row is not None else 0.0)
-        assert lo_kept >= hi_drop - 2 * tol
+        tol = LOGIT_REL * np.abs(ref_row)
+        if mag_row is not None:
+            tol = tol + LOGIT_MAG * np.asarray(mag_row, np.float64)
+        assert (ref_row[kept] + tol[kept]).min() >= (ref_row[mask] - tol[mask]).max()
 
 
-def check_attention(out_gpu: np.ndarray, lse_gpu: np.ndarray, out_ref: np.ndarray, lse_ref: np.ndarray):
+def check_attention(out_gpu: np.ndarray, lse_gpu: np.ndarray, out_ref: np.ndarray, lse_ref: np.ndarray, key=None):
     err = np.abs(out_gpu - out_ref)
     assert err.max() <= ATTN_ABS, f"attention max abs err {err.max()}"
     fin = np.isfinite(lse_ref)
     assert np.array_equal(fin, np.isfinite(lse_gpu))
     if fin.any():
         assert np.abs(lse_gpu[fin] - lse_ref[fin]).max() <= LSE_ABS
+    if key is not None:
+        record(key, outputs=err.size, rows=err.shape[0])
+        d = PARITY_COUNTS[key]
+        d["max_abs_err_x1e6"] = max(d.get("max_abs_err_x1e6", 0), int(round(float(err.max()) * 1e6)))
     return float(err.max())
 
 

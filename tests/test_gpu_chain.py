@@ -1,6 +1,8 @@
 """End-to-end GPU parity of one decode step (store -> logits -> top-k -> sparse MLA) against the
-CPU oracle: the whole tiny workload, and sampled rows of every full-size workload in the launch
-configuration the benchmark times (same DeviceBatch.step() calls)."""
+CPU oracle, in the launch configuration the benchmark times (the same DeviceBatch.step() calls,
+row-tiled logits included): the whole tiny workload; every row of the 32 x 8K, 64-request 64K and
+MTP 128K decode batches; every 64th row (and the last) of the 4096-row prefill chunk; and the whole
+index-K cache of every workload byte for byte."""
 import numpy as np
 import pytest
 import torch
@@ -10,66 +12,79 @@ from deepseek_sparse_attention_paged_gb300 import capi, workloads
 from deepseek_sparse_attention_paged_gb300.pipeline import DeviceBatch
 
 from helpers import (bf16_to_np_f64, check_attention, check_logits, check_topk_valid, kth_gap_ok,
-                     oracle_pool)
+                     oracle_pool, record)
 
 pytestmark = pytest.mark.gpu
 
 
-def oracle_pool_for_requests(wl, reqs):
-    """Oracle index-K cache holding only the tokens of the requests ``reqs`` (enough to score their
-    rows), built by the oracle's own store."""
-    pool = np.zeros((wl.num_pages, oracle.PAGE_BYTES), np.uint8)
-    starts = np.concatenate([[0], np.cumsum(wl.seq_lens.astype(np.int64))])
-    keys, slots = wl.index_keys(), wl.token_slots()
-    for b in sorted(set(reqs)):
-        lo, hi = starts[b], starts[b + 1]
-        assert oracle.store_index_k(keys[lo:hi], slots[lo:hi], pool) == 0
-    return pool
+def run_step_capturing_logits(db, rows):
+    """One step; the logits of `rows` are copied out of each logits tile right after its indexer
+    call (the tile buffer is reused by the next tile).  Returns them as a host array [n, ld]."""
+    rows = np.asarray(rows, np.int64)
+    got = torch.empty((len(rows), db.ld), dtype=torch.float32, device=db.device)
+    pos = {int(r): i for i, r in enumerate(rows)}
+
+    def hook(rb, re, lg):
+        sel = [r for r in range(rb, re) if r in pos]
+        if sel:
+            dst = torch.tensor([pos[r] for r in sel], device=db.device)
+            src = torch.tensor([r - rb for r in sel], device=db.device)
+            got[dst] = lg[src]
+
+    db.step(logits_hook=hook)
+    torch.cuda.synchronize()
+    return got.cpu().numpy()
 
 
-def check_rows(wl, db, rows, pool):
+def check_rows(wl, db, rows, pool, got_lg, key):
     rows = np.asarray(rows, np.int64)
     vis = wl.visible_lens()[rows]
     ld = db.ld
-    got_lg = db.logits[torch.from_numpy(rows).cuda()].cpu().numpy()
     ref_lg, mag, bad = oracle.indexer_logits(wl.index_q(), wl.weights(), pool, wl.block_table, wl.seq_lens,
                                              wl.cu_q, rows, ld, want_mag=True)
     assert bad == 0
-    check_logits(got_lg, ref_lg, mag, vis)
+    check_logits(got_lg, ref_lg, mag, vis, key=key)
     # top-k: GPU indices from GPU logits vs oracle indices from oracle logits
     ref_idx = oracle.topk(ref_lg, wl.seq_lens, wl.cu_q, rows, wl.topk)
     got_idx = db.idx[torch.from_numpy(rows).cuda()].cpu().numpy()
-    exact_rows = []
+    exact_rows, gap_rows = [], 0
     for i, r in enumerate(rows):
         v = int(vis[i])
         if kth_gap_ok(ref_lg[i, :v], wl.topk):
+            gap_rows += 1
             assert np.array_equal(got_idx[i], ref_idx[i]), f"row {r}: top-k set differs outside the tie band"
         check_topk_valid(got_idx[i], ref_lg[i, :v].astype(np.float64), wl.topk, mag[i, :v])
         if np.array_equal(got_idx[i], ref_idx[i]):
             exact_rows.append(i)
+    record(key, topk_rows=len(rows), topk_rows_outside_tie_band=gap_rows, topk_rows_equal_to_oracle=len(exact_rows))
     # the GPU top-k kernel on the oracle's logits must match the oracle's top-k bit for bit
     lg_t = torch.from_numpy(np.ascontiguousarray(ref_lg)).cuda()
-    for i, r in enumerate(rows):
-        one = torch.empty((1, wl.topk), dtype=torch.int32, device="cuda")
-        db.topk(logits=lg_t[i:i + 1], idx=one, row_begin=int(r), row_end=int(r) + 1)
-        assert np.array_equal(one.cpu().numpy()[0], ref_idx[i])
+    if np.array_equal(rows, np.arange(rows[0], rows[0] + len(rows))):
+        got = torch.empty((len(rows), wl.topk), dtype=torch.int32, device="cuda")
+        db.topk(logits=lg_t, idx=got, row_begin=int(rows[0]), row_end=int(rows[0]) + len(rows))
+        assert np.array_equal(got.cpu().numpy(), ref_idx)
+    else:
+        for i, r in enumerate(rows):
+            one = torch.empty((1, wl.topk), dtype=torch.int32, device="cuda")
+            db.topk(logits=lg_t[i:i + 1], idx=one, row_begin=int(r), row_end=int(r) + 1)
+            assert np.array_equal(one.cpu().numpy()[0], ref_idx[i]), f"row {r}"
+    record(key, topk_on_oracle_logits_rows=len(rows))
     # attention: rows whose GPU selection equals the oracle's compare the step's own output
     if db.kv_pool is not None:
         ref_o, ref_l = oracle.sparse_mla(wl.mla_q(), wl.latent_pool(), wl.block_table, wl.seq_lens, wl.cu_q,
-                                         _full_idx(wl, rows, ref_idx),
-                                         wl.scale, rows)
+                                         _full_idx(wl, rows, ref_idx), wl.scale, rows)
         out = bf16_to_np_f64(db.out[torch.from_numpy(rows).cuda()])
         lse = db.lse[torch.from_numpy(rows).cuda()].cpu().numpy().astype(np.float64)
         ex = np.asarray(exact_rows, np.int64)
         if ex.size:
-            check_attention(out[ex], lse[ex], ref_o[ex], ref_l[ex])
-        # and the GPU attention fed the oracle's selection for every sampled row
+            check_attention(out[ex], lse[ex], ref_o[ex], ref_l[ex], key=key + "/attention_of_step")
+        # and the GPU attention fed the oracle's selection for every checked row
         idx_all = db.idx.clone()
         idx_all[torch.from_numpy(rows).cuda()] = torch.from_numpy(ref_idx).cuda()
         db.sparse_mla(idx=idx_all)
         out2 = bf16_to_np_f64(db.out[torch.from_numpy(rows).cuda()])
         lse2 = db.lse[torch.from_numpy(rows).cuda()].cpu().numpy().astype(np.float64)
-        check_attention(out2, lse2, ref_o, ref_l)
+        check_attention(out2, lse2, ref_o, ref_l, key=key + "/attention_of_oracle_selection")
     return len(exact_rows)
 
 
@@ -82,39 +97,36 @@ def _full_idx(wl, rows, ref_idx):
 def test_chain_tiny_all_rows():
     wl = workloads.make("tiny")
     db = DeviceBatch(wl)
-    db.step()
-    torch.cuda.synchronize()
+    got_lg = run_step_capturing_logits(db, np.arange(wl.T))
     assert db.device_error() == (0, 0)
     pool = oracle_pool(wl)
     assert np.array_equal(db.index_pool.cpu().numpy(), pool)
-    n_exact = check_rows(wl, db, np.arange(wl.T), pool)
+    n_exact = check_rows(wl, db, np.arange(wl.T), pool, got_lg, "chain/tiny")
     assert n_exact == wl.T
 
 
-SAMPLES = {
-    "decode_b32_8k": lambda wl: [0, 17, 31],
-    "decode_b64_logu64k": lambda wl: [int(np.argmax(wl.seq_lens)), int(np.argmin(wl.seq_lens)), 40],
-    "mtp_b8_128k": lambda wl: [0, 1, 15],
-    "prefill_32k_4k": lambda wl: [0, 1, 2047, 4095],
+ROWS = {
+    "decode_b32_8k": lambda wl: np.arange(wl.T),
+    "decode_b64_logu64k": lambda wl: np.arange(wl.T),
+    "mtp_b8_128k": lambda wl: np.arange(wl.T),
+    "prefill_32k_4k": lambda wl: np.unique(np.concatenate([np.arange(0, wl.T, 64), [wl.T - 1]])),
 }
 
 
-@pytest.mark.parametrize("name", list(SAMPLES))
-def test_chain_full_size_sampled_rows(name):
+@pytest.mark.parametrize("name", list(ROWS))
+def test_chain_full_size(name):
     wl = workloads.make(name)
     db = DeviceBatch(wl)
-    db.step()
-    torch.cuda.synchronize()
+    rows = ROWS[name](wl)
+    got_lg = run_step_capturing_logits(db, rows)
     assert db.device_error() == (0, 0)
-    rows = SAMPLES[name](wl)
-    cu = wl.cu_q
-    reqs = [int(np.searchsorted(cu, r, side="right") - 1) for r in rows]
-    pool = oracle_pool_for_requests(wl, reqs)
-    # the stored index-K pages of those requests are bit-exact
-    pages = np.unique(np.concatenate([wl.block_table[b][wl.block_table[b] >= 0] for b in set(reqs)]))
-    got_pages = db.index_pool[torch.from_numpy(pages.astype(np.int64)).cuda()].cpu().numpy()
-    assert np.array_equal(got_pages, pool[pages])
-    check_rows(wl, db, rows, pool)
+    if name == "prefill_32k_4k":
+        assert len(db.tiles()) > 1          # the 4096 x 36864 logits are produced in row tiles
+    # the whole index-K cache (every request's pages, this step's keys included) is bit-exact
+    pool = oracle_pool(wl)
+    assert np.array_equal(db.index_pool.cpu().numpy(), pool)
+    record(f"chain/{name}", index_pages=wl.num_pages)
+    check_rows(wl, db, rows, pool, got_lg, f"chain/{name}")
 
 
 def test_step_io_graph_matches_eager_step():

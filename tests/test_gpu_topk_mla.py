@@ -8,7 +8,7 @@ import oracle
 from deepseek_sparse_attention_paged_gb300 import capi, workloads
 from deepseek_sparse_attention_paged_gb300.pipeline import DeviceBatch
 
-from helpers import bf16_to_np_f64, check_attention, oracle_pool
+from helpers import bf16_to_np_f64, check_attention, check_topk_valid, kth_gap_ok, oracle_pool
 
 pytestmark = pytest.mark.gpu
 
@@ -192,3 +192,44 @@ def test_lightning_indexer_equals_logits_then_topk():
     with pytest.raises(capi.DSAError):     # short workspace
         capi.dsa_lightning_indexer(db.index_q, db.weights, db.index_pool, db.block_table, db.seq_lens, db.cu_q,
                                    wl.max_seq_len, wl.max_q_len, wl.topk, got, ws[:1024])
+
+
+def test_lightning_indexer_matches_oracle():
+    """The one-call indexer against the oracle: oracle.topk_forced on the oracle's logits, exactly
+    wherever the k-th / (k+1)-th gap (with the forced positions at +inf) is outside the tie band,
+    and a valid selection everywhere (forced positions kept, every other kept logit >= every dropped
+    one up to the logit tolerance), with and without forced initial / local tokens."""
+    from helpers import oracle_pool, record
+    wl = workloads.make_custom("li_oracle", 241, [500, 64, 3000, 17000, 40000, 70000], [1, 2, 3, 1, 1, 2], topk=256,
+                               heads=16)
+    db = DeviceBatch(wl, with_latent=False)
+    pool = oracle_pool(wl)
+    rows = np.arange(wl.T)
+    ref_lg, mag, bad = oracle.indexer_logits(wl.index_q(), wl.weights(), pool, wl.block_table, wl.seq_lens, wl.cu_q,
+                                             rows, db.ld, want_mag=True)
+    assert bad == 0
+    vis = wl.visible_lens()
+    ws = torch.empty(capi.dsa_lightning_indexer_workspace_size(wl.T, wl.max_seq_len), dtype=torch.uint8,
+                     device="cuda")
+    for n_init, n_local in ((0, 0), (2, 8)):
+        got = torch.full((wl.T, wl.topk), -7, dtype=torch.int32, device="cuda")
+        capi.dsa_lightning_indexer(db.index_q, db.weights, db.index_pool, db.block_table, db.seq_lens, db.cu_q,
+                                   wl.max_seq_len, wl.max_q_len, wl.topk, got, ws, n_init=n_init, n_local=n_local)
+        got = got.cpu().numpy()
+        ref = oracle.topk_forced(ref_lg, wl.seq_lens, wl.cu_q, rows, wl.topk, n_init, n_local)
+        exact = 0
+        for r in rows:
+            v = int(vis[r])
+            row = ref_lg[r, :v].astype(np.float64).copy()
+            forced = np.zeros(v, bool)
+            forced[:min(n_init, v)] = True
+            if n_local:
+                forced[max(0, v - n_local):] = True
+            row[forced] = np.inf
+            assert np.all(np.isin(np.flatnonzero(forced), got[r])), f"row {r}: a forced position is missing"
+            finite = row[np.isfinite(row)]
+            if forced.sum() >= wl.topk or v <= wl.topk or kth_gap_ok(np.concatenate([row[forced], finite]), wl.topk):
+                assert np.array_equal(got[r], ref[r]), f"row {r}: differs from the oracle outside the tie band"
+                exact += 1
+            check_topk_valid(got[r], row, wl.topk, mag[r, :v])
+        record("lightning_indexer_vs_oracle", rows=len(rows), rows_exact=exact)

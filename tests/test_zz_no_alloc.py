@@ -3,7 +3,8 @@ memory (it takes no workspace and uses the library's fixed 16 MiB scratch instea
 
 Checked through the C ABI against the workspace-taking dsa_sparse_mla_decode on the same inputs,
 on two calls in a row with different inputs (the scratch is shared between calls and keeps the
-previous call's contents), and for the size limit.  This file is collected last so that a run that
+previous call's contents), for device memory left unchanged by a call after the first, and for the
+size limit.  This file is collected last so that a run that
 stops at the first failure has already run every other test."""
 import numpy as np
 import pytest
@@ -64,6 +65,29 @@ def test_no_alloc_matches_workspace_entry_point_twice_in_a_row():
     got = _no_alloc(wl2, db2, idx2)
     _compare(got, _with_workspace(wl2, db2, idx2))
     assert float(got[0][2].abs().max()) == 0.0 and bool(torch.isneginf(got[1][2]).all())
+
+
+def test_no_alloc_call_after_the_first_leaves_device_memory_unchanged():
+    """After one call on the device (which may load the library's device code and with it the
+    fixed scratch), further calls take no device memory: the driver's free-memory count is the
+    same before and after a call that uses the scratch (8 splits of 3 rows)."""
+    wl, db, idx = _inputs(904, [4000, 2500, 9000], 128, 2048)
+    assert capi.dsa_sparse_mla_workspace_size(wl.T, wl.heads, wl.topk) > 0
+    out = torch.empty_like(db.out)
+    lse = torch.empty_like(db.lse)
+
+    def call():
+        capi.dsa_sparse_mla_decode_noalloc(db.mla_q, db.kv_pool, db.block_table, db.seq_lens, db.cu_q, idx,
+                                           wl.scale, out, lse=lse)
+
+    call()
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    call()
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+    _compare((out, lse), _with_workspace(wl, db, idx))
 
 
 def test_no_alloc_rejects_problems_larger_than_its_scratch():
