@@ -6,39 +6,44 @@
 // MLACommonImpl.forward decode branch (absorbed 576-wide query, one shared KV head; _forward_decode
 // returns (out, lse); merge_attn_states merges partial results by their log-sum-exp).
 //
-// Work split.  CTA = (query row r, split j of the k selected entries, rank h of a 2-CTA cluster).
-// The 576 latent dims are cut into 9 chunks of 64; rank 0 owns chunks 0-3 and 8 (value dims
-// 0..255 and the 64 rope dims), rank 1 owns chunks 4-7 (value dims 256..511).  Each CTA reads only
-// its own chunks of every selected row (16-byte cp.async straight into the swizzled operand
-// layout), keeps only its own query chunks (in tensor memory), computes the partial score tile
-// over its dims, and the two CTAs swap partial score tiles through distributed shared memory
-// (st.async, counted as transaction bytes on the receiver's mbarrier; the receiver answers with a
-// 4-byte st.async per warp once it has consumed them, so no fence is needed); both then hold the
-// full scores, run the same softmax (identical P: the fp32 sum is commutative) and
-// each accumulates its 256 output dims from its own value chunks.  Nothing of a latent row is read
-// twice or copied between the CTAs, and their key stages are private, so each CTA runs a 4-deep
-// load pipeline of its own.
+// Work split.  CTA = (query row r, split j of the k selected entries, rank c of a 2-CTA cluster).
+// Rank c owns the value dims 256 c .. 256 c + 255 (latent chunks 4c .. 4c+3 of 64 dims) and half of
+// the rope dims, 512 + 32 c .. 512 + 32 c + 31: 288 of the 576 dims each.  A CTA reads only its own
+// dims of every selected row (16-byte cp.async straight into the tensor-core operand layouts),
+// keeps only its own query dims, computes the partial score tile over them, and the two CTAs swap
+// partial score tiles through distributed shared memory (st.async, counted as transaction bytes on
+// the receiver's mbarrier; the receiver returns a 4-byte st.async per warp once it has read them).
+// Both then hold the full scores, run the same softmax (identical P: the fp32 sum is commutative)
+// and each accumulates its 256 output dims from its own value chunks.  Nothing of a latent row is
+// read twice or copied between the CTAs.
+//
+// Pipelining.  Score tiles are double-buffered in tensor memory and the swap buffers in shared
+// memory, so the score MMAs of tile t+1 and the swap of its partial scores overlap the softmax of
+// tile t; P is written back over its score tile in tensor memory (bf16) and read from there by the
+// PV MMA, which leaves shared memory for a 4-deep load ring.
 //
 // Tensor memory (512 columns x 128 lanes, lane = head):
-//   [0, 256)   O, this CTA's 256 output dims (fp32)
-//   [256, 320) partial score tile of 64 keys (fp32)
-//   [320, 480) this CTA's query chunks, the A operand of the score MMA (two bf16 per column)
-// Shared memory: 4 stages of 64 rows x this CTA's chunks (128-byte swizzle, K-major; the first 4
-// chunks double as the MN-major value operand); the peer's partial scores (32 KB); 2 buffers of P.
+//   [0, 256)    O, this CTA's 256 output dims (fp32)
+//   [256, 320)  score tile buffer 0 (fp32, 64 keys); P of that tile over its first 32 columns
+//   [320, 384)  score tile buffer 1
+//   [384, 512)  this CTA's 4 value-dim query chunks, the A operand of the score MMA (two bf16 per column)
+// Shared memory: 4 stages of 64 keys x (4 chunks of 128 B, 128-byte swizzle, K-major; they double as
+// the MN-major value operand) + (32 rope dims, no swizzle); 2 buffers of the peer's partial scores
+// (32 KB each); the query's rope half (8 KB, no swizzle).
 //
-// Roles (288 threads), for tiles of 64 selected entries:
-//   warps 0-3 (thread = head = TMEM lane): query chunks into TMEM; per tile: read the partial
-//           scores, send them to the peer, add the peer's, online softmax in the log2 domain with
-//           lazy rescaling (O and l are rescaled only when the running max grows by more than 8,
-//           so p <= 2^8 otherwise), P to shared memory as bf16; O / l and lse at the end;
-//   warp 4 (MMA):  S_h = Q_h K_h^T (M = 128 heads, N = 64 keys, K = 320 or 256) and O += P V_h
-//           (M = 128, N = 256 dims, K = 64 keys), bf16 in, fp32 accumulate in TMEM; issues
-//           whichever of the next score MMA and the next PV is ready first;
-//   warps 5-8 (producers): warp 5 + w resolves entries 16 w .. 16 w + 15 of each tile to latent
-//           rows two batches ahead (independent loads) and copies this CTA's chunks of those rows
+// Roles (416 threads), for tiles of 64 selected entries:
+//   warps 0-7 (softmax): warp w reads TMEM lanes 32 (w % 4) .. +31 (head = lane), keys 32 (w / 4) ..
+//           +31 of each tile.  Query into TMEM / shared memory; per tile: read its partial scores,
+//           send them to the peer, add the peer's, tile max shared with the warp holding the other
+//           keys of the same heads, online softmax in the log2 domain with lazy rescaling (O and l
+//           are rescaled only when the running max grows by more than 8, so p <= 2^8 otherwise), P
+//           into tensor memory as bf16; O / l and lse at the end (each warp 128 of the 256 dims);
+//   warp 8 (MMA):  S = Q_c K_c^T (M = 128 heads, N = 64 keys, K = 288) and O += P V_c (M = 128,
+//           N = 256 dims, K = 64 keys), bf16 in, fp32 accumulate in TMEM; issues whichever of the
+//           next score MMA and the next PV is ready first;
+//   warps 9-12 (producers): warp 9 + w resolves entries 16 w .. 16 w + 15 of each tile to latent
+//           rows two batches ahead (independent loads) and copies this CTA's dims of those rows
 //           (padding / invalid entries read row 0 and get probability 0).
-// Score MMAs are issued with N = 64: on this tensor core an M = 128, K = 16 MMA takes the same time
-// for N = 32 and N = 64, so wider key tiles halve the score cost per key.
 // With one split the CTA writes bf16 output directly; with several, normalised fp32 partials and
 // their lse go to the workspace and a combine kernel merges them.
 #include <cuda_bf16.h>
@@ -51,37 +56,34 @@ namespace {
 
 constexpr int kHeadsPerCta = 128;                 // M of both MMAs (fewer heads: rows unused)
 constexpr int kKeysPerTile = 64;
-constexpr int kChunks = kLatentDim / 64;          // 9 chunks of 64 dims (128 bytes)
-constexpr int kMaxOwnChunks = 5;                  // rank 0: chunks 0-3 and 8; rank 1: chunks 4-7
+constexpr int kOwnChunks = 4;                     // value chunks per CTA (64 dims, 128 B each)
+constexpr int kRopeHalf = 32;                     // rope dims per CTA
 constexpr int kHalfDims = kValueDim / 2;          // 256 output dims per CTA
 constexpr int kKvChunkBytes = kKeysPerTile * 128;               // 8192
-constexpr int kKvStageBytes = kMaxOwnChunks * kKvChunkBytes;    // 40960
+constexpr int kRopeBytes = kKeysPerTile * kRopeHalf * 2;        // 4096
+constexpr int kKvStageBytes = kOwnChunks * kKvChunkBytes + kRopeBytes;   // 36864 (1024-aligned)
 constexpr int kKvStages = 4;
 constexpr int kXBytes = kHeadsPerCta * kKeysPerTile * 4;        // 32768: the peer's partial scores
-constexpr int kPBytes = kHeadsPerCta * kKeysPerTile * 2;        // 16384
-constexpr int kSoftmaxWarps = 4;
-constexpr int kMmaWarp = 4;
-constexpr int kProducerWarp0 = 5;
+constexpr int kQRopeBytes = kHeadsPerCta * kRopeHalf * 2;       // 8192
+constexpr int kSoftmaxWarps = 8;
+constexpr int kMmaWarp = 8;
+constexpr int kProducerWarp0 = 9;
 constexpr int kProducerWarps = 4;
-constexpr int kMlaThreads = 32 * (kProducerWarp0 + kProducerWarps);   // 288
+constexpr int kMlaThreads = 32 * (kProducerWarp0 + kProducerWarps);   // 416
 constexpr int kKeysPerProducer = kKeysPerTile / kProducerWarps;       // 16
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = kHalfDims;                          // partial scores at columns 256 .. 319
-constexpr uint32_t kTmemQ = kTmemS + kKeysPerTile;              // query chunks at columns 320 .. 479
+constexpr uint32_t kTmemS = kHalfDims;                          // score buffers at columns 256 and 320
+constexpr uint32_t kTmemQ = kTmemS + 2 * kKeysPerTile;          // query chunks at columns 384 .. 511
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;                       // log2 units
 constexpr int kBatch = 4;                                       // tiles resolved per batch
-constexpr size_t kMlaSmemBytes = 1024 + size_t(kKvStages) * kKvStageBytes + kXBytes + 2 * kPBytes + 512;
+constexpr size_t kBarBytes = 4096;
+constexpr size_t kMlaSmemBytes = 1024 + size_t(kKvStages) * kKvStageBytes + 2 * size_t(kXBytes) + kQRopeBytes +
+                                 kBarBytes;
 
-static_assert(kChunks == 9 && kMaxOwnChunks + 4 == kChunks, "chunk ownership: 5 + 4");
-static_assert(kTmemQ + kMaxOwnChunks * 32 <= kTmemCols, "tensor-memory budget");
+static_assert(kKvStageBytes % 1024 == 0, "stages keep the 1024-byte alignment of the swizzled chunks");
+static_assert(kTmemQ + kOwnChunks * 32 == kTmemCols, "tensor-memory budget");
 static_assert(kMlaSmemBytes <= 232448, "shared-memory budget");
-
-// Global chunk index of this CTA's local chunk j.
-__device__ __forceinline__ int own_chunk(uint32_t rank, int j) {
-    return rank == 0 ? (j < 4 ? j : 8) : 4 + j;
-}
-
 // Shared-memory matrix descriptor (sm_100 format): start, leading / stride byte offsets, layout.
 __device__ __forceinline__ uint64_t make_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
     uint64_t d = 0;
@@ -173,23 +175,42 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+// Byte offset of 16-byte piece j (dims 8 j .. 8 j + 7) of row i in a K-major operand without
+// swizzle whose rows hold 4 pieces (64 bytes): 8-row core matrices of 128 contiguous bytes, the 4
+// core matrices of a row group 128 bytes apart (leading byte offset), row groups 512 bytes apart
+// (stride byte offset).
+__device__ __forceinline__ uint32_t rope_off(int i, int j) {
+    return static_cast<uint32_t>((i >> 3) * 512 + j * 128 + (i & 7) * 16);
+}
+
 struct MlaBars {
-    uint64_t q_full;               // query chunks in TMEM (4 softmax warps)
+    uint64_t q_full;               // query in TMEM / shared memory (8 softmax warps)
     uint64_t kv_full[kKvStages];   // every producer thread's cp.async landed + one arrive per producer warp
     uint64_t kv_empty[kKvStages];  // PV of the stage's tile completed
-    uint64_t s_full;               // partial score MMAs completed
-    uint64_t s_empty;              // partial scores read out of TMEM
-    uint64_t x_full;               // the peer's partial scores are in x (local arm + the peer's 32 KB)
-    uint64_t x_free;               // the peer consumed the scores this CTA sent (local arm + 4 x 4 B)
-    uint32_t x_sink[4];            // target of the peer's 4-byte consumed signals
-    uint64_t p_full[2];
-    uint64_t p_empty[2];
-    uint64_t o_full;
+    uint64_t s_full[2];            // score MMAs of the buffer's tile completed
+    uint64_t s_free[2];            // PV that read P from the buffer completed (buffer reusable)
+    uint64_t p_full[2];            // P of the buffer's tile in TMEM (8 softmax warps)
+    uint64_t x_full[2];            // the peer's partial scores are in x[b] (local arm + the peer's 32 KB)
+    uint64_t x_free[2];            // the peer read the scores this CTA sent into its x[b] (local arm + 8 x 4 B)
+    uint64_t o_full;               // last PV completed
+    uint64_t pair[4];              // the two softmax warps of lane quadrant q (all 64 threads arrive)
+    uint32_t x_sink[2][kSoftmaxWarps];   // targets of the peer's 4-byte consumed signals
     uint32_t tmem_slot;
     uint32_t pad;
     uint32_t valid[kKvStages][kProducerWarps];   // bit i: entry 16 w + i of the stage's tile is real
+    float tmax[2][2][kHeadsPerCta];   // [tile parity][key half]: this tile's maximum (shared by the warp pair)
+    float lsum[2][kHeadsPerCta];   // per key half: the final partial row sums
 };
-static_assert(sizeof(MlaBars) <= 512, "barrier block");
+static_assert(sizeof(MlaBars) <= kBarBytes, "barrier block");
 
 __global__ void __launch_bounds__(kMlaThreads, 1)
 sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restrict__ q, int64_t num_pages,
@@ -200,10 +221,10 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw_addr = ptx::smem_addr(smem_raw);
     unsigned char* base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-    unsigned char* kvs = base;                                  // [4][5 chunks][64 keys][128 B], SW128
-    float* xs = reinterpret_cast<float*>(kvs + kKvStages * kKvStageBytes);   // [2][16 key quads][128 heads][4]
-    unsigned char* ps = reinterpret_cast<unsigned char*>(xs) + kXBytes;     // [2][16 head groups][8 key groups][8][16 B]
-    MlaBars& bar = *reinterpret_cast<MlaBars*>(ps + 2 * kPBytes);
+    unsigned char* kvs = base;                                         // [4][4 chunks x 8 KB | rope 4 KB]
+    float* xs = reinterpret_cast<float*>(kvs + kKvStages * kKvStageBytes);   // [2][2 halves][8 quads][128 heads][4]
+    unsigned char* qrope = reinterpret_cast<unsigned char*>(xs) + 2 * kXBytes;   // [128 heads x 32 dims], no swizzle
+    MlaBars& bar = *reinterpret_cast<MlaBars*>(qrope + kQRopeBytes);
 
     const int split = blockIdx.y;
     const int r = blockIdx.z;
@@ -217,8 +238,7 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
     const int ntiles = e_end > e_begin ? (e_end - e_begin + kKeysPerTile - 1) / kKeysPerTile : 0;
     const uint32_t crank = cluster_ctarank();
     const uint32_t peer = crank ^ 1u;
-    const int nown = crank == 0 ? kMaxOwnChunks : kMaxOwnChunks - 1;   // own chunks: 5 or 4
-    const int half = static_cast<int>(crank);                          // output dims 256 half ..
+    const int half = static_cast<int>(crank);   // output dims 256 half .., rope dims 512 + 32 half ..
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(&bar.q_full, kSoftmaxWarps);
@@ -226,15 +246,15 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
             ptx::mbar_init(&bar.kv_full[s], kProducerWarps * 32 + kProducerWarps);
             ptx::mbar_init(&bar.kv_empty[s], 1);
         }
-        ptx::mbar_init(&bar.s_full, 1);
-        ptx::mbar_init(&bar.s_empty, kSoftmaxWarps);
-        ptx::mbar_init(&bar.x_full, 1);
-        ptx::mbar_init(&bar.x_free, 1);
         for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(&bar.s_full[a], 1);
+            ptx::mbar_init(&bar.s_free[a], 1);
             ptx::mbar_init(&bar.p_full[a], kSoftmaxWarps);
-            ptx::mbar_init(&bar.p_empty[a], 1);
+            ptx::mbar_init(&bar.x_full[a], 1);
+            ptx::mbar_init(&bar.x_free[a], 1);
         }
         ptx::mbar_init(&bar.o_full, 1);
+        for (int qd = 0; qd < 4; ++qd) ptx::mbar_init(&bar.pair[qd], 64);
         ptx::fence_barrier_init();
     }
     if (warp == kMmaWarp) {
@@ -279,11 +299,12 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
         for (int u = 0; u < kBatch; ++u) page1[u] = load_page(pos1[u]);
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) pos2[u] = load_pos(kBatch + u);
-        // copy lane layout: lane = 8 * (key % 4) + 16-byte piece of a 128-byte chunk row
+        // value chunks: lane = 8 * (key % 4) + 16-byte piece of a 128-byte chunk row;
+        // rope half: lane = 4 * (key % 8) + 16-byte piece of the 64-byte rope row
         const int piece = lane & 7;
-        int gch[kMaxOwnChunks];
-#pragma unroll
-        for (int j = 0; j < kMaxOwnChunks; ++j) gch[j] = own_chunk(crank, j);
+        const int rpiece = lane & 3;
+        const uint16_t* kv_val = kv + half * kHalfDims + piece * 8;
+        const uint16_t* kv_rope = kv + kValueDim + half * kRopeHalf + rpiece * 8;
         for (int t0 = 0; t0 < ntiles && !timed_out; t0 += kBatch) {
             int rows[kBatch];
 #pragma unroll
@@ -307,20 +328,23 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
                 if (lane == 0 && !ptx::mbar_wait(&bar.kv_empty[s], ph ^ 1u, deadline)) timed_out = true;
                 timed_out = __shfl_sync(0xffffffffu, timed_out ? 1 : 0, 0) != 0;
                 if (timed_out) break;
-                int rk[kKeysPerProducer / 4];
-#pragma unroll
-                for (int kq = 0; kq < kKeysPerProducer / 4; ++kq)
-                    rk[kq] = __shfl_sync(0xffffffffu, row_src, kq * 4 + (lane >> 3));
                 const uint32_t stage = kv_addr0 + s * kKvStageBytes;
 #pragma unroll
-                for (int j = 0; j < kMaxOwnChunks; ++j) {
-                    if (j >= nown) break;
+                for (int kq = 0; kq < kKeysPerProducer / 4; ++kq) {
+                    const int kl = kq * 4 + (lane >> 3);                 // key within this warp's 16
+                    const int key = pw * kKeysPerProducer + kl;
+                    const int64_t row = __shfl_sync(0xffffffffu, row_src, kl);
+                    const uint16_t* src = kv_val + row * kLatentDim;
 #pragma unroll
-                    for (int kq = 0; kq < kKeysPerProducer / 4; ++kq) {
-                        const int key = pw * kKeysPerProducer + kq * 4 + (lane >> 3);
-                        const uint32_t dst = stage + j * kKvChunkBytes + key * 128 + ((piece ^ (key & 7)) << 4);
-                        cp_async_16(dst, kv + static_cast<int64_t>(rk[kq]) * kLatentDim + gch[j] * 64 + piece * 8);
-                    }
+                    for (int j = 0; j < kOwnChunks; ++j)
+                        cp_async_16(stage + j * kKvChunkBytes + key * 128 + ((piece ^ (key & 7)) << 4), src + j * 64);
+                }
+#pragma unroll
+                for (int kq = 0; kq < kKeysPerProducer / 8; ++kq) {
+                    const int kl = kq * 8 + (lane >> 2);
+                    const int key = pw * kKeysPerProducer + kl;
+                    const int64_t row = __shfl_sync(0xffffffffu, row_src, kl);
+                    cp_async_16(stage + kOwnChunks * kKvChunkBytes + rope_off(key, rpiece), kv_rope + row * kLatentDim);
                 }
                 cp_async_arrive_noinc(&bar.kv_full[s]);
                 if (lane == 0) {
@@ -335,44 +359,49 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
         if (lane == 0) {
             constexpr uint32_t idesc_qk = ptx::instr_desc(1, 1, kHeadsPerCta, kKeysPerTile);
             constexpr uint32_t idesc_pv = ptx::instr_desc(1, 1, kHeadsPerCta, kHalfDims) | (1u << 16);  // B MN-major
-            const uint32_t p_addr = ptx::smem_addr(ps);
+            const uint32_t qrope_addr = ptx::smem_addr(qrope);
             bool ok = ptx::mbar_wait(&bar.q_full, 0, deadline);
             int tq = 0, tp = 0;   // next score tile, next PV tile
             while (ok && tp < ntiles) {
                 bool issued = false;
-                // score MMAs of tile tq: its chunks landed and the previous partial scores were read
+                // score MMAs of tile tq: its dims landed and its score buffer's previous PV completed
                 if (tq < ntiles && ptx::mbar_test_wait(&bar.kv_full[tq % kKvStages], (tq / kKvStages) & 1) &&
-                    ptx::mbar_test_wait(&bar.s_empty, (tq & 1) ^ 1u)) {
-                    ptx::fence_proxy_async_smem();   // chunks written by cp.async, read by the tensor cores
+                    ptx::mbar_test_wait(&bar.s_free[tq & 1], ((tq >> 1) & 1) ^ 1u)) {
+                    ptx::fence_proxy_async_smem();   // rows written by cp.async, read by the tensor cores
                     ptx::tc_fence_after_sync();
                     const uint32_t kb = kv_addr0 + (tq % kKvStages) * kKvStageBytes;
-                    const uint32_t d = tmem + kTmemS;
+                    const uint32_t d = tmem + kTmemS + (tq & 1) * kKeysPerTile;
 #pragma unroll 1
-                    for (int j = 0; j < nown; ++j) {
+                    for (int j = 0; j < kOwnChunks; ++j) {
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
                             const uint64_t db = make_desc(kb + j * kKvChunkBytes + kk * 32, 16, 1024, kLayoutSw128);
                             umma_f16_ts(d, tmem + kTmemQ + j * 32 + kk * 8, db, idesc_qk, (j | kk) != 0 ? 1u : 0u);
                         }
                     }
-                    ptx::umma_commit(&bar.s_full);
+#pragma unroll
+                    for (int kk = 0; kk < kRopeHalf / 16; ++kk) {
+                        const uint64_t da = make_desc(qrope_addr + kk * 256, 128, 512, kLayoutNone);
+                        const uint64_t db = make_desc(kb + kOwnChunks * kKvChunkBytes + kk * 256, 128, 512, kLayoutNone);
+                        ptx::umma_f16(d, da, db, idesc_qk, 1u);
+                    }
+                    ptx::umma_commit(&bar.s_full[tq & 1]);
                     ++tq;
                     issued = true;
                 }
-                // O += P(tp) V(tp)
+                // O += P(tp) V(tp), P read from its score buffer in TMEM
                 if (tp < tq && ptx::mbar_test_wait(&bar.p_full[tp & 1], (tp >> 1) & 1)) {
                     ptx::tc_fence_after_sync();
                     const int s = tp % kKvStages;
-                    const int pb = tp & 1;
                     const uint32_t vb = kv_addr0 + s * kKvStageBytes;   // own chunks 0-3 = this CTA's value dims
+                    const uint32_t pa = tmem + kTmemS + (tp & 1) * kKeysPerTile;
 #pragma unroll
                     for (int ks = 0; ks < kKeysPerTile / 16; ++ks) {
-                        const uint64_t da = make_desc(p_addr + pb * kPBytes + ks * 256, 128, 1024, kLayoutNone);
                         const uint64_t db = make_desc(vb + ks * 16 * 128, kKvChunkBytes, 1024, kLayoutSw128);
-                        ptx::umma_f16(tmem, da, db, idesc_pv, (tp | ks) != 0 ? 1u : 0u);
+                        umma_f16_ts(tmem, pa + ks * 8, db, idesc_pv, (tp | ks) != 0 ? 1u : 0u);
                     }
                     ptx::umma_commit(&bar.kv_empty[s]);
-                    ptx::umma_commit(&bar.p_empty[pb]);
+                    ptx::umma_commit(&bar.s_free[tp & 1]);
                     ++tp;
                     issued = true;
                 }
@@ -382,17 +411,20 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
             if (!ok) timed_out = true;
         }
     } else {
-        // ---------------------------------------------------------------- query -> TMEM, softmax, epilogue
-        const int quad = warp;                      // warps 0..3: TMEM lanes 32 quad .. +31
+        // ---------------------------------------------------------------- query, softmax, epilogue
+        const int quad = warp & 3;                  // TMEM lanes 32 quad .. +31
+        const int kh = warp >> 2;                   // keys 32 kh .. 32 kh + 31 of every tile
         const int head = quad * 32 + lane;          // TMEM lane = head
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         {
-            // this CTA's query chunks of this head into TMEM columns 320.., two bf16 per column
+            // value chunks 2 kh, 2 kh + 1 of this CTA into TMEM; rope pieces 2 kh, 2 kh + 1 into
+            // shared memory
             const uint4* src = reinterpret_cast<const uint4*>(q + (static_cast<int64_t>(r) * H + head) * kLatentDim);
             const bool live = head < H;
 #pragma unroll 1
-            for (int j = 0; j < nown; ++j) {
-                const int c = own_chunk(crank, j);
+            for (int jj = 0; jj < 2; ++jj) {
+                const int j = 2 * kh + jj;
+                const int c = 4 * half + j;           // global chunk
                 uint4 raw[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) raw[i] = live ? __ldg(src + c * 8 + i) : make_uint4(0u, 0u, 0u, 0u);
@@ -406,73 +438,95 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
                 }
                 tmem_st_32x32b_x32(tmem + lane_base + kTmemQ + j * 32, w);
             }
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                const int j = 2 * kh + jj;
+                const uint4 pr = live ? __ldg(src + (kValueDim + half * kRopeHalf) / 8 + j) : make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(qrope + rope_off(head, j)) = pr;
+            }
+            ptx::fence_proxy_async_smem();
             tmem_wait_st();
             ptx::tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&bar.q_full);
         }
         const float cscale = scale * kLog2e;
-        const uint32_t x_peer = map_to_rank(ptx::smem_addr(xs), peer) + head * 16;
-        const uint32_t xf_peer = map_to_rank(ptx::smem_addr(&bar.x_full), peer);
-        const uint32_t xfree_peer = map_to_rank(ptx::smem_addr(&bar.x_free), peer);
-        const uint32_t xsink_peer = map_to_rank(ptx::smem_addr(&bar.x_sink[warp]), peer);
+        // the peer's x[b] for this thread's 32 scores: [b][kh][8 quads][128 heads][4]
+        const uint32_t x_peer0 = map_to_rank(ptx::smem_addr(xs), peer) + (kh * 8 * kHeadsPerCta + head) * 16;
         float m_run = -INFINITY, l_run = 0.0f;
-        for (int t = 0; t < ntiles; ++t) {
-            const int s = t % kKvStages;
-            const int pb = t & 1;
-            if (threadIdx.x == 0) ptx::mbar_arrive_expect_tx(&bar.x_full, kXBytes);   // the peer's tile-t scores
-            if (!ptx::mbar_wait(&bar.s_full, t & 1, deadline)) { timed_out = true; break; }
-            if (!ptx::mbar_wait(&bar.kv_full[s], (t / kKvStages) & 1, deadline)) { timed_out = true; break; }
+        // Tile u's partial scores: wait for its score MMAs, read this warp's 32 columns, send them to
+        // the peer's x[u & 1] (once the peer has read what this CTA sent there for tile u - 2).  Tile
+        // t + 1 is fetched and sent right after P(t), so its transfer overlaps the peer finishing
+        // tile t and this warp's next receive finds the data there.
+        uint32_t sr[32];
+        auto fetch_send = [&](int u) -> bool {
+            const int su = u % kKvStages;
+            const int bu = u & 1;
+            const uint32_t pu = (u >> 1) & 1;
+            if (threadIdx.x == 0) ptx::mbar_arrive_expect_tx(&bar.x_full[bu], kXBytes);   // the peer's tile-u scores
+            if (!ptx::mbar_wait(&bar.s_full[bu], pu, deadline)) return false;
+            // the stage's tile landed (orders the producers' valid-bit words before they are read)
+            if (!ptx::mbar_wait(&bar.kv_full[su], (u / kKvStages) & 1, deadline)) return false;
             ptx::tc_fence_after_sync();
-            uint32_t sr[64];
-            ptx::tmem_ld_32x32b_x32(tmem + lane_base + kTmemS, *reinterpret_cast<uint32_t(*)[32]>(sr));
-            ptx::tmem_ld_32x32b_x32(tmem + lane_base + kTmemS + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+            ptx::tmem_ld_32x32b_x32(tmem + lane_base + kTmemS + bu * kKeysPerTile + kh * 32, sr);
             ptx::tmem_wait_ld();
-            ptx::tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&bar.s_empty);
-            // our tile-t scores go to the peer's x once it consumed our tile t-1 ones
-            if (t > 0 && !ptx::mbar_wait(&bar.x_free, (t - 1) & 1, deadline)) { timed_out = true; break; }
-            // arm the next phase (the peer's 4 consumed signals of tile t) only after phase t-1 completed
-            if (threadIdx.x == 0) ptx::mbar_arrive_expect_tx(&bar.x_free, 16);
+            if (u >= 2 && !ptx::mbar_wait(&bar.x_free[bu], pu ^ 1u, deadline)) return false;
+            // arm the next phase (the peer's consumed signals of tile u) after the previous one completed
+            if (threadIdx.x == 0) ptx::mbar_arrive_expect_tx(&bar.x_free[bu], kSoftmaxWarps * 4);
+            const uint32_t xp = x_peer0 + bu * kXBytes;
+            const uint32_t xf_peer = map_to_rank(ptx::smem_addr(&bar.x_full[bu]), peer);
 #pragma unroll
-            for (int kq = 0; kq < 16; ++kq)
-                st_async_v4(x_peer + kq * (kHeadsPerCta * 16), __uint_as_float(sr[4 * kq]), __uint_as_float(sr[4 * kq + 1]),
+            for (int kq = 0; kq < 8; ++kq)
+                st_async_v4(xp + kq * (kHeadsPerCta * 16), __uint_as_float(sr[4 * kq]), __uint_as_float(sr[4 * kq + 1]),
                             __uint_as_float(sr[4 * kq + 2]), __uint_as_float(sr[4 * kq + 3]), xf_peer);
-            if (!ptx::mbar_wait(&bar.x_full, t & 1, deadline)) { timed_out = true; break; }
-            const float* xr = xs;
+            return true;
+        };
+        if (ntiles > 0 && !fetch_send(0)) timed_out = true;
+        for (int t = 0; t < ntiles && !timed_out; ++t) {
+            const int s = t % kKvStages;
+            const int bb = t & 1;
+            const uint32_t ph = (t >> 1) & 1;
+            if (!ptx::mbar_wait(&bar.x_full[bb], ph, deadline)) { timed_out = true; break; }
+            {
+                const float* xr = xs + bb * (kXBytes / 4) + (kh * 8 * kHeadsPerCta + head) * 4;
 #pragma unroll
-            for (int kq = 0; kq < 16; ++kq) {
-                const float4 o = *reinterpret_cast<const float4*>(xr + kq * (kHeadsPerCta * 4) + head * 4);
-                sr[4 * kq + 0] = __float_as_uint(__uint_as_float(sr[4 * kq + 0]) + o.x);
-                sr[4 * kq + 1] = __float_as_uint(__uint_as_float(sr[4 * kq + 1]) + o.y);
-                sr[4 * kq + 2] = __float_as_uint(__uint_as_float(sr[4 * kq + 2]) + o.z);
-                sr[4 * kq + 3] = __float_as_uint(__uint_as_float(sr[4 * kq + 3]) + o.w);
+                for (int kq = 0; kq < 8; ++kq) {
+                    const float4 o = *reinterpret_cast<const float4*>(xr + kq * (kHeadsPerCta * 4));
+                    sr[4 * kq + 0] = __float_as_uint(__uint_as_float(sr[4 * kq + 0]) + o.x);
+                    sr[4 * kq + 1] = __float_as_uint(__uint_as_float(sr[4 * kq + 1]) + o.y);
+                    sr[4 * kq + 2] = __float_as_uint(__uint_as_float(sr[4 * kq + 2]) + o.z);
+                    sr[4 * kq + 3] = __float_as_uint(__uint_as_float(sr[4 * kq + 3]) + o.w);
+                }
             }
             __syncwarp();   // every lane's reads of x have returned (their values are in sr)
-            if (lane == 0) st_async_b32(xsink_peer, 1u, xfree_peer);
-            const uint64_t vbits = static_cast<uint64_t>(bar.valid[s][0]) | (static_cast<uint64_t>(bar.valid[s][1]) << 16) |
-                                   (static_cast<uint64_t>(bar.valid[s][2]) << 32) |
-                                   (static_cast<uint64_t>(bar.valid[s][3]) << 48);
+            if (lane == 0)
+                st_async_b32(map_to_rank(ptx::smem_addr(&bar.x_sink[bb][warp]), peer), 1u,
+                             map_to_rank(ptx::smem_addr(&bar.x_free[bb]), peer));
+            const uint32_t vbits = bar.valid[s][2 * kh] | (bar.valid[s][2 * kh + 1] << 16);
             float tmax = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
+            for (int i = 0; i < 32; ++i) {
                 const float sv = ((vbits >> i) & 1u) ? __uint_as_float(sr[i]) * cscale : -INFINITY;
                 sr[i] = __float_as_uint(sv);
                 tmax = fmaxf(tmax, sv);
             }
+            // the tile maximum of this head over all 64 keys: shared with the other key half's warp
+            // (phase t of the pair barrier; the values double-buffered by tile parity, so a value is
+            // overwritten only after the partner has passed the next phase, i.e. has read it)
+            bar.tmax[bb][kh][head] = tmax;
+            ptx::mbar_arrive(&bar.pair[quad]);
+            if (!ptx::mbar_wait(&bar.pair[quad], t & 1, deadline)) { timed_out = true; break; }
+            tmax = fmaxf(tmax, bar.tmax[bb][kh ^ 1][head]);
             // lazy rescale: move the reference max only when the tile max exceeds it by > 8
             const bool grow = tmax > m_run + kRescaleThreshold || (m_run == -INFINITY && tmax > -INFINITY);
             const float m_new = grow ? tmax : m_run;
             const float alpha = grow ? ((m_run == -INFINITY) ? 0.0f : exp2f(m_run - m_new)) : 1.0f;
-            // this P buffer is free once PV(t-2) has completed
-            if (!ptx::mbar_wait(&bar.p_empty[pb], ((t >> 1) & 1) ^ 1u, deadline)) { timed_out = true; break; }
             if (t > 0 && __any_sync(0xffffffffu, grow)) {
-                // O may only be rescaled once PV(t-1) has completed
-                if (!ptx::mbar_wait(&bar.p_empty[pb ^ 1], ((t - 1) >> 1) & 1, deadline)) { timed_out = true; break; }
+                // O may only be rescaled once PV(t-1) has completed; this warp rescales its 128 columns
+                if (!ptx::mbar_wait(&bar.s_free[(t - 1) & 1], ((t - 1) >> 1) & 1, deadline)) { timed_out = true; break; }
                 ptx::tc_fence_after_sync();
 #pragma unroll 1
-                for (int cc = 0; cc < kHalfDims; cc += 32) {
+                for (int cc = kh * 128; cc < kh * 128 + 128; cc += 32) {
                     uint32_t o[32];
                     ptx::tmem_ld_32x32b_x32(tmem + lane_base + cc, o);
                     ptx::tmem_wait_ld();
@@ -485,40 +539,46 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
             l_run *= alpha;
             m_run = m_new;
             float psum = 0.0f;
-            uint32_t pk[32];
+            uint32_t pk[16];
             const bool any = m_run != -INFINITY;
 #pragma unroll
-            for (int i = 0; i < 64; i += 2) {
+            for (int i = 0; i < 32; i += 2) {
                 const float p0 = any ? fast_exp2(__uint_as_float(sr[i]) - m_run) : 0.0f;
                 const float p1 = any ? fast_exp2(__uint_as_float(sr[i + 1]) - m_run) : 0.0f;
                 psum += p0 + p1;
                 pk[i / 2] = pack_bf16x2(p0, p1);
             }
             l_run += psum;
-            // P row of this head: 8 core matrices (8 keys x 16 B each) along K, 128 B apart
-            unsigned char* prow = ps + pb * kPBytes + (head >> 3) * 1024 + (head & 7) * 16;
-#pragma unroll
-            for (int kg = 0; kg < 8; ++kg)
-                *reinterpret_cast<uint4*>(prow + kg * 128) = make_uint4(pk[4 * kg], pk[4 * kg + 1], pk[4 * kg + 2], pk[4 * kg + 3]);
-            ptx::fence_proxy_async_smem();
+            // P of keys 32 kh .. +31 over columns 16 kh .. +15 of this tile's score buffer (both
+            // warps of the pair read their scores before the pair barrier above)
+            tmem_st_32x32b_x16(tmem + lane_base + kTmemS + bb * kKeysPerTile + kh * 16, pk);
+            tmem_wait_st();
             ptx::tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&bar.p_full[pb]);
+            if (lane == 0) ptx::mbar_arrive(&bar.p_full[bb]);
+            if (t + 1 < ntiles && !fetch_send(t + 1)) { timed_out = true; break; }
         }
         // the peer's last consumed signals land here before this CTA may finish
-        if (ntiles > 0 && !timed_out && !ptx::mbar_wait(&bar.x_free, (ntiles - 1) & 1, deadline)) timed_out = true;
+        if (!timed_out) {
+            for (int t = (ntiles >= 2 ? ntiles - 2 : 0); t < ntiles; ++t)
+                if (!ptx::mbar_wait(&bar.x_free[t & 1], (t >> 1) & 1, deadline)) { timed_out = true; break; }
+        }
         // ---------------- epilogue: O / l, lse
+        bar.lsum[kh][head] = l_run;
+        ptx::mbar_arrive(&bar.pair[quad]);
+        if (!timed_out && !ptx::mbar_wait(&bar.pair[quad], ntiles & 1, deadline)) timed_out = true;
+        const float l_tot = l_run + bar.lsum[kh ^ 1][head];
         bool have_o = ntiles > 0 && !timed_out;
         if (have_o && !ptx::mbar_wait(&bar.o_full, 0, deadline)) { timed_out = true; have_o = false; }
         ptx::tc_fence_after_sync();
-        const float inv_l = l_run > 0.0f ? 1.0f / l_run : 0.0f;
-        const float lse = l_run > 0.0f ? (m_run + log2f(l_run)) / kLog2e : -INFINITY;
+        const float inv_l = l_tot > 0.0f ? 1.0f / l_tot : 0.0f;
+        const float lse = l_tot > 0.0f ? (m_run + log2f(l_tot)) / kLog2e : -INFINITY;
         const bool write_head = head < H;
         const int64_t rh = static_cast<int64_t>(r) * H + head;
         if (splits == 1) {
             uint16_t* dst = out + rh * kValueDim + half * kHalfDims;
 #pragma unroll 1
-            for (int cc = 0; cc < kHalfDims; cc += 32) {
+            for (int cc = kh * 128; cc < kh * 128 + 128; cc += 32) {
                 uint32_t o[32];
                 if (have_o) {
                     ptx::tmem_ld_32x32b_x32(tmem + lane_base + cc, o);
@@ -539,11 +599,11 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
                     }
                 }
             }
-            if (write_head && half == 0 && lse_out != nullptr) lse_out[rh] = lse;
+            if (write_head && half == 0 && kh == 0 && lse_out != nullptr) lse_out[rh] = lse;
         } else {
             float* dst = part_o + (rh * splits + split) * kValueDim + half * kHalfDims;
 #pragma unroll 1
-            for (int cc = 0; cc < kHalfDims; cc += 32) {
+            for (int cc = kh * 128; cc < kh * 128 + 128; cc += 32) {
                 uint32_t o[32];
                 if (have_o) {
                     ptx::tmem_ld_32x32b_x32(tmem + lane_base + cc, o);
@@ -560,7 +620,7 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
                                         __uint_as_float(o[i + 2]) * inv_l, __uint_as_float(o[i + 3]) * inv_l);
                 }
             }
-            if (write_head && half == 0) part_lse[rh * splits + split] = lse;
+            if (write_head && half == 0 && kh == 0) part_lse[rh * splits + split] = lse;
         }
     }
     if (timed_out) raise_error(err, DSA_DEVERR_TIMEOUT);
