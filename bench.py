@@ -287,8 +287,10 @@ def workload_config(wl):
             "context_total": int(wl.seq_lens.astype(np.int64).sum()), "q_per_request": int(wl.max_q_len),
             "topk": wl.topk, "mla_heads": wl.heads, "index_heads": 64, "index_dim": 128, "page_size": 64,
             "index_pool_pages": wl.num_pages, "seed": wl.seed,
-            "l2": "flushed between timed steps (256 MiB write, untimed)",
-            "timing": "CUDA events around one CUDA-graph replay of the step per timed iteration"}
+            "l2": "flushed between timed steps (256 MiB write, then 256 MiB read of another buffer; untimed)",
+            "timing": "per timed iteration one replay of a CUDA graph holding the L2 flush, a timing event, "
+                      "the step's kernels and a second timing event (events recorded by the graph, so the "
+                      "graph's launch latency and the flush are outside the measured interval)"}
 
 
 def capture(fn, stream):
@@ -305,6 +307,66 @@ def capture(fn, stream):
         n = capi.launch_count() - n0
     torch.cuda.synchronize()
     return g, n
+
+
+class TimedGraph:
+    """One CUDA graph per measured unit: an L2 flush (a 256 MiB write, then a 256 MiB read so that
+    the written lines are back in HBM), then a timing event, the unit's kernels, a second timing
+    event.  The events are recorded by the graph itself (external event nodes), so a replay's
+    elapsed time is the device time of the kernels alone: neither the flush nor the graph's launch
+    latency is inside it.  Where torch cannot record events inside a graph, the events are recorded
+    around the replay instead (launch latency then included)."""
+
+    _read = None   # the flush's read buffer, shared by every instance
+
+    def __init__(self, fn, stream, flush):
+        import torch
+        from deepseek_sparse_attention_paged_gb300 import capi
+        self.stream, self.flush = stream, flush
+        # a second buffer read after the flush write: the write's dirty lines are written back to HBM
+        # before the timed interval starts instead of during it
+        if TimedGraph._read is None or TimedGraph._read.numel() != flush.numel():
+            TimedGraph._read = torch.ones_like(flush)
+        self.flush_read = TimedGraph._read
+        try:
+            self.a = torch.cuda.Event(enable_timing=True, external=True)
+            self.b = torch.cuda.Event(enable_timing=True, external=True)
+            self.inside = True
+        except TypeError:
+            self.a = torch.cuda.Event(enable_timing=True)
+            self.b = torch.cuda.Event(enable_timing=True)
+            self.inside = False
+        self.g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            fn()  # warm the path outside capture
+            torch.cuda.synchronize()
+            n0 = capi.launch_count()
+            with torch.cuda.graph(self.g, stream=stream):
+                if self.inside:
+                    flush.fill_(1.0)
+                    self.sink = self.flush_read.amax()
+                    self.a.record(stream)
+                fn()
+                if self.inside:
+                    self.b.record(stream)
+            self.kernels = capi.launch_count() - n0
+        torch.cuda.synchronize()
+
+    def time(self, iters):
+        """Per-replay device time (ms) of the unit's kernels, L2 flushed before each."""
+        import torch
+        out = []
+        with torch.cuda.stream(self.stream):
+            for _ in range(iters):
+                if not self.inside:
+                    self.flush.fill_(1.0)
+                    self.a.record(self.stream)
+                self.g.replay()
+                if not self.inside:
+                    self.b.record(self.stream)
+                self.b.synchronize()
+                out.append(self.a.elapsed_time(self.b))
+        return out
 
 
 def time_graph(g, stream, iters, flush):
@@ -350,12 +412,13 @@ def run_gpu(args):
     stream = torch.cuda.Stream()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
 
-    step_graph, step_kernels = capture(lambda: db.step(), stream)
+    step_graph = TimedGraph(lambda: db.step(), stream, flush)
+    step_kernels = step_graph.kernels
     stage_graphs = {
-        "store": capture(lambda: db.store_new_keys(), stream),
-        "indexer": capture(lambda: db.indexer_stage(), stream),
-        "topk": capture(lambda: db.topk_stage(), stream),
-        "mla": capture(lambda: db.sparse_mla(), stream),
+        "store": TimedGraph(lambda: db.store_new_keys(), stream, flush),
+        "indexer": TimedGraph(lambda: db.indexer_stage(), stream, flush),
+        "topk": TimedGraph(lambda: db.topk_stage(), stream, flush),
+        "mla": TimedGraph(lambda: db.sparse_mla(), stream, flush),
     }
     st, word = db.device_error()
     if st != 0:
@@ -364,12 +427,12 @@ def run_gpu(args):
     clk = ClockSampler(local).__enter__()   # samples from warm-up through the e2e run
     clk.wait_first_sample()
     # warm-up steps (untimed)
-    time_graph(step_graph, stream, args.warmup, flush)
+    step_graph.time(args.warmup)
     if pg is not None:
         pg.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.perf_counter()
-    step_ms = time_graph(step_graph, stream, args.steps, flush)
+    step_ms = step_graph.time(args.steps)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
     if pg is not None:
@@ -377,7 +440,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
     # stage breakdown (each stage alone in its own graph, same flush discipline), outside the K steps
     stage_iters = max(3, args.steps // 2)
-    stage_ms = {k: time_graph(g, stream, stage_iters, flush) for k, (g, _) in stage_graphs.items()}
+    stage_ms = {k: g.time(stage_iters) for k, g in stage_graphs.items()}
     timed_launches = step_kernels * args.steps
     mean_step = D.max_over_ranks(sum(step_ms) / len(step_ms), device=torch.device("cuda", local))
     value = D.aggregate_rate(wl.T, world, mean_step)
@@ -473,8 +536,8 @@ def run_prologues(wl, stream, flush, iters):
         slots = torch.randperm(pages * 64, generator=g)[:n].cuda()
         pool = torch.zeros(pages, capi.INDEX_PAGE_BYTES, dtype=torch.uint8, device="cuda")
         pos = positions.cuda()
-        gr, _ = capture(lambda: capi.dsa_store_index_k_prologue(k, w, b, 1e-6, cos_sin, pos, slots, pool), stream)
-        ms = sum(time_graph(gr, stream, iters, flush)) / iters
+        tg = TimedGraph(lambda: capi.dsa_store_index_k_prologue(k, w, b, 1e-6, cos_sin, pos, slots, pool), stream, flush)
+        ms = sum(tg.time(iters)) / iters
         by = n * (256 + 256 + 16 + 132)
         return {"tokens": n, "us": ms * 1e3, "algorithmic_bytes": by, "gbs": by / (ms * 1e-3) / 1e9}
 
@@ -482,8 +545,8 @@ def run_prologues(wl, stream, flush, iters):
         q = torch.randn(T, 64, 128, generator=g).to(torch.bfloat16).cuda()
         qo = torch.empty_like(q)
         pos = torch.randint(0, max_pos, (T,), generator=g).cuda()
-        gr, _ = capture(lambda: capi.dsa_indexer_rope_q(q, cos_sin, pos, qo), stream)
-        ms = sum(time_graph(gr, stream, iters, flush)) / iters
+        tg = TimedGraph(lambda: capi.dsa_indexer_rope_q(q, cos_sin, pos, qo), stream, flush)
+        ms = sum(tg.time(iters)) / iters
         by = T * (64 * 256 * 2 + 256 + 8)
         return {"rows": T, "us": ms * 1e3, "algorithmic_bytes": by, "gbs": by / (ms * 1e-3) / 1e9}
 
@@ -519,8 +582,8 @@ def run_projections(stream, flush, iters, heads=128):
                               wbytes + T * heads * (128 + 512) * 2),
                              ("v_up", lambda: capi.dsa_mla_v_up(o, w_uv, y.view(T, heads, 128)),
                               wbytes + T * heads * (512 + 128) * 2)):
-            gr, _ = capture(fn, stream)
-            ms = sum(time_graph(gr, stream, iters, flush)) / iters
+            tg = TimedGraph(fn, stream, flush)
+            ms = sum(tg.time(iters)) / iters
             out[f"{name}_T{T}"] = {"rows": T, "heads": heads, "us": ms * 1e3, "algorithmic_bytes": by, "flops": flop,
                                    "gbs": by / (ms * 1e-3) / 1e9, "tflops": flop / (ms * 1e-3) / 1e12}
     return out
