@@ -185,7 +185,7 @@ STAGE_SOURCES = {"store": ["store_index_k.cu"], "indexer": ["indexer_logits.cu"]
                  "mla": ["sparse_mla.cu"]}
 # tensor peak of each stage relative to the measured dense bf16 peak: the indexer contracts FP8
 # operands (nominal dense FP8 : BF16 = 4.5 : 2.25 PFLOP/s), the attention bf16
-STAGE_TENSOR_PEAK_RATIO = {"indexer": 2.0, "mla": 1.0}
+STAGE_TENSOR_PEAK_RATIO = {"indexer": 2.0, "select": 2.0, "mla": 1.0}
 
 
 # ----------------------------------------------------------------------------- CPU oracle arm
@@ -418,6 +418,7 @@ def run_gpu(args):
         "store": TimedGraph(lambda: db.store_new_keys(), stream, flush),
         "indexer": TimedGraph(lambda: db.indexer_stage(), stream, flush),
         "topk": TimedGraph(lambda: db.topk_stage(), stream, flush),
+        "select": TimedGraph(lambda: db.select(), stream, flush),
         "mla": TimedGraph(lambda: db.sparse_mla(), stream, flush),
     }
     st, word = db.device_error()
@@ -455,6 +456,7 @@ def run_gpu(args):
         return
     hbm, bf16, peak_kind = measured_peaks()
     work = algorithmic_work(wl)
+    work["select"] = tuple(a + b for a, b in zip(work["indexer"], work["topk"]))
     stages = {}
     for k, ms_list in stage_ms.items():
         ms = sum(ms_list) / len(ms_list)

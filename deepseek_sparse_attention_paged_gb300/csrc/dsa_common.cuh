@@ -72,4 +72,18 @@ inline dsa_status launch_status() {
     return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
+// Internal launchers shared by the one-call indexer: the logits call and the top-k call, each with
+// an optional per-row 4096-bin histogram of the top 12 bits of the logits' order keys (written by
+// the logits kernel into zeroed memory, read by the top-k kernels instead of a first pass).
+constexpr int kHistBins = 4096;
+dsa_status indexer_logits_launch(const void* q_bf16, const float* weights, const uint8_t* index_k_pool,
+                                 int64_t num_pages, const int32_t* block_table, int32_t max_pages,
+                                 const int32_t* seq_lens, const int32_t* cu_q, int32_t B, int32_t max_seq_len,
+                                 int32_t max_q_len, int32_t row_begin, int32_t row_end, float* logits, int64_t ld,
+                                 uint32_t flags, void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream,
+                                 uint32_t* hist_g);
+dsa_status topk_launch(const float* logits, int64_t ld, const int32_t* seq_lens, const int32_t* cu_q, int32_t B,
+                       int32_t max_seq_len, int32_t row_begin, int32_t row_end, int32_t k, int32_t n_init,
+                       int32_t n_local, int32_t* idx, void* stream, const uint32_t* hist_g);
+
 }  // namespace dsa

@@ -75,6 +75,17 @@ __device__ __forceinline__ uint32_t quantise_head(float x[4], bool rotate, bool 
     return packed;
 }
 
+// Per-row histogram of the top 12 bits of each logit's order key (HIST variant, for the fused
+// indexer + top-k): the key maps larger floats to larger unsigned values, -0 and +0 to one key and
+// NaN to the smallest key -- the mapping the top-k kernels select on.
+constexpr int kTopBins = 4096;
+__device__ __forceinline__ uint32_t logit_order_key(float f) {
+    uint32_t u = __float_as_uint(f);
+    if ((u & 0x7fffffffu) > 0x7f800000u) return 0u;
+    if (u == 0x80000000u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 constexpr int kTileKeys = 128;
 constexpr int kTileCodeBytes = kTileKeys * kIndexDim;    // 16 KB: two pages of codes
 constexpr int kQRowBytes = kIndexHeads * kIndexDim;       // 8 KB of codes per query row
@@ -191,10 +202,12 @@ __device__ __forceinline__ int64_t epi_scan(int64_t v, int64_t* scratch, int64_t
 // two epilogue warpgroups taking alternate tiles (warp w reads TMEM lanes 32 (w % 4) .. +31, one
 // key per thread: ReLU, gates w', head sum, key scale, store), warp 10 = query-tile loader.
 // ---------------------------------------------------------------------------------------------
-template <int R>
+template <int R, bool HIST = false>
 struct IdxCfg {
+    static_assert(!HIST || R <= 2, "the per-row histograms fit shared memory for row groups of up to 2 rows");
     static constexpr int N = 64 * R;
-    static constexpr int kStages = (R == 1) ? 12 : (R == 2 ? 11 : 9);
+    // with HIST, the R 16 KB histograms take the place of R (or, for R = 2, two) key stages
+    static constexpr int kStages = (R == 1) ? (HIST ? 11 : 12) : (R == 2 ? (HIST ? 9 : 11) : 9);
     static constexpr int kAcc = (R == 4) ? 2 : 4;                 // accumulators of N columns
     static constexpr uint32_t kTmemCols = kAcc * N;               // 256 / 512 / 512
     static constexpr int kQBytes = R * kQRowBytes;
@@ -203,20 +216,24 @@ struct IdxCfg {
     static constexpr size_t kScalesOff = kQOff + 2 * size_t(kQBytes);
     static constexpr size_t kGatesOff = kScalesOff + size_t(kStages) * kTileKeys * 4;
     static constexpr size_t kBarOff = kGatesOff + 2 * size_t(R) * kQGateBytes;
-    static constexpr int kBars = 2 * kStages + 2 * kAcc + 4;
+    static constexpr int kBars = 2 * kStages + 2 * kAcc + 4 + 1;   // + the epilogue warps' histogram barrier
     static constexpr size_t kMiscOff = kBarOff + size_t(kBars) * 8;   // tmem slot, partition, scan
     static constexpr size_t kPageOkOff = kMiscOff + 16 + 8 * 8;
-    static constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kPageOkOff + 2 * kStages;
+    static constexpr size_t kHistOff = (kPageOkOff + 2 * kStages + 15) / 16 * 16;
+    static constexpr size_t kHistBytes = HIST ? size_t(R) * kTopBins * 4 : 0;
+    static constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kHistOff + kHistBytes;
+    static_assert(kSmemBytes <= 232448, "shared-memory budget");
 };
 
-template <int R>
+template <int R, bool HIST>
 __global__ void __launch_bounds__(kThreads, 1)
 indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8_t* __restrict__ q_codes,
                            const float* __restrict__ q_gates, const uint8_t* __restrict__ pool, int64_t num_pages,
                            const int32_t* __restrict__ block_table, int max_pages,
                            const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q, int B, int G,
-                           int row_begin, int row_end, float* __restrict__ logits, int64_t ld, int32_t* err) {
-    using C = IdxCfg<R>;
+                           int row_begin, int row_end, float* __restrict__ logits, int64_t ld, int32_t* err,
+                           uint32_t* __restrict__ hist_g) {
+    using C = IdxCfg<R, HIST>;
     constexpr int S = C::kStages;
     constexpr int N = C::N;
     constexpr int NA = C::kAcc;
@@ -233,10 +250,12 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
     uint64_t* tempty = tfull + NA;
     uint64_t* qfull = tempty + NA;     // [2]
     uint64_t* qempty = qfull + 2;      // [2]
+    uint64_t* hsync = qempty + 2;      // HIST: the 8 epilogue warps meet before / after a histogram flush
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + C::kMiscOff);
     int32_t* part = reinterpret_cast<int32_t*>(base + C::kMiscOff + 4);      // start segment, tile, count
     int64_t* scan_scratch = reinterpret_cast<int64_t*>(base + C::kMiscOff + 16);
     uint8_t* page_ok = base + C::kPageOkOff;                                  // [S][2]
+    uint32_t* hist_s = reinterpret_cast<uint32_t*>(base + C::kHistOff);       // HIST: [R][4096]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const SegArgs sa{seq_lens, cu_q, B, G, R, row_begin, row_end};
@@ -256,6 +275,7 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
             ptx::mbar_init(&qfull[b2], 1);
             ptx::mbar_init(&qempty[b2], 1 + 8);  // MMA commit + every epilogue warp
         }
+        ptx::mbar_init(hsync, 8);
         ptx::fence_barrier_init();
     }
     if (warp == 1) {
@@ -311,6 +331,8 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
             }
         }
     }
+    if (HIST && warp >= kEpiWarp0 && warp < kEpiWarp0 + 8)
+        for (int i = threadIdx.x - kEpiWarp0 * 32; i < R * kTopBins; i += 256) hist_s[i] = 0u;
     ptx::tc_fence_before_sync();
     __syncthreads();
     ptx::tc_fence_after_sync();
@@ -433,6 +455,7 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
         }
     } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 8 && count > 0) {   // ---------------- epilogue
         const int grp = (warp - kEpiWarp0) >> 2;          // takes the tiles i with i % 2 == grp
+        uint32_t hph = 0;                                  // HIST: next phase of hsync
         const int quad = warp & 3;
         const int key_in_tile = quad * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
@@ -467,8 +490,17 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
                     for (int h = 0; h < 32; ++h) acc = fmaf(g[32 + h], fmaxf(__uint_as_float(r1[h]), 0.0f), acc);
                     const int r = sg.q0 + sg.j0 + jj;
                     const int v = visible_len(sg.L, sg.q_len, sg.j0 + jj);
-                    if (ok && key < v && key < ld && r >= row_begin && r < row_end)
+                    if (HIST) {
+                        // every visible key gets a logit (-inf where its page id was bad) and is
+                        // counted, so the histogram describes exactly the row the top-k reads
+                        if (key < v && key < ld && r >= row_begin && r < row_end) {
+                            const float val = ok ? acc * ks : -INFINITY;
+                            logits[static_cast<int64_t>(r - row_begin) * ld + key] = val;
+                            atomicAdd(&hist_s[jj * kTopBins + (logit_order_key(val) >> 20)], 1u);
+                        }
+                    } else if (ok && key < v && key < ld && r >= row_begin && r < row_end) {
                         logits[static_cast<int64_t>(r - row_begin) * ld + key] = acc * ks;
+                    }
                 }
                 ptx::tc_fence_before_sync();
                 __syncwarp();
@@ -479,6 +511,31 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
             }
             if (++s == S) { s = 0; ph ^= 1u; }
             if (++sg.tile == sg.ntiles || i + 1 == count) {   // leaving the segment: its gates are free
+                if (HIST) {
+                    // every epilogue warp's counts of this segment are in; add the non-empty bins to
+                    // the rows' global histograms and clear them for the next segment
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(hsync);
+                    if (!ptx::mbar_wait(hsync, hph, deadline)) { timed_out = true; break; }
+                    hph ^= 1u;
+                    const int t = threadIdx.x - kEpiWarp0 * 32;
+                    for (int jj = 0; jj < sg.nrows; ++jj) {
+                        const int r = sg.q0 + sg.j0 + jj;
+                        const bool live = r >= row_begin && r < row_end;
+                        uint32_t* hg = hist_g + static_cast<int64_t>(r - row_begin) * kTopBins;
+                        for (int bin = t; bin < kTopBins; bin += 256) {
+                            const uint32_t c = hist_s[jj * kTopBins + bin];
+                            if (c != 0u) {
+                                if (live) atomicAdd(hg + bin, c);
+                                hist_s[jj * kTopBins + bin] = 0u;
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(hsync);
+                    if (!ptx::mbar_wait(hsync, hph, deadline)) { timed_out = true; break; }
+                    hph ^= 1u;
+                }
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&qempty[qb]);
                 ++n;
@@ -518,13 +575,16 @@ extern "C" size_t dsa_indexer_logits_workspace_size(int32_t rows) {
     return rows <= 0 ? 0 : static_cast<size_t>(rows) * (kQRowBytes + kQGateBytes);
 }
 
-extern "C" dsa_status dsa_indexer_logits(const void* q_bf16, const float* weights, const uint8_t* index_k_pool,
-                                         int64_t num_pages, const int32_t* block_table, int32_t max_pages,
-                                         const int32_t* seq_lens, const int32_t* cu_q, int32_t B,
-                                         int32_t max_seq_len, int32_t max_q_len, int32_t row_begin,
-                                         int32_t row_end, float* logits, int64_t ld, uint32_t flags,
-                                         void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream) {
-    using namespace dsa;
+namespace dsa {
+
+// The logits call; with hist_g != nullptr (row groups of at most 2 rows) the kernel also adds each
+// row's top-12-bit order-key histogram into hist_g[(r - row_begin) * 4096 ..] (zeroed by the caller).
+dsa_status indexer_logits_launch(const void* q_bf16, const float* weights, const uint8_t* index_k_pool,
+                                 int64_t num_pages, const int32_t* block_table, int32_t max_pages,
+                                 const int32_t* seq_lens, const int32_t* cu_q, int32_t B, int32_t max_seq_len,
+                                 int32_t max_q_len, int32_t row_begin, int32_t row_end, float* logits, int64_t ld,
+                                 uint32_t flags, void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream,
+                                 uint32_t* hist_g) {
     if (B < 0 || max_seq_len < 0 || max_q_len < 0 || row_begin < 0 || row_end < row_begin || max_pages < 0 ||
         num_pages < 0)
         return DSA_ERR_INVALID_ARG;
@@ -537,6 +597,7 @@ extern "C" dsa_status dsa_indexer_logits(const void* q_bf16, const float* weight
     if (ld < max_seq_len) return DSA_ERR_INVALID_ARG;
     if (static_cast<int64_t>(max_pages) * kPage < max_seq_len) return DSA_ERR_INVALID_ARG;
     const int R = max_q_len >= 4 ? 4 : (max_q_len >= 2 ? 2 : 1);
+    if (hist_g != nullptr && R > 2) return DSA_ERR_UNSUPPORTED;
     const int groups = (max_q_len + R - 1) / R;
     if (static_cast<int64_t>(groups) * B > 0x7fffffffLL - 1) return DSA_ERR_UNSUPPORTED;
     if (num_pages > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
@@ -587,22 +648,38 @@ extern "C" dsa_status dsa_indexer_logits(const void* q_bf16, const float* weight
     cfg.numAttrs = 1;
     const uint8_t* qc = q_codes;
     const float* qg = q_gates;
-#define DSA_LAUNCH_IDX(RR)                                                                                      \
+#define DSA_LAUNCH_IDX(RR, HH)                                                                                  \
     do {                                                                                                        \
-        const size_t smem = IdxCfg<RR>::kSmemBytes;                                                             \
-        if (cudaFuncSetAttribute(indexer_logits_umma_kernel<RR>, cudaFuncAttributeMaxDynamicSharedMemorySize,    \
+        const size_t smem = IdxCfg<RR, HH>::kSmemBytes;                                                         \
+        if (cudaFuncSetAttribute(indexer_logits_umma_kernel<RR, HH>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                                  static_cast<int>(smem)) != cudaSuccess)                                        \
             return DSA_ERR_CUDA;                                                                                \
         cfg.dynamicSmemBytes = smem;                                                                            \
-        if (cudaLaunchKernelEx(&cfg, indexer_logits_umma_kernel<RR>, kmap, qc, qg, index_k_pool, num_pages,     \
+        if (cudaLaunchKernelEx(&cfg, indexer_logits_umma_kernel<RR, HH>, kmap, qc, qg, index_k_pool, num_pages,  \
                                block_table, static_cast<int>(max_pages), seq_lens, cu_q, static_cast<int>(B),  \
                                groups, static_cast<int>(row_begin), static_cast<int>(row_end), logits, ld,     \
-                               dev_err) != cudaSuccess)                                                         \
+                               dev_err, hist_g) != cudaSuccess)                                                 \
             return DSA_ERR_CUDA;                                                                                \
     } while (0)
-    if (R == 1) DSA_LAUNCH_IDX(1);
-    else if (R == 2) DSA_LAUNCH_IDX(2);
-    else DSA_LAUNCH_IDX(4);
+    if (hist_g != nullptr) {
+        if (R == 1) DSA_LAUNCH_IDX(1, true);
+        else DSA_LAUNCH_IDX(2, true);
+    } else if (R == 1) DSA_LAUNCH_IDX(1, false);
+    else if (R == 2) DSA_LAUNCH_IDX(2, false);
+    else DSA_LAUNCH_IDX(4, false);
 #undef DSA_LAUNCH_IDX
     return launch_status();
+}
+
+}  // namespace dsa
+
+extern "C" dsa_status dsa_indexer_logits(const void* q_bf16, const float* weights, const uint8_t* index_k_pool,
+                                         int64_t num_pages, const int32_t* block_table, int32_t max_pages,
+                                         const int32_t* seq_lens, const int32_t* cu_q, int32_t B,
+                                         int32_t max_seq_len, int32_t max_q_len, int32_t row_begin,
+                                         int32_t row_end, float* logits, int64_t ld, uint32_t flags,
+                                         void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream) {
+    return dsa::indexer_logits_launch(q_bf16, weights, index_k_pool, num_pages, block_table, max_pages, seq_lens,
+                                      cu_q, B, max_seq_len, max_q_len, row_begin, row_end, logits, ld, flags,
+                                      workspace, ws_bytes, dev_err, stream, nullptr);
 }

@@ -256,11 +256,32 @@ __device__ void select_bin(uint32_t* hist, BitmapSmem& sm, int bins, uint32_t ne
     __syncthreads();
 }
 
+// The row's top-12-bit histogram produced by the logits kernel (fused indexer + top-k) into
+// hist[0, 4096): counts of the order keys of every visible logit of the row.  Positions forced to
+// +inf leave their own bin for the +inf bin (the same mapping the key visits apply).
 template <bool FORCED>
+__device__ void load_row_histogram(uint32_t* hist, const uint32_t* __restrict__ hist_row, const float* __restrict__ row,
+                                   const Forced<FORCED>& Fg, int v) {
+    for (int i = threadIdx.x; i < kTopBins; i += kTopkThreads) hist[i] = __ldg(hist_row + i);
+    __syncthreads();
+    if (FORCED) {
+        const int n1 = Fg.init_end;                    // [0, init_end)
+        const int s2 = max(Fg.local_begin, Fg.init_end);   // [s2, v), not counted twice
+        const int nf = n1 + (v - s2);
+        for (int t = threadIdx.x; t < nf; t += kTopkThreads) {
+            const int s = t < n1 ? t : s2 + (t - n1);
+            atomicSub(&hist[order_key(__ldg(row + s)) >> 20], 1u);
+            atomicAdd(&hist[0xFF800000u >> 20], 1u);
+        }
+        __syncthreads();
+    }
+}
+
+template <bool FORCED, bool PREHIST>
 __global__ void __launch_bounds__(kTopkThreads)
 topk_bitmap_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* __restrict__ seq_lens,
                    const int32_t* __restrict__ cu_q, int B, int row_begin, int k, int n_init, int n_local, int32_t* __restrict__ idx,
-                   int words_cap) {
+                   int words_cap, const uint32_t* __restrict__ hist_g) {
     extern __shared__ __align__(16) unsigned char dsm[];
     BitmapSmem& sm = *reinterpret_cast<BitmapSmem*>(dsm);
     uint32_t* sel = reinterpret_cast<uint32_t*>(dsm + sizeof(BitmapSmem));   // key > k-th: kept
@@ -311,11 +332,15 @@ topk_bitmap_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* 
         for (int s = 4 * v4 + threadIdx.x; s < v; s += kTopkThreads) fn(s, F(s, order_key(__ldg(row + s))));
     };
 
-    // ---- read 1: top-12-bit histogram
-    for (int i = threadIdx.x; i < kTopBins; i += kTopkThreads) sm.hist[i] = 0;
-    __syncthreads();
-    for_each_key([&](int, uint32_t key) { atomicAdd(&sm.hist[key >> 20], 1u); });
-    __syncthreads();
+    // ---- read 1: top-12-bit histogram (given by the logits kernel in the fused call)
+    if (PREHIST) {
+        load_row_histogram<FORCED>(sm.hist, hist_g + static_cast<int64_t>(rl) * kTopBins, row, F, v);
+    } else {
+        for (int i = threadIdx.x; i < kTopBins; i += kTopkThreads) sm.hist[i] = 0;
+        __syncthreads();
+        for_each_key([&](int, uint32_t key) { atomicAdd(&sm.hist[key >> 20], 1u); });
+        __syncthreads();
+    }
     select_bin(sm.hist, sm, kTopBins, static_cast<uint32_t>(k));
     const uint32_t b1 = sm.sel_digit;
     uint32_t need = sm.sel_remaining;
@@ -399,11 +424,15 @@ topk_bitmap_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* 
             const int bit = __ffs(bits) - 1;
             bits &= bits - 1;
             const int s = w * 32 + bit;
+            // positions stay below k whenever the selection counts are consistent; the guard keeps
+            // every store inside the row regardless
             if ((sw >> bit) & 1u) {
-                out[gt_before + min(eq_before, take_equal)] = s;
+                const uint32_t p = gt_before + min(eq_before, take_equal);
+                if (p < static_cast<uint32_t>(k)) out[p] = s;
                 ++gt_before;
             } else {
-                if (eq_before < take_equal) out[gt_before + eq_before] = s;
+                const uint32_t p = gt_before + eq_before;
+                if (eq_before < take_equal && p < static_cast<uint32_t>(k)) out[p] = s;
                 ++eq_before;
             }
         }
@@ -455,11 +484,11 @@ __device__ __forceinline__ void sum_with_peer(const uint32_t* hist, uint32_t* to
     __syncthreads();
 }
 
-template <bool FORCED>
+template <bool FORCED, bool PREHIST>
 __global__ void __launch_bounds__(kTopkThreads)
 topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* __restrict__ seq_lens,
                     const int32_t* __restrict__ cu_q, int B, int row_begin, int k, int n_init, int n_local, int32_t* __restrict__ idx,
-                    int words_cap) {
+                    int words_cap, const uint32_t* __restrict__ hist_g) {
     extern __shared__ __align__(16) unsigned char dsm[];
     BitmapSmem& sm = *reinterpret_cast<BitmapSmem*>(dsm);                      // hist: the top digit
     uint32_t* total = reinterpret_cast<uint32_t*>(dsm + sizeof(BitmapSmem));   // summed histogram
@@ -524,10 +553,15 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t*
         for (int s = 4 * v4 + threadIdx.x; s < nloc; s += kTopkThreads) fn(s, F(s, order_key(__ldg(part + s))));
     };
 
-    // ---- read 1: top-12-bit histogram of this half, summed with the peer's
-    for_each_key([&](int, uint32_t key) { atomicAdd(&sm.hist[key >> 20], 1u); });
-    __syncthreads();
-    sum_with_peer(sm.hist, total, kTopBins, peer);
+    // ---- read 1: top-12-bit histogram of this half, summed with the peer's (in the fused call: the
+    // whole row's histogram from the logits kernel, the same in both CTAs)
+    if (PREHIST) {
+        load_row_histogram<FORCED>(total, hist_g + static_cast<int64_t>(rl) * kTopBins, row, Fg, v);
+    } else {
+        for_each_key([&](int, uint32_t key) { atomicAdd(&sm.hist[key >> 20], 1u); });
+        __syncthreads();
+        sum_with_peer(sm.hist, total, kTopBins, peer);
+    }
     select_bin(total, sm, kTopBins, static_cast<uint32_t>(k));
     const uint32_t b1 = sm.sel_digit;
     uint32_t need = sm.sel_remaining;
@@ -619,11 +653,15 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t*
             const int bit = __ffs(bits) - 1;
             bits &= bits - 1;
             const int s = lo + w * 32 + bit;
+            // positions stay below k whenever the selection counts are consistent; the guard keeps
+            // every store inside the row regardless
             if ((sw >> bit) & 1u) {
-                out[gt_before + min(eq_before, take_equal)] = s;
+                const uint32_t p = gt_before + min(eq_before, take_equal);
+                if (p < static_cast<uint32_t>(k)) out[p] = s;
                 ++gt_before;
             } else {
-                if (eq_before < take_equal) out[gt_before + eq_before] = s;
+                const uint32_t p = gt_before + eq_before;
+                if (eq_before < take_equal && p < static_cast<uint32_t>(k)) out[p] = s;
                 ++eq_before;
             }
         }
@@ -648,11 +686,18 @@ extern "C" size_t dsa_topk_workspace_size(int32_t rows, int32_t k, int32_t max_s
     return 0;
 }
 
-extern "C" dsa_status dsa_topk_forced(const float* logits, int64_t ld, const int32_t* seq_lens, const int32_t* cu_q,
-                                      int32_t B, int32_t max_seq_len, int32_t row_begin, int32_t row_end, int32_t k,
-                                      int32_t n_init, int32_t n_local, int32_t* idx, void* workspace,
-                                      size_t workspace_bytes, void* stream) {
-    (void)workspace; (void)workspace_bytes;
+namespace dsa {
+
+template <bool F, bool P>
+void* topk_cluster_fn() { return reinterpret_cast<void*>(topk_cluster_kernel<F, P>); }
+template <bool F, bool P>
+void* topk_bitmap_fn() { return reinterpret_cast<void*>(topk_bitmap_kernel<F, P>); }
+
+// The top-k call; with hist_g != nullptr (the fused indexer + top-k) every row's top-12-bit key
+// histogram comes from hist_g[(r - row_begin) * 4096 ..] instead of a first read of the row.
+dsa_status topk_launch(const float* logits, int64_t ld, const int32_t* seq_lens, const int32_t* cu_q, int32_t B,
+                       int32_t max_seq_len, int32_t row_begin, int32_t row_end, int32_t k, int32_t n_init,
+                       int32_t n_local, int32_t* idx, void* stream, const uint32_t* hist_g) {
     if (k < 1 || k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
     if (n_init < 0 || n_local < 0) return DSA_ERR_INVALID_ARG;
     const bool forced = n_init > 0 || n_local > 0;
@@ -677,13 +722,16 @@ extern "C" dsa_status dsa_topk_forced(const float* logits, int64_t ld, const int
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
         return DSA_ERR_CUDA;
+    const bool pre = hist_g != nullptr;
+    if (pre && words > dsa::kMaxBitmapWords) return DSA_ERR_UNSUPPORTED;
     if (words <= dsa::kMaxBitmapWords && max_seq_len >= 16384 && (row_end - row_begin) <= sms / 2) {
         // long rows, fewer rows than SM pairs: each row on a 2-CTA cluster
         const int half_keys = ((max_seq_len + 1) / 2 + 127) & ~127;
         int words_cap = ((half_keys + 256 + 31) / 32 + 3) & ~3;
         if (words_cap < 32) words_cap = 32;
         const size_t smem = dsa::cluster_smem_bytes(words_cap);
-        auto kern = forced ? dsa::topk_cluster_kernel<true> : dsa::topk_cluster_kernel<false>;
+        void* kern = forced ? (pre ? topk_cluster_fn<true, true>() : topk_cluster_fn<true, false>())
+                            : (pre ? topk_cluster_fn<false, true>() : topk_cluster_fn<false, false>());
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
             cudaSuccess)
             return DSA_ERR_CUDA;
@@ -697,22 +745,23 @@ extern "C" dsa_status dsa_topk_forced(const float* logits, int64_t ld, const int
         cfg.attrs = cattr;
         cfg.numAttrs = 2;
         cfg.dynamicSmemBytes = smem;
-        if (cudaLaunchKernelEx(&cfg, kern, logits, ld, seq_lens, cu_q, static_cast<int>(B),
-                               static_cast<int>(row_begin), static_cast<int>(k), n_init, n_local, idx, words_cap) !=
-                                   cudaSuccess)
-            return DSA_ERR_CUDA;
+        int a_B = B, a_rb = row_begin, a_k = k, a_ni = n_init, a_nl = n_local, a_wc = words_cap;
+        void* args[] = {const_cast<float**>(&logits), &ld, const_cast<int32_t**>(&seq_lens), const_cast<int32_t**>(&cu_q),
+                        &a_B, &a_rb, &a_k, &a_ni, &a_nl, &idx, &a_wc, const_cast<uint32_t**>(&hist_g)};
+        if (cudaLaunchKernelExC(&cfg, kern, args) != cudaSuccess) return DSA_ERR_CUDA;
     } else if (words <= dsa::kMaxBitmapWords) {
         const int words_cap = words < 32 ? 32 : words;
         const size_t smem = dsa::bitmap_smem_bytes(words_cap);
-        auto kern = forced ? dsa::topk_bitmap_kernel<true> : dsa::topk_bitmap_kernel<false>;
+        void* kern = forced ? (pre ? topk_bitmap_fn<true, true>() : topk_bitmap_fn<true, false>())
+                            : (pre ? topk_bitmap_fn<false, true>() : topk_bitmap_fn<false, false>());
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
             cudaSuccess)
             return DSA_ERR_CUDA;
         cfg.dynamicSmemBytes = smem;
-        if (cudaLaunchKernelEx(&cfg, kern, logits, ld, seq_lens, cu_q, static_cast<int>(B),
-                               static_cast<int>(row_begin), static_cast<int>(k), n_init, n_local, idx, words_cap) !=
-                                   cudaSuccess)
-            return DSA_ERR_CUDA;
+        int a_B = B, a_rb = row_begin, a_k = k, a_ni = n_init, a_nl = n_local, a_wc = words_cap;
+        void* args[] = {const_cast<float**>(&logits), &ld, const_cast<int32_t**>(&seq_lens), const_cast<int32_t**>(&cu_q),
+                        &a_B, &a_rb, &a_k, &a_ni, &a_nl, &idx, &a_wc, const_cast<uint32_t**>(&hist_g)};
+        if (cudaLaunchKernelExC(&cfg, kern, args) != cudaSuccess) return DSA_ERR_CUDA;
     } else {
         cfg.dynamicSmemBytes = 0;
         auto kern = forced ? dsa::topk_kernel<true> : dsa::topk_kernel<false>;
@@ -722,6 +771,17 @@ extern "C" dsa_status dsa_topk_forced(const float* logits, int64_t ld, const int
             return DSA_ERR_CUDA;
     }
     return dsa::launch_status();
+}
+
+}  // namespace dsa
+
+extern "C" dsa_status dsa_topk_forced(const float* logits, int64_t ld, const int32_t* seq_lens, const int32_t* cu_q,
+                                      int32_t B, int32_t max_seq_len, int32_t row_begin, int32_t row_end, int32_t k,
+                                      int32_t n_init, int32_t n_local, int32_t* idx, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+    (void)workspace; (void)workspace_bytes;
+    return dsa::topk_launch(logits, ld, seq_lens, cu_q, B, max_seq_len, row_begin, row_end, k, n_init, n_local, idx,
+                            stream, nullptr);
 }
 
 extern "C" dsa_status dsa_topk(const float* logits, int64_t ld, const int32_t* seq_lens, const int32_t* cu_q,

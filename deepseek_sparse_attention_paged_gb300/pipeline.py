@@ -6,8 +6,9 @@ with ``dsa_store_index_k`` and owns the outputs (logits, top-k indices, attentio
 the scratch space.  ``step()`` runs one decode step of the hot path:
 
     dsa_store_index_k    this step's new keys -> paged FP8 index-K cache
-    dsa_indexer_logits   lightning-indexer logits of every query row
-    dsa_topk             per-row top-k indices
+    dsa_lightning_indexer  lightning-indexer logits and per-row top-k indices in one call (the
+                         logits kernel feeding the top-k its first-digit histograms), or for
+                         long prefill chunks dsa_indexer_logits + dsa_topk per row tile
     dsa_sparse_mla_decode  absorbed sparse MLA over the selected latent rows
 
 Nothing here computes: every step is a call into the CUDA library.
@@ -40,6 +41,16 @@ LOGITS_STATIC_SKIP_ELEMS = 8_000_000
 LOGITS_TILE_BUDGET_BYTES = 64 << 20
 
 
+def _align256(n: int) -> int:
+    return (n + 255) // 256 * 256
+
+
+def lightning_logits_offset(T: int) -> int:
+    """Byte offset of the logits in the one-call indexer's workspace (layout of
+    dsa_lightning_indexer: the per-row 4096-bin histograms, the logits call's scratch, the logits)."""
+    return _align256(T * 4096 * 4) + _align256(capi.dsa_indexer_logits_workspace_size(T))
+
+
 def logits_tile_rows(T: int, ld: int, budget_bytes: int = LOGITS_TILE_BUDGET_BYTES) -> int:
     """Query rows per logits tile: all T rows when T * ld is below the static skip size or the
     whole buffer fits the budget, else as many rows as fit the budget (at least one)."""
@@ -53,7 +64,7 @@ def logits_tile_rows(T: int, ld: int, budget_bytes: int = LOGITS_TILE_BUDGET_BYT
 class DeviceBatch:
     def __init__(self, wl: Workload, device: str = "cuda", with_latent: bool = True,
                  build_index_cache: bool = True, key_chunk: int = 1 << 20,
-                 logits_budget_bytes: int = LOGITS_TILE_BUDGET_BYTES):
+                 logits_budget_bytes: int = LOGITS_TILE_BUDGET_BYTES, fused: bool = True):
         self.wl = wl
         self.device = torch.device(device)
         dev = self.device
@@ -78,7 +89,18 @@ class DeviceBatch:
         self.ld = logits_ld(wl.max_seq_len)
         # the logits buffer holds one row tile; the step walks the tiles (indexer, then top-k)
         self.tile_rows = logits_tile_rows(wl.T, self.ld, logits_budget_bytes)
-        self.logits = torch.empty((self.tile_rows, self.ld), dtype=torch.float32, device=dev)
+        # one call for logits + top-k (dsa_lightning_indexer, histogram-fused) when the whole batch
+        # is one tile and its row groups / rows suit the fused kernels; its logits stay readable in
+        # its workspace
+        self.fused = (fused and self.tile_rows == wl.T and wl.max_q_len < 4 and wl.max_seq_len <= 131072
+                      and wl.T > 0)
+        if self.fused:
+            self.li_ws = torch.empty(capi.dsa_lightning_indexer_workspace_size(wl.T, wl.max_seq_len),
+                                     dtype=torch.uint8, device=dev)
+            off = lightning_logits_offset(wl.T)
+            self.logits = self.li_ws[off:off + wl.T * self.ld * 4].view(torch.float32).view(wl.T, self.ld)
+        else:
+            self.logits = torch.empty((self.tile_rows, self.ld), dtype=torch.float32, device=dev)
         self.idx = torch.empty((wl.T, wl.topk), dtype=torch.int32, device=dev)
         self.idx_ws = torch.empty(max(16, capi.dsa_indexer_logits_workspace_size(self.tile_rows)), dtype=torch.uint8,
                                   device=dev)
@@ -224,10 +246,18 @@ class DeviceBatch:
         return [(rb, min(T, rb + n)) for rb in range(0, T, n)]
 
     def select(self, stream=None, logits_hook=None):
-        """Indexer logits and top-k of every query row, tile by tile (one tile when the whole
-        logits buffer is small): the logits of rows [rb, re) go to logits[0 : re - rb], their top-k
-        to idx[rb : re].  `logits_hook(rb, re, logits)`, if given, runs after each tile's logits
-        call (tests read the tile there)."""
+        """Indexer logits and top-k of every query row: one fused dsa_lightning_indexer call when
+        self.fused, else tile by tile (one tile when the whole logits buffer is small): the logits of
+        rows [rb, re) go to logits[0 : re - rb], their top-k to idx[rb : re].  `logits_hook(rb, re,
+        logits)`, if given, runs after each tile's logits (tests read the tile there)."""
+        if self.fused:
+            wl = self.wl
+            capi.dsa_lightning_indexer(self.index_q, self.weights, self.index_pool, self.block_table, self.seq_lens,
+                                       self.cu_q, wl.max_seq_len, wl.max_q_len, wl.topk, self.idx, self.li_ws,
+                                       dev_err=self.dev_err, stream=stream)
+            if logits_hook is not None:
+                logits_hook(0, wl.T, self.logits)
+            return
         for rb, re in self.tiles():
             self.indexer_logits(row_begin=rb, row_end=re, stream=stream)
             if logits_hook is not None:

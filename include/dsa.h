@@ -279,7 +279,16 @@ dsa_status dsa_topk_forced(const float* logits, int64_t ld, const int32_t* seq_l
  * init / local token mask, then topk_transform).
  *   idx[r] = dsa_topk_forced(dsa_indexer_logits(...)[r]) for every row r < T.  The logits are
  *   kept in `workspace` (dsa_lightning_indexer_workspace_size(T, max_seq_len) bytes, 16-byte
- *   aligned) and are dead afterwards; the two stages are chained on the device.
+ *   aligned); the stages are chained on the device.
+ *   Fused (max_q_len < 4, i.e. row groups of 1 or 2 query rows, and max_seq_len <= 131072): the
+ *   logits kernel also counts, per row, the top 12 bits of each logit's order key (the key the
+ *   top-k selects on) and the top-k kernels take that histogram instead of a first read of the row.
+ *   Selected indices are the same as unfused; a visible key whose page id is out of range gets the
+ *   logit -inf (unfused: left unwritten).  Otherwise the two calls run as they are.
+ *   Workspace layout, each part starting 256-byte aligned: T x 4096 uint32 histograms; the logits
+ *   call's query scratch (dsa_indexer_logits_workspace_size(T) bytes); the fp32 logits, row r at
+ *   row r * ld, ld = max_seq_len rounded up to a multiple of 4 (at least 4).  They stay there
+ *   after the call.
  * Arguments: as for dsa_indexer_logits (all rows, 0 .. T) and dsa_topk_forced; flags: as for
  * dsa_indexer_logits.
  */

@@ -85,6 +85,7 @@ def test_host_side_validation_of_the_next_row_calls(lib):
     assert L.dsa_lightning_indexer(None, None, None, 0, None, 0, None, None, 1, 100, 1, 0, 16, 0, 0, 0, None,
                                    None, 0, None, None) == 0
     need = L.dsa_lightning_indexer_workspace_size(2, 100)
-    assert need == (2 * (64 * 128 + 64 * 4) + 255) // 256 * 256 + 2 * 100 * 4
+    # the per-row histograms, the logits call's scratch, the logits (each part 256-byte aligned)
+    assert need == 2 * 4096 * 4 + (2 * (64 * 128 + 64 * 4) + 255) // 256 * 256 + 2 * 100 * 4
     assert L.dsa_lightning_indexer(None, None, None, 0, None, 0, None, None, 1, 100, 1, 2, 16, 0, 0, 0,
                                    ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000), need - 16, None, None) == 1

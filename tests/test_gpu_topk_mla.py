@@ -194,14 +194,27 @@ def test_lightning_indexer_equals_logits_then_topk():
                                    wl.max_seq_len, wl.max_q_len, wl.topk, got, ws[:1024])
 
 
-def test_lightning_indexer_matches_oracle():
-    """The one-call indexer against the oracle: oracle.topk_forced on the oracle's logits, exactly
-    wherever the k-th / (k+1)-th gap (with the forced positions at +inf) is outside the tie band,
-    and a valid selection everywhere (forced positions kept, every other kept logit >= every dropped
-    one up to the logit tolerance), with and without forced initial / local tokens."""
-    from helpers import oracle_pool, record
-    wl = workloads.make_custom("li_oracle", 241, [500, 64, 3000, 17000, 40000, 70000], [1, 2, 3, 1, 1, 2], topk=256,
-                               heads=16)
+def _li_case(name):
+    if name == "cluster":   # long rows, few of them: the 2-CTA cluster top-k; row groups of 2
+        return workloads.make_custom("li_oracle", 241, [500, 64, 3000, 17000, 40000, 70000], [1, 2, 3, 1, 1, 2],
+                                     topk=256, heads=16)
+    rng = np.random.default_rng(242)   # many short rows: the one-CTA bitmap top-k
+    lens = rng.integers(100, 12000, 90).tolist()
+    return workloads.make_custom("li_oracle_b", 242, lens, rng.integers(1, 3, 90).tolist(), topk=512, heads=16)
+
+
+@pytest.mark.parametrize("case", ["cluster", "bitmap"])
+def test_lightning_indexer_matches_oracle(case):
+    """The one-call indexer (histogram-fused: both cases have row groups of at most 2 rows) against
+    the oracle: oracle.topk_forced on the oracle's logits, exactly wherever the k-th / (k+1)-th gap
+    (with the forced positions at +inf) is outside the tie band, and a valid selection everywhere
+    (forced positions kept, every other kept logit >= every dropped one up to the logit
+    tolerance), with and without forced initial / local tokens; its logits stay in the workspace
+    and match the oracle's."""
+    from helpers import check_logits, oracle_pool, record
+    from deepseek_sparse_attention_paged_gb300.pipeline import lightning_logits_offset
+    wl = _li_case(case)
+    assert wl.max_q_len < 4
     db = DeviceBatch(wl, with_latent=False)
     pool = oracle_pool(wl)
     rows = np.arange(wl.T)
@@ -211,10 +224,14 @@ def test_lightning_indexer_matches_oracle():
     vis = wl.visible_lens()
     ws = torch.empty(capi.dsa_lightning_indexer_workspace_size(wl.T, wl.max_seq_len), dtype=torch.uint8,
                      device="cuda")
+    off = lightning_logits_offset(wl.T)
     for n_init, n_local in ((0, 0), (2, 8)):
         got = torch.full((wl.T, wl.topk), -7, dtype=torch.int32, device="cuda")
+        ws.fill_(0xAB)   # stale histograms / logits from elsewhere must not matter
         capi.dsa_lightning_indexer(db.index_q, db.weights, db.index_pool, db.block_table, db.seq_lens, db.cu_q,
                                    wl.max_seq_len, wl.max_q_len, wl.topk, got, ws, n_init=n_init, n_local=n_local)
+        lg = ws[off:off + wl.T * db.ld * 4].view(torch.float32).view(wl.T, db.ld).cpu().numpy()
+        check_logits(lg, ref_lg, mag, vis, key=f"lightning_indexer_vs_oracle/{case}")
         got = got.cpu().numpy()
         ref = oracle.topk_forced(ref_lg, wl.seq_lens, wl.cu_q, rows, wl.topk, n_init, n_local)
         exact = 0
@@ -232,4 +249,4 @@ def test_lightning_indexer_matches_oracle():
                 assert np.array_equal(got[r], ref[r]), f"row {r}: differs from the oracle outside the tie band"
                 exact += 1
             check_topk_valid(got[r], row, wl.topk, mag[r, :v])
-        record("lightning_indexer_vs_oracle", rows=len(rows), rows_exact=exact)
+        record(f"lightning_indexer_vs_oracle/{case}", rows=len(rows), rows_exact=exact)
