@@ -96,6 +96,10 @@ def _load():
         "dsa_oracle_topk": (None, [P, i64, P, P, i32, P, i64, i32, P]),
         "dsa_oracle_sparse_mla": (i64, [P, P, i64, P, i32, P, P, i32, P, i32, i32, f64, P, i64, P, P, P]),
         "dsa_oracle_dense_mla": (None, [P, P, i64, P, i32, P, P, i32, i32, f64, P, i64, P, P]),
+        "dsa_oracle_quant_fp8_tensor": (None, [P, i64, ctypes.c_float, P]),
+        "dsa_oracle_store_latent_fp8": (i64, [P, P, i64, ctypes.c_float, P, i64]),
+        "dsa_oracle_sparse_mla_fp8": (i64, [P, ctypes.c_float, P, ctypes.c_float, i64, P, i32, P, P, i32, P, i32, i32,
+                                            f64, P, i64, P, P]),
         "dsa_oracle_lse_merge": (None, [P, P, P, P, i64, i32, P, P]),
         "dsa_oracle_num_threads": (ctypes.c_int, []),
         "dsa_oracle_set_num_threads": (None, [ctypes.c_int]),
@@ -316,6 +320,41 @@ def sparse_mla(q_bf16, kv_bf16, block_table, seq_lens, cu_q, idx, scale, rows, w
                                         _p(out), _p(lse), _p(psum))
     if want_psum:
         return out, lse, psum, int(bad)
+    return out, lse
+
+
+def quant_fp8_tensor(x_bf16: np.ndarray, scale: float) -> np.ndarray:
+    """Per-tensor FP8 codes of bf16 values: E4M3FN(x / scale) (fp32 division, RNE, saturating)."""
+    x = _c(x_bf16, np.uint16)
+    out = np.empty(x.shape, np.uint8)
+    _load().dsa_oracle_quant_fp8_tensor(_p(x), x.size, float(scale), _p(out))
+    return out
+
+
+def store_latent_fp8(latent_bf16: np.ndarray, slot_mapping: np.ndarray, k_scale: float, pool: np.ndarray) -> int:
+    """Latent rows [n, 576] (bf16 bits) into the FP8 cache ``pool`` (uint8 [num_pages, 64, 576]) by slot."""
+    x = _c(latent_bf16, np.uint16).reshape(-1, DQK)
+    slots = _c(slot_mapping, np.int64)
+    assert pool.dtype == np.uint8 and pool.flags["C_CONTIGUOUS"] and pool.shape[-1] == DQK
+    return int(_load().dsa_oracle_store_latent_fp8(_p(x), _p(slots), x.shape[0], float(k_scale), _p(pool),
+                                                     pool.shape[0]))
+
+
+def sparse_mla_fp8(q_bf16, q_scale, kv_fp8, k_scale, block_table, seq_lens, cu_q, idx, scale, rows):
+    """Sparse MLA over the FP8 latent cache (query quantised with q_scale): (out [n, H, 512], lse [n, H])."""
+    q = _c(q_bf16, np.uint16)
+    T, H = q.shape[0], q.shape[1]
+    kv = _c(kv_fp8, np.uint8)
+    bt = _c(block_table, np.int32)
+    sl = _c(seq_lens, np.int32)
+    cq = _c(cu_q, np.int32)
+    ix = _c(idx, np.int32)
+    rw = _c(rows, np.int64)
+    out = np.empty((rw.size, H, DV), np.float64)
+    lse = np.empty((rw.size, H), np.float64)
+    _load().dsa_oracle_sparse_mla_fp8(_p(q), float(q_scale), _p(kv), float(k_scale), kv.shape[0], _p(bt), bt.shape[1],
+                                      _p(sl), _p(cq), sl.size, _p(ix), ix.shape[1], H, float(scale), _p(rw), rw.size,
+                                      _p(out), _p(lse))
     return out, lse
 
 

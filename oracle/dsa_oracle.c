@@ -576,6 +576,99 @@ int64_t dsa_oracle_sparse_mla(const uint16_t* q_bf16, const uint16_t* kv, int64_
     return bad_total;
 }
 
+/* ---------------------------------------------------------------- FP8 latent cache */
+
+/* Per-tensor FP8 quantisation ([mla] MLACommonImpl.forward with kv_cache_dtype "fp8": the latent
+ * cache is written by concat_and_cache_mla(k_c_normed, k_pe, kv_cache, slot_mapping, kv_cache_dtype,
+ * scale = layer._k_scale) and the decode query by ops.scaled_fp8_quant(decode_ql_nope /
+ * decode_q_pe, layer._q_scale); the cache is then viewed as the fp8 dtype).  Reading: code =
+ * E4M3FN(x / scale) with x the bf16 value, the division one IEEE fp32 operation, round to nearest
+ * even with saturation to +-448 (the encoder above); one fp32 scale for the whole tensor. */
+void dsa_oracle_quant_fp8_tensor(const uint16_t* x_bf16, int64_t n, float scale, uint8_t* codes) {
+    for (int64_t i = 0; i < n; ++i) codes[i] = dsa_oracle_e4m3_encode(bf16_bits_to_f32(x_bf16[i]) / scale);
+}
+
+/* Latent rows (512 latent + 64 rope dims, bf16) into the FP8 cache [num_pages, 64, 576] by slot
+ * ([mla] concat_and_cache_mla with the fp8 cache): row slot & 63 of page slot >> 6 gets the 576
+ * codes.  A negative slot is padding (skipped); a slot past the pool is skipped and counted. */
+int64_t dsa_oracle_store_latent_fp8(const uint16_t* latent_bf16, const int64_t* slot_mapping, int64_t n, float k_scale,
+                                    uint8_t* pool, int64_t num_pages) {
+    int64_t bad = 0;
+    for (int64_t t = 0; t < n; ++t) {
+        const int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot / PAGE >= num_pages) { ++bad; continue; }
+        dsa_oracle_quant_fp8_tensor(latent_bf16 + t * DQK, DQK, k_scale, pool + slot * DQK);
+    }
+    return bad;
+}
+
+/* Attention of one (row, head) over FP8 latent rows: the query quantised per tensor with q_scale,
+ * keys and values the cached codes times k_scale ([mla] _forward_decode on the fp8 query and cache):
+ * S_i = scale * sum_d (dec(qc_d) q_scale)(dec(kc_id) k_scale); P = softmax(S);
+ * o = sum_i P_i dec(kc_i[0:512]) k_scale; the same steps as attend_rows on the dequantised values. */
+static void attend_rows_fp8(const uint16_t* qh, float q_scale, const uint8_t* kv, float k_scale, const int64_t* g,
+                            int64_t n, double scale, double* o, double* lse) {
+    for (int d = 0; d < DV; ++d) o[d] = 0.0;
+    if (n == 0) {
+        *lse = -INFINITY;
+        return;
+    }
+    double q[DQK];
+    for (int d = 0; d < DQK; ++d)
+        q[d] = dsa_oracle_e4m3_decode(dsa_oracle_e4m3_encode(bf16_bits_to_f32(qh[d]) / q_scale)) * (double)q_scale;
+    double* S = (double*)malloc(sizeof(double) * (size_t)n);
+    double m = -INFINITY;
+    for (int64_t i = 0; i < n; ++i) {
+        const uint8_t* c = kv + g[i] * DQK;
+        double dot = 0.0;
+        for (int d = 0; d < DQK; ++d) dot += q[d] * (dsa_oracle_e4m3_decode(c[d]) * (double)k_scale);
+        S[i] = scale * dot;
+        if (S[i] > m) m = S[i];
+    }
+    double l = 0.0;
+    for (int64_t i = 0; i < n; ++i) l += exp(S[i] - m);
+    for (int64_t i = 0; i < n; ++i) {
+        const double p = exp(S[i] - m) / l;
+        const uint8_t* c = kv + g[i] * DQK;
+        for (int d = 0; d < DV; ++d) o[d] += p * (dsa_oracle_e4m3_decode(c[d]) * (double)k_scale);
+    }
+    *lse = m + log(l);
+    free(S);
+}
+
+/* Sparse MLA decode over the FP8 latent cache: dsa_oracle_sparse_mla with the query quantised by
+ * q_scale and the cache rows as FP8 codes with k_scale (kv: uint8 [num_pages, 64, 576]). */
+int64_t dsa_oracle_sparse_mla_fp8(const uint16_t* q_bf16, float q_scale, const uint8_t* kv, float k_scale,
+                                  int64_t num_pages, const int32_t* block_table, int32_t max_pages,
+                                  const int32_t* seq_lens, const int32_t* cu_q, int32_t B, const int32_t* idx, int32_t k,
+                                  int32_t H, double scale, const int64_t* rows, int64_t n_rows, double* out,
+                                  double* lse) {
+    int64_t bad_total = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : bad_total)
+    for (int64_t i = 0; i < n_rows * H; ++i) {
+        int64_t ri = i / H;
+        int h = (int)(i % H);
+        int64_t r = rows[ri];
+        int b = row_request(cu_q, B, r);
+        int32_t v = dsa_oracle_visible_len(seq_lens, cu_q, B, r);
+        int64_t* g = (int64_t*)malloc(sizeof(int64_t) * (size_t)k);
+        int64_t n = 0, bad = 0;
+        for (int32_t j = 0; j < k; ++j) {
+            int32_t pos = idx[r * (int64_t)k + j];
+            if (pos < 0) continue;
+            int64_t gr = (b >= 0 && pos < v) ? latent_row(block_table, max_pages, num_pages, b, pos) : -1;
+            if (gr < 0) { ++bad; continue; }
+            g[n++] = gr;
+        }
+        attend_rows_fp8(q_bf16 + (r * H + h) * DQK, q_scale, kv, k_scale, g, n, scale, out + (ri * H + h) * DV,
+                        lse + ri * H + h);
+        free(g);
+        if (h == 0) bad_total += bad;
+    }
+    return bad_total;
+}
+
 /* Dense MLA decode over every visible position [0, v_r) of the request, the same attention with
  * no selection ([mla] _forward_decode over the whole paged latent cache).  Used to pin the sparse
  * form: with k >= v_r the selection keeps every position and the two must agree. */
