@@ -186,6 +186,9 @@ STAGE_SOURCES = {"store": ["store_index_k.cu"], "indexer": ["indexer_logits.cu"]
 # tensor peak of each stage relative to the measured dense bf16 peak: the indexer contracts FP8
 # operands (nominal dense FP8 : BF16 = 4.5 : 2.25 PFLOP/s), the attention bf16
 STAGE_TENSOR_PEAK_RATIO = {"indexer": 2.0, "select": 2.0, "mla": 1.0}
+# per-tensor scales of the FP8 latent-cache stage (~ max |N(0,1)| / 448 for the synthetic cache)
+FP8_K_SCALE = 0.0125
+FP8_Q_SCALE = 0.0125
 
 
 # ----------------------------------------------------------------------------- CPU oracle arm
@@ -421,6 +424,17 @@ def run_gpu(args):
         "select": TimedGraph(lambda: db.select(), stream, flush),
         "mla": TimedGraph(lambda: db.sparse_mla(), stream, flush),
     }
+    # the FP8 latent-cache variant of the attention on the same selections (cache quantised on the
+    # device by dsa_store_latent_fp8, per-tensor scales; timed as a stage of its own)
+    kv8 = torch.empty((wl.num_pages, 64, 576), dtype=torch.uint8, device="cuda")
+    capi.dsa_store_latent_fp8(db.kv_pool.view(-1, 576), torch.arange(wl.num_pages * 64, device="cuda"), FP8_K_SCALE,
+                              kv8)
+    out8 = torch.empty_like(db.out)
+    lse8 = torch.empty_like(db.lse)
+    stage_graphs["mla_fp8"] = TimedGraph(
+        lambda: capi.dsa_sparse_mla_decode_fp8(db.mla_q, FP8_Q_SCALE, kv8, FP8_K_SCALE, db.block_table, db.seq_lens,
+                                               db.cu_q, db.idx, wl.scale, out8, db.mla_ws, lse=lse8,
+                                               dev_err=db.dev_err), stream, flush)
     st, word = db.device_error()
     if st != 0:
         raise RuntimeError(f"device error word {word} after warm-up")
@@ -457,6 +471,8 @@ def run_gpu(args):
     hbm, bf16, peak_kind = measured_peaks()
     work = algorithmic_work(wl)
     work["select"] = tuple(a + b for a, b in zip(work["indexer"], work["topk"]))
+    mb, mf = work["mla"]
+    work["mla_fp8"] = (mb - int(np.minimum(wl.visible_lens(), wl.topk).sum()) * 576, mf)   # 576 B rows, not 1152
     stages = {}
     for k, ms_list in stage_ms.items():
         ms = sum(ms_list) / len(ms_list)

@@ -96,6 +96,9 @@ def load(path: str = LIB_PATH):
         "dsa_selftest_wait_timeout": (ctypes.c_int, [P, ctypes.c_uint64, P]),
         "dsa_sparse_mla_decode_noalloc": (ctypes.c_int, [P, P, i64, P, i32, P, P, i32, P, i32, i32, i32,
                                                          ctypes.c_float, P, P, P, P]),
+        "dsa_store_latent_fp8": (ctypes.c_int, [P, P, i64, ctypes.c_float, P, i64, P, P]),
+        "dsa_sparse_mla_decode_fp8": (ctypes.c_int, [P, ctypes.c_float, P, ctypes.c_float, i64, P, i32, P, P, i32, P,
+                                                     i32, i32, i32, ctypes.c_float, P, P, P, sz, P, P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -381,6 +384,55 @@ def dsa_sparse_mla_decode(q_bf16: torch.Tensor, kv_pool: torch.Tensor, block_tab
         _ptr(q_bf16), _ptr(kv_pool), kv_pool.shape[0], _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
         _ptr(cu_q), B, _ptr(idx), idx.shape[1], T, H, float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(dev_err), _stream(stream)))
+    _count(2 if T > 0 else 0)
+
+
+def dsa_store_latent_fp8(latent_bf16: torch.Tensor, slot_mapping: torch.Tensor, k_scale: float,
+                         kv_pool_fp8: torch.Tensor, dev_err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Latent rows [n, 576] (bf16) into the FP8 latent cache (uint8 [pages, 64, 576]) by slot."""
+    lib = load()
+    _cuda(latent_bf16, torch.bfloat16, "latent_bf16")
+    _cuda(slot_mapping, torch.int64, "slot_mapping")
+    _cuda(kv_pool_fp8, torch.uint8, "kv_pool_fp8")
+    _need(latent_bf16.dim() == 2 and latent_bf16.shape[1] == LATENT_DIM, "latent_bf16 must be [n, 576]")
+    _need(slot_mapping.numel() == latent_bf16.shape[0], "one slot per row")
+    _need(kv_pool_fp8.dim() == 3 and tuple(kv_pool_fp8.shape[1:]) == (64, LATENT_DIM),
+          "kv_pool_fp8 must be [pages, 64, 576]")
+    n = latent_bf16.shape[0]
+    _check("dsa_store_latent_fp8", lib.dsa_store_latent_fp8(_ptr(latent_bf16), _ptr(slot_mapping), n, float(k_scale),
+                                                            _ptr(kv_pool_fp8), kv_pool_fp8.shape[0], _ptr(dev_err),
+                                                            _stream(stream)))
+    _count(1 if n > 0 else 0)
+
+
+def dsa_sparse_mla_decode_fp8(q_bf16: torch.Tensor, q_scale: float, kv_pool_fp8: torch.Tensor, k_scale: float,
+                              block_table: torch.Tensor, seq_lens: torch.Tensor, cu_q: torch.Tensor, idx: torch.Tensor,
+                              scale: float, out: torch.Tensor, workspace: torch.Tensor,
+                              lse: Optional[torch.Tensor] = None, dev_err: Optional[torch.Tensor] = None,
+                              stream=None) -> None:
+    """Sparse MLA over the FP8 latent cache; the query is quantised with q_scale inside the call."""
+    lib = load()
+    _cuda(q_bf16, torch.bfloat16, "q_bf16")
+    _cuda(kv_pool_fp8, torch.uint8, "kv_pool_fp8")
+    _cuda(block_table, torch.int32, "block_table")
+    _cuda(seq_lens, torch.int32, "seq_lens")
+    _cuda(cu_q, torch.int32, "cu_q")
+    _cuda(idx, torch.int32, "idx")
+    _cuda(out, torch.bfloat16, "out")
+    _need(workspace.is_cuda and workspace.is_contiguous(), "workspace must be a contiguous CUDA tensor")
+    if lse is not None:
+        _cuda(lse, torch.float32, "lse")
+    _need(q_bf16.dim() == 3 and q_bf16.shape[2] == LATENT_DIM, "q_bf16 must be [T, H, 576]")
+    T, H, _ = q_bf16.shape
+    _need(kv_pool_fp8.dim() == 3 and tuple(kv_pool_fp8.shape[1:]) == (64, LATENT_DIM),
+          "kv_pool_fp8 must be [pages, 64, 576]")
+    _need(idx.dim() == 2 and idx.shape[0] == T, "idx must be [T, k]")
+    _need(tuple(out.shape) == (T, H, VALUE_DIM), "out must be [T, H, 512]")
+    B = seq_lens.numel()
+    _check("dsa_sparse_mla_decode_fp8", lib.dsa_sparse_mla_decode_fp8(
+        _ptr(q_bf16), float(q_scale), _ptr(kv_pool_fp8), float(k_scale), kv_pool_fp8.shape[0], _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), _ptr(cu_q), B, _ptr(idx), idx.shape[1], T, H, float(scale), _ptr(out),
+        _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_err), _stream(stream)))
     _count(2 if T > 0 else 0)
 
 

@@ -47,6 +47,8 @@
 // With one split the CTA writes bf16 output directly; with several, normalised fp32 partials and
 // their lse go to the workspace and a combine kernel merges them.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "dsa_common.cuh"
 #include "sm100_ptx.cuh"
@@ -633,6 +635,480 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
     cluster_sync_all();   // neither CTA leaves while its peer may still signal or write into it
 }
 
+// ---------------------------------------------------------------------------------------------
+// FP8 latent cache (vllm mla/common.py, MLACommonImpl.forward with kv_cache_dtype "fp8": the cache
+// rows are E4M3 codes of x / k_scale, the decode query is quantised by ops.scaled_fp8_quant with
+// q_scale, and _forward_decode runs on the FP8 query and cache).  Same work split, swap and
+// softmax as the bf16 kernel; the differences:
+//   * a stage holds this CTA's FP8 codes of the 64 selected rows -- value dims 256 c .. + 255 as two
+//     128-byte swizzled K-major chunks, rope dims 512 + 32 c .. + 31 without swizzle -- and the same
+//     value dims widened to bf16 (exact: E4M3 values are bf16 values) in the MN-major value layout;
+//     each producer lane widens exactly the 16-byte pieces it copied, once they have landed;
+//   * the score MMA is E4M3 x E4M3 (kind::f8f6f4, K = 32) with the query's codes in tensor memory
+//     (quantised there by the softmax warps with q_scale); S is scaled by scale * q_scale * k_scale;
+//   * P stays bf16 and PV stays bf16 x bf16; O is scaled by k_scale at the end.
+// ---------------------------------------------------------------------------------------------
+constexpr int kF8ChunkBytes = kKeysPerTile * 128;                        // 128 value codes per row
+constexpr int kF8RopeBytes = kKeysPerTile * kRopeHalf;                   // 32 rope codes per row
+constexpr int kF8CodeBytes = 2 * kF8ChunkBytes + kF8RopeBytes;           // 18432
+constexpr int kF8VBytes = kOwnChunks * kKvChunkBytes;                    // 32768: bf16 value dims
+constexpr int kF8StageBytes = kF8CodeBytes + kF8VBytes;                  // 51200
+constexpr int kF8Stages = 3;
+constexpr uint32_t kF8TmemQRope = kTmemQ + 64;                           // query codes: value 64 + rope 8 columns
+constexpr size_t kF8SmemBytes = 1024 + size_t(kF8Stages) * kF8StageBytes + 2 * size_t(kXBytes) + kBarBytes;
+static_assert(kF8CodeBytes % 1024 == 0 && kF8StageBytes % 1024 == 0, "1024-byte alignment of the swizzled parts");
+static_assert(kF8Stages <= kKvStages, "barrier arrays");
+static_assert(kF8SmemBytes <= 232448, "shared-memory budget");
+
+// Byte offset of 16-byte piece p (codes 16 p .. 16 p + 15) of row i of the rope codes: K-major without
+// swizzle, rows of 32 bytes = two core matrices, 8-row groups 256 bytes apart.
+__device__ __forceinline__ uint32_t rope8_off(int i, int p) {
+    return static_cast<uint32_t>((i >> 3) * 256 + p * 128 + (i & 7) * 16);
+}
+
+// D[tmem] (+)= A[tmem] x B[smem]^T, E4M3 operands, fp32 accumulate (one thread issues).
+__device__ __forceinline__ void umma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, const uint32_t (&r)[4]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
+                 "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
+
+// Four bf16 -> E4M3 codes of x / qs (one IEEE division each, round to nearest even, saturating).
+__device__ __forceinline__ uint32_t quant4_e4m3(uint32_t lo, uint32_t hi, float qs) {
+    const float v[4] = {bf16_lo(lo), bf16_hi(lo), bf16_lo(hi), bf16_hi(hi)};
+    uint32_t w = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        w |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(__fdiv_rn(v[e], qs), __NV_SATFINITE, __NV_E4M3)) << (8 * e);
+    return w;
+}
+
+// Two E4M3 codes -> two bf16 (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t two) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
+    const float a = __half2float(__ushort_as_half(h.x)), b = __half2float(__ushort_as_half(h.y));
+    return pack_bf16x2(a, b);
+}
+
+__global__ void __launch_bounds__(kMlaThreads, 1)
+sparse_mla_fp8_kernel(const uint8_t* __restrict__ kv8, float k_scale, const uint16_t* __restrict__ q, float q_scale,
+                      int64_t num_pages, const int32_t* __restrict__ block_table, int max_pages,
+                      const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q, int B,
+                      const int32_t* __restrict__ idx, int k, int H, float scale, int splits, uint16_t* __restrict__ out,
+                      float* __restrict__ lse_out, float* __restrict__ part_o, float* __restrict__ part_lse, int32_t* err) {
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw_addr = ptx::smem_addr(smem_raw);
+    unsigned char* base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    unsigned char* kvs = base;                                                   // [3][codes 18 KB | bf16 values 32 KB]
+    float* xs = reinterpret_cast<float*>(kvs + kF8Stages * kF8StageBytes);       // [2][2 halves][8 quads][128 heads][4]
+    MlaBars& bar = *reinterpret_cast<MlaBars*>(reinterpret_cast<unsigned char*>(xs) + 2 * kXBytes);
+
+    const int split = blockIdx.y;
+    const int r = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = row_request(cu_q, B, r);
+    const int q0 = __ldg(cu_q + b);
+    const int v = visible_len(__ldg(seq_lens + b), __ldg(cu_q + b + 1) - q0, r - q0);
+    const int per_split = (k + splits - 1) / splits;
+    const int e_begin = split * per_split;
+    const int e_end = min(k, e_begin + per_split);
+    const int ntiles = e_end > e_begin ? (e_end - e_begin + kKeysPerTile - 1) / kKeysPerTile : 0;
+    const uint32_t crank = cluster_ctarank();
+    const uint32_t peer = crank ^ 1u;
+    const int half = static_cast<int>(crank);
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(&bar.q_full, kSoftmaxWarps);
+        for (int s = 0; s < kF8Stages; ++s) {
+            ptx::mbar_init(&bar.kv_full[s], kProducerWarps);   // each producer warp once its rows are widened
+            ptx::mbar_init(&bar.kv_empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(&bar.s_full[a], 1);
+            ptx::mbar_init(&bar.s_free[a], 1);
+            ptx::mbar_init(&bar.p_full[a], kSoftmaxWarps);
+            ptx::mbar_init(&bar.x_full[a], 1);
+            ptx::mbar_init(&bar.x_free[a], 1);
+        }
+        ptx::mbar_init(&bar.o_full, 1);
+        for (int qd = 0; qd < 4; ++qd) ptx::mbar_init(&bar.pair[qd], 64);
+        ptx::fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        ptx::tmem_alloc(&bar.tmem_slot, kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before_sync();
+    cluster_sync_all();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem = bar.tmem_slot;
+    const uint64_t deadline = ptx::wait_deadline();
+    bool timed_out = false;
+    const uint32_t kv_addr0 = ptx::smem_addr(kvs);
+
+    if (warp >= kProducerWarp0) {
+        // ---------------------------------------------------------------- producers
+        const int pw = warp - kProducerWarp0;
+        ptx::griddep_wait();
+        const int my_entry = pw * kKeysPerProducer + lane;
+        auto load_pos = [&](int tile) -> int {
+            const int e = e_begin + tile * kKeysPerTile + my_entry;
+            return (lane < kKeysPerProducer && tile < ntiles && e < e_end) ? __ldg(idx + static_cast<int64_t>(r) * k + e)
+                                                                          : -1;
+        };
+        auto pos_ok = [&](int pos) -> bool { return pos >= 0 && pos < v && (pos >> 6) < max_pages; };
+        auto load_page = [&](int pos) -> int {
+            return pos_ok(pos) ? __ldg(block_table + static_cast<int64_t>(b) * max_pages + (pos >> 6)) : -1;
+        };
+        auto to_row = [&](int pos, int page) -> int {
+            if (pos < 0) return -1;
+            if (!pos_ok(pos)) { raise_error(err, DSA_DEVERR_INDEX_RANGE); return -1; }
+            if (page < 0 || page >= num_pages) { raise_error(err, DSA_DEVERR_PAGE_RANGE); return -1; }
+            return page * kPage + (pos & 63);
+        };
+        // widen this lane's value pieces of tile u (the 16-byte pieces it copied) to bf16, then the
+        // warp's arrival on the stage's full barrier
+        auto widen = [&](int u) {
+            const uint32_t st = kv_addr0 + (u % kF8Stages) * kF8StageBytes;
+            const unsigned char* sp = kvs + (u % kF8Stages) * kF8StageBytes;
+#pragma unroll
+            for (int kq = 0; kq < kKeysPerProducer / 2; ++kq) {
+                const int key = pw * kKeysPerProducer + 2 * kq + (lane >> 4);
+                const int j = lane & 15;   // codes 16 j .. 16 j + 15 of this CTA's value dims
+                const uint4 c = *reinterpret_cast<const uint4*>(sp + (j >> 3) * kF8ChunkBytes + key * 128 +
+                                                                (((j & 7) ^ (key & 7)) << 4));
+                uint4 lo, hi;
+                lo.x = e4m3x2_to_bf16x2(static_cast<uint16_t>(c.x));
+                lo.y = e4m3x2_to_bf16x2(static_cast<uint16_t>(c.x >> 16));
+                lo.z = e4m3x2_to_bf16x2(static_cast<uint16_t>(c.y));
+                lo.w = e4m3x2_to_bf16x2(static_cast<uint16_t>(c.y >> 16));
+                hi.x = e4m3x2_to_bf16x2(static_cast<uint16_t>(c.z));
+                hi.y = e4m3x2_to_bf16x2(static_cast<uint16_t>(c.z >> 16));
+                hi.z = e4m3x2_to_bf16x2(static_cast<uint16_t>(c.w));
+                hi.w = e4m3x2_to_bf16x2(static_cast<uint16_t>(c.w >> 16));
+                // dims 16 j .. 16 j + 7 and 16 j + 8 .. 16 j + 15: chunk j / 4 of 64 dims, pieces 2 (j % 4), + 1
+                unsigned char* vb = const_cast<unsigned char*>(sp) + kF8CodeBytes + (j >> 2) * kKvChunkBytes + key * 128;
+                *reinterpret_cast<uint4*>(vb + (((2 * (j & 3)) ^ (key & 7)) << 4)) = lo;
+                *reinterpret_cast<uint4*>(vb + (((2 * (j & 3) + 1) ^ (key & 7)) << 4)) = hi;
+            }
+            (void)st;
+            ptx::fence_proxy_async_smem();   // the bf16 values are read by the tensor cores
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&bar.kv_full[u % kF8Stages]);
+        };
+        int pos1[kBatch], page1[kBatch], pos2[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) pos1[u] = load_pos(u);
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) page1[u] = load_page(pos1[u]);
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) pos2[u] = load_pos(kBatch + u);
+        const uint8_t* kv_val = kv8 + half * kHalfDims + (lane & 15) * 16;
+        const uint8_t* kv_rope = kv8 + kValueDim + half * kRopeHalf + (lane & 1) * 16;
+        for (int t0 = 0; t0 < ntiles && !timed_out; t0 += kBatch) {
+            int rows[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) rows[u] = to_row(pos1[u], page1[u]);
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                pos1[u] = pos2[u];
+                page1[u] = load_page(pos2[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) pos2[u] = load_pos(t0 + 2 * kBatch + u);
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int t = t0 + u;
+                if (t >= ntiles) break;
+                const int s = t % kF8Stages;
+                const uint32_t ph = (t / kF8Stages) & 1;
+                const uint32_t vbits = __ballot_sync(0xffffffffu, rows[u] >= 0) & 0xffffu;
+                const int row_src = rows[u] >= 0 ? rows[u] : 0;
+                if (lane == 0 && !ptx::mbar_wait(&bar.kv_empty[s], ph ^ 1u, deadline)) timed_out = true;
+                timed_out = __shfl_sync(0xffffffffu, timed_out ? 1 : 0, 0) != 0;
+                if (timed_out) break;
+                const uint32_t stage = kv_addr0 + s * kF8StageBytes;
+#pragma unroll
+                for (int kq = 0; kq < kKeysPerProducer / 2; ++kq) {
+                    const int kl = 2 * kq + (lane >> 4);
+                    const int key = pw * kKeysPerProducer + kl;
+                    const int64_t row = __shfl_sync(0xffffffffu, row_src, kl);
+                    const int j = lane & 15;
+                    cp_async_16(stage + (j >> 3) * kF8ChunkBytes + key * 128 + (((j & 7) ^ (key & 7)) << 4),
+                                kv_val + row * kLatentDim);
+                }
+                {
+                    const int kl = lane >> 1;
+                    const int key = pw * kKeysPerProducer + kl;
+                    const int64_t row = __shfl_sync(0xffffffffu, row_src, kl);
+                    cp_async_16(stage + 2 * kF8ChunkBytes + rope8_off(key, lane & 1), kv_rope + row * kLatentDim);
+                }
+                asm volatile("cp.async.commit_group;" ::: "memory");
+                if (lane == 0) bar.valid[s][pw] = vbits;
+                if (t >= 1) {
+                    asm volatile("cp.async.wait_group 1;" ::: "memory");   // this lane's copies of tile t - 1 landed
+                    widen(t - 1);
+                }
+            }
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        if (!timed_out && ntiles > 0) widen(ntiles - 1);
+    } else if (warp == kMmaWarp) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = ptx::instr_desc(0, 0, kHeadsPerCta, kKeysPerTile);   // E4M3 x E4M3
+            constexpr uint32_t idesc_pv = ptx::instr_desc(1, 1, kHeadsPerCta, kHalfDims) | (1u << 16);
+            bool ok = ptx::mbar_wait(&bar.q_full, 0, deadline);
+            int tq = 0, tp = 0;
+            while (ok && tp < ntiles) {
+                bool issued = false;
+                if (tq < ntiles && ptx::mbar_test_wait(&bar.kv_full[tq % kF8Stages], (tq / kF8Stages) & 1) &&
+                    ptx::mbar_test_wait(&bar.s_free[tq & 1], ((tq >> 1) & 1) ^ 1u)) {
+                    ptx::fence_proxy_async_smem();
+                    ptx::tc_fence_after_sync();
+                    const uint32_t kb = kv_addr0 + (tq % kF8Stages) * kF8StageBytes;
+                    const uint32_t d = tmem + kTmemS + (tq & 1) * kKeysPerTile;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t db = make_desc(kb + (kk >> 2) * kF8ChunkBytes + (kk & 3) * 32, 16, 1024, kLayoutSw128);
+                        umma_f8_ts(d, tmem + kTmemQ + kk * 8, db, idesc_qk, kk != 0 ? 1u : 0u);
+                    }
+                    umma_f8_ts(d, tmem + kF8TmemQRope, make_desc(kb + 2 * kF8ChunkBytes, 128, 256, kLayoutNone), idesc_qk,
+                               1u);
+                    ptx::umma_commit(&bar.s_full[tq & 1]);
+                    ++tq;
+                    issued = true;
+                }
+                if (tp < tq && ptx::mbar_test_wait(&bar.p_full[tp & 1], (tp >> 1) & 1)) {
+                    ptx::tc_fence_after_sync();
+                    const int s = tp % kF8Stages;
+                    const uint32_t vb = kv_addr0 + s * kF8StageBytes + kF8CodeBytes;
+                    const uint32_t pa = tmem + kTmemS + (tp & 1) * kKeysPerTile;
+#pragma unroll
+                    for (int ks = 0; ks < kKeysPerTile / 16; ++ks) {
+                        const uint64_t db = make_desc(vb + ks * 16 * 128, kKvChunkBytes, 1024, kLayoutSw128);
+                        umma_f16_ts(tmem, pa + ks * 8, db, idesc_pv, (tp | ks) != 0 ? 1u : 0u);
+                    }
+                    ptx::umma_commit(&bar.kv_empty[s]);
+                    ptx::umma_commit(&bar.s_free[tp & 1]);
+                    ++tp;
+                    issued = true;
+                }
+                if (!issued && static_cast<uint64_t>(clock64()) > deadline) ok = false;
+            }
+            if (ok && ntiles > 0) ptx::umma_commit(&bar.o_full);
+            if (!ok) timed_out = true;
+        }
+    } else {
+        // ---------------------------------------------------------------- query, softmax, epilogue
+        const int quad = warp & 3;
+        const int kh = warp >> 2;
+        const int head = quad * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        {
+            // the query's codes (x / q_scale): value dims 128 kh .. + 127 of this CTA -> columns
+            // 384 + 32 kh .., rope dims 16 kh .. + 15 of this CTA -> columns 448 + 4 kh ..
+            const uint4* src = reinterpret_cast<const uint4*>(q + (static_cast<int64_t>(r) * H + head) * kLatentDim);
+            const bool live = head < H;
+            uint32_t w[32];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint4 raw = live ? __ldg(src + (half * kHalfDims + kh * 128) / 8 + i) : make_uint4(0u, 0u, 0u, 0u);
+                w[2 * i] = quant4_e4m3(raw.x, raw.y, q_scale);
+                w[2 * i + 1] = quant4_e4m3(raw.z, raw.w, q_scale);
+            }
+            tmem_st_32x32b_x32(tmem + lane_base + kTmemQ + 32 * kh, w);
+            uint32_t wr[4];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const uint4 raw =
+                    live ? __ldg(src + (kValueDim + half * kRopeHalf + kh * 16) / 8 + i) : make_uint4(0u, 0u, 0u, 0u);
+                wr[2 * i] = quant4_e4m3(raw.x, raw.y, q_scale);
+                wr[2 * i + 1] = quant4_e4m3(raw.z, raw.w, q_scale);
+            }
+            tmem_st_32x32b_x4(tmem + lane_base + kF8TmemQRope + 4 * kh, wr);
+            tmem_wait_st();
+            ptx::tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&bar.q_full);
+        }
+        const float cscale = scale * q_scale * k_scale * kLog2e;
+        const uint32_t x_peer0 = map_to_rank(ptx::smem_addr(xs), peer) + (kh * 8 * kHeadsPerCta + head) * 16;
+        float m_run = -INFINITY, l_run = 0.0f;
+        uint32_t sr[32];
+        auto fetch_send = [&](int u) -> bool {
+            const int su = u % kF8Stages;
+            const int bu = u & 1;
+            const uint32_t pu = (u >> 1) & 1;
+            if (threadIdx.x == 0) ptx::mbar_arrive_expect_tx(&bar.x_full[bu], kXBytes);
+            if (!ptx::mbar_wait(&bar.s_full[bu], pu, deadline)) return false;
+            if (!ptx::mbar_wait(&bar.kv_full[su], (u / kF8Stages) & 1, deadline)) return false;
+            ptx::tc_fence_after_sync();
+            ptx::tmem_ld_32x32b_x32(tmem + lane_base + kTmemS + bu * kKeysPerTile + kh * 32, sr);
+            ptx::tmem_wait_ld();
+            if (u >= 2 && !ptx::mbar_wait(&bar.x_free[bu], pu ^ 1u, deadline)) return false;
+            if (threadIdx.x == 0) ptx::mbar_arrive_expect_tx(&bar.x_free[bu], kSoftmaxWarps * 4);
+            const uint32_t xp = x_peer0 + bu * kXBytes;
+            const uint32_t xf_peer = map_to_rank(ptx::smem_addr(&bar.x_full[bu]), peer);
+#pragma unroll
+            for (int kq = 0; kq < 8; ++kq)
+                st_async_v4(xp + kq * (kHeadsPerCta * 16), __uint_as_float(sr[4 * kq]), __uint_as_float(sr[4 * kq + 1]),
+                            __uint_as_float(sr[4 * kq + 2]), __uint_as_float(sr[4 * kq + 3]), xf_peer);
+            return true;
+        };
+        if (ntiles > 0 && !fetch_send(0)) timed_out = true;
+        for (int t = 0; t < ntiles && !timed_out; ++t) {
+            const int s = t % kF8Stages;
+            const int bb = t & 1;
+            const uint32_t ph = (t >> 1) & 1;
+            if (!ptx::mbar_wait(&bar.x_full[bb], ph, deadline)) { timed_out = true; break; }
+            {
+                const float* xr = xs + bb * (kXBytes / 4) + (kh * 8 * kHeadsPerCta + head) * 4;
+#pragma unroll
+                for (int kq = 0; kq < 8; ++kq) {
+                    const float4 o = *reinterpret_cast<const float4*>(xr + kq * (kHeadsPerCta * 4));
+                    sr[4 * kq + 0] = __float_as_uint(__uint_as_float(sr[4 * kq + 0]) + o.x);
+                    sr[4 * kq + 1] = __float_as_uint(__uint_as_float(sr[4 * kq + 1]) + o.y);
+                    sr[4 * kq + 2] = __float_as_uint(__uint_as_float(sr[4 * kq + 2]) + o.z);
+                    sr[4 * kq + 3] = __float_as_uint(__uint_as_float(sr[4 * kq + 3]) + o.w);
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                st_async_b32(map_to_rank(ptx::smem_addr(&bar.x_sink[bb][warp]), peer), 1u,
+                             map_to_rank(ptx::smem_addr(&bar.x_free[bb]), peer));
+            const uint32_t vbits = bar.valid[s][2 * kh] | (bar.valid[s][2 * kh + 1] << 16);
+            float tmax = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float sv = ((vbits >> i) & 1u) ? __uint_as_float(sr[i]) * cscale : -INFINITY;
+                sr[i] = __float_as_uint(sv);
+                tmax = fmaxf(tmax, sv);
+            }
+            bar.tmax[bb][kh][head] = tmax;
+            ptx::mbar_arrive(&bar.pair[quad]);
+            if (!ptx::mbar_wait(&bar.pair[quad], t & 1, deadline)) { timed_out = true; break; }
+            tmax = fmaxf(tmax, bar.tmax[bb][kh ^ 1][head]);
+            const bool grow = tmax > m_run + kRescaleThreshold || (m_run == -INFINITY && tmax > -INFINITY);
+            const float m_new = grow ? tmax : m_run;
+            const float alpha = grow ? ((m_run == -INFINITY) ? 0.0f : exp2f(m_run - m_new)) : 1.0f;
+            if (t > 0 && __any_sync(0xffffffffu, grow)) {
+                if (!ptx::mbar_wait(&bar.s_free[(t - 1) & 1], ((t - 1) >> 1) & 1, deadline)) { timed_out = true; break; }
+                ptx::tc_fence_after_sync();
+#pragma unroll 1
+                for (int cc = kh * 128; cc < kh * 128 + 128; cc += 32) {
+                    uint32_t o[32];
+                    ptx::tmem_ld_32x32b_x32(tmem + lane_base + cc, o);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st_32x32b_x32(tmem + lane_base + cc, o);
+                }
+                tmem_wait_st();
+            }
+            l_run *= alpha;
+            m_run = m_new;
+            float psum = 0.0f;
+            uint32_t pk[16];
+            const bool any = m_run != -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                const float p0 = any ? fast_exp2(__uint_as_float(sr[i]) - m_run) : 0.0f;
+                const float p1 = any ? fast_exp2(__uint_as_float(sr[i + 1]) - m_run) : 0.0f;
+                psum += p0 + p1;
+                pk[i / 2] = pack_bf16x2(p0, p1);
+            }
+            l_run += psum;
+            tmem_st_32x32b_x16(tmem + lane_base + kTmemS + bb * kKeysPerTile + kh * 16, pk);
+            tmem_wait_st();
+            ptx::tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&bar.p_full[bb]);
+            if (t + 1 < ntiles && !fetch_send(t + 1)) { timed_out = true; break; }
+        }
+        if (!timed_out) {
+            for (int t = (ntiles >= 2 ? ntiles - 2 : 0); t < ntiles; ++t)
+                if (!ptx::mbar_wait(&bar.x_free[t & 1], (t >> 1) & 1, deadline)) { timed_out = true; break; }
+        }
+        bar.lsum[kh][head] = l_run;
+        ptx::mbar_arrive(&bar.pair[quad]);
+        if (!timed_out && !ptx::mbar_wait(&bar.pair[quad], ntiles & 1, deadline)) timed_out = true;
+        const float l_tot = l_run + bar.lsum[kh ^ 1][head];
+        bool have_o = ntiles > 0 && !timed_out;
+        if (have_o && !ptx::mbar_wait(&bar.o_full, 0, deadline)) { timed_out = true; have_o = false; }
+        ptx::tc_fence_after_sync();
+        const float inv_l = l_tot > 0.0f ? k_scale / l_tot : 0.0f;   // the values are codes times k_scale
+        const float lse = l_tot > 0.0f ? (m_run + log2f(l_tot)) / kLog2e : -INFINITY;
+        const bool write_head = head < H;
+        const int64_t rh = static_cast<int64_t>(r) * H + head;
+        if (splits == 1) {
+            uint16_t* dst = out + rh * kValueDim + half * kHalfDims;
+#pragma unroll 1
+            for (int cc = kh * 128; cc < kh * 128 + 128; cc += 32) {
+                uint32_t o[32];
+                if (have_o) {
+                    ptx::tmem_ld_32x32b_x32(tmem + lane_base + cc, o);
+                    ptx::tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = 0u;
+                }
+                if (write_head) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) {
+                        uint4 wv;
+                        wv.x = pack_bf16x2(__uint_as_float(o[i]) * inv_l, __uint_as_float(o[i + 1]) * inv_l);
+                        wv.y = pack_bf16x2(__uint_as_float(o[i + 2]) * inv_l, __uint_as_float(o[i + 3]) * inv_l);
+                        wv.z = pack_bf16x2(__uint_as_float(o[i + 4]) * inv_l, __uint_as_float(o[i + 5]) * inv_l);
+                        wv.w = pack_bf16x2(__uint_as_float(o[i + 6]) * inv_l, __uint_as_float(o[i + 7]) * inv_l);
+                        *reinterpret_cast<uint4*>(dst + cc + i) = wv;
+                    }
+                }
+            }
+            if (write_head && half == 0 && kh == 0 && lse_out != nullptr) lse_out[rh] = lse;
+        } else {
+            float* dst = part_o + (rh * splits + split) * kValueDim + half * kHalfDims;
+#pragma unroll 1
+            for (int cc = kh * 128; cc < kh * 128 + 128; cc += 32) {
+                uint32_t o[32];
+                if (have_o) {
+                    ptx::tmem_ld_32x32b_x32(tmem + lane_base + cc, o);
+                    ptx::tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = 0u;
+                }
+                if (write_head) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        *reinterpret_cast<float4*>(dst + cc + i) =
+                            make_float4(__uint_as_float(o[i]) * inv_l, __uint_as_float(o[i + 1]) * inv_l,
+                                        __uint_as_float(o[i + 2]) * inv_l, __uint_as_float(o[i + 3]) * inv_l);
+                }
+            }
+            if (write_head && half == 0 && kh == 0) part_lse[rh * splits + split] = lse;
+        }
+    }
+    if (timed_out) raise_error(err, DSA_DEVERR_TIMEOUT);
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        ptx::tc_fence_after_sync();
+        ptx::tmem_dealloc(tmem, kTmemCols);
+    }
+    cluster_sync_all();
+}
+
 __global__ void __launch_bounds__(128)
 sparse_mla_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse, int splits,
                           uint16_t* __restrict__ out, float* __restrict__ lse) {
@@ -732,6 +1208,63 @@ extern "C" dsa_status dsa_sparse_mla_decode(const void* q_bf16, const void* kv_p
                            static_cast<const uint16_t*>(q_bf16), num_pages, block_table, static_cast<int>(max_pages),
                            seq_lens, cu_q, static_cast<int>(B), idx, static_cast<int>(k), static_cast<int>(H), scale,
                            splits, static_cast<uint16_t*>(out_bf16), lse, part_o, part_lse, dev_err) != cudaSuccess)
+        return DSA_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
+    if (splits > 1) {
+        sparse_mla_combine_kernel<<<static_cast<unsigned>(static_cast<int64_t>(T) * H), 128, 0, s>>>(
+            part_o, part_lse, splits, static_cast<uint16_t*>(out_bf16), lse);
+        if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
+    }
+    return DSA_OK;
+}
+
+extern "C" dsa_status dsa_sparse_mla_decode_fp8(const void* q_bf16, float q_scale, const uint8_t* kv_pool_fp8,
+                                                float k_scale, int64_t num_pages, const int32_t* block_table,
+                                                int32_t max_pages, const int32_t* seq_lens, const int32_t* cu_q,
+                                                int32_t B, const int32_t* idx, int32_t k, int32_t T, int32_t H,
+                                                float scale, void* out_bf16, float* lse, void* workspace,
+                                                size_t workspace_bytes, int32_t* dev_err, void* stream) {
+    using namespace dsa;
+    if (k < 1 || k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
+    if (H != 16 && H != 32 && H != 64 && H != 128) return DSA_ERR_UNSUPPORTED;
+    if (T < 0 || B < 0 || max_pages < 0 || num_pages < 0) return DSA_ERR_INVALID_ARG;
+    if (T == 0) return DSA_OK;
+    if (num_pages < 1) return DSA_ERR_INVALID_ARG;
+    if (B == 0 || !q_bf16 || !kv_pool_fp8 || !block_table || !seq_lens || !cu_q || !idx || !out_bf16)
+        return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q_bf16) || !aligned16(kv_pool_fp8) || !aligned16(out_bf16)) return DSA_ERR_INVALID_ARG;
+    if (!(scale > 0.0f) || !(q_scale > 0.0f) || !(k_scale > 0.0f) || !(q_scale < INFINITY) || !(k_scale < INFINITY) ||
+        T > 65535)
+        return DSA_ERR_INVALID_ARG;
+    if (num_pages * kPage >= 0x7fffffffLL || static_cast<int64_t>(T) * H >= 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
+    const size_t ws_need = dsa_sparse_mla_workspace_size(T, H, k);
+    if (ws_need > 0 && (workspace == nullptr || !aligned16(workspace) || workspace_bytes < ws_need))
+        return DSA_ERR_INVALID_ARG;
+    const int splits = mla_splits(T, k);
+    float* part_o = static_cast<float*>(workspace);
+    float* part_lse = splits > 1 ? part_o + static_cast<size_t>(T) * H * splits * kValueDim : nullptr;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaFuncSetAttribute(sparse_mla_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kF8SmemBytes)) != cudaSuccess)
+        return DSA_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, splits, T);
+    cfg.blockDim = dim3(kMlaThreads, 1, 1);
+    cfg.dynamicSmemBytes = kF8SmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    if (cudaLaunchKernelEx(&cfg, sparse_mla_fp8_kernel, kv_pool_fp8, k_scale, static_cast<const uint16_t*>(q_bf16),
+                           q_scale, num_pages, block_table, static_cast<int>(max_pages), seq_lens, cu_q,
+                           static_cast<int>(B), idx, static_cast<int>(k), static_cast<int>(H), scale, splits,
+                           static_cast<uint16_t*>(out_bf16), lse, part_o, part_lse, dev_err) != cudaSuccess)
         return DSA_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
     if (splits > 1) {

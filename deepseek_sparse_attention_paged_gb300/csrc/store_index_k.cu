@@ -353,3 +353,55 @@ extern "C" dsa_status dsa_indexer_rope_q(const void* q_raw_bf16, const float* co
                                                                                     positions, T, flags, qo, dev_err);
     return dsa::launch_status();
 }
+
+// ---------------------------------------------------------------- FP8 latent cache store
+
+namespace dsa {
+namespace {
+
+// One warp per token: the 576 bf16 latent + rope values (lane l: the pairs 2 (l + 32 i), i < 9) to
+// E4M3FN codes of x / k_scale (one IEEE fp32 division, round to nearest even, saturating), written
+// to row slot & 63 of page slot >> 6 of the FP8 cache.  Follows vllm mla/common.py,
+// MLACommonImpl.forward: concat_and_cache_mla(k_c_normed, k_pe, kv_cache, slot_mapping,
+// kv_cache_dtype = "fp8", scale = layer._k_scale).
+__global__ void __launch_bounds__(256)
+store_latent_fp8_kernel(const uint32_t* __restrict__ latent, const int64_t* __restrict__ slots, int64_t n,
+                        float k_scale, uint16_t* __restrict__ pool, int64_t num_pages, int32_t* err) {
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t >= n) return;
+    const int64_t slot = __ldg(slots + t);
+    if (slot < 0) return;
+    if ((slot >> 6) >= num_pages) {
+        if (lane == 0) raise_error(err, DSA_DEVERR_SLOT_RANGE);
+        return;
+    }
+    const uint32_t* src = latent + t * (kLatentDim / 2);
+    uint16_t* dst = pool + slot * (kLatentDim / 2);
+#pragma unroll
+    for (int i = 0; i < kLatentDim / 64; ++i) {
+        const uint32_t two = __ldg(src + lane + 32 * i);
+        const __nv_fp8_storage_t c0 = __nv_cvt_float_to_fp8(__fdiv_rn(bf16_lo(two), k_scale), __NV_SATFINITE, __NV_E4M3);
+        const __nv_fp8_storage_t c1 = __nv_cvt_float_to_fp8(__fdiv_rn(bf16_hi(two), k_scale), __NV_SATFINITE, __NV_E4M3);
+        dst[lane + 32 * i] = static_cast<uint16_t>(c0) | (static_cast<uint16_t>(c1) << 8);
+    }
+}
+
+}  // namespace
+}  // namespace dsa
+
+extern "C" dsa_status dsa_store_latent_fp8(const void* latent_bf16, const int64_t* slot_mapping, int64_t n,
+                                           float k_scale, uint8_t* kv_pool_fp8, int64_t num_pages, int32_t* dev_err,
+                                           void* stream) {
+    if (n < 0 || num_pages < 0) return DSA_ERR_INVALID_ARG;
+    if (!(k_scale > 0.0f) || !(k_scale < INFINITY)) return DSA_ERR_INVALID_ARG;
+    if (n == 0) return DSA_OK;
+    if (!latent_bf16 || !slot_mapping || !kv_pool_fp8) return DSA_ERR_INVALID_ARG;
+    if (!dsa::aligned16(latent_bf16) || !dsa::aligned16(kv_pool_fp8)) return DSA_ERR_INVALID_ARG;
+    const int64_t blocks = (n + 7) / 8;
+    if (blocks > 0x7fffffffLL) return DSA_ERR_INVALID_ARG;
+    dsa::store_latent_fp8_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint32_t*>(latent_bf16), slot_mapping, n, k_scale, reinterpret_cast<uint16_t*>(kv_pool_fp8),
+        num_pages, dev_err);
+    return dsa::launch_status();
+}

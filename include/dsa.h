@@ -365,6 +365,44 @@ dsa_status dsa_sparse_mla_decode_noalloc(const void* q_bf16, const void* kv_pool
                                          void* stream);
 
 /*
+ * dsa_store_latent_fp8 -- latent rows into an FP8 latent cache (the fp8 kv-cache variant).
+ * Source: vllm mla/common.py, MLACommonImpl.forward: concat_and_cache_mla(k_c_normed, k_pe,
+ * kv_cache, slot_mapping, kv_cache_dtype = "fp8", scale = layer._k_scale), then kv_cache viewed as
+ * the fp8 dtype.
+ *   For each token t with slot = slot_mapping[t] >= 0: row slot & 63 of page slot >> 6 of the
+ *   cache gets code_d = E4M3FN(x_d / k_scale), d < 576 (x: the bf16 latent (512) + rope (64)
+ *   values; one IEEE fp32 division; round to nearest even; saturating to +-448).  One k_scale for
+ *   the whole cache (per-tensor, as the pages' layer._k_scale).
+ * Arguments:
+ *   latent_bf16   [n, 576] bf16 (16-byte aligned).   slot_mapping  int64 [n] (< 0: padding).
+ *   k_scale       > 0, finite.   kv_pool_fp8  uint8 [num_pages, 64, 576] (16-byte aligned).
+ *   dev_err       nullable; DSA_DEVERR_SLOT_RANGE for a slot past the pool (token skipped).
+ */
+dsa_status dsa_store_latent_fp8(const void* latent_bf16, const int64_t* slot_mapping, int64_t n, float k_scale,
+                                uint8_t* kv_pool_fp8, int64_t num_pages, int32_t* dev_err, void* stream);
+
+/*
+ * dsa_sparse_mla_decode_fp8 -- dsa_sparse_mla_decode over an FP8 latent cache.
+ * Source: vllm mla/common.py, MLACommonImpl.forward decode branch with fp8_attention:
+ * ops.scaled_fp8_quant(decode_ql_nope, layer._q_scale) and (decode_q_pe, layer._q_scale), then
+ * _forward_decode on the fp8 query and the fp8 cache.
+ *   The query is quantised here: qc = E4M3FN(q / q_scale) (all 576 dims, as above).  With
+ *   c = code * k_scale the cached rows and q^ = qc * q_scale the query, the result is that of
+ *   dsa_sparse_mla_decode on (q^, c): S_i = scale * <q^, c_g(i)>, P = softmax(S),
+ *   out = bf16_rn(sum_i P_i c_g(i)[0:512]), lse.  Score products are exact (E4M3 x E4M3 on the
+ *   tensor cores, fp32 accumulation); P stays bf16 and multiplies the cached values widened to bf16
+ *   (exact), so the rounding is that of the bf16 call.
+ * Arguments: as dsa_sparse_mla_decode, plus q_scale and k_scale (> 0, finite); kv_pool_fp8 is
+ * uint8 [num_pages, 64, 576] (16-byte aligned) written by dsa_store_latent_fp8.  The workspace is
+ * the bf16 call's (dsa_sparse_mla_workspace_size).
+ */
+dsa_status dsa_sparse_mla_decode_fp8(const void* q_bf16, float q_scale, const uint8_t* kv_pool_fp8, float k_scale,
+                                     int64_t num_pages, const int32_t* block_table, int32_t max_pages,
+                                     const int32_t* seq_lens, const int32_t* cu_q, int32_t B, const int32_t* idx,
+                                     int32_t k, int32_t T, int32_t H, float scale, void* out_bf16, float* lse,
+                                     void* workspace, size_t workspace_bytes, int32_t* dev_err, void* stream);
+
+/*
  * dsa_mla_absorb_q -- absorbed latent query: ql[t, n, 0:512] = q_nope[t, n, 0:128] W_UK_T[n].
  * Source: vllm mla/common.py, MLACommonImpl.forward decode branch and _q_proj_and_k_up_proj
  * (torch.bmm(q_nope as (N, B, P), W_UK_T (N, P, L)); W_UK_T = W_UK.permute(1, 2, 0) where W_UK is
