@@ -73,6 +73,7 @@ constexpr int kProducerWarp0 = 9;
 constexpr int kProducerWarps = 4;
 constexpr int kMlaThreads = 32 * (kProducerWarp0 + kProducerWarps);   // 416
 constexpr int kKeysPerProducer = kKeysPerTile / kProducerWarps;       // 16
+static_assert(kKeysPerProducer == 8 || kKeysPerProducer == 16, "copy lane maps");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = kHalfDims;                          // score buffers at columns 256 and 320
 constexpr uint32_t kTmemQ = kTmemS + 2 * kKeysPerTile;          // query chunks at columns 384 .. 511
@@ -194,6 +195,15 @@ __device__ __forceinline__ uint32_t rope_off(int i, int j) {
     return static_cast<uint32_t>((i >> 3) * 512 + j * 128 + (i & 7) * 16);
 }
 
+// Bit i: entry 32 kh + i of a tile is real, from the valid words of its producer warps.
+__device__ __forceinline__ uint32_t half_valid_bits(const uint32_t (&words)[kProducerWarps], int kh) {
+    constexpr int per_half = 32 / kKeysPerProducer;
+    uint32_t v = 0;
+#pragma unroll
+    for (int w = 0; w < per_half; ++w) v |= words[kh * per_half + w] << (w * kKeysPerProducer);
+    return v;
+}
+
 struct MlaBars {
     uint64_t q_full;               // query in TMEM / shared memory (8 softmax warps)
     uint64_t kv_full[kKvStages];   // every producer thread's cp.async landed + one arrive per producer warp
@@ -208,7 +218,7 @@ struct MlaBars {
     uint32_t x_sink[2][kSoftmaxWarps];   // targets of the peer's 4-byte consumed signals
     uint32_t tmem_slot;
     uint32_t pad;
-    uint32_t valid[kKvStages][kProducerWarps];   // bit i: entry 16 w + i of the stage's tile is real
+    uint32_t valid[kKvStages][kProducerWarps];   // bit i: entry kKeysPerProducer w + i of the stage's tile is real
     float tmax[2][2][kHeadsPerCta];   // [tile parity][key half]: this tile's maximum (shared by the warp pair)
     float lsum[2][kHeadsPerCta];   // per key half: the final partial row sums
 };
@@ -324,7 +334,7 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
                 if (t >= ntiles) break;
                 const int s = t % kKvStages;
                 const uint32_t ph = (t / kKvStages) & 1;
-                const uint32_t vbits = __ballot_sync(0xffffffffu, rows[u] >= 0) & 0xffffu;
+                const uint32_t vbits = __ballot_sync(0xffffffffu, rows[u] >= 0) & ((1u << kKeysPerProducer) - 1u);
                 const int row_src = rows[u] >= 0 ? rows[u] : 0;
                 // the stage is free once PV of its previous tile completed
                 if (lane == 0 && !ptx::mbar_wait(&bar.kv_empty[s], ph ^ 1u, deadline)) timed_out = true;
@@ -504,7 +514,7 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
             if (lane == 0)
                 st_async_b32(map_to_rank(ptx::smem_addr(&bar.x_sink[bb][warp]), peer), 1u,
                              map_to_rank(ptx::smem_addr(&bar.x_free[bb]), peer));
-            const uint32_t vbits = bar.valid[s][2 * kh] | (bar.valid[s][2 * kh + 1] << 16);
+            const uint32_t vbits = half_valid_bits(bar.valid[s], kh);
             float tmax = -INFINITY;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
@@ -640,10 +650,12 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
 // rows are E4M3 codes of x / k_scale, the decode query is quantised by ops.scaled_fp8_quant with
 // q_scale, and _forward_decode runs on the FP8 query and cache).  Same work split, swap and
 // softmax as the bf16 kernel; the differences:
-//   * a stage holds this CTA's FP8 codes of the 64 selected rows -- value dims 256 c .. + 255 as two
-//     128-byte swizzled K-major chunks, rope dims 512 + 32 c .. + 31 without swizzle -- and the same
-//     value dims widened to bf16 (exact: E4M3 values are bf16 values) in the MN-major value layout;
-//     each producer lane widens exactly the 16-byte pieces it copied, once they have landed;
+//   * a code stage (5 in a ring) holds this CTA's FP8 codes of the 64 selected rows -- value dims
+//     256 c .. + 255 as two 128-byte swizzled K-major chunks, rope dims 512 + 32 c .. + 31 without
+//     swizzle; the score MMA starts as soon as they land;
+//   * the value dims are widened to bf16 (exact: E4M3 values are bf16 values) into one of two value
+//     buffers in the MN-major value layout; each producer lane widens the 16-byte pieces it copied,
+//     three tiles after issuing them, so that three tiles of loads stay in flight meanwhile;
 //   * the score MMA is E4M3 x E4M3 (kind::f8f6f4, K = 32) with the query's codes in tensor memory
 //     (quantised there by the softmax warps with q_scale); S is scaled by scale * q_scale * k_scale;
 //   * P stays bf16 and PV stays bf16 x bf16; O is scaled by k_scale at the end.
@@ -652,13 +664,33 @@ constexpr int kF8ChunkBytes = kKeysPerTile * 128;                        // 128 
 constexpr int kF8RopeBytes = kKeysPerTile * kRopeHalf;                   // 32 rope codes per row
 constexpr int kF8CodeBytes = 2 * kF8ChunkBytes + kF8RopeBytes;           // 18432
 constexpr int kF8VBytes = kOwnChunks * kKvChunkBytes;                    // 32768: bf16 value dims
-constexpr int kF8StageBytes = kF8CodeBytes + kF8VBytes;                  // 51200
-constexpr int kF8Stages = 3;
+constexpr int kF8Stages = 5;                                             // code stages (tiles in flight)
+constexpr int kF8VBufs = 2;                                              // bf16 value buffers
+constexpr int kF8Lag = 3;                                                // a tile is widened 3 issues after its own
 constexpr uint32_t kF8TmemQRope = kTmemQ + 64;                           // query codes: value 64 + rope 8 columns
-constexpr size_t kF8SmemBytes = 1024 + size_t(kF8Stages) * kF8StageBytes + 2 * size_t(kXBytes) + kBarBytes;
-static_assert(kF8CodeBytes % 1024 == 0 && kF8StageBytes % 1024 == 0, "1024-byte alignment of the swizzled parts");
-static_assert(kF8Stages <= kKvStages, "barrier arrays");
+constexpr size_t kF8SmemBytes = 1024 + size_t(kF8Stages) * kF8CodeBytes + size_t(kF8VBufs) * kF8VBytes +
+                                2 * size_t(kXBytes) + kBarBytes;
+static_assert(kF8CodeBytes % 1024 == 0 && kF8VBytes % 1024 == 0, "1024-byte alignment of the swizzled parts");
+static_assert(kF8Lag < kF8Stages, "a tile is widened before its code stage is refilled");
 static_assert(kF8SmemBytes <= 232448, "shared-memory budget");
+
+struct Mla8Bars {
+    uint64_t q_full;               // query codes in TMEM (8 softmax warps)
+    uint64_t k_full[kF8Stages];    // every producer thread's cp.async landed + one arrive per producer warp
+    uint64_t k_empty[kF8Stages];   // score MMAs done (1), codes widened (4 producer warps), valid bits read (8 warps)
+    uint64_t v_full[kF8VBufs];     // values widened to bf16 (4 producer warps)
+    uint64_t v_empty[kF8VBufs];    // PV that read the buffer completed
+    uint64_t s_full[2], s_free[2], p_full[2], x_full[2], x_free[2];   // as in the bf16 kernel
+    uint64_t o_full;
+    uint64_t pair[4];
+    uint32_t x_sink[2][kSoftmaxWarps];
+    uint32_t tmem_slot;
+    uint32_t pad;
+    uint32_t valid[kF8Stages][kProducerWarps];
+    float tmax[2][2][kHeadsPerCta];
+    float lsum[2][kHeadsPerCta];
+};
+static_assert(sizeof(Mla8Bars) <= kBarBytes, "barrier block");
 
 // Byte offset of 16-byte piece p (codes 16 p .. 16 p + 15) of row i of the rope codes: K-major without
 // swizzle, rows of 32 bytes = two core matrices, 8-row groups 256 bytes apart.
@@ -693,11 +725,18 @@ __device__ __forceinline__ uint32_t quant4_e4m3(uint32_t lo, uint32_t hi, float 
     return w;
 }
 
-// Two E4M3 codes -> two bf16 (exact).
+// Two E4M3 codes -> two bf16 (exact) with one conversion instruction.  The codes are widened to
+// f16 (exact); every finite E4M3 value is a normal f16 whose low 7 mantissa bits are zero, so
+// moving each half's exponent and mantissa right by 3 bits gives the bf16 bits of value * 2^-112
+// (a normal bf16, smallest 2^-121), and one bf16 multiply by 2^112 (exact) restores the value.
+// Zeros keep their sign.  The NaN codes 0x7F / 0xFF are never written by the latent store
+// (saturating quantisation) and are not decoded faithfully here.
 __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t two) {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
-    const float a = __half2float(__ushort_as_half(h.x)), b = __half2float(__ushort_as_half(h.y));
-    return pack_bf16x2(a, b);
+    uint32_t h, d;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(two));
+    const uint32_t t = ((h & 0x7fff7fffu) >> 3) | (h & 0x80008000u);
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(t), "r"(0x77807780u));   // 2^112 = bf16 0x7780
+    return d;
 }
 
 __global__ void __launch_bounds__(kMlaThreads, 1)
@@ -709,9 +748,10 @@ sparse_mla_fp8_kernel(const uint8_t* __restrict__ kv8, float k_scale, const uint
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw_addr = ptx::smem_addr(smem_raw);
     unsigned char* base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-    unsigned char* kvs = base;                                                   // [3][codes 18 KB | bf16 values 32 KB]
-    float* xs = reinterpret_cast<float*>(kvs + kF8Stages * kF8StageBytes);       // [2][2 halves][8 quads][128 heads][4]
-    MlaBars& bar = *reinterpret_cast<MlaBars*>(reinterpret_cast<unsigned char*>(xs) + 2 * kXBytes);
+    unsigned char* kvs = base;                                                   // [5][codes 18 KB]
+    unsigned char* vbs = kvs + kF8Stages * kF8CodeBytes;                         // [2][bf16 values 32 KB]
+    float* xs = reinterpret_cast<float*>(vbs + kF8VBufs * kF8VBytes);            // [2][2 halves][8 quads][128 heads][4]
+    Mla8Bars& bar = *reinterpret_cast<Mla8Bars*>(reinterpret_cast<unsigned char*>(xs) + 2 * kXBytes);
 
     const int split = blockIdx.y;
     const int r = blockIdx.z;
@@ -730,8 +770,12 @@ sparse_mla_fp8_kernel(const uint8_t* __restrict__ kv8, float k_scale, const uint
     if (threadIdx.x == 0) {
         ptx::mbar_init(&bar.q_full, kSoftmaxWarps);
         for (int s = 0; s < kF8Stages; ++s) {
-            ptx::mbar_init(&bar.kv_full[s], kProducerWarps);   // each producer warp once its rows are widened
-            ptx::mbar_init(&bar.kv_empty[s], 1);
+            ptx::mbar_init(&bar.k_full[s], kProducerWarps * 32 + kProducerWarps);
+            ptx::mbar_init(&bar.k_empty[s], 1 + kProducerWarps + kSoftmaxWarps);
+        }
+        for (int s = 0; s < kF8VBufs; ++s) {
+            ptx::mbar_init(&bar.v_full[s], kProducerWarps);
+            ptx::mbar_init(&bar.v_empty[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(&bar.s_full[a], 1);
@@ -776,11 +820,16 @@ sparse_mla_fp8_kernel(const uint8_t* __restrict__ kv8, float k_scale, const uint
             if (page < 0 || page >= num_pages) { raise_error(err, DSA_DEVERR_PAGE_RANGE); return -1; }
             return page * kPage + (pos & 63);
         };
-        // widen this lane's value pieces of tile u (the 16-byte pieces it copied) to bf16, then the
-        // warp's arrival on the stage's full barrier
-        auto widen = [&](int u) {
-            const uint32_t st = kv_addr0 + (u % kF8Stages) * kF8StageBytes;
-            const unsigned char* sp = kvs + (u % kF8Stages) * kF8StageBytes;
+        // widen this lane's value pieces of tile u (the 16-byte pieces it copied, landed) to bf16 in
+        // value buffer u % 2 once the PV of tile u - 2 has released it; then the warp's arrivals on
+        // the buffer's full barrier and on the code stage's empty barrier
+        auto widen = [&](int u) -> bool {
+            const int vi = u % kF8VBufs;
+            if (lane == 0 && !ptx::mbar_wait(&bar.v_empty[vi], ((u / kF8VBufs) & 1) ^ 1u, deadline)) timed_out = true;
+            timed_out = __shfl_sync(0xffffffffu, timed_out ? 1 : 0, 0) != 0;
+            if (timed_out) return false;
+            const unsigned char* sp = kvs + (u % kF8Stages) * kF8CodeBytes;
+            unsigned char* vp = vbs + vi * kF8VBytes;
 #pragma unroll
             for (int kq = 0; kq < kKeysPerProducer / 2; ++kq) {
                 const int key = pw * kKeysPerProducer + 2 * kq + (lane >> 4);
@@ -797,14 +846,17 @@ sparse_mla_fp8_kernel(const uint8_t* __restrict__ kv8, float k_scale, const uint
                 hi.z = e4m3x2_to_bf16x2(static_cast<uint16_t>(c.w));
                 hi.w = e4m3x2_to_bf16x2(static_cast<uint16_t>(c.w >> 16));
                 // dims 16 j .. 16 j + 7 and 16 j + 8 .. 16 j + 15: chunk j / 4 of 64 dims, pieces 2 (j % 4), + 1
-                unsigned char* vb = const_cast<unsigned char*>(sp) + kF8CodeBytes + (j >> 2) * kKvChunkBytes + key * 128;
-                *reinterpret_cast<uint4*>(vb + (((2 * (j & 3)) ^ (key & 7)) << 4)) = lo;
-                *reinterpret_cast<uint4*>(vb + (((2 * (j & 3) + 1) ^ (key & 7)) << 4)) = hi;
+                unsigned char* vrow = vp + (j >> 2) * kKvChunkBytes + key * 128;
+                *reinterpret_cast<uint4*>(vrow + (((2 * (j & 3)) ^ (key & 7)) << 4)) = lo;
+                *reinterpret_cast<uint4*>(vrow + (((2 * (j & 3) + 1) ^ (key & 7)) << 4)) = hi;
             }
-            (void)st;
             ptx::fence_proxy_async_smem();   // the bf16 values are read by the tensor cores
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&bar.kv_full[u % kF8Stages]);
+            if (lane == 0) {
+                ptx::mbar_arrive(&bar.v_full[vi]);
+                ptx::mbar_arrive(&bar.k_empty[u % kF8Stages]);
+            }
+            return true;
         };
         int pos1[kBatch], page1[kBatch], pos2[kBatch];
 #pragma unroll
@@ -832,12 +884,12 @@ sparse_mla_fp8_kernel(const uint8_t* __restrict__ kv8, float k_scale, const uint
                 if (t >= ntiles) break;
                 const int s = t % kF8Stages;
                 const uint32_t ph = (t / kF8Stages) & 1;
-                const uint32_t vbits = __ballot_sync(0xffffffffu, rows[u] >= 0) & 0xffffu;
+                const uint32_t vbits = __ballot_sync(0xffffffffu, rows[u] >= 0) & ((1u << kKeysPerProducer) - 1u);
                 const int row_src = rows[u] >= 0 ? rows[u] : 0;
-                if (lane == 0 && !ptx::mbar_wait(&bar.kv_empty[s], ph ^ 1u, deadline)) timed_out = true;
+                if (lane == 0 && !ptx::mbar_wait(&bar.k_empty[s], ph ^ 1u, deadline)) timed_out = true;
                 timed_out = __shfl_sync(0xffffffffu, timed_out ? 1 : 0, 0) != 0;
                 if (timed_out) break;
-                const uint32_t stage = kv_addr0 + s * kF8StageBytes;
+                const uint32_t stage = kv_addr0 + s * kF8CodeBytes;
 #pragma unroll
                 for (int kq = 0; kq < kKeysPerProducer / 2; ++kq) {
                     const int kl = 2 * kq + (lane >> 4);
@@ -848,21 +900,27 @@ sparse_mla_fp8_kernel(const uint8_t* __restrict__ kv8, float k_scale, const uint
                                 kv_val + row * kLatentDim);
                 }
                 {
-                    const int kl = lane >> 1;
+                    const int kl = lane >> 1;   // two 16-byte rope pieces per key
                     const int key = pw * kKeysPerProducer + kl;
-                    const int64_t row = __shfl_sync(0xffffffffu, row_src, kl);
-                    cp_async_16(stage + 2 * kF8ChunkBytes + rope8_off(key, lane & 1), kv_rope + row * kLatentDim);
+                    const int64_t row = __shfl_sync(0xffffffffu, row_src, kl & (kKeysPerProducer - 1));
+                    if (kl < kKeysPerProducer)
+                        cp_async_16(stage + 2 * kF8ChunkBytes + rope8_off(key, lane & 1), kv_rope + row * kLatentDim);
                 }
                 asm volatile("cp.async.commit_group;" ::: "memory");
-                if (lane == 0) bar.valid[s][pw] = vbits;
-                if (t >= 1) {
-                    asm volatile("cp.async.wait_group 1;" ::: "memory");   // this lane's copies of tile t - 1 landed
-                    widen(t - 1);
+                cp_async_arrive_noinc(&bar.k_full[s]);
+                if (lane == 0) {
+                    bar.valid[s][pw] = vbits;
+                    ptx::mbar_arrive(&bar.k_full[s]);
+                }
+                if (t >= kF8Lag) {
+                    asm volatile("cp.async.wait_group 3;" ::: "memory");   // this lane's copies of tile t - 3 landed
+                    if (!widen(t - kF8Lag)) break;
                 }
             }
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
-        if (!timed_out && ntiles > 0) widen(ntiles - 1);
+        for (int u = ntiles > kF8Lag ? ntiles - kF8Lag : 0; u < ntiles && !timed_out; ++u)
+            if (!widen(u)) break;
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
@@ -872,11 +930,11 @@ sparse_mla_fp8_kernel(const uint8_t* __restrict__ kv8, float k_scale, const uint
             int tq = 0, tp = 0;
             while (ok && tp < ntiles) {
                 bool issued = false;
-                if (tq < ntiles && ptx::mbar_test_wait(&bar.kv_full[tq % kF8Stages], (tq / kF8Stages) & 1) &&
+                if (tq < ntiles && ptx::mbar_test_wait(&bar.k_full[tq % kF8Stages], (tq / kF8Stages) & 1) &&
                     ptx::mbar_test_wait(&bar.s_free[tq & 1], ((tq >> 1) & 1) ^ 1u)) {
                     ptx::fence_proxy_async_smem();
                     ptx::tc_fence_after_sync();
-                    const uint32_t kb = kv_addr0 + (tq % kF8Stages) * kF8StageBytes;
+                    const uint32_t kb = kv_addr0 + (tq % kF8Stages) * kF8CodeBytes;
                     const uint32_t d = tmem + kTmemS + (tq & 1) * kKeysPerTile;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
@@ -886,20 +944,21 @@ sparse_mla_fp8_kernel(const uint8_t* __restrict__ kv8, float k_scale, const uint
                     umma_f8_ts(d, tmem + kF8TmemQRope, make_desc(kb + 2 * kF8ChunkBytes, 128, 256, kLayoutNone), idesc_qk,
                                1u);
                     ptx::umma_commit(&bar.s_full[tq & 1]);
+                    ptx::umma_commit(&bar.k_empty[tq % kF8Stages]);
                     ++tq;
                     issued = true;
                 }
-                if (tp < tq && ptx::mbar_test_wait(&bar.p_full[tp & 1], (tp >> 1) & 1)) {
+                if (tp < tq && ptx::mbar_test_wait(&bar.p_full[tp & 1], (tp >> 1) & 1) &&
+                    ptx::mbar_test_wait(&bar.v_full[tp % kF8VBufs], (tp / kF8VBufs) & 1)) {
                     ptx::tc_fence_after_sync();
-                    const int s = tp % kF8Stages;
-                    const uint32_t vb = kv_addr0 + s * kF8StageBytes + kF8CodeBytes;
+                    const uint32_t vb = ptx::smem_addr(vbs) + (tp % kF8VBufs) * kF8VBytes;
                     const uint32_t pa = tmem + kTmemS + (tp & 1) * kKeysPerTile;
 #pragma unroll
                     for (int ks = 0; ks < kKeysPerTile / 16; ++ks) {
                         const uint64_t db = make_desc(vb + ks * 16 * 128, kKvChunkBytes, 1024, kLayoutSw128);
                         umma_f16_ts(tmem, pa + ks * 8, db, idesc_pv, (tp | ks) != 0 ? 1u : 0u);
                     }
-                    ptx::umma_commit(&bar.kv_empty[s]);
+                    ptx::umma_commit(&bar.v_empty[tp % kF8VBufs]);
                     ptx::umma_commit(&bar.s_free[tp & 1]);
                     ++tp;
                     issued = true;
@@ -946,13 +1005,17 @@ sparse_mla_fp8_kernel(const uint8_t* __restrict__ kv8, float k_scale, const uint
         const uint32_t x_peer0 = map_to_rank(ptx::smem_addr(xs), peer) + (kh * 8 * kHeadsPerCta + head) * 16;
         float m_run = -INFINITY, l_run = 0.0f;
         uint32_t sr[32];
+        uint32_t vbits_next = 0;   // valid bits of the fetched tile, read before its code stage is released
         auto fetch_send = [&](int u) -> bool {
             const int su = u % kF8Stages;
             const int bu = u & 1;
             const uint32_t pu = (u >> 1) & 1;
             if (threadIdx.x == 0) ptx::mbar_arrive_expect_tx(&bar.x_full[bu], kXBytes);
             if (!ptx::mbar_wait(&bar.s_full[bu], pu, deadline)) return false;
-            if (!ptx::mbar_wait(&bar.kv_full[su], (u / kF8Stages) & 1, deadline)) return false;
+            if (!ptx::mbar_wait(&bar.k_full[su], (u / kF8Stages) & 1, deadline)) return false;
+            vbits_next = half_valid_bits(bar.valid[su], kh);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&bar.k_empty[su]);
             ptx::tc_fence_after_sync();
             ptx::tmem_ld_32x32b_x32(tmem + lane_base + kTmemS + bu * kKeysPerTile + kh * 32, sr);
             ptx::tmem_wait_ld();
@@ -968,9 +1031,9 @@ sparse_mla_fp8_kernel(const uint8_t* __restrict__ kv8, float k_scale, const uint
         };
         if (ntiles > 0 && !fetch_send(0)) timed_out = true;
         for (int t = 0; t < ntiles && !timed_out; ++t) {
-            const int s = t % kF8Stages;
             const int bb = t & 1;
             const uint32_t ph = (t >> 1) & 1;
+            const uint32_t vbits = vbits_next;
             if (!ptx::mbar_wait(&bar.x_full[bb], ph, deadline)) { timed_out = true; break; }
             {
                 const float* xr = xs + bb * (kXBytes / 4) + (kh * 8 * kHeadsPerCta + head) * 4;
@@ -987,7 +1050,6 @@ sparse_mla_fp8_kernel(const uint8_t* __restrict__ kv8, float k_scale, const uint
             if (lane == 0)
                 st_async_b32(map_to_rank(ptx::smem_addr(&bar.x_sink[bb][warp]), peer), 1u,
                              map_to_rank(ptx::smem_addr(&bar.x_free[bb]), peer));
-            const uint32_t vbits = bar.valid[s][2 * kh] | (bar.valid[s][2 * kh + 1] << 16);
             float tmax = -INFINITY;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
