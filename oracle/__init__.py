@@ -29,6 +29,7 @@ DI = 128
 HI = 64
 ROW_BYTES = 132
 PAGE_BYTES = PAGE * ROW_BYTES
+C8_PAGE_BYTES = PAGE * DI + PAGE * 2      # int8 cache page: 64 x 128 codes + 64 fp16 scales
 DQK = 576
 DV = 512
 
@@ -101,6 +102,12 @@ def _load():
         "dsa_oracle_sparse_mla_fp8": (i64, [P, ctypes.c_float, P, ctypes.c_float, i64, P, i32, P, P, i32, P, i32, i32,
                                             f64, P, i64, P, P]),
         "dsa_oracle_lse_merge": (None, [P, P, P, P, i64, i32, P, P]),
+        "dsa_oracle_f16_decode": (f64, [ctypes.c_uint16]),
+        "dsa_oracle_f32_to_f16": (ctypes.c_uint16, [ctypes.c_float]),
+        "dsa_oracle_c8_rotate128": (None, [P, P]),
+        "dsa_oracle_quant_int8": (None, [P, ctypes.c_int, P, P]),
+        "dsa_oracle_store_index_k_c8": (i64, [P, P, i64, P, i64]),
+        "dsa_oracle_indexer_logits_c8": (i64, [P, P, P, i64, P, i32, P, P, i32, P, i64, P, i64, P]),
         "dsa_oracle_num_threads": (ctypes.c_int, []),
         "dsa_oracle_set_num_threads": (None, [ctypes.c_int]),
     }
@@ -321,6 +328,60 @@ def sparse_mla(q_bf16, kv_bf16, block_table, seq_lens, cu_q, idx, scale, rows, w
     if want_psum:
         return out, lse, psum, int(bad)
     return out, lse
+
+
+def f16_decode(h: int) -> float:
+    return _load().dsa_oracle_f16_decode(int(h))
+
+
+def f32_to_f16(x: float) -> int:
+    return int(_load().dsa_oracle_f32_to_f16(float(x)))
+
+
+def c8_rotate128(x_bf16: np.ndarray) -> np.ndarray:
+    """The c8 rotation of one bf16 128-vector (bits): bf16(x @ (bf16 Hadamard / sqrt(128)))."""
+    x = _c(x_bf16, np.uint16)
+    assert x.size == DI
+    out = np.empty(DI, np.uint16)
+    _load().dsa_oracle_c8_rotate128(_p(x), _p(out))
+    return out
+
+
+def quant_int8(y: np.ndarray):
+    """Dynamic int8 quantisation of one fp32 vector: (codes int8, fp32 scale)."""
+    yy = _c(y, np.float32)
+    codes = np.empty(yy.size, np.int8)
+    sc = np.empty(1, np.float32)
+    _load().dsa_oracle_quant_int8(_p(yy), yy.size, _p(codes), _p(sc))
+    return codes, float(sc[0])
+
+
+def store_index_k_c8(k_bf16: np.ndarray, slot_mapping: np.ndarray, pool: np.ndarray) -> int:
+    """Keys [n, 128] (bf16 bits) into the int8 cache ``pool`` (uint8 [num_pages, C8_PAGE_BYTES]) by slot."""
+    k = _c(k_bf16, np.uint16).reshape(-1, DI)
+    slots = _c(slot_mapping, np.int64)
+    assert pool.dtype == np.uint8 and pool.flags["C_CONTIGUOUS"] and pool.shape[1] == C8_PAGE_BYTES
+    return int(_load().dsa_oracle_store_index_k_c8(_p(k), _p(slots), k.shape[0], _p(pool), pool.shape[0]))
+
+
+def indexer_logits_c8(q_bf16, w, pool, block_table, seq_lens, cu_q, rows, ld, want_mag=False):
+    """Logits over the int8 cache for the listed rows: fp32 [n, ld] (NaN where not written)."""
+    q = _c(q_bf16, np.uint16)
+    ww = _c(w, np.float32)
+    pl = _c(pool, np.uint8)
+    assert pl.shape[1] == C8_PAGE_BYTES
+    bt = _c(block_table, np.int32)
+    sl = _c(seq_lens, np.int32)
+    cq = _c(cu_q, np.int32)
+    rw = _c(rows, np.int64)
+    out = np.full((rw.size, ld), np.nan, np.float32)
+    mag = np.full((rw.size, ld), np.nan, np.float64) if want_mag else None
+    bad = _load().dsa_oracle_indexer_logits_c8(_p(q), _p(ww), _p(pl), pl.shape[0], _p(bt), bt.shape[1], _p(sl),
+                                              _p(cq), sl.size, _p(rw), rw.size, _p(out), ld,
+                                              _p(mag) if want_mag else None)
+    if want_mag:
+        return out, mag, int(bad)
+    return out, int(bad)
 
 
 def quant_fp8_tensor(x_bf16: np.ndarray, scale: float) -> np.ndarray:

@@ -39,6 +39,7 @@
 #define PAGE_BYTES (PAGE * ROW_BYTES)
 #define DQK 576          /* absorbed MLA query/key width: 512 latent + 64 rope ([mla] head size 576) */
 #define DV 512           /* latent value width */
+#define C8_PAGE_BYTES (PAGE * DI + PAGE * 2)   /* int8 cache page: 64 x 128 codes + 64 fp16 scales */
 
 /* ---------------------------------------------------------------- number formats */
 
@@ -425,6 +426,183 @@ int64_t dsa_oracle_indexer_logits(const uint16_t* q_bf16, const float* w, const 
                 double dot = 0.0;
                 for (int d = 0; d < DI; ++d) dot += dq[h][d] * dk[d];
                 double relu = (double)ks * dot;
+                if (relu < 0.0) relu = 0.0;
+                acc += wq[h] * relu;
+                accm += fabs(wq[h]) * relu;
+            }
+            logits[i * ld + s] = (float)acc;
+            if (mag) mag[i * ld + s] = accm;
+        }
+        bad += row_bad;
+    }
+    return bad;
+}
+
+/* ---------------------------------------------------------------- int8 ("c8") index-K cache */
+
+/* IEEE binary16 (torch.float16): 1 sign bit, 5 exponent bits with bias 15, 10 mantissa bits;
+ * exponent field 0 encodes subnormals m * 2^-24; field 31 encodes infinity (m = 0) and NaN. */
+double dsa_oracle_f16_decode(uint16_t h) {
+    int e = (h >> 10) & 31, m = h & 1023;
+    double v;
+    if (e == 0) v = ldexp((double)m, -24);
+    else if (e == 31) v = m ? NAN : INFINITY;
+    else v = ldexp((double)(1024 + m), e - 25);
+    return (h & 0x8000) ? -v : v;
+}
+
+/* fp32 -> fp16, round to nearest with ties to even, overflow to infinity (the IEEE default that
+ * torch's .to(float16) follows).  From the definition: the fp16 grid spacing in the binade of |x|
+ * is 2^(e-10) for exponents e >= -14 and 2^-24 below (subnormals); divide by it (exact, a power of
+ * two), round to an integer with ties to even, multiply back, and encode that value (a carry into
+ * the next binade is encoded there; anything from 65520 up has become infinity). */
+uint16_t dsa_oracle_f32_to_f16(float x) {
+    const uint16_t sign = signbit(x) ? 0x8000 : 0;
+    if (isnan(x)) return 0x7e00;
+    if (isinf(x)) return sign | 0x7c00;
+    const double a = fabs((double)x);
+    if (a == 0.0) return sign;
+    int e;
+    frexp(a, &e);                    /* a in [2^(e-1), 2^e) */
+    int ue = e - 1;
+    if (ue < -14) ue = -14;
+    const double ulp = ldexp(1.0, ue - 10);
+    const double v = nearbyint(a / ulp) * ulp;   /* default rounding mode: nearest, ties to even */
+    if (v < ldexp(1.0, -14)) return sign | (uint16_t)(v / ldexp(1.0, -24));
+    frexp(v, &e);
+    ue = e - 1;
+    if (ue > 15) return sign | 0x7c00;
+    const int m = (int)(v / ldexp(1.0, ue - 10)) - 1024;
+    return sign | (uint16_t)(((ue + 15) << 10) | m);
+}
+
+/* The c8 rotation ([sfa] AscendSFAImpl: qk_hadamard = torch.tensor(scipy.linalg.hadamard(128),
+ * dtype=bf16) / 128**0.5, so every entry is +-c with c = bf16(128^-0.5) = 181 * 2^-11; the c8 path
+ * multiplies k_li and every query head q_li by it in bf16):
+ *     y_j = bf16( sum_i x_i * H[i][j] ),   H[i][j] = c * (-1)^popcount(i & j)  (Sylvester order).
+ * Reading: the bf16 matmul is the exact dot product rounded once to bf16 (float64 stands in for the
+ * exact sum, in index order). */
+void dsa_oracle_c8_rotate128(const uint16_t* in_bf16, uint16_t* out_bf16) {
+    const double c = (double)bf16_bits_to_f32(dsa_oracle_f64_to_bf16(1.0 / sqrt(128.0)));
+    double x[DI];
+    for (int i = 0; i < DI; ++i) x[i] = (double)bf16_bits_to_f32(in_bf16[i]);
+    for (int j = 0; j < DI; ++j) {
+        double acc = 0.0;
+        for (int i = 0; i < DI; ++i) {
+            int par = 0;
+            for (int t = i & j; t; t >>= 1) par ^= t & 1;
+            acc += (par ? -c : c) * x[i];
+        }
+        out_bf16[j] = dsa_oracle_f64_to_bf16(acc);
+    }
+}
+
+/* Dynamic symmetric int8 quantisation of one vector ([sfa] torch_npu.npu_dynamic_quant(x.view(-1,
+ * 128), dst_type=int8): one scale per row, i.e. per key token and per (query token, head); the
+ * scale comes back in fp32 and is cast to fp16 for the cache and the logits call).  The formula is
+ * not printed; reading: amax = max |y|; scale = amax / 127 (fp32, IEEE division); code =
+ * round-to-nearest-even(y / scale) (fp32 IEEE division), so |code| <= 127; a vector of zeros has
+ * scale 0 and codes 0.  The codes use the fp32 scale; only the stored scale is rounded to fp16. */
+void dsa_oracle_quant_int8(const float* y, int n, int8_t* codes, float* scale) {
+    float amax = 0.0f;
+    for (int i = 0; i < n; ++i) {
+        float a = fabsf(y[i]);
+        if (a > amax) amax = a;
+    }
+    const float s = amax / 127.0f;
+    *scale = s;
+    for (int i = 0; i < n; ++i) {
+        if (s == 0.0f) {
+            codes[i] = 0;
+            continue;
+        }
+        const float q = rintf(y[i] / s);
+        codes[i] = (int8_t)(q > 127.0f ? 127.0f : (q < -127.0f ? -127.0f : q));
+    }
+}
+
+/* Store new indexer keys into the paged int8 cache ([sfa] indexer_select_pre_process with
+ * use_sparse_c8_indexer: k_li @ qk_hadamard, npu_dynamic_quant per token, scale to fp16; then
+ * npu_scatter_nd_update_ of the codes into kv_cache[2] and of the scales into kv_cache[3] by
+ * slot_mapping).  slot < 0 is padding and is skipped.  Page layout (reading: the pages keep codes
+ * [pages, 64, 1, 128] int8 and scales [pages, 64, 1, 1] fp16 as two tensors; here one page-blocked
+ * pool like the FP8 cache): bytes [0, 8192) hold the 64 x 128 codes row by row, bytes
+ * [8192, 8320) the 64 fp16 scales.  Returns the number of tokens whose slot pointed past the pool. */
+int64_t dsa_oracle_store_index_k_c8(const uint16_t* k_bf16, const int64_t* slot_mapping, int64_t n,
+                                    uint8_t* pool, int64_t num_pages) {
+    int64_t bad = 0;
+    for (int64_t t = 0; t < n; ++t) {
+        const int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        const int64_t page = slot / PAGE;
+        if (page >= num_pages) {
+            ++bad;
+            continue;
+        }
+        uint16_t rot[DI];
+        float y[DI], sc;
+        int8_t codes[DI];
+        dsa_oracle_c8_rotate128(k_bf16 + t * DI, rot);
+        for (int d = 0; d < DI; ++d) y[d] = bf16_bits_to_f32(rot[d]);
+        dsa_oracle_quant_int8(y, DI, codes, &sc);
+        uint8_t* pg = pool + page * C8_PAGE_BYTES;
+        memcpy(pg + (slot % PAGE) * DI, codes, DI);
+        const uint16_t h = dsa_oracle_f32_to_f16(sc);
+        pg[PAGE * DI + (slot % PAGE) * 2] = (uint8_t)(h & 0xff);
+        pg[PAGE * DI + (slot % PAGE) * 2 + 1] = (uint8_t)(h >> 8);
+    }
+    return bad;
+}
+
+/* Lightning-indexer logits over the int8 cache ([sfa] indexer_select_post_process with
+ * use_sparse_c8_indexer: the query heads rotated by qk_hadamard and quantised per (token, head) by
+ * npu_dynamic_quant, the weights cast to fp16, then npu_lightning_indexer_quant(query, key, weights,
+ * query_dequant_scale, key_dequant_scale, ..., query_quant_mode=0, key_quant_mode=0)).  Reading: the
+ * lightning-indexer score on the dequantised query and key,
+ *     I[r,s] = sum_h w16[r,h] * ReLU( qs16[r,h] * ks16[s] * sum_d cq[r,h,d] * ck[s,d] ),
+ * with w16, qs16, ks16 the fp16 weight and scales.  Computed in double (the integer dot product is
+ * exact), rounded once to fp32; only s < v_r is written.  mag as in dsa_oracle_indexer_logits.
+ * Returns the number of (row, key) pairs skipped because the page id was out of range. */
+int64_t dsa_oracle_indexer_logits_c8(const uint16_t* q_bf16, const float* w, const uint8_t* pool,
+                                     int64_t num_pages, const int32_t* block_table, int32_t max_pages,
+                                     const int32_t* seq_lens, const int32_t* cu_q, int32_t B,
+                                     const int64_t* rows, int64_t n_rows, float* logits, int64_t ld,
+                                     double* mag) {
+    int64_t bad = 0;
+    for (int64_t i = 0; i < n_rows; ++i) {
+        const int64_t r = rows[i];
+        const int b = row_request(cu_q, B, r);
+        if (b < 0) continue;
+        const int32_t v = dsa_oracle_visible_len(seq_lens, cu_q, B, r);
+        int8_t cq[HI][DI];
+        double wq[HI], qs[HI];
+        for (int h = 0; h < HI; ++h) {
+            uint16_t rot[DI];
+            float y[DI], sc;
+            dsa_oracle_c8_rotate128(q_bf16 + (r * HI + h) * DI, rot);
+            for (int d = 0; d < DI; ++d) y[d] = bf16_bits_to_f32(rot[d]);
+            dsa_oracle_quant_int8(y, DI, cq[h], &sc);
+            qs[h] = dsa_oracle_f16_decode(dsa_oracle_f32_to_f16(sc));
+            wq[h] = dsa_oracle_f16_decode(dsa_oracle_f32_to_f16(w[r * HI + h]));
+        }
+        int64_t row_bad = 0;
+#pragma omp parallel for schedule(static) reduction(+ : row_bad)
+        for (int64_t s = 0; s < v; ++s) {
+            const int64_t lp = s / PAGE;
+            const int32_t page = (lp < max_pages) ? block_table[(int64_t)b * max_pages + lp] : -1;
+            if (page < 0 || page >= num_pages) {
+                ++row_bad;
+                continue;
+            }
+            const uint8_t* pg = pool + (int64_t)page * C8_PAGE_BYTES;
+            const int8_t* ck = (const int8_t*)(pg + (s % PAGE) * DI);
+            const uint16_t kh = (uint16_t)(pg[PAGE * DI + (s % PAGE) * 2] | (pg[PAGE * DI + (s % PAGE) * 2 + 1] << 8));
+            const double ks = dsa_oracle_f16_decode(kh);
+            double acc = 0.0, accm = 0.0;
+            for (int h = 0; h < HI; ++h) {
+                int64_t dot = 0;
+                for (int d = 0; d < DI; ++d) dot += (int64_t)cq[h][d] * (int64_t)ck[d];
+                double relu = qs[h] * ks * (double)dot;
                 if (relu < 0.0) relu = 0.0;
                 acc += wq[h] * relu;
                 accm += fabs(wq[h]) * relu;
