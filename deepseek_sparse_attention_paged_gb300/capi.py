@@ -36,6 +36,7 @@ DSA_K_NO_ROTATE = 0x8
 DSA_SCALE_UE8M0 = 0x10
 PAGE_SIZE = 64
 INDEX_PAGE_BYTES = 64 * 132
+C8_PAGE_BYTES = 64 * 130      # int8 index cache page: 64 x 128 codes + 64 fp16 scales
 LATENT_DIM = 576
 VALUE_DIM = 512
 MAX_TOPK = 2048
@@ -97,6 +98,10 @@ def load(path: str = LIB_PATH):
         "dsa_sparse_mla_decode_noalloc": (ctypes.c_int, [P, P, i64, P, i32, P, P, i32, P, i32, i32, i32,
                                                          ctypes.c_float, P, P, P, P]),
         "dsa_store_latent_fp8": (ctypes.c_int, [P, P, i64, ctypes.c_float, P, i64, P, P]),
+        "dsa_store_index_k_c8": (ctypes.c_int, [P, P, i64, P, i64, i32, P, P]),
+        "dsa_indexer_logits_c8_workspace_size": (sz, [i32]),
+        "dsa_indexer_logits_c8": (ctypes.c_int, [P, P, P, i64, P, i32, P, P, i32, i32, i32, i32, i32, P, i64, P, sz,
+                                                 P, P]),
         "dsa_sparse_mla_decode_fp8": (ctypes.c_int, [P, ctypes.c_float, P, ctypes.c_float, i64, P, i32, P, P, i32, P,
                                                      i32, i32, i32, ctypes.c_float, P, P, P, sz, P, P]),
     }
@@ -291,6 +296,60 @@ def dsa_indexer_logits(q_bf16: torch.Tensor, weights: torch.Tensor, index_k_pool
 
 def dsa_indexer_logits_workspace_size(rows: int) -> int:
     return int(load().dsa_indexer_logits_workspace_size(int(rows)))
+
+
+def dsa_store_index_k_c8(k_bf16: torch.Tensor, slot_mapping: torch.Tensor, index_k_pool_c8: torch.Tensor,
+                         dev_err: Optional[torch.Tensor] = None, stream=None) -> None:
+    lib = load()
+    _cuda(k_bf16, torch.bfloat16, "k_bf16")
+    _cuda(slot_mapping, torch.int64, "slot_mapping")
+    _cuda(index_k_pool_c8, torch.uint8, "index_k_pool_c8")
+    _need(k_bf16.dim() == 2 and k_bf16.shape[1] == 128, "k_bf16 must be [n, 128]")
+    _need(slot_mapping.numel() == k_bf16.shape[0], "slot_mapping must have n entries")
+    _need(index_k_pool_c8.dim() == 2 and index_k_pool_c8.shape[1] == C8_PAGE_BYTES, "pool must be [pages, 8320]")
+    _check("dsa_store_index_k_c8", lib.dsa_store_index_k_c8(
+        _ptr(k_bf16), _ptr(slot_mapping), k_bf16.shape[0], _ptr(index_k_pool_c8), index_k_pool_c8.shape[0],
+        PAGE_SIZE, _ptr(dev_err), _stream(stream)))
+    _count(1 if k_bf16.shape[0] > 0 else 0)
+
+
+def dsa_indexer_logits_c8_workspace_size(rows: int) -> int:
+    return int(load().dsa_indexer_logits_c8_workspace_size(int(rows)))
+
+
+def dsa_indexer_logits_c8(q_bf16: torch.Tensor, weights: torch.Tensor, index_k_pool_c8: torch.Tensor,
+                          block_table: torch.Tensor, seq_lens: torch.Tensor, cu_q: torch.Tensor,
+                          max_seq_len: int, max_q_len: int, logits: torch.Tensor, row_begin: int = 0,
+                          row_end: Optional[int] = None, dev_err: Optional[torch.Tensor] = None,
+                          stream=None, workspace: Optional[torch.Tensor] = None) -> None:
+    """Logits of rows [row_begin, row_end) over the int8 cache (dsa_store_index_k_c8)."""
+    lib = load()
+    _cuda(q_bf16, torch.bfloat16, "q_bf16")
+    _cuda(weights, torch.float32, "weights")
+    _cuda(index_k_pool_c8, torch.uint8, "index_k_pool_c8")
+    _cuda(block_table, torch.int32, "block_table")
+    _cuda(seq_lens, torch.int32, "seq_lens")
+    _cuda(cu_q, torch.int32, "cu_q")
+    _rows(logits, torch.float32, "logits")
+    _need(q_bf16.dim() == 3 and tuple(q_bf16.shape[1:]) == (64, 128), "q_bf16 must be [T, 64, 128]")
+    _need(index_k_pool_c8.dim() == 2 and index_k_pool_c8.shape[1] == C8_PAGE_BYTES, "pool must be [pages, 8320]")
+    T = q_bf16.shape[0]
+    _need(tuple(weights.shape) == (T, 64), "weights must be [T, 64]")
+    B = seq_lens.numel()
+    _need(cu_q.numel() == B + 1 and block_table.dim() == 2 and block_table.shape[0] == B, "metadata shapes")
+    row_end = T if row_end is None else row_end
+    _need(0 <= row_begin <= row_end <= T, "row range")
+    _need(logits.dim() == 2 and logits.shape[0] >= row_end - row_begin, "logits rows")
+    if workspace is None:
+        workspace = torch.empty(max(16, dsa_indexer_logits_c8_workspace_size(row_end - row_begin)),
+                                dtype=torch.uint8, device=q_bf16.device)
+    _need(workspace.is_cuda and workspace.is_contiguous(), "workspace must be a contiguous CUDA tensor")
+    _check("dsa_indexer_logits_c8", lib.dsa_indexer_logits_c8(
+        _ptr(q_bf16), _ptr(weights), _ptr(index_k_pool_c8), index_k_pool_c8.shape[0], _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), _ptr(cu_q), B, int(max_seq_len), int(max_q_len), int(row_begin),
+        int(row_end), _ptr(logits), logits.stride(0), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(dev_err), _stream(stream)))
+    _count(2 if row_end > row_begin else 0)
 
 
 def dsa_topk_workspace_size(rows: int, k: int, max_seq_len: int) -> int:

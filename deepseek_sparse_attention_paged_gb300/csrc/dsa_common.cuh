@@ -1,6 +1,7 @@
 // dsa_common.cuh -- small device/host helpers shared by the DSA kernels (sm_103a).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -13,6 +14,8 @@ constexpr int kIndexHeads = 64;           // lightning-indexer heads
 constexpr int kIndexDim = 128;            // lightning-indexer head dim
 constexpr int kIndexPageBytes = 64 * 132; // 64 x (128 FP8 codes + fp32 scale), page-blocked
 constexpr int kIndexScaleOffset = 64 * 128;
+constexpr int kC8PageBytes = 64 * 130;    // int8 ("c8") index cache: 64 x 128 codes, then 64 fp16 scales
+constexpr int kC8ScaleOffset = 64 * 128;
 constexpr int kLatentDim = 576;           // 512 latent + 64 rope
 constexpr int kValueDim = 512;
 
@@ -53,6 +56,66 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// The int8 ("c8") indexer transform of one 128-vector held by a warp (lane l: elements 4l .. 4l+3,
+// exact fp32 values of bf16 numbers).  Follows vllm-ascend sfa_v1.py with use_sparse_c8_indexer:
+// x @ qk_hadamard, where qk_hadamard = bf16(scipy.linalg.hadamard(128)) / 128**0.5 has entries +-c,
+// c = bf16(128^-0.5) = 181 * 2^-11; then npu_dynamic_quant to int8 with one scale per vector.
+//   * y_j = bf16(c * sum_i (-1)^popcount(i & j) x_i): the Sylvester butterflies (h = 1, 2 inside the
+//     lane, 4 .. 64 across lanes l ^ h / 4) run in fp64, where sums of 128 bf16 values are exact and
+//     so is the product by c, so the one rounding to bf16 gives the correctly rounded product;
+//   * scale = amax / 127 (fp32, IEEE division); code = round-to-nearest-even(y / scale) (fp32 IEEE
+//     division), within [-127, 127]; all codes 0 when amax = 0.
+// Returns the lane's 4 codes packed little-endian; *scale_out = the fp32 scale.
+__device__ __forceinline__ uint32_t c8_rotate_quant(const float (&xin)[4], int lane, float* scale_out) {
+    constexpr double kC = 181.0 / 2048.0;
+    double x[4] = {xin[0], xin[1], xin[2], xin[3]};
+    {
+        double a = x[0], b = x[1];
+        x[0] = a + b; x[1] = a - b;
+        a = x[2]; b = x[3];
+        x[2] = a + b; x[3] = a - b;
+    }
+    {
+        double a = x[0], b = x[2];
+        x[0] = a + b; x[2] = a - b;
+        a = x[1]; b = x[3];
+        x[1] = a + b; x[3] = a - b;
+    }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const double other = __shfl_xor_sync(0xffffffffu, x[e], m);
+            x[e] = upper ? other - x[e] : x[e] + other;
+        }
+    }
+    float y[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) y[e] = __bfloat162float(__double2bfloat16(x[e] * kC));
+    const float amax = warp_max(fmaxf(fmaxf(fabsf(y[0]), fabsf(y[1])), fmaxf(fabsf(y[2]), fabsf(y[3]))));
+    const float scale = __fdiv_rn(amax, 127.0f);
+    uint32_t packed = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        int c = 0;
+        if (amax > 0.0f) c = max(-127, min(127, __float2int_rn(__fdiv_rn(y[e], scale))));
+        packed |= static_cast<uint32_t>(c & 0xff) << (8 * e);
+    }
+    *scale_out = scale;
+    return packed;
+}
+
+// Four int8 values (packed little-endian) -> four f16 (exact), as two f16x2 words: with u = b ^ 0x80
+// (the value + 128), the f16 bits 0x6400 | u encode 1024 + u, and subtracting 1152 leaves the value.
+__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);
+    const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
+}
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Multiprocessor count of the current device (the launch heuristics size grids by it); `fallback`
@@ -82,6 +145,11 @@ dsa_status indexer_logits_launch(const void* q_bf16, const float* weights, const
                                  int32_t max_q_len, int32_t row_begin, int32_t row_end, float* logits, int64_t ld,
                                  uint32_t flags, void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream,
                                  uint32_t* hist_g);
+dsa_status indexer_logits_c8_launch(const void* q_bf16, const float* weights, const uint8_t* index_k_pool_c8,
+                                    int64_t num_pages, const int32_t* block_table, int32_t max_pages,
+                                    const int32_t* seq_lens, const int32_t* cu_q, int32_t B, int32_t max_seq_len,
+                                    int32_t max_q_len, int32_t row_begin, int32_t row_end, float* logits, int64_t ld,
+                                    void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream);
 dsa_status topk_launch(const float* logits, int64_t ld, const int32_t* seq_lens, const int32_t* cu_q, int32_t B,
                        int32_t max_seq_len, int32_t row_begin, int32_t row_end, int32_t k, int32_t n_init,
                        int32_t n_local, int32_t* idx, void* stream, const uint32_t* hist_g);

@@ -16,6 +16,7 @@
 // The logits kernel is launched as a programmatic dependent of the prologue, so its setup and its
 // first key pages overlap the prologue; only the query-tile loads wait for it.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
 #include "dsa_common.cuh"
@@ -93,6 +94,9 @@ constexpr int kQGateBytes = kIndexHeads * 4;              // 64 fp32 gates w' pe
 constexpr int kThreads = 352;                             // 11 warps
 constexpr int kEpiWarp0 = 2;                              // warps 2..9: two epilogue warpgroups
 constexpr int kLoaderWarp = 10;
+constexpr int kWidenWarp0 = 11;                           // c8: warps 11..14 widen int8 key tiles to f16
+constexpr int kQRowBytesC8 = kIndexHeads * kIndexDim * 2; // c8: 16 KB of f16 query codes per row
+constexpr int kWTileBytes = kTileKeys * kIndexDim * 2;    // c8: 32 KB, one key tile widened to f16
 
 // ---------------------------------------------------------------------------------------------
 // Query prologue: one warp per (row, head) vector.  Writes the 128 codes of the vector into the
@@ -118,6 +122,36 @@ indexer_q_prologue_kernel(const uint16_t* __restrict__ q, const float* __restric
     const uint32_t off = h * 128 + (((lane >> 2) ^ (h & 7)) << 4) + ((lane & 3) << 2);
     *reinterpret_cast<uint32_t*>(dst + off) = packed;
     if (lane == 0) q_gates[v] = __ldg(w + r * kIndexHeads + h) * scale;
+}
+
+// Query prologue of the int8 cache: one warp per (row, head) vector, rotated with the bf16 Hadamard
+// / sqrt(128) and quantised to int8 with one scale (c8_rotate_quant), the codes written as f16
+// (exact) into the row's 16 KB block: dim chunk c (dims 64 c ..) of head h at c * 8 KB + h * 128
+// with the 128-byte swizzle; the gate w16 * q_scale16 (the weight and the scale rounded to fp16, as
+// the c8 path casts weights and scales; their product is exact in fp32).
+__global__ void __launch_bounds__(256)
+indexer_q_prologue_c8_kernel(const uint16_t* __restrict__ q, const float* __restrict__ w,
+                             const int32_t* __restrict__ cu_q, int B, int row_begin, int row_end,
+                             uint8_t* __restrict__ q_codes, float* __restrict__ q_gates) {
+    ptx::griddep_launch_dependents();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t v = static_cast<int64_t>(blockIdx.x) * 8 + warp;   // (row - row_begin) * 64 + head
+    if (v >= static_cast<int64_t>(row_end - row_begin) * kIndexHeads) return;
+    const int64_t r = row_begin + v / kIndexHeads;
+    const int h = static_cast<int>(v % kIndexHeads);
+    if (r >= __ldg(cu_q + B)) return;
+    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(q + (r * kIndexHeads + h) * kIndexDim) + lane);
+    const float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
+    float scale;
+    const uint32_t packed = c8_rotate_quant(x, lane, &scale);
+    uint32_t lo, hi;
+    i8x4_to_f16x4(packed, lo, hi);
+    // dims 4 lane .. + 3 = f16 bytes 8 lane .. + 7: chunk lane / 16, 16-byte piece (lane % 16) / 2
+    uint8_t* dst = q_codes + (v / kIndexHeads) * kQRowBytesC8 + (lane >> 4) * 8192 + h * 128 +
+                   ((((lane & 15) >> 1) ^ (h & 7)) << 4) + (lane & 1) * 8;
+    *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
+    if (lane == 0)
+        q_gates[v] = __half2float(__float2half_rn(__ldg(w + r * kIndexHeads + h))) * __half2float(__float2half_rn(scale));
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -202,21 +236,32 @@ __device__ __forceinline__ int64_t epi_scan(int64_t v, int64_t* scratch, int64_t
 // two epilogue warpgroups taking alternate tiles (warp w reads TMEM lanes 32 (w % 4) .. +31, one
 // key per thread: ReLU, gates w', head sum, key scale, store), warp 10 = query-tile loader.
 // ---------------------------------------------------------------------------------------------
-template <int R, bool HIST = false>
+template <int R, bool HIST = false, bool C8 = false>
 struct IdxCfg {
     static_assert(!HIST || R <= 2, "the per-row histograms fit shared memory for row groups of up to 2 rows");
+    static_assert(!C8 || (R <= 2 && !HIST), "the int8 cache: row groups of up to 2 rows, no histograms");
     static constexpr int N = 64 * R;
-    // with HIST, the R 16 KB histograms take the place of R (or, for R = 2, two) key stages
-    static constexpr int kStages = (R == 1) ? (HIST ? 11 : 12) : (R == 2 ? (HIST ? 9 : 11) : 9);
+    static constexpr int kThreadsCfg = C8 ? kThreads + 4 * 32 : kThreads;
+    // with HIST, the R 16 KB histograms take the place of R (or, for R = 2, two) key stages; with C8
+    // the two 32 KB f16 key tiles and the f16 query take the place of key stages
+    static constexpr int kStages =
+        C8 ? (R == 1 ? 7 : 5) : ((R == 1) ? (HIST ? 11 : 12) : (R == 2 ? (HIST ? 9 : 11) : 9));
     static constexpr int kAcc = (R == 4) ? 2 : 4;                 // accumulators of N columns
     static constexpr uint32_t kTmemCols = kAcc * N;               // 256 / 512 / 512
-    static constexpr int kQBytes = R * kQRowBytes;
+    static constexpr int kQRowB = C8 ? kQRowBytesC8 : kQRowBytes;
+    static constexpr int kQBytes = R * kQRowB;
+    static constexpr int kScaleElem = C8 ? 2 : 4;                 // fp16 / fp32 key scales
+    static constexpr int kPoolPageBytes = C8 ? kC8PageBytes : kIndexPageBytes;
+    static constexpr int kPoolScaleOff = C8 ? kC8ScaleOffset : kIndexScaleOffset;
     static constexpr size_t kCodesOff = 0;
     static constexpr size_t kQOff = kCodesOff + size_t(kStages) * kTileCodeBytes;
-    static constexpr size_t kScalesOff = kQOff + 2 * size_t(kQBytes);
-    static constexpr size_t kGatesOff = kScalesOff + size_t(kStages) * kTileKeys * 4;
+    static constexpr size_t kWOff = kQOff + 2 * size_t(kQBytes);
+    static constexpr size_t kScalesOff = kWOff + (C8 ? 2 * size_t(kWTileBytes) : 0);
+    static constexpr size_t kGatesOff = kScalesOff + size_t(kStages) * kTileKeys * kScaleElem;
     static constexpr size_t kBarOff = kGatesOff + 2 * size_t(R) * kQGateBytes;
-    static constexpr int kBars = 2 * kStages + 2 * kAcc + 4 + 1;   // + the epilogue warps' histogram barrier
+    // full / empty per stage, tfull / tempty per accumulator, qfull / qempty, the epilogue warps'
+    // histogram barrier, and with C8 wfull / wempty per f16 tile
+    static constexpr int kBars = 2 * kStages + 2 * kAcc + 4 + 1 + (C8 ? 4 : 0);
     static constexpr size_t kMiscOff = kBarOff + size_t(kBars) * 8;   // tmem slot, partition, scan
     static constexpr size_t kPageOkOff = kMiscOff + 16 + 8 * 8;
     static constexpr size_t kHistOff = (kPageOkOff + 2 * kStages + 15) / 16 * 16;
@@ -225,15 +270,15 @@ struct IdxCfg {
     static_assert(kSmemBytes <= 232448, "shared-memory budget");
 };
 
-template <int R, bool HIST>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int R, bool HIST, bool C8>
+__global__ void __launch_bounds__(IdxCfg<R, HIST, C8>::kThreadsCfg, 1)
 indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8_t* __restrict__ q_codes,
                            const float* __restrict__ q_gates, const uint8_t* __restrict__ pool, int64_t num_pages,
                            const int32_t* __restrict__ block_table, int max_pages,
                            const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q, int B, int G,
                            int row_begin, int row_end, float* __restrict__ logits, int64_t ld, int32_t* err,
                            uint32_t* __restrict__ hist_g) {
-    using C = IdxCfg<R, HIST>;
+    using C = IdxCfg<R, HIST, C8>;
     constexpr int S = C::kStages;
     constexpr int N = C::N;
     constexpr int NA = C::kAcc;
@@ -241,8 +286,10 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
     const uint32_t raw_addr = ptx::smem_addr(smem_raw);
     unsigned char* base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     unsigned char* codes = base + C::kCodesOff;                               // [S][16 KB]
-    unsigned char* qtile = base + C::kQOff;                                   // [2][R * 8 KB]
-    float* scales = reinterpret_cast<float*>(base + C::kScalesOff);           // [S][128]
+    unsigned char* qtile = base + C::kQOff;                                   // [2][R * 8 KB] (C8: 16 KB)
+    unsigned char* wtile = base + C::kWOff;                                   // C8: [2][32 KB] f16 key tiles
+    unsigned char* scales_b = base + C::kScalesOff;                           // [S][128] fp32 (C8: fp16)
+    float* scales = reinterpret_cast<float*>(scales_b);
     float* gates = reinterpret_cast<float*>(base + C::kGatesOff);             // [2][R * 64]
     uint64_t* full = reinterpret_cast<uint64_t*>(base + C::kBarOff);
     uint64_t* empty = full + S;
@@ -251,6 +298,8 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
     uint64_t* qfull = tempty + NA;     // [2]
     uint64_t* qempty = qfull + 2;      // [2]
     uint64_t* hsync = qempty + 2;      // HIST: the 8 epilogue warps meet before / after a histogram flush
+    uint64_t* wfull = hsync + 1;       // C8: [2] an f16 key tile is written (4 widen warps)
+    uint64_t* wempty = wfull + 2;      // C8: [2] the MMAs that read it completed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + C::kMiscOff);
     int32_t* part = reinterpret_cast<int32_t*>(base + C::kMiscOff + 4);      // start segment, tile, count
     int64_t* scan_scratch = reinterpret_cast<int64_t*>(base + C::kMiscOff + 16);
@@ -265,7 +314,15 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(&full[s], 1);
-            ptx::mbar_init(&empty[s], 1 + 4);   // MMA commit + the 4 warps of the tile's epilogue group
+            // the stage's readers: the MMA commit (C8: the 4 widen warps) + the 4 warps of the tile's
+            // epilogue group (scales, page flags)
+            ptx::mbar_init(&empty[s], (C8 ? 4 : 1) + 4);
+        }
+        if (C8) {
+            for (int b2 = 0; b2 < 2; ++b2) {
+                ptx::mbar_init(&wfull[b2], 4);
+                ptx::mbar_init(&wempty[b2], 1);
+            }
         }
         for (int a = 0; a < NA; ++a) {
             ptx::mbar_init(&tfull[a], 1);
@@ -372,21 +429,21 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
                     if (!ok0 || (need1 && !ok1)) raise_error(err, DSA_DEVERR_PAGE_RANGE);
                     page_ok[2 * s] = ok0;
                     page_ok[2 * s + 1] = ok1;
-                    const uint32_t bytes = (ok0 ? (kPage * kIndexDim + kPage * 4) : 0) +
-                                           (ok1 ? (kPage * kIndexDim + kPage * 4) : 0);
+                    const uint32_t bytes = (ok0 ? (kPage * kIndexDim + kPage * C::kScaleElem) : 0) +
+                                           (ok1 ? (kPage * kIndexDim + kPage * C::kScaleElem) : 0);
                     ptx::mbar_arrive_expect_tx(&full[s], bytes);
                     unsigned char* dst = codes + s * kTileCodeBytes;
                     if (ok0) {
                         ptx::tma_load_3d(dst, &kmap, &full[s], 0, 0, pg0);
-                        ptx::bulk_load(scales + s * kTileKeys,
-                                       pool + static_cast<int64_t>(pg0) * kIndexPageBytes + kIndexScaleOffset,
-                                       kPage * 4, &full[s]);
+                        ptx::bulk_load(scales_b + s * kTileKeys * C::kScaleElem,
+                                       pool + static_cast<int64_t>(pg0) * C::kPoolPageBytes + C::kPoolScaleOff,
+                                       kPage * C::kScaleElem, &full[s]);
                     }
                     if (ok1) {
                         ptx::tma_load_3d(dst + kPage * kIndexDim, &kmap, &full[s], 0, 0, pg1);
-                        ptx::bulk_load(scales + s * kTileKeys + kPage,
-                                       pool + static_cast<int64_t>(pg1) * kIndexPageBytes + kIndexScaleOffset,
-                                       kPage * 4, &full[s]);
+                        ptx::bulk_load(scales_b + (s * kTileKeys + kPage) * C::kScaleElem,
+                                       pool + static_cast<int64_t>(pg1) * C::kPoolPageBytes + C::kPoolScaleOff,
+                                       kPage * C::kScaleElem, &full[s]);
                     }
                 }
             }
@@ -404,15 +461,21 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
                 uint32_t bytes = 0;
                 for (int jj = 0; jj < sg.nrows; ++jj) {
                     const int r = sg.q0 + sg.j0 + jj;
-                    if (r >= row_begin && r < row_end) bytes += kQRowBytes + kQGateBytes;
+                    if (r >= row_begin && r < row_end) bytes += C::kQRowB + kQGateBytes;
                 }
                 ptx::mbar_arrive_expect_tx(&qfull[qb], bytes);
                 for (int jj = 0; jj < sg.nrows; ++jj) {
                     const int r = sg.q0 + sg.j0 + jj;
                     if (r < row_begin || r >= row_end) continue;
                     const int64_t rr = r - row_begin;
-                    ptx::bulk_load(qtile + qb * C::kQBytes + jj * kQRowBytes, q_codes + rr * kQRowBytes, kQRowBytes,
-                                   &qfull[qb]);
+                    if (C8) {   // the row's two 8 KB dim chunks go to the two chunk columns of the tile
+                        for (int c = 0; c < 2; ++c)
+                            ptx::bulk_load(qtile + qb * C::kQBytes + c * (R * 8192) + jj * 8192,
+                                           q_codes + rr * kQRowBytesC8 + c * 8192, 8192, &qfull[qb]);
+                    } else {
+                        ptx::bulk_load(qtile + qb * C::kQBytes + jj * kQRowBytes, q_codes + rr * kQRowBytes,
+                                       kQRowBytes, &qfull[qb]);
+                    }
                     ptx::bulk_load(gates + (qb * R + jj) * kIndexHeads, q_gates + rr * kIndexHeads, kQGateBytes,
                                    &qfull[qb]);
                 }
@@ -432,17 +495,37 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
                 seg_start = false;
                 const int a = i % NA;
                 const uint32_t aph = (i / NA) & 1;
-                if (!ptx::mbar_wait(&full[s], ph, deadline)) { timed_out = true; break; }
+                if (C8) {
+                    if (!ptx::mbar_wait(&wfull[i & 1], (i >> 1) & 1, deadline)) { timed_out = true; break; }
+                } else if (!ptx::mbar_wait(&full[s], ph, deadline)) {
+                    timed_out = true;
+                    break;
+                }
                 if (!ptx::mbar_wait(&tempty[a], aph ^ 1u, deadline)) { timed_out = true; break; }
                 ptx::tc_fence_after_sync();
-                const uint32_t a_addr = ptx::smem_addr(codes + s * kTileCodeBytes);
                 const uint32_t q_addr = ptx::smem_addr(qtile + qb * C::kQBytes);
                 const uint32_t d = tmem + static_cast<uint32_t>(a * N);
+                if (C8) {
+                    // f16 x f16 (kind::f16, format code 0 for both): K = 16 per instruction, the 128
+                    // dims in two 64-dim chunk columns of both operands
+                    ptx::fence_proxy_async_smem();
+                    const uint32_t a_addr = ptx::smem_addr(wtile + (i & 1) * kWTileBytes);
 #pragma unroll
-                for (int k = 0; k < kIndexDim / 32; ++k)
-                    ptx::umma_f8f6f4(d, ptx::sw128_kmajor_desc(a_addr + k * 32),
-                                     ptx::sw128_kmajor_desc(q_addr + k * 32), idesc, k > 0 ? 1u : 0u);
-                ptx::umma_commit(&empty[s]);
+                    for (int k = 0; k < kIndexDim / 16; ++k) {
+                        const uint32_t off = (k & 3) * 32;
+                        ptx::umma_f16(d, ptx::sw128_kmajor_desc(a_addr + (k >> 2) * (kTileKeys * 128) + off),
+                                      ptx::sw128_kmajor_desc(q_addr + (k >> 2) * (R * 8192) + off), idesc,
+                                      k > 0 ? 1u : 0u);
+                    }
+                    ptx::umma_commit(&wempty[i & 1]);
+                } else {
+                    const uint32_t a_addr = ptx::smem_addr(codes + s * kTileCodeBytes);
+#pragma unroll
+                    for (int k = 0; k < kIndexDim / 32; ++k)
+                        ptx::umma_f8f6f4(d, ptx::sw128_kmajor_desc(a_addr + k * 32),
+                                         ptx::sw128_kmajor_desc(q_addr + k * 32), idesc, k > 0 ? 1u : 0u);
+                    ptx::umma_commit(&empty[s]);
+                }
                 ptx::umma_commit(&tfull[a]);
                 if (++s == S) { s = 0; ph ^= 1u; }
                 if (++sg.tile == sg.ntiles || i + 1 == count) {   // last tile of the segment here
@@ -452,6 +535,39 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
                     if (i + 1 < count) seg_next(sa, sg);
                 }
             }
+        }
+    } else if (C8 && warp >= kWidenWarp0 && warp < kWidenWarp0 + 4 && count > 0) {   // ------- int8 -> f16
+        // thread t of the 4 warps owns key row t of every tile: its 8 swizzled 16-byte pieces of
+        // int8 codes become 16 f16 pieces in the two 64-dim chunk columns of the f16 tile
+        const int key = (warp - kWidenWarp0) * 32 + lane;
+        int s = 0;
+        uint32_t ph = 0;
+        for (int i = 0; i < count; ++i) {
+            const int wb = i & 1;
+            if (!ptx::mbar_wait(&full[s], ph, deadline)) { timed_out = true; break; }
+            if (!ptx::mbar_wait(&wempty[wb], ((i >> 1) & 1) ^ 1u, deadline)) { timed_out = true; break; }
+            const unsigned char* src = codes + s * kTileCodeBytes + key * 128;
+            unsigned char* dst = wtile + wb * kWTileBytes + key * 128;
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+                const uint4 c = *reinterpret_cast<const uint4*>(src + ((p ^ (key & 7)) << 4));
+                uint4 lo, hi;
+                i8x4_to_f16x4(c.x, lo.x, lo.y);
+                i8x4_to_f16x4(c.y, lo.z, lo.w);
+                i8x4_to_f16x4(c.z, hi.x, hi.y);
+                i8x4_to_f16x4(c.w, hi.z, hi.w);
+                unsigned char* row = dst + (p >> 2) * (kTileKeys * 128);
+                const int j0 = 2 * (p & 3);
+                *reinterpret_cast<uint4*>(row + ((j0 ^ (key & 7)) << 4)) = lo;
+                *reinterpret_cast<uint4*>(row + (((j0 + 1) ^ (key & 7)) << 4)) = hi;
+            }
+            ptx::fence_proxy_async_smem();   // read by the tensor cores
+            __syncwarp();
+            if (lane == 0) {
+                ptx::mbar_arrive(&wfull[wb]);
+                ptx::mbar_arrive(&empty[s]);
+            }
+            if (++s == S) { s = 0; ph ^= 1u; }
         }
     } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 8 && count > 0) {   // ---------------- epilogue
         const int grp = (warp - kEpiWarp0) >> 2;          // takes the tiles i with i % 2 == grp
@@ -473,7 +589,9 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
                 if (!ptx::mbar_wait(&tfull[a], aph, deadline)) { timed_out = true; break; }
                 ptx::tc_fence_after_sync();
                 const bool ok = page_ok[2 * s + (key_in_tile >> 6)] != 0;
-                const float ks = scales[s * kTileKeys + key_in_tile];
+                float ks;
+                if (C8) ks = __half2float(reinterpret_cast<const __half*>(scales_b)[s * kTileKeys + key_in_tile]);
+                else ks = scales[s * kTileKeys + key_in_tile];
                 const int key = sg.tile * kTileKeys + key_in_tile;
 #pragma unroll 1
                 for (int jj = 0; jj < sg.nrows; ++jj) {   // one query row at a time: 64 accumulator columns
@@ -575,6 +693,11 @@ extern "C" size_t dsa_indexer_logits_workspace_size(int32_t rows) {
     return rows <= 0 ? 0 : static_cast<size_t>(rows) * (kQRowBytes + kQGateBytes);
 }
 
+extern "C" size_t dsa_indexer_logits_c8_workspace_size(int32_t rows) {
+    using namespace dsa;
+    return rows <= 0 ? 0 : static_cast<size_t>(rows) * (kQRowBytesC8 + kQGateBytes);
+}
+
 namespace dsa {
 
 // The logits call; with hist_g != nullptr (row groups of at most 2 rows) the kernel also adds each
@@ -651,11 +774,11 @@ dsa_status indexer_logits_launch(const void* q_bf16, const float* weights, const
 #define DSA_LAUNCH_IDX(RR, HH)                                                                                  \
     do {                                                                                                        \
         const size_t smem = IdxCfg<RR, HH>::kSmemBytes;                                                         \
-        if (cudaFuncSetAttribute(indexer_logits_umma_kernel<RR, HH>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                                 static_cast<int>(smem)) != cudaSuccess)                                        \
+        if (cudaFuncSetAttribute(indexer_logits_umma_kernel<RR, HH, false>,                                     \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess) \
             return DSA_ERR_CUDA;                                                                                \
         cfg.dynamicSmemBytes = smem;                                                                            \
-        if (cudaLaunchKernelEx(&cfg, indexer_logits_umma_kernel<RR, HH>, kmap, qc, qg, index_k_pool, num_pages,  \
+        if (cudaLaunchKernelEx(&cfg, indexer_logits_umma_kernel<RR, HH, false>, kmap, qc, qg, index_k_pool, num_pages, \
                                block_table, static_cast<int>(max_pages), seq_lens, cu_q, static_cast<int>(B),  \
                                groups, static_cast<int>(row_begin), static_cast<int>(row_end), logits, ld,     \
                                dev_err, hist_g) != cudaSuccess)                                                 \
@@ -682,4 +805,103 @@ extern "C" dsa_status dsa_indexer_logits(const void* q_bf16, const float* weight
     return dsa::indexer_logits_launch(q_bf16, weights, index_k_pool, num_pages, block_table, max_pages, seq_lens,
                                       cu_q, B, max_seq_len, max_q_len, row_begin, row_end, logits, ld, flags,
                                       workspace, ws_bytes, dev_err, stream, nullptr);
+}
+
+namespace dsa {
+
+// The logits call over the int8 ("c8") cache: query prologue (rotation, int8 quantisation, f16
+// codes, fp16 gates), then the logits kernel with f16 tensor-core products of the int8 values.
+dsa_status indexer_logits_c8_launch(const void* q_bf16, const float* weights, const uint8_t* pool,
+                                    int64_t num_pages, const int32_t* block_table, int32_t max_pages,
+                                    const int32_t* seq_lens, const int32_t* cu_q, int32_t B, int32_t max_seq_len,
+                                    int32_t max_q_len, int32_t row_begin, int32_t row_end, float* logits, int64_t ld,
+                                    void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream) {
+    if (B < 0 || max_seq_len < 0 || max_q_len < 0 || row_begin < 0 || row_end < row_begin || max_pages < 0 ||
+        num_pages < 0)
+        return DSA_ERR_INVALID_ARG;
+    if (B == 0 || row_end == row_begin || max_seq_len == 0 || max_q_len == 0) return DSA_OK;
+    if (!q_bf16 || !weights || !pool || !block_table || !seq_lens || !cu_q || !logits || !workspace)
+        return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q_bf16) || !aligned16(pool) || !aligned16(workspace)) return DSA_ERR_INVALID_ARG;
+    if (ws_bytes < dsa_indexer_logits_c8_workspace_size(row_end - row_begin)) return DSA_ERR_INVALID_ARG;
+    if (ld < max_seq_len) return DSA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(max_pages) * kPage < max_seq_len) return DSA_ERR_INVALID_ARG;
+    const int R = max_q_len >= 2 ? 2 : 1;
+    const int groups = (max_q_len + R - 1) / R;
+    if (static_cast<int64_t>(groups) * B > 0x7fffffffLL - 1) return DSA_ERR_UNSUPPORTED;
+    if (num_pages > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
+    const int64_t tiles_per_seg = (max_seq_len + kTileKeys - 1) / kTileKeys;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        return DSA_ERR_CUDA;
+    const int64_t upper = tiles_per_seg * groups * B;
+    const int ctas = static_cast<int>(upper < sms ? upper : sms);
+
+    // tensor map over the code bytes of the page-blocked int8 pool: (byte in row, row in page, page)
+    CUtensorMap kmap;
+    {
+        auto encode = tensor_map_encoder();
+        if (encode == nullptr) return DSA_ERR_CUDA;
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kIndexDim), static_cast<cuuint64_t>(kPage),
+                                    static_cast<cuuint64_t>(num_pages)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kIndexDim), static_cast<cuuint64_t>(kC8PageBytes)};
+        const cuuint32_t box[3] = {static_cast<cuuint32_t>(kIndexDim), static_cast<cuuint32_t>(kPage), 1};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        if (encode(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(pool), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return DSA_ERR_CUDA;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int rows = row_end - row_begin;
+    uint8_t* q_codes = static_cast<uint8_t*>(workspace);
+    float* q_gates = reinterpret_cast<float*>(q_codes + static_cast<size_t>(rows) * kQRowBytesC8);
+    indexer_q_prologue_c8_kernel<<<static_cast<unsigned>(rows) * (kIndexHeads / 8), 256, 0, st>>>(
+        static_cast<const uint16_t*>(q_bf16), weights, cu_q, B, row_begin, row_end, q_codes, q_gates);
+    if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
+
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas, 1, 1);
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const uint8_t* qc = q_codes;
+    const float* qg = q_gates;
+    uint32_t* no_hist = nullptr;
+#define DSA_LAUNCH_IDX_C8(RR)                                                                                   \
+    do {                                                                                                        \
+        using Cfg = IdxCfg<RR, false, true>;                                                                    \
+        if (cudaFuncSetAttribute(indexer_logits_umma_kernel<RR, false, true>,                                   \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,                                   \
+                                 static_cast<int>(Cfg::kSmemBytes)) != cudaSuccess)                             \
+            return DSA_ERR_CUDA;                                                                                \
+        cfg.blockDim = dim3(Cfg::kThreadsCfg, 1, 1);                                                            \
+        cfg.dynamicSmemBytes = Cfg::kSmemBytes;                                                                 \
+        if (cudaLaunchKernelEx(&cfg, indexer_logits_umma_kernel<RR, false, true>, kmap, qc, qg, pool, num_pages, \
+                               block_table, static_cast<int>(max_pages), seq_lens, cu_q, static_cast<int>(B),  \
+                               groups, static_cast<int>(row_begin), static_cast<int>(row_end), logits, ld,     \
+                               dev_err, no_hist) != cudaSuccess)                                                \
+            return DSA_ERR_CUDA;                                                                                \
+    } while (0)
+    if (R == 1) DSA_LAUNCH_IDX_C8(1);
+    else DSA_LAUNCH_IDX_C8(2);
+#undef DSA_LAUNCH_IDX_C8
+    return launch_status();
+}
+
+}  // namespace dsa
+
+extern "C" dsa_status dsa_indexer_logits_c8(const void* q_bf16, const float* weights, const uint8_t* index_k_pool_c8,
+                                            int64_t num_pages, const int32_t* block_table, int32_t max_pages,
+                                            const int32_t* seq_lens, const int32_t* cu_q, int32_t B,
+                                            int32_t max_seq_len, int32_t max_q_len, int32_t row_begin,
+                                            int32_t row_end, float* logits, int64_t ld, void* workspace,
+                                            size_t ws_bytes, int32_t* dev_err, void* stream) {
+    return dsa::indexer_logits_c8_launch(q_bf16, weights, index_k_pool_c8, num_pages, block_table, max_pages,
+                                         seq_lens, cu_q, B, max_seq_len, max_q_len, row_begin, row_end, logits, ld,
+                                         workspace, ws_bytes, dev_err, stream);
 }

@@ -12,6 +12,7 @@
 // definition, so the rotated key is bit-identical to it.  The work is HBM-bound: 256 bytes read
 // and 132 bytes written per token.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
 #include "dsa_common.cuh"
@@ -403,5 +404,56 @@ extern "C" dsa_status dsa_store_latent_fp8(const void* latent_bf16, const int64_
     dsa::store_latent_fp8_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint32_t*>(latent_bf16), slot_mapping, n, k_scale, reinterpret_cast<uint16_t*>(kv_pool_fp8),
         num_pages, dev_err);
+    return dsa::launch_status();
+}
+
+// ---------------------------------------------------------------- int8 ("c8") index cache
+
+namespace dsa {
+namespace {
+
+// One warp per token: rotate with the bf16 Hadamard / sqrt(128), quantise to int8 with one scale
+// (c8_rotate_quant), write the 128 codes to row slot & 63 of page slot >> 6 and the scale, rounded
+// to fp16, to the page's scale area.  Follows vllm-ascend sfa_v1.py, indexer_select_pre_process with
+// use_sparse_c8_indexer (k_li @ qk_hadamard, npu_dynamic_quant, scale .to(float16)) and the
+// npu_scatter_nd_update_ of codes and scales by slot_mapping.
+__global__ void __launch_bounds__(256)
+store_index_k_c8_kernel(const uint16_t* __restrict__ keys, const int64_t* __restrict__ slots, int64_t n,
+                        uint8_t* __restrict__ pool, int64_t num_pages, int32_t* err) {
+    const int64_t token = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (token >= n) return;                      // warp-uniform
+    const int64_t slot = __ldg(slots + token);
+    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(keys + token * kIndexDim) + lane);
+    if (slot < 0) return;                        // padding token
+    const int64_t page = slot >> 6;
+    const int row = static_cast<int>(slot & 63);
+    if (page >= num_pages) {
+        if (lane == 0) raise_error(err, DSA_DEVERR_SLOT_RANGE);
+        return;
+    }
+    const float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
+    float scale;
+    const uint32_t packed = c8_rotate_quant(x, lane, &scale);
+    uint8_t* pg = pool + page * kC8PageBytes;
+    reinterpret_cast<uint32_t*>(pg + row * kIndexDim)[lane] = packed;
+    if (lane == 0) reinterpret_cast<__half*>(pg + kC8ScaleOffset)[row] = __float2half_rn(scale);
+}
+
+}  // namespace
+}  // namespace dsa
+
+extern "C" dsa_status dsa_store_index_k_c8(const void* k_bf16, const int64_t* slot_mapping, int64_t n,
+                                           uint8_t* index_k_pool_c8, int64_t num_pages, int32_t page_size,
+                                           int32_t* dev_err, void* stream) {
+    if (n < 0 || num_pages < 0) return DSA_ERR_INVALID_ARG;
+    if (page_size != dsa::kPage) return DSA_ERR_UNSUPPORTED;
+    if (n == 0) return DSA_OK;
+    if (!k_bf16 || !slot_mapping || !index_k_pool_c8) return DSA_ERR_INVALID_ARG;
+    if (!dsa::aligned16(k_bf16) || !dsa::aligned16(index_k_pool_c8)) return DSA_ERR_INVALID_ARG;
+    const int64_t blocks = (n + 7) / 8;
+    if (blocks > 0x7fffffffLL) return DSA_ERR_INVALID_ARG;
+    dsa::store_index_k_c8_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t*>(k_bf16), slot_mapping, n, index_k_pool_c8, num_pages, dev_err);
     return dsa::launch_status();
 }

@@ -21,6 +21,7 @@ import numpy as np
 import torch
 
 from . import capi
+from .capi import C8_PAGE_BYTES
 from .workloads import INDEX_DIM, INDEX_HEADS, INDEX_PAGE_BYTES, LATENT_DIM, VALUE_DIM, Workload
 
 
@@ -64,7 +65,7 @@ def logits_tile_rows(T: int, ld: int, budget_bytes: int = LOGITS_TILE_BUDGET_BYT
 class DeviceBatch:
     def __init__(self, wl: Workload, device: str = "cuda", with_latent: bool = True,
                  build_index_cache: bool = True, key_chunk: int = 1 << 20,
-                 logits_budget_bytes: int = LOGITS_TILE_BUDGET_BYTES, fused: bool = True):
+                 logits_budget_bytes: int = LOGITS_TILE_BUDGET_BYTES, fused: bool = True, c8: bool = False):
         self.wl = wl
         self.device = torch.device(device)
         dev = self.device
@@ -86,6 +87,18 @@ class DeviceBatch:
                 s = torch.from_numpy(slots[lo:lo + key_chunk]).to(dev)
                 capi.dsa_store_index_k(k, s, self.index_pool, self.dev_err)
             torch.cuda.synchronize(dev)
+        # the int8 ("c8") index cache of the same keys, when asked for
+        self.index_pool_c8 = None
+        if c8:
+            self.index_pool_c8 = torch.zeros((wl.num_pages, C8_PAGE_BYTES), dtype=torch.uint8, device=dev)
+            if build_index_cache:
+                keys = wl.index_keys()
+                slots = wl.token_slots()
+                for lo in range(0, keys.shape[0], key_chunk):
+                    k = _bf16(keys[lo:lo + key_chunk], dev)
+                    s = torch.from_numpy(slots[lo:lo + key_chunk]).to(dev)
+                    capi.dsa_store_index_k_c8(k, s, self.index_pool_c8, self.dev_err)
+                torch.cuda.synchronize(dev)
         self.ld = logits_ld(wl.max_seq_len)
         # the logits buffer holds one row tile; the step walks the tiles (indexer, then top-k)
         self.tile_rows = logits_tile_rows(wl.T, self.ld, logits_budget_bytes)
@@ -227,6 +240,14 @@ class DeviceBatch:
                                 self.wl.max_q_len, self.logits if logits is None else logits,
                                 row_begin=row_begin, row_end=row_end, flags=flags, dev_err=self.dev_err,
                                 stream=stream, workspace=self.idx_ws)
+
+    def indexer_logits_c8(self, row_begin: int = 0, row_end: Optional[int] = None, logits=None, stream=None,
+                          workspace=None):
+        """Logits over the int8 cache (DeviceBatch(c8=True)) of rows [row_begin, row_end)."""
+        capi.dsa_indexer_logits_c8(self.index_q, self.weights, self.index_pool_c8, self.block_table, self.seq_lens,
+                                   self.cu_q, self.wl.max_seq_len, self.wl.max_q_len,
+                                   self.logits if logits is None else logits, row_begin=row_begin, row_end=row_end,
+                                   dev_err=self.dev_err, stream=stream, workspace=workspace)
 
     def topk(self, logits=None, idx=None, row_begin: int = 0, row_end: Optional[int] = None, stream=None):
         lg = self.logits if logits is None else logits

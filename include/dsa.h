@@ -236,6 +236,62 @@ dsa_status dsa_indexer_logits(const void* q_bf16, const float* weights, const ui
                               void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream);
 
 /*
+ * dsa_store_index_k_c8 -- write n new indexer keys into the paged int8 ("c8") index-K cache.
+ * Source: vllm_ascend sfa_v1.py, AscendSFAImpl with enable_sparse_c8 (c8 k cache dtype int8, scale
+ * cache dtype float16; qk_hadamard = bf16 tensor of scipy.linalg.hadamard(128) / 128**0.5) and
+ * indexer_select_pre_process (k_li @ qk_hadamard; npu_dynamic_quant(k_li.view(-1, 128),
+ * dst_type=int8); scale .to(float16)); the npu_scatter_nd_update_ of codes (kv_cache[2]) and scales
+ * (kv_cache[3]) by slot_mapping.
+ * Per token t (c = bf16(128^-0.5) = 181 * 2^-11, the value of every entry of the bf16 matrix):
+ *   y_j = bf16_rn(c * sum_i (-1)^popcount(i & j) x_i)  (the exact sum rounded once: the correctly
+ *         rounded bf16 matrix product; the kernel's fp64 butterflies are exact for 128 bf16 values);
+ *   scale = max_j |y_j| / 127 (fp32, IEEE division);
+ *   code_j = round-to-nearest-even(y_j / scale) (fp32 IEEE division), in [-127, 127]; all 0 when
+ *            every y_j is 0;
+ *   page = slot >> 6, row = slot & 63: the 128 int8 codes to bytes [row*128, +128) of the page, the
+ *   scale rounded to fp16 (nearest even) to bytes [8192 + row*2, +2).
+ * (npu_dynamic_quant is not printed on the pages: the fp32 scale amax / 127 with nearest-even codes
+ * is the plain symmetric per-row quantisation.)
+ * Arguments:
+ *   k_bf16           [n, 128] bf16, row-major (16-byte aligned).
+ *   slot_mapping     [n] int64; slot < 0 marks a padding token and is skipped.
+ *   index_k_pool_c8  uint8 [num_pages, 8320] (16-byte aligned), written in place.
+ *   page_size        must be 64 (DSA_ERR_UNSUPPORTED otherwise).
+ *   dev_err          nullable; DSA_DEVERR_SLOT_RANGE when slot >= num_pages * 64 (token skipped).
+ * Results are bit-exact with the CPU definition above.
+ */
+dsa_status dsa_store_index_k_c8(const void* k_bf16, const int64_t* slot_mapping, int64_t n,
+                                uint8_t* index_k_pool_c8, int64_t num_pages, int32_t page_size,
+                                int32_t* dev_err, void* stream);
+
+/*
+ * dsa_indexer_logits_c8 -- lightning-indexer logits over the int8 ("c8") index-K cache.
+ * Source: vllm_ascend sfa_v1.py, indexer_select_post_process with use_sparse_c8_indexer: q_li @
+ * qk_hadamard, npu_dynamic_quant per (token, head), weights.to(float16), then
+ * npu_lightning_indexer_quant(query, key, weights, query_dequant_scale, key_dequant_scale,
+ * query_quant_mode=0, key_quant_mode=0, ...).
+ *   Query prologue, per row r and head h: the transform of dsa_store_index_k_c8 (rotation, int8
+ *   codes cq[r,h,:], fp32 scale rounded to fp16 qs16[r,h]); g[r,h] = w16[r,h] * qs16[r,h] with
+ *   w16 = fp16_rn(weights[r,h]) (exact in fp32).
+ *   I[r,s] = ks16[s] * sum_h g[r,h] * ReLU(sum_d cq[r,h,d] * ck[s,d]),  s < v_r
+ *   -- the lightning-indexer score on the dequantised query and keys.  The integer dot products are
+ *   exact (the int8 values are widened to f16 and multiplied on the tensor cores with fp32
+ *   accumulation, exact below 2^24); the head sum is fp32.
+ * Arguments: as dsa_indexer_logits, without flags; index_k_pool_c8 is uint8 [num_pages, 8320]
+ *   written by dsa_store_index_k_c8; workspace at least dsa_indexer_logits_c8_workspace_size(
+ *   row_end - row_begin) bytes (16-byte aligned, caller-owned; it holds the rows' f16 query codes).
+ * Two kernels are enqueued on `stream` (query prologue, then the logits kernel as its programmatic
+ * dependent).  The top-k over these logits is dsa_topk.
+ */
+size_t dsa_indexer_logits_c8_workspace_size(int32_t rows);
+dsa_status dsa_indexer_logits_c8(const void* q_bf16, const float* weights, const uint8_t* index_k_pool_c8,
+                                 int64_t num_pages, const int32_t* block_table, int32_t max_pages,
+                                 const int32_t* seq_lens, const int32_t* cu_q, int32_t B,
+                                 int32_t max_seq_len, int32_t max_q_len, int32_t row_begin,
+                                 int32_t row_end, float* logits, int64_t ld, void* workspace,
+                                 size_t ws_bytes, int32_t* dev_err, void* stream);
+
+/*
  * dsa_topk -- per-row top-k of the indexer logits.
  * Source: sglang dsa_indexer.py, forward_indexer (logits.topk(min(topk, seq_len)) then -1
  * padding to 2048), Indexer._get_topk_paged (topk_transform; rows not scored are -1).

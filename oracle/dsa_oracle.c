@@ -530,6 +530,19 @@ void dsa_oracle_quant_int8(const float* y, int n, int8_t* codes, float* scale) {
  * [8192, 8320) the 64 fp16 scales.  Returns the number of tokens whose slot pointed past the pool. */
 int64_t dsa_oracle_store_index_k_c8(const uint16_t* k_bf16, const int64_t* slot_mapping, int64_t n,
                                     uint8_t* pool, int64_t num_pages) {
+    /* every token's codes and scale (independent per token), then the scatter in token order */
+    int8_t* codes = (int8_t*)malloc((size_t)(n > 0 ? n : 1) * DI);
+    uint16_t* sc16 = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(n > 0 ? n : 1));
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < n; ++t) {
+        if (slot_mapping[t] < 0 || slot_mapping[t] / PAGE >= num_pages) continue;
+        uint16_t rot[DI];
+        float y[DI], sc;
+        dsa_oracle_c8_rotate128(k_bf16 + t * DI, rot);
+        for (int d = 0; d < DI; ++d) y[d] = bf16_bits_to_f32(rot[d]);
+        dsa_oracle_quant_int8(y, DI, codes + t * DI, &sc);
+        sc16[t] = dsa_oracle_f32_to_f16(sc);
+    }
     int64_t bad = 0;
     for (int64_t t = 0; t < n; ++t) {
         const int64_t slot = slot_mapping[t];
@@ -539,18 +552,13 @@ int64_t dsa_oracle_store_index_k_c8(const uint16_t* k_bf16, const int64_t* slot_
             ++bad;
             continue;
         }
-        uint16_t rot[DI];
-        float y[DI], sc;
-        int8_t codes[DI];
-        dsa_oracle_c8_rotate128(k_bf16 + t * DI, rot);
-        for (int d = 0; d < DI; ++d) y[d] = bf16_bits_to_f32(rot[d]);
-        dsa_oracle_quant_int8(y, DI, codes, &sc);
         uint8_t* pg = pool + page * C8_PAGE_BYTES;
-        memcpy(pg + (slot % PAGE) * DI, codes, DI);
-        const uint16_t h = dsa_oracle_f32_to_f16(sc);
-        pg[PAGE * DI + (slot % PAGE) * 2] = (uint8_t)(h & 0xff);
-        pg[PAGE * DI + (slot % PAGE) * 2 + 1] = (uint8_t)(h >> 8);
+        memcpy(pg + (slot % PAGE) * DI, codes + t * DI, DI);
+        pg[PAGE * DI + (slot % PAGE) * 2] = (uint8_t)(sc16[t] & 0xff);
+        pg[PAGE * DI + (slot % PAGE) * 2 + 1] = (uint8_t)(sc16[t] >> 8);
     }
+    free(codes);
+    free(sc16);
     return bad;
 }
 

@@ -89,3 +89,22 @@ def test_host_side_validation_of_the_next_row_calls(lib):
     assert need == 2 * 4096 * 4 + (2 * (64 * 128 + 64 * 4) + 255) // 256 * 256 + 2 * 100 * 4
     assert L.dsa_lightning_indexer(None, None, None, 0, None, 0, None, None, 1, 100, 1, 2, 16, 0, 0, 0,
                                    ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000), need - 16, None, None) == 1
+
+
+def test_host_side_validation_of_the_c8_calls(lib):
+    """The int8 ("c8") cache's store and logits calls check their arguments before any CUDA call."""
+    capi.load()
+    L = capi._lib
+    assert L.dsa_store_index_k_c8(None, None, 0, None, 0, 64, None, None) == 0      # n = 0
+    assert L.dsa_store_index_k_c8(None, None, 4, None, 1, 32, None, None) == 2      # page size 32
+    assert L.dsa_store_index_k_c8(None, None, 4, None, 1, 64, None, None) == 1      # null pointers
+    assert L.dsa_store_index_k_c8(ctypes.c_void_p(0x1008), ctypes.c_void_p(0x2000), 4, ctypes.c_void_p(0x3000), 1,
+                                  64, None, None) == 1                              # misaligned keys
+    # f16 query codes (64 heads x 128 dims x 2 B) + fp32 gates per row
+    assert L.dsa_indexer_logits_c8_workspace_size(3) == 3 * (64 * 128 * 2 + 64 * 4)
+    assert L.dsa_indexer_logits_c8_workspace_size(0) == 0
+    assert L.dsa_indexer_logits_c8(None, None, None, 0, None, 0, None, None, 1, 10, 1, 0, 1, None, 10, None, 0,
+                                   None, None) == 1                                 # null pointers
+    assert L.dsa_indexer_logits_c8(None, None, None, 0, None, 0, None, None, 0, 10, 1, 0, 1, None, 10, None, 0,
+                                   None, None) == 0                                 # empty batch
+
