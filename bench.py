@@ -59,7 +59,8 @@ def algorithmic_work(wl):
     top-k:   4 B per (row, visible key) read + 4k B per row written.
     MLA:     per row: k * 1152 B gathered + q (H*576*2) + out (H*512*2) + idx (4k) + lse (4H);
              2 * H * k_valid * (576 + 512) FLOP.
-    store:   per new token 256 B read + 132 B written + 8 B slot."""
+    store:   per new token 256 B read + 132 B written + 8 B slot.
+    indexer_c8: as indexer with 130 B per key (128 int8 codes + an fp16 scale)."""
     import numpy as np
     vis = wl.visible_lens().astype(np.int64)
     keys_per_req = wl.seq_lens.astype(np.int64)
@@ -71,7 +72,9 @@ def algorithmic_work(wl):
     mla_b = int(kvalid.sum()) * 1152 + T * H * 576 * 2 + T * H * 512 * 2 + T * k * 4 + T * H * 4
     mla_f = int(kvalid.sum()) * 2 * H * (576 + 512)
     store_b = T * (256 + 132 + 8)
-    return {"store": (store_b, 0), "indexer": (idx_b, idx_f), "topk": (topk_b, 0), "mla": (mla_b, mla_f)}
+    idx8_b = idx_b - int(keys_per_req.sum()) * 2
+    return {"store": (store_b, 0), "indexer": (idx_b, idx_f), "topk": (topk_b, 0), "mla": (mla_b, mla_f),
+            "indexer_c8": (idx8_b, idx_f)}
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -411,7 +414,7 @@ def run_gpu(args):
 
     from deepseek_sparse_attention_paged_gb300 import distributed as D
     wl = D.rank_workload(args.workload, rank)   # every rank its own batch of the same shape
-    db = DeviceBatch(wl)
+    db = DeviceBatch(wl, c8=True)   # the int8 index cache too, for its stage line
     stream = torch.cuda.Stream()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
 
@@ -435,6 +438,8 @@ def run_gpu(args):
         lambda: capi.dsa_sparse_mla_decode_fp8(db.mla_q, FP8_Q_SCALE, kv8, FP8_K_SCALE, db.block_table, db.seq_lens,
                                                db.cu_q, db.idx, wl.scale, out8, db.mla_ws, lse=lse8,
                                                dev_err=db.dev_err), stream, flush)
+    # the int8 ("c8") index-cache variant of the indexer logits over the same keys
+    stage_graphs["indexer_c8"] = TimedGraph(lambda: db.indexer_c8_stage(), stream, flush)
     st, word = db.device_error()
     if st != 0:
         raise RuntimeError(f"device error word {word} after warm-up")

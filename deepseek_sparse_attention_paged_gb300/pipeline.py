@@ -290,6 +290,15 @@ class DeviceBatch:
         for rb, re in self.tiles():
             self.indexer_logits(row_begin=rb, row_end=re, stream=stream)
 
+    def indexer_c8_stage(self, stream=None):
+        """The indexer logits of every tile over the int8 cache (DeviceBatch(c8=True)), into the
+        logits buffer, with a workspace of its own (allocated once)."""
+        if getattr(self, "_c8_ws", None) is None:
+            self._c8_ws = torch.empty(max(16, capi.dsa_indexer_logits_c8_workspace_size(self.tile_rows)),
+                                      dtype=torch.uint8, device=self.device)
+        for rb, re in self.tiles():
+            self.indexer_logits_c8(row_begin=rb, row_end=re, logits=self.logits, stream=stream, workspace=self._c8_ws)
+
     def topk_stage(self, stream=None):
         """The top-k of every tile over the logits buffer as it stands: the top-k stage timed alone."""
         for rb, re in self.tiles():
