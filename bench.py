@@ -724,12 +724,25 @@ def run_profile(args):
         torch.cuda.synchronize()
         print(json.dumps({"profile": args.profile, "launches": args.warmup + args.steps}))
         return
-    need_latent = args.profile in ("mla", "step")
-    db = DeviceBatch(wl, with_latent=need_latent)
-    if args.profile in ("topk", "mla"):
+    need_latent = args.profile in ("mla", "step", "mla_fp8")
+    db = DeviceBatch(wl, with_latent=need_latent, c8=args.profile == "indexer_c8")
+    if args.profile in ("topk", "mla", "mla_fp8"):
         db.select()
-    fn = {"store": db.store_new_keys, "indexer": db.indexer_stage, "topk": db.topk_stage,
-          "mla": db.sparse_mla, "step": db.step}[args.profile]
+    if args.profile == "mla_fp8":
+        # the FP8 latent cache of the same rows; the bf16 cache is dropped once it is quantised
+        kv8 = torch.empty((wl.num_pages, 64, 576), dtype=torch.uint8, device="cuda")
+        capi.dsa_store_latent_fp8(db.kv_pool.view(-1, 576), torch.arange(wl.num_pages * 64, device="cuda"),
+                                  FP8_K_SCALE, kv8)
+        torch.cuda.synchronize()
+        db.kv_pool = None
+        torch.cuda.empty_cache()
+        out8, lse8 = torch.empty_like(db.out), torch.empty_like(db.lse)
+        fn = lambda: capi.dsa_sparse_mla_decode_fp8(db.mla_q, FP8_Q_SCALE, kv8, FP8_K_SCALE, db.block_table,
+                                                    db.seq_lens, db.cu_q, db.idx, wl.scale, out8, db.mla_ws,
+                                                    lse=lse8, dev_err=db.dev_err)
+    else:
+        fn = {"store": db.store_new_keys, "indexer": db.indexer_stage, "topk": db.topk_stage,
+              "mla": db.sparse_mla, "step": db.step, "indexer_c8": db.indexer_c8_stage}[args.profile]
     for _ in range(args.warmup + args.steps):
         fn()
     torch.cuda.synchronize()
@@ -742,7 +755,8 @@ def run_profile(args):
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
-    ap.add_argument("--profile", choices=["store", "indexer", "topk", "mla", "step", "prologue", "rope_q", "absorb",
+    ap.add_argument("--profile", choices=["store", "indexer", "topk", "mla", "step", "indexer_c8", "mla_fp8",
+                                          "prologue", "rope_q", "absorb",
                                           "v_up", "absorb4k"],
                     default=None,
                     help="launch one stage warmup+steps times without timing (for ncu) and exit")
