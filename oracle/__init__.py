@@ -103,6 +103,11 @@ def _load():
                                             f64, P, i64, P, P]),
         "dsa_oracle_lse_merge": (None, [P, P, P, P, i64, i32, P, P]),
         "dsa_oracle_f16_decode": (f64, [ctypes.c_uint16]),
+        "dsa_oracle_visible_len_cmp": (i32, [P, P, i32, i64, i32]),
+        "dsa_oracle_indexer_logits_cmp": (i64, [P, P, P, i64, P, i32, P, P, i32, i32, i32, P, i64, P, i64, P]),
+        "dsa_oracle_topk_cmp": (None, [P, i64, P, P, i32, P, i64, i32, i32, P]),
+        "dsa_oracle_dsv4_attention": (i64, [P, P, i64, P, i32, P, i64, P, i32, P, P, i32, P, i32, i32, i32, P, i32,
+                                            f64, P, i64, P, P]),
         "dsa_oracle_f32_to_f16": (ctypes.c_uint16, [ctypes.c_float]),
         "dsa_oracle_c8_rotate128": (None, [P, P]),
         "dsa_oracle_quant_int8": (None, [P, ctypes.c_int, P, P]),
@@ -257,10 +262,10 @@ def visible_len(seq_lens, cu_q, r: int) -> int:
 
 
 def indexer_logits(q_bf16, w, pool, block_table, seq_lens, cu_q, rows, ld, rotate_q=False,
-                   want_mag=False, fill=np.nan, ue8m0_q=False):
+                   want_mag=False, fill=np.nan, ue8m0_q=False, cmp_ratio=1):
     """Indexer logits for the global rows ``rows``; returns float32 [len(rows), ld] (and the
-    float64 magnitude array when ``want_mag``).  Entries past each row's visible length keep
-    ``fill``."""
+    float64 magnitude array when ``want_mag``).  Entries past each row's visible length (of
+    compressed entries when ``cmp_ratio`` > 1) keep ``fill``."""
     q = _c(q_bf16, np.uint16)
     wv = _c(w, np.float32)
     pool = _c(pool, np.uint8)
@@ -270,25 +275,54 @@ def indexer_logits(q_bf16, w, pool, block_table, seq_lens, cu_q, rows, ld, rotat
     rr = _c(rows, np.int64)
     out = np.full((rr.shape[0], ld), fill, np.float32)
     mag = np.zeros((rr.shape[0], ld), np.float64) if want_mag else None
-    bad = _load().dsa_oracle_indexer_logits(
+    bad = _load().dsa_oracle_indexer_logits_cmp(
         _p(q), _p(wv), _p(pool), pool.shape[0], _p(bt), bt.shape[1], _p(sl), _p(cq), sl.shape[0],
-        int(bool(rotate_q)) | (int(bool(ue8m0_q)) << 1), _p(rr), rr.shape[0], _p(out), ld,
+        int(bool(rotate_q)) | (int(bool(ue8m0_q)) << 1), int(cmp_ratio), _p(rr), rr.shape[0], _p(out), ld,
         _p(mag) if mag is not None else None)
     if want_mag:
         return out, mag, int(bad)
     return out
 
 
-def topk(logits, seq_lens, cu_q, rows, k):
+def topk(logits, seq_lens, cu_q, rows, k, cmp_ratio=1):
     """Per-row top-k indices (ascending index order, -1 padded) for logits rows of ``rows``."""
     lg = _c(logits, np.float32)
     sl = _c(seq_lens, np.int32)
     cq = _c(cu_q, np.int32)
     rr = _c(rows, np.int64)
     idx = np.empty((rr.shape[0], k), np.int32)
-    _load().dsa_oracle_topk(_p(lg), lg.shape[1], _p(sl), _p(cq), sl.shape[0], _p(rr), rr.shape[0],
-                            int(k), _p(idx))
+    _load().dsa_oracle_topk_cmp(_p(lg), lg.shape[1], _p(sl), _p(cq), sl.shape[0], _p(rr), rr.shape[0],
+                                int(k), int(cmp_ratio), _p(idx))
     return idx
+
+
+def visible_len_cmp(seq_lens, cu_q, r: int, ratio: int) -> int:
+    sl = _c(seq_lens, np.int32)
+    cq = _c(cu_q, np.int32)
+    return int(_load().dsa_oracle_visible_len_cmp(_p(sl), _p(cq), sl.size, int(r), int(ratio)))
+
+
+def dsv4_attention(q_bf16, swa_kv_bf16, swa_block_table, cmp_kv_bf16, cmp_block_table, seq_lens, cu_q, cmp_idx,
+                   window, sinks, scale, rows, ratio=4):
+    """Window + selected compressed entries + per-head sinks: (out [n, H, 512] f64, lse [n, H] f64, skipped)."""
+    q = _c(q_bf16, np.uint16)
+    T, H = q.shape[0], q.shape[1]
+    sw = _c(swa_kv_bf16, np.uint16).reshape(-1, PAGE, DQK)
+    ck = _c(cmp_kv_bf16, np.uint16).reshape(-1, PAGE, DQK)
+    sbt = _c(swa_block_table, np.int32)
+    cbt = _c(cmp_block_table, np.int32)
+    sl = _c(seq_lens, np.int32)
+    cq = _c(cu_q, np.int32)
+    ix = _c(cmp_idx, np.int32)
+    sk = _c(sinks, np.float32)
+    rw = _c(rows, np.int64)
+    out = np.empty((rw.size, H, DV), np.float64)
+    lse = np.empty((rw.size, H), np.float64)
+    bad = _load().dsa_oracle_dsv4_attention(_p(q), _p(sw), sw.shape[0], _p(sbt), sbt.shape[1], _p(ck), ck.shape[0],
+                                            _p(cbt), cbt.shape[1], _p(sl), _p(cq), sl.size, _p(ix), ix.shape[1],
+                                            int(window), int(ratio), _p(sk), H, float(scale), _p(rw), rw.size,
+                                            _p(out), _p(lse))
+    return out, lse, int(bad)
 
 
 def topk_forced(logits, seq_lens, cu_q, rows, k, n_init, n_local):

@@ -363,6 +363,16 @@ int32_t dsa_oracle_visible_len(const int32_t* seq_lens, const int32_t* cu_q, int
     return (int32_t)v;
 }
 
+/* Visible entries of a compressed cache ([dsa] AscendDSAImpl._forward_decode with compress_ratio
+ * 4: npu_vllm_quant_lightning_indexer(..., actual_seq_lengths_key = seq_lens, sparse_mode = 3,
+ * cmp_ratio = 4) and the attention's cmp_mask_mode = 3).  Reading: compressed entry e stands for
+ * the tokens [ratio e, ratio e + ratio) and a row sees it once all of them are visible, i.e. the
+ * row's visible length (above) divided by the ratio, rounded down. */
+int32_t dsa_oracle_visible_len_cmp(const int32_t* seq_lens, const int32_t* cu_q, int32_t B, int64_t r,
+                                   int32_t ratio) {
+    return dsa_oracle_visible_len(seq_lens, cu_q, B, r) / ratio;
+}
+
 /* ---------------------------------------------------------------- indexer logits */
 
 /* Lightning-indexer logits over the paged FP8 cache ([idx] Indexer._get_topk_paged: paged MQA
@@ -379,17 +389,20 @@ int32_t dsa_oracle_visible_len(const int32_t* seq_lens, const int32_t* cu_q, int
  * mag (nullable, double [n_rows, ld]) receives sum_h |w'| * ReLU(...), the magnitude of the
  * terms, which bounds the rounding error of any evaluation order.
  * Returns the number of (row, key) pairs skipped because the page id was out of range. */
-int64_t dsa_oracle_indexer_logits(const uint16_t* q_bf16, const float* w, const uint8_t* pool,
-                                  int64_t num_pages, const int32_t* block_table, int32_t max_pages,
-                                  const int32_t* seq_lens, const int32_t* cu_q, int32_t B,
-                                  int32_t q_mode, const int64_t* rows, int64_t n_rows,
-                                  float* logits, int64_t ld, double* mag) {
+/* With cmp_ratio > 1 the cache holds compressed entries and row r scores entries
+ * s < dsa_oracle_visible_len_cmp(r) (the DSV4 indexer over the compressed index keys, [dsa]
+ * indexer_select_qli / npu_vllm_quant_lightning_indexer(..., cmp_ratio = 4)). */
+int64_t dsa_oracle_indexer_logits_cmp(const uint16_t* q_bf16, const float* w, const uint8_t* pool,
+                                      int64_t num_pages, const int32_t* block_table, int32_t max_pages,
+                                      const int32_t* seq_lens, const int32_t* cu_q, int32_t B,
+                                      int32_t q_mode, int32_t cmp_ratio, const int64_t* rows, int64_t n_rows,
+                                      float* logits, int64_t ld, double* mag) {
     int64_t bad = 0;
     for (int64_t i = 0; i < n_rows; ++i) {
         int64_t r = rows[i];
         int b = row_request(cu_q, B, r);
         if (b < 0) continue;
-        int32_t v = dsa_oracle_visible_len(seq_lens, cu_q, B, r);
+        int32_t v = dsa_oracle_visible_len_cmp(seq_lens, cu_q, B, r, cmp_ratio);
         /* query prologue: per head, optional rotation, then per-128 quantisation */
         uint8_t cq[HI][DI];
         double wq[HI];
@@ -436,6 +449,15 @@ int64_t dsa_oracle_indexer_logits(const uint16_t* q_bf16, const float* w, const 
         bad += row_bad;
     }
     return bad;
+}
+
+int64_t dsa_oracle_indexer_logits(const uint16_t* q_bf16, const float* w, const uint8_t* pool,
+                                  int64_t num_pages, const int32_t* block_table, int32_t max_pages,
+                                  const int32_t* seq_lens, const int32_t* cu_q, int32_t B,
+                                  int32_t q_mode, const int64_t* rows, int64_t n_rows,
+                                  float* logits, int64_t ld, double* mag) {
+    return dsa_oracle_indexer_logits_cmp(q_bf16, w, pool, num_pages, block_table, max_pages, seq_lens, cu_q, B,
+                                         q_mode, 1, rows, n_rows, logits, ld, mag);
 }
 
 /* ---------------------------------------------------------------- int8 ("c8") index-K cache */
@@ -654,11 +676,12 @@ static int cmp_i32(const void* pa, const void* pb) {
  * the first min(k, v) entries of a stable descending sort of I[r, 0:v) (lower index wins ties),
  * returned in ascending index order, padded with -1 to k.  rows[i] gives the global row (for its
  * visible length); logits row i is logits[i*ld ...]. */
-void dsa_oracle_topk(const float* logits, int64_t ld, const int32_t* seq_lens, const int32_t* cu_q,
-                     int32_t B, const int64_t* rows, int64_t n_rows, int32_t k, int32_t* idx) {
+/* With cmp_ratio > 1 the row's visible length is that of the compressed entries. */
+void dsa_oracle_topk_cmp(const float* logits, int64_t ld, const int32_t* seq_lens, const int32_t* cu_q,
+                         int32_t B, const int64_t* rows, int64_t n_rows, int32_t k, int32_t cmp_ratio, int32_t* idx) {
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t i = 0; i < n_rows; ++i) {
-        int32_t v = dsa_oracle_visible_len(seq_lens, cu_q, B, rows[i]);
+        int32_t v = dsa_oracle_visible_len_cmp(seq_lens, cu_q, B, rows[i], cmp_ratio);
         int32_t* out = idx + i * (int64_t)k;
         keyed_t* keys = (keyed_t*)malloc(sizeof(keyed_t) * (size_t)(v > 0 ? v : 1));
         for (int32_t s = 0; s < v; ++s) {
@@ -672,6 +695,11 @@ void dsa_oracle_topk(const float* logits, int64_t ld, const int32_t* seq_lens, c
         for (int32_t j = n; j < k; ++j) out[j] = -1;
         free(keys);
     }
+}
+
+void dsa_oracle_topk(const float* logits, int64_t ld, const int32_t* seq_lens, const int32_t* cu_q,
+                     int32_t B, const int64_t* rows, int64_t n_rows, int32_t k, int32_t* idx) {
+    dsa_oracle_topk_cmp(logits, ld, seq_lens, cu_q, B, rows, n_rows, k, 1, idx);
 }
 
 /* ---------------------------------------------------------------- sparse MLA */
@@ -757,6 +785,81 @@ int64_t dsa_oracle_sparse_mla(const uint16_t* q_bf16, const uint16_t* kv, int64_
         attend_rows(q_bf16 + (r * H + h) * DQK, kv, g, n, scale, out + (ri * H + h) * DV,
                     lse + ri * H + h, psum ? psum + ri * H + h : NULL);
         free(g);
+        if (h == 0) bad_total += bad;
+    }
+    return bad_total;
+}
+
+/* ---------------------------------------------------------------- DSV4: window + compressed entries + sinks */
+
+/* Decode attention of the compressed-KV variant with compress ratio 4 ([dsa]
+ * AscendDSAImpl._forward_decode: attn_op(q, ori_kv = swa_kv_cache, cmp_kv = compress_kv_cache,
+ * cmp_sparse_indices = compress_topk_idxs, ori_block_table, cmp_block_table, seqused_kv = seq_lens,
+ * sinks = attn_sink, softmax_scale, cmp_ratio = 4, ori_mask_mode = 4 (sliding window),
+ * cmp_mask_mode = 3, ori_win_left = window_size - 1, ori_win_right = 0)).  For row r at absolute
+ * position p (visible length v = p + 1) and head h, the keys are
+ *   - the window: original-cache positions max(0, p - window + 1) .. p (through swa_block_table);
+ *   - the selected compressed entries: cmp_idx[r, j] >= 0 with cmp_idx < v / ratio (through
+ *     cmp_block_table; other entries are skipped and counted);
+ * one softmax over all of them with the head's sink logit in the denominator:
+ *   S_i = scale * <q, c_i>;  D = sum_i exp(S_i) + exp(sink_h);  o = sum_i exp(S_i) / D * c_i[0:512];
+ *   lse = log D.
+ * Readings (the op's source is not printed): the rows are 576-wide latent rows like the MLA cache
+ * (score over all 576 dims, value = the first 512); an entry present in both sets counts twice
+ * (they are different vectors); with no key at all o = 0 and lse = sink_h.
+ * out: double [n_rows, H, 512], lse: double [n_rows, H].  Returns the skipped entries. */
+int64_t dsa_oracle_dsv4_attention(const uint16_t* q_bf16, const uint16_t* swa_kv, int64_t swa_pages,
+                                  const int32_t* swa_block_table, int32_t swa_max_pages, const uint16_t* cmp_kv,
+                                  int64_t cmp_pages, const int32_t* cmp_block_table, int32_t cmp_max_pages,
+                                  const int32_t* seq_lens, const int32_t* cu_q, int32_t B, const int32_t* cmp_idx,
+                                  int32_t k, int32_t window, int32_t ratio, const float* sinks, int32_t H,
+                                  double scale, const int64_t* rows, int64_t n_rows, double* out, double* lse) {
+    int64_t bad_total = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : bad_total)
+    for (int64_t i = 0; i < n_rows * H; ++i) {
+        const int64_t ri = i / H;
+        const int h = (int)(i % H);
+        const int64_t r = rows[ri];
+        const int b = row_request(cu_q, B, r);
+        const int32_t v = dsa_oracle_visible_len(seq_lens, cu_q, B, r);
+        const int32_t vc = v / ratio;
+        const int64_t nmax = (int64_t)window + k;
+        const uint16_t** rowp = (const uint16_t**)malloc(sizeof(uint16_t*) * (size_t)(nmax > 0 ? nmax : 1));
+        int64_t n = 0, bad = 0;
+        for (int32_t pos = v - window > 0 ? v - window : 0; b >= 0 && pos < v; ++pos) {
+            const int64_t g = latent_row(swa_block_table, swa_max_pages, swa_pages, b, pos);
+            if (g < 0) { ++bad; continue; }
+            rowp[n++] = swa_kv + g * DQK;
+        }
+        for (int32_t j = 0; b >= 0 && j < k; ++j) {
+            const int32_t e = cmp_idx[r * (int64_t)k + j];
+            if (e < 0) continue;
+            const int64_t g = e < vc ? latent_row(cmp_block_table, cmp_max_pages, cmp_pages, b, e) : -1;
+            if (g < 0) { ++bad; continue; }
+            rowp[n++] = cmp_kv + g * DQK;
+        }
+        double q[DQK];
+        for (int d = 0; d < DQK; ++d) q[d] = (double)bf16_bits_to_f32(q_bf16[(r * H + h) * DQK + d]);
+        double* S = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+        const double sink = (double)sinks[h];
+        double m = sink;
+        for (int64_t t = 0; t < n; ++t) {
+            double dot = 0.0;
+            for (int d = 0; d < DQK; ++d) dot += q[d] * (double)bf16_bits_to_f32(rowp[t][d]);
+            S[t] = scale * dot;
+            if (S[t] > m) m = S[t];
+        }
+        double D = exp(sink - m);
+        for (int64_t t = 0; t < n; ++t) D += exp(S[t] - m);
+        double* o = out + (ri * H + h) * DV;
+        for (int d = 0; d < DV; ++d) o[d] = 0.0;
+        for (int64_t t = 0; t < n; ++t) {
+            const double pw = exp(S[t] - m) / D;
+            for (int d = 0; d < DV; ++d) o[d] += pw * (double)bf16_bits_to_f32(rowp[t][d]);
+        }
+        lse[ri * H + h] = m + log(D);
+        free(S);
+        free(rowp);
         if (h == 0) bad_total += bad;
     }
     return bad_total;
