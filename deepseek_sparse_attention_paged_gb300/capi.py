@@ -34,6 +34,7 @@ DSA_NORM_RMS = 0x2
 DSA_ROPE_INTERLEAVED = 0x4
 DSA_K_NO_ROTATE = 0x8
 DSA_SCALE_UE8M0 = 0x10
+DSA_KEYS_CMP4 = 0x20          # the index cache holds compressed keys, one per 4 tokens
 PAGE_SIZE = 64
 INDEX_PAGE_BYTES = 64 * 132
 C8_PAGE_BYTES = 64 * 130      # int8 index cache page: 64 x 128 codes + 64 fp16 scales
@@ -99,6 +100,9 @@ def load(path: str = LIB_PATH):
                                                          ctypes.c_float, P, P, P, P]),
         "dsa_store_latent_fp8": (ctypes.c_int, [P, P, i64, ctypes.c_float, P, i64, P, P]),
         "dsa_store_index_k_c8": (ctypes.c_int, [P, P, i64, P, i64, i32, P, P]),
+        "dsa_sparse_attn_swa_cmp_workspace_size": (sz, [i32, i32, i32]),
+        "dsa_sparse_attn_swa_cmp": (ctypes.c_int, [P, P, i64, P, i32, P, i64, P, i32, P, P, i32, P, i32, i32, i32, P,
+                                                   i32, i32, ctypes.c_float, P, P, P, sz, P, P]),
         "dsa_indexer_logits_c8_workspace_size": (sz, [i32]),
         "dsa_indexer_logits_c8": (ctypes.c_int, [P, P, P, i64, P, i32, P, P, i32, i32, i32, i32, i32, P, i64, P, sz,
                                                  P, P]),
@@ -444,6 +448,48 @@ def dsa_sparse_mla_decode(q_bf16: torch.Tensor, kv_pool: torch.Tensor, block_tab
         _ptr(cu_q), B, _ptr(idx), idx.shape[1], T, H, float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(dev_err), _stream(stream)))
     _count(2 if T > 0 else 0)
+
+
+def dsa_sparse_attn_swa_cmp_workspace_size(T: int, H: int, window: int) -> int:
+    return int(load().dsa_sparse_attn_swa_cmp_workspace_size(int(T), int(H), int(window)))
+
+
+def dsa_sparse_attn_swa_cmp(q_bf16: torch.Tensor, swa_kv: torch.Tensor, swa_block_table: torch.Tensor,
+                            cmp_kv: torch.Tensor, cmp_block_table: torch.Tensor, seq_lens: torch.Tensor,
+                            cu_q: torch.Tensor, cmp_idx: torch.Tensor, window: int, cmp_ratio: int,
+                            sinks: torch.Tensor, scale: float, out: torch.Tensor,
+                            workspace: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                            dev_err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Sliding window of the original cache + selected compressed entries + per-head sinks."""
+    lib = load()
+    _cuda(q_bf16, torch.bfloat16, "q_bf16")
+    _cuda(swa_kv, torch.bfloat16, "swa_kv")
+    _cuda(cmp_kv, torch.bfloat16, "cmp_kv")
+    for t, n in ((swa_block_table, "swa_block_table"), (cmp_block_table, "cmp_block_table"), (seq_lens, "seq_lens"),
+                 (cu_q, "cu_q"), (cmp_idx, "cmp_idx")):
+        _cuda(t, torch.int32, n)
+    _cuda(sinks, torch.float32, "sinks")
+    _cuda(out, torch.bfloat16, "out")
+    if lse is not None:
+        _cuda(lse, torch.float32, "lse")
+    _need(q_bf16.dim() == 3 and q_bf16.shape[2] == LATENT_DIM, "q_bf16 must be [T, H, 576]")
+    T, H, _ = q_bf16.shape
+    for kv, n in ((swa_kv, "swa_kv"), (cmp_kv, "cmp_kv")):
+        _need(kv.dim() == 3 and tuple(kv.shape[1:]) == (64, LATENT_DIM), f"{n} must be [pages, 64, 576]")
+    _need(cmp_idx.dim() == 2 and cmp_idx.shape[0] == T, "cmp_idx must be [T, k]")
+    _need(sinks.numel() == H, "sinks must be [H]")
+    _need(tuple(out.shape) == (T, H, VALUE_DIM), "out must be [T, H, 512]")
+    if workspace is None:
+        workspace = torch.empty(max(16, dsa_sparse_attn_swa_cmp_workspace_size(T, H, window)), dtype=torch.uint8,
+                                device=q_bf16.device)
+    _need(workspace.is_cuda and workspace.is_contiguous(), "workspace must be a contiguous CUDA tensor")
+    B = seq_lens.numel()
+    _check("dsa_sparse_attn_swa_cmp", lib.dsa_sparse_attn_swa_cmp(
+        _ptr(q_bf16), _ptr(swa_kv), swa_kv.shape[0], _ptr(swa_block_table), swa_block_table.shape[1], _ptr(cmp_kv),
+        cmp_kv.shape[0], _ptr(cmp_block_table), cmp_block_table.shape[1], _ptr(seq_lens), _ptr(cu_q), B,
+        _ptr(cmp_idx), cmp_idx.shape[1], int(window), int(cmp_ratio), _ptr(sinks), T, H, float(scale), _ptr(out),
+        _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_err), _stream(stream)))
+    _count(4 if T > 0 else 0)
 
 
 def dsa_store_latent_fp8(latent_bf16: torch.Tensor, slot_mapping: torch.Tensor, k_scale: float,

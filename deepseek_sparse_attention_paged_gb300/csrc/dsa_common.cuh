@@ -152,6 +152,6 @@ dsa_status indexer_logits_c8_launch(const void* q_bf16, const float* weights, co
                                     void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream);
 dsa_status topk_launch(const float* logits, int64_t ld, const int32_t* seq_lens, const int32_t* cu_q, int32_t B,
                        int32_t max_seq_len, int32_t row_begin, int32_t row_end, int32_t k, int32_t n_init,
-                       int32_t n_local, int32_t* idx, void* stream, const uint32_t* hist_g);
+                       int32_t n_local, int32_t* idx, void* stream, const uint32_t* hist_g, int32_t cmp_shift = 0);
 
 }  // namespace dsa

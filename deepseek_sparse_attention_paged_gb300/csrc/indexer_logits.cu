@@ -171,6 +171,7 @@ struct SegArgs {
     const int32_t* seq_lens;
     const int32_t* cu_q;
     int B, G, R, row_begin, row_end;
+    int shift;   // compressed keys: visible entries = visible tokens >> shift
 };
 
 __device__ __forceinline__ int seg_load(const SegArgs& a, int sidx, Seg& s) {
@@ -187,7 +188,7 @@ __device__ __forceinline__ int seg_load(const SegArgs& a, int sidx, Seg& s) {
     if (q0 + j0 >= a.row_end || q0 + j0 + nrows <= a.row_begin) return 0;
     const int L = __ldg(a.seq_lens + b);
     s.b = b; s.L = L; s.q0 = q0; s.q_len = q_len; s.j0 = j0; s.nrows = nrows;
-    s.vmax = visible_len(L, q_len, j0 + nrows - 1);
+    s.vmax = visible_len(L, q_len, j0 + nrows - 1) >> a.shift;
     s.ntiles = (s.vmax + kTileKeys - 1) / kTileKeys;
     return s.ntiles;
 }
@@ -277,7 +278,7 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
                            const int32_t* __restrict__ block_table, int max_pages,
                            const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q, int B, int G,
                            int row_begin, int row_end, float* __restrict__ logits, int64_t ld, int32_t* err,
-                           uint32_t* __restrict__ hist_g) {
+                           uint32_t* __restrict__ hist_g, int cmp_shift) {
     using C = IdxCfg<R, HIST, C8>;
     constexpr int S = C::kStages;
     constexpr int N = C::N;
@@ -307,7 +308,7 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
     uint32_t* hist_s = reinterpret_cast<uint32_t*>(base + C::kHistOff);       // HIST: [R][4096]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const SegArgs sa{seq_lens, cu_q, B, G, R, row_begin, row_end};
+    const SegArgs sa{seq_lens, cu_q, B, G, R, row_begin, row_end, cmp_shift};
     ptx::griddep_launch_dependents();   // the top-k kernel may be scheduled; it waits for this grid
     const int nseg = B * G;
 
@@ -607,7 +608,7 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
 #pragma unroll
                     for (int h = 0; h < 32; ++h) acc = fmaf(g[32 + h], fmaxf(__uint_as_float(r1[h]), 0.0f), acc);
                     const int r = sg.q0 + sg.j0 + jj;
-                    const int v = visible_len(sg.L, sg.q_len, sg.j0 + jj);
+                    const int v = visible_len(sg.L, sg.q_len, sg.j0 + jj) >> cmp_shift;
                     if (HIST) {
                         // every visible key gets a logit (-inf where its page id was bad) and is
                         // counted, so the histogram describes exactly the row the top-k reads
@@ -711,7 +712,8 @@ dsa_status indexer_logits_launch(const void* q_bf16, const float* weights, const
     if (B < 0 || max_seq_len < 0 || max_q_len < 0 || row_begin < 0 || row_end < row_begin || max_pages < 0 ||
         num_pages < 0)
         return DSA_ERR_INVALID_ARG;
-    if ((flags & ~(DSA_Q_ROTATE | DSA_SCALE_UE8M0)) != 0u) return DSA_ERR_INVALID_ARG;
+    if ((flags & ~(DSA_Q_ROTATE | DSA_SCALE_UE8M0 | DSA_KEYS_CMP4)) != 0u) return DSA_ERR_INVALID_ARG;
+    const int cmp_shift = (flags & DSA_KEYS_CMP4) != 0u ? 2 : 0;
     if (B == 0 || row_end == row_begin || max_seq_len == 0 || max_q_len == 0) return DSA_OK;
     if (!q_bf16 || !weights || !index_k_pool || !block_table || !seq_lens || !cu_q || !logits || !workspace)
         return DSA_ERR_INVALID_ARG;
@@ -781,7 +783,7 @@ dsa_status indexer_logits_launch(const void* q_bf16, const float* weights, const
         if (cudaLaunchKernelEx(&cfg, indexer_logits_umma_kernel<RR, HH, false>, kmap, qc, qg, index_k_pool, num_pages, \
                                block_table, static_cast<int>(max_pages), seq_lens, cu_q, static_cast<int>(B),  \
                                groups, static_cast<int>(row_begin), static_cast<int>(row_end), logits, ld,     \
-                               dev_err, hist_g) != cudaSuccess)                                                 \
+                               dev_err, hist_g, cmp_shift) != cudaSuccess)                                      \
             return DSA_ERR_CUDA;                                                                                \
     } while (0)
     if (hist_g != nullptr) {
@@ -884,7 +886,7 @@ dsa_status indexer_logits_c8_launch(const void* q_bf16, const float* weights, co
         if (cudaLaunchKernelEx(&cfg, indexer_logits_umma_kernel<RR, false, true>, kmap, qc, qg, pool, num_pages, \
                                block_table, static_cast<int>(max_pages), seq_lens, cu_q, static_cast<int>(B),  \
                                groups, static_cast<int>(row_begin), static_cast<int>(row_end), logits, ld,     \
-                               dev_err, no_hist) != cudaSuccess)                                                \
+                               dev_err, no_hist, 0) != cudaSuccess)                                             \
             return DSA_ERR_CUDA;                                                                                \
     } while (0)
     if (R == 1) DSA_LAUNCH_IDX_C8(1);

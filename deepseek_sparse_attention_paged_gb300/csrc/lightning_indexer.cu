@@ -60,5 +60,5 @@ extern "C" dsa_status dsa_lightning_indexer(const void* q_bf16, const float* wei
                                                logits_ws, idx_ws, dev_err, stream, fused ? hist : nullptr);
     if (st != DSA_OK) return st;
     return dsa::topk_launch(logits, ld, seq_lens, cu_q, B, max_seq_len, 0, T, k, n_init, n_local, idx, stream,
-                            fused ? hist : nullptr);
+                            fused ? hist : nullptr, (flags & DSA_KEYS_CMP4) != 0u ? 2 : 0);
 }

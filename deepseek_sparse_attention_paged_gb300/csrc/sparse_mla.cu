@@ -228,8 +228,9 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
 sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restrict__ q, int64_t num_pages,
                        const int32_t* __restrict__ block_table, int max_pages, const int32_t* __restrict__ seq_lens,
                        const int32_t* __restrict__ cu_q, int B, const int32_t* __restrict__ idx, int k, int H,
-                       float scale, int splits, uint16_t* __restrict__ out, float* __restrict__ lse_out,
-                       float* __restrict__ part_o, float* __restrict__ part_lse, int32_t* err) {
+                       float scale, int splits, int cmp_shift, int part_stride, int part_base,
+                       uint16_t* __restrict__ out, float* __restrict__ lse_out, float* __restrict__ part_o,
+                       float* __restrict__ part_lse, int32_t* err) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw_addr = ptx::smem_addr(smem_raw);
     unsigned char* base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -243,7 +244,7 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = row_request(cu_q, B, r);
     const int q0 = __ldg(cu_q + b);
-    const int v = visible_len(__ldg(seq_lens + b), __ldg(cu_q + b + 1) - q0, r - q0);
+    const int v = visible_len(__ldg(seq_lens + b), __ldg(cu_q + b + 1) - q0, r - q0) >> cmp_shift;
     const int per_split = (k + splits - 1) / splits;
     const int e_begin = split * per_split;
     const int e_end = min(k, e_begin + per_split);
@@ -587,7 +588,7 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
         const float lse = l_tot > 0.0f ? (m_run + log2f(l_tot)) / kLog2e : -INFINITY;
         const bool write_head = head < H;
         const int64_t rh = static_cast<int64_t>(r) * H + head;
-        if (splits == 1) {
+        if (part_o == nullptr) {
             uint16_t* dst = out + rh * kValueDim + half * kHalfDims;
 #pragma unroll 1
             for (int cc = kh * 128; cc < kh * 128 + 128; cc += 32) {
@@ -613,7 +614,7 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
             }
             if (write_head && half == 0 && kh == 0 && lse_out != nullptr) lse_out[rh] = lse;
         } else {
-            float* dst = part_o + (rh * splits + split) * kValueDim + half * kHalfDims;
+            float* dst = part_o + (rh * part_stride + part_base + split) * kValueDim + half * kHalfDims;
 #pragma unroll 1
             for (int cc = kh * 128; cc < kh * 128 + 128; cc += 32) {
                 uint32_t o[32];
@@ -632,7 +633,7 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
                                         __uint_as_float(o[i + 2]) * inv_l, __uint_as_float(o[i + 3]) * inv_l);
                 }
             }
-            if (write_head && half == 0 && kh == 0) part_lse[rh * splits + split] = lse;
+            if (write_head && half == 0 && kh == 0) part_lse[rh * part_stride + part_base + split] = lse;
         }
     }
     if (timed_out) raise_error(err, DSA_DEVERR_TIMEOUT);
@@ -1205,6 +1206,81 @@ sparse_mla_combine_kernel(const float* __restrict__ part_o, const float* __restr
     if (lse != nullptr && threadIdx.x == 0) lse[rh] = (m == -INFINITY) ? -INFINITY : m + logf(wsum);
 }
 
+// Window entries of the compressed-KV attention: row r (visible length v) gets the positions
+// v - window .. v - 1 of the original cache, -1 where negative.
+__global__ void __launch_bounds__(128)
+window_index_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q, int B, int window,
+                    int32_t* __restrict__ idx) {
+    const int r = blockIdx.x;
+    const int b = row_request(cu_q, B, r);
+    const int q0 = __ldg(cu_q + b);
+    const int v = visible_len(__ldg(seq_lens + b), __ldg(cu_q + b + 1) - q0, r - q0);
+    for (int j = threadIdx.x; j < window; j += blockDim.x) {
+        const int pos = v - window + j;
+        idx[static_cast<int64_t>(r) * window + j] = pos >= 0 ? pos : -1;
+    }
+}
+
+// One CTA (128 threads) per (row, head): the normalised partials of the window and of the
+// compressed entries merged by their log-sum-exps, with the head's sink logit added to the softmax
+// denominator: D = e^lse_w + e^lse_c + e^sink, out = (e^lse_w o_w + e^lse_c o_c) / D, lse = log D.
+__global__ void __launch_bounds__(128)
+sink_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse, const float* __restrict__ sinks,
+                  int H, uint16_t* __restrict__ out, float* __restrict__ lse) {
+    const int64_t rh = blockIdx.x;
+    const float l0 = __ldg(part_lse + rh * 2), l1 = __ldg(part_lse + rh * 2 + 1);
+    const float sink = __ldg(sinks + rh % H);
+    const float m = fmaxf(fmaxf(l0, l1), sink);
+    float w0 = 0.0f, w1 = 0.0f, d = 0.0f;
+    if (m != -INFINITY) {
+        w0 = l0 == -INFINITY ? 0.0f : expf(l0 - m);
+        w1 = l1 == -INFINITY ? 0.0f : expf(l1 - m);
+        d = w0 + w1 + (sink == -INFINITY ? 0.0f : expf(sink - m));
+        w0 /= d;
+        w1 /= d;
+    }
+    const int dd = threadIdx.x * 4;
+    const float4 a = __ldg(reinterpret_cast<const float4*>(part_o + (rh * 2) * kValueDim + dd));
+    const float4 c = __ldg(reinterpret_cast<const float4*>(part_o + (rh * 2 + 1) * kValueDim + dd));
+    uint2 packed;
+    packed.x = pack_bf16x2(w0 * a.x + w1 * c.x, w0 * a.y + w1 * c.y);
+    packed.y = pack_bf16x2(w0 * a.z + w1 * c.z, w0 * a.w + w1 * c.w);
+    reinterpret_cast<uint2*>(out + rh * kValueDim + dd)[0] = packed;
+    if (lse != nullptr && threadIdx.x == 0) lse[rh] = m == -INFINITY ? -INFINITY : m + logf(d);
+}
+
+// One pass of the bf16 sparse-attention kernel, one split per row, its normalised fp32 partial and
+// lse written to slot `part_base` of the two per (row, head).
+dsa_status launch_partial_pass(const void* q, const void* kv, int64_t num_pages, const int32_t* block_table,
+                               int32_t max_pages, const int32_t* seq_lens, const int32_t* cu_q, int32_t B,
+                               const int32_t* idx, int32_t k, int32_t T, int32_t H, float scale, int cmp_shift,
+                               int part_base, float* part_o, float* part_lse, int32_t* dev_err, cudaStream_t s) {
+    if (cudaFuncSetAttribute(sparse_mla_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kMlaSmemBytes)) != cudaSuccess)
+        return DSA_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, T);
+    cfg.blockDim = dim3(kMlaThreads, 1, 1);
+    cfg.dynamicSmemBytes = kMlaSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    if (cudaLaunchKernelEx(&cfg, sparse_mla_umma_kernel, static_cast<const uint16_t*>(kv), static_cast<const uint16_t*>(q),
+                           num_pages, block_table, static_cast<int>(max_pages), seq_lens, cu_q, static_cast<int>(B), idx,
+                           static_cast<int>(k), static_cast<int>(H), scale, 1, cmp_shift, 2, part_base,
+                           static_cast<uint16_t*>(nullptr), static_cast<float*>(nullptr), part_o, part_lse,
+                           dev_err) != cudaSuccess)
+        return DSA_ERR_CUDA;
+    return launch_status();
+}
+
 // Splits of the k entries per row: the largest power of two (<= 8) for which the (row, split,
 // half) grid still fits one wave of one CTA per SM and every split keeps >= 256 entries.
 int mla_splits(int T, int k) {
@@ -1269,7 +1345,8 @@ extern "C" dsa_status dsa_sparse_mla_decode(const void* q_bf16, const void* kv_p
     if (cudaLaunchKernelEx(&cfg, sparse_mla_umma_kernel, static_cast<const uint16_t*>(kv_pool),
                            static_cast<const uint16_t*>(q_bf16), num_pages, block_table, static_cast<int>(max_pages),
                            seq_lens, cu_q, static_cast<int>(B), idx, static_cast<int>(k), static_cast<int>(H), scale,
-                           splits, static_cast<uint16_t*>(out_bf16), lse, part_o, part_lse, dev_err) != cudaSuccess)
+                           splits, 0, splits, 0, static_cast<uint16_t*>(out_bf16), lse,
+                           splits > 1 ? part_o : nullptr, part_lse, dev_err) != cudaSuccess)
         return DSA_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
     if (splits > 1) {
@@ -1335,4 +1412,56 @@ extern "C" dsa_status dsa_sparse_mla_decode_fp8(const void* q_bf16, float q_scal
         if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
     }
     return DSA_OK;
+}
+
+extern "C" size_t dsa_sparse_attn_swa_cmp_workspace_size(int32_t T, int32_t H, int32_t window) {
+    if (T <= 0 || H <= 0 || window <= 0) return 0;
+    const size_t parts = static_cast<size_t>(T) * H * 2 * (dsa::kValueDim + 1) * sizeof(float);
+    return (parts + 255) / 256 * 256 + static_cast<size_t>(T) * window * sizeof(int32_t);
+}
+
+extern "C" dsa_status dsa_sparse_attn_swa_cmp(const void* q_bf16, const void* swa_kv, int64_t swa_num_pages,
+                                              const int32_t* swa_block_table, int32_t swa_max_pages, const void* cmp_kv,
+                                              int64_t cmp_num_pages, const int32_t* cmp_block_table,
+                                              int32_t cmp_max_pages, const int32_t* seq_lens, const int32_t* cu_q,
+                                              int32_t B, const int32_t* cmp_idx, int32_t k, int32_t window,
+                                              int32_t cmp_ratio, const float* sinks, int32_t T, int32_t H, float scale,
+                                              void* out_bf16, float* lse, void* workspace, size_t workspace_bytes,
+                                              int32_t* dev_err, void* stream) {
+    using namespace dsa;
+    if (k < 1 || k > DSA_MAX_TOPK || window < 1 || window > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
+    if (H != 16 && H != 32 && H != 64 && H != 128) return DSA_ERR_UNSUPPORTED;
+    int shift = 0;
+    while (shift < 8 && (1 << shift) < cmp_ratio) ++shift;
+    if (cmp_ratio < 1 || (1 << shift) != cmp_ratio || shift > 7) return DSA_ERR_UNSUPPORTED;
+    if (T < 0 || B < 0 || swa_max_pages < 0 || cmp_max_pages < 0 || swa_num_pages < 0 || cmp_num_pages < 0)
+        return DSA_ERR_INVALID_ARG;
+    if (T == 0) return DSA_OK;
+    if (swa_num_pages < 1 || cmp_num_pages < 1 || B == 0) return DSA_ERR_INVALID_ARG;
+    if (!q_bf16 || !swa_kv || !swa_block_table || !cmp_kv || !cmp_block_table || !seq_lens || !cu_q || !cmp_idx ||
+        !sinks || !out_bf16 || !workspace)
+        return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q_bf16) || !aligned16(swa_kv) || !aligned16(cmp_kv) || !aligned16(out_bf16) || !aligned16(workspace))
+        return DSA_ERR_INVALID_ARG;
+    if (!(scale > 0.0f) || T > 65535) return DSA_ERR_INVALID_ARG;
+    if (swa_num_pages * kPage >= 0x7fffffffLL || cmp_num_pages * kPage >= 0x7fffffffLL ||
+        static_cast<int64_t>(T) * H >= 0x7fffffffLL)
+        return DSA_ERR_UNSUPPORTED;
+    if (workspace_bytes < dsa_sparse_attn_swa_cmp_workspace_size(T, H, window)) return DSA_ERR_INVALID_ARG;
+    float* part_o = static_cast<float*>(workspace);
+    float* part_lse = part_o + static_cast<size_t>(T) * H * 2 * kValueDim;
+    const size_t parts = static_cast<size_t>(T) * H * 2 * (kValueDim + 1) * sizeof(float);
+    int32_t* win_idx = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) + (parts + 255) / 256 * 256);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    window_index_kernel<<<static_cast<unsigned>(T), 128, 0, s>>>(seq_lens, cu_q, B, window, win_idx);
+    if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
+    dsa_status st = launch_partial_pass(q_bf16, swa_kv, swa_num_pages, swa_block_table, swa_max_pages, seq_lens, cu_q,
+                                        B, win_idx, window, T, H, scale, 0, 0, part_o, part_lse, dev_err, s);
+    if (st != DSA_OK) return st;
+    st = launch_partial_pass(q_bf16, cmp_kv, cmp_num_pages, cmp_block_table, cmp_max_pages, seq_lens, cu_q, B, cmp_idx,
+                             k, T, H, scale, shift, 1, part_o, part_lse, dev_err, s);
+    if (st != DSA_OK) return st;
+    sink_merge_kernel<<<static_cast<unsigned>(static_cast<int64_t>(T) * H), 128, 0, s>>>(
+        part_o, part_lse, sinks, H, static_cast<uint16_t*>(out_bf16), lse);
+    return launch_status();
 }

@@ -104,7 +104,8 @@ __device__ void select_digit(TopkSmem& sm, int bins, uint32_t need) {
 template <bool FORCED>
 __global__ void __launch_bounds__(kTopkThreads)
 topk_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* __restrict__ seq_lens,
-            const int32_t* __restrict__ cu_q, int B, int row_begin, int k, int n_init, int n_local, int32_t* __restrict__ idx) {
+            const int32_t* __restrict__ cu_q, int B, int row_begin, int k, int n_init, int n_local, int cmp_shift,
+            int32_t* __restrict__ idx) {
     __shared__ TopkSmem sm;
     ptx::griddep_wait();   // launched as a programmatic dependent: the logits are complete from here on
     ptx::griddep_launch_dependents();
@@ -112,7 +113,7 @@ topk_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* __restr
     const int r = row_begin + rl;
     const int b = row_request(cu_q, B, r);
     const int q0 = __ldg(cu_q + b);
-    int v = visible_len(__ldg(seq_lens + b), __ldg(cu_q + b + 1) - q0, r - q0);
+    int v = visible_len(__ldg(seq_lens + b), __ldg(cu_q + b + 1) - q0, r - q0) >> cmp_shift;
     if (v > ld) v = static_cast<int>(ld);       // never read past the row
     const float* row = logits + static_cast<int64_t>(rl) * ld;
     const Forced<FORCED> F = make_forced<FORCED>(v, n_init, n_local);
@@ -192,12 +193,12 @@ struct BitmapSmem {
 // Visible length of global row r, looked up by all threads at once: thread t < B tests whether r
 // falls in request t (one round of independent loads instead of a chain of dependent ones).
 __device__ __forceinline__ int locate_visible(const int32_t* __restrict__ cu_q, const int32_t* __restrict__ seq_lens,
-                                              int B, int r, BitmapSmem& sm) {
+                                              int B, int r, int cmp_shift, BitmapSmem& sm) {
     if (threadIdx.x == 0) sm.row_v = 0;
     __syncthreads();
     for (int t = threadIdx.x; t < B; t += kTopkThreads) {
         const int a = __ldg(cu_q + t), e = __ldg(cu_q + t + 1), L = __ldg(seq_lens + t);
-        if (a <= r && r < e) sm.row_v = visible_len(L, e - a, r - a);
+        if (a <= r && r < e) sm.row_v = visible_len(L, e - a, r - a) >> cmp_shift;
     }
     __syncthreads();
     return sm.row_v;
@@ -280,7 +281,8 @@ __device__ void load_row_histogram(uint32_t* hist, const uint32_t* __restrict__ 
 template <bool FORCED, bool PREHIST>
 __global__ void __launch_bounds__(kTopkThreads)
 topk_bitmap_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* __restrict__ seq_lens,
-                   const int32_t* __restrict__ cu_q, int B, int row_begin, int k, int n_init, int n_local, int32_t* __restrict__ idx,
+                   const int32_t* __restrict__ cu_q, int B, int row_begin, int k, int n_init, int n_local, int cmp_shift,
+                   int32_t* __restrict__ idx,
                    int words_cap, const uint32_t* __restrict__ hist_g) {
     extern __shared__ __align__(16) unsigned char dsm[];
     BitmapSmem& sm = *reinterpret_cast<BitmapSmem*>(dsm);
@@ -293,7 +295,7 @@ topk_bitmap_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* 
     ptx::griddep_launch_dependents();
     const int rl = blockIdx.x;
     const int r = row_begin + rl;
-    int v = locate_visible(cu_q, seq_lens, B, r, sm);
+    int v = locate_visible(cu_q, seq_lens, B, r, cmp_shift, sm);
     if (v > ld) v = static_cast<int>(ld);
     if (v > words_cap * 32) v = words_cap * 32;   // the launcher guarantees this never clips
     const float* row = logits + static_cast<int64_t>(rl) * ld;
@@ -487,7 +489,8 @@ __device__ __forceinline__ void sum_with_peer(const uint32_t* hist, uint32_t* to
 template <bool FORCED, bool PREHIST>
 __global__ void __launch_bounds__(kTopkThreads)
 topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* __restrict__ seq_lens,
-                    const int32_t* __restrict__ cu_q, int B, int row_begin, int k, int n_init, int n_local, int32_t* __restrict__ idx,
+                    const int32_t* __restrict__ cu_q, int B, int row_begin, int k, int n_init, int n_local, int cmp_shift,
+                    int32_t* __restrict__ idx,
                     int words_cap, const uint32_t* __restrict__ hist_g) {
     extern __shared__ __align__(16) unsigned char dsm[];
     BitmapSmem& sm = *reinterpret_cast<BitmapSmem*>(dsm);                      // hist: the top digit
@@ -509,7 +512,7 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t*
     for (int i = threadIdx.x; i < kTopBins; i += kTopkThreads) sm.hist[i] = 0;
     for (int i = threadIdx.x; i < 2 * 1024; i += kTopkThreads) lo_hist[i] = 0;
     if (threadIdx.x == 0) sm.cand_count = 0;
-    int v = locate_visible(cu_q, seq_lens, B, r, sm);
+    int v = locate_visible(cu_q, seq_lens, B, r, cmp_shift, sm);
     if (v > ld) v = static_cast<int>(ld);
     if (v > 2 * words_cap * 32 - 256) v = 2 * words_cap * 32 - 256;   // the launcher guarantees this never clips
     const float* row = logits + static_cast<int64_t>(rl) * ld;
@@ -697,9 +700,9 @@ void* topk_bitmap_fn() { return reinterpret_cast<void*>(topk_bitmap_kernel<F, P>
 // histogram comes from hist_g[(r - row_begin) * 4096 ..] instead of a first read of the row.
 dsa_status topk_launch(const float* logits, int64_t ld, const int32_t* seq_lens, const int32_t* cu_q, int32_t B,
                        int32_t max_seq_len, int32_t row_begin, int32_t row_end, int32_t k, int32_t n_init,
-                       int32_t n_local, int32_t* idx, void* stream, const uint32_t* hist_g) {
+                       int32_t n_local, int32_t* idx, void* stream, const uint32_t* hist_g, int32_t cmp_shift) {
     if (k < 1 || k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
-    if (n_init < 0 || n_local < 0) return DSA_ERR_INVALID_ARG;
+    if (n_init < 0 || n_local < 0 || cmp_shift < 0 || cmp_shift > 7) return DSA_ERR_INVALID_ARG;
     const bool forced = n_init > 0 || n_local > 0;
     if (B < 0 || row_begin < 0 || row_end < row_begin || max_seq_len < 0) return DSA_ERR_INVALID_ARG;
     if (row_end == row_begin) return DSA_OK;
@@ -745,9 +748,9 @@ dsa_status topk_launch(const float* logits, int64_t ld, const int32_t* seq_lens,
         cfg.attrs = cattr;
         cfg.numAttrs = 2;
         cfg.dynamicSmemBytes = smem;
-        int a_B = B, a_rb = row_begin, a_k = k, a_ni = n_init, a_nl = n_local, a_wc = words_cap;
+        int a_B = B, a_rb = row_begin, a_k = k, a_ni = n_init, a_nl = n_local, a_sh = cmp_shift, a_wc = words_cap;
         void* args[] = {const_cast<float**>(&logits), &ld, const_cast<int32_t**>(&seq_lens), const_cast<int32_t**>(&cu_q),
-                        &a_B, &a_rb, &a_k, &a_ni, &a_nl, &idx, &a_wc, const_cast<uint32_t**>(&hist_g)};
+                        &a_B, &a_rb, &a_k, &a_ni, &a_nl, &a_sh, &idx, &a_wc, const_cast<uint32_t**>(&hist_g)};
         if (cudaLaunchKernelExC(&cfg, kern, args) != cudaSuccess) return DSA_ERR_CUDA;
     } else if (words <= dsa::kMaxBitmapWords) {
         const int words_cap = words < 32 ? 32 : words;
@@ -758,15 +761,16 @@ dsa_status topk_launch(const float* logits, int64_t ld, const int32_t* seq_lens,
             cudaSuccess)
             return DSA_ERR_CUDA;
         cfg.dynamicSmemBytes = smem;
-        int a_B = B, a_rb = row_begin, a_k = k, a_ni = n_init, a_nl = n_local, a_wc = words_cap;
+        int a_B = B, a_rb = row_begin, a_k = k, a_ni = n_init, a_nl = n_local, a_sh = cmp_shift, a_wc = words_cap;
         void* args[] = {const_cast<float**>(&logits), &ld, const_cast<int32_t**>(&seq_lens), const_cast<int32_t**>(&cu_q),
-                        &a_B, &a_rb, &a_k, &a_ni, &a_nl, &idx, &a_wc, const_cast<uint32_t**>(&hist_g)};
+                        &a_B, &a_rb, &a_k, &a_ni, &a_nl, &a_sh, &idx, &a_wc, const_cast<uint32_t**>(&hist_g)};
         if (cudaLaunchKernelExC(&cfg, kern, args) != cudaSuccess) return DSA_ERR_CUDA;
     } else {
         cfg.dynamicSmemBytes = 0;
         auto kern = forced ? dsa::topk_kernel<true> : dsa::topk_kernel<false>;
         if (cudaLaunchKernelEx(&cfg, kern, logits, ld, seq_lens, cu_q, static_cast<int>(B),
-                               static_cast<int>(row_begin), static_cast<int>(k), n_init, n_local, idx) !=
+                               static_cast<int>(row_begin), static_cast<int>(k), n_init, n_local,
+                               static_cast<int>(cmp_shift), idx) !=
                                    cudaSuccess)
             return DSA_ERR_CUDA;
     }
@@ -781,7 +785,7 @@ extern "C" dsa_status dsa_topk_forced(const float* logits, int64_t ld, const int
                                       size_t workspace_bytes, void* stream) {
     (void)workspace; (void)workspace_bytes;
     return dsa::topk_launch(logits, ld, seq_lens, cu_q, B, max_seq_len, row_begin, row_end, k, n_init, n_local, idx,
-                            stream, nullptr);
+                            stream, nullptr, 0);
 }
 
 extern "C" dsa_status dsa_topk(const float* logits, int64_t ld, const int32_t* seq_lens, const int32_t* cu_q,

@@ -258,3 +258,81 @@ def make(name: str) -> Workload:
 
 
 NAMES = ("tiny", "decode_b32_8k", "decode_b64_logu64k", "mtp_b8_128k", "prefill_32k_4k")
+
+
+@dataclass
+class CompressedKV:
+    """The compressed-KV companion of a workload (the DSV4 layers with compress ratio 4): request b
+    holds floor(L_b / ratio) compressed entries, each with an indexer key and a 576-wide latent row
+    drawn N(0, 1) as if written by the model's compressor (a trained module, not drawn here), on
+    pages of its own; per-head sink logits N(0, 1); the sliding window and the top-k width over the
+    compressed entries.  Streams: SeedSequence(seed + 1000).spawn(4) = pages, index keys, latent
+    rows, sinks."""
+
+    base: Workload
+    ratio: int
+    window: int
+    topk: int
+    cmp_lens: np.ndarray          # int32 [B]
+    block_table: np.ndarray       # int32 [B, max_cmp_pages], unused tail entries = -1
+    num_pages: int
+    _streams: dict = field(default_factory=dict, repr=False)
+    _cache: dict = field(default_factory=dict, repr=False)
+
+    @property
+    def max_cmp_len(self) -> int:
+        return max(1, int(self.cmp_lens.max()))
+
+    def visible_cmp_lens(self) -> np.ndarray:
+        """Compressed entries each query row may see: its visible tokens // ratio."""
+        return self.base.visible_lens() // self.ratio
+
+    def slots(self) -> np.ndarray:
+        """Slot (page * 64 + offset) of every compressed entry, requests in order (int64)."""
+        parts = []
+        for b, n in enumerate(self.cmp_lens.tolist()):
+            e = np.arange(n, dtype=np.int64)
+            parts.append(self.block_table[b, e // PAGE].astype(np.int64) * PAGE + e % PAGE)
+        return np.concatenate(parts) if parts else np.zeros(0, np.int64)
+
+    def index_keys(self) -> np.ndarray:
+        """bf16 bits [sum cmp_lens, 128]: the indexer key of every compressed entry."""
+        if "ik" not in self._cache:
+            n = int(self.cmp_lens.astype(np.int64).sum())
+            chunks = max(1, -(-n // _KEY_CHUNK))
+            self._cache["ik"] = _normal_bf16_chunked(self._streams["keys"], chunks, _KEY_CHUNK * INDEX_DIM,
+                                                     n * INDEX_DIM).reshape(n, INDEX_DIM)
+        return self._cache["ik"]
+
+    def latent_pool(self) -> np.ndarray:
+        """bf16 bits [num_pages, 64, 576]: the compressed latent rows."""
+        if "kv" not in self._cache:
+            chunks = max(1, -(-self.num_pages // _LATENT_CHUNK_PAGES))
+            per = _LATENT_CHUNK_PAGES * PAGE * LATENT_DIM
+            flat = _normal_bf16_chunked(self._streams["latent"], chunks, per, self.num_pages * PAGE * LATENT_DIM)
+            self._cache["kv"] = flat.reshape(self.num_pages, PAGE, LATENT_DIM)
+        return self._cache["kv"]
+
+    def sinks(self) -> np.ndarray:
+        """fp32 [heads]: per-head sink logits."""
+        g = np.random.Generator(np.random.PCG64(self._streams["sinks"]))
+        return g.standard_normal(self.base.heads, dtype=np.float32)
+
+
+def make_compressed(wl: Workload, ratio: int = 4, window: int = 128, topk: int = 512) -> CompressedKV:
+    """The compressed-KV companion of ``wl`` (see CompressedKV)."""
+    ss = np.random.SeedSequence(wl.seed + 1000)
+    streams = dict(zip(("pages", "keys", "latent", "sinks"), ss.spawn(4)))
+    cmp_lens = (wl.seq_lens // ratio).astype(np.int32)
+    need = [-(-int(n) // PAGE) for n in cmp_lens]
+    pool = max(1, sum(need))
+    gp = np.random.Generator(np.random.PCG64(streams["pages"]))
+    page_ids = gp.permutation(pool).astype(np.int32)
+    width = max(1, max(need))
+    bt = np.full((wl.B, width), -1, np.int32)
+    off = 0
+    for b, n in enumerate(need):
+        bt[b, :n] = page_ids[off:off + n]
+        off += n
+    return CompressedKV(base=wl, ratio=ratio, window=window, topk=topk, cmp_lens=cmp_lens, block_table=bt,
+                        num_pages=pool, _streams=streams)

@@ -87,6 +87,12 @@ typedef enum {
  * quantisation scale is the smallest power of two not below the fp32 scale max(amax, 1e-4) / 448
  * (sglang dsa_indexer.py, Indexer(scale_fmt) handed to act_quant). */
 #define DSA_SCALE_UE8M0 0x10u
+/* Flag of dsa_indexer_logits / dsa_lightning_indexer: the cache holds compressed keys, one entry per
+ * 4 tokens (DSV4 compress ratio 4: vllm_ascend dsa_v1.py, npu_vllm_quant_lightning_indexer(...,
+ * cmp_ratio = 4)).  Row r then sees the entries s < v_r / 4 (entry s stands for tokens
+ * [4s, 4s + 4), visible once all four are); seq_lens stay the token counts, and max_seq_len bounds
+ * the entries (>= every v_r / 4).  The top-k of dsa_lightning_indexer uses the same rule. */
+#define DSA_KEYS_CMP4 0x20u
 
 /* Fixed shape constants of the path. */
 #define DSA_PAGE_SIZE 64
@@ -457,6 +463,46 @@ dsa_status dsa_sparse_mla_decode_fp8(const void* q_bf16, float q_scale, const ui
                                      const int32_t* seq_lens, const int32_t* cu_q, int32_t B, const int32_t* idx,
                                      int32_t k, int32_t T, int32_t H, float scale, void* out_bf16, float* lse,
                                      void* workspace, size_t workspace_bytes, int32_t* dev_err, void* stream);
+
+/*
+ * dsa_sparse_attn_swa_cmp -- decode attention of the compressed-KV (DSV4) variant: a sliding window
+ * of the original cache plus the selected compressed entries, with per-head attention sinks.
+ * Source: vllm_ascend dsa_v1.py, AscendDSAImpl._forward_decode with compress_ratio 4:
+ * attn_op(q, ori_kv = swa_kv_cache, cmp_kv = compress_kv_cache, cmp_sparse_indices =
+ * compress_topk_idxs, ori_block_table, cmp_block_table, seqused_kv = seq_lens, sinks = attn_sink,
+ * softmax_scale, cmp_ratio, ori_mask_mode = 4 (sliding window), cmp_mask_mode = 3,
+ * ori_win_left = window_size - 1, ori_win_right = 0).
+ *   For row r with visible length v (absolute position v - 1) and head h the keys are the
+ *   original-cache positions max(0, v - window) .. v - 1 and the compressed entries
+ *   cmp_idx[r, j] with 0 <= cmp_idx < v / cmp_ratio (others: -1 padding, or skipped with
+ *   DSA_DEVERR_INDEX_RANGE); S_i = scale * <q[r,h], c_i> over the 576 dims;
+ *   D = sum_i e^{S_i} + e^{sinks[h]};  out[r,h] = bf16_rn(sum_i e^{S_i} / D * c_i[0:512]);
+ *   lse[r,h] = log D.  The rows of both caches are 576-wide latent rows (512 value + 64 rope dims,
+ *   as dsa_sparse_mla_decode's cache); an entry in both sets counts twice (different vectors).
+ * (The op's source is not printed: the union under one softmax, the sink in the denominator only,
+ * and the 576-wide rows are the reading taken.)
+ * Arguments:
+ *   q_bf16           [T, H, 576] bf16.   swa_kv / cmp_kv  bf16 [pages, 64, 576] (16-byte aligned).
+ *   swa_block_table  int32 [B, swa_max_pages] over token positions; cmp_block_table int32
+ *                    [B, cmp_max_pages] over compressed entries.   seq_lens / cu_q as elsewhere.
+ *   cmp_idx          int32 [T, k] compressed entries (dsa_lightning_indexer with DSA_KEYS_CMP4).
+ *   window           1 .. 2048.   cmp_ratio a power of two 1 .. 128 (4 for the pages' indexed layers).
+ *   sinks            fp32 [H] per-head sink logits (-inf: none).   H in {16, 32, 64, 128}.
+ *   out_bf16 [T, H, 512]; lse fp32 [T, H] (nullable).
+ *   workspace        >= dsa_sparse_attn_swa_cmp_workspace_size(T, H, window) bytes, 16-byte aligned
+ *                    (fp32 partials of the two key sets and the window's positions).
+ * Four kernels on `stream`: the window positions, the attention over the window and over the
+ * selected compressed entries (the sparse-MLA kernel, each writing a normalised fp32 partial), and a
+ * merge that adds the sink.
+ */
+size_t dsa_sparse_attn_swa_cmp_workspace_size(int32_t T, int32_t H, int32_t window);
+dsa_status dsa_sparse_attn_swa_cmp(const void* q_bf16, const void* swa_kv, int64_t swa_num_pages,
+                                   const int32_t* swa_block_table, int32_t swa_max_pages, const void* cmp_kv,
+                                   int64_t cmp_num_pages, const int32_t* cmp_block_table, int32_t cmp_max_pages,
+                                   const int32_t* seq_lens, const int32_t* cu_q, int32_t B, const int32_t* cmp_idx,
+                                   int32_t k, int32_t window, int32_t cmp_ratio, const float* sinks, int32_t T,
+                                   int32_t H, float scale, void* out_bf16, float* lse, void* workspace,
+                                   size_t workspace_bytes, int32_t* dev_err, void* stream);
 
 /*
  * dsa_mla_absorb_q -- absorbed latent query: ql[t, n, 0:512] = q_nope[t, n, 0:128] W_UK_T[n].

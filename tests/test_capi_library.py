@@ -108,3 +108,24 @@ def test_host_side_validation_of_the_c8_calls(lib):
     assert L.dsa_indexer_logits_c8(None, None, None, 0, None, 0, None, None, 0, 10, 1, 0, 1, None, 10, None, 0,
                                    None, None) == 0                                 # empty batch
 
+
+def test_host_side_validation_of_the_compressed_kv_calls(lib):
+    """The compressed-KV attention and the DSA_KEYS_CMP4 flag are checked before any CUDA call."""
+    capi.load()
+    L = capi._lib
+    f = ctypes.c_float
+    # T = 0: nothing to do; ratio 3 and window 0 unsupported; null pointers rejected
+    assert L.dsa_sparse_attn_swa_cmp(None, None, 0, None, 0, None, 0, None, 0, None, None, 1, None, 64, 128, 4, None,
+                                     0, 128, f(0.1), None, None, None, 0, None, None) == 0
+    assert L.dsa_sparse_attn_swa_cmp(None, None, 0, None, 0, None, 0, None, 0, None, None, 1, None, 64, 128, 3, None,
+                                     1, 128, f(0.1), None, None, None, 0, None, None) == 2
+    assert L.dsa_sparse_attn_swa_cmp(None, None, 0, None, 0, None, 0, None, 0, None, None, 1, None, 64, 0, 4, None,
+                                     1, 128, f(0.1), None, None, None, 0, None, None) == 2
+    assert L.dsa_sparse_attn_swa_cmp(None, None, 1, None, 1, None, 1, None, 1, None, None, 1, None, 64, 128, 4, None,
+                                     1, 128, f(0.1), None, None, None, 0, None, None) == 1
+    # partials of the two key sets (T * H * 2 * 513 floats, 256-byte aligned) + the window positions
+    assert L.dsa_sparse_attn_swa_cmp_workspace_size(2, 16, 128) == (2 * 16 * 2 * 513 * 4 + 255) // 256 * 256 + 2 * 128 * 4
+    # the compressed-keys flag is a known flag of the logits call (null pointers are what is rejected)
+    assert L.dsa_indexer_logits(None, None, None, 0, None, 0, None, None, 1, 10, 1, 0, 1, None, 10,
+                                capi.DSA_KEYS_CMP4, None, 0, None, None) == 1
+
