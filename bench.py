@@ -77,6 +77,48 @@ def algorithmic_work(wl):
             "indexer_c8": (idx8_b, idx_f)}
 
 
+def compressed_device(c, db):
+    """Device buffers of the compressed-KV stages: the FP8 index cache of the compressed keys, the
+    compressed latent rows, their page table, sinks, the selection and the workspaces."""
+    import numpy as np
+    import torch
+    from deepseek_sparse_attention_paged_gb300 import capi
+    dev = db.device
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+    pool = torch.zeros((c.num_pages, capi.INDEX_PAGE_BYTES), dtype=torch.uint8, device=dev)
+    capi.dsa_store_index_k(bf(c.index_keys()), torch.from_numpy(c.slots()).to(dev), pool, db.dev_err)
+    T, H = c.base.T, c.base.heads
+    return {"pool": pool, "bt": torch.from_numpy(c.block_table).to(dev), "kv": bf(c.latent_pool()),
+            "sinks": torch.from_numpy(c.sinks()).to(dev),
+            "idx": torch.empty((T, c.topk), dtype=torch.int32, device=dev),
+            "li_ws": torch.empty(capi.dsa_lightning_indexer_workspace_size(T, c.max_cmp_len), dtype=torch.uint8,
+                                 device=dev),
+            "attn_ws": torch.empty(capi.dsa_sparse_attn_swa_cmp_workspace_size(T, H, c.window), dtype=torch.uint8,
+                                   device=dev),
+            "out": torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev),
+            "lse": torch.empty((T, H), dtype=torch.float32, device=dev)}
+
+
+def compressed_work(c):
+    """Algorithmic bytes / FLOPs of the compressed-KV stages.
+    dsv4_select: 132 B per compressed entry per request + 4 B per (row, visible entry) logit written
+                 and read back by the top-k + the query and gates; 2*64*128 FLOP per (row, entry).
+    dsv4_attn:   per row: (window keys + selected entries) * 1152 B + query, output, indices, lse;
+                 2 * H * keys * (576 + 512) FLOP."""
+    import numpy as np
+    wl = c.base
+    vis = wl.visible_lens().astype(np.int64)
+    visc = vis // c.ratio
+    T, H = wl.T, wl.heads
+    sel_b = int(c.cmp_lens.astype(np.int64).sum()) * 132 + int(visc.sum()) * 8 + T * 64 * 128 * 2 + T * 64 * 4 \
+        + T * c.topk * 4
+    sel_f = int(visc.sum()) * 2 * 64 * 128
+    keys = np.minimum(vis, c.window) + np.minimum(visc, c.topk)
+    att_b = int(keys.sum()) * 1152 + T * H * 576 * 2 + T * H * 512 * 2 + T * c.topk * 4 + T * H * 4
+    att_f = int(keys.sum()) * 2 * H * (576 + 512)
+    return {"dsv4_select": (sel_b, sel_f), "dsv4_attn": (att_b, att_f)}
+
+
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -188,7 +230,7 @@ STAGE_SOURCES = {"store": ["store_index_k.cu"], "indexer": ["indexer_logits.cu"]
                  "mla": ["sparse_mla.cu"]}
 # tensor peak of each stage relative to the measured dense bf16 peak: the indexer contracts FP8
 # operands (nominal dense FP8 : BF16 = 4.5 : 2.25 PFLOP/s), the attention bf16
-STAGE_TENSOR_PEAK_RATIO = {"indexer": 2.0, "select": 2.0, "mla": 1.0}
+STAGE_TENSOR_PEAK_RATIO = {"indexer": 2.0, "select": 2.0, "mla": 1.0, "dsv4_select": 2.0}
 # per-tensor scales of the FP8 latent-cache stage (~ max |N(0,1)| / 448 for the synthetic cache)
 FP8_K_SCALE = 0.0125
 FP8_Q_SCALE = 0.0125
@@ -440,6 +482,23 @@ def run_gpu(args):
                                                dev_err=db.dev_err), stream, flush)
     # the int8 ("c8") index-cache variant of the indexer logits over the same keys
     stage_graphs["indexer_c8"] = TimedGraph(lambda: db.indexer_c8_stage(), stream, flush)
+    # the compressed-KV (ratio 4) layers: the one-call indexer over compressed keys, then the attention
+    # over a 128-token window plus the selected compressed entries with per-head sinks
+    cmp = workloads.make_compressed(wl)
+    cmp_dev = compressed_device(cmp, db)
+    capi.dsa_lightning_indexer(db.index_q, db.weights, cmp_dev["pool"], cmp_dev["bt"], db.seq_lens, db.cu_q,
+                               cmp.max_cmp_len, wl.max_q_len, cmp.topk, cmp_dev["idx"], cmp_dev["li_ws"],
+                               flags=capi.DSA_KEYS_CMP4, dev_err=db.dev_err)
+    stage_graphs["dsv4_select"] = TimedGraph(
+        lambda: capi.dsa_lightning_indexer(db.index_q, db.weights, cmp_dev["pool"], cmp_dev["bt"], db.seq_lens,
+                                           db.cu_q, cmp.max_cmp_len, wl.max_q_len, cmp.topk, cmp_dev["idx"],
+                                           cmp_dev["li_ws"], flags=capi.DSA_KEYS_CMP4, dev_err=db.dev_err),
+        stream, flush)
+    stage_graphs["dsv4_attn"] = TimedGraph(
+        lambda: capi.dsa_sparse_attn_swa_cmp(db.mla_q, db.kv_pool, db.block_table, cmp_dev["kv"], cmp_dev["bt"],
+                                             db.seq_lens, db.cu_q, cmp_dev["idx"], cmp.window, cmp.ratio,
+                                             cmp_dev["sinks"], wl.scale, cmp_dev["out"], workspace=cmp_dev["attn_ws"],
+                                             lse=cmp_dev["lse"], dev_err=db.dev_err), stream, flush)
     st, word = db.device_error()
     if st != 0:
         raise RuntimeError(f"device error word {word} after warm-up")
@@ -478,6 +537,7 @@ def run_gpu(args):
     work["select"] = tuple(a + b for a, b in zip(work["indexer"], work["topk"]))
     mb, mf = work["mla"]
     work["mla_fp8"] = (mb - int(np.minimum(wl.visible_lens(), wl.topk).sum()) * 576, mf)   # 576 B rows, not 1152
+    work.update(compressed_work(cmp))
     stages = {}
     for k, ms_list in stage_ms.items():
         ms = sum(ms_list) / len(ms_list)
