@@ -56,43 +56,92 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Error of the fp32 sum s = a + b (Knuth's TwoSum: s + err == a + b exactly).
+__device__ __forceinline__ float two_sum_err(float a, float b, float s) {
+    const float bb = __fsub_rn(s, a);
+    return __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
 // The int8 ("c8") indexer transform of one 128-vector held by a warp (lane l: elements 4l .. 4l+3,
 // exact fp32 values of bf16 numbers).  Follows vllm-ascend sfa_v1.py with use_sparse_c8_indexer:
 // x @ qk_hadamard, where qk_hadamard = bf16(scipy.linalg.hadamard(128)) / 128**0.5 has entries +-c,
 // c = bf16(128^-0.5) = 181 * 2^-11; then npu_dynamic_quant to int8 with one scale per vector.
-//   * y_j = bf16(c * sum_i (-1)^popcount(i & j) x_i): the Sylvester butterflies (h = 1, 2 inside the
-//     lane, 4 .. 64 across lanes l ^ h / 4) run in fp64, where sums of 128 bf16 values are exact and
-//     so is the product by c, so the one rounding to bf16 gives the correctly rounded product;
+//   * y_j = bf16(c * sum_i (-1)^popcount(i & j) x_i), the exact value rounded once: the Sylvester
+//     butterflies (h = 1, 2 inside the lane, 4 .. 64 across lanes l ^ h / 4) run in fp32 with every
+//     add checked exact by TwoSum; c * S is the fp32 product p plus its exact FMA error e, and the
+//     one rounding of p + e to bf16 equals that of p except when p sits on a bf16 midpoint, where p
+//     is first moved one fp32 ulp towards p + e.  If any add of the warp's vector was inexact (an
+//     exponent spread beyond fp32's 24 bits) or a product is too small for the FMA error to be
+//     exact, the warp redoes the vector in fp64, where sums of 128 bf16 values are exact;
 //   * scale = amax / 127 (fp32, IEEE division); code = round-to-nearest-even(y / scale) (fp32 IEEE
 //     division), within [-127, 127]; all codes 0 when amax = 0.
 // Returns the lane's 4 codes packed little-endian; *scale_out = the fp32 scale.
 __device__ __forceinline__ uint32_t c8_rotate_quant(const float (&xin)[4], int lane, float* scale_out) {
+    constexpr float kCf = 181.0f / 2048.0f;
     constexpr double kC = 181.0 / 2048.0;
-    double x[4] = {xin[0], xin[1], xin[2], xin[3]};
+    float y[4];
     {
-        double a = x[0], b = x[1];
-        x[0] = a + b; x[1] = a - b;
-        a = x[2]; b = x[3];
-        x[2] = a + b; x[3] = a - b;
-    }
-    {
-        double a = x[0], b = x[2];
-        x[0] = a + b; x[2] = a - b;
-        a = x[1]; b = x[3];
-        x[1] = a + b; x[3] = a - b;
-    }
+        float x[4] = {xin[0], xin[1], xin[2], xin[3]};
+        bool inexact = false;
+        auto bfly = [&](float& lo, float& hi) {
+            const float a = lo, b = hi;
+            lo = __fadd_rn(a, b);
+            hi = __fsub_rn(a, b);
+            inexact |= two_sum_err(a, b, lo) != 0.0f || two_sum_err(a, -b, hi) != 0.0f;
+        };
+        bfly(x[0], x[1]);
+        bfly(x[2], x[3]);
+        bfly(x[0], x[2]);
+        bfly(x[1], x[3]);
 #pragma unroll
-    for (int m = 1; m < 32; m <<= 1) {
-        const bool upper = (lane & m) != 0;
+        for (int m = 1; m < 32; m <<= 1) {
+            const bool upper = (lane & m) != 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float other = __shfl_xor_sync(0xffffffffu, x[e], m);
+                const float a = upper ? other : x[e];
+                const float b = upper ? -x[e] : other;
+                x[e] = __fadd_rn(a, b);
+                inexact |= two_sum_err(a, b, x[e]) != 0.0f;
+            }
+        }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const double other = __shfl_xor_sync(0xffffffffu, x[e], m);
-            x[e] = upper ? other - x[e] : x[e] + other;
+            float p = __fmul_rn(x[e], kCf);
+            const float err = __fmaf_rn(x[e], kCf, -p);
+            if (x[e] != 0.0f && !(fabsf(p) >= 0x1p-100f)) inexact = true;   // also catches inf / NaN
+            const uint32_t pb = __float_as_uint(p);
+            if ((pb & 0xffffu) == 0x8000u && err != 0.0f)                      // on a bf16 midpoint
+                p = __uint_as_float(((err > 0.0f) == (p > 0.0f)) ? pb + 1u : pb - 1u);
+            y[e] = __bfloat162float(__float2bfloat16_rn(p));
+        }
+        if (__any_sync(0xffffffffu, inexact)) {
+            double d[4] = {xin[0], xin[1], xin[2], xin[3]};
+            {
+                double a = d[0], b = d[1];
+                d[0] = a + b; d[1] = a - b;
+                a = d[2]; b = d[3];
+                d[2] = a + b; d[3] = a - b;
+            }
+            {
+                double a = d[0], b = d[2];
+                d[0] = a + b; d[2] = a - b;
+                a = d[1]; b = d[3];
+                d[1] = a + b; d[3] = a - b;
+            }
+#pragma unroll
+            for (int m = 1; m < 32; m <<= 1) {
+                const bool upper = (lane & m) != 0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const double other = __shfl_xor_sync(0xffffffffu, d[e], m);
+                    d[e] = upper ? other - d[e] : d[e] + other;
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) y[e] = __bfloat162float(__double2bfloat16(d[e] * kC));
         }
     }
-    float y[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) y[e] = __bfloat162float(__double2bfloat16(x[e] * kC));
     const float amax = warp_max(fmaxf(fmaxf(fabsf(y[0]), fabsf(y[1])), fmaxf(fabsf(y[2]), fabsf(y[3]))));
     const float scale = __fdiv_rn(amax, 127.0f);
     uint32_t packed = 0;

@@ -42,6 +42,9 @@ def test_store_c8_scaled_zero_spike_padding_and_range():
     x[201, :] = 0.0
     x[201, 5] = 3.0                           # single spike: every rotated entry +-3c
     x[202] = 1e-30                            # subnormal-range fp16 scale
+    x[203, :] = rng.standard_normal(128) * 1e-6
+    x[203, 7] = 3000.0                        # exponent spread beyond fp32's 24 bits: the fp64 fallback
+    x[204, ::2] = 1.0 + 2.0 ** -7             # products on bf16 midpoints
     keys = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     pages = 20
     slots = rng.permutation(pages * 64)[:n].astype(np.int64)
