@@ -93,8 +93,8 @@ def compressed_device(c, db):
             "idx": torch.empty((T, c.topk), dtype=torch.int32, device=dev),
             "li_ws": torch.empty(capi.dsa_lightning_indexer_workspace_size(T, c.max_cmp_len), dtype=torch.uint8,
                                  device=dev),
-            "attn_ws": torch.empty(capi.dsa_sparse_attn_swa_cmp_workspace_size(T, H, c.window), dtype=torch.uint8,
-                                   device=dev),
+            "attn_ws": torch.empty(max(16, capi.dsa_sparse_attn_swa_cmp_workspace_size(T, H, c.window, c.topk)),
+                                   dtype=torch.uint8, device=dev),
             "out": torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev),
             "lse": torch.empty((T, H), dtype=torch.float32, device=dev)}
 

@@ -100,7 +100,7 @@ def load(path: str = LIB_PATH):
                                                          ctypes.c_float, P, P, P, P]),
         "dsa_store_latent_fp8": (ctypes.c_int, [P, P, i64, ctypes.c_float, P, i64, P, P]),
         "dsa_store_index_k_c8": (ctypes.c_int, [P, P, i64, P, i64, i32, P, P]),
-        "dsa_sparse_attn_swa_cmp_workspace_size": (sz, [i32, i32, i32]),
+        "dsa_sparse_attn_swa_cmp_workspace_size": (sz, [i32, i32, i32, i32]),
         "dsa_sparse_attn_swa_cmp": (ctypes.c_int, [P, P, i64, P, i32, P, i64, P, i32, P, P, i32, P, i32, i32, i32, P,
                                                    i32, i32, ctypes.c_float, P, P, P, sz, P, P]),
         "dsa_indexer_logits_c8_workspace_size": (sz, [i32]),
@@ -450,8 +450,8 @@ def dsa_sparse_mla_decode(q_bf16: torch.Tensor, kv_pool: torch.Tensor, block_tab
     _count(2 if T > 0 else 0)
 
 
-def dsa_sparse_attn_swa_cmp_workspace_size(T: int, H: int, window: int) -> int:
-    return int(load().dsa_sparse_attn_swa_cmp_workspace_size(int(T), int(H), int(window)))
+def dsa_sparse_attn_swa_cmp_workspace_size(T: int, H: int, window: int, k: int) -> int:
+    return int(load().dsa_sparse_attn_swa_cmp_workspace_size(int(T), int(H), int(window), int(k)))
 
 
 def dsa_sparse_attn_swa_cmp(q_bf16: torch.Tensor, swa_kv: torch.Tensor, swa_block_table: torch.Tensor,
@@ -480,8 +480,8 @@ def dsa_sparse_attn_swa_cmp(q_bf16: torch.Tensor, swa_kv: torch.Tensor, swa_bloc
     _need(sinks.numel() == H, "sinks must be [H]")
     _need(tuple(out.shape) == (T, H, VALUE_DIM), "out must be [T, H, 512]")
     if workspace is None:
-        workspace = torch.empty(max(16, dsa_sparse_attn_swa_cmp_workspace_size(T, H, window)), dtype=torch.uint8,
-                                device=q_bf16.device)
+        workspace = torch.empty(max(16, dsa_sparse_attn_swa_cmp_workspace_size(T, H, window, cmp_idx.shape[1])),
+                                dtype=torch.uint8, device=q_bf16.device)
     _need(workspace.is_cuda and workspace.is_contiguous(), "workspace must be a contiguous CUDA tensor")
     B = seq_lens.numel()
     _check("dsa_sparse_attn_swa_cmp", lib.dsa_sparse_attn_swa_cmp(
@@ -489,7 +489,7 @@ def dsa_sparse_attn_swa_cmp(q_bf16: torch.Tensor, swa_kv: torch.Tensor, swa_bloc
         cmp_kv.shape[0], _ptr(cmp_block_table), cmp_block_table.shape[1], _ptr(seq_lens), _ptr(cu_q), B,
         _ptr(cmp_idx), cmp_idx.shape[1], int(window), int(cmp_ratio), _ptr(sinks), T, H, float(scale), _ptr(out),
         _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_err), _stream(stream)))
-    _count(4 if T > 0 else 0)
+    _count(1 if T > 0 else 0)   # (+ the combine when the rows are split)
 
 
 def dsa_store_latent_fp8(latent_bf16: torch.Tensor, slot_mapping: torch.Tensor, k_scale: float,

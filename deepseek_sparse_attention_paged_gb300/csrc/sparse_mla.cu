@@ -224,13 +224,31 @@ struct MlaBars {
 };
 static_assert(sizeof(MlaBars) <= kBarBytes, "barrier block");
 
+// The second source of entries of the compressed-KV attention (TWO = true): entries [0, win) of a
+// row are the window positions v - win .. v - 1 of the main cache, entries [win, win + k2) the
+// listed compressed entries of cache 2 (visible while < v >> shift2).  An entry's source travels
+// in bit 30 of its position and of its row id (both caches hold fewer than 2^30 rows).
+struct TwoSrc {
+    const uint16_t* kv2;
+    int64_t num_pages2;
+    const int32_t* block_table2;
+    int max_pages2;
+    int shift2;
+    const int32_t* idx2;
+    int k2;
+    int win;
+    const float* sinks;   // [H] sink logits, folded into the softmax denominator (one split)
+};
+constexpr int kSrc2 = 1 << 30;
+
+template <bool TWO>
 __global__ void __launch_bounds__(kMlaThreads, 1)
 sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restrict__ q, int64_t num_pages,
                        const int32_t* __restrict__ block_table, int max_pages, const int32_t* __restrict__ seq_lens,
                        const int32_t* __restrict__ cu_q, int B, const int32_t* __restrict__ idx, int k, int H,
                        float scale, int splits, int cmp_shift, int part_stride, int part_base,
                        uint16_t* __restrict__ out, float* __restrict__ lse_out, float* __restrict__ part_o,
-                       float* __restrict__ part_lse, int32_t* err) {
+                       float* __restrict__ part_lse, int32_t* err, TwoSrc ts) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw_addr = ptx::smem_addr(smem_raw);
     unsigned char* base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -292,18 +310,34 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
         const int my_entry = pw * kKeysPerProducer + lane;
         auto load_pos = [&](int tile) -> int {
             const int e = e_begin + tile * kKeysPerTile + my_entry;
-            return (lane < kKeysPerProducer && tile < ntiles && e < e_end) ? __ldg(idx + static_cast<int64_t>(r) * k + e)
-                                                                          : -1;
+            if (!(lane < kKeysPerProducer && tile < ntiles && e < e_end)) return -1;
+            if (TWO) {
+                if (e < ts.win) return v - ts.win + e;   // the window (negative: before the first token)
+                const int p2 = __ldg(ts.idx2 + static_cast<int64_t>(r) * ts.k2 + (e - ts.win));
+                return p2 >= 0 ? (p2 | kSrc2) : -1;
+            }
+            return __ldg(idx + static_cast<int64_t>(r) * k + e);
         };
-        auto pos_ok = [&](int pos) -> bool { return pos >= 0 && pos < v && (pos >> 6) < max_pages; };
+        auto pos_ok = [&](int pos) -> bool {
+            if (pos < 0) return false;
+            if (TWO && (pos & kSrc2)) {
+                const int p = pos & (kSrc2 - 1);
+                return p < (v >> ts.shift2) && (p >> 6) < ts.max_pages2;
+            }
+            return pos >= 0 && pos < v && (pos >> 6) < max_pages;
+        };
         auto load_page = [&](int pos) -> int {
-            return pos_ok(pos) ? __ldg(block_table + static_cast<int64_t>(b) * max_pages + (pos >> 6)) : -1;
+            if (!pos_ok(pos)) return -1;
+            if (TWO && (pos & kSrc2))
+                return __ldg(ts.block_table2 + static_cast<int64_t>(b) * ts.max_pages2 + ((pos & (kSrc2 - 1)) >> 6));
+            return __ldg(block_table + static_cast<int64_t>(b) * max_pages + (pos >> 6));
         };
         auto to_row = [&](int pos, int page) -> int {   // -1: padding or invalid (reported)
             if (pos < 0) return -1;
             if (!pos_ok(pos)) { raise_error(err, DSA_DEVERR_INDEX_RANGE); return -1; }
-            if (page < 0 || page >= num_pages) { raise_error(err, DSA_DEVERR_PAGE_RANGE); return -1; }
-            return page * kPage + (pos & 63);
+            const bool two = TWO && (pos & kSrc2);
+            if (page < 0 || page >= (two ? ts.num_pages2 : num_pages)) { raise_error(err, DSA_DEVERR_PAGE_RANGE); return -1; }
+            return (page * kPage + (pos & 63)) | (two ? kSrc2 : 0);
         };
         int pos1[kBatch], page1[kBatch], pos2[kBatch];
 #pragma unroll
@@ -318,6 +352,8 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
         const int rpiece = lane & 3;
         const uint16_t* kv_val = kv + half * kHalfDims + piece * 8;
         const uint16_t* kv_rope = kv + kValueDim + half * kRopeHalf + rpiece * 8;
+        const uint16_t* kv2_val = TWO ? ts.kv2 + half * kHalfDims + piece * 8 : nullptr;
+        const uint16_t* kv2_rope = TWO ? ts.kv2 + kValueDim + half * kRopeHalf + rpiece * 8 : nullptr;
         for (int t0 = 0; t0 < ntiles && !timed_out; t0 += kBatch) {
             int rows[kBatch];
 #pragma unroll
@@ -346,8 +382,9 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
                 for (int kq = 0; kq < kKeysPerProducer / 4; ++kq) {
                     const int kl = kq * 4 + (lane >> 3);                 // key within this warp's 16
                     const int key = pw * kKeysPerProducer + kl;
-                    const int64_t row = __shfl_sync(0xffffffffu, row_src, kl);
-                    const uint16_t* src = kv_val + row * kLatentDim;
+                    const int rr = __shfl_sync(0xffffffffu, row_src, kl);
+                    const uint16_t* src = (TWO && (rr & kSrc2)) ? kv2_val + static_cast<int64_t>(rr & (kSrc2 - 1)) * kLatentDim
+                                                                : kv_val + static_cast<int64_t>(rr) * kLatentDim;
 #pragma unroll
                     for (int j = 0; j < kOwnChunks; ++j)
                         cp_async_16(stage + j * kKvChunkBytes + key * 128 + ((piece ^ (key & 7)) << 4), src + j * 64);
@@ -356,8 +393,10 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
                 for (int kq = 0; kq < kKeysPerProducer / 8; ++kq) {
                     const int kl = kq * 8 + (lane >> 2);
                     const int key = pw * kKeysPerProducer + kl;
-                    const int64_t row = __shfl_sync(0xffffffffu, row_src, kl);
-                    cp_async_16(stage + kOwnChunks * kKvChunkBytes + rope_off(key, rpiece), kv_rope + row * kLatentDim);
+                    const int rr = __shfl_sync(0xffffffffu, row_src, kl);
+                    const uint16_t* src = (TWO && (rr & kSrc2)) ? kv2_rope + static_cast<int64_t>(rr & (kSrc2 - 1)) * kLatentDim
+                                                                : kv_rope + static_cast<int64_t>(rr) * kLatentDim;
+                    cp_async_16(stage + kOwnChunks * kKvChunkBytes + rope_off(key, rpiece), src);
                 }
                 cp_async_arrive_noinc(&bar.kv_full[s]);
                 if (lane == 0) {
@@ -584,10 +623,25 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
         bool have_o = ntiles > 0 && !timed_out;
         if (have_o && !ptx::mbar_wait(&bar.o_full, 0, deadline)) { timed_out = true; have_o = false; }
         ptx::tc_fence_after_sync();
-        const float inv_l = l_tot > 0.0f ? 1.0f / l_tot : 0.0f;
-        const float lse = l_tot > 0.0f ? (m_run + log2f(l_tot)) / kLog2e : -INFINITY;
+        float inv_l = l_tot > 0.0f ? 1.0f / l_tot : 0.0f;
+        float lse = l_tot > 0.0f ? (m_run + log2f(l_tot)) / kLog2e : -INFINITY;
         const bool write_head = head < H;
         const int64_t rh = static_cast<int64_t>(r) * H + head;
+        if (TWO && part_o == nullptr) {
+            // the head's sink logit joins the denominator: D = l 2^m + 2^sink (log2 units)
+            const float sl2 = (write_head ? __ldg(ts.sinks + head) : -INFINITY) * kLog2e;
+            const float m_run_eff = l_tot > 0.0f ? m_run : -INFINITY;
+            const float mf = fmaxf(m_run_eff, sl2);
+            if (mf == -INFINITY) {
+                inv_l = 0.0f;
+                lse = -INFINITY;
+            } else {
+                const float a = l_tot > 0.0f ? l_tot * exp2f(m_run_eff - mf) : 0.0f;
+                const float d = a + exp2f(sl2 - mf);
+                inv_l = l_tot > 0.0f ? exp2f(m_run_eff - mf) / d : 0.0f;
+                lse = (mf + log2f(d)) / kLog2e;
+            }
+        }
         if (part_o == nullptr) {
             uint16_t* dst = out + rh * kValueDim + half * kHalfDims;
 #pragma unroll 1
@@ -1174,12 +1228,14 @@ sparse_mla_fp8_kernel(const uint8_t* __restrict__ kv8, float k_scale, const uint
 
 __global__ void __launch_bounds__(128)
 sparse_mla_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse, int splits,
-                          uint16_t* __restrict__ out, float* __restrict__ lse) {
+                          uint16_t* __restrict__ out, float* __restrict__ lse, const float* __restrict__ sinks,
+                          int H) {
     const int64_t rh = blockIdx.x;   // row * H + head
     const float* pl = part_lse + rh * splits;
-    float m = -INFINITY;
+    const float sink = sinks != nullptr ? __ldg(sinks + rh % H) : -INFINITY;   // joins the denominator
+    float m = sink;
     for (int j = 0; j < splits; ++j) m = fmaxf(m, __ldg(pl + j));
-    float wsum = 0.0f;
+    float wsum = (sink == -INFINITY || m == -INFINITY) ? 0.0f : expf(sink - m);
     for (int j = 0; j < splits; ++j) {
         const float lj = __ldg(pl + j);
         wsum += (lj == -INFINITY) ? 0.0f : expf(lj - m);
@@ -1204,81 +1260,6 @@ sparse_mla_combine_kernel(const float* __restrict__ part_o, const float* __restr
         reinterpret_cast<uint2*>(out + rh * kValueDim + d)[0] = packed;
     }
     if (lse != nullptr && threadIdx.x == 0) lse[rh] = (m == -INFINITY) ? -INFINITY : m + logf(wsum);
-}
-
-// Window entries of the compressed-KV attention: row r (visible length v) gets the positions
-// v - window .. v - 1 of the original cache, -1 where negative.
-__global__ void __launch_bounds__(128)
-window_index_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q, int B, int window,
-                    int32_t* __restrict__ idx) {
-    const int r = blockIdx.x;
-    const int b = row_request(cu_q, B, r);
-    const int q0 = __ldg(cu_q + b);
-    const int v = visible_len(__ldg(seq_lens + b), __ldg(cu_q + b + 1) - q0, r - q0);
-    for (int j = threadIdx.x; j < window; j += blockDim.x) {
-        const int pos = v - window + j;
-        idx[static_cast<int64_t>(r) * window + j] = pos >= 0 ? pos : -1;
-    }
-}
-
-// One CTA (128 threads) per (row, head): the normalised partials of the window and of the
-// compressed entries merged by their log-sum-exps, with the head's sink logit added to the softmax
-// denominator: D = e^lse_w + e^lse_c + e^sink, out = (e^lse_w o_w + e^lse_c o_c) / D, lse = log D.
-__global__ void __launch_bounds__(128)
-sink_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse, const float* __restrict__ sinks,
-                  int H, uint16_t* __restrict__ out, float* __restrict__ lse) {
-    const int64_t rh = blockIdx.x;
-    const float l0 = __ldg(part_lse + rh * 2), l1 = __ldg(part_lse + rh * 2 + 1);
-    const float sink = __ldg(sinks + rh % H);
-    const float m = fmaxf(fmaxf(l0, l1), sink);
-    float w0 = 0.0f, w1 = 0.0f, d = 0.0f;
-    if (m != -INFINITY) {
-        w0 = l0 == -INFINITY ? 0.0f : expf(l0 - m);
-        w1 = l1 == -INFINITY ? 0.0f : expf(l1 - m);
-        d = w0 + w1 + (sink == -INFINITY ? 0.0f : expf(sink - m));
-        w0 /= d;
-        w1 /= d;
-    }
-    const int dd = threadIdx.x * 4;
-    const float4 a = __ldg(reinterpret_cast<const float4*>(part_o + (rh * 2) * kValueDim + dd));
-    const float4 c = __ldg(reinterpret_cast<const float4*>(part_o + (rh * 2 + 1) * kValueDim + dd));
-    uint2 packed;
-    packed.x = pack_bf16x2(w0 * a.x + w1 * c.x, w0 * a.y + w1 * c.y);
-    packed.y = pack_bf16x2(w0 * a.z + w1 * c.z, w0 * a.w + w1 * c.w);
-    reinterpret_cast<uint2*>(out + rh * kValueDim + dd)[0] = packed;
-    if (lse != nullptr && threadIdx.x == 0) lse[rh] = m == -INFINITY ? -INFINITY : m + logf(d);
-}
-
-// One pass of the bf16 sparse-attention kernel, one split per row, its normalised fp32 partial and
-// lse written to slot `part_base` of the two per (row, head).
-dsa_status launch_partial_pass(const void* q, const void* kv, int64_t num_pages, const int32_t* block_table,
-                               int32_t max_pages, const int32_t* seq_lens, const int32_t* cu_q, int32_t B,
-                               const int32_t* idx, int32_t k, int32_t T, int32_t H, float scale, int cmp_shift,
-                               int part_base, float* part_o, float* part_lse, int32_t* dev_err, cudaStream_t s) {
-    if (cudaFuncSetAttribute(sparse_mla_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kMlaSmemBytes)) != cudaSuccess)
-        return DSA_ERR_CUDA;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2, 1, T);
-    cfg.blockDim = dim3(kMlaThreads, 1, 1);
-    cfg.dynamicSmemBytes = kMlaSmemBytes;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    if (cudaLaunchKernelEx(&cfg, sparse_mla_umma_kernel, static_cast<const uint16_t*>(kv), static_cast<const uint16_t*>(q),
-                           num_pages, block_table, static_cast<int>(max_pages), seq_lens, cu_q, static_cast<int>(B), idx,
-                           static_cast<int>(k), static_cast<int>(H), scale, 1, cmp_shift, 2, part_base,
-                           static_cast<uint16_t*>(nullptr), static_cast<float*>(nullptr), part_o, part_lse,
-                           dev_err) != cudaSuccess)
-        return DSA_ERR_CUDA;
-    return launch_status();
 }
 
 // Splits of the k entries per row: the largest power of two (<= 8) for which the (row, split,
@@ -1323,7 +1304,7 @@ extern "C" dsa_status dsa_sparse_mla_decode(const void* q_bf16, const void* kv_p
     float* part_o = static_cast<float*>(workspace);
     float* part_lse = splits > 1 ? part_o + static_cast<size_t>(T) * H * splits * kValueDim : nullptr;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaFuncSetAttribute(sparse_mla_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(sparse_mla_umma_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kMlaSmemBytes)) != cudaSuccess)
         return DSA_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
@@ -1342,16 +1323,16 @@ extern "C" dsa_status dsa_sparse_mla_decode(const void* q_bf16, const void* kv_p
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    if (cudaLaunchKernelEx(&cfg, sparse_mla_umma_kernel, static_cast<const uint16_t*>(kv_pool),
+    if (cudaLaunchKernelEx(&cfg, sparse_mla_umma_kernel<false>, static_cast<const uint16_t*>(kv_pool),
                            static_cast<const uint16_t*>(q_bf16), num_pages, block_table, static_cast<int>(max_pages),
                            seq_lens, cu_q, static_cast<int>(B), idx, static_cast<int>(k), static_cast<int>(H), scale,
                            splits, 0, splits, 0, static_cast<uint16_t*>(out_bf16), lse,
-                           splits > 1 ? part_o : nullptr, part_lse, dev_err) != cudaSuccess)
+                           splits > 1 ? part_o : nullptr, part_lse, dev_err, TwoSrc{}) != cudaSuccess)
         return DSA_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
     if (splits > 1) {
         sparse_mla_combine_kernel<<<static_cast<unsigned>(static_cast<int64_t>(T) * H), 128, 0, s>>>(
-            part_o, part_lse, splits, static_cast<uint16_t*>(out_bf16), lse);
+            part_o, part_lse, splits, static_cast<uint16_t*>(out_bf16), lse, nullptr, H);
         if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
     }
     return DSA_OK;
@@ -1408,16 +1389,17 @@ extern "C" dsa_status dsa_sparse_mla_decode_fp8(const void* q_bf16, float q_scal
     if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
     if (splits > 1) {
         sparse_mla_combine_kernel<<<static_cast<unsigned>(static_cast<int64_t>(T) * H), 128, 0, s>>>(
-            part_o, part_lse, splits, static_cast<uint16_t*>(out_bf16), lse);
+            part_o, part_lse, splits, static_cast<uint16_t*>(out_bf16), lse, nullptr, H);
         if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
     }
     return DSA_OK;
 }
 
-extern "C" size_t dsa_sparse_attn_swa_cmp_workspace_size(int32_t T, int32_t H, int32_t window) {
-    if (T <= 0 || H <= 0 || window <= 0) return 0;
-    const size_t parts = static_cast<size_t>(T) * H * 2 * (dsa::kValueDim + 1) * sizeof(float);
-    return (parts + 255) / 256 * 256 + static_cast<size_t>(T) * window * sizeof(int32_t);
+extern "C" size_t dsa_sparse_attn_swa_cmp_workspace_size(int32_t T, int32_t H, int32_t window, int32_t k) {
+    if (T <= 0 || H <= 0 || window <= 0 || k <= 0) return 0;
+    const size_t splits = static_cast<size_t>(dsa::mla_splits(T, window + k));
+    if (splits == 1) return 0;
+    return static_cast<size_t>(T) * H * splits * (dsa::kValueDim + 1) * sizeof(float);
 }
 
 extern "C" dsa_status dsa_sparse_attn_swa_cmp(const void* q_bf16, const void* swa_kv, int64_t swa_num_pages,
@@ -1439,29 +1421,52 @@ extern "C" dsa_status dsa_sparse_attn_swa_cmp(const void* q_bf16, const void* sw
     if (T == 0) return DSA_OK;
     if (swa_num_pages < 1 || cmp_num_pages < 1 || B == 0) return DSA_ERR_INVALID_ARG;
     if (!q_bf16 || !swa_kv || !swa_block_table || !cmp_kv || !cmp_block_table || !seq_lens || !cu_q || !cmp_idx ||
-        !sinks || !out_bf16 || !workspace)
+        !sinks || !out_bf16)
         return DSA_ERR_INVALID_ARG;
-    if (!aligned16(q_bf16) || !aligned16(swa_kv) || !aligned16(cmp_kv) || !aligned16(out_bf16) || !aligned16(workspace))
-        return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q_bf16) || !aligned16(swa_kv) || !aligned16(cmp_kv) || !aligned16(out_bf16)) return DSA_ERR_INVALID_ARG;
     if (!(scale > 0.0f) || T > 65535) return DSA_ERR_INVALID_ARG;
-    if (swa_num_pages * kPage >= 0x7fffffffLL || cmp_num_pages * kPage >= 0x7fffffffLL ||
-        static_cast<int64_t>(T) * H >= 0x7fffffffLL)
+    // rows of both caches carry their source in bit 30
+    if (swa_num_pages * kPage >= kSrc2 || cmp_num_pages * kPage >= kSrc2 || static_cast<int64_t>(T) * H >= 0x7fffffffLL)
         return DSA_ERR_UNSUPPORTED;
-    if (workspace_bytes < dsa_sparse_attn_swa_cmp_workspace_size(T, H, window)) return DSA_ERR_INVALID_ARG;
+    const int ktot = window + k;
+    const size_t ws_need = dsa_sparse_attn_swa_cmp_workspace_size(T, H, window, k);
+    if (ws_need > 0 && (workspace == nullptr || !aligned16(workspace) || workspace_bytes < ws_need))
+        return DSA_ERR_INVALID_ARG;
+    const int splits = mla_splits(T, ktot);
     float* part_o = static_cast<float*>(workspace);
-    float* part_lse = part_o + static_cast<size_t>(T) * H * 2 * kValueDim;
-    const size_t parts = static_cast<size_t>(T) * H * 2 * (kValueDim + 1) * sizeof(float);
-    int32_t* win_idx = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) + (parts + 255) / 256 * 256);
+    float* part_lse = splits > 1 ? part_o + static_cast<size_t>(T) * H * splits * kValueDim : nullptr;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    window_index_kernel<<<static_cast<unsigned>(T), 128, 0, s>>>(seq_lens, cu_q, B, window, win_idx);
+    if (cudaFuncSetAttribute(sparse_mla_umma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kMlaSmemBytes)) != cudaSuccess)
+        return DSA_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, splits, T);
+    cfg.blockDim = dim3(kMlaThreads, 1, 1);
+    cfg.dynamicSmemBytes = kMlaSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    const TwoSrc ts{static_cast<const uint16_t*>(cmp_kv), cmp_num_pages, cmp_block_table, static_cast<int>(cmp_max_pages),
+                    shift, cmp_idx, static_cast<int>(k), static_cast<int>(window), sinks};
+    if (cudaLaunchKernelEx(&cfg, sparse_mla_umma_kernel<true>, static_cast<const uint16_t*>(swa_kv),
+                           static_cast<const uint16_t*>(q_bf16), swa_num_pages, swa_block_table,
+                           static_cast<int>(swa_max_pages), seq_lens, cu_q, static_cast<int>(B),
+                           static_cast<const int32_t*>(nullptr), ktot, static_cast<int>(H), scale, splits, 0, splits, 0,
+                           static_cast<uint16_t*>(out_bf16), lse, splits > 1 ? part_o : nullptr, part_lse, dev_err,
+                           ts) != cudaSuccess)
+        return DSA_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
-    dsa_status st = launch_partial_pass(q_bf16, swa_kv, swa_num_pages, swa_block_table, swa_max_pages, seq_lens, cu_q,
-                                        B, win_idx, window, T, H, scale, 0, 0, part_o, part_lse, dev_err, s);
-    if (st != DSA_OK) return st;
-    st = launch_partial_pass(q_bf16, cmp_kv, cmp_num_pages, cmp_block_table, cmp_max_pages, seq_lens, cu_q, B, cmp_idx,
-                             k, T, H, scale, shift, 1, part_o, part_lse, dev_err, s);
-    if (st != DSA_OK) return st;
-    sink_merge_kernel<<<static_cast<unsigned>(static_cast<int64_t>(T) * H), 128, 0, s>>>(
-        part_o, part_lse, sinks, H, static_cast<uint16_t*>(out_bf16), lse);
-    return launch_status();
+    if (splits > 1) {
+        sparse_mla_combine_kernel<<<static_cast<unsigned>(static_cast<int64_t>(T) * H), 128, 0, s>>>(
+            part_o, part_lse, splits, static_cast<uint16_t*>(out_bf16), lse, sinks, H);
+        if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
+    }
+    return DSA_OK;
 }

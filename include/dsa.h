@@ -489,13 +489,15 @@ dsa_status dsa_sparse_mla_decode_fp8(const void* q_bf16, float q_scale, const ui
  *   window           1 .. 2048.   cmp_ratio a power of two 1 .. 128 (4 for the pages' indexed layers).
  *   sinks            fp32 [H] per-head sink logits (-inf: none).   H in {16, 32, 64, 128}.
  *   out_bf16 [T, H, 512]; lse fp32 [T, H] (nullable).
- *   workspace        >= dsa_sparse_attn_swa_cmp_workspace_size(T, H, window) bytes, 16-byte aligned
- *                    (fp32 partials of the two key sets and the window's positions).
- * Four kernels on `stream`: the window positions, the attention over the window and over the
- * selected compressed entries (the sparse-MLA kernel, each writing a normalised fp32 partial), and a
- * merge that adds the sink.
+ *   workspace        >= dsa_sparse_attn_swa_cmp_workspace_size(T, H, window, k) bytes, 16-byte
+ *                    aligned (split-K partials for small batches; 0 bytes, nullable, when each row
+ *                    is one split).
+ * One pass of the sparse-attention kernel over both key sets (the window positions computed in
+ * the kernel, the compressed entries through their own cache, page table and visibility), the sink
+ * folded into the softmax denominator of its epilogue; for small batches split over the entries,
+ * with the sink added by the split-K combine.
  */
-size_t dsa_sparse_attn_swa_cmp_workspace_size(int32_t T, int32_t H, int32_t window);
+size_t dsa_sparse_attn_swa_cmp_workspace_size(int32_t T, int32_t H, int32_t window, int32_t k);
 dsa_status dsa_sparse_attn_swa_cmp(const void* q_bf16, const void* swa_kv, int64_t swa_num_pages,
                                    const int32_t* swa_block_table, int32_t swa_max_pages, const void* cmp_kv,
                                    int64_t cmp_num_pages, const int32_t* cmp_block_table, int32_t cmp_max_pages,

@@ -123,8 +123,10 @@ def test_host_side_validation_of_the_compressed_kv_calls(lib):
                                      1, 128, f(0.1), None, None, None, 0, None, None) == 2
     assert L.dsa_sparse_attn_swa_cmp(None, None, 1, None, 1, None, 1, None, 1, None, None, 1, None, 64, 128, 4, None,
                                      1, 128, f(0.1), None, None, None, 0, None, None) == 1
-    # partials of the two key sets (T * H * 2 * 513 floats, 256-byte aligned) + the window positions
-    assert L.dsa_sparse_attn_swa_cmp_workspace_size(2, 16, 128) == (2 * 16 * 2 * 513 * 4 + 255) // 256 * 256 + 2 * 128 * 4
+    # split-K partials only when the rows are split (as dsa_sparse_mla_workspace_size for window + k entries)
+    assert L.dsa_sparse_attn_swa_cmp_workspace_size(64, 128, 128, 512) == L.dsa_sparse_mla_workspace_size(64, 128, 640)
+    assert L.dsa_sparse_attn_swa_cmp_workspace_size(2, 16, 128, 2048) == L.dsa_sparse_mla_workspace_size(2, 16, 2176)
+    assert L.dsa_sparse_attn_swa_cmp_workspace_size(0, 16, 128, 64) == 0
     # the compressed-keys flag is a known flag of the logits call (null pointers are what is rejected)
     assert L.dsa_indexer_logits(None, None, None, 0, None, 0, None, None, 1, 10, 1, 0, 1, None, 10,
                                 capi.DSA_KEYS_CMP4, None, 0, None, None) == 1

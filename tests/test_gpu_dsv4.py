@@ -104,15 +104,26 @@ def test_dsv4_full_size_every_row():
 def test_dsv4_attention_rejects_bad_ratio_and_short_workspace():
     wl = workloads.make_custom("dsv4_args", 303, [300], 1, topk=64, heads=16)
     c = workloads.make_compressed(wl, ratio=4, window=64, topk=64)
-    T, H = wl.T, wl.heads
+    T, H, k = wl.T, wl.heads, 2048                  # one row over 2112 entries: split, so scratch is needed
     args = (_dev_bf16(wl.mla_q()), _dev_bf16(wl.latent_pool()), _i32(wl.block_table), _dev_bf16(c.latent_pool()),
-            _i32(c.block_table), _i32(wl.seq_lens), _i32(wl.cu_q), _i32(np.zeros((T, 64), np.int32)))
+            _i32(c.block_table), _i32(wl.seq_lens), _i32(wl.cu_q), _i32(np.zeros((T, k), np.int32)))
     out = torch.empty((T, H, 512), dtype=torch.bfloat16, device="cuda")
     sinks = torch.zeros(H, dtype=torch.float32, device="cuda")
     with pytest.raises(capi.DSAError) as e:
         capi.dsa_sparse_attn_swa_cmp(*args, 64, 3, sinks, wl.scale, out)
     assert e.value.status == capi.DSA_ERR_UNSUPPORTED
+    need = capi.dsa_sparse_attn_swa_cmp_workspace_size(T, H, 64, k)
+    assert need > 0
     with pytest.raises(capi.DSAError) as e:
-        short = torch.empty(capi.dsa_sparse_attn_swa_cmp_workspace_size(T, H, 64) - 16, dtype=torch.uint8, device="cuda")
+        short = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
         capi.dsa_sparse_attn_swa_cmp(*args, 64, 4, sinks, wl.scale, out, workspace=short)
     assert e.value.status == capi.DSA_ERR_INVALID_ARG
+
+
+def test_dsv4_split_rows_add_the_sink_in_the_combine():
+    """Few rows and many entries: each row is split over several clusters and the sink enters in
+    the split-K combine instead of the kernel's epilogue."""
+    wl = workloads.make_custom("dsv4_split", 304, [20000, 9000], 1, topk=64, heads=32)
+    c = workloads.make_compressed(wl, ratio=4, window=256, topk=2048)
+    assert capi.dsa_sparse_attn_swa_cmp_workspace_size(wl.T, wl.heads, c.window, c.topk) > 0
+    _run_case(wl, c, "dsv4/split")
