@@ -709,8 +709,9 @@ sparse_mla_umma_kernel(const uint16_t* __restrict__ kv, const uint16_t* __restri
 //     256 c .. + 255 as two 128-byte swizzled K-major chunks, rope dims 512 + 32 c .. + 31 without
 //     swizzle; the score MMA starts as soon as they land;
 //   * the value dims are widened to bf16 (exact: E4M3 values are bf16 values) into one of two value
-//     buffers in the MN-major value layout; each producer lane widens the 16-byte pieces it copied,
-//     three tiles after issuing them, so that three tiles of loads stay in flight meanwhile;
+//     buffers in the MN-major value layout by two widen warps (one thread per key), as soon as the
+//     codes have landed and the PV that read the buffer before has completed; the producers only
+//     issue copies;
 //   * the score MMA is E4M3 x E4M3 (kind::f8f6f4, K = 32) with the query's codes in tensor memory
 //     (quantised there by the softmax warps with q_scale); S is scaled by scale * q_scale * k_scale;
 //   * P stays bf16 and PV stays bf16 x bf16; O is scaled by k_scale at the end.
@@ -721,19 +722,21 @@ constexpr int kF8CodeBytes = 2 * kF8ChunkBytes + kF8RopeBytes;           // 1843
 constexpr int kF8VBytes = kOwnChunks * kKvChunkBytes;                    // 32768: bf16 value dims
 constexpr int kF8Stages = 5;                                             // code stages (tiles in flight)
 constexpr int kF8VBufs = 2;                                              // bf16 value buffers
-constexpr int kF8Lag = 3;                                                // a tile is widened 3 issues after its own
+constexpr int kF8WidenWarp0 = kProducerWarp0 + kProducerWarps;          // warps 13, 14 widen the value codes
+constexpr int kF8WidenWarps = 2;
+constexpr int kF8Threads = 32 * (kF8WidenWarp0 + kF8WidenWarps);         // 480
 constexpr uint32_t kF8TmemQRope = kTmemQ + 64;                           // query codes: value 64 + rope 8 columns
 constexpr size_t kF8SmemBytes = 1024 + size_t(kF8Stages) * kF8CodeBytes + size_t(kF8VBufs) * kF8VBytes +
                                 2 * size_t(kXBytes) + kBarBytes;
 static_assert(kF8CodeBytes % 1024 == 0 && kF8VBytes % 1024 == 0, "1024-byte alignment of the swizzled parts");
-static_assert(kF8Lag < kF8Stages, "a tile is widened before its code stage is refilled");
+static_assert(kF8WidenWarps * 32 == kKeysPerTile, "one widen thread per key of a tile");
 static_assert(kF8SmemBytes <= 232448, "shared-memory budget");
 
 struct Mla8Bars {
     uint64_t q_full;               // query codes in TMEM (8 softmax warps)
     uint64_t k_full[kF8Stages];    // every producer thread's cp.async landed + one arrive per producer warp
-    uint64_t k_empty[kF8Stages];   // score MMAs done (1), codes widened (4 producer warps), valid bits read (8 warps)
-    uint64_t v_full[kF8VBufs];     // values widened to bf16 (4 producer warps)
+    uint64_t k_empty[kF8Stages];   // score MMAs done (1), codes widened (2 widen warps), valid bits read (8 warps)
+    uint64_t v_full[kF8VBufs];     // values widened to bf16 (2 widen warps)
     uint64_t v_empty[kF8VBufs];    // PV that read the buffer completed
     uint64_t s_full[2], s_free[2], p_full[2], x_full[2], x_free[2];   // as in the bf16 kernel
     uint64_t o_full;
@@ -794,7 +797,7 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t two) {
     return d;
 }
 
-__global__ void __launch_bounds__(kMlaThreads, 1)
+__global__ void __launch_bounds__(kF8Threads, 1)
 sparse_mla_fp8_kernel(const uint8_t* __restrict__ kv8, float k_scale, const uint16_t* __restrict__ q, float q_scale,
                       int64_t num_pages, const int32_t* __restrict__ block_table, int max_pages,
                       const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q, int B,
@@ -826,10 +829,10 @@ sparse_mla_fp8_kernel(const uint8_t* __restrict__ kv8, float k_scale, const uint
         ptx::mbar_init(&bar.q_full, kSoftmaxWarps);
         for (int s = 0; s < kF8Stages; ++s) {
             ptx::mbar_init(&bar.k_full[s], kProducerWarps * 32 + kProducerWarps);
-            ptx::mbar_init(&bar.k_empty[s], 1 + kProducerWarps + kSoftmaxWarps);
+            ptx::mbar_init(&bar.k_empty[s], 1 + kF8WidenWarps + kSoftmaxWarps);
         }
         for (int s = 0; s < kF8VBufs; ++s) {
-            ptx::mbar_init(&bar.v_full[s], kProducerWarps);
+            ptx::mbar_init(&bar.v_full[s], kF8WidenWarps);
             ptx::mbar_init(&bar.v_empty[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -855,7 +858,45 @@ sparse_mla_fp8_kernel(const uint8_t* __restrict__ kv8, float k_scale, const uint
     bool timed_out = false;
     const uint32_t kv_addr0 = ptx::smem_addr(kvs);
 
-    if (warp >= kProducerWarp0) {
+    if (warp >= kF8WidenWarp0) {
+        // ---------------------------------------------------------------- widen warps
+        // thread t owns key t of every tile: once the tile's codes landed and the PV that read
+        // value buffer u % 2 before completed, its 256 value codes (16 swizzled 16-byte pieces in
+        // two 128-byte chunks) become 32 bf16 pieces in the MN-major value layout
+        const int key = (warp - kF8WidenWarp0) * 32 + lane;
+        for (int u = 0; u < ntiles; ++u) {
+            const int s = u % kF8Stages;
+            const int vi = u % kF8VBufs;
+            const bool ok = ptx::mbar_wait(&bar.k_full[s], (u / kF8Stages) & 1, deadline) &&
+                            ptx::mbar_wait(&bar.v_empty[vi], ((u / kF8VBufs) & 1) ^ 1u, deadline);
+            if (__any_sync(0xffffffffu, !ok)) { timed_out = true; break; }
+            const unsigned char* sp = kvs + s * kF8CodeBytes + key * 128;
+            unsigned char* vp = vbs + vi * kF8VBytes + key * 128;
+#pragma unroll
+            for (int p = 0; p < 16; ++p) {
+                const uint4 c = *reinterpret_cast<const uint4*>(sp + (p >> 3) * kF8ChunkBytes + (((p & 7) ^ (key & 7)) << 4));
+                uint4 lo, hi;
+                lo.x = e4m3x2_to_bf16x2(static_cast<uint16_t>(c.x));
+                lo.y = e4m3x2_to_bf16x2(static_cast<uint16_t>(c.x >> 16));
+                lo.z = e4m3x2_to_bf16x2(static_cast<uint16_t>(c.y));
+                lo.w = e4m3x2_to_bf16x2(static_cast<uint16_t>(c.y >> 16));
+                hi.x = e4m3x2_to_bf16x2(static_cast<uint16_t>(c.z));
+                hi.y = e4m3x2_to_bf16x2(static_cast<uint16_t>(c.z >> 16));
+                hi.z = e4m3x2_to_bf16x2(static_cast<uint16_t>(c.w));
+                hi.w = e4m3x2_to_bf16x2(static_cast<uint16_t>(c.w >> 16));
+                // dims 16 p .. 16 p + 15: chunk p / 4 of 64 dims, pieces 2 (p % 4) and 2 (p % 4) + 1
+                unsigned char* vrow = vp + (p >> 2) * kKvChunkBytes;
+                *reinterpret_cast<uint4*>(vrow + (((2 * (p & 3)) ^ (key & 7)) << 4)) = lo;
+                *reinterpret_cast<uint4*>(vrow + (((2 * (p & 3) + 1) ^ (key & 7)) << 4)) = hi;
+            }
+            ptx::fence_proxy_async_smem();   // the bf16 values are read by the tensor cores
+            __syncwarp();
+            if (lane == 0) {
+                ptx::mbar_arrive(&bar.v_full[vi]);
+                ptx::mbar_arrive(&bar.k_empty[s]);
+            }
+        }
+    } else if (warp >= kProducerWarp0) {
         // ---------------------------------------------------------------- producers
         const int pw = warp - kProducerWarp0;
         ptx::griddep_wait();
@@ -874,44 +915,6 @@ sparse_mla_fp8_kernel(const uint8_t* __restrict__ kv8, float k_scale, const uint
             if (!pos_ok(pos)) { raise_error(err, DSA_DEVERR_INDEX_RANGE); return -1; }
             if (page < 0 || page >= num_pages) { raise_error(err, DSA_DEVERR_PAGE_RANGE); return -1; }
             return page * kPage + (pos & 63);
-        };
-        // widen this lane's value pieces of tile u (the 16-byte pieces it copied, landed) to bf16 in
-        // value buffer u % 2 once the PV of tile u - 2 has released it; then the warp's arrivals on
-        // the buffer's full barrier and on the code stage's empty barrier
-        auto widen = [&](int u) -> bool {
-            const int vi = u % kF8VBufs;
-            if (lane == 0 && !ptx::mbar_wait(&bar.v_empty[vi], ((u / kF8VBufs) & 1) ^ 1u, deadline)) timed_out = true;
-            timed_out = __shfl_sync(0xffffffffu, timed_out ? 1 : 0, 0) != 0;
-            if (timed_out) return false;
-            const unsigned char* sp = kvs + (u % kF8Stages) * kF8CodeBytes;
-            unsigned char* vp = vbs + vi * kF8VBytes;
-#pragma unroll
-            for (int kq = 0; kq < kKeysPerProducer / 2; ++kq) {
-                const int key = pw * kKeysPerProducer + 2 * kq + (lane >> 4);
-                const int j = lane & 15;   // codes 16 j .. 16 j + 15 of this CTA's value dims
-                const uint4 c = *reinterpret_cast<const uint4*>(sp + (j >> 3) * kF8ChunkBytes + key * 128 +
-                                                                (((j & 7) ^ (key & 7)) << 4));
-                uint4 lo, hi;
-                lo.x = e4m3x2_to_bf16x2(static_cast<uint16_t>(c.x));
-                lo.y = e4m3x2_to_bf16x2(static_cast<uint16_t>(c.x >> 16));
-                lo.z = e4m3x2_to_bf16x2(static_cast<uint16_t>(c.y));
-                lo.w = e4m3x2_to_bf16x2(static_cast<uint16_t>(c.y >> 16));
-                hi.x = e4m3x2_to_bf16x2(static_cast<uint16_t>(c.z));
-                hi.y = e4m3x2_to_bf16x2(static_cast<uint16_t>(c.z >> 16));
-                hi.z = e4m3x2_to_bf16x2(static_cast<uint16_t>(c.w));
-                hi.w = e4m3x2_to_bf16x2(static_cast<uint16_t>(c.w >> 16));
-                // dims 16 j .. 16 j + 7 and 16 j + 8 .. 16 j + 15: chunk j / 4 of 64 dims, pieces 2 (j % 4), + 1
-                unsigned char* vrow = vp + (j >> 2) * kKvChunkBytes + key * 128;
-                *reinterpret_cast<uint4*>(vrow + (((2 * (j & 3)) ^ (key & 7)) << 4)) = lo;
-                *reinterpret_cast<uint4*>(vrow + (((2 * (j & 3) + 1) ^ (key & 7)) << 4)) = hi;
-            }
-            ptx::fence_proxy_async_smem();   // the bf16 values are read by the tensor cores
-            __syncwarp();
-            if (lane == 0) {
-                ptx::mbar_arrive(&bar.v_full[vi]);
-                ptx::mbar_arrive(&bar.k_empty[u % kF8Stages]);
-            }
-            return true;
         };
         int pos1[kBatch], page1[kBatch], pos2[kBatch];
 #pragma unroll
@@ -967,15 +970,9 @@ sparse_mla_fp8_kernel(const uint8_t* __restrict__ kv8, float k_scale, const uint
                     bar.valid[s][pw] = vbits;
                     ptx::mbar_arrive(&bar.k_full[s]);
                 }
-                if (t >= kF8Lag) {
-                    asm volatile("cp.async.wait_group 3;" ::: "memory");   // this lane's copies of tile t - 3 landed
-                    if (!widen(t - kF8Lag)) break;
-                }
             }
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
-        for (int u = ntiles > kF8Lag ? ntiles - kF8Lag : 0; u < ntiles && !timed_out; ++u)
-            if (!widen(u)) break;
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
@@ -1369,7 +1366,7 @@ extern "C" dsa_status dsa_sparse_mla_decode_fp8(const void* q_bf16, float q_scal
         return DSA_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, splits, T);
-    cfg.blockDim = dim3(kMlaThreads, 1, 1);
+    cfg.blockDim = dim3(kF8Threads, 1, 1);
     cfg.dynamicSmemBytes = kF8SmemBytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
