@@ -773,27 +773,13 @@ __device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, const uint32_t
                  : "memory");
 }
 
-// E4M3 code (round to nearest even, saturating) of the IEEE fp32 quotient x / qs, given
-// rq = the correctly rounded fp32 reciprocal of qs.  y = x * rq and the quotient are within
-// 1.5 * 2^-23 of x / qs relative to each other (two roundings of relative size 2^-24 in y, one in the
-// quotient), i.e. at most 3 ulps of y apart, and their E4M3 roundings differ only if an E4M3
-// rounding midpoint lies between them or on one of them.  In E4M3's normal range the midpoints are
-// the fp32 numbers whose low 20 mantissa bits are 0x80000, so y decides unless it lies within 3 ulps
-// of one; there, and below 2^-6 (E4M3 subnormals, coarser midpoints), the IEEE division is done.
-// The code therefore always equals the code of the division.
-__device__ __forceinline__ uint8_t e4m3_of_quotient(float x, float qs, float rq) {
-    const float y = __fmul_rn(x, rq);
-    const int d = static_cast<int>(__float_as_uint(y) & 0xfffffu) - 0x80000;
-    const float z = (fabsf(y) < 0x1p-6f || (d >= -3 && d <= 3)) ? __fdiv_rn(x, qs) : y;
-    return static_cast<uint8_t>(__nv_cvt_float_to_fp8(z, __NV_SATFINITE, __NV_E4M3));
-}
-
-// Four bf16 -> E4M3 codes of x / qs (the IEEE fp32 quotient, round to nearest even, saturating).
-__device__ __forceinline__ uint32_t quant4_e4m3(uint32_t lo, uint32_t hi, float qs, float rq) {
+// Four bf16 -> E4M3 codes of x / qs (one IEEE division each, round to nearest even, saturating).
+__device__ __forceinline__ uint32_t quant4_e4m3(uint32_t lo, uint32_t hi, float qs) {
     const float v[4] = {bf16_lo(lo), bf16_hi(lo), bf16_lo(hi), bf16_hi(hi)};
     uint32_t w = 0;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) w |= static_cast<uint32_t>(e4m3_of_quotient(v[e], qs, rq)) << (8 * e);
+    for (int e = 0; e < 4; ++e)
+        w |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(__fdiv_rn(v[e], qs), __NV_SATFINITE, __NV_E4M3)) << (8 * e);
     return w;
 }
 
@@ -1046,12 +1032,11 @@ sparse_mla_fp8_kernel(const uint8_t* __restrict__ kv8, float k_scale, const uint
             const uint4* src = reinterpret_cast<const uint4*>(q + (static_cast<int64_t>(r) * H + head) * kLatentDim);
             const bool live = head < H;
             uint32_t w[32];
-            const float rq = __frcp_rn(q_scale);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const uint4 raw = live ? __ldg(src + (half * kHalfDims + kh * 128) / 8 + i) : make_uint4(0u, 0u, 0u, 0u);
-                w[2 * i] = quant4_e4m3(raw.x, raw.y, q_scale, rq);
-                w[2 * i + 1] = quant4_e4m3(raw.z, raw.w, q_scale, rq);
+                w[2 * i] = quant4_e4m3(raw.x, raw.y, q_scale);
+                w[2 * i + 1] = quant4_e4m3(raw.z, raw.w, q_scale);
             }
             tmem_st_32x32b_x32(tmem + lane_base + kTmemQ + 32 * kh, w);
             uint32_t wr[4];
@@ -1059,8 +1044,8 @@ sparse_mla_fp8_kernel(const uint8_t* __restrict__ kv8, float k_scale, const uint
             for (int i = 0; i < 2; ++i) {
                 const uint4 raw =
                     live ? __ldg(src + (kValueDim + half * kRopeHalf + kh * 16) / 8 + i) : make_uint4(0u, 0u, 0u, 0u);
-                wr[2 * i] = quant4_e4m3(raw.x, raw.y, q_scale, rq);
-                wr[2 * i + 1] = quant4_e4m3(raw.z, raw.w, q_scale, rq);
+                wr[2 * i] = quant4_e4m3(raw.x, raw.y, q_scale);
+                wr[2 * i + 1] = quant4_e4m3(raw.z, raw.w, q_scale);
             }
             tmem_st_32x32b_x4(tmem + lane_base + kF8TmemQRope + 4 * kh, wr);
             tmem_wait_st();
