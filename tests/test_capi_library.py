@@ -131,3 +131,23 @@ def test_host_side_validation_of_the_compressed_kv_calls(lib):
     assert L.dsa_indexer_logits(None, None, None, 0, None, 0, None, None, 1, 10, 1, 0, 1, None, 10,
                                 capi.DSA_KEYS_CMP4, None, 0, None, None) == 1
 
+
+def test_host_side_validation_of_the_fp8_latent_calls(lib):
+    """The FP8 latent store and attention check their arguments before any CUDA call."""
+    capi.load()
+    L = capi._lib
+    f = ctypes.c_float
+    assert L.dsa_store_latent_fp8(None, None, 0, f(0.5), None, 1, None, None) == 0          # n = 0
+    assert L.dsa_store_latent_fp8(None, None, 4, f(0.0), None, 1, None, None) == 1          # k_scale <= 0
+    assert L.dsa_store_latent_fp8(None, None, 4, f(float("inf")), None, 1, None, None) == 1  # k_scale not finite
+    assert L.dsa_store_latent_fp8(None, None, 4, f(0.5), None, 1, None, None) == 1          # null pointers
+    args = [None, f(0.5), None, f(0.5), 1, None, 1, None, None, 1, None, 64, 1, 128, f(0.1), None, None, None, 0,
+            None, None]
+    a = list(args); a[11] = 0
+    assert L.dsa_sparse_mla_decode_fp8(*a) == 2                                              # k = 0
+    a = list(args); a[13] = 24
+    assert L.dsa_sparse_mla_decode_fp8(*a) == 2                                              # H = 24
+    a = list(args); a[12] = 0
+    assert L.dsa_sparse_mla_decode_fp8(*a) == 0                                              # T = 0
+    assert L.dsa_sparse_mla_decode_fp8(*args) == 1                                           # null pointers
+
