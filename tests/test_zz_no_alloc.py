@@ -1,7 +1,8 @@
 """dsa_sparse_mla_decode_noalloc: the sparse-MLA entry point for callers that may not allocate device
 memory (it takes no workspace and uses the library's fixed 16 MiB scratch instead).
 
-Checked through the C ABI against the workspace-taking dsa_sparse_mla_decode on the same inputs,
+Checked through the C ABI against the oracle and against the workspace-taking dsa_sparse_mla_decode
+on the same inputs,
 on two calls in a row with different inputs (the scratch is shared between calls and keeps the
 previous call's contents), for device memory left unchanged by a call after the first, and for the
 size limit.  This file is collected last so that a run that
@@ -10,8 +11,11 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from deepseek_sparse_attention_paged_gb300 import capi, workloads
 from deepseek_sparse_attention_paged_gb300.pipeline import DeviceBatch
+
+from helpers import bf16_to_np_f64, check_attention
 
 pytestmark = pytest.mark.gpu
 
@@ -55,15 +59,26 @@ def _compare(a, b):
     assert float((la[fin] - lb[fin]).abs().max()) <= 1e-3 if bool(fin.any()) else True
 
 
+def _against_oracle(wl, idx, got, key):
+    torch.cuda.synchronize()
+    rows = np.arange(wl.T)
+    ref_o, ref_l = oracle.sparse_mla(wl.mla_q(), wl.latent_pool(), wl.block_table, wl.seq_lens, wl.cu_q,
+                                     idx.cpu().numpy(), wl.scale, rows)
+    check_attention(bf16_to_np_f64(got[0]), got[1].cpu().numpy().astype(np.float64), ref_o, ref_l, key=key)
+
+
 def test_no_alloc_matches_workspace_entry_point_twice_in_a_row():
     # first call: 3 rows, 128 heads, k = 2048 (8 splits: 6.3 MB of the 16 MiB scratch)
     wl1, db1, idx1 = _inputs(901, [4000, 2500, 9000], 128, 2048)
-    _compare(_no_alloc(wl1, db1, idx1), _with_workspace(wl1, db1, idx1))
+    got1 = _no_alloc(wl1, db1, idx1)
+    _compare(got1, _with_workspace(wl1, db1, idx1))
+    _against_oracle(wl1, idx1, got1, "no_alloc/first_call")
     # second call, different shapes and values: nothing left over from the first call may leak in
     wl2, db2, idx2 = _inputs(902, [700, 3000, 150, 2048, 64], 64, 512)
     idx2[2] = -1                                      # an empty row: out = 0, lse = -inf
     got = _no_alloc(wl2, db2, idx2)
     _compare(got, _with_workspace(wl2, db2, idx2))
+    _against_oracle(wl2, idx2, got, "no_alloc/second_call")
     assert float(got[0][2].abs().max()) == 0.0 and bool(torch.isneginf(got[1][2]).all())
 
 
