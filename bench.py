@@ -784,11 +784,23 @@ def run_profile(args):
         torch.cuda.synchronize()
         print(json.dumps({"profile": args.profile, "launches": args.warmup + args.steps}))
         return
-    need_latent = args.profile in ("mla", "step", "mla_fp8")
+    need_latent = args.profile in ("mla", "step", "mla_fp8", "dsv4")
     db = DeviceBatch(wl, with_latent=need_latent, c8=args.profile == "indexer_c8")
     if args.profile in ("topk", "mla", "mla_fp8"):
         db.select()
-    if args.profile == "mla_fp8":
+    if args.profile == "dsv4":
+        # the compressed-KV layers: the one-call indexer over compressed keys, then the attention
+        cmp = workloads.make_compressed(wl)
+        cd = compressed_device(cmp, db)
+
+        def fn():
+            capi.dsa_lightning_indexer(db.index_q, db.weights, cd["pool"], cd["bt"], db.seq_lens, db.cu_q,
+                                       cmp.max_cmp_len, wl.max_q_len, cmp.topk, cd["idx"], cd["li_ws"],
+                                       flags=capi.DSA_KEYS_CMP4, dev_err=db.dev_err)
+            capi.dsa_sparse_attn_swa_cmp(db.mla_q, db.kv_pool, db.block_table, cd["kv"], cd["bt"], db.seq_lens,
+                                         db.cu_q, cd["idx"], cmp.window, cmp.ratio, cd["sinks"], wl.scale, cd["out"],
+                                         workspace=cd["attn_ws"], lse=cd["lse"], dev_err=db.dev_err)
+    elif args.profile == "mla_fp8":
         # the FP8 latent cache of the same rows; the bf16 cache is dropped once it is quantised
         kv8 = torch.empty((wl.num_pages, 64, 576), dtype=torch.uint8, device="cuda")
         capi.dsa_store_latent_fp8(db.kv_pool.view(-1, 576), torch.arange(wl.num_pages * 64, device="cuda"),
@@ -815,7 +827,7 @@ def run_profile(args):
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
-    ap.add_argument("--profile", choices=["store", "indexer", "topk", "mla", "step", "indexer_c8", "mla_fp8",
+    ap.add_argument("--profile", choices=["store", "indexer", "topk", "mla", "step", "indexer_c8", "mla_fp8", "dsv4",
                                           "prologue", "rope_q", "absorb",
                                           "v_up", "absorb4k"],
                     default=None,
