@@ -447,7 +447,8 @@ def dsa_sparse_mla_decode(q_bf16: torch.Tensor, kv_pool: torch.Tensor, block_tab
         _ptr(q_bf16), _ptr(kv_pool), kv_pool.shape[0], _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
         _ptr(cu_q), B, _ptr(idx), idx.shape[1], T, H, float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(dev_err), _stream(stream)))
-    _count(2 if T > 0 else 0)
+    # the attention kernel, and the split-K combine when the rows are split (scratch needed)
+    _count((1 + (1 if dsa_sparse_mla_workspace_size(T, H, idx.shape[1]) > 0 else 0)) if T > 0 else 0)
 
 
 def dsa_sparse_attn_swa_cmp_workspace_size(T: int, H: int, window: int, k: int) -> int:
@@ -489,7 +490,8 @@ def dsa_sparse_attn_swa_cmp(q_bf16: torch.Tensor, swa_kv: torch.Tensor, swa_bloc
         cmp_kv.shape[0], _ptr(cmp_block_table), cmp_block_table.shape[1], _ptr(seq_lens), _ptr(cu_q), B,
         _ptr(cmp_idx), cmp_idx.shape[1], int(window), int(cmp_ratio), _ptr(sinks), T, H, float(scale), _ptr(out),
         _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_err), _stream(stream)))
-    _count(1 if T > 0 else 0)   # (+ the combine when the rows are split)
+    split = dsa_sparse_attn_swa_cmp_workspace_size(T, H, window, cmp_idx.shape[1]) > 0
+    _count((1 + (1 if split else 0)) if T > 0 else 0)   # the kernel (+ the combine when the rows are split)
 
 
 def dsa_store_latent_fp8(latent_bf16: torch.Tensor, slot_mapping: torch.Tensor, k_scale: float,
@@ -538,7 +540,7 @@ def dsa_sparse_mla_decode_fp8(q_bf16: torch.Tensor, q_scale: float, kv_pool_fp8:
         _ptr(q_bf16), float(q_scale), _ptr(kv_pool_fp8), float(k_scale), kv_pool_fp8.shape[0], _ptr(block_table),
         block_table.shape[1], _ptr(seq_lens), _ptr(cu_q), B, _ptr(idx), idx.shape[1], T, H, float(scale), _ptr(out),
         _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_err), _stream(stream)))
-    _count(2 if T > 0 else 0)
+    _count((1 + (1 if dsa_sparse_mla_workspace_size(T, H, idx.shape[1]) > 0 else 0)) if T > 0 else 0)
 
 
 def dsa_sparse_mla_decode_noalloc(q_bf16: torch.Tensor, kv_pool: torch.Tensor, block_table: torch.Tensor,
