@@ -106,8 +106,15 @@ constexpr int kWTileBytes = kTileKeys * kIndexDim * 2;    // c8: 32 KB, one key 
 __global__ void __launch_bounds__(256)
 indexer_q_prologue_kernel(const uint16_t* __restrict__ q, const float* __restrict__ w,
                           const int32_t* __restrict__ cu_q, int B, int row_begin, int row_end, int mode,
-                          uint8_t* __restrict__ q_codes, float* __restrict__ q_gates) {
+                          uint8_t* __restrict__ q_codes, float* __restrict__ q_gates, uint32_t* __restrict__ hist_zero) {
     ptx::griddep_launch_dependents();
+    // the rows' top-12-bit histograms (one-call indexer) start at zero: block b clears words
+    // 512 b .. 512 b + 511 (8 blocks per row, 4096 words per row).  The logits kernel adds into them
+    // only after its query loads, which wait for this whole grid.
+    if (hist_zero != nullptr) {
+        hist_zero[blockIdx.x * 512 + threadIdx.x] = 0u;
+        hist_zero[blockIdx.x * 512 + 256 + threadIdx.x] = 0u;
+    }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t v = static_cast<int64_t>(blockIdx.x) * 8 + warp;   // (row - row_begin) * 64 + head
     if (v >= static_cast<int64_t>(row_end - row_begin) * kIndexHeads) return;
@@ -702,7 +709,8 @@ extern "C" size_t dsa_indexer_logits_c8_workspace_size(int32_t rows) {
 namespace dsa {
 
 // The logits call; with hist_g != nullptr (row groups of at most 2 rows) the kernel also adds each
-// row's top-12-bit order-key histogram into hist_g[(r - row_begin) * 4096 ..] (zeroed by the caller).
+// row's top-12-bit order-key histogram into hist_g[(r - row_begin) * 4096 ..] (zeroed here by the
+// query prologue).
 dsa_status indexer_logits_launch(const void* q_bf16, const float* weights, const uint8_t* index_k_pool,
                                  int64_t num_pages, const int32_t* block_table, int32_t max_pages,
                                  const int32_t* seq_lens, const int32_t* cu_q, int32_t B, int32_t max_seq_len,
@@ -759,7 +767,7 @@ dsa_status indexer_logits_launch(const void* q_bf16, const float* weights, const
 
     // query prologue: 8 vectors per 256-thread block
     indexer_q_prologue_kernel<<<static_cast<unsigned>(rows) * (kIndexHeads / 8), 256, 0, st>>>(
-        static_cast<const uint16_t*>(q_bf16), weights, cu_q, B, row_begin, row_end, mode, q_codes, q_gates);
+        static_cast<const uint16_t*>(q_bf16), weights, cu_q, B, row_begin, row_end, mode, q_codes, q_gates, hist_g);
     if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
 
     cudaLaunchAttribute attr[1];

@@ -52,9 +52,6 @@ extern "C" dsa_status dsa_lightning_indexer(const void* q_bf16, const float* wei
     float* logits = reinterpret_cast<float*>(ws + hist_bytes(T) + idx_ws);
     const int64_t ld = lightning_logits_ld(max_seq_len);
     const bool fused = fused_ok(max_seq_len, max_q_len);
-    if (fused && cudaMemsetAsync(hist, 0, static_cast<size_t>(T) * dsa::kHistBins * 4,
-                                 static_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return DSA_ERR_CUDA;
     dsa_status st = dsa::indexer_logits_launch(q_bf16, weights, index_k_pool, num_pages, block_table, max_pages,
                                                seq_lens, cu_q, B, max_seq_len, max_q_len, 0, T, logits, ld, flags,
                                                logits_ws, idx_ws, dev_err, stream, fused ? hist : nullptr);
