@@ -95,6 +95,8 @@ constexpr int kThreads = 352;                             // 11 warps
 constexpr int kEpiWarp0 = 2;                              // warps 2..9: two epilogue warpgroups
 constexpr int kLoaderWarp = 10;
 constexpr int kWidenWarp0 = 11;                           // c8: warps 11..14 widen int8 key tiles to f16
+constexpr int kProducer1Warp = 11;                        // two pipelines: key producer of pipeline 1
+constexpr int kMma1Warp = 12;                             // two pipelines: MMA issuer of pipeline 1
 constexpr int kQRowBytesC8 = kIndexHeads * kIndexDim * 2; // c8: 16 KB of f16 query codes per row
 constexpr int kWTileBytes = kTileKeys * kIndexDim * 2;    // c8: 32 KB, one key tile widened to f16
 
@@ -242,19 +244,30 @@ __device__ __forceinline__ int64_t epi_scan(int64_t v, int64_t* scratch, int64_t
 //
 // Warp roles (352 threads): warp 0 = key producer, warp 1 = TMEM owner + MMA issuer, warps 2-9 =
 // two epilogue warpgroups taking alternate tiles (warp w reads TMEM lanes 32 (w % 4) .. +31, one
-// key per thread: ReLU, gates w', head sum, key scale, store), warp 10 = query-tile loader.
+// key per thread: ReLU, gates w', head sum, key scale, store), warp 10 = query-tile loader.  With
+// two pipelines (416 threads) the alternate tiles form two independent streams: warps 0 / 1 /
+// epilogue group 0 handle the even tiles with stage ring 0 and accumulators 0-1, warps 11 / 12 /
+// epilogue group 1 the odd tiles with ring 1 and accumulators 2-3.
 // ---------------------------------------------------------------------------------------------
 template <int R, bool HIST = false, bool C8 = false>
 struct IdxCfg {
     static_assert(!HIST || R <= 2, "the per-row histograms fit shared memory for row groups of up to 2 rows");
     static_assert(!C8 || (R <= 2 && !HIST), "the int8 cache: row groups of up to 2 rows, no histograms");
     static constexpr int N = 64 * R;
-    static constexpr int kThreadsCfg = C8 ? kThreads + 4 * 32 : kThreads;
+    // Independent pipelines per CTA: pipeline p takes the CTA's tiles i with i % kPipes == p and has
+    // its own key producer, stage ring, MMA issuer, accumulators and epilogue warpgroup, so a key
+    // page that is late stalls only its own pipeline (one in-order ring streams random pages ~12 %
+    // slower: every stage behind a late page waits for it).
+    static constexpr int kPipes = (C8 || R == 4) ? 1 : 2;
+    static constexpr int kThreadsCfg = C8 ? kThreads + 4 * 32 : (kPipes == 2 ? kThreads + 2 * 32 : kThreads);
     // with HIST, the R 16 KB histograms take the place of R (or, for R = 2, two) key stages; with C8
     // the two 32 KB f16 key tiles and the f16 query take the place of key stages
     static constexpr int kStages =
-        C8 ? (R == 1 ? 7 : 5) : ((R == 1) ? (HIST ? 11 : 12) : (R == 2 ? (HIST ? 9 : 11) : 9));
+        C8 ? (R == 1 ? 7 : 5) : ((R == 1) ? (HIST ? 10 : 12) : (R == 2 ? (HIST ? 8 : 10) : 9));
+    static_assert(kStages % kPipes == 0, "equal rings");
+    static constexpr int kStagesPipe = kStages / kPipes;
     static constexpr int kAcc = (R == 4) ? 2 : 4;                 // accumulators of N columns
+    static constexpr int kAccPipe = kAcc / kPipes;
     static constexpr uint32_t kTmemCols = kAcc * N;               // 256 / 512 / 512
     static constexpr int kQRowB = C8 ? kQRowBytesC8 : kQRowBytes;
     static constexpr int kQBytes = R * kQRowB;
@@ -290,6 +303,15 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
     constexpr int S = C::kStages;
     constexpr int N = C::N;
     constexpr int NA = C::kAcc;
+    constexpr int P = C::kPipes;
+    constexpr int SP = C::kStagesPipe;
+    constexpr int NAP = C::kAccPipe;
+    // tile i of this CTA: pipeline i % P, stage and accumulator of that pipeline's ring, and the
+    // parities of their barriers on this use
+    auto stage_of = [](int i) { return (i % P) * SP + (i / P) % SP; };
+    auto stage_ph = [](int i) { return static_cast<uint32_t>((i / P) / SP) & 1u; };
+    auto acc_of = [](int i) { return (i % P) * NAP + (i / P) % NAP; };
+    auto acc_ph = [](int i) { return static_cast<uint32_t>((i / P) / NAP) & 1u; };
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw_addr = ptx::smem_addr(smem_raw);
     unsigned char* base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -338,7 +360,7 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
         }
         for (int b2 = 0; b2 < 2; ++b2) {
             ptx::mbar_init(&qfull[b2], 1);
-            ptx::mbar_init(&qempty[b2], 1 + 8);  // MMA commit + every epilogue warp
+            ptx::mbar_init(&qempty[b2], P + 8);  // each MMA issuer's commit + every epilogue warp
         }
         ptx::mbar_init(hsync, 8);
         ptx::fence_barrier_init();
@@ -411,12 +433,14 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
         sg.tile = part[1];
     }
 
-    if (warp == 0 && count > 0) {   // ---------------- key producer
+    if ((warp == 0 || (P == 2 && warp == kProducer1Warp)) && count > 0) {   // ---------------- key producer
+        const int pipe = warp == 0 ? 0 : 1;   // issues the tiles i with i % P == pipe
         int32_t win = -1;           // block-table entries 2 * wbase + lane of segment wseg
         int wbase = -1, wseg = -1;
-        int s = 0;
-        uint32_t ph = 0;
         for (int i = 0; i < count; ++i) {
+          if (i % P == pipe) {
+            const int s = stage_of(i);
+            const uint32_t ph = stage_ph(i);
             const int wb = sg.tile & ~15;
             if (wb != wbase || sg.sidx != wseg) {
                 wbase = wb;
@@ -456,7 +480,7 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
                 }
             }
             if (__shfl_sync(0xffffffffu, timed_out ? 1 : 0, 0)) { timed_out = true; break; }
-            if (++s == S) { s = 0; ph ^= 1u; }
+          }
             if (++sg.tile == sg.ntiles && i + 1 < count) seg_next(sa, sg);
         }
     } else if (warp == kLoaderWarp && count > 0) {   // ---------------- query-tile loader
@@ -491,18 +515,23 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
                 if (remaining > 0) seg_next(sa, sg);
             }
         }
-    } else if (warp == 1 && count > 0) {   // ---------------- MMA issuer
+    } else if ((warp == 1 || (P == 2 && warp == kMma1Warp)) && count > 0) {   // ---------------- MMA issuer
         if (lane == 0) {
+            const int pipe = warp == 1 ? 0 : 1;   // issues the tiles i with i % P == pipe
             constexpr uint32_t idesc = ptx::instr_desc(0, 0, kTileKeys, N);
-            int s = 0, n = 0;
-            uint32_t ph = 0;
+            int n = 0;
             bool seg_start = true;
             for (int i = 0; i < count && !timed_out; ++i) {
                 const int qb = n & 1;
+                // every issuer meets every segment's query tile, so that each segment's release of
+                // the tile (qempty) gets one commit per issuer after its last MMA on it
                 if (seg_start && !ptx::mbar_wait(&qfull[qb], (n >> 1) & 1, deadline)) { timed_out = true; break; }
                 seg_start = false;
-                const int a = i % NA;
-                const uint32_t aph = (i / NA) & 1;
+              if (i % P == pipe) {
+                const int s = stage_of(i);
+                const uint32_t ph = stage_ph(i);
+                const int a = acc_of(i);
+                const uint32_t aph = acc_ph(i);
                 if (C8) {
                     if (!ptx::mbar_wait(&wfull[i & 1], (i >> 1) & 1, deadline)) { timed_out = true; break; }
                 } else if (!ptx::mbar_wait(&full[s], ph, deadline)) {
@@ -535,7 +564,7 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
                     ptx::umma_commit(&empty[s]);
                 }
                 ptx::umma_commit(&tfull[a]);
-                if (++s == S) { s = 0; ph ^= 1u; }
+              }
                 if (++sg.tile == sg.ntiles || i + 1 == count) {   // last tile of the segment here
                     ptx::umma_commit(&qempty[qb]);
                     ++n;
@@ -583,16 +612,17 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
         const int quad = warp & 3;
         const int key_in_tile = quad * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        int s = 0, n = 0;
-        uint32_t ph = 0;
+        int n = 0;
         bool seg_start = true;
         for (int i = 0; i < count; ++i) {
             const int qb = n & 1;
             if (seg_start && !ptx::mbar_wait(&qfull[qb], (n >> 1) & 1, deadline)) { timed_out = true; break; }
             seg_start = false;
-            if ((i & 1) == grp) {
-                const int a = i % NA;
-                const uint32_t aph = (i / NA) & 1;
+            if ((i & 1) == grp) {   // with two pipelines: the tiles of pipeline grp
+                const int s = stage_of(i);
+                const uint32_t ph = stage_ph(i);
+                const int a = acc_of(i);
+                const uint32_t aph = acc_ph(i);
                 if (!ptx::mbar_wait(&full[s], ph, deadline)) { timed_out = true; break; }
                 if (!ptx::mbar_wait(&tfull[a], aph, deadline)) { timed_out = true; break; }
                 ptx::tc_fence_after_sync();
@@ -635,7 +665,6 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
                     ptx::mbar_arrive(&empty[s]);
                 }
             }
-            if (++s == S) { s = 0; ph ^= 1u; }
             if (++sg.tile == sg.ntiles || i + 1 == count) {   // leaving the segment: its gates are free
                 if (HIST) {
                     // every epilogue warp's counts of this segment are in; add the non-empty bins to
@@ -784,6 +813,7 @@ dsa_status indexer_logits_launch(const void* q_bf16, const float* weights, const
 #define DSA_LAUNCH_IDX(RR, HH)                                                                                  \
     do {                                                                                                        \
         const size_t smem = IdxCfg<RR, HH>::kSmemBytes;                                                         \
+        cfg.blockDim = dim3(IdxCfg<RR, HH>::kThreadsCfg, 1, 1);                                                 \
         if (cudaFuncSetAttribute(indexer_logits_umma_kernel<RR, HH, false>,                                     \
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess) \
             return DSA_ERR_CUDA;                                                                                \
