@@ -107,13 +107,15 @@ topk_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* __restr
             const int32_t* __restrict__ cu_q, int B, int row_begin, int k, int n_init, int n_local, int cmp_shift,
             int32_t* __restrict__ idx) {
     __shared__ TopkSmem sm;
-    ptx::griddep_wait();   // launched as a programmatic dependent: the logits are complete from here on
+    // launched as a programmatic dependent of the logits kernel: the row's request is looked up in
+    // the inputs (not written by that kernel) while it finishes, the logits are read after the wait
     ptx::griddep_launch_dependents();
     const int rl = blockIdx.x;                  // local row
     const int r = row_begin + rl;
     const int b = row_request(cu_q, B, r);
     const int q0 = __ldg(cu_q + b);
     int v = visible_len(__ldg(seq_lens + b), __ldg(cu_q + b + 1) - q0, r - q0) >> cmp_shift;
+    ptx::griddep_wait();
     if (v > ld) v = static_cast<int>(ld);       // never read past the row
     const float* row = logits + static_cast<int64_t>(rl) * ld;
     const Forced<FORCED> F = make_forced<FORCED>(v, n_init, n_local);
@@ -291,11 +293,13 @@ topk_bitmap_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* 
     uint32_t* ckey = tie + words_cap;
     int32_t* cidx = reinterpret_cast<int32_t*>(ckey + kCandidateCap);
 
-    ptx::griddep_wait();   // launched as a programmatic dependent: the logits are complete from here on
+    // launched as a programmatic dependent of the logits kernel: the row's request is looked up in
+    // the inputs (not written by that kernel) while it finishes, the logits are read after the wait
     ptx::griddep_launch_dependents();
     const int rl = blockIdx.x;
     const int r = row_begin + rl;
     int v = locate_visible(cu_q, seq_lens, B, r, cmp_shift, sm);
+    ptx::griddep_wait();
     if (v > ld) v = static_cast<int>(ld);
     if (v > words_cap * 32) v = words_cap * 32;   // the launcher guarantees this never clips
     const float* row = logits + static_cast<int64_t>(rl) * ld;
@@ -502,7 +506,9 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t*
     uint32_t* ckey = tie + words_cap;
     int32_t* cidx = reinterpret_cast<int32_t*>(ckey + kCandidateCap);
 
-    ptx::griddep_wait();   // launched as a programmatic dependent: the logits are complete from here on
+    // launched as a programmatic dependent of the logits kernel: shared buffers are cleared and the
+    // row's request is looked up in the inputs (not written by that kernel) while it finishes, the
+    // logits and histograms are read after the wait
     ptx::griddep_launch_dependents();
     const uint32_t half = cluster_rank();
     const uint32_t peer = half ^ 1u;
@@ -513,6 +519,7 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t*
     for (int i = threadIdx.x; i < 2 * 1024; i += kTopkThreads) lo_hist[i] = 0;
     if (threadIdx.x == 0) sm.cand_count = 0;
     int v = locate_visible(cu_q, seq_lens, B, r, cmp_shift, sm);
+    ptx::griddep_wait();
     if (v > ld) v = static_cast<int>(ld);
     if (v > 2 * words_cap * 32 - 256) v = 2 * words_cap * 32 - 256;   // the launcher guarantees this never clips
     const float* row = logits + static_cast<int64_t>(rl) * ld;
