@@ -191,6 +191,7 @@ struct BitmapSmem {
     uint32_t cand_count;
     int32_t row_v;
 };
+static_assert(sizeof(BitmapSmem) % 16 == 0, "16-byte alignment of the buffers after BitmapSmem");
 
 // Visible length of global row r, looked up by all threads at once: thread t < B tests whether r
 // falls in request t (one round of independent loads instead of a chain of dependent ones).
@@ -452,7 +453,10 @@ topk_bitmap_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* 
 // buffer of its own) is built locally in shared memory and summed with the peer's through
 // distributed shared memory after one cluster barrier (16-byte remote reads, no remote atomics),
 // so both CTAs take the same digit decisions; each marks its own half's bitmaps and writes its
-// kept indices, the second half offset by the first half's counts.
+// kept indices, the second half offset by the first half's counts.  Given the histogram (the fused
+// indexer), each CTA copies its half row into shared memory (16-byte cp.async by every thread)
+// while it loads the histogram and finds the threshold bin, and its pass over the keys reads that
+// copy (when the half row fits beside the other buffers: up to ~29 K keys on this GPU).
 // ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
@@ -495,7 +499,7 @@ __global__ void __launch_bounds__(kTopkThreads)
 topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* __restrict__ seq_lens,
                     const int32_t* __restrict__ cu_q, int B, int row_begin, int k, int n_init, int n_local, int cmp_shift,
                     int32_t* __restrict__ idx,
-                    int words_cap, const uint32_t* __restrict__ hist_g) {
+                    int words_cap, const uint32_t* __restrict__ hist_g, int cand_cap, int row_cap) {
     extern __shared__ __align__(16) unsigned char dsm[];
     BitmapSmem& sm = *reinterpret_cast<BitmapSmem*>(dsm);                      // hist: the top digit
     uint32_t* total = reinterpret_cast<uint32_t*>(dsm + sizeof(BitmapSmem));   // summed histogram
@@ -504,7 +508,11 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t*
     uint32_t* sel = xcnt + 4;
     uint32_t* tie = sel + words_cap;
     uint32_t* ckey = tie + words_cap;
-    int32_t* cidx = reinterpret_cast<int32_t*>(ckey + kCandidateCap);
+    int32_t* cidx = reinterpret_cast<int32_t*>(ckey + cand_cap);
+    // with the histograms given (PREHIST) and row_cap > 0: a copy of this half of the row, fetched
+    // while the threshold bin is found, so that the pass over the keys reads shared memory (16-byte
+    // aligned: BitmapSmem's size, cand_cap and words_cap are multiples of 16 bytes / 4 words)
+    float* rowbuf = reinterpret_cast<float*>(cidx + cand_cap);
 
     // launched as a programmatic dependent of the logits kernel: shared buffers are cleared and the
     // row's request is looked up in the inputs (not written by that kernel) while it finishes, the
@@ -540,6 +548,17 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t*
 
     const bool vec = (reinterpret_cast<uintptr_t>(part) & 15u) == 0;
     const int v4 = vec ? (nloc >> 2) : 0;
+    // PREHIST: this half of the row into shared memory (16-byte copies by every thread, in flight
+    // while the histogram is loaded and its threshold bin found; the bytes read stay inside the
+    // row: lo and ld are multiples of 4)
+    const bool use_row = PREHIST && vec && row_cap > 0 && nloc <= row_cap;
+    if (use_row) {
+        const uint32_t dst0 = ptx::smem_addr(rowbuf);
+        const float4* src4 = reinterpret_cast<const float4*>(part);
+        for (int i = threadIdx.x; i < (nloc + 3) >> 2; i += kTopkThreads)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst0 + 16u * i), "l"(src4 + i) : "memory");
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
     auto for_each_key = [&](auto&& fn) {   // (local index, key) of this half
         const float4* p4 = reinterpret_cast<const float4*>(part);
         constexpr int U = 4;
@@ -577,21 +596,36 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t*
     uint32_t need = sm.sel_remaining;
 
     // ---- read 2: mark keys above the threshold bin, collect the threshold bin (this half)
-    for_each_key([&](int s, uint32_t key) {
+    if (use_row) {   // every thread's copies landed, then all of them are visible
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        __syncthreads();
+    }
+    auto mark = [&](int s, uint32_t key) {
         const uint32_t bin = key >> 20;
         if (bin > b1) {
             atomicOr(&sel[s >> 5], 1u << (s & 31));
         } else if (bin == b1) {
             const uint32_t p = atomicAdd(&sm.cand_count, 1u);
-            if (p < static_cast<uint32_t>(kCandidateCap)) {
+            if (p < static_cast<uint32_t>(cand_cap)) {
                 ckey[p] = key;
                 cidx[p] = s;
             }
         }
-    });
+    };
+    if (use_row) {
+        const float4* r4 = reinterpret_cast<const float4*>(rowbuf);
+        for (int i = threadIdx.x; i < v4; i += kTopkThreads) {
+            const float4 a = r4[i];
+            mark(4 * i, F(4 * i, order_key(a.x))); mark(4 * i + 1, F(4 * i + 1, order_key(a.y)));
+            mark(4 * i + 2, F(4 * i + 2, order_key(a.z))); mark(4 * i + 3, F(4 * i + 3, order_key(a.w)));
+        }
+        for (int s = 4 * v4 + threadIdx.x; s < nloc; s += kTopkThreads) mark(s, F(s, order_key(rowbuf[s])));
+    } else {
+        for_each_key(mark);
+    }
     __syncthreads();
     const uint32_t n = sm.cand_count;
-    const bool in_smem = n <= static_cast<uint32_t>(kCandidateCap);
+    const bool in_smem = n <= static_cast<uint32_t>(cand_cap);
     // ---- low digits: bits [19:10], then [9:0], over both halves' threshold-bin keys
     uint32_t prefix = b1 << 20;
     for (int pass = 0; pass < 2; ++pass) {
@@ -679,9 +713,9 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t*
     cluster_sync();   // the peer has read this CTA's histograms and counts before either leaves
 }
 
-size_t cluster_smem_bytes(int words) {
+size_t cluster_smem_bytes(int words, int cand_cap, int row_cap) {
     return sizeof(BitmapSmem) + static_cast<size_t>(kTopBins) * 4 + 2 * 1024 * 4 + 16 +
-           2 * static_cast<size_t>(words) * 4 + static_cast<size_t>(kCandidateCap) * 8;
+           2 * static_cast<size_t>(words) * 4 + static_cast<size_t>(cand_cap) * 8 + static_cast<size_t>(row_cap) * 4;
 }
 
 size_t bitmap_smem_bytes(int words) {
@@ -739,7 +773,18 @@ dsa_status topk_launch(const float* logits, int64_t ld, const int32_t* seq_lens,
         const int half_keys = ((max_seq_len + 1) / 2 + 127) & ~127;
         int words_cap = ((half_keys + 256 + 31) / 32 + 3) & ~3;
         if (words_cap < 32) words_cap = 32;
-        const size_t smem = dsa::cluster_smem_bytes(words_cap);
+        // with the histograms given: the half row in shared memory as well when it fits (the
+        // threshold-bin candidates then get 4096 slots instead of 8192; more fall back to rows)
+        int cand_cap = dsa::kCandidateCap, row_cap = 0;
+        int smem_max = 0;
+        if (cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return DSA_ERR_CUDA;
+        const int row_keys = (half_keys + 3) & ~3;
+        if (pre && dsa::cluster_smem_bytes(words_cap, 4096, row_keys) <= static_cast<size_t>(smem_max)) {
+            cand_cap = 4096;
+            row_cap = row_keys;
+        }
+        const size_t smem = dsa::cluster_smem_bytes(words_cap, cand_cap, row_cap);
         void* kern = forced ? (pre ? topk_cluster_fn<true, true>() : topk_cluster_fn<true, false>())
                             : (pre ? topk_cluster_fn<false, true>() : topk_cluster_fn<false, false>());
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
@@ -757,7 +802,8 @@ dsa_status topk_launch(const float* logits, int64_t ld, const int32_t* seq_lens,
         cfg.dynamicSmemBytes = smem;
         int a_B = B, a_rb = row_begin, a_k = k, a_ni = n_init, a_nl = n_local, a_sh = cmp_shift, a_wc = words_cap;
         void* args[] = {const_cast<float**>(&logits), &ld, const_cast<int32_t**>(&seq_lens), const_cast<int32_t**>(&cu_q),
-                        &a_B, &a_rb, &a_k, &a_ni, &a_nl, &a_sh, &idx, &a_wc, const_cast<uint32_t**>(&hist_g)};
+                        &a_B, &a_rb, &a_k, &a_ni, &a_nl, &a_sh, &idx, &a_wc, const_cast<uint32_t**>(&hist_g),
+                        &cand_cap, &row_cap};
         if (cudaLaunchKernelExC(&cfg, kern, args) != cudaSuccess) return DSA_ERR_CUDA;
     } else if (words <= dsa::kMaxBitmapWords) {
         const int words_cap = words < 32 ? 32 : words;
