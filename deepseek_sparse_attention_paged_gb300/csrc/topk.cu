@@ -262,11 +262,18 @@ __device__ void select_bin(uint32_t* hist, BitmapSmem& sm, int bins, uint32_t ne
 
 // The row's top-12-bit histogram produced by the logits kernel (fused indexer + top-k) into
 // hist[0, 4096): counts of the order keys of every visible logit of the row.  Positions forced to
-// +inf leave their own bin for the +inf bin (the same mapping the key visits apply).
-template <bool FORCED>
+// +inf leave their own bin for the +inf bin (the same mapping the key visits apply).  `issued`
+// runs once the histogram's loads are in flight (work queued behind them, not ahead).
+template <bool FORCED, class Issued>
 __device__ void load_row_histogram(uint32_t* hist, const uint32_t* __restrict__ hist_row, const float* __restrict__ row,
-                                   const Forced<FORCED>& Fg, int v) {
-    for (int i = threadIdx.x; i < kTopBins; i += kTopkThreads) hist[i] = __ldg(hist_row + i);
+                                   const Forced<FORCED>& Fg, int v, Issued&& issued) {
+    constexpr int kPer = kTopBins / kTopkThreads;
+    uint32_t h[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) h[j] = __ldg(hist_row + threadIdx.x + j * kTopkThreads);
+    issued();
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) hist[threadIdx.x + j * kTopkThreads] = h[j];
     __syncthreads();
     if (FORCED) {
         const int n1 = Fg.init_end;                    // [0, init_end)
@@ -341,7 +348,7 @@ topk_bitmap_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* 
 
     // ---- read 1: top-12-bit histogram (given by the logits kernel in the fused call)
     if (PREHIST) {
-        load_row_histogram<FORCED>(sm.hist, hist_g + static_cast<int64_t>(rl) * kTopBins, row, F, v);
+        load_row_histogram<FORCED>(sm.hist, hist_g + static_cast<int64_t>(rl) * kTopBins, row, F, v, [] {});
     } else {
         for (int i = threadIdx.x; i < kTopBins; i += kTopkThreads) sm.hist[i] = 0;
         __syncthreads();
@@ -548,17 +555,18 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t*
 
     const bool vec = (reinterpret_cast<uintptr_t>(part) & 15u) == 0;
     const int v4 = vec ? (nloc >> 2) : 0;
-    // PREHIST: this half of the row into shared memory (16-byte copies by every thread, in flight
-    // while the histogram is loaded and its threshold bin found; the bytes read stay inside the
-    // row: lo and ld are multiples of 4)
+    // PREHIST: this half of the row into shared memory (16-byte copies by every thread, issued right
+    // after the histogram's loads and in flight while the threshold bin is found; the bytes read
+    // stay inside the row: lo and ld are multiples of 4)
     const bool use_row = PREHIST && vec && row_cap > 0 && nloc <= row_cap;
-    if (use_row) {
+    auto copy_row = [&] {
+        if (!use_row) return;
         const uint32_t dst0 = ptx::smem_addr(rowbuf);
         const float4* src4 = reinterpret_cast<const float4*>(part);
         for (int i = threadIdx.x; i < (nloc + 3) >> 2; i += kTopkThreads)
             asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst0 + 16u * i), "l"(src4 + i) : "memory");
         asm volatile("cp.async.commit_group;" ::: "memory");
-    }
+    };
     auto for_each_key = [&](auto&& fn) {   // (local index, key) of this half
         const float4* p4 = reinterpret_cast<const float4*>(part);
         constexpr int U = 4;
@@ -585,7 +593,7 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t*
     // ---- read 1: top-12-bit histogram of this half, summed with the peer's (in the fused call: the
     // whole row's histogram from the logits kernel, the same in both CTAs)
     if (PREHIST) {
-        load_row_histogram<FORCED>(total, hist_g + static_cast<int64_t>(rl) * kTopBins, row, Fg, v);
+        load_row_histogram<FORCED>(total, hist_g + static_cast<int64_t>(rl) * kTopBins, row, Fg, v, copy_row);
     } else {
         for_each_key([&](int, uint32_t key) { atomicAdd(&sm.hist[key >> 20], 1u); });
         __syncthreads();
