@@ -454,16 +454,17 @@ topk_bitmap_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* 
 }
 
 // ---------------------------------------------------------------------------------------------
-// Cluster kernel: the same two-read scheme with each long row split over a 2-CTA cluster (for
-// batches with fewer rows than SM pairs).  CTA h takes keys [h ? split : 0, h ? v : split), split
-// a multiple of 128.  Every histogram (the 12-bit top digit, then each 10-bit low digit, each in a
-// buffer of its own) is built locally in shared memory and summed with the peer's through
-// distributed shared memory after one cluster barrier (16-byte remote reads, no remote atomics),
-// so both CTAs take the same digit decisions; each marks its own half's bitmaps and writes its
-// kept indices, the second half offset by the first half's counts.  Given the histogram (the fused
-// indexer), each CTA copies its half row into shared memory (16-byte cp.async by every thread)
-// while it loads the histogram and finds the threshold bin, and its pass over the keys reads that
-// copy (when the half row fits beside the other buffers: up to ~29 K keys on this GPU).
+// Cluster kernel: the same two-read scheme with each long row split over a cluster of N = 2 or 4
+// CTAs (for batches with few rows: N rows' worth of CTAs fit the GPU at once).  CTA c takes the
+// keys [c w, (c + 1) w) of the row (clipped to v), w = ceil(v / N) rounded up to a multiple of 128.
+// Every histogram (the 12-bit top digit, then each 10-bit low digit, each in a buffer of its own)
+// is built locally in shared memory and summed over the cluster through distributed shared memory
+// after one cluster barrier (16-byte remote reads, no remote atomics), so every CTA takes the same
+// digit decisions; each marks its own part's bitmaps and writes its kept indices, offset by the
+// kept counts of the CTAs before it.  Given the histogram (the fused indexer), each CTA copies its
+// part of the row into shared memory (16-byte cp.async by every thread) while it loads the
+// histogram and finds the threshold bin, and its pass over the keys reads that copy (when the part
+// fits beside the other buffers: up to ~29 K keys on this GPU).
 // ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
@@ -487,21 +488,25 @@ __device__ __forceinline__ uint4 ld_rank_v4(const uint32_t* p, uint32_t rank) {
     return v;
 }
 
-// total[b] = this CTA's hist[b] + the peer's hist[b], b < bins (a multiple of 4).  Both CTAs'
-// histograms are complete on entry.  A histogram buffer is never written again after it has been
-// summed, and the kernel ends with a cluster barrier, so no barrier is needed after the reads.
-__device__ __forceinline__ void sum_with_peer(const uint32_t* hist, uint32_t* total, int bins, uint32_t peer) {
-    cluster_sync();   // the peer's histogram is complete and visible
+// total[b] = the sum over the cluster's CTAs of their hist[b], b < bins (a multiple of 4).  Every
+// CTA's histogram is complete on entry.  A histogram buffer is never written again after it has
+// been summed, and the kernel ends with a cluster barrier, so no barrier is needed after the reads.
+template <int NC>
+__device__ __forceinline__ void sum_over_cluster(const uint32_t* hist, uint32_t* total, int bins, uint32_t rank) {
+    cluster_sync();   // every CTA's histogram is complete and visible
     for (int q = threadIdx.x; q < bins / 4; q += kTopkThreads) {
-        const uint4 mine = reinterpret_cast<const uint4*>(hist)[q];
-        const uint4 theirs = ld_rank_v4(hist + 4 * q, peer);
-        reinterpret_cast<uint4*>(total)[q] =
-            make_uint4(mine.x + theirs.x, mine.y + theirs.y, mine.z + theirs.z, mine.w + theirs.w);
+        uint4 acc = reinterpret_cast<const uint4*>(hist)[q];
+#pragma unroll
+        for (int j = 1; j < NC; ++j) {
+            const uint4 o = ld_rank_v4(hist + 4 * q, (rank + j) % NC);
+            acc.x += o.x; acc.y += o.y; acc.z += o.z; acc.w += o.w;
+        }
+        reinterpret_cast<uint4*>(total)[q] = acc;
     }
     __syncthreads();
 }
 
-template <bool FORCED, bool PREHIST>
+template <bool FORCED, bool PREHIST, int NC>
 __global__ void __launch_bounds__(kTopkThreads)
 topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* __restrict__ seq_lens,
                     const int32_t* __restrict__ cu_q, int B, int row_begin, int k, int n_init, int n_local, int cmp_shift,
@@ -511,12 +516,12 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t*
     BitmapSmem& sm = *reinterpret_cast<BitmapSmem*>(dsm);                      // hist: the top digit
     uint32_t* total = reinterpret_cast<uint32_t*>(dsm + sizeof(BitmapSmem));   // summed histogram
     uint32_t* lo_hist = total + kTopBins;                                        // [2][1024]: low digits
-    uint32_t* xcnt = lo_hist + 2 * 1024;                                         // this half's kept counts
+    uint32_t* xcnt = lo_hist + 2 * 1024;                                         // this part's kept counts
     uint32_t* sel = xcnt + 4;
     uint32_t* tie = sel + words_cap;
     uint32_t* ckey = tie + words_cap;
     int32_t* cidx = reinterpret_cast<int32_t*>(ckey + cand_cap);
-    // with the histograms given (PREHIST) and row_cap > 0: a copy of this half of the row, fetched
+    // with the histograms given (PREHIST) and row_cap > 0: a copy of this CTA's part of the row, fetched
     // while the threshold bin is found, so that the pass over the keys reads shared memory (16-byte
     // aligned: BitmapSmem's size, cand_cap and words_cap are multiples of 16 bytes / 4 words)
     float* rowbuf = reinterpret_cast<float*>(cidx + cand_cap);
@@ -525,8 +530,8 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t*
     // row's request is looked up in the inputs (not written by that kernel) while it finishes, the
     // logits and histograms are read after the wait
     ptx::griddep_launch_dependents();
-    const uint32_t half = cluster_rank();
-    const uint32_t peer = half ^ 1u;
+    const uint32_t rank = cluster_rank();
+    constexpr uint32_t ncta = NC;   // CTAs in the cluster (the launch's cluster size)
     const int rl = blockIdx.y;
     const int r = row_begin + rl;
     // histogram buffers zeroed while the row's request is looked up
@@ -536,26 +541,28 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t*
     int v = locate_visible(cu_q, seq_lens, B, r, cmp_shift, sm);
     ptx::griddep_wait();
     if (v > ld) v = static_cast<int>(ld);
-    if (v > 2 * words_cap * 32 - 256) v = 2 * words_cap * 32 - 256;   // the launcher guarantees this never clips
+    // every CTA's part fits its bitmaps (the launcher guarantees this never clips)
+    const int v_fit = static_cast<int>(ncta) * (words_cap * 32 - 256);
+    if (v > v_fit) v = v_fit;
     const float* row = logits + static_cast<int64_t>(rl) * ld;
     int32_t* out = idx + static_cast<int64_t>(rl) * k;
-    if (v <= k) {   // both CTAs leave here, before any cluster barrier
-        if (half == 0)
+    if (v <= k) {   // every CTA leaves here, before any cluster barrier
+        if (rank == 0)
             for (int j = threadIdx.x; j < k; j += kTopkThreads) out[j] = j < v ? j : -1;
         return;
     }
-    const int split = min(v, ((v + 1) / 2 + 127) & ~127);
-    const int lo = half == 0 ? 0 : split;
-    const int nloc = (half == 0 ? split : v) - lo;
+    const int chunk = ((v + static_cast<int>(ncta) - 1) / static_cast<int>(ncta) + 127) & ~127;
+    const int lo = min(v, static_cast<int>(rank) * chunk);
+    const int nloc = min(v, lo + chunk) - lo;
     const int W = (nloc + 31) / 32;
     const float* part = row + lo;
     const Forced<FORCED> Fg = make_forced<FORCED>(v, n_init, n_local);
-    const Forced<FORCED> F = {Fg.init_end - lo, Fg.local_begin - lo};   // in this half's local indices
+    const Forced<FORCED> F = {Fg.init_end - lo, Fg.local_begin - lo};   // in this part's local indices
     for (int w = threadIdx.x; w < W; w += kTopkThreads) sel[w] = tie[w] = 0u;
 
     const bool vec = (reinterpret_cast<uintptr_t>(part) & 15u) == 0;
     const int v4 = vec ? (nloc >> 2) : 0;
-    // PREHIST: this half of the row into shared memory (16-byte copies by every thread, issued right
+    // PREHIST: this part of the row into shared memory (16-byte copies by every thread, issued right
     // after the histogram's loads and in flight while the threshold bin is found; the bytes read
     // stay inside the row: lo and ld are multiples of 4)
     const bool use_row = PREHIST && vec && row_cap > 0 && nloc <= row_cap;
@@ -567,7 +574,7 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t*
             asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst0 + 16u * i), "l"(src4 + i) : "memory");
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
-    auto for_each_key = [&](auto&& fn) {   // (local index, key) of this half
+    auto for_each_key = [&](auto&& fn) {   // (local index, key) of this part
         const float4* p4 = reinterpret_cast<const float4*>(part);
         constexpr int U = 4;
         int i = threadIdx.x;
@@ -590,20 +597,20 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t*
         for (int s = 4 * v4 + threadIdx.x; s < nloc; s += kTopkThreads) fn(s, F(s, order_key(__ldg(part + s))));
     };
 
-    // ---- read 1: top-12-bit histogram of this half, summed with the peer's (in the fused call: the
-    // whole row's histogram from the logits kernel, the same in both CTAs)
+    // ---- read 1: top-12-bit histogram of this part, summed over the cluster (in the fused call: the
+    // whole row's histogram from the logits kernel, the same in every CTA)
     if (PREHIST) {
         load_row_histogram<FORCED>(total, hist_g + static_cast<int64_t>(rl) * kTopBins, row, Fg, v, copy_row);
     } else {
         for_each_key([&](int, uint32_t key) { atomicAdd(&sm.hist[key >> 20], 1u); });
         __syncthreads();
-        sum_with_peer(sm.hist, total, kTopBins, peer);
+        sum_over_cluster<NC>(sm.hist, total, kTopBins, rank);
     }
     select_bin(total, sm, kTopBins, static_cast<uint32_t>(k));
     const uint32_t b1 = sm.sel_digit;
     uint32_t need = sm.sel_remaining;
 
-    // ---- read 2: mark keys above the threshold bin, collect the threshold bin (this half)
+    // ---- read 2: mark keys above the threshold bin, collect the threshold bin (this part)
     if (use_row) {   // every thread's copies landed, then all of them are visible
         asm volatile("cp.async.wait_all;" ::: "memory");
         __syncthreads();
@@ -634,7 +641,7 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t*
     __syncthreads();
     const uint32_t n = sm.cand_count;
     const bool in_smem = n <= static_cast<uint32_t>(cand_cap);
-    // ---- low digits: bits [19:10], then [9:0], over both halves' threshold-bin keys
+    // ---- low digits: bits [19:10], then [9:0], over the cluster's threshold-bin keys
     uint32_t prefix = b1 << 20;
     for (int pass = 0; pass < 2; ++pass) {
         const int shift = pass == 0 ? 10 : 0;
@@ -652,7 +659,7 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t*
             }
         }
         __syncthreads();
-        sum_with_peer(h, total, 1024, peer);
+        sum_over_cluster<NC>(h, total, 1024, rank);
         select_bin(total, sm, 1024, need);
         prefix |= sm.sel_digit << shift;
         need = sm.sel_remaining;
@@ -677,7 +684,7 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t*
     }
     __syncthreads();
 
-    // ---- index-ordered output; the second half starts after the first half's kept keys
+    // ---- index-ordered output; each part starts after the kept keys of the parts before it
     const int wpt = (W + kTopkThreads - 1) / kTopkThreads;
     const int w0 = min(W, threadIdx.x * wpt), w1 = min(W, w0 + wpt);
     uint32_t gt_before = 0, eq_before = 0;
@@ -692,11 +699,11 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t*
         xcnt[1] = eq_tot;
     }
     __syncthreads();
-    cluster_sync();   // both halves' counts are visible
-    if (half == 1) {
-        const uint4 c = ld_rank_v4(xcnt, peer);
-        gt_before += c.x;
-        eq_before += c.y;
+    cluster_sync();   // every CTA's counts are visible
+    for (uint32_t c = 0; c < rank; ++c) {
+        const uint4 cc = ld_rank_v4(xcnt, c);
+        gt_before += cc.x;
+        eq_before += cc.y;
     }
     for (int w = w0; w < w1; ++w) {
         const uint32_t sw = sel[w], tw = tie[w];
@@ -718,7 +725,7 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t*
             }
         }
     }
-    cluster_sync();   // the peer has read this CTA's histograms and counts before either leaves
+    cluster_sync();   // every CTA has read this CTA's histograms and counts before any leaves
 }
 
 size_t cluster_smem_bytes(int words, int cand_cap, int row_cap) {
@@ -740,8 +747,8 @@ extern "C" size_t dsa_topk_workspace_size(int32_t rows, int32_t k, int32_t max_s
 
 namespace dsa {
 
-template <bool F, bool P>
-void* topk_cluster_fn() { return reinterpret_cast<void*>(topk_cluster_kernel<F, P>); }
+template <bool F, bool P, int NC>
+void* topk_cluster_fn() { return reinterpret_cast<void*>(topk_cluster_kernel<F, P, NC>); }
 template <bool F, bool P>
 void* topk_bitmap_fn() { return reinterpret_cast<void*>(topk_bitmap_kernel<F, P>); }
 
@@ -777,34 +784,43 @@ dsa_status topk_launch(const float* logits, int64_t ld, const int32_t* seq_lens,
     const bool pre = hist_g != nullptr;
     if (pre && words > dsa::kMaxBitmapWords) return DSA_ERR_UNSUPPORTED;
     if (words <= dsa::kMaxBitmapWords && max_seq_len >= 16384 && (row_end - row_begin) <= sms / 2) {
-        // long rows, fewer rows than SM pairs: each row on a 2-CTA cluster
-        const int half_keys = ((max_seq_len + 1) / 2 + 127) & ~127;
-        int words_cap = ((half_keys + 256 + 31) / 32 + 3) & ~3;
+        // long rows, fewer rows than SM pairs: each row on a cluster of ncta CTAs -- 4 when the
+        // clusters of all rows fit 128 SMs at once and every CTA keeps at least 4096 keys of the
+        // longest row, else 2 (8-CTA clusters measured slower: 16 rows of 128K keys 75 us
+        // against 61 us with 4)
+        const int rows = row_end - row_begin;
+        const int ncta = (rows * 4 <= 128 && max_seq_len >= 4 * 4096) ? 4 : 2;
+        const int part_keys = ((max_seq_len + ncta - 1) / ncta + 127) & ~127;
+        int words_cap = ((part_keys + 256 + 31) / 32 + 3) & ~3;
         if (words_cap < 32) words_cap = 32;
-        // with the histograms given: the half row in shared memory as well when it fits (the
-        // threshold-bin candidates then get 4096 slots instead of 8192; more fall back to rows)
+        // with the histograms given: each CTA's part of the row in shared memory as well when it
+        // fits (the threshold-bin candidates then get 4096 slots instead of 8192; more fall back to
+        // reading the row)
         int cand_cap = dsa::kCandidateCap, row_cap = 0;
         int smem_max = 0;
         if (cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
             return DSA_ERR_CUDA;
-        const int row_keys = (half_keys + 3) & ~3;
+        const int row_keys = (part_keys + 3) & ~3;
         if (pre && dsa::cluster_smem_bytes(words_cap, 4096, row_keys) <= static_cast<size_t>(smem_max)) {
             cand_cap = 4096;
             row_cap = row_keys;
         }
         const size_t smem = dsa::cluster_smem_bytes(words_cap, cand_cap, row_cap);
-        void* kern = forced ? (pre ? topk_cluster_fn<true, true>() : topk_cluster_fn<true, false>())
-                            : (pre ? topk_cluster_fn<false, true>() : topk_cluster_fn<false, false>());
+        void* kern = ncta == 4
+                         ? (forced ? (pre ? topk_cluster_fn<true, true, 4>() : topk_cluster_fn<true, false, 4>())
+                                   : (pre ? topk_cluster_fn<false, true, 4>() : topk_cluster_fn<false, false, 4>()))
+                         : (forced ? (pre ? topk_cluster_fn<true, true, 2>() : topk_cluster_fn<true, false, 2>())
+                                   : (pre ? topk_cluster_fn<false, true, 2>() : topk_cluster_fn<false, false, 2>()));
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
             cudaSuccess)
             return DSA_ERR_CUDA;
         cudaLaunchAttribute cattr[2];
         cattr[0].id = cudaLaunchAttributeClusterDimension;
-        cattr[0].val.clusterDim.x = 2;
+        cattr[0].val.clusterDim.x = static_cast<unsigned>(ncta);
         cattr[0].val.clusterDim.y = 1;
         cattr[0].val.clusterDim.z = 1;
         cattr[1] = attr[0];
-        cfg.gridDim = dim3(2, static_cast<unsigned>(row_end - row_begin), 1);
+        cfg.gridDim = dim3(static_cast<unsigned>(ncta), static_cast<unsigned>(rows), 1);
         cfg.attrs = cattr;
         cfg.numAttrs = 2;
         cfg.dynamicSmemBytes = smem;
