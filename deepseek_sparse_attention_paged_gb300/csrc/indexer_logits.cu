@@ -110,6 +110,9 @@ indexer_q_prologue_kernel(const uint16_t* __restrict__ q, const float* __restric
                           const int32_t* __restrict__ cu_q, int B, int row_begin, int row_end, int mode,
                           uint8_t* __restrict__ q_codes, float* __restrict__ q_gates, uint32_t* __restrict__ hist_zero) {
     ptx::griddep_launch_dependents();
+    // launched as a programmatic dependent of the previous kernel on the stream: its CTAs are
+    // resident early and start once that kernel has completed (nothing is read or written before)
+    ptx::griddep_wait();
     // the rows' top-12-bit histograms (one-call indexer) start at zero: block b clears words
     // 512 b .. 512 b + 511 (8 blocks per row, 4096 words per row).  The logits kernel adds into them
     // only after its query loads, which wait for this whole grid.
@@ -794,14 +797,23 @@ dsa_status indexer_logits_launch(const void* q_bf16, const float* weights, const
     uint8_t* q_codes = static_cast<uint8_t*>(workspace);
     float* q_gates = reinterpret_cast<float*>(q_codes + static_cast<size_t>(rows) * kQRowBytes);
 
-    // query prologue: 8 vectors per 256-thread block
-    indexer_q_prologue_kernel<<<static_cast<unsigned>(rows) * (kIndexHeads / 8), 256, 0, st>>>(
-        static_cast<const uint16_t*>(q_bf16), weights, cu_q, B, row_begin, row_end, mode, q_codes, q_gates, hist_g);
-    if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
-
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    // query prologue: 8 vectors per 256-thread block; a programmatic dependent of the previous kernel
+    // on the stream (it waits on the device for that kernel's completion before any access)
+    {
+        cudaLaunchConfig_t pcfg = {};
+        pcfg.gridDim = dim3(static_cast<unsigned>(rows) * (kIndexHeads / 8), 1, 1);
+        pcfg.blockDim = dim3(256, 1, 1);
+        pcfg.stream = st;
+        pcfg.attrs = attr;
+        pcfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&pcfg, indexer_q_prologue_kernel, static_cast<const uint16_t*>(q_bf16), weights, cu_q,
+                               static_cast<int>(B), static_cast<int>(row_begin), static_cast<int>(row_end), mode,
+                               q_codes, q_gates, hist_g) != cudaSuccess)
+            return DSA_ERR_CUDA;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ctas, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);

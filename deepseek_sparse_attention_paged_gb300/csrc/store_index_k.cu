@@ -16,6 +16,7 @@
 #include <cuda_fp8.h>
 
 #include "dsa_common.cuh"
+#include "sm100_ptx.cuh"
 
 namespace dsa {
 namespace {
@@ -85,6 +86,9 @@ __device__ __forceinline__ void rotate_quant_store(float (&x)[4], int lane, uint
 __global__ void __launch_bounds__(256)
 store_index_k_kernel(const uint16_t* __restrict__ keys, const int64_t* __restrict__ slots, int64_t n,
                      uint8_t* __restrict__ pool, int64_t num_pages, int32_t* err) {
+    // the next kernel on the stream may be scheduled (the indexer's query prologue waits on the device
+    // for this grid before it reads or writes anything)
+    ptx::griddep_launch_dependents();
     const int64_t token = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (token >= n) return;                      // warp-uniform
