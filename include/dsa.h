@@ -232,6 +232,9 @@ dsa_status dsa_indexer_rope_q(const void* q_raw_bf16, const float* cos_sin_cache
  *                keys' logits are not written).
  * Two kernels are enqueued on `stream`: the query prologue, then the logits kernel as its
  * programmatic dependent (it may start before the prologue ends and waits for it on the device).
+ * The prologue is itself a programmatic dependent of whatever kernel precedes it on the stream: it
+ * may be scheduled early but waits on the device for that kernel's completion before it reads or
+ * writes anything.
  */
 size_t dsa_indexer_logits_workspace_size(int32_t rows);
 dsa_status dsa_indexer_logits(const void* q_bf16, const float* weights, const uint8_t* index_k_pool,
