@@ -109,10 +109,12 @@ __global__ void __launch_bounds__(256)
 indexer_q_prologue_kernel(const uint16_t* __restrict__ q, const float* __restrict__ w,
                           const int32_t* __restrict__ cu_q, int B, int row_begin, int row_end, int mode,
                           uint8_t* __restrict__ q_codes, float* __restrict__ q_gates, uint32_t* __restrict__ hist_zero) {
-    ptx::griddep_launch_dependents();
     // launched as a programmatic dependent of the previous kernel on the stream: its CTAs are
-    // resident early and start once that kernel has completed (nothing is read or written before)
+    // resident early and start once that kernel has completed (nothing is read or written before).
+    // Only then may the logits kernel be scheduled: it reads key pages before its own wait, and the
+    // previous kernel may be the store writing them.
     ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     // the rows' top-12-bit histograms (one-call indexer) start at zero: block b clears words
     // 512 b .. 512 b + 511 (8 blocks per row, 4096 words per row).  The logits kernel adds into them
     // only after its query loads, which wait for this whole grid.
