@@ -238,3 +238,36 @@ def test_back_to_back_calls_keep_stream_order():
     torch.cuda.synchronize()
     assert torch.equal(idx_first, ref_idx)
     assert db.device_error() == (0, 0)
+
+
+def test_indexer_right_after_a_long_store_sees_the_stored_keys():
+    """The one-call indexer enqueued right after a store of every key of its rows (no sync): the
+    query prologue is a programmatic dependent of the store and the logits kernel streams key
+    pages before its own wait, so the prologue lets it start only after its wait on the store.
+    The store writes 240 K keys into a zeroed pool; the one-call indexer's logits are compared
+    with the oracle's.  (An end-to-end check of the order: a premature start would show only where
+    it overlapped the last pages written, which this timing does not force.)"""
+    from helpers import check_logits, oracle_pool
+    from deepseek_sparse_attention_paged_gb300.pipeline import lightning_logits_offset
+    wl = workloads.make_custom("store_then_index", 261, [60000, 59000, 61000, 58000], 1, topk=2048, heads=16)
+    db = DeviceBatch(wl, with_latent=False, build_index_cache=False)
+    keys = torch.from_numpy(np.ascontiguousarray(wl.index_keys()).view(np.int16)).cuda().view(torch.bfloat16)
+    slots = torch.from_numpy(wl.token_slots()).cuda()
+    ws = torch.empty(capi.dsa_lightning_indexer_workspace_size(wl.T, wl.max_seq_len), dtype=torch.uint8,
+                     device="cuda")
+    idx = torch.empty((wl.T, wl.topk), dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    capi.dsa_store_index_k(keys, slots, db.index_pool, db.dev_err)
+    capi.dsa_lightning_indexer(db.index_q, db.weights, db.index_pool, db.block_table, db.seq_lens, db.cu_q,
+                               wl.max_seq_len, wl.max_q_len, wl.topk, idx, ws, dev_err=db.dev_err)
+    torch.cuda.synchronize()
+    pool = oracle_pool(wl)
+    assert np.array_equal(db.index_pool.cpu().numpy(), pool)
+    rows = np.arange(wl.T)
+    ref, mag, bad = oracle.indexer_logits(wl.index_q(), wl.weights(), pool, wl.block_table, wl.seq_lens, wl.cu_q,
+                                          rows, db.ld, want_mag=True)
+    assert bad == 0
+    off = lightning_logits_offset(wl.T)
+    lg = ws[off:off + wl.T * db.ld * 4].view(torch.float32).view(wl.T, db.ld).cpu().numpy()
+    check_logits(lg, ref, mag, wl.visible_lens(), key="chain/store_then_index")
+    assert db.device_error() == (0, 0)
