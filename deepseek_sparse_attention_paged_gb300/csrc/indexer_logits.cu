@@ -181,14 +181,24 @@ struct Seg {
     int tile;     // current tile within the segment
 };
 
+constexpr int kSegTab = 8;   // segments of a CTA's share kept in shared memory
+
 struct SegArgs {
     const int32_t* seq_lens;
     const int32_t* cu_q;
     int B, G, R, row_begin, row_end;
     int shift;   // compressed keys: visible entries = visible tokens >> shift
+    // the first segments of this CTA's share (tab_base .. tab_base + tab_n - 1), read from shared
+    // memory instead of global memory during the stream
+    const Seg* tab;
+    int tab_base, tab_n;
 };
 
 __device__ __forceinline__ int seg_load(const SegArgs& a, int sidx, Seg& s) {
+    if (a.tab != nullptr && sidx >= a.tab_base && sidx < a.tab_base + a.tab_n) {
+        s = a.tab[sidx - a.tab_base];
+        return s.ntiles;
+    }
     s.sidx = sidx;
     s.ntiles = 0;
     const int b = sidx / a.G;
@@ -289,7 +299,8 @@ struct IdxCfg {
     // histogram barrier, and with C8 wfull / wempty per f16 tile
     static constexpr int kBars = 2 * kStages + 2 * kAcc + 4 + 1 + (C8 ? 4 : 0);
     static constexpr size_t kMiscOff = kBarOff + size_t(kBars) * 8;   // tmem slot, partition, scan
-    static constexpr size_t kPageOkOff = kMiscOff + 16 + 8 * 8;
+    static constexpr size_t kSegTabOff = kMiscOff + 16 + 8 * 8;   // [kSegTab] Seg + the count
+    static constexpr size_t kPageOkOff = kSegTabOff + kSegTab * sizeof(Seg) + 16;
     static constexpr size_t kHistOff = (kPageOkOff + 2 * kStages + 15) / 16 * 16;
     static constexpr size_t kHistBytes = HIST ? size_t(R) * kTopBins * 4 : 0;
     static constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kHistOff + kHistBytes;
@@ -338,11 +349,13 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + C::kMiscOff);
     int32_t* part = reinterpret_cast<int32_t*>(base + C::kMiscOff + 4);      // start segment, tile, count
     int64_t* scan_scratch = reinterpret_cast<int64_t*>(base + C::kMiscOff + 16);
+    Seg* segtab = reinterpret_cast<Seg*>(base + C::kSegTabOff);
+    int32_t* segtab_n = reinterpret_cast<int32_t*>(base + C::kSegTabOff + kSegTab * sizeof(Seg));
     uint8_t* page_ok = base + C::kPageOkOff;                                  // [S][2]
     uint32_t* hist_s = reinterpret_cast<uint32_t*>(base + C::kHistOff);       // HIST: [R][4096]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const SegArgs sa{seq_lens, cu_q, B, G, R, row_begin, row_end, cmp_shift};
+    const SegArgs sa{seq_lens, cu_q, B, G, R, row_begin, row_end, cmp_shift, nullptr, 0, 0};
     ptx::griddep_launch_dependents();   // the top-k kernel may be scheduled; it waits for this grid
     const int nseg = B * G;
 
@@ -395,7 +408,13 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
                 part[0] = t;
                 part[1] = static_cast<int32_t>(t0 - (incl - n));
             }
+            asm volatile("bar.sync 1, 256;" ::: "memory");   // the start segment is known
+            // the share's first segments into the table (each thread holds its own segment)
+            const int s0 = part[0];
+            if (t >= s0 && t < s0 + kSegTab && t < nseg) segtab[t - s0] = tmp;
+            if (t == 0) *segtab_n = s0 < nseg ? min(kSegTab, nseg - s0) : 0;
         } else {
+            if (t == 0) *segtab_n = 0;
             int64_t mine = 0;
             for (int sidx = t; sidx < nseg; sidx += 256) mine += seg_load(sa, sidx, tmp);
             int64_t total;
@@ -432,9 +451,10 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
     const int count = part[2];
     const uint64_t deadline = ptx::wait_deadline();
     bool timed_out = false;
+    const SegArgs sat{seq_lens, cu_q, B, G, R, row_begin, row_end, cmp_shift, segtab, part[0], *segtab_n};
     Seg sg;
     if (count > 0) {
-        seg_load(sa, part[0], sg);
+        seg_load(sat, part[0], sg);
         sg.tile = part[1];
     }
 
@@ -486,7 +506,7 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
             }
             if (__shfl_sync(0xffffffffu, timed_out ? 1 : 0, 0)) { timed_out = true; break; }
           }
-            if (++sg.tile == sg.ntiles && i + 1 < count) seg_next(sa, sg);
+            if (++sg.tile == sg.ntiles && i + 1 < count) seg_next(sat, sg);
         }
     } else if (warp == kLoaderWarp && count > 0) {   // ---------------- query-tile loader
         if (lane == 0) {
@@ -517,7 +537,7 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
                                    &qfull[qb]);
                 }
                 remaining -= sg.ntiles - sg.tile;
-                if (remaining > 0) seg_next(sa, sg);
+                if (remaining > 0) seg_next(sat, sg);
             }
         }
     } else if ((warp == 1 || (P == 2 && warp == kMma1Warp)) && count > 0) {   // ---------------- MMA issuer
@@ -574,7 +594,7 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
                     ptx::umma_commit(&qempty[qb]);
                     ++n;
                     seg_start = true;
-                    if (i + 1 < count) seg_next(sa, sg);
+                    if (i + 1 < count) seg_next(sat, sg);
                 }
             }
         }
@@ -700,7 +720,7 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
                 if (lane == 0) ptx::mbar_arrive(&qempty[qb]);
                 ++n;
                 seg_start = true;
-                if (i + 1 < count) seg_next(sa, sg);
+                if (i + 1 < count) seg_next(sat, sg);
             }
         }
     }
