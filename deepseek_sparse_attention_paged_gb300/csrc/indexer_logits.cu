@@ -388,26 +388,48 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
         ptx::tmem_relinquish();
     }
     if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 8) {
-        // this CTA's share of the tiles: total over all segments, then the segment holding t0
-        // (one scan when every segment has its own thread, else a total pass and a search pass)
+        // This CTA's share of the work.  A segment of n > 0 tiles weighs n + kSegCost: with the
+        // histogram, leaving a segment (both epilogue groups meet, flush the bins, meet again)
+        // costs about two tiles' time, without it next to nothing.  The CTAs take equal ranges
+        // [w0, w1) of the total weight, and a CTA's tiles are the tiles whose positions fall in its
+        // range (the first kSegCost positions of a segment hold none).  Scans carry
+        // (weight << 32) + tiles: one scan when every segment has its own thread, else a total pass
+        // and a search pass over chunks of 256 segments.
+        constexpr int kSegCost = HIST ? 2 : 0;
         const int t = threadIdx.x - kEpiWarp0 * 32;
         Seg tmp;
+        auto packed = [&](int n) -> int64_t {
+            return n > 0 ? ((static_cast<int64_t>(n) + kSegCost) << 32) + n : 0;
+        };
+        // (this thread's segment ends at packed prefix incl and holds n tiles) claim the share's
+        // first tile and add / subtract the tile positions of w1 and w0 into the count
+        auto claim = [&](int sidx, int n, int64_t incl, int64_t w0, int64_t w1) {
+            if (n <= 0) return;
+            const int64_t e = incl >> 32, s = e - (n + kSegCost);   // weight range [s, e)
+            const int64_t tiles_before = (incl & 0xffffffffLL) - n;
+            if (w1 > w0 && s <= w0 && w0 < e) {
+                const int64_t k = w0 - s > kSegCost ? w0 - s - kSegCost : 0;
+                part[0] = sidx;
+                part[1] = static_cast<int32_t>(k);
+                atomicSub(&part[2], static_cast<int32_t>(tiles_before + k));
+            }
+            if (w1 > w0 && s <= w1 && w1 < e)
+                atomicAdd(&part[2], static_cast<int32_t>(tiles_before + (w1 - s > kSegCost ? w1 - s - kSegCost : 0)));
+        };
         if (nseg <= 256) {
             const int n = (t < nseg) ? seg_load(sa, t, tmp) : 0;
             int64_t total;
-            const int64_t incl = epi_scan(n, scan_scratch, &total);
-            const int64_t t0 = total * blockIdx.x / gridDim.x;
-            const int64_t t1 = total * (blockIdx.x + 1) / gridDim.x;
+            const int64_t incl = epi_scan(packed(n), scan_scratch, &total);
+            const int64_t W = total >> 32;
+            const int64_t w0 = W * blockIdx.x / gridDim.x;
+            const int64_t w1 = W * (blockIdx.x + 1) / gridDim.x;
             if (t == 0) {
                 part[0] = nseg;
                 part[1] = 0;
-                part[2] = static_cast<int32_t>(t1 - t0);
+                part[2] = (w1 > w0 && w1 == W) ? static_cast<int32_t>(total & 0xffffffffLL) : 0;
             }
-            asm volatile("bar.sync 1, 256;" ::: "memory");   // the defaults above before the search result
-            if (t1 > t0 && n > 0 && incl - n <= t0 && t0 < incl) {
-                part[0] = t;
-                part[1] = static_cast<int32_t>(t0 - (incl - n));
-            }
+            asm volatile("bar.sync 1, 256;" ::: "memory");   // the defaults above before the claims
+            claim(t, n, incl, w0, w1);
             asm volatile("bar.sync 1, 256;" ::: "memory");   // the start segment is known
             // the share's first segments into the table (each thread holds its own segment)
             const int s0 = part[0];
@@ -416,28 +438,27 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
         } else {
             if (t == 0) *segtab_n = 0;
             int64_t mine = 0;
-            for (int sidx = t; sidx < nseg; sidx += 256) mine += seg_load(sa, sidx, tmp);
+            for (int sidx = t; sidx < nseg; sidx += 256) mine += packed(seg_load(sa, sidx, tmp));
             int64_t total;
             epi_scan(mine, scan_scratch, &total);
-            const int64_t t0 = total * blockIdx.x / gridDim.x;
-            const int64_t t1 = total * (blockIdx.x + 1) / gridDim.x;
+            const int64_t W = total >> 32;
+            const int64_t w0 = W * blockIdx.x / gridDim.x;
+            const int64_t w1 = W * (blockIdx.x + 1) / gridDim.x;
             if (t == 0) {
                 part[0] = nseg;
                 part[1] = 0;
-                part[2] = static_cast<int32_t>(t1 - t0);
+                part[2] = (w1 > w0 && w1 == W) ? static_cast<int32_t>(total & 0xffffffffLL) : 0;
             }
-            if (t1 > t0) {
-                int64_t seen = 0;
+            asm volatile("bar.sync 1, 256;" ::: "memory");   // the defaults above before the claims
+            if (w1 > w0) {
+                int64_t seen = 0;   // packed sum over the chunks before
                 for (int c0 = 0; c0 < nseg; c0 += 256) {
                     const int n = (c0 + t < nseg) ? seg_load(sa, c0 + t, tmp) : 0;
                     int64_t chunk_total;
-                    const int64_t incl = epi_scan(n, scan_scratch, &chunk_total) + seen;
-                    if (n > 0 && incl - n <= t0 && t0 < incl) {
-                        part[0] = c0 + t;
-                        part[1] = static_cast<int32_t>(t0 - (incl - n));
-                    }
+                    const int64_t incl = epi_scan(packed(n), scan_scratch, &chunk_total) + seen;
+                    claim(c0 + t, n, incl, w0, w1);
                     seen += chunk_total;
-                    if (seen > t0) break;
+                    if ((seen >> 32) > w1) break;
                 }
             }
         }
