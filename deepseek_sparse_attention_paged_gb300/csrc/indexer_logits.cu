@@ -108,11 +108,20 @@ constexpr int kWTileBytes = kTileKeys * kIndexDim * 2;    // c8: 32 KB, one key 
 __global__ void __launch_bounds__(256)
 indexer_q_prologue_kernel(const uint16_t* __restrict__ q, const float* __restrict__ w,
                           const int32_t* __restrict__ cu_q, int B, int row_begin, int row_end, int mode,
-                          uint8_t* __restrict__ q_codes, float* __restrict__ q_gates, uint32_t* __restrict__ hist_zero) {
+                          uint8_t* __restrict__ q_codes, float* __restrict__ q_gates, uint32_t* __restrict__ hist_zero,
+                          const int32_t* __restrict__ seq_lens) {
+    // Before anything else, L2 prefetches of what every CTA of the logits kernel reads in its setup:
+    // the row offsets and the lengths (inputs that no kernel of the step writes; a prefetch changes
+    // no memory, so it may overlap the previous kernel).
+    {
+        const int64_t gt = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
+        if (gt < (B + 32) / 32) ptx::prefetch_l2(cu_q + gt * 32);
+        if (gt < (B + 31) / 32) ptx::prefetch_l2(seq_lens + gt * 32);
+    }
     // launched as a programmatic dependent of the previous kernel on the stream: its CTAs are
-    // resident early and start once that kernel has completed (nothing is read or written before).
-    // Only then may the logits kernel be scheduled: it reads key pages before its own wait, and the
-    // previous kernel may be the store writing them.
+    // resident early and start once that kernel has completed (nothing else is read or written
+    // before).  Only then may the logits kernel be scheduled: it reads key pages before its own
+    // wait, and the previous kernel may be the store writing them.
     ptx::griddep_wait();
     ptx::griddep_launch_dependents();
     // the rows' top-12-bit histograms (one-call indexer) start at zero: block b clears words
@@ -357,6 +366,14 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const SegArgs sa{seq_lens, cu_q, B, G, R, row_begin, row_end, cmp_shift, nullptr, 0, 0};
     ptx::griddep_launch_dependents();   // the top-k kernel may be scheduled; it waits for this grid
+    if (warp == kLoaderWarp) {
+        // while the other warps set up: L2 prefetch of this CTA's slice of the block table (of its
+        // first 8 MB), which the producers read right after the setup
+        const int64_t bytes = static_cast<int64_t>(B) * max_pages * 4;
+        const int64_t lines = (bytes < (int64_t(8) << 20) ? bytes : (int64_t(8) << 20)) / 128;
+        const int64_t l1 = lines * (blockIdx.x + 1) / gridDim.x;
+        for (int64_t l = lines * blockIdx.x / gridDim.x + lane; l < l1; l += 32) ptx::prefetch_l2(block_table + l * 32);
+    }
     const int nseg = B * G;
 
     if (threadIdx.x == 0) {
@@ -844,7 +861,8 @@ dsa_status indexer_logits_launch(const void* q_bf16, const float* weights, const
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     // query prologue: 8 vectors per 256-thread block; a programmatic dependent of the previous kernel
-    // on the stream (it waits on the device for that kernel's completion before any access)
+    // on the stream (it waits on the device for that kernel's completion before any access but its
+    // L2 prefetches of the lengths and row offsets)
     {
         cudaLaunchConfig_t pcfg = {};
         pcfg.gridDim = dim3(static_cast<unsigned>(rows) * (kIndexHeads / 8), 1, 1);
@@ -854,7 +872,7 @@ dsa_status indexer_logits_launch(const void* q_bf16, const float* weights, const
         pcfg.numAttrs = 1;
         if (cudaLaunchKernelEx(&pcfg, indexer_q_prologue_kernel, static_cast<const uint16_t*>(q_bf16), weights, cu_q,
                                static_cast<int>(B), static_cast<int>(row_begin), static_cast<int>(row_end), mode,
-                               q_codes, q_gates, hist_g) != cudaSuccess)
+                               q_codes, q_gates, hist_g, seq_lens) != cudaSuccess)
             return DSA_ERR_CUDA;
     }
     cudaLaunchConfig_t cfg = {};
