@@ -488,6 +488,14 @@ __device__ __forceinline__ uint4 ld_rank_v4(const uint32_t* p, uint32_t rank) {
     return v;
 }
 
+// The 4 bytes at the same shared-memory offset as `p` in CTA `rank`.
+__device__ __forceinline__ uint32_t ld_rank_u32(const uint32_t* p, uint32_t rank) {
+    uint32_t a, v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(ptx::smem_addr(p)), "r"(rank));
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+    return v;
+}
+
 // total[b] = the sum over the cluster's CTAs of their hist[b], b < bins (a multiple of 4).  Every
 // CTA's histogram is complete on entry.  A histogram buffer is never written again after it has
 // been summed, and the kernel ends with a cluster barrier, so no barrier is needed after the reads.
@@ -643,7 +651,58 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t*
     const bool in_smem = n <= static_cast<uint32_t>(cand_cap);
     // ---- low digits: bits [19:10], then [9:0], over the cluster's threshold-bin keys
     uint32_t prefix = b1 << 20;
-    for (int pass = 0; pass < 2; ++pass) {
+    // When every CTA's candidates are in its shared memory and together fit 4096 keys, each CTA
+    // copies all of them (its peers' by distributed shared-memory loads) into `total` (free once
+    // the threshold bin is known) and finds both digits alone: one cluster barrier instead of one
+    // per digit with the digit histograms summed across the cluster.  Every CTA sees the same
+    // counts, so all take the same branch.
+    cluster_sync();   // every CTA's candidates and count are complete and visible
+    uint32_t coff[NC];
+    uint32_t ntot = 0;
+    bool all_in = true;
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        const uint32_t nc = static_cast<uint32_t>(c) == rank ? n : ld_rank_u32(&sm.cand_count, c);
+        coff[c] = ntot;
+        ntot += nc;
+        all_in = all_in && nc <= static_cast<uint32_t>(cand_cap);
+    }
+    const bool gathered = all_in && ntot <= static_cast<uint32_t>(kTopBins);
+    if (gathered) {
+        uint32_t* ukey = total;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            const uint32_t nc = (c + 1 < NC ? coff[c + 1] : ntot) - coff[c];
+            if (static_cast<uint32_t>(c) == rank) {
+                for (uint32_t i = threadIdx.x; i < nc; i += kTopkThreads) ukey[coff[c] + i] = ckey[i];
+            } else {   // 16-byte loads (ckey is 16-byte aligned and cand_cap a multiple of 4)
+                for (uint32_t q = threadIdx.x; 4 * q < nc; q += kTopkThreads) {
+                    const uint4 v4 = ld_rank_v4(ckey + 4 * q, c);
+                    const uint32_t i = 4 * q;
+                    ukey[coff[c] + i] = v4.x;
+                    if (i + 1 < nc) ukey[coff[c] + i + 1] = v4.y;
+                    if (i + 2 < nc) ukey[coff[c] + i + 2] = v4.z;
+                    if (i + 3 < nc) ukey[coff[c] + i + 3] = v4.w;
+                }
+            }
+        }
+        __syncthreads();
+        for (int pass = 0; pass < 2; ++pass) {
+            const int shift = pass == 0 ? 10 : 0;
+            const int hi = shift + 10;
+            uint32_t* h = lo_hist + pass * 1024;
+            for (uint32_t i = threadIdx.x; i < ntot; i += kTopkThreads) {
+                const uint32_t key = ukey[i];
+                if ((key >> hi) == (prefix >> hi)) atomicAdd(&h[(key >> shift) & 1023u], 1u);
+            }
+            __syncthreads();
+            select_bin(h, sm, 1024, need);
+            prefix |= sm.sel_digit << shift;
+            need = sm.sel_remaining;
+            __syncthreads();
+        }
+    }
+    for (int pass = 0; pass < 2 && !gathered; ++pass) {
         const int shift = pass == 0 ? 10 : 0;
         const int hi = shift + 10;
         uint32_t* h = lo_hist + pass * 1024;
