@@ -100,6 +100,9 @@ constexpr int kMma1Warp = 12;                             // two pipelines: MMA 
 constexpr int kQRowBytesC8 = kIndexHeads * kIndexDim * 2; // c8: 16 KB of f16 query codes per row
 constexpr int kWTileBytes = kTileKeys * kIndexDim * 2;    // c8: 32 KB, one key tile widened to f16
 
+// Bring the 128-byte line holding p into L2 (no register result, no memory change).
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+
 // ---------------------------------------------------------------------------------------------
 // Query prologue: one warp per (row, head) vector.  Writes the 128 codes of the vector into the
 // row's 8 KB block of the workspace at the position the 128-byte swizzle gives B-operand row
@@ -115,8 +118,8 @@ indexer_q_prologue_kernel(const uint16_t* __restrict__ q, const float* __restric
     // no memory, so it may overlap the previous kernel).
     {
         const int64_t gt = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
-        if (gt < (B + 32) / 32) ptx::prefetch_l2(cu_q + gt * 32);
-        if (gt < (B + 31) / 32) ptx::prefetch_l2(seq_lens + gt * 32);
+        if (gt < (B + 32) / 32) prefetch_l2(cu_q + gt * 32);
+        if (gt < (B + 31) / 32) prefetch_l2(seq_lens + gt * 32);
     }
     // launched as a programmatic dependent of the previous kernel on the stream: its CTAs are
     // resident early and start once that kernel has completed (nothing else is read or written
@@ -372,7 +375,7 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
         const int64_t bytes = static_cast<int64_t>(B) * max_pages * 4;
         const int64_t lines = (bytes < (int64_t(8) << 20) ? bytes : (int64_t(8) << 20)) / 128;
         const int64_t l1 = lines * (blockIdx.x + 1) / gridDim.x;
-        for (int64_t l = lines * blockIdx.x / gridDim.x + lane; l < l1; l += 32) ptx::prefetch_l2(block_table + l * 32);
+        for (int64_t l = lines * blockIdx.x / gridDim.x + lane; l < l1; l += 32) prefetch_l2(block_table + l * 32);
     }
     const int nseg = B * G;
 

@@ -20,10 +20,6 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
 // has completed and its memory is visible; it is a no-op for a normally launched grid); the
 // previous grid calls griddep_launch_dependents() to let the dependent grid be scheduled.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-// Bring the 128-byte line holding p into L2 (no register result, no memory change).
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
 __device__ __forceinline__ void griddep_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
