@@ -519,6 +519,10 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
             const int32_t pg0 = __shfl_sync(0xffffffffu, win, 2 * (sg.tile - wb));
             const int32_t pg1 = __shfl_sync(0xffffffffu, win, 2 * (sg.tile - wb) + 1);
             if (lane == 0) {
+                // (without the histograms) the rest of the ring after each pipeline's first tile goes
+                // out 0.4 us later, so that the first tiles of all CTAs are served ahead of the
+                // start-up burst (~25 MB): the CTAs then start together instead of up to ~2 us apart
+                if (!HIST && i == P + pipe) __nanosleep(400);
                 if (!ptx::mbar_wait(&empty[s], ph ^ 1u, deadline)) timed_out = true;
                 if (!timed_out) {
                     const bool need1 = sg.tile * kTileKeys + kPage < sg.vmax;
