@@ -114,6 +114,14 @@ def test_logits_many_requests_shares_split_inside_requests():
     _logits_case(workloads.make_custom("many", 108, lens, 1, topk=64, heads=16))
 
 
+def test_logits_shares_spanning_many_short_segments():
+    # 200 one-tile requests, then 56 long ones (256 segments): the CTAs holding the short requests
+    # each span ~18 segments, more than the first ones they keep in shared memory
+    rng = np.random.default_rng(109)
+    lens = rng.integers(1, 129, size=200).tolist() + rng.integers(5000, 6001, size=56).tolist()
+    _logits_case(workloads.make_custom("segments", 109, lens, 1, topk=64, heads=16))
+
+
 def test_logits_rotate_q_flag():
     _logits_case(workloads.make("tiny"), flags=capi.DSA_Q_ROTATE)
 

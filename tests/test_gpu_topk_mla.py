@@ -198,12 +198,16 @@ def _li_case(name):
     if name == "cluster":   # long rows, few of them: the 2-CTA cluster top-k; row groups of 2
         return workloads.make_custom("li_oracle", 241, [500, 64, 3000, 17000, 40000, 70000], [1, 2, 3, 1, 1, 2],
                                      topk=256, heads=16)
+    if name == "segments":   # 200 one-tile requests then 56 long ones: shares spanning many segments
+        rng = np.random.default_rng(243)
+        lens = rng.integers(1, 129, size=200).tolist() + rng.integers(5000, 6001, size=56).tolist()
+        return workloads.make_custom("li_oracle_s", 243, lens, 1, topk=512, heads=16)
     rng = np.random.default_rng(242)   # many short rows: the one-CTA bitmap top-k
     lens = rng.integers(100, 12000, 90).tolist()
     return workloads.make_custom("li_oracle_b", 242, lens, rng.integers(1, 3, 90).tolist(), topk=512, heads=16)
 
 
-@pytest.mark.parametrize("case", ["cluster", "bitmap"])
+@pytest.mark.parametrize("case", ["cluster", "bitmap", "segments"])
 def test_lightning_indexer_matches_oracle(case):
     """The one-call indexer (histogram-fused: both cases have row groups of at most 2 rows) against
     the oracle: oracle.topk_forced on the oracle's logits, exactly wherever the k-th / (k+1)-th gap
