@@ -114,8 +114,8 @@ indexer_q_prologue_kernel(const uint16_t* __restrict__ q, const float* __restric
                           uint8_t* __restrict__ q_codes, float* __restrict__ q_gates, uint32_t* __restrict__ hist_zero,
                           const int32_t* __restrict__ seq_lens) {
     // Before anything else, L2 prefetches of what every CTA of the logits kernel reads in its setup:
-    // the row offsets and the lengths (inputs that no kernel of the step writes; a prefetch changes
-    // no memory, so it may overlap the previous kernel).
+    // the row offsets and the lengths.  A prefetch changes no memory and fills only L2, where any
+    // later write of the previous kernel lands as well, so it may overlap that kernel.
     {
         const int64_t gt = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
         if (gt < (B + 32) / 32) prefetch_l2(cu_q + gt * 32);
