@@ -40,7 +40,9 @@ struct ProjCfg {
     static constexpr int kStageBytes = kAChunkBytes + kBChunkBytes;
     static constexpr int kStages = kRingBytes / kStageBytes < kMaxStages ? kRingBytes / kStageBytes : kMaxStages;
     static constexpr uint32_t kTmemCols = 2 * TN < 32 ? 32 : 2 * TN;   // two accumulators
-    static constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStageBytes + 256;
+    // up to 64 rows: one item's output tile as bf16 in shared memory, written out as 16-byte rows
+    static constexpr int kOutBytes = TN <= 64 ? TN * kMTile * 2 : 0;
+    static constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStageBytes + kOutBytes + 256;
     static_assert(kStages >= 2, "ring");
     static_assert(kTmemCols <= 512, "tensor memory");
 };
@@ -88,12 +90,13 @@ __device__ __forceinline__ Item item_of(int i, int heads, int mtiles) {
 template <int TN>
 __global__ void __launch_bounds__(kProjThreads, 1)
 mla_proj_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap, int heads, int K,
-                int M, int T, uint16_t* __restrict__ y, int64_t sy_t, int64_t sy_n, int32_t* err) {
+                int M, int T, uint16_t* __restrict__ y, int64_t sy_t, int64_t sy_n, int vec, int32_t* err) {
     using C = ProjCfg<TN>;
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw_addr = ptx::smem_addr(smem_raw);
     unsigned char* base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-    ProjBars& bar = *reinterpret_cast<ProjBars*>(base + C::kStages * C::kStageBytes);
+    uint16_t* out_s = reinterpret_cast<uint16_t*>(base + C::kStages * C::kStageBytes);   // [TN][128] bf16
+    ProjBars& bar = *reinterpret_cast<ProjBars*>(base + C::kStages * C::kStageBytes + C::kOutBytes);
     const uint32_t ring = ptx::smem_addr(base);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -185,10 +188,45 @@ mla_proj_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant_
         for (int i = blockIdx.x; i < items; i += gridDim.x, ++local) {
             const Item it = item_of(i, heads, mtiles);
             const int a = local & 1;
-            if (!ptx::mbar_wait(&bar.acc_full[a], (local >> 1) & 1, deadline)) { timed_out = true; break; }
-            ptx::tc_fence_after_sync();
+            // the same answer for the whole warp (a deadline could fall between its lanes' checks)
+            const bool got = __all_sync(0xffffffffu, ptx::mbar_wait(&bar.acc_full[a], (local >> 1) & 1, deadline));
             const int m = it.mt * kMTile + quad * 32 + lane;
             const int t0 = it.tt * TN;
+            if (C::kOutBytes > 0 && vec) {
+                // the tile through shared memory: thread (dim quad * 32 + lane) writes its column of
+                // bf16 values and the accumulator is released; once the four warps have met (and
+                // leave together if any wait ran out), 16 threads per row store its 256 bytes as
+                // 16-byte pieces
+                if (got) {
+                    ptx::tc_fence_after_sync();
+#pragma unroll 1
+                    for (int c0 = 0; c0 < TN; c0 += 32) {
+                        uint32_t r[32];
+                        ptx::tmem_ld_32x32b_x32(tmem + lane_base + static_cast<uint32_t>(a * TN + c0), r);
+                        ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            out_s[(c0 + j) * kMTile + quad * 32 + lane] = to_bf16_bits(__uint_as_float(r[j]));
+                    }
+                    ptx::tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(&bar.acc_empty[a]);
+                }
+                uint32_t any_late;
+                asm volatile("{\n\t.reg .pred q, p;\n\tsetp.eq.u32 q, %1, 0;\n\tbar.red.or.pred p, 2, 128, q;\n\t"
+                             "selp.u32 %0, 1, 0, p;\n\t}"
+                             : "=r"(any_late) : "r"(got ? 1u : 0u) : "memory");
+                if (any_late) { timed_out = true; break; }
+                const int e = threadIdx.x - 64;   // 0 .. 127
+                uint16_t* yrow = y + static_cast<int64_t>(it.n) * sy_n + it.mt * kMTile + (e & 15) * 8;
+                for (int rr = e >> 4; rr < TN && t0 + rr < T; rr += 8)
+                    *reinterpret_cast<uint4*>(yrow + static_cast<int64_t>(t0 + rr) * sy_t) =
+                        *reinterpret_cast<const uint4*>(out_s + rr * kMTile + (e & 15) * 8);
+                asm volatile("bar.sync 2, 128;" ::: "memory");   // read before the next item writes it
+                continue;
+            }
+            if (!got) { timed_out = true; break; }
+            ptx::tc_fence_after_sync();
             uint16_t* yb = y + static_cast<int64_t>(it.n) * sy_n + m;
 #pragma unroll 1
             for (int c0 = 0; c0 < TN; c0 += 32) {
@@ -399,7 +437,8 @@ dsa_status launch_proj(const void* x, int64_t sx_t, int64_t sx_n, const void* w,
     auto encode = proj_tensor_map_encoder();
     if (encode == nullptr) return DSA_ERR_CUDA;
     // row orientation (16-byte row stores) from 65 rows on, when the output allows vector stores
-    const bool rows = T > 64 && aligned16(y) && (sy_t % 8) == 0 && (sy_n % 8) == 0;
+    const bool vec = aligned16(y) && (sy_t % 8) == 0 && (sy_n % 8) == 0;   // 16-byte output rows
+    const bool rows = T > 64 && vec;
     const int NT = M >= 256 ? 256 : 128;   // output dims per row-orientation item
     const int TN = rows ? 128 : (T <= 64 ? 64 : (T <= 128 ? 128 : 256));
     CUtensorMap wmap, xmap;
@@ -456,7 +495,7 @@ dsa_status launch_proj(const void* x, int64_t sx_t, int64_t sx_n, const void* w,
                                  static_cast<int>(smem)) != cudaSuccess)                                       \
             return DSA_ERR_CUDA;                                                                               \
         mla_proj_kernel<TNV><<<ctas, kProjThreads, smem, stream>>>(wmap, xmap, heads, K, M, T, yb, sy_t, sy_n, \
-                                                                   dev_err);                                   \
+                                                                   vec ? 1 : 0, dev_err);                      \
     } while (0)
     if (TN == 64) DSA_LAUNCH_PROJ(64);
     else if (TN == 128) DSA_LAUNCH_PROJ(128);

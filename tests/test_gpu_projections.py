@@ -93,6 +93,20 @@ def test_absorb_attention_v_up_chain():
     assert np.all(np.abs(got - _val(ref)) <= bound)
 
 
+@pytest.mark.parametrize("T", [64, 5])
+def test_v_up_into_output_rows_without_16_byte_strides(T):
+    # head stride 130 elements: the 16-byte row stores do not apply, each value is stored alone
+    H = 8
+    g = torch.Generator().manual_seed(720 + T)
+    o = torch.randn(T, H, 512, generator=g).to(torch.bfloat16).cuda()
+    w = (torch.randn(H, 512, 128, generator=g) / math.sqrt(512)).to(torch.bfloat16).cuda()
+    out = torch.full((T, H, 130), 3.0, dtype=torch.bfloat16, device="cuda")
+    capi.dsa_mla_v_up(o, w, out[..., :128])
+    ref, mag = oracle.mla_v_up(_bits(o), _bits(w), want_mag=True)
+    _check(_bits(out[..., :128]), ref, mag)
+    assert bool((out[..., 128:] == 3.0).all())
+
+
 def test_bad_strides_are_rejected():
     q = torch.zeros(4, 2, 132, dtype=torch.bfloat16, device="cuda")               # head stride 132: not 16-byte
     w = torch.zeros(2, 128, 512, dtype=torch.bfloat16, device="cuda")
