@@ -100,6 +100,13 @@ constexpr int kMma1Warp = 12;                             // two pipelines: MMA 
 constexpr int kQRowBytesC8 = kIndexHeads * kIndexDim * 2; // c8: 16 KB of f16 query codes per row
 constexpr int kWTileBytes = kTileKeys * kIndexDim * 2;    // c8: 32 KB, one key tile widened to f16
 
+// acc2 += gates2 * (ReLU(x0), ReLU(x1)) on two fp32 lanes at once (packed FMA, round to nearest)
+__device__ __forceinline__ void fma2_relu(uint64_t& acc2, uint64_t gates2, uint32_t x0, uint32_t x1) {
+    uint64_t x2;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x2) : "f"(fmaxf(__uint_as_float(x0), 0.0f)), "f"(fmaxf(__uint_as_float(x1), 0.0f)));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2) : "l"(gates2), "l"(x2));
+}
+
 // Bring the 128-byte line holding p into L2 (no register result, no memory change).
 __device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 
@@ -710,10 +717,27 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
                     ptx::tmem_wait_ld();
                     const float* g = gates + (qb * R + jj) * kIndexHeads;
                     float acc = 0.0f;
+                    if constexpr (R == 4) {
+                        // four-row groups (prefill, where the epilogue's issue rate bounds the kernel):
+                        // the head sum as two interleaved partial sums (even / odd heads) with packed
+                        // two-lane FMAs, added at the end
+                        uint64_t acc2 = 0;   // the bit pattern of (0.0f, 0.0f)
+                        const uint64_t* g2 = reinterpret_cast<const uint64_t*>(g);
 #pragma unroll
-                    for (int h = 0; h < 32; ++h) acc = fmaf(g[h], fmaxf(__uint_as_float(r0[h]), 0.0f), acc);
+                        for (int h = 0; h < 32; h += 2)
+                            fma2_relu(acc2, g2[h / 2], r0[h], r0[h + 1]);
 #pragma unroll
-                    for (int h = 0; h < 32; ++h) acc = fmaf(g[32 + h], fmaxf(__uint_as_float(r1[h]), 0.0f), acc);
+                        for (int h = 0; h < 32; h += 2)
+                            fma2_relu(acc2, g2[16 + h / 2], r1[h], r1[h + 1]);
+                        float lo, hi;
+                        asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(acc2));
+                        acc = lo + hi;
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < 32; ++h) acc = fmaf(g[h], fmaxf(__uint_as_float(r0[h]), 0.0f), acc);
+#pragma unroll
+                        for (int h = 0; h < 32; ++h) acc = fmaf(g[32 + h], fmaxf(__uint_as_float(r1[h]), 0.0f), acc);
+                    }
                     const int r = sg.q0 + sg.j0 + jj;
                     const int v = visible_len(sg.L, sg.q_len, sg.j0 + jj) >> cmp_shift;
                     if (HIST) {
