@@ -717,10 +717,11 @@ indexer_logits_umma_kernel(const __grid_constant__ CUtensorMap kmap, const uint8
                     ptx::tmem_wait_ld();
                     const float* g = gates + (qb * R + jj) * kIndexHeads;
                     float acc = 0.0f;
-                    if constexpr (R == 4) {
-                        // four-row groups (prefill, where the epilogue's issue rate bounds the kernel):
+                    if constexpr (!C8) {
                         // the head sum as two interleaved partial sums (even / odd heads) with packed
-                        // two-lane FMAs, added at the end
+                        // two-lane FMAs, added at the end: half the FMA instructions of the epilogue
+                        // (with int8 keys, where the widen warps share the issue slots, it measured
+                        // no better and keeps one sum in head order)
                         uint64_t acc2 = 0;   // the bit pattern of (0.0f, 0.0f)
                         const uint64_t* g2 = reinterpret_cast<const uint64_t*>(g);
 #pragma unroll
