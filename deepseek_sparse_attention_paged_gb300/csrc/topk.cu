@@ -293,13 +293,16 @@ __global__ void __launch_bounds__(kTopkThreads)
 topk_bitmap_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* __restrict__ seq_lens,
                    const int32_t* __restrict__ cu_q, int B, int row_begin, int k, int n_init, int n_local, int cmp_shift,
                    int32_t* __restrict__ idx,
-                   int words_cap, const uint32_t* __restrict__ hist_g) {
+                   int words_cap, const uint32_t* __restrict__ hist_g, int row_cap) {
     extern __shared__ __align__(16) unsigned char dsm[];
     BitmapSmem& sm = *reinterpret_cast<BitmapSmem*>(dsm);
     uint32_t* sel = reinterpret_cast<uint32_t*>(dsm + sizeof(BitmapSmem));   // key > k-th: kept
     uint32_t* tie = sel + words_cap;                                         // key == k-th
     uint32_t* ckey = tie + words_cap;
     int32_t* cidx = reinterpret_cast<int32_t*>(ckey + kCandidateCap);
+    // with the histograms given (PREHIST) and row_cap > 0: a copy of the row, fetched while the
+    // threshold bin is found (16-byte aligned: words_cap is then a multiple of 4 words)
+    float* rowbuf = reinterpret_cast<float*>(cidx + kCandidateCap);
 
     // launched as a programmatic dependent of the logits kernel: the row's request is looked up in
     // the inputs (not written by that kernel) while it finishes, the logits are read after the wait
@@ -346,9 +349,22 @@ topk_bitmap_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* 
         for (int s = 4 * v4 + threadIdx.x; s < v; s += kTopkThreads) fn(s, F(s, order_key(__ldg(row + s))));
     };
 
+    // PREHIST: the row into shared memory (16-byte copies by every thread, issued right after the
+    // histogram's loads and in flight while the threshold bin is found): its whole 16-byte groups,
+    // so nothing at or past the visible length is read; the last < 4 keys come from global memory
+    const bool use_row = PREHIST && vec && row_cap > 0 && v <= row_cap;
+    auto copy_row = [&] {
+        if (!use_row) return;
+        const uint32_t dst0 = ptx::smem_addr(rowbuf);
+        const float4* src4 = reinterpret_cast<const float4*>(row);
+        for (int i = threadIdx.x; i < v4; i += kTopkThreads)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst0 + 16u * i), "l"(src4 + i) : "memory");
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+
     // ---- read 1: top-12-bit histogram (given by the logits kernel in the fused call)
     if (PREHIST) {
-        load_row_histogram<FORCED>(sm.hist, hist_g + static_cast<int64_t>(rl) * kTopBins, row, F, v, [] {});
+        load_row_histogram<FORCED>(sm.hist, hist_g + static_cast<int64_t>(rl) * kTopBins, row, F, v, copy_row);
     } else {
         for (int i = threadIdx.x; i < kTopBins; i += kTopkThreads) sm.hist[i] = 0;
         __syncthreads();
@@ -362,8 +378,9 @@ topk_bitmap_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* 
     // ---- read 2: mark keys above the threshold bin, collect the threshold bin
     for (int w = threadIdx.x; w < W; w += kTopkThreads) sel[w] = tie[w] = 0u;
     if (threadIdx.x == 0) sm.cand_count = 0;
-    __syncthreads();
-    for_each_key([&](int s, uint32_t key) {
+    if (use_row) asm volatile("cp.async.wait_all;" ::: "memory");   // this thread's copies landed
+    __syncthreads();   // (and with them every thread's)
+    auto mark = [&](int s, uint32_t key) {
         const uint32_t bin = key >> 20;
         if (bin > b1) {
             atomicOr(&sel[s >> 5], 1u << (s & 31));
@@ -374,7 +391,18 @@ topk_bitmap_kernel(const float* __restrict__ logits, int64_t ld, const int32_t* 
                 cidx[p] = s;
             }
         }
-    });
+    };
+    if (use_row) {
+        const float4* r4 = reinterpret_cast<const float4*>(rowbuf);
+        for (int i = threadIdx.x; i < v4; i += kTopkThreads) {
+            const float4 a = r4[i];
+            mark(4 * i, F(4 * i, order_key(a.x))); mark(4 * i + 1, F(4 * i + 1, order_key(a.y)));
+            mark(4 * i + 2, F(4 * i + 2, order_key(a.z))); mark(4 * i + 3, F(4 * i + 3, order_key(a.w)));
+        }
+        for (int s = 4 * v4 + threadIdx.x; s < v; s += kTopkThreads) mark(s, F(s, order_key(__ldg(row + s))));
+    } else {
+        for_each_key(mark);
+    }
     __syncthreads();
     const uint32_t n = sm.cand_count;
     const bool in_smem = n <= static_cast<uint32_t>(kCandidateCap);
@@ -571,14 +599,15 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t*
     const bool vec = (reinterpret_cast<uintptr_t>(part) & 15u) == 0;
     const int v4 = vec ? (nloc >> 2) : 0;
     // PREHIST: this part of the row into shared memory (16-byte copies by every thread, issued right
-    // after the histogram's loads and in flight while the threshold bin is found; the bytes read
-    // stay inside the row: lo and ld are multiples of 4)
+    // after the histogram's loads and in flight while the threshold bin is found): its whole 16-byte
+    // groups, so nothing at or past the row's visible length is read; the last < 4 keys are read
+    // from global memory in the pass over the keys
     const bool use_row = PREHIST && vec && row_cap > 0 && nloc <= row_cap;
     auto copy_row = [&] {
         if (!use_row) return;
         const uint32_t dst0 = ptx::smem_addr(rowbuf);
         const float4* src4 = reinterpret_cast<const float4*>(part);
-        for (int i = threadIdx.x; i < (nloc + 3) >> 2; i += kTopkThreads)
+        for (int i = threadIdx.x; i < v4; i += kTopkThreads)
             asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst0 + 16u * i), "l"(src4 + i) : "memory");
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
@@ -642,7 +671,7 @@ topk_cluster_kernel(const float* __restrict__ logits, int64_t ld, const int32_t*
             mark(4 * i, F(4 * i, order_key(a.x))); mark(4 * i + 1, F(4 * i + 1, order_key(a.y)));
             mark(4 * i + 2, F(4 * i + 2, order_key(a.z))); mark(4 * i + 3, F(4 * i + 3, order_key(a.w)));
         }
-        for (int s = 4 * v4 + threadIdx.x; s < nloc; s += kTopkThreads) mark(s, F(s, order_key(rowbuf[s])));
+        for (int s = 4 * v4 + threadIdx.x; s < nloc; s += kTopkThreads) mark(s, F(s, order_key(__ldg(part + s))));
     } else {
         for_each_key(mark);
     }
@@ -889,8 +918,21 @@ dsa_status topk_launch(const float* logits, int64_t ld, const int32_t* seq_lens,
                         &cand_cap, &row_cap};
         if (cudaLaunchKernelExC(&cfg, kern, args) != cudaSuccess) return DSA_ERR_CUDA;
     } else if (words <= dsa::kMaxBitmapWords) {
-        const int words_cap = words < 32 ? 32 : words;
-        const size_t smem = dsa::bitmap_smem_bytes(words_cap);
+        int words_cap = words < 32 ? 32 : words;
+        // with the histograms given: the row in shared memory as well when it fits
+        int row_cap = 0;
+        if (pre) {
+            int smem_max = 0;
+            if (cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+                return DSA_ERR_CUDA;
+            const int wc4 = (words_cap + 3) & ~3;
+            const int row_keys = (max_seq_len + 3) & ~3;
+            if (dsa::bitmap_smem_bytes(wc4) + static_cast<size_t>(row_keys) * 4 <= static_cast<size_t>(smem_max)) {
+                words_cap = wc4;
+                row_cap = row_keys;
+            }
+        }
+        const size_t smem = dsa::bitmap_smem_bytes(words_cap) + static_cast<size_t>(row_cap) * 4;
         void* kern = forced ? (pre ? topk_bitmap_fn<true, true>() : topk_bitmap_fn<true, false>())
                             : (pre ? topk_bitmap_fn<false, true>() : topk_bitmap_fn<false, false>());
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
@@ -899,7 +941,8 @@ dsa_status topk_launch(const float* logits, int64_t ld, const int32_t* seq_lens,
         cfg.dynamicSmemBytes = smem;
         int a_B = B, a_rb = row_begin, a_k = k, a_ni = n_init, a_nl = n_local, a_sh = cmp_shift, a_wc = words_cap;
         void* args[] = {const_cast<float**>(&logits), &ld, const_cast<int32_t**>(&seq_lens), const_cast<int32_t**>(&cu_q),
-                        &a_B, &a_rb, &a_k, &a_ni, &a_nl, &a_sh, &idx, &a_wc, const_cast<uint32_t**>(&hist_g)};
+                        &a_B, &a_rb, &a_k, &a_ni, &a_nl, &a_sh, &idx, &a_wc, const_cast<uint32_t**>(&hist_g),
+                        &row_cap};
         if (cudaLaunchKernelExC(&cfg, kern, args) != cudaSuccess) return DSA_ERR_CUDA;
     } else {
         cfg.dynamicSmemBytes = 0;
